@@ -1,0 +1,176 @@
+"""Oracle for the S6 selective scan: plain f64 CPU reference (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library in
+``selective_state_space_s6_gb300``) never imports it, and it imports nothing
+from there.
+
+The arithmetic lives in ``ssm_oracle.c`` (plain sequential C, f64); this
+module only compiles it with gcc (``build()``) and marshals numpy arrays.
+What it computes, and which page each step follows, is in that file's header:
+the recurrence, discretisation and readout of the final selective_scan_kernel
+on the POPCORNBENCH transcript page (FW-GLM-5-1__l2_p30), with the softplus,
+exp_negate, SiLU-gate and gating-backward steps named by the mamba-rs
+kernels.rs page (MambaKernels doc comments), and a chain-rule backward that no
+page writes out (pinned in tests by finite differences).
+"""
+from __future__ import annotations
+
+import contextlib
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ssm_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libssm_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``ssm_oracle.c`` into ``_build/libssm_oracle.so`` (gcc, -O2, pthreads)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    # -ffp-contract=off: no fused multiply-adds, so every product and sum is
+    # rounded exactly as written; the oracle stays a literal reading of the math.
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
+           "-fno-fast-math", "-Wall", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _open(path):
+    lib = ctypes.CDLL(path)
+    i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    lib.s6o_fwd.argtypes = [i64] * 4 + [vp] * 9 + [vp] * 2 + [i64] * 4 + [ci]
+    lib.s6o_fwd.restype = ci
+    lib.s6o_bwd.argtypes = [i64] * 4 + [vp] * 9 + [vp] * 2 + [vp] * 9 + [i64] * 4 + [ci]
+    lib.s6o_bwd.restype = ci
+    lib.s6o_step.argtypes = [i64] * 3 + [vp] * 8 + [vp] * 2
+    lib.s6o_step.restype = ci
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _open(build())
+    return _lib
+
+
+@contextlib.contextmanager
+def override_library(path):
+    """Run the wrappers against another build of the oracle source (used by the
+    tests that plant a mistake in a copy of ``ssm_oracle.c``)."""
+    global _lib
+    prev = _load()
+    with _lock:
+        _lib = _open(path)
+    try:
+        yield
+    finally:
+        with _lock:
+            _lib = prev
+
+
+def _f64(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor: widen exactly (bf16/f32 -> f64)
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def default_threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count() or 1)
+
+
+def _shapes(u, Bm):
+    B, L, D = u.shape
+    N = Bm.shape[2]
+    return B, L, D, N
+
+
+def fwd(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0=None, *, b_range=None,
+        d_range=None, threads=None):
+    """Forward scan.  Returns ``(out [B,L,D], h_last [B,D,N])`` as f64 arrays.
+
+    With ``b_range``/``d_range`` only those batches/channels are computed; the
+    other entries of the returned arrays are NaN.
+    """
+    u, delta_raw, z, Bm, Cm = map(_f64, (u, delta_raw, z, Bm, Cm))
+    A_log, Dp, delta_bias, h0 = map(_f64, (A_log, Dp, delta_bias, h0))
+    B, L, D, N = _shapes(u, Bm)
+    b0, b1 = b_range or (0, B)
+    d0, d1 = d_range or (0, D)
+    out = np.full((B, L, D), np.nan)
+    h_last = np.full((B, D, N), np.nan)
+    rc = _load().s6o_fwd(B, L, D, N, _ptr(u), _ptr(delta_raw), _ptr(z), _ptr(Bm), _ptr(Cm),
+                         _ptr(A_log), _ptr(Dp), _ptr(delta_bias), _ptr(h0), _ptr(out),
+                         _ptr(h_last), b0, b1, d0, d1, threads or default_threads())
+    if rc != 0:
+        raise ValueError(f"s6o_fwd failed with code {rc}")
+    return out, h_last
+
+
+def bwd(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0, dout, dh_last=None, *,
+        b_range=None, d_range=None, threads=None):
+    """Backward of ``loss = sum(dout*out) + sum(dh_last*h_last)``.
+
+    Returns a dict of f64 arrays: du, d_delta_raw, dz (NaN where not computed),
+    dBm, dCm (sums over the selected channels), dA_log, dD, d_delta_bias (sums
+    over the selected batches), dh0.
+    """
+    u, delta_raw, z, Bm, Cm = map(_f64, (u, delta_raw, z, Bm, Cm))
+    A_log, Dp, delta_bias, h0, dout, dh_last = map(_f64, (A_log, Dp, delta_bias, h0, dout, dh_last))
+    B, L, D, N = _shapes(u, Bm)
+    b0, b1 = b_range or (0, B)
+    d0, d1 = d_range or (0, D)
+    r = {
+        "du": np.full((B, L, D), np.nan), "d_delta_raw": np.full((B, L, D), np.nan),
+        "dz": np.full((B, L, D), np.nan) if z is not None else None,
+        "dBm": np.zeros((B, L, N)), "dCm": np.zeros((B, L, N)),
+        "dA_log": np.full((D, N), np.nan), "dD": np.full((D,), np.nan),
+        "d_delta_bias": np.full((D,), np.nan), "dh0": np.full((B, D, N), np.nan),
+    }
+    rc = _load().s6o_bwd(B, L, D, N, _ptr(u), _ptr(delta_raw), _ptr(z), _ptr(Bm), _ptr(Cm),
+                         _ptr(A_log), _ptr(Dp), _ptr(delta_bias), _ptr(h0), _ptr(dout),
+                         _ptr(dh_last), _ptr(r["du"]), _ptr(r["d_delta_raw"]), _ptr(r["dz"]),
+                         _ptr(r["dBm"]), _ptr(r["dCm"]), _ptr(r["dA_log"]), _ptr(r["dD"]),
+                         _ptr(r["d_delta_bias"]), _ptr(r["dh0"]), b0, b1, d0, d1,
+                         threads or default_threads())
+    if rc != 0:
+        raise ValueError(f"s6o_bwd failed with code {rc}")
+    return r
+
+
+def step(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h):
+    """One decode step (T = 1).  u, delta_raw, z: [B,D]; Bm, Cm: [B,N]; h: [B,D,N].
+
+    Returns ``(out [B,D], h_new [B,D,N])``; the input ``h`` is not modified.
+    """
+    u, delta_raw, z, Bm, Cm = map(_f64, (u, delta_raw, z, Bm, Cm))
+    A_log, Dp, delta_bias = map(_f64, (A_log, Dp, delta_bias))
+    h_new = _f64(h).copy()
+    B, D = u.shape
+    N = Bm.shape[1]
+    out = np.full((B, D), np.nan)
+    rc = _load().s6o_step(B, D, N, _ptr(u), _ptr(delta_raw), _ptr(z), _ptr(Bm), _ptr(Cm),
+                          _ptr(A_log), _ptr(Dp), _ptr(delta_bias), _ptr(h_new), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"s6o_step failed with code {rc}")
+    return out, h_new
