@@ -1,0 +1,433 @@
+#!/usr/bin/env python3
+"""Benchmark: S6 selective-scan forward + backward on one GB300 (per rank).
+
+A step is one pass of the whole training hot path on one batch of the
+Mamba-1.4B-shaped workload (B=4, L=4096, d_inner=4096, N=16, bf16 activations,
+f32 parameters and state): ssm_scan_fwd (with chunk-state saves) followed by
+ssm_scan_bwd (backward scan + fixed-order reductions), all through the C ABI.
+
+Printed (rank 0, one JSON line): the metric in G(B*L*D*N)/s over fwd+bwd,
+device-timed with CUDA events on the launching stream (inputs resident in
+HBM, larger than L2), the same metric end to end from pinned host buffers
+(e2e), the HBM roofline of the dominant kernel, and the oracle timed on the
+host cores on a bounded sample (cpu_baseline).
+
+--impl reference times the oracle (plain f64 C, all host cores) instead, on
+a bounded sample of the same workload, and prints the same kind of line.
+
+Multi-GPU (torchrun, N > 1): every rank runs an independent replica on its
+own batch (weak scaling, no collective on the data path); the step time is
+the max over ranks and value = all ranks' cells / that time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from selective_state_space_s6_gb300 import inputs  # noqa: E402
+
+WORKLOAD = "mamba1p4b"
+METRIC = "fwd+bwd selective-scan G(B*L*D*N)/s"
+UNIT = "G(B*L*D*N)/s"
+ARGS = ("u", "delta_raw", "z", "Bm", "Cm", "A_log", "Dp", "delta_bias")
+KERNELS_PER_STEP = 4  # s6_fwd_kernel, s6_bwd_kernel, s6_reduce_dbc_kernel, s6_reduce_params_kernel
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def algorithmic_bytes(B, L, D, N, e, chunk):
+    """Bytes each kernel must move at minimum (inputs read once, outputs written once).
+
+    fwd: u, delta_raw, z read + out write (4*BLD*e); Bm, Cm read (2*BLN*e);
+         chunk states written (4*B*nc*D*N); A_log, Dp, delta_bias read.
+    bwd: u, delta_raw, z, dout read + du, d_delta_raw, dz write (7*BLD*e);
+         Bm, Cm read + dBm, dCm written (4*BLN*e); chunk states read;
+         A_log, Dp, delta_bias read + dA_log, dDp, d_delta_bias written.
+    """
+    nc = -(-L // chunk)
+    bld, bln = B * L * D, B * L * N
+    params = 4 * (D * N + 2 * D)
+    fwd = 4 * bld * e + 2 * bln * e + 4 * B * nc * D * N + params
+    bwd = 7 * bld * e + 4 * bln * e + 4 * B * nc * D * N + 2 * params
+    return fwd, bwd
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """Samples nvidia-smi clocks/throttle reasons while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle (CPU baseline)
+
+def oracle_sample(w, seqlen, rank=0, threads=None):
+    """A bounded sample of the workload for the oracle: batch 0, the first
+    64*threads channels, the first ``seqlen``
+    steps; same distributions as the full workload."""
+    import oracle
+    threads = threads or oracle.default_threads()
+    channels = min(w.dim, 64 * threads)
+    seqlen = max(1, min(seqlen, w.seqlen))
+    x = inputs.make_inputs(1, seqlen, channels, w.dstate, w.act, seed=rank,
+                           delta_lo=w.delta_lo, delta_hi=w.delta_hi)
+    x64 = {k: (oracle._f64(v) if v is not None else None) for k, v in x.items()}
+    cells = seqlen * channels * w.dstate
+    desc = (f"batch 0 of {w.batch}, channels 0..{channels - 1} of {w.dim}, "
+            f"steps 0..{seqlen - 1} of {w.seqlen}")
+    return x64, cells, desc, threads
+
+
+def oracle_step(x64, threads):
+    import oracle
+    oracle.fwd(*[x64[k] for k in ARGS], None, threads=threads)
+    oracle.bwd(*[x64[k] for k in ARGS], None, x64["dout"], None, threads=threads)
+
+
+def time_oracle(w, steps, warmup, target_s, rank=0):
+    """Oracle fwd+bwd throughput on a sample sized so that one step takes about
+    ``target_s`` seconds (calibrated on a 128-step sample first)."""
+    x64, cells, _, threads = oracle_sample(w, 128, rank)
+    t0 = time.perf_counter()
+    oracle_step(x64, threads)
+    per_step = (time.perf_counter() - t0) / 128
+    seqlen = int(max(128, min(w.seqlen, target_s / max(per_step, 1e-9))))
+    x64, cells, desc, threads = oracle_sample(w, seqlen, rank, threads)
+    for _ in range(warmup):
+        oracle_step(x64, threads)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_step(x64, threads)
+    dt = (time.perf_counter() - t0) / max(steps, 1)
+    return cells / dt / 1e9, desc, threads, dt
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, world, rank, local):
+    from selective_state_space_s6_gb300 import s6
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = inputs.WORKLOADS[args.workload]
+    B, L, D, N = w.batch, w.seqlen, w.dim, w.dstate
+    e = 2 if w.act == "bf16" else 4
+    act = s6.SSM_BF16 if w.act == "bf16" else s6.SSM_F32
+    x_cpu = inputs.make_workload(args.workload, seed=rank)
+    x = {k: (v.to(dev) if v is not None else None) for k, v in x_cpu.items()}
+    stream = torch.cuda.current_stream(dev)
+
+    out = torch.empty_like(x["u"])
+    h_last = torch.empty((B, D, N), dtype=torch.float32, device=dev)
+    cs = torch.empty((B, s6.num_chunks(L), D, N), dtype=torch.float32, device=dev)
+    g = {"du": torch.empty_like(x["u"]), "d_delta_raw": torch.empty_like(x["u"]),
+         "dz": torch.empty_like(x["u"]), "dBm": torch.empty_like(x["Bm"]),
+         "dCm": torch.empty_like(x["Cm"]), "dA_log": torch.empty_like(x["A_log"]),
+         "dD": torch.empty_like(x["Dp"]), "d_delta_bias": torch.empty_like(x["delta_bias"]),
+         "dh0": None}
+    ws_bytes = max(s6.bwd_workspace_bytes(B, L, D, N, act), s6.fwd_workspace_bytes(B, L, D, N, act))
+    ws = torch.empty((ws_bytes + 256,), dtype=torch.uint8, device=dev)
+
+    def fwd():
+        s6.ssm_scan_fwd(*[x[k] for k in ARGS], None, out=out, h_last=h_last, chunk_states=cs,
+                        ws=ws, stream=stream)
+
+    def bwd_partials():
+        s6.bwd_partials(*[x[k] for k in ARGS], cs, x["dout"], None, g, ws, stream)
+
+    def bwd_finalize():
+        s6.bwd_finalize(B, L, D, N, act, g, ws, stream)
+
+    for _ in range(args.warmup):
+        fwd(); bwd_partials(); bwd_finalize()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(K):
+        ev[k][0].record(stream)
+        fwd()
+        ev[k][1].record(stream)
+        bwd_partials()
+        ev[k][2].record(stream)
+        bwd_finalize()
+        ev[k][3].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    total_ms = start.elapsed_time(end)
+    clk = clocks.stop()
+    t_fwd = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(K)) / K
+    t_bwd = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(K)) / K
+    t_fin = sum(ev[k][2].elapsed_time(ev[k][3]) for k in range(K)) / K
+
+    ms_step = max_over_ranks(total_ms / K, world)
+    cells = w.cells
+    value = world * cells / (ms_step * 1e-3) / 1e9
+
+    # ---- e2e: pinned host inputs -> device -> fwd + bwd -> results back to pinned host
+    in_keys = ["u", "delta_raw", "z", "Bm", "Cm", "A_log", "Dp", "delta_bias", "dout"]
+    h_in = {k: x_cpu[k].pin_memory() for k in in_keys}
+    out_keys = ["du", "d_delta_raw", "dz", "dBm", "dCm", "dA_log", "dD", "d_delta_bias"]
+    h_out = {k: torch.empty(g[k].shape, dtype=g[k].dtype, pin_memory=True) for k in out_keys}
+    h_out["out"] = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+
+    def e2e_step():
+        for k in in_keys:
+            x[k].copy_(h_in[k], non_blocking=True)
+        fwd(); bwd_partials(); bwd_finalize()
+        h_out["out"].copy_(out, non_blocking=True)
+        for k in out_keys:
+            h_out[k].copy_(g[k], non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    ke = max(1, min(K, args.e2e_steps))
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / ke, world)
+    e2e_value = world * cells / (e2e_ms * 1e-3) / 1e9
+
+    # ---- roofline of the dominant kernel (the backward scan), live event timing
+    peak, peak_kind = load_peaks()
+    fwd_bytes, bwd_bytes = algorithmic_bytes(B, L, D, N, e, s6.CHUNK_LEN)
+    kern = {
+        "s6_fwd_kernel": {"ms": t_fwd, "bytes": fwd_bytes},
+        "s6_bwd_kernel": {"ms": t_bwd, "bytes": bwd_bytes},
+        "s6_reduce (finalize)": {"ms": t_fin, "bytes": None},
+    }
+    dom = max(("s6_fwd_kernel", "s6_bwd_kernel"), key=lambda k: kern[k]["ms"])
+    achieved = kern[dom]["bytes"] / (kern[dom]["ms"] * 1e-3) / 1e9
+    traffic = load_traffic(dom)
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
+                "algorithmic_bytes_per_launch": kern[dom]["bytes"]}
+    per_kernel = {}
+    for k in ("s6_fwd_kernel", "s6_bwd_kernel"):
+        gbs = kern[k]["bytes"] / (kern[k]["ms"] * 1e-3) / 1e9
+        per_kernel[k] = {"ms": round(kern[k]["ms"], 4), "gcells_s": round(cells / (kern[k]["ms"] * 1e-3) / 1e9, 1),
+                         "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4)}
+    per_kernel["s6_reduce_dbc+params (finalize)"] = {"ms": round(t_fin, 4)}
+
+    cpu_base = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, desc, threads, dt = time_oracle(w, steps=1, warmup=0, target_s=15.0)
+        cpu_base = {"value": round(v, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+                    "sample": desc + f" ({dt:.1f} s per fwd+bwd)"}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,1) activations, Mamba dt/A/D initialisation)",
+        "config": {"workload": f"{args.workload}: {w.description}", "B": B, "L": L, "D": D,
+                   "N": N, "act_dtype": w.act, "state_dtype": "f32",
+                   "l2": f"no flush; each step reads {(4 * B * L * D * e) / 1e6:.0f} MB of "
+                         f"[B,L,D] inputs, larger than the 129 MB L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": KERNELS_PER_STEP * K,
+        "roofline": roofline,
+        "kernels": per_kernel,
+        "cpu_baseline": cpu_base,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def load_traffic(kernel):
+    """dram bytes per launch from the committed ncu summary, if it matches the
+    current build of that kernel (else null)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    ent = t.get(kernel)
+    if not ent:
+        return None
+    try:
+        from selective_state_space_s6_gb300 import build as _b
+        src = _b.kernel_source_digest()
+    except Exception:
+        return None
+    return ent.get("bytes_per_launch") if ent.get("source_digest") == src else None
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = inputs.WORKLOADS[args.workload]
+    # whole run within a few minutes: about 150 s of oracle work over all steps
+    target = max(0.5, 150.0 / max(1, args.steps + args.warmup))
+    v, desc, threads, dt = time_oracle(w, steps=args.steps, warmup=args.warmup, target_s=target)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {w.description}", "B": w.batch, "L": w.seqlen,
+                   "D": w.dim, "N": w.dstate, "act_dtype": w.act,
+                   "sample_per_step": desc},
+        "cpu_baseline": {"value": round(v, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,180 @@
+/*
+ * ssm_scan.h — C ABI of the GB300 (sm_103a) S6 selective-scan library.
+ *
+ * The operation (Mamba S6, "selective state space"): for every batch b,
+ * channel d and state n,
+ *     s      = delta_raw[b,t,d] + delta_bias[d]
+ *     delta  = softplus(s)
+ *     Abar   = exp(delta * A[d,n]),   A = -exp(A_log[d,n])
+ *     h_t    = Abar * h_{t-1} + delta * Bm[b,t,n] * u[b,t,d]      (h_{-1} = h0, or 0)
+ *     y      = sum_n Cm[b,t,n] * h_t + Dp[d] * u[b,t,d]
+ *     out    = y * silu(z[b,t,d])                                  (out = y when z is NULL)
+ * This is the recurrence, discretisation and readout of the final
+ * selective_scan_kernel on the POPCORNBENCH transcript page (FW-GLM-5-1__l2_p30),
+ * with the softplus / exp_negate / SiLU-gate steps and the "SSM recurrence"
+ * entry points (single-step forward, multi-step forward with and without
+ * activation saves, local backward plus dB/dC/dD/dA_log reductions) of the
+ * mamba-rs kernels.rs page (MambaKernels).
+ *
+ * Conventions shared by every entry point
+ *   - Shapes: B = batch, L = seqlen, D = dim (d_inner), N = dstate, 1 <= N <= 16.
+ *   - Layouts are dense row-major, last index contiguous:
+ *       u, delta_raw, z, dout, du, d_delta_raw, dz : [B][L][D]   (activation dtype)
+ *       Bm, Cm, dBm, dCm                            : [B][L][N]   (activation dtype)
+ *       A_log, dA_log : [D][N] f32;  Dp, dDp, delta_bias, d_delta_bias : [D] f32
+ *       h0, h_last, dh0, dh_last, h (step)          : [B][D][N] f32
+ *       chunk_states : [B][ssm_num_chunks(L)][D][N] f32
+ *   - The activation dtype `act` is SSM_F32 or SSM_BF16; parameters, states
+ *     and parameter gradients are always f32; arithmetic is f32.
+ *   - All tensor pointers are DEVICE pointers owned by the caller, aligned
+ *     to their element size; outputs must not overlap inputs (except `h` of
+ *     ssm_step, which is updated in place).  Pointers marked "nullable" may
+ *     be NULL.  The library never allocates or frees device memory; scratch
+ *     space is the caller's `ws` buffer.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *     only enqueues work on it and returns; errors found while enqueueing are
+ *     returned, errors of the asynchronous work surface at the caller's next
+ *     synchronisation.
+ *   - Gradients overwrite their outputs (no accumulation).
+ *   - Results are deterministic: the same inputs give bit-identical outputs
+ *     on every call (fixed-order reductions, no floating-point atomics).
+ *   - Return value: SSM_OK (0) or an ssm_status error code; on error nothing
+ *     has been enqueued unless the code is SSM_ERR_CUDA.  ssm_last_error()
+ *     returns a message for the calling thread's last error.
+ */
+#ifndef SSM_SCAN_H
+#define SSM_SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SSM_OK = 0,
+  SSM_ERR_INVALID_ARG = 1, /* bad shape, NULL required pointer, misaligned pointer */
+  SSM_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. N > 16) */
+  SSM_ERR_WORKSPACE = 3,   /* ws NULL or ws_bytes below the required size */
+  SSM_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  SSM_ERR_TIMEOUT = 5,     /* reserved: a bounded device-side wait gave up */
+  SSM_ERR_INTERNAL = 6     /* reserved: a device-side consistency check failed */
+} ssm_status;
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
+
+/* Steps between saved chunk states (the forward's checkpoints for the backward). */
+#define SSM_CHUNK_LEN 64
+/* Largest supported state size N. */
+#define SSM_MAX_DSTATE 16
+
+/* Human-readable name of a status code.  Never NULL. */
+const char *ssm_status_string(int status);
+
+/* Message describing the calling thread's most recent error ("" if none). */
+const char *ssm_last_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int ssm_version(void);
+
+/* Number of saved chunk states: ceil(seqlen / SSM_CHUNK_LEN); 0 for seqlen <= 0. */
+int64_t ssm_num_chunks(int64_t seqlen);
+
+/* Scratch bytes ssm_scan_fwd / ssm_scan_fwd_nosave need in `ws` for this
+ * shape; -1 for an invalid shape.  May be 0, in which case ws may be NULL. */
+int64_t ssm_fwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act);
+
+/* Scratch bytes ssm_scan_bwd needs in `ws` (per-tile partial sums of dBm/dCm
+ * and per-batch partial sums of the parameter gradients); -1 if invalid. */
+int64_t ssm_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act);
+
+/*
+ * Forward scan with saves for the backward (mamba-rs kernels.rs page:
+ * MambaKernels "Multi-step SSM forward with activation saves for backward").
+ *   inputs : u, delta_raw, Bm, Cm, A_log, Dp, delta_bias;  z nullable (no gate);
+ *            h0 nullable (zero initial state)
+ *   outputs: out [B][L][D];  h_last nullable (final state h_{L-1});
+ *            chunk_states [B][nc][D][N] = state before step c*SSM_CHUNK_LEN
+ *            (chunk 0 holds h0); it is what ssm_scan_bwd reads.
+ *   ws/ws_bytes: scratch of ssm_fwd_workspace_bytes() bytes (nullable when 0).
+ */
+int ssm_scan_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
+                 const void *u, const void *delta_raw, const void *z, const void *Bm,
+                 const void *Cm, const float *A_log, const float *Dp, const float *delta_bias,
+                 const float *h0, void *out, float *h_last, float *chunk_states, void *ws,
+                 size_t ws_bytes, void *stream);
+
+/*
+ * Forward scan without saves (kernels.rs page: "Multi-step SSM forward
+ * without activation saves (target network)").  Same as ssm_scan_fwd without
+ * the chunk_states output.
+ */
+int ssm_scan_fwd_nosave(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
+                        const void *u, const void *delta_raw, const void *z, const void *Bm,
+                        const void *Cm, const float *A_log, const float *Dp,
+                        const float *delta_bias, const float *h0, void *out, float *h_last,
+                        void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Backward of  loss = sum(dout * out) + sum(dh_last * h_last)  (kernels.rs
+ * page: "Per-(b,t,d,n) local SSM backward" and the dB / dC / dD / d_a_log
+ * reductions; no page writes the equations, which follow from the chain rule):
+ *   inputs : the forward's inputs (same pointers/values), chunk_states from
+ *            ssm_scan_fwd on those inputs, dout [B][L][D]; dh_last nullable.
+ *   outputs: du, d_delta_raw [B][L][D]; dz [B][L][D] (required iff z != NULL);
+ *            dBm, dCm [B][L][N]; dA_log [D][N]; dDp, d_delta_bias [D];
+ *            dh0 nullable ([B][D][N], gradient w.r.t. h0).
+ *   d_delta_raw is the gradient w.r.t. delta_raw (softplus' already applied);
+ *   d_delta_bias is its sum over (b, t).  Reductions over channels (dBm, dCm)
+ *   and over (b, t) (dA_log, dDp, d_delta_bias) use fixed summation trees, so
+ *   repeated calls are bit-identical (the determinism policy of the
+ *   deterministic_backward.py page: single writer, fixed order, no atomics).
+ *   ws/ws_bytes: at least ssm_bwd_workspace_bytes() bytes.
+ */
+int ssm_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
+                 const void *u, const void *delta_raw, const void *z, const void *Bm,
+                 const void *Cm, const float *A_log, const float *Dp, const float *delta_bias,
+                 const float *h0, const float *chunk_states, const void *dout,
+                 const float *dh_last, void *du, void *d_delta_raw, void *dz, void *dBm,
+                 void *dCm, float *dA_log, float *dDp, float *d_delta_bias, float *dh0,
+                 void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * The two halves of ssm_scan_bwd, for callers that want to schedule (or time)
+ * them separately; ssm_scan_bwd is exactly ssm_scan_bwd_partials followed by
+ * ssm_scan_bwd_finalize on the same stream with the same ws.
+ *   ssm_scan_bwd_partials: the backward scan.  Writes du, d_delta_raw, dz and
+ *     dh0 (same meaning as above) and leaves the per-tile / per-batch partial
+ *     sums of dBm, dCm, dA_log, dDp, d_delta_bias in ws.
+ *   ssm_scan_bwd_finalize: adds those partials in fixed order into dBm, dCm
+ *     ([B][L][N], act dtype), dA_log, dDp, d_delta_bias (f32).  It reads only
+ *     ws, so the shape must match the partials call.
+ */
+int ssm_scan_bwd_partials(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
+                          const void *u, const void *delta_raw, const void *z, const void *Bm,
+                          const void *Cm, const float *A_log, const float *Dp,
+                          const float *delta_bias, const float *chunk_states, const void *dout,
+                          const float *dh_last, void *du, void *d_delta_raw, void *dz,
+                          float *dh0, void *ws, size_t ws_bytes, void *stream);
+
+int ssm_scan_bwd_finalize(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
+                          void *dBm, void *dCm, float *dA_log, float *dDp, float *d_delta_bias,
+                          const void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * One decode step, T = 1 (kernels.rs page: "Single-step SSM forward (T=1
+ * inference)").  u, delta_raw, z [B][D] (z nullable), Bm, Cm [B][N], h
+ * [B][D][N] f32 read and overwritten in place with the new state, out [B][D].
+ * Calling it L times on the slices t = 0..L-1 equals ssm_scan_fwd from h0 = h.
+ */
+int ssm_step(int64_t batch, int64_t dim, int64_t dstate, int act, const void *u,
+             const void *delta_raw, const void *z, const void *Bm, const void *Cm,
+             const float *A_log, const float *Dp, const float *delta_bias, float *h, void *out,
+             void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_SCAN_H */

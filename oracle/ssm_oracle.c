@@ -38,7 +38,7 @@
  *            dh0 = a_0 * g_0
  *
  * Sums over (b,t) for the parameter gradients run in ascending b, then t.
- * Sums over d for dBm/dCm run in ascending d inside fixed blocks of 64
+ * Sums over d for dBm/dCm run in ascending d inside fixed blocks of 16
  * channels, the block partials then added in ascending block order; the
  * result does not depend on the thread count.  Threads (pthreads) only split
  * independent channels; every (b,d) scan is the plain sequential loop below.
@@ -49,7 +49,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-#define S6O_DBLOCK 64
+#define S6O_DBLOCK 16
 
 typedef struct {
   int64_t B, L, D, N;

@@ -1,0 +1,285 @@
+// Host side of the C ABI declared in include/ssm_scan.h: argument checks,
+// workspace sizing and kernel dispatch.  No allocation, no synchronisation.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "s6_internal.cuh"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+  return fail(SSM_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+size_t act_size(int act) { return act == SSM_BF16 ? 2 : 4; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr int64_t kMaxElems = (int64_t)1 << 31;  // every per-tensor index fits in 31 bits
+
+int check_shape(int64_t B, int64_t L, int64_t D, int64_t N, int act) {
+  if (act != SSM_F32 && act != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "act must be SSM_F32 or SSM_BF16, got %d", act);
+  if (B < 0 || L < 0 || D < 0) return fail(SSM_ERR_INVALID_ARG, "negative shape (B=%lld L=%lld D=%lld)", (long long)B, (long long)L, (long long)D);
+  if (N < 1) return fail(SSM_ERR_INVALID_ARG, "dstate must be >= 1, got %lld", (long long)N);
+  if (N > SSM_MAX_DSTATE) return fail(SSM_ERR_UNSUPPORTED, "dstate %lld > %d is not supported", (long long)N, SSM_MAX_DSTATE);
+  if (B > 65535) return fail(SSM_ERR_UNSUPPORTED, "batch %lld > 65535 is not supported", (long long)B);
+  if (B * L * D >= kMaxElems || B * L * N >= kMaxElems || B * D * N * (L / SSM_CHUNK_LEN + 1) >= kMaxElems)
+    return fail(SSM_ERR_UNSUPPORTED, "problem too large for 31-bit indexing");
+  return SSM_OK;
+}
+
+// A required pointer must be non-NULL and aligned to its element size.
+int need(const void* p, size_t align, const char* name) {
+  if (!p) return fail(SSM_ERR_INVALID_ARG, "%s must not be NULL", name);
+  if (!aligned(p, align)) return fail(SSM_ERR_INVALID_ARG, "%s is not %zu-byte aligned", name, align);
+  return SSM_OK;
+}
+int opt(const void* p, size_t align, const char* name) {
+  return p ? need(p, align, name) : SSM_OK;
+}
+
+#define S6_TRY(x)                    \
+  do {                               \
+    const int _rc = (x);             \
+    if (_rc != SSM_OK) return _rc;   \
+  } while (0)
+
+int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+int check_ws(const void* ws, size_t ws_bytes, int64_t total) {
+  if (total <= 0) return SSM_OK;
+  if (!ws) return fail(SSM_ERR_WORKSPACE, "ws is NULL but %lld bytes are required", (long long)total);
+  if ((int64_t)ws_bytes < total)
+    return fail(SSM_ERR_WORKSPACE, "ws_bytes=%zu < required %lld", ws_bytes, (long long)total);
+  if (!aligned(ws, 256)) return fail(SSM_ERR_INVALID_ARG, "ws is not 256-byte aligned");
+  return SSM_OK;
+}
+
+struct BwdWorkspace {
+  int64_t dbc_off, dbc_bytes, param_off, param_bytes, total;
+};
+
+BwdWorkspace bwd_ws_layout(int64_t B, int64_t L, int64_t D, int64_t N) {
+  BwdWorkspace w;
+  const int64_t ndt = (D + s6::kDTile - 1) / s6::kDTile;
+  w.dbc_off = 0;
+  w.dbc_bytes = ndt * B * L * 2 * N * (int64_t)sizeof(float);
+  w.param_off = align_up(w.dbc_bytes, 256);
+  w.param_bytes = B * D * (N + 2) * (int64_t)sizeof(float);
+  w.total = align_up(w.param_off + w.param_bytes, 256);
+  return w;
+}
+
+int fwd_common(int64_t B, int64_t L, int64_t D, int64_t N, int act, const void* u,
+               const void* delta_raw, const void* z, const void* Bm, const void* Cm,
+               const float* A_log, const float* Dp, const float* delta_bias, const float* h0,
+               void* out, float* h_last, float* chunk_states, bool save, void* stream) {
+  S6_TRY(check_shape(B, L, D, N, act));
+  const size_t e = act_size(act);
+  S6_TRY(need(u, e, "u"));
+  S6_TRY(need(delta_raw, e, "delta_raw"));
+  S6_TRY(opt(z, e, "z"));
+  S6_TRY(need(Bm, e, "Bm"));
+  S6_TRY(need(Cm, e, "Cm"));
+  S6_TRY(need(A_log, 4, "A_log"));
+  S6_TRY(need(Dp, 4, "Dp"));
+  S6_TRY(need(delta_bias, 4, "delta_bias"));
+  S6_TRY(opt(h0, 4, "h0"));
+  S6_TRY(need(out, e, "out"));
+  S6_TRY(opt(h_last, 4, "h_last"));
+  if (save) S6_TRY(need(chunk_states, 4, "chunk_states"));
+  g_last_error[0] = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (B == 0 || D == 0) return SSM_OK;
+  if (L == 0) {
+    // No steps: the final state is the initial state.
+    if (h_last) {
+      cudaError_t ce = h0 ? cudaMemcpyAsync(h_last, h0, sizeof(float) * B * D * N, cudaMemcpyDeviceToDevice, st)
+                          : cudaMemsetAsync(h_last, 0, sizeof(float) * B * D * N, st);
+      if (ce != cudaSuccess) return cuda_fail(ce, "ssm_scan_fwd(L=0)");
+    }
+    return SSM_OK;
+  }
+  s6::FwdParams p;
+  p.u = u; p.delta_raw = delta_raw; p.z = z; p.Bm = Bm; p.Cm = Cm;
+  p.A_log = A_log; p.Dp = Dp; p.delta_bias = delta_bias; p.h0 = h0;
+  p.out = out; p.h_last = h_last; p.chunk_states = save ? chunk_states : nullptr;
+  p.B = (int)B; p.L = (int)L; p.D = (int)D; p.N = (int)N;
+  p.nchunks = (int)ssm_num_chunks(L);
+  cudaError_t ce = s6::launch_fwd(p, act, st);
+  if (ce != cudaSuccess) return cuda_fail(ce, "ssm_scan_fwd launch");
+  return SSM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ssm_status_string(int status) {
+  switch (status) {
+    case SSM_OK: return "SSM_OK";
+    case SSM_ERR_INVALID_ARG: return "SSM_ERR_INVALID_ARG";
+    case SSM_ERR_UNSUPPORTED: return "SSM_ERR_UNSUPPORTED";
+    case SSM_ERR_WORKSPACE: return "SSM_ERR_WORKSPACE";
+    case SSM_ERR_CUDA: return "SSM_ERR_CUDA";
+    case SSM_ERR_TIMEOUT: return "SSM_ERR_TIMEOUT";
+    case SSM_ERR_INTERNAL: return "SSM_ERR_INTERNAL";
+    default: return "SSM_ERR_UNKNOWN";
+  }
+}
+
+const char* ssm_last_error(void) { return g_last_error; }
+
+int ssm_version(void) { return 100; }
+
+int64_t ssm_num_chunks(int64_t seqlen) {
+  return seqlen <= 0 ? 0 : (seqlen + SSM_CHUNK_LEN - 1) / SSM_CHUNK_LEN;
+}
+
+int64_t ssm_fwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act) {
+  if (check_shape(batch, seqlen, dim, dstate, act) != SSM_OK) return -1;
+  return 0;
+}
+
+int64_t ssm_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act) {
+  if (check_shape(batch, seqlen, dim, dstate, act) != SSM_OK) return -1;
+  return bwd_ws_layout(batch, seqlen, dim, dstate).total;
+}
+
+int ssm_scan_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
+                 const void* u, const void* delta_raw, const void* z, const void* Bm,
+                 const void* Cm, const float* A_log, const float* Dp, const float* delta_bias,
+                 const float* h0, void* out, float* h_last, float* chunk_states, void* ws,
+                 size_t ws_bytes, void* stream) {
+  (void)ws; (void)ws_bytes;
+  return fwd_common(batch, seqlen, dim, dstate, act, u, delta_raw, z, Bm, Cm, A_log, Dp,
+                    delta_bias, h0, out, h_last, chunk_states, true, stream);
+}
+
+int ssm_scan_fwd_nosave(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
+                        const void* u, const void* delta_raw, const void* z, const void* Bm,
+                        const void* Cm, const float* A_log, const float* Dp,
+                        const float* delta_bias, const float* h0, void* out, float* h_last,
+                        void* ws, size_t ws_bytes, void* stream) {
+  (void)ws; (void)ws_bytes;
+  return fwd_common(batch, seqlen, dim, dstate, act, u, delta_raw, z, Bm, Cm, A_log, Dp,
+                    delta_bias, h0, out, h_last, nullptr, false, stream);
+}
+
+int ssm_scan_bwd_partials(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
+                          const void* u, const void* delta_raw, const void* z, const void* Bm,
+                          const void* Cm, const float* A_log, const float* Dp,
+                          const float* delta_bias, const float* chunk_states, const void* dout,
+                          const float* dh_last, void* du, void* d_delta_raw, void* dz,
+                          float* dh0, void* ws, size_t ws_bytes, void* stream) {
+  const int64_t B = batch, L = seqlen, D = dim, N = dstate;
+  S6_TRY(check_shape(B, L, D, N, act));
+  const size_t e = act_size(act);
+  S6_TRY(need(u, e, "u"));
+  S6_TRY(need(delta_raw, e, "delta_raw"));
+  S6_TRY(opt(z, e, "z"));
+  S6_TRY(need(Bm, e, "Bm"));
+  S6_TRY(need(Cm, e, "Cm"));
+  S6_TRY(need(A_log, 4, "A_log"));
+  S6_TRY(need(Dp, 4, "Dp"));
+  S6_TRY(need(delta_bias, 4, "delta_bias"));
+  S6_TRY(need(chunk_states, 4, "chunk_states"));
+  S6_TRY(need(dout, e, "dout"));
+  S6_TRY(opt(dh_last, 4, "dh_last"));
+  S6_TRY(need(du, e, "du"));
+  S6_TRY(need(d_delta_raw, e, "d_delta_raw"));
+  if (z) S6_TRY(need(dz, e, "dz (required when z is given)"));
+  S6_TRY(opt(dh0, 4, "dh0"));
+  const BwdWorkspace w = bwd_ws_layout(B, L, D, N);
+  S6_TRY(check_ws(ws, ws_bytes, w.total));
+  g_last_error[0] = 0;
+  if (B == 0 || D == 0) return SSM_OK;
+  s6::BwdParams p;
+  p.u = u; p.delta_raw = delta_raw; p.z = z; p.Bm = Bm; p.Cm = Cm;
+  p.A_log = A_log; p.Dp = Dp; p.delta_bias = delta_bias; p.chunk_states = chunk_states;
+  p.dout = dout; p.dh_last = dh_last; p.du = du; p.d_delta_raw = d_delta_raw; p.dz = dz;
+  p.dh0 = dh0;
+  p.ws_dbc = reinterpret_cast<float*>(static_cast<char*>(ws) + w.dbc_off);
+  p.ws_param = reinterpret_cast<float*>(static_cast<char*>(ws) + w.param_off);
+  p.B = (int)B; p.L = (int)L; p.D = (int)D; p.N = (int)N;
+  p.nchunks = (int)ssm_num_chunks(L);
+  const cudaError_t ce = s6::launch_bwd(p, act, static_cast<cudaStream_t>(stream));
+  if (ce != cudaSuccess) return cuda_fail(ce, "ssm_scan_bwd_partials launch");
+  return SSM_OK;
+}
+
+int ssm_scan_bwd_finalize(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
+                          void* dBm, void* dCm, float* dA_log, float* dDp, float* d_delta_bias,
+                          const void* ws, size_t ws_bytes, void* stream) {
+  const int64_t B = batch, L = seqlen, D = dim, N = dstate;
+  S6_TRY(check_shape(B, L, D, N, act));
+  const size_t e = act_size(act);
+  S6_TRY(need(dBm, e, "dBm"));
+  S6_TRY(need(dCm, e, "dCm"));
+  S6_TRY(need(dA_log, 4, "dA_log"));
+  S6_TRY(need(dDp, 4, "dDp"));
+  S6_TRY(need(d_delta_bias, 4, "d_delta_bias"));
+  const BwdWorkspace w = bwd_ws_layout(B, L, D, N);
+  S6_TRY(check_ws(ws, ws_bytes, w.total));
+  g_last_error[0] = 0;
+  if (D == 0) return SSM_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float* ws_dbc = reinterpret_cast<const float*>(static_cast<const char*>(ws) + w.dbc_off);
+  const float* ws_param = reinterpret_cast<const float*>(static_cast<const char*>(ws) + w.param_off);
+  cudaError_t ce;
+  if (B > 0) {
+    const int ndt = (int)((D + s6::kDTile - 1) / s6::kDTile);
+    ce = s6::launch_reduce_dbc(ws_dbc, ndt, (int)B, (int)L, (int)N, dBm, dCm, act, st);
+    if (ce != cudaSuccess) return cuda_fail(ce, "ssm_scan_bwd_finalize dBm/dCm reduction");
+  }
+  ce = s6::launch_reduce_params(ws_param, (int)B, (int)D, (int)N, dA_log, dDp, d_delta_bias, st);
+  if (ce != cudaSuccess) return cuda_fail(ce, "ssm_scan_bwd_finalize parameter reduction");
+  return SSM_OK;
+}
+
+int ssm_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
+                 const void* u, const void* delta_raw, const void* z, const void* Bm,
+                 const void* Cm, const float* A_log, const float* Dp, const float* delta_bias,
+                 const float* h0, const float* chunk_states, const void* dout,
+                 const float* dh_last, void* du, void* d_delta_raw, void* dz, void* dBm,
+                 void* dCm, float* dA_log, float* dDp, float* d_delta_bias, float* dh0,
+                 void* ws, size_t ws_bytes, void* stream) {
+  // h0 is not read: the chunk states already start from it.  It is checked so
+  // that a caller passing a bad pointer hears about it.
+  S6_TRY(opt(h0, 4, "h0"));
+  const size_t e = (act == SSM_BF16) ? 2 : 4;
+  // validate the finalize outputs before enqueueing the first half
+  S6_TRY(check_shape(batch, seqlen, dim, dstate, act));
+  S6_TRY(need(dBm, e, "dBm"));
+  S6_TRY(need(dCm, e, "dCm"));
+  S6_TRY(need(dA_log, 4, "dA_log"));
+  S6_TRY(need(dDp, 4, "dDp"));
+  S6_TRY(need(d_delta_bias, 4, "d_delta_bias"));
+  S6_TRY(ssm_scan_bwd_partials(batch, seqlen, dim, dstate, act, u, delta_raw, z, Bm, Cm, A_log,
+                               Dp, delta_bias, chunk_states, dout, dh_last, du, d_delta_raw, dz,
+                               dh0, ws, ws_bytes, stream));
+  return ssm_scan_bwd_finalize(batch, seqlen, dim, dstate, act, dBm, dCm, dA_log, dDp,
+                               d_delta_bias, ws, ws_bytes, stream);
+}
+
+int ssm_step(int64_t batch, int64_t dim, int64_t dstate, int act, const void* u,
+             const void* delta_raw, const void* z, const void* Bm, const void* Cm,
+             const float* A_log, const float* Dp, const float* delta_bias, float* h, void* out,
+             void* stream) {
+  S6_TRY(need(h, 4, "h"));
+  return fwd_common(batch, 1, dim, dstate, act, u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias,
+                    h, out, h, nullptr, false, stream);
+}
+
+}  // extern "C"

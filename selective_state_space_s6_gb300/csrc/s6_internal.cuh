@@ -1,0 +1,98 @@
+// Internal declarations shared by the S6 kernels and the C-ABI host code.
+// Not part of the public interface (that is include/ssm_scan.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ssm_scan.h"
+
+namespace s6 {
+
+constexpr int kChunk = SSM_CHUNK_LEN;  // steps between saved chunk states
+constexpr int kDTile = 64;             // channels per CTA in the scan kernels
+constexpr int kThreadsPerChannel = 2;  // each channel's N states are split over 2 lanes
+constexpr int kScanThreads = kDTile * kThreadsPerChannel;
+constexpr int kSub = 8;                // backward: steps kept in registers per sub-chunk
+
+// ---------------------------------------------------------------- params
+
+struct FwdParams {
+  const void* u;
+  const void* delta_raw;
+  const void* z;  // nullable
+  const void* Bm;
+  const void* Cm;
+  const float* A_log;
+  const float* Dp;
+  const float* delta_bias;
+  const float* h0;      // nullable
+  void* out;
+  float* h_last;        // nullable (may alias h0 for the decode step)
+  float* chunk_states;  // nullable (nosave)
+  int B, L, D, N, nchunks;
+};
+
+struct BwdParams {
+  const void* u;
+  const void* delta_raw;
+  const void* z;  // nullable
+  const void* Bm;
+  const void* Cm;
+  const float* A_log;
+  const float* Dp;
+  const float* delta_bias;
+  const float* chunk_states;
+  const void* dout;
+  const float* dh_last;  // nullable
+  void* du;
+  void* d_delta_raw;
+  void* dz;    // non-null iff z non-null
+  float* dh0;  // nullable
+  float* ws_dbc;    // [ndt][B][L][2][N] per-CTA sums of the dBm / dCm terms
+  float* ws_param;  // [B][D][N+2] per-batch sums: A*sum(...), dDp, d_delta_bias
+  int B, L, D, N, nchunks;
+};
+
+// ---------------------------------------------------------------- launchers
+// Each returns the cudaError_t of its launch(es).
+
+cudaError_t launch_fwd(const FwdParams& p, int act, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdParams& p, int act, cudaStream_t stream);
+cudaError_t launch_reduce_dbc(const float* ws_dbc, int ndt, int B, int L, int N, void* dBm,
+                              void* dCm, int act, cudaStream_t stream);
+cudaError_t launch_reduce_params(const float* ws_param, int B, int D, int N, float* dA_log,
+                                 float* dDp, float* d_delta_bias, cudaStream_t stream);
+
+// ---------------------------------------------------------------- device helpers
+
+template <typename T>
+__device__ __forceinline__ float ld_act(const T* p);
+template <>
+__device__ __forceinline__ float ld_act<float>(const float* p) {
+  return __ldg(p);
+}
+template <>
+__device__ __forceinline__ float ld_act<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(__ldg(p));
+}
+
+template <typename T>
+__device__ __forceinline__ void st_act(T* p, float v);
+template <>
+__device__ __forceinline__ void st_act<float>(float* p, float v) {
+  *p = v;
+}
+template <>
+__device__ __forceinline__ void st_act<__nv_bfloat16>(__nv_bfloat16* p, float v) {
+  *p = __float2bfloat16_rn(v);
+}
+
+// softplus(s) = log(1 + e^s); above 20 it equals s to within 2e-9 relative
+// (the threshold the POPCORNBENCH kernel's softplus uses).
+__device__ __forceinline__ float softplus_f(float s) { return s > 20.f ? s : log1pf(expf(s)); }
+
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
+
+}  // namespace s6

@@ -6,13 +6,14 @@ tests/benchmark and the oracle's checks take their inputs from.
 
 Recipe (every workload):
   * one ``torch.Generator`` on the CPU, ``manual_seed(seed)`` (seed 0 by default);
-  * draw order: u, z, delta_raw, U (for delta_bias), Bm, Cm, dout, h0;
+  * draw order: u, z, delta_raw, U (for delta_bias), Bm, Cm, dout, h0, dh_last;
   * u, z, delta_raw, Bm, Cm, dout ~ N(0, 1) in float32;
   * delta_bias[d] = log(expm1(U[d])), U ~ Uniform[lo, hi], so that
     softplus(delta_bias) = U (the usual Mamba dt initialisation);
   * A_log[d, n] = log(n + 1) (S4D-real initialisation, A = -(n+1));
   * Dp[d] = 1;
   * h0 ~ N(0, h0_std^2) when requested (the decode workload uses std 0.5);
+  * dh_last ~ N(0, 1) when requested (gradient arriving at the final state);
   * activations (u, delta_raw, z, Bm, Cm, dout) are rounded once to bf16
     (round-to-nearest-even) when the workload is bf16; parameters and state
     stay float32.  Both sides then see exactly the same values.
@@ -73,11 +74,11 @@ def act_dtype(act: str) -> torch.dtype:
 def make_inputs(batch: int, seqlen: int, dim: int, dstate: int, act: str = "f32", *,
                 seed: int = 0, delta_lo: float = 1e-3, delta_hi: float = 0.1,
                 h0_std: Optional[float] = None, with_z: bool = True,
-                with_dout: bool = True) -> dict:
+                with_dout: bool = True, with_dh_last: bool = False) -> dict:
     """Draw one problem on the CPU.  Returns a dict of tensors:
 
     u, delta_raw, z, dout : [B, L, D] (act dtype);  Bm, Cm : [B, L, N] (act dtype)
-    A_log : [D, N], Dp : [D], delta_bias : [D] (float32);  h0 : [B, D, N] float32 or None
+    A_log : [D, N], Dp : [D], delta_bias : [D] (float32);  h0, dh_last : [B, D, N] float32 or None
     """
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
@@ -98,6 +99,7 @@ def make_inputs(batch: int, seqlen: int, dim: int, dstate: int, act: str = "f32"
     if not with_dout:
         dout = None
     h0 = normal((batch, dim, dstate)) * h0_std if h0_std is not None else None
+    dh_last = normal((batch, dim, dstate)) if with_dh_last else None
 
     delta_bias = torch.log(torch.expm1(U)).to(torch.float32)
     A_log = torch.log(torch.arange(1, dstate + 1, dtype=torch.float64)).to(torch.float32)
@@ -108,7 +110,7 @@ def make_inputs(batch: int, seqlen: int, dim: int, dstate: int, act: str = "f32"
     return {
         "u": cast(u), "delta_raw": cast(delta_raw), "z": cast(z) if with_z else None,
         "Bm": cast(Bm), "Cm": cast(Cm), "A_log": A_log, "Dp": Dp, "delta_bias": delta_bias,
-        "dout": cast(dout) if dout is not None else None, "h0": h0,
+        "dout": cast(dout) if dout is not None else None, "h0": h0, "dh_last": dh_last,
     }
 
 

@@ -1,0 +1,233 @@
+"""Thin Python binding of the C-ABI library ``libssm_s6.so`` (include/ssm_scan.h).
+
+Argument marshalling only: every step of the scan runs in the library's CUDA
+kernels.  PyTorch supplies the device memory (output tensors are allocated
+with ``torch.empty`` when not passed in) and the stream (the current torch
+stream unless one is given).  There is no CPU fallback: if the library is
+missing or a call fails, these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libssm_s6.so")
+_lock = threading.Lock()
+_lib = None
+
+SSM_F32, SSM_BF16 = 0, 1
+CHUNK_LEN = 64
+MAX_DSTATE = 16
+
+
+class SSMError(RuntimeError):
+    def __init__(self, fn, code, msg):
+        super().__init__(f"{fn} failed: {code} ({msg})")
+        self.code = code
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load ``libssm_s6.so`` (building it first if it is absent and nvcc exists)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            from . import build as _build
+            _build.build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        i64, vp, ci, sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        lib.ssm_status_string.argtypes = [ci]
+        lib.ssm_status_string.restype = ctypes.c_char_p
+        lib.ssm_last_error.argtypes = []
+        lib.ssm_last_error.restype = ctypes.c_char_p
+        lib.ssm_version.argtypes = []
+        lib.ssm_version.restype = ci
+        lib.ssm_num_chunks.argtypes = [i64]
+        lib.ssm_num_chunks.restype = i64
+        for f in (lib.ssm_fwd_workspace_bytes, lib.ssm_bwd_workspace_bytes):
+            f.argtypes = [i64, i64, i64, i64, ci]
+            f.restype = i64
+        lib.ssm_scan_fwd.argtypes = [i64] * 4 + [ci] + [vp] * 12 + [vp, sz, vp]
+        lib.ssm_scan_fwd.restype = ci
+        lib.ssm_scan_fwd_nosave.argtypes = [i64] * 4 + [ci] + [vp] * 11 + [vp, sz, vp]
+        lib.ssm_scan_fwd_nosave.restype = ci
+        lib.ssm_scan_bwd.argtypes = [i64] * 4 + [ci] + [vp] * 21 + [vp, sz, vp]
+        lib.ssm_scan_bwd.restype = ci
+        lib.ssm_scan_bwd_partials.argtypes = [i64] * 4 + [ci] + [vp] * 15 + [vp, sz, vp]
+        lib.ssm_scan_bwd_partials.restype = ci
+        lib.ssm_scan_bwd_finalize.argtypes = [i64] * 4 + [ci] + [vp] * 5 + [vp, sz, vp]
+        lib.ssm_scan_bwd_finalize.restype = ci
+        lib.ssm_step.argtypes = [i64] * 3 + [ci] + [vp] * 10 + [vp]
+        lib.ssm_step.restype = ci
+        _lib = lib
+        return lib
+
+
+def _check(fn, rc):
+    if rc != 0:
+        lib = load_library()
+        raise SSMError(fn, lib.ssm_status_string(rc).decode(), lib.ssm_last_error().decode())
+
+
+def _act(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SSM_F32
+    if t.dtype == torch.bfloat16:
+        return SSM_BF16
+    raise TypeError(f"activation dtype must be float32 or bfloat16, got {t.dtype}")
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def num_chunks(seqlen: int) -> int:
+    return int(load_library().ssm_num_chunks(seqlen))
+
+
+def fwd_workspace_bytes(batch, seqlen, dim, dstate, act) -> int:
+    return int(load_library().ssm_fwd_workspace_bytes(batch, seqlen, dim, dstate, act))
+
+
+def bwd_workspace_bytes(batch, seqlen, dim, dstate, act) -> int:
+    return int(load_library().ssm_bwd_workspace_bytes(batch, seqlen, dim, dstate, act))
+
+
+def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]):
+    if nbytes <= 0:
+        return ws, 0
+    if ws is None:
+        ws = torch.empty((nbytes + 256,), dtype=torch.uint8, device=device)
+    # the library wants 256-byte alignment; torch's caching allocator gives 512
+    if ws.numel() < nbytes or ws.data_ptr() % 256:
+        raise ValueError("workspace too small or misaligned")
+    return ws, ws.numel()
+
+
+def ssm_scan_fwd(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0=None, *, out=None,
+                 h_last=None, chunk_states=None, save=True, want_h_last=True, ws=None,
+                 stream=None):
+    """Forward scan.  Returns ``(out, h_last, chunk_states)`` (chunk_states None when
+    ``save=False``).  Shapes as in include/ssm_scan.h."""
+    B, L, D = u.shape
+    N = Bm.shape[-1]
+    act = _act(u)
+    dev = u.device
+    if out is None:
+        out = torch.empty_like(u)
+    if h_last is None and want_h_last:
+        h_last = torch.empty((B, D, N), dtype=torch.float32, device=dev)
+    lib = load_library()
+    ws, ws_bytes = _workspace(fwd_workspace_bytes(B, L, D, N, act), dev, ws)
+    if save:
+        if chunk_states is None:
+            chunk_states = torch.empty((B, num_chunks(L), D, N), dtype=torch.float32, device=dev)
+        rc = lib.ssm_scan_fwd(B, L, D, N, act, _p(u), _p(delta_raw), _p(z), _p(Bm), _p(Cm),
+                              _p(A_log), _p(Dp), _p(delta_bias), _p(h0), _p(out), _p(h_last),
+                              _p(chunk_states), _p(ws), ws_bytes, _stream(stream))
+        _check("ssm_scan_fwd", rc)
+        return out, h_last, chunk_states
+    rc = lib.ssm_scan_fwd_nosave(B, L, D, N, act, _p(u), _p(delta_raw), _p(z), _p(Bm), _p(Cm),
+                                 _p(A_log), _p(Dp), _p(delta_bias), _p(h0), _p(out),
+                                 _p(h_last), _p(ws), ws_bytes, _stream(stream))
+    _check("ssm_scan_fwd_nosave", rc)
+    return out, h_last, None
+
+
+def ssm_scan_fwd_nosave(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0=None, **kw):
+    out, h_last, _ = ssm_scan_fwd(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0,
+                                  save=False, **kw)
+    return out, h_last
+
+
+def ssm_scan_bwd(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0, chunk_states, dout,
+                 dh_last=None, *, grads=None, want_dh0=True, ws=None, stream=None, split=False):
+    """Backward.  Returns a dict with du, d_delta_raw, dz (None without z), dBm, dCm,
+    dA_log, dD, d_delta_bias, dh0 (None unless ``want_dh0``).  Pass ``grads`` (a dict
+    of preallocated tensors with those keys) to write into existing buffers."""
+    B, L, D = u.shape
+    N = Bm.shape[-1]
+    act = _act(u)
+    dev = u.device
+    g = dict(grads) if grads else {}
+    g.setdefault("du", torch.empty_like(u))
+    g.setdefault("d_delta_raw", torch.empty_like(u))
+    g.setdefault("dz", torch.empty_like(u) if z is not None else None)
+    g.setdefault("dBm", torch.empty_like(Bm))
+    g.setdefault("dCm", torch.empty_like(Cm))
+    g.setdefault("dA_log", torch.empty_like(A_log))
+    g.setdefault("dD", torch.empty_like(Dp))
+    g.setdefault("d_delta_bias", torch.empty_like(delta_bias))
+    g.setdefault("dh0", torch.empty((B, D, N), dtype=torch.float32, device=dev) if want_dh0 else None)
+    lib = load_library()
+    ws, ws_bytes = _workspace(bwd_workspace_bytes(B, L, D, N, act), dev, ws)
+    if split:
+        bwd_partials(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, chunk_states, dout, dh_last,
+                     g, ws, stream)
+        bwd_finalize(B, L, D, N, act, g, ws, stream)
+        return g
+    rc = lib.ssm_scan_bwd(B, L, D, N, act, _p(u), _p(delta_raw), _p(z), _p(Bm), _p(Cm),
+                          _p(A_log), _p(Dp), _p(delta_bias), _p(h0), _p(chunk_states),
+                          _p(dout), _p(dh_last), _p(g["du"]), _p(g["d_delta_raw"]),
+                          _p(g["dz"]), _p(g["dBm"]), _p(g["dCm"]), _p(g["dA_log"]),
+                          _p(g["dD"]), _p(g["d_delta_bias"]), _p(g["dh0"]), _p(ws), ws_bytes,
+                          _stream(stream))
+    _check("ssm_scan_bwd", rc)
+    return g
+
+
+def bwd_partials(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, chunk_states, dout, dh_last,
+                 g, ws, stream=None):
+    """First half of the backward (the scan); ``g`` holds preallocated outputs."""
+    B, L, D = u.shape
+    N = Bm.shape[-1]
+    rc = load_library().ssm_scan_bwd_partials(
+        B, L, D, N, _act(u), _p(u), _p(delta_raw), _p(z), _p(Bm), _p(Cm), _p(A_log), _p(Dp),
+        _p(delta_bias), _p(chunk_states), _p(dout), _p(dh_last), _p(g["du"]),
+        _p(g["d_delta_raw"]), _p(g["dz"]), _p(g.get("dh0")), _p(ws),
+        0 if ws is None else ws.numel(), _stream(stream))
+    _check("ssm_scan_bwd_partials", rc)
+
+
+def bwd_finalize(B, L, D, N, act, g, ws, stream=None):
+    """Second half of the backward: fixed-order sums of the partials left in ``ws``."""
+    rc = load_library().ssm_scan_bwd_finalize(
+        B, L, D, N, act, _p(g["dBm"]), _p(g["dCm"]), _p(g["dA_log"]), _p(g["dD"]),
+        _p(g["d_delta_bias"]), _p(ws), 0 if ws is None else ws.numel(), _stream(stream))
+    _check("ssm_scan_bwd_finalize", rc)
+
+
+def ssm_step(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h, *, out=None, stream=None):
+    """One decode step; ``h`` [B,D,N] f32 is updated in place.  Returns ``out`` [B,D]."""
+    B, D = u.shape
+    N = Bm.shape[-1]
+    act = _act(u)
+    if out is None:
+        out = torch.empty_like(u)
+    rc = load_library().ssm_step(B, D, N, act, _p(u), _p(delta_raw), _p(z), _p(Bm), _p(Cm),
+                                 _p(A_log), _p(Dp), _p(delta_bias), _p(h), _p(out),
+                                 _stream(stream))
+    _check("ssm_step", rc)
+    return out

@@ -1,0 +1,95 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function the
+header declares, and its host-only calls (status strings, sizes, argument
+validation that fails before any launch) behave as documented."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from selective_state_space_s6_gb300 import build, s6
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssm_scan.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssm_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return s6.load_library()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for f in ("ssm_scan_fwd", "ssm_scan_fwd_nosave", "ssm_scan_bwd", "ssm_step"):
+        assert f in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(s6.library_path())
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_status_strings_and_sizes(lib):
+    assert lib.ssm_status_string(0) == b"SSM_OK"
+    assert lib.ssm_status_string(3) == b"SSM_ERR_WORKSPACE"
+    assert lib.ssm_status_string(99) == b"SSM_ERR_UNKNOWN"
+    assert lib.ssm_version() >= 100
+    assert [lib.ssm_num_chunks(x) for x in (0, 1, 64, 65, 4096)] == [0, 1, 1, 2, 64]
+    assert lib.ssm_fwd_workspace_bytes(1, 64, 16, 4, 0) == 0
+    ws = lib.ssm_bwd_workspace_bytes(4, 4096, 4096, 16, 1)
+    # per-64-channel-tile dBm/dCm partials plus per-batch parameter partials
+    assert ws >= 64 * 4 * 4096 * 2 * 16 * 4 + 4 * 4096 * 18 * 4
+    assert ws % 256 == 0
+    assert lib.ssm_bwd_workspace_bytes(1, 8, 8, 0, 0) == -1
+    assert lib.ssm_bwd_workspace_bytes(1, 8, 8, 4, 7) == -1
+
+
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: every call below fails validation first
+
+
+def _fwd(lib, B=1, L=8, D=8, N=4, act=0, **over):
+    args = dict(u=FAKE, delta_raw=FAKE, z=None, Bm=FAKE, Cm=FAKE, A_log=FAKE, Dp=FAKE,
+                delta_bias=FAKE, h0=None, out=FAKE, h_last=None, chunk_states=FAKE)
+    args.update(over)
+    return lib.ssm_scan_fwd(B, L, D, N, act, *args.values(), None, 0, None)
+
+
+def test_fwd_argument_validation(lib):
+    assert _fwd(lib, N=0) == 1
+    assert _fwd(lib, N=17) == 2
+    assert _fwd(lib, B=-1) == 1
+    assert _fwd(lib, act=5) == 1
+    assert _fwd(lib, u=None) == 1
+    assert b"u must not be NULL" in lib.ssm_last_error()
+    assert _fwd(lib, chunk_states=None) == 1
+    assert _fwd(lib, Bm=ctypes.c_void_p(0x10002)) == 1  # f32 needs 4-byte alignment
+    assert b"aligned" in lib.ssm_last_error()
+
+
+def test_bwd_workspace_and_gradient_checks(lib):
+    B, L, D, N = 2, 16, 8, 4
+    need = lib.ssm_bwd_workspace_bytes(B, L, D, N, 0)
+    ptrs = [FAKE] * 21
+    # z given (index 2) but dz (index 14) missing -> invalid argument
+    p = list(ptrs)
+    p[14] = None
+    assert lib.ssm_scan_bwd(B, L, D, N, 0, *p, FAKE, need, None) == 1
+    assert b"dz" in lib.ssm_last_error()
+    # workspace too small
+    assert lib.ssm_scan_bwd(B, L, D, N, 0, *ptrs, FAKE, need - 4, None) == 3
+    assert lib.ssm_scan_bwd(B, L, D, N, 0, *ptrs, None, need, None) == 3
+
+
+def test_step_validation(lib):
+    args = [FAKE] * 10
+    args[8] = None  # h
+    assert lib.ssm_step(2, 8, 4, 0, *args, None) == 1
+    assert b"h must not be NULL" in lib.ssm_last_error()

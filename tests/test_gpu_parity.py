@@ -1,0 +1,263 @@
+"""Parity of the CUDA path (through the C ABI) with the f64 oracle.
+
+Small shapes are compared element by element on every output; they span
+several 64-channel tiles and 64-step chunks with ragged tails, every state
+count 1..16 (padded lanes), with and without the gate, initial state and
+final-state gradient.  Full-size workloads are compared on sampled channels
+(every batch, every step) and, for the channel sums dBm/dCm, on one whole
+batch, all in the launch configuration the benchmark times.
+"""
+import hashlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import (ARGS, GRAD_KEYS, TOL, act_of, compare_all, gpu_fwd_bwd, np64,
+                         oracle_fwd_bwd, rel_err, to_dev)
+from selective_state_space_s6_gb300 import inputs, s6
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(B, L, D, N, act, seed=0, z=True, h0=True, dh=True, **kw):
+    return inputs.make_inputs(B, L, D, N, act, seed=seed, with_z=z,
+                              h0_std=0.5 if h0 else None, with_dh_last=dh, **kw)
+
+
+SMALL = [
+    # B, L, D, N, act
+    (1, 64, 16, 4, "f32"),     # the tiny workload's shape
+    (2, 1, 3, 1, "f32"),       # single step, single state
+    (1, 65, 17, 3, "f32"),     # ragged chunk (65 = 64 + 1), ragged tile, odd N
+    (3, 130, 70, 16, "f32"),   # two tiles, three chunks
+    (2, 200, 65, 5, "bf16"),
+    (1, 64, 64, 16, "bf16"),
+    (2, 129, 128, 8, "f32"),
+    (1, 300, 33, 2, "bf16"),
+    (1, 77, 130, 16, "bf16"),
+]
+
+
+@pytest.mark.parametrize("B,L,D,N,act", SMALL)
+@pytest.mark.parametrize("variant", ["full", "nogate_noh0"])
+def test_small_parity(B, L, D, N, act, variant):
+    full = variant == "full"
+    x = _inputs(B, L, D, N, act, seed=B * 1000 + L + D + N, z=full, h0=full, dh=full)
+    gpu = gpu_fwd_bwd(to_dev(x), dh_last=x["dh_last"].cuda() if full else None)
+    ref = oracle_fwd_bwd(x, dh_last=x["dh_last"])
+    errs = compare_all(gpu, ref, TOL[act])
+    assert errs
+
+
+def test_tiny_workload_every_output_and_chunk_states():
+    x = inputs.make_workload("tiny")
+    gpu = gpu_fwd_bwd(to_dev(x))
+    ref = oracle_fwd_bwd(x)
+    compare_all(gpu, ref, TOL["f32"])
+    # chunk state c = state before step c*64 = h_last of the first c*64 steps
+    x2 = _inputs(2, 200, 24, 16, "f32", seed=5)
+    g2 = gpu_fwd_bwd(to_dev(x2), want_bwd=False)
+    cs = np64(g2["chunk_states"])
+    assert cs.shape == (2, 4, 24, 16)
+    assert np.array_equal(cs[:, 0], x2["h0"].double().numpy())
+    for c in range(1, 4):
+        sub = {k: (v[:, : c * 64].contiguous() if k in ("u", "delta_raw", "z", "Bm", "Cm") else v)
+               for k, v in x2.items()}
+        _, h_ref = oracle.fwd(*[sub[k] for k in ARGS], sub["h0"])
+        assert rel_err(cs[:, c], h_ref) <= TOL["f32"]
+
+
+def test_nosave_matches_save():
+    x = to_dev(_inputs(2, 150, 70, 16, "bf16", seed=3))
+    o1, h1, _ = s6.ssm_scan_fwd(*[x[k] for k in ARGS], x["h0"])
+    o2, h2 = s6.ssm_scan_fwd_nosave(*[x[k] for k in ARGS], x["h0"])
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
+@pytest.mark.parametrize("act", ["f32", "bf16"])
+def test_step_chain_equals_scan(act):
+    B, L, D, N = 3, 40, 70, 16
+    x = _inputs(B, L, D, N, act, seed=11)
+    xd = to_dev(x)
+    out_scan, h_scan, _ = s6.ssm_scan_fwd(*[xd[k] for k in ARGS], xd["h0"])
+    h = xd["h0"].clone()
+    outs = []
+    for t in range(L):
+        sl = {k: xd[k][:, t].contiguous() for k in ("u", "delta_raw", "z", "Bm", "Cm")}
+        outs.append(s6.ssm_step(sl["u"], sl["delta_raw"], sl["z"], sl["Bm"], sl["Cm"],
+                                xd["A_log"], xd["Dp"], xd["delta_bias"], h))
+    out_step = torch.stack(outs, dim=1)
+    # same per-step arithmetic in registers vs. through memory: bit-identical
+    assert torch.equal(out_step, out_scan)
+    assert torch.equal(h, h_scan)
+    ref_out, ref_h = oracle.fwd(*[x[k] for k in ARGS], x["h0"])
+    assert rel_err(np64(out_step), ref_out) <= TOL[act]
+    assert rel_err(np64(h), ref_h) <= TOL[act]
+
+
+def _digest(tensors):
+    m = hashlib.sha256()
+    for t in tensors:
+        if t is not None:
+            m.update(t.detach().contiguous().view(torch.uint8).cpu().numpy().tobytes())
+    return m.hexdigest()
+
+
+@pytest.mark.parametrize("shape", [(1, 64, 16, 4, "f32"), (3, 700, 200, 16, "bf16")])
+def test_bitwise_deterministic_10_runs(shape):
+    x = to_dev(_inputs(*shape, seed=21))
+    digests = set()
+    for _ in range(10):
+        r = gpu_fwd_bwd(x, dh_last=x["dh_last"])
+        digests.add(_digest([r["out"], r["h_last"], r["chunk_states"]] + [r[k] for k in GRAD_KEYS]))
+    assert len(digests) == 1
+
+
+def test_empty_inputs():
+    # L = 0: no steps; h_last = h0, parameter gradients 0, dh0 = dh_last
+    x = to_dev(_inputs(2, 0, 5, 3, "f32", seed=1))
+    r = gpu_fwd_bwd(x, dh_last=x["dh_last"])
+    assert r["out"].numel() == 0 and r["chunk_states"].numel() == 0
+    assert torch.equal(r["h_last"], x["h0"])
+    assert torch.equal(r["dh0"], x["dh_last"])
+    for k in ("dA_log", "dD", "d_delta_bias"):
+        assert torch.count_nonzero(r[k]) == 0
+    # B = 0: parameter gradients 0
+    x = to_dev(_inputs(0, 10, 5, 3, "bf16", seed=1))
+    r = gpu_fwd_bwd(x)
+    for k in ("dA_log", "dD", "d_delta_bias"):
+        assert torch.count_nonzero(r[k]) == 0
+    # D = 0: nothing to do, no error
+    x = to_dev(_inputs(2, 10, 0, 3, "f32", seed=1))
+    gpu_fwd_bwd(x)
+    torch.cuda.synchronize()
+
+
+def test_extreme_decay_and_skip():
+    """Large |A| (state resets every step) and delta -> 0 (skip path only)."""
+    x = _inputs(2, 100, 70, 16, "f32", seed=8)
+    x["A_log"] = torch.full_like(x["A_log"], 60.0)
+    gpu = gpu_fwd_bwd(to_dev(x), dh_last=x["dh_last"].cuda())
+    ref = oracle_fwd_bwd(x, dh_last=x["dh_last"])
+    compare_all(gpu, ref, TOL["f32"])
+    x = _inputs(2, 100, 70, 16, "f32", seed=9)
+    x["delta_raw"] = torch.full_like(x["delta_raw"], -120.0)  # softplus underflows in f32
+    gpu = gpu_fwd_bwd(to_dev(x), dh_last=x["dh_last"].cuda())
+    ref = oracle_fwd_bwd(x, dh_last=x["dh_last"])
+    compare_all(gpu, ref, TOL["f32"], keys=("out", "h_last", "du", "dz", "dCm", "dD", "dh0"))
+    # the rest scale with delta ~ e^-120 in the oracle and must be (close to) zero here
+    for k in ("d_delta_raw", "dBm", "dA_log", "d_delta_bias"):
+        assert float(torch.max(torch.abs(gpu[k]))) <= 1e-30, k
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+def _windows(D):
+    # tile edges and the middle: channels 0..3, D/2-2..D/2+1, D-4..D-1
+    return [(0, 4), (D // 2 - 2, D // 2 + 2), (D - 4, D)]
+
+
+BLD = ("u", "delta_raw", "z", "dout")
+PER_D = ("A_log", "Dp", "delta_bias")
+
+
+def slice_problem(x, b=None, d=None):
+    """The sub-problem on batches ``b`` / channels ``d`` (slices).  Channels are
+    independent scans, so every per-channel output of the sub-problem equals the
+    full problem's; only the channel sums dBm/dCm become partial sums."""
+    bs = b if b is not None else slice(None)
+    ds = d if d is not None else slice(None)
+    y = {}
+    for k, v in x.items():
+        if v is None:
+            y[k] = None
+        elif k in BLD:
+            y[k] = v[bs, :, ds].contiguous()
+        elif k in ("Bm", "Cm"):
+            y[k] = v[bs].contiguous()
+        elif k in PER_D:
+            y[k] = v[ds].contiguous()
+        elif k in ("h0", "dh_last"):
+            y[k] = v[bs, ds].contiguous()
+        else:
+            y[k] = v
+    return y
+
+
+def _check_sampled(x, gpu, act):
+    """Per-channel outputs and parameter gradients on sampled channel windows."""
+    tol = TOL[act]
+    errs = {}
+    for (d0, d1) in _windows(x["u"].shape[2]):
+        ref = oracle_fwd_bwd(slice_problem(x, d=slice(d0, d1)))
+        for k in ("out", "du", "d_delta_raw", "dz"):
+            errs[(k, d0)] = rel_err(np64(gpu[k][:, :, d0:d1]), ref[k])
+        errs[("h_last", d0)] = rel_err(np64(gpu["h_last"][:, d0:d1]), ref["h_last"])
+        for k in ("dA_log", "dD", "d_delta_bias"):
+            errs[(k, d0)] = rel_err(np64(gpu[k][d0:d1]), ref[k])
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"sampled errors above {tol}: {bad}"
+    return errs
+
+
+@pytest.mark.parametrize("name", ["mamba130m", "mamba1p4b"])
+def test_full_size_training_workloads(name):
+    x = inputs.make_workload(name)
+    act = inputs.WORKLOADS[name].act
+    xd = to_dev(x)
+    gpu = gpu_fwd_bwd(xd)
+    _check_sampled(x, gpu, act)
+    # channel sums dBm / dCm: one whole batch against the oracle over all channels
+    B = x["u"].shape[0]
+    xb = slice_problem(x, b=slice(B - 1, B))
+    ref = oracle.bwd(*[xb[k] for k in ARGS], None, xb["dout"])
+    for k in ("dBm", "dCm"):
+        assert rel_err(np64(gpu[k][B - 1:]), ref[k]) <= TOL[act], k
+    # bit-identical on repeat
+    d1 = _digest([gpu[k] for k in GRAD_KEYS])
+    d2 = _digest([v for k, v in gpu_fwd_bwd(xd).items() if k in GRAD_KEYS])
+    assert d1 == d2
+
+
+def test_full_size_long_sequence():
+    name = "long"
+    x = inputs.make_workload(name)
+    xd = to_dev(x)
+    gpu = gpu_fwd_bwd(xd)
+    _check_sampled(x, gpu, "f32")
+    # channel sums over a 128-channel slice (two tiles): the scan restricted to channels 0..127
+    sl = slice_problem(x, d=slice(0, 128))
+    gs = gpu_fwd_bwd(to_dev(sl))
+    ref = oracle.bwd(*[sl[k] for k in ARGS], None, sl["dout"])
+    for k in ("dBm", "dCm"):
+        assert rel_err(np64(gs[k]), ref[k]) <= TOL["f32"], k
+    # whole-problem identity at any size: sum dBm*Bm = sum (du - Dp*dy) * u
+    z = xd["z"].double()
+    dy = xd["dout"].double() * z * torch.sigmoid(z)
+    lhs = (gpu["dBm"].double() * xd["Bm"].double()).sum()
+    rhs = ((gpu["du"].double() - xd["Dp"].double() * dy) * xd["u"].double()).sum()
+    assert abs(float(lhs - rhs)) <= 1e-4 * float(torch.abs(gpu["dBm"].double() * xd["Bm"].double()).sum())
+
+
+def test_decode_1000_chained_steps():
+    w = inputs.WORKLOADS["decode"]
+    x = inputs.make_workload("decode", with_dout=False)
+    xd = to_dev(x)
+    h = xd["h0"].clone()
+    out_steps = torch.empty_like(xd["u"])
+    for t in range(w.seqlen):
+        sl = {k: xd[k][:, t].contiguous() for k in ("u", "delta_raw", "z", "Bm", "Cm")}
+        out_steps[:, t] = s6.ssm_step(sl["u"], sl["delta_raw"], sl["z"], sl["Bm"], sl["Cm"],
+                                      xd["A_log"], xd["Dp"], xd["delta_bias"], h)
+    out_scan, h_scan, _ = s6.ssm_scan_fwd(*[xd[k] for k in ARGS], xd["h0"], save=False)
+    assert torch.equal(out_steps, out_scan)
+    assert torch.equal(h, h_scan)
+    errs = []
+    for (d0, d1) in _windows(w.dim):
+        xs = slice_problem(x, d=slice(d0, d1))
+        ref_out, ref_h = oracle.fwd(*[xs[k] for k in ARGS], xs["h0"])
+        errs.append(rel_err(np64(out_steps[:, :, d0:d1]), ref_out))
+        errs.append(rel_err(np64(h[:, d0:d1]), ref_h))
+    assert max(errs) <= TOL["f32"], errs
