@@ -39,14 +39,18 @@ int check_shape(int64_t B, int64_t L, int64_t D, int64_t N, int act) {
   return SSM_OK;
 }
 
-// A required pointer must be non-NULL and aligned to its element size.
-int need(const void* p, size_t align, const char* name) {
-  if (!p) return fail(SSM_ERR_INVALID_ARG, "%s must not be NULL", name);
+// A required pointer to `count` elements must be non-NULL (unless the tensor
+// is empty) and aligned to its element size.
+int need(const void* p, int64_t count, size_t align, const char* name) {
+  if (!p) {
+    if (count == 0) return SSM_OK;
+    return fail(SSM_ERR_INVALID_ARG, "%s must not be NULL", name);
+  }
   if (!aligned(p, align)) return fail(SSM_ERR_INVALID_ARG, "%s is not %zu-byte aligned", name, align);
   return SSM_OK;
 }
 int opt(const void* p, size_t align, const char* name) {
-  return p ? need(p, align, name) : SSM_OK;
+  return p ? need(p, 1, align, name) : SSM_OK;
 }
 
 #define S6_TRY(x)                    \
@@ -87,18 +91,19 @@ int fwd_common(int64_t B, int64_t L, int64_t D, int64_t N, int act, const void* 
                void* out, float* h_last, float* chunk_states, bool save, void* stream) {
   S6_TRY(check_shape(B, L, D, N, act));
   const size_t e = act_size(act);
-  S6_TRY(need(u, e, "u"));
-  S6_TRY(need(delta_raw, e, "delta_raw"));
+  const int64_t bld = B * L * D, bln = B * L * N, dn = D * N;
+  S6_TRY(need(u, bld, e, "u"));
+  S6_TRY(need(delta_raw, bld, e, "delta_raw"));
   S6_TRY(opt(z, e, "z"));
-  S6_TRY(need(Bm, e, "Bm"));
-  S6_TRY(need(Cm, e, "Cm"));
-  S6_TRY(need(A_log, 4, "A_log"));
-  S6_TRY(need(Dp, 4, "Dp"));
-  S6_TRY(need(delta_bias, 4, "delta_bias"));
+  S6_TRY(need(Bm, bln, e, "Bm"));
+  S6_TRY(need(Cm, bln, e, "Cm"));
+  S6_TRY(need(A_log, dn, 4, "A_log"));
+  S6_TRY(need(Dp, D, 4, "Dp"));
+  S6_TRY(need(delta_bias, D, 4, "delta_bias"));
   S6_TRY(opt(h0, 4, "h0"));
-  S6_TRY(need(out, e, "out"));
+  S6_TRY(need(out, bld, e, "out"));
   S6_TRY(opt(h_last, 4, "h_last"));
-  if (save) S6_TRY(need(chunk_states, 4, "chunk_states"));
+  if (save) S6_TRY(need(chunk_states, B * ssm_num_chunks(L) * dn, 4, "chunk_states"));
   g_last_error[0] = 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (B == 0 || D == 0) return SSM_OK;
@@ -186,20 +191,21 @@ int ssm_scan_bwd_partials(int64_t batch, int64_t seqlen, int64_t dim, int64_t ds
   const int64_t B = batch, L = seqlen, D = dim, N = dstate;
   S6_TRY(check_shape(B, L, D, N, act));
   const size_t e = act_size(act);
-  S6_TRY(need(u, e, "u"));
-  S6_TRY(need(delta_raw, e, "delta_raw"));
+  const int64_t bld = B * L * D, bln = B * L * N, dn = D * N;
+  S6_TRY(need(u, bld, e, "u"));
+  S6_TRY(need(delta_raw, bld, e, "delta_raw"));
   S6_TRY(opt(z, e, "z"));
-  S6_TRY(need(Bm, e, "Bm"));
-  S6_TRY(need(Cm, e, "Cm"));
-  S6_TRY(need(A_log, 4, "A_log"));
-  S6_TRY(need(Dp, 4, "Dp"));
-  S6_TRY(need(delta_bias, 4, "delta_bias"));
-  S6_TRY(need(chunk_states, 4, "chunk_states"));
-  S6_TRY(need(dout, e, "dout"));
+  S6_TRY(need(Bm, bln, e, "Bm"));
+  S6_TRY(need(Cm, bln, e, "Cm"));
+  S6_TRY(need(A_log, dn, 4, "A_log"));
+  S6_TRY(need(Dp, D, 4, "Dp"));
+  S6_TRY(need(delta_bias, D, 4, "delta_bias"));
+  S6_TRY(need(chunk_states, B * ssm_num_chunks(L) * dn, 4, "chunk_states"));
+  S6_TRY(need(dout, bld, e, "dout"));
   S6_TRY(opt(dh_last, 4, "dh_last"));
-  S6_TRY(need(du, e, "du"));
-  S6_TRY(need(d_delta_raw, e, "d_delta_raw"));
-  if (z) S6_TRY(need(dz, e, "dz (required when z is given)"));
+  S6_TRY(need(du, bld, e, "du"));
+  S6_TRY(need(d_delta_raw, bld, e, "d_delta_raw"));
+  if (z) S6_TRY(need(dz, bld, e, "dz (required when z is given)"));
   S6_TRY(opt(dh0, 4, "dh0"));
   const BwdWorkspace w = bwd_ws_layout(B, L, D, N);
   S6_TRY(check_ws(ws, ws_bytes, w.total));
@@ -225,11 +231,11 @@ int ssm_scan_bwd_finalize(int64_t batch, int64_t seqlen, int64_t dim, int64_t ds
   const int64_t B = batch, L = seqlen, D = dim, N = dstate;
   S6_TRY(check_shape(B, L, D, N, act));
   const size_t e = act_size(act);
-  S6_TRY(need(dBm, e, "dBm"));
-  S6_TRY(need(dCm, e, "dCm"));
-  S6_TRY(need(dA_log, 4, "dA_log"));
-  S6_TRY(need(dDp, 4, "dDp"));
-  S6_TRY(need(d_delta_bias, 4, "d_delta_bias"));
+  S6_TRY(need(dBm, B * L * N, e, "dBm"));
+  S6_TRY(need(dCm, B * L * N, e, "dCm"));
+  S6_TRY(need(dA_log, D * N, 4, "dA_log"));
+  S6_TRY(need(dDp, D, 4, "dDp"));
+  S6_TRY(need(d_delta_bias, D, 4, "d_delta_bias"));
   const BwdWorkspace w = bwd_ws_layout(B, L, D, N);
   S6_TRY(check_ws(ws, ws_bytes, w.total));
   g_last_error[0] = 0;
@@ -261,11 +267,11 @@ int ssm_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int
   const size_t e = (act == SSM_BF16) ? 2 : 4;
   // validate the finalize outputs before enqueueing the first half
   S6_TRY(check_shape(batch, seqlen, dim, dstate, act));
-  S6_TRY(need(dBm, e, "dBm"));
-  S6_TRY(need(dCm, e, "dCm"));
-  S6_TRY(need(dA_log, 4, "dA_log"));
-  S6_TRY(need(dDp, 4, "dDp"));
-  S6_TRY(need(d_delta_bias, 4, "d_delta_bias"));
+  S6_TRY(need(dBm, batch * seqlen * dstate, e, "dBm"));
+  S6_TRY(need(dCm, batch * seqlen * dstate, e, "dCm"));
+  S6_TRY(need(dA_log, dim * dstate, 4, "dA_log"));
+  S6_TRY(need(dDp, dim, 4, "dDp"));
+  S6_TRY(need(d_delta_bias, dim, 4, "d_delta_bias"));
   S6_TRY(ssm_scan_bwd_partials(batch, seqlen, dim, dstate, act, u, delta_raw, z, Bm, Cm, A_log,
                                Dp, delta_bias, chunk_states, dout, dh_last, du, d_delta_raw, dz,
                                dh0, ws, ws_bytes, stream));
@@ -277,7 +283,7 @@ int ssm_step(int64_t batch, int64_t dim, int64_t dstate, int act, const void* u,
              const void* delta_raw, const void* z, const void* Bm, const void* Cm,
              const float* A_log, const float* Dp, const float* delta_bias, float* h, void* out,
              void* stream) {
-  S6_TRY(need(h, 4, "h"));
+  S6_TRY(need(h, batch * dim * (dstate > 0 ? dstate : 0), 4, "h"));
   return fwd_common(batch, 1, dim, dstate, act, u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias,
                     h, out, h, nullptr, false, stream);
 }

@@ -32,6 +32,14 @@ struct RedLayout {
   __device__ static int at(int q, int d, int n) { return q * kQ + (d >> 4) * kGroup + (d & 15) * NP + n; }
 };
 
+// sum += x with a running compensation term (Kahan); plain IEEE ops, no reassociation.
+__device__ __forceinline__ void kahan_add(float& sum, float& comp, float x) {
+  const float y = __fsub_rn(x, comp);
+  const float t = __fadd_rn(sum, y);
+  comp = __fsub_rn(__fsub_rn(t, sum), y);
+  sum = t;
+}
+
 template <typename Act, int NG>
 __global__ void __launch_bounds__(kScanThreads)
     s6_bwd_kernel(const BwdParams p) {
@@ -50,18 +58,22 @@ __global__ void __launch_bounds__(kScanThreads)
   const int dc = dvalid ? d : p.D - 1;
   const int L = p.L, D = p.D, N = p.N;
 
-  float A[NG], g[NG], accA[NG];
+  // Parameter-gradient sums over t: each chunk sums its kChunk terms in
+  // registers (accA, accD, accBias), and the chunk sums are added into the
+  // totals with a compensated (Kahan) add, so long sequences keep f32 accuracy.
+  float A[NG], g[NG], accA[NG], totA[NG], cmpA[NG];
 #pragma unroll
   for (int i = 0; i < NG; ++i) {
     const int n = half * NG + i;
     const bool nv = n < N;
     A[i] = nv ? -expf(p.A_log[dc * N + n]) : 0.f;
     g[i] = (nv && p.dh_last && dvalid) ? p.dh_last[((size_t)b * D + d) * N + n] : 0.f;
-    accA[i] = 0.f;
+    totA[i] = 0.f;
+    cmpA[i] = 0.f;
   }
   const float bias = p.delta_bias[dc];
   const float Dd = p.Dp[dc];
-  float accD = 0.f, accBias = 0.f;
+  float totD = 0.f, cmpD = 0.f, totBias = 0.f, cmpBias = 0.f;
 
   const size_t row0 = (size_t)b * L * D + dc;
   const Act* up = static_cast<const Act*>(p.u) + row0;
@@ -78,12 +90,14 @@ __global__ void __launch_bounds__(kScanThreads)
   const int red_o = tid >> 2, red_r = tid & 3;
   const int red_q = red_o / NP, red_n = red_o % NP;
   const bool red_active = red_o < 2 * NP;
-  const int ndt = gridDim.x;
 
   int step_parity = 0;
   for (int c = p.nchunks - 1; c >= 0; --c) {
     const int t0 = c * kChunk;
     const int t1 = min(t0 + kChunk, L);
+    float accD = 0.f, accBias = 0.f;
+#pragma unroll
+    for (int i = 0; i < NG; ++i) accA[i] = 0.f;
     // ---- pass A: forward recompute from the chunk state, checkpoint every kSub steps
     float h[NG];
     {
@@ -202,8 +216,11 @@ __global__ void __launch_bounds__(kScanThreads)
         }
       }
     }
+#pragma unroll
+    for (int i = 0; i < NG; ++i) kahan_add(totA[i], cmpA[i], accA[i]);
+    kahan_add(totD, cmpD, accD);
+    kahan_add(totBias, cmpBias, accBias);
   }
-  (void)ndt;
   // ---- per-batch parameter-gradient partials and dh0
   if (dvalid) {
     float* wp = p.ws_param + ((size_t)b * D + d) * (N + 2);
@@ -211,13 +228,13 @@ __global__ void __launch_bounds__(kScanThreads)
     for (int i = 0; i < NG; ++i) {
       const int n = half * NG + i;
       if (n < N) {
-        wp[n] = A[i] * accA[i];
+        wp[n] = A[i] * totA[i];
         if (p.dh0) p.dh0[((size_t)b * D + d) * N + n] = g[i];
       }
     }
     if (half == 0) {
-      wp[N] = accD;
-      wp[N + 1] = accBias;
+      wp[N] = totD;
+      wp[N + 1] = totBias;
     }
   }
 }
