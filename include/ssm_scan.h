@@ -78,6 +78,12 @@ const char *ssm_last_error(void);
 /* Library version as major*10000 + minor*100 + patch. */
 int ssm_version(void);
 
+/* Synchronises `stream`, then reads and clears the library's device status
+ * word on the current device.  Returns SSM_ERR_TIMEOUT if a kernel's bounded
+ * pipeline wait gave up since the last check (its outputs are then invalid),
+ * SSM_ERR_CUDA if the stream reports an error, else SSM_OK. */
+int ssm_check_device_status(void *stream);
+
 /* Number of saved chunk states: ceil(seqlen / SSM_CHUNK_LEN); 0 for seqlen <= 0. */
 int64_t ssm_num_chunks(int64_t seqlen);
 

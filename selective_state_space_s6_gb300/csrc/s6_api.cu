@@ -4,7 +4,32 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "s6_internal.cuh"
+
+namespace s6 {
+
+// The library's device status word: bounded device-side waits that give up
+// set bits here (kStatusWaitTimeout); ssm_check_device_status() reads and
+// clears it.  One copy per device; its address is looked up per device.
+__device__ unsigned int g_s6_status = 0;
+
+unsigned int* device_status_word() {
+  static std::mutex mu;
+  static unsigned int* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_s6_status) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<unsigned int*>(a);
+  }
+  return addr[dev];
+}
+
+}  // namespace s6
 
 namespace {
 
@@ -122,7 +147,9 @@ int fwd_common(int64_t B, int64_t L, int64_t D, int64_t N, int act, const void* 
   p.out = out; p.h_last = h_last; p.chunk_states = save ? chunk_states : nullptr;
   p.B = (int)B; p.L = (int)L; p.D = (int)D; p.N = (int)N;
   p.nchunks = (int)ssm_num_chunks(L);
-  cudaError_t ce = s6::launch_fwd(p, act, st);
+  p.status = s6::device_status_word();
+  if (!p.status) return fail(SSM_ERR_CUDA, "cannot locate the device status word");
+  cudaError_t ce = s6::fwd_tma_supported(p, act) ? s6::launch_fwd_tma(p, act, st) : s6::launch_fwd(p, act, st);
   if (ce != cudaSuccess) return cuda_fail(ce, "ssm_scan_fwd launch");
   return SSM_OK;
 }
@@ -147,6 +174,20 @@ const char* ssm_status_string(int status) {
 const char* ssm_last_error(void) { return g_last_error; }
 
 int ssm_version(void) { return 100; }
+
+int ssm_check_device_status(void* stream) {
+  unsigned int* w = s6::device_status_word();
+  if (!w) return fail(SSM_ERR_CUDA, "cannot locate the device status word");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned int v = 0;
+  cudaError_t ce = cudaMemcpyAsync(&v, w, sizeof(v), cudaMemcpyDeviceToHost, st);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(st);
+  if (ce == cudaSuccess && v != 0) ce = cudaMemsetAsync(w, 0, sizeof(v), st);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(st);
+  if (ce != cudaSuccess) return cuda_fail(ce, "ssm_check_device_status");
+  if (v & s6::kStatusWaitTimeoutBit) return fail(SSM_ERR_TIMEOUT, "a device-side wait gave up (status 0x%x)", v);
+  return SSM_OK;
+}
 
 int64_t ssm_num_chunks(int64_t seqlen) {
   return seqlen <= 0 ? 0 : (seqlen + SSM_CHUNK_LEN - 1) / SSM_CHUNK_LEN;

@@ -1,0 +1,380 @@
+// S6 forward, TMA-pipelined (sm_103a).
+//
+// CTA = (64-channel tile, batch); 6 warps:
+//   warps 0-3  consumers: lane pair (d, half) holds states half*NG .. half*NG+NG-1
+//              of channel d in registers and walks the sequence in order;
+//   warp 4     producer: one lane streams [TT x 64] tiles of u, delta_raw, z and
+//              [TT x N] tiles of Bm, Cm into an S-stage shared-memory ring with
+//              cp.async.bulk.tensor (TMA), completion tracked by mbarriers;
+//   warp 5     converter (bf16 only): widens each stage's Bm/Cm tile to f32 once,
+//              for all 64 channels.
+// Per step a lane does, for its NG states, x = delta*A*log2(e), Abar = 2^x,
+// h = Abar*h + (delta*u)*B, y += C*h with packed f32x2 multiplies / FMAs, so
+// one instruction covers two states.  The softplus of a step is computed by
+// one lane of the pair (even steps: lane 0, odd steps: lane 1) and shared by
+// a shuffle; the two partial readouts are exchanged the same way, and each
+// lane of the pair then gates and stores the output of "its" step.  Every
+// SSM_CHUNK_LEN steps the state is stored as a chunk state (the activation
+// saves of the kernels.rs page's multi-step forward).
+//
+// All pipeline waits are bounded (s6_tma.cuh); nothing else spins.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+#include <type_traits>
+
+#include "s6_internal.cuh"
+#include "s6_tma.cuh"
+
+namespace s6 {
+
+namespace {
+
+constexpr int kTT = 32;          // steps per pipeline stage
+constexpr int kFwdWarps = 6;     // 4 consumers + producer + converter
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <typename Act>
+struct FwdCfg {
+  static constexpr int kStages = std::is_same<Act, float>::value ? 3 : 4;
+};
+
+struct FwdTmaParams {
+  CUtensorMap map_u, map_raw, map_z, map_B, map_C;  // 64-byte aligned members first
+  FwdParams p;
+};
+
+template <typename Act>
+__device__ __forceinline__ float lds_act(const Act* p);
+template <>
+__device__ __forceinline__ float lds_act<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float lds_act<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+
+// softplus(s) = max(s, 0) + log1p(e^-|s|), evaluated on the special-function
+// unit; the series e - e^2/2 + e^3/3 covers e < 2^-6, where log2(1 + e) loses
+// relative precision.
+__device__ __forceinline__ float softplus_fast(float s) {
+  const float e = ex2_approx(-fabsf(s) * kLog2e);
+  const float lg = lg2_approx(1.f + e) * kLn2;
+  const float ser = e * fmaf(e, fmaf(e, 1.f / 3.f, -0.5f), 1.f);
+  return fmaxf(s, 0.f) + (e < 0.015625f ? ser : lg);
+}
+
+__device__ __forceinline__ float silu_fast(float z) {
+  return z * rcp_approx(1.f + ex2_approx(-z * kLog2e));
+}
+
+template <bool kFast>
+__device__ __forceinline__ float softplus_k(float s) {
+  return kFast ? softplus_fast(s) : softplus_f(s);
+}
+template <bool kFast>
+__device__ __forceinline__ float silu_k(float z) {
+  return kFast ? silu_fast(z) : z * sigmoid_f(z);
+}
+
+// Abar for a pair of states: fast path 2^(delta * A*log2e) on the SFU,
+// accurate path expf(delta * A).
+template <bool kFast>
+__device__ __forceinline__ float2 decay2(float2 dd, float2 A) {
+  const float2 x = fmul2(dd, A);
+  if (kFast) return make_float2(ex2_approx(x.x), ex2_approx(x.y));
+  return make_float2(expf(x.x), expf(x.y));
+}
+
+template <typename Act, int NG, bool kSave, bool kFast, bool kGate>
+__global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid_constant__ FwdTmaParams P) {
+  constexpr int N2 = 2 * NG;  // == N on this path
+  constexpr int S = FwdCfg<Act>::kStages;
+  constexpr int kTile = kTT * kDTile;  // elements of a [TT x 64] tile
+  constexpr int kBC = kTT * N2;        // elements of a [TT x N] tile
+  constexpr bool kBf16 = std::is_same<Act, __nv_bfloat16>::value;
+  constexpr int kStageElems = 3 * kTile + 2 * kBC;
+
+  extern __shared__ __align__(1024) unsigned char smem[];
+  Act* stages = reinterpret_cast<Act*>(smem);
+  float* bcf = reinterpret_cast<float*>(smem + (size_t)S * kStageElems * sizeof(Act));  // [S][TT][2][N2]
+  uint64_t* full = reinterpret_cast<uint64_t*>(bcf + (kBf16 ? S * kTT * 2 * N2 : 0));
+  uint64_t* conv = full + S;
+  uint64_t* empty = conv + S;
+
+  const FwdParams& p = P.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.y, d0 = blockIdx.x * kDTile;
+  const int L = p.L, D = p.D;
+  const int ntiles = (L + kTT - 1) / kTT;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&conv[s], 32);
+      mbar_init(&empty[s], 4);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  auto tile_u = [&](int s) { return stages + (size_t)s * kStageElems; };
+  auto tile_raw = [&](int s) { return stages + (size_t)s * kStageElems + kTile; };
+  auto tile_z = [&](int s) { return stages + (size_t)s * kStageElems + 2 * kTile; };
+  auto tile_B = [&](int s) { return stages + (size_t)s * kStageElems + 3 * kTile; };
+  auto tile_C = [&](int s) { return stages + (size_t)s * kStageElems + 3 * kTile + kBC; };
+
+  if (warp == 4) {
+    // ---------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&P.map_u);
+      tma_prefetch_desc(&P.map_raw);
+      if (kGate) tma_prefetch_desc(&P.map_z);
+      tma_prefetch_desc(&P.map_B);
+      tma_prefetch_desc(&P.map_C);
+      const uint32_t bytes = (uint32_t)(((kGate ? 3 : 2) * kTile + 2 * kBC) * sizeof(Act));
+      int issued = 0;
+      for (int k = 0; k < ntiles; ++k) {
+        const int s = k % S;
+        const uint32_t use = (uint32_t)(k / S);
+        if (k >= S && !mbar_wait(&empty[s], (use - 1) & 1, p.status)) break;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        const int row = b * L + k * kTT;
+        tma_load_2d(tile_u(s), &P.map_u, &full[s], d0, row);
+        tma_load_2d(tile_raw(s), &P.map_raw, &full[s], d0, row);
+        if (kGate) tma_load_2d(tile_z(s), &P.map_z, &full[s], d0, row);
+        tma_load_2d(tile_B(s), &P.map_B, &full[s], 0, row);
+        tma_load_2d(tile_C(s), &P.map_C, &full[s], 0, row);
+        issued = k + 1;
+      }
+      // never leave with copies in flight: wait for the last use of every stage
+      for (int s = 0; s < S && s < issued; ++s) {
+        const int k_last = s + S * ((issued - 1 - s) / S);
+        mbar_wait(&full[s], (uint32_t)(k_last / S) & 1, p.status);
+      }
+    }
+    return;
+  }
+  if (warp == 5) {
+    // ---------------- converter: bf16 Bm/Cm tile -> f32, once per stage use
+    if (kBf16) {
+      for (int k = 0; k < ntiles; ++k) {
+        const int s = k % S;
+        if (!mbar_wait(&full[s], (uint32_t)(k / S) & 1, p.status)) break;
+        const Act* tb = tile_B(s);
+        const Act* tc = tile_C(s);
+        float* dst = bcf + (size_t)s * kTT * 2 * N2;
+        for (int e = lane; e < kBC; e += 32) {
+          const int t = e / N2, n = e % N2;
+          dst[(t * 2 + 0) * N2 + n] = lds_act(tb + e);
+          dst[(t * 2 + 1) * N2 + n] = lds_act(tc + e);
+        }
+        mbar_arrive(&conv[s]);
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers
+  const int half = tid & 1;
+  const int dl = tid >> 1;
+  const int d = d0 + dl;
+  const bool dvalid = d < D;
+  const int dc = dvalid ? d : D - 1;
+  constexpr int NH = NG / 2;  // float2 pairs per lane
+
+  float2 A2[NH], h[NH];
+#pragma unroll
+  for (int i = 0; i < NH; ++i) {
+    const int n = half * NG + 2 * i;
+    const float a0 = -expf(p.A_log[dc * N2 + n]);
+    const float a1 = -expf(p.A_log[dc * N2 + n + 1]);
+    A2[i] = kFast ? make_float2(a0 * kLog2e, a1 * kLog2e) : make_float2(a0, a1);
+    h[i] = p.h0 ? make_float2(p.h0[((size_t)b * D + dc) * N2 + n], p.h0[((size_t)b * D + dc) * N2 + n + 1])
+                : make_float2(0.f, 0.f);
+  }
+  const float bias = p.delta_bias[dc];
+  const float Dd = p.Dp[dc];
+  Act* outp = static_cast<Act*>(p.out) + (size_t)b * L * D + d;
+
+  // one step over this lane's NG states; returns the partial readout
+  auto step = [&](float dlt, float dlu, const float* Brow, const float* Crow) -> float {
+    const float2 dd = make_float2(dlt, dlt);
+    const float2 uu = make_float2(dlu, dlu);
+    float2 yacc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < NH; ++i) {
+      const float2 Bv = *reinterpret_cast<const float2*>(Brow + 2 * i);
+      const float2 Cv = *reinterpret_cast<const float2*>(Crow + 2 * i);
+      const float2 a = decay2<kFast>(dd, A2[i]);
+      h[i] = ffma2(a, h[i], fmul2(uu, Bv));
+      yacc = ffma2(Cv, h[i], yacc);
+    }
+    return yacc.x + yacc.y;
+  };
+
+  for (int k = 0; k < ntiles; ++k) {
+    const int s = k % S;
+    const uint32_t par = (uint32_t)(k / S) & 1;
+    if (!mbar_wait(&full[s], par, p.status)) break;
+    if (kBf16 && !mbar_wait(&conv[s], par, p.status)) break;
+    const int tbase = k * kTT;
+    const int cnt = min(kTT, L - tbase);
+    if (kSave && (tbase % kChunk) == 0 && dvalid) {
+      float* cs = p.chunk_states + (((size_t)b * p.nchunks + tbase / kChunk) * D + d) * N2 + half * NG;
+#pragma unroll
+      for (int i = 0; i < NH; ++i) reinterpret_cast<float2*>(cs)[i] = h[i];
+    }
+    const Act* su = tile_u(s);
+    const Act* sr = tile_raw(s);
+    const Act* sz = tile_z(s);
+    const float* Bt;
+    const float* Ct;
+    int bstride, coff;
+    if (kBf16) {
+      Bt = bcf + (size_t)s * kTT * 2 * N2 + half * NG;
+      Ct = Bt + N2;
+      bstride = 2 * N2;
+    } else {
+      Bt = reinterpret_cast<const float*>(tile_B(s)) + half * NG;
+      Ct = reinterpret_cast<const float*>(tile_C(s)) + half * NG;
+      bstride = N2;
+    }
+    (void)coff;
+#pragma unroll 2
+    for (int j = 0; j < cnt; j += 2) {
+      const int tm = j + half;  // the step whose softplus / output this lane owns
+      const bool vm = tm < cnt;
+      const float uu = lds_act(su + tm * kDTile + dl);
+      const float sp = vm ? softplus_k<kFast>(lds_act(sr + tm * kDTile + dl) + bias) : 0.f;
+      const float spu = sp * uu;
+      const float o_sp = __shfl_xor_sync(0xffffffffu, sp, 1);
+      const float o_spu = __shfl_xor_sync(0xffffffffu, spu, 1);
+      const float dA = half ? o_sp : sp, duA = half ? o_spu : spu;
+      const float dB = half ? sp : o_sp, duB = half ? spu : o_spu;
+      const float yA = step(dA, duA, Bt + j * bstride, Ct + j * bstride);
+      float yB = 0.f;
+      if (j + 1 < cnt) yB = step(dB, duB, Bt + (j + 1) * bstride, Ct + (j + 1) * bstride);
+      const float send = half ? yA : yB;
+      const float keep = half ? yB : yA;
+      const float y = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+      if (vm && dvalid) {
+        float o = fmaf(Dd, uu, y);
+        if (kGate) o *= silu_k<kFast>(lds_act(sz + tm * kDTile + dl));
+        st_act(outp + (size_t)(tbase + tm) * D, o);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+  if (p.h_last && dvalid) {
+    float* hl = p.h_last + ((size_t)b * D + d) * N2 + half * NG;
+#pragma unroll
+    for (int i = 0; i < NH; ++i) reinterpret_cast<float2*>(hl)[i] = h[i];
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2D map over a row-major [rows][cols] tensor, box [box_rows][box_cols].
+bool make_map(CUtensorMap* m, const void* base, int act, uint64_t rows, uint64_t cols, uint32_t box_rows,
+              uint32_t box_cols) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  const size_t e = act == SSM_BF16 ? 2 : 4;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * e};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, act == SSM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <typename Act>
+constexpr size_t fwd_smem_bytes(int NG) {
+  return (size_t)FwdCfg<Act>::kStages * (3 * kTT * kDTile + 2 * kTT * 2 * NG) * sizeof(Act) +
+         (std::is_same<Act, float>::value ? 0 : (size_t)FwdCfg<Act>::kStages * kTT * 2 * 2 * NG * 4) +
+         3 * FwdCfg<Act>::kStages * 8;
+}
+
+template <typename Act, int NG, bool kSave, bool kFast, bool kGate>
+cudaError_t launch_one(const FwdTmaParams& P, cudaStream_t stream) {
+  auto kern = s6_fwd_tma_kernel<Act, NG, kSave, kFast, kGate>;
+  const size_t smem = fwd_smem_bytes<Act>(NG);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((P.p.D + kDTile - 1) / kDTile, P.p.B);
+  kern<<<grid, kFwdWarps * 32, smem, stream>>>(P);
+  return cudaGetLastError();
+}
+
+template <typename Act, int NG, bool kFast>
+cudaError_t launch_ng(const FwdTmaParams& P, cudaStream_t stream) {
+  const bool save = P.p.chunk_states != nullptr, gate = P.p.z != nullptr;
+  if (save)
+    return gate ? launch_one<Act, NG, true, kFast, true>(P, stream) : launch_one<Act, NG, true, kFast, false>(P, stream);
+  return gate ? launch_one<Act, NG, false, kFast, true>(P, stream) : launch_one<Act, NG, false, kFast, false>(P, stream);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+// The TMA path covers N in {4, 8, 16} with N*e and D*e multiples of 16 bytes
+// and 16-byte aligned activation pointers; everything else takes the generic
+// kernel.  bf16 activations use the SFU exp/log (ex2/lg2.approx); f32
+// activations keep expf/log1pf.
+bool fwd_tma_supported(const FwdParams& p, int act) {
+  const int e = act == SSM_BF16 ? 2 : 4;
+  if (!(p.N == 4 || p.N == 8 || p.N == 16)) return false;
+  if ((p.N * e) % 16 != 0 || (p.D * e) % 16 != 0) return false;
+  if (!aligned16(p.u) || !aligned16(p.delta_raw) || !aligned16(p.Bm) || !aligned16(p.Cm)) return false;
+  if (p.z && !aligned16(p.z)) return false;
+  if (p.chunk_states && !aligned16(p.chunk_states)) return false;
+  if (p.h_last && !aligned16(p.h_last)) return false;
+  if (p.h0 && (reinterpret_cast<uintptr_t>(p.h0) & 7)) return false;
+  return get_encode() != nullptr;
+}
+
+cudaError_t launch_fwd_tma(const FwdParams& p, int act, cudaStream_t stream) {
+  FwdTmaParams P;
+  memset(&P, 0, sizeof(P));
+  P.p = p;
+  const uint64_t rows = (uint64_t)p.B * p.L;
+  bool ok = make_map(&P.map_u, p.u, act, rows, p.D, kTT, kDTile) &&
+            make_map(&P.map_raw, p.delta_raw, act, rows, p.D, kTT, kDTile) &&
+            make_map(&P.map_B, p.Bm, act, rows, p.N, kTT, p.N) &&
+            make_map(&P.map_C, p.Cm, act, rows, p.N, kTT, p.N);
+  if (p.z) ok = ok && make_map(&P.map_z, p.z, act, rows, p.D, kTT, kDTile);
+  if (!ok) return cudaErrorInvalidValue;
+  const int NG = p.N / 2;
+  if (act == SSM_BF16) {
+    if (NG == 8) return launch_ng<__nv_bfloat16, 8, true>(P, stream);
+    if (NG == 4) return launch_ng<__nv_bfloat16, 4, true>(P, stream);
+    return cudaErrorInvalidValue;
+  }
+  if (NG == 8) return launch_ng<float, 8, false>(P, stream);
+  if (NG == 4) return launch_ng<float, 4, false>(P, stream);
+  if (NG == 2) return launch_ng<float, 2, false>(P, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace s6

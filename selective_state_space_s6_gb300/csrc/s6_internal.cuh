@@ -15,6 +15,7 @@ constexpr int kDTile = 64;             // channels per CTA in the scan kernels
 constexpr int kThreadsPerChannel = 2;  // each channel's N states are split over 2 lanes
 constexpr int kScanThreads = kDTile * kThreadsPerChannel;
 constexpr int kSub = 8;                // backward: steps kept in registers per sub-chunk
+constexpr unsigned int kStatusWaitTimeoutBit = 1u;  // same bit as kStatusWaitTimeout
 
 // ---------------------------------------------------------------- params
 
@@ -31,6 +32,7 @@ struct FwdParams {
   void* out;
   float* h_last;        // nullable (may alias h0 for the decode step)
   float* chunk_states;  // nullable (nosave)
+  unsigned int* status;  // device status word (bounded waits report here)
   int B, L, D, N, nchunks;
 };
 
@@ -59,6 +61,10 @@ struct BwdParams {
 // Each returns the cudaError_t of its launch(es).
 
 cudaError_t launch_fwd(const FwdParams& p, int act, cudaStream_t stream);
+bool fwd_tma_supported(const FwdParams& p, int act);
+cudaError_t launch_fwd_tma(const FwdParams& p, int act, cudaStream_t stream);
+// Device address of the library's status word on the current device (nullptr on error).
+unsigned int* device_status_word();
 cudaError_t launch_bwd(const BwdParams& p, int act, cudaStream_t stream);
 cudaError_t launch_reduce_dbc(const float* ws_dbc, int ndt, int B, int L, int N, void* dBm,
                               void* dCm, int act, cudaStream_t stream);

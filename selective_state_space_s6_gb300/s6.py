@@ -52,6 +52,8 @@ def load_library():
         lib.ssm_last_error.restype = ctypes.c_char_p
         lib.ssm_version.argtypes = []
         lib.ssm_version.restype = ci
+        lib.ssm_check_device_status.argtypes = [vp]
+        lib.ssm_check_device_status.restype = ci
         lib.ssm_num_chunks.argtypes = [i64]
         lib.ssm_num_chunks.restype = i64
         for f in (lib.ssm_fwd_workspace_bytes, lib.ssm_bwd_workspace_bytes):
@@ -231,3 +233,8 @@ def ssm_step(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h, *, out=None, str
                                  _stream(stream))
     _check("ssm_step", rc)
     return out
+
+
+def check_device_status(stream=None):
+    """Synchronise the stream and raise if a kernel's bounded wait gave up."""
+    _check("ssm_check_device_status", load_library().ssm_check_device_status(_stream(stream)))

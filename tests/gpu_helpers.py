@@ -47,6 +47,7 @@ def gpu_fwd_bwd(xd, dh_last=None, want_bwd=True):
     if want_bwd:
         g = s6.ssm_scan_bwd(*[xd[k] for k in ARGS], xd.get("h0"), cs, xd["dout"], dh_last)
         r.update(g)
+    s6.check_device_status()  # synchronises; raises if a bounded device wait gave up
     return r
 
 

@@ -37,6 +37,13 @@ SMALL = [
     (2, 129, 128, 8, "f32"),
     (1, 300, 33, 2, "bf16"),
     (1, 77, 130, 16, "bf16"),
+    # shapes on the TMA path (N*e and D*e multiples of 16 bytes) with ragged tails
+    (2, 100, 72, 16, "bf16"),   # ragged 64-channel tile, L not a multiple of 32 or 64
+    (1, 33, 8, 8, "bf16"),      # a tile that is mostly out of bounds
+    (3, 95, 136, 16, "f32"),
+    (1, 1, 64, 16, "bf16"),     # one step
+    (2, 31, 24, 4, "f32"),
+    (2, 160, 64, 8, "f32"),
 ]
 
 
