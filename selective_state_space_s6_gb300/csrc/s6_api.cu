@@ -261,7 +261,11 @@ int ssm_scan_bwd_partials(int64_t batch, int64_t seqlen, int64_t dim, int64_t ds
   p.ws_param = reinterpret_cast<float*>(static_cast<char*>(ws) + w.param_off);
   p.B = (int)B; p.L = (int)L; p.D = (int)D; p.N = (int)N;
   p.nchunks = (int)ssm_num_chunks(L);
-  const cudaError_t ce = s6::launch_bwd(p, act, static_cast<cudaStream_t>(stream));
+  p.status = s6::device_status_word();
+  if (!p.status) return fail(SSM_ERR_CUDA, "cannot locate the device status word");
+  const cudaError_t ce = (L > 0 && s6::bwd_tma_supported(p, act))
+                             ? s6::launch_bwd_tma(p, act, static_cast<cudaStream_t>(stream))
+                             : s6::launch_bwd(p, act, static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess) return cuda_fail(ce, "ssm_scan_bwd_partials launch");
   return SSM_OK;
 }

@@ -1,0 +1,615 @@
+// S6 backward, TMA-pipelined (sm_103a).
+//
+// CTA = (64-channel tile, batch), 6 warps: 4 consumer warps (lane pair =
+// channel, NG states per lane, as in the forward), a TMA producer warp and a
+// converter warp (bf16: Bm/Cm tiles widened to f32 once per tile).
+//
+// Each lane walks its chunks (SSM_CHUNK_LEN = 64 steps, restarted from the
+// forward's chunk states) from last to first.  The producer streams each
+// chunk twice through an S-stage ring of 32-step tiles:
+//   pass A (tiles in forward order; delta_raw, u, Bm): recompute h from the
+//     chunk state, store delta = softplus(.) in shared memory for the chunk,
+//     and keep the state at every 8th step (checkpoints, shared memory);
+//   pass B (tiles in reverse order; all inputs): for each 8-step sub-chunk,
+//     last first, recompute its 8 states into registers, then step backward
+//     with the adjoint g_t = dy_t*C_t + Abar_{t+1}*g_{t+1}, producing
+//     du, d_delta_raw, dz and the dBm/dCm/dA_log/dDp/d_delta_bias terms.
+// (The second read of a chunk's tiles comes from L2.)
+//
+// Per step, the channel sums of the dBm and dCm terms over the CTA's 64
+// channels are taken in shared memory in a fixed order (8 channels per
+// thread with packed adds, then a 3-level xor butterfly) and stored as one
+// partial per CTA; the sums over t of the parameter terms stay in registers
+// per chunk and are added into per-lane totals with a compensated (Kahan)
+// add.  A small kernel adds the partials in ascending tile / batch order
+// (s6_bwd.cu).  No floating-point atomics: results are bit-identical from run
+// to run (the single-writer, fixed-order policy of deterministic_backward.py).
+//
+// Work that depends only on (t, d) -- softplus, the gate's sigmoid, dy,
+// the softplus derivative -- is done once per step by one lane of the pair
+// (even steps: lane 0, odd steps: lane 1) and shared with a shuffle.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+#include <type_traits>
+
+#include "s6_internal.cuh"
+#include "s6_tma.cuh"
+
+namespace s6 {
+
+namespace {
+
+constexpr int kTT = 32;           // steps per tile
+constexpr int kTilesPerChunk = kChunk / kTT;
+constexpr int kBwdWarps = 6;
+constexpr int kStages = 3;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+// Reduction scratch of one step: [q][state half][channel group][8 channels][8 states].
+// Groups of 8 channels are padded to 68 floats and state halves to 548, so
+// that 128-bit writes (a quarter-warp: 4 channels x 2 halves) and 64-bit
+// reads (a half-warp: 8 channel groups x 2 state pairs) hit distinct banks.
+constexpr int kRedGroup = 8 * 8 + 4;
+constexpr int kRedHalf = 8 * kRedGroup + 4;
+constexpr int kRedQ = 2 * kRedHalf;
+constexpr int kRedBuf = 2 * kRedQ;
+
+struct BwdTmaParams {
+  CUtensorMap map_u, map_raw, map_z, map_dout, map_B, map_C;
+  BwdParams p;
+};
+
+template <typename Act>
+__device__ __forceinline__ float lds_act(const Act* p);
+template <>
+__device__ __forceinline__ float lds_act<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float lds_act<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+
+__device__ __forceinline__ float softplus_fast(float s) {
+  const float e = ex2_approx(-fabsf(s) * kLog2e);
+  const float lg = lg2_approx(1.f + e) * kLn2;
+  const float ser = e * fmaf(e, fmaf(e, 1.f / 3.f, -0.5f), 1.f);
+  return fmaxf(s, 0.f) + (e < 0.015625f ? ser : lg);
+}
+
+// sigmoid(s) written through delta = softplus(s): sigmoid(s) = 1 - e^{-delta}
+// (the identity the oarust Slang page uses for its dt gradient), with a
+// series for small delta where 1 - e^{-delta} would cancel.
+__device__ __forceinline__ float dsoftplus_fast(float delta) {
+  const float em = ex2_approx(-delta * kLog2e);
+  const float ser = delta * fmaf(delta, fmaf(delta, 1.f / 6.f, -0.5f), 1.f);
+  return delta < 0.03125f ? ser : 1.f - em;
+}
+
+__device__ __forceinline__ float sigmoid_fast(float z) { return rcp_approx(1.f + ex2_approx(-z * kLog2e)); }
+
+template <bool kFast>
+__device__ __forceinline__ float2 decay2(float2 dd, float2 A) {
+  const float2 x = fmul2(dd, A);
+  if (kFast) return make_float2(ex2_approx(x.x), ex2_approx(x.y));
+  return make_float2(expf(x.x), expf(x.y));
+}
+
+__device__ __forceinline__ void kahan_add(float& sum, float& comp, float x) {
+  const float y = __fsub_rn(x, comp);
+  const float t = __fadd_rn(sum, y);
+  comp = __fsub_rn(__fsub_rn(t, sum), y);
+  sum = t;
+}
+
+__device__ __forceinline__ int red_at(int q, int d, int n) {
+  return q * kRedQ + (n >> 3) * kRedHalf + (d >> 3) * kRedGroup + (d & 7) * 8 + (n & 7);
+}
+
+template <typename Act, int NG, bool kFast, bool kGate>
+__global__ void __launch_bounds__(kBwdWarps * 32) s6_bwd_tma_kernel(const __grid_constant__ BwdTmaParams P) {
+  constexpr int N2 = 2 * NG;
+  constexpr int NH = NG / 2;
+  constexpr int kTile = kTT * kDTile;
+  constexpr int kBC = kTT * N2;
+  constexpr bool kBf16 = std::is_same<Act, __nv_bfloat16>::value;
+  constexpr int kStageElems = 4 * kTile + 2 * kBC;
+  constexpr int kNSub = kChunk / kSub;  // checkpoints per chunk
+
+  extern __shared__ __align__(1024) unsigned char smem[];
+  Act* stages = reinterpret_cast<Act*>(smem);
+  float* fbase = reinterpret_cast<float*>(smem + (size_t)kStages * kStageElems * sizeof(Act));
+  float* bcf = fbase;                                           // [S][TT][2][N2] (bf16 only)
+  float* dbuf = bcf + (kBf16 ? kStages * kTT * 2 * N2 : 0);     // [kChunk][64] delta of the chunk
+  float* ckpt = dbuf + kChunk * kDTile;                         // [kNSub][128][NG]
+  float* red = ckpt + kNSub * kScanThreads * NG;                // [2][kRedBuf]
+  float* tot = red + 2 * kRedBuf;                               // [2 (sum, comp)][128][NG + 2]
+  uint64_t* full = reinterpret_cast<uint64_t*>(tot + 2 * kScanThreads * (NG + 2));
+  uint64_t* conv = full + kStages;
+  uint64_t* empty = conv + kStages;
+
+  const BwdParams& p = P.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.y, d0 = blockIdx.x * kDTile;
+  const int L = p.L, D = p.D;
+  const int nchunks = p.nchunks;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&conv[s], 32);
+      mbar_init(&empty[s], 4);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  auto tile_u = [&](int s) { return stages + (size_t)s * kStageElems; };
+  auto tile_raw = [&](int s) { return stages + (size_t)s * kStageElems + kTile; };
+  auto tile_z = [&](int s) { return stages + (size_t)s * kStageElems + 2 * kTile; };
+  auto tile_g = [&](int s) { return stages + (size_t)s * kStageElems + 3 * kTile; };
+  auto tile_B = [&](int s) { return stages + (size_t)s * kStageElems + 4 * kTile; };
+  auto tile_C = [&](int s) { return stages + (size_t)s * kStageElems + 4 * kTile + kBC; };
+
+  // The item sequence every role walks: for chunk c = last..0 with ntl tiles:
+  // pass A tiles 0..ntl-1, then pass B tiles ntl-1..0.
+  auto chunk_tiles = [&](int c) { return (min(kChunk, L - c * kChunk) + kTT - 1) / kTT; };
+
+  if (warp == 4) {
+    // ---------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&P.map_u);
+      tma_prefetch_desc(&P.map_raw);
+      tma_prefetch_desc(&P.map_dout);
+      if (kGate) tma_prefetch_desc(&P.map_z);
+      tma_prefetch_desc(&P.map_B);
+      tma_prefetch_desc(&P.map_C);
+      const uint32_t bytesA = (uint32_t)((2 * kTile + kBC) * sizeof(Act));
+      const uint32_t bytesB = (uint32_t)(((kGate ? 4 : 3) * kTile + 2 * kBC) * sizeof(Act));
+      int item = 0;
+      bool ok = true;
+      for (int c = nchunks - 1; c >= 0 && ok; --c) {
+        const int ntl = chunk_tiles(c);
+        for (int it = 0; it < 2 * ntl; ++it, ++item) {
+          const bool passA = it < ntl;
+          const int j = passA ? it : 2 * ntl - 1 - it;
+          const int s = item % kStages;
+          const uint32_t use = (uint32_t)(item / kStages);
+          if (item >= kStages && !mbar_wait(&empty[s], (use - 1) & 1, p.status)) {
+            ok = false;
+            break;
+          }
+          const int row = b * L + c * kChunk + j * kTT;
+          mbar_arrive_expect_tx(&full[s], passA ? bytesA : bytesB);
+          tma_load_2d(tile_u(s), &P.map_u, &full[s], d0, row);
+          tma_load_2d(tile_raw(s), &P.map_raw, &full[s], d0, row);
+          tma_load_2d(tile_B(s), &P.map_B, &full[s], 0, row);
+          if (!passA) {
+            if (kGate) tma_load_2d(tile_z(s), &P.map_z, &full[s], d0, row);
+            tma_load_2d(tile_g(s), &P.map_dout, &full[s], d0, row);
+            tma_load_2d(tile_C(s), &P.map_C, &full[s], 0, row);
+          }
+        }
+      }
+      // never leave with copies in flight: wait for the last use of every stage
+      for (int s = 0; s < kStages && s < item; ++s) {
+        const int k_last = s + kStages * ((item - 1 - s) / kStages);
+        mbar_wait(&full[s], (uint32_t)(k_last / kStages) & 1, p.status);
+      }
+    }
+    return;
+  }
+  if (warp == 5) {
+    // ---------------- converter (bf16): Bm (and Cm in pass B) -> f32
+    if (kBf16) {
+      int item = 0;
+      bool ok = true;
+      for (int c = nchunks - 1; c >= 0; --c) {
+        const int ntl = chunk_tiles(c);
+        for (int it = 0; it < 2 * ntl; ++it, ++item) {
+          const bool passA = it < ntl;
+          const int s = item % kStages;
+          if (ok) ok = mbar_wait(&full[s], (uint32_t)(item / kStages) & 1, p.status);
+          const Act* tb = tile_B(s);
+          const Act* tc = tile_C(s);
+          float* dst = bcf + (size_t)s * kTT * 2 * N2;
+          for (int e = lane; e < kBC; e += 32) {
+            const int t = e / N2, n = e % N2;
+            dst[(t * 2 + 0) * N2 + n] = lds_act(tb + e);
+            if (!passA) dst[(t * 2 + 1) * N2 + n] = lds_act(tc + e);
+          }
+          mbar_arrive(&conv[s]);
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers
+  const int half = tid & 1;
+  const int dl = tid >> 1;
+  const int d = d0 + dl;
+  const bool dvalid = d < D;
+  const int dc = dvalid ? d : D - 1;
+
+  // A2 = A*log2(e) on the fast path (2^x decays), A itself otherwise; sums
+  // weighted by A are taken with A2 and scaled by kAscale = A / A2 at the end.
+  constexpr float kAscale = kFast ? kLn2 : 1.f;
+  float2 A2[NH], carry[NH];
+#pragma unroll
+  for (int i = 0; i < NH; ++i) {
+    const int n = half * NG + 2 * i;
+    const float a0 = -expf(p.A_log[dc * N2 + n]);
+    const float a1 = -expf(p.A_log[dc * N2 + n + 1]);
+    A2[i] = kFast ? make_float2(a0 * kLog2e, a1 * kLog2e) : make_float2(a0, a1);
+    carry[i] = (p.dh_last && dvalid)
+                   ? make_float2(p.dh_last[((size_t)b * D + d) * N2 + n], p.dh_last[((size_t)b * D + d) * N2 + n + 1])
+                   : make_float2(0.f, 0.f);
+  }
+  const float bias = p.delta_bias[dc];
+  const float Dd = p.Dp[dc];
+  float* my_tot = tot + tid * (NG + 2);                          // running totals
+  float* my_cmp = tot + kScanThreads * (NG + 2) + tid * (NG + 2);  // Kahan compensation
+#pragma unroll
+  for (int i = 0; i < NG + 2; ++i) {
+    my_tot[i] = 0.f;
+    my_cmp[i] = 0.f;
+  }
+
+  // reducer role: output pair op (q = op >> 3, states 2*(op&7), +1), channel group r of 8
+  const int red_op = tid >> 3, red_r = tid & 7;
+  const int red_q = red_op >> 3, red_n = 2 * (red_op & 7);
+  const bool red_store = red_r == 0 && red_n < N2 && (red_n + 1) < N2 + 1;
+
+  Act* dup = static_cast<Act*>(p.du) + (size_t)b * L * D + d;
+  Act* drp = static_cast<Act*>(p.d_delta_raw) + (size_t)b * L * D + d;
+  Act* dzp = kGate ? static_cast<Act*>(p.dz) + (size_t)b * L * D + d : nullptr;
+
+  bool failed = false;
+  int item = 0;
+  int red_parity = 0;
+  for (int c = nchunks - 1; c >= 0; --c) {
+    const int t0 = c * kChunk;
+    const int clen = min(kChunk, L - t0);
+    const int ntl = (clen + kTT - 1) / kTT;
+    float2 accA[NH];
+    float accD = 0.f, accBias = 0.f;
+#pragma unroll
+    for (int i = 0; i < NH; ++i) accA[i] = make_float2(0.f, 0.f);
+    float2 h[NH];
+    {
+      const float* cs = p.chunk_states + (((size_t)b * nchunks + c) * D + dc) * N2 + half * NG;
+#pragma unroll
+      for (int i = 0; i < NH; ++i) h[i] = *reinterpret_cast<const float2*>(cs + 2 * i);
+    }
+    for (int it = 0; it < 2 * ntl; ++it, ++item) {
+      const bool passA = it < ntl;
+      const int j = passA ? it : 2 * ntl - 1 - it;
+      const int s = item % kStages;
+      const uint32_t par = (uint32_t)(item / kStages) & 1;
+      if (!failed) failed = !mbar_wait(&full[s], par, p.status);
+      if (kBf16 && !failed) failed = !mbar_wait(&conv[s], par, p.status);
+      __syncwarp();
+      const int tb = j * kTT;  // first step of the tile within the chunk
+      const int cnt = min(kTT, clen - tb);
+      const Act* su = tile_u(s);
+      const Act* sr = tile_raw(s);
+      const float* Bt;
+      const float* Ct;
+      int bst;
+      if (kBf16) {
+        Bt = bcf + (size_t)s * kTT * 2 * N2 + half * NG;
+        Ct = Bt + N2;
+        bst = 2 * N2;
+      } else {
+        Bt = reinterpret_cast<const float*>(tile_B(s)) + half * NG;
+        Ct = reinterpret_cast<const float*>(tile_C(s)) + half * NG;
+        bst = N2;
+      }
+      if (passA) {
+        // ---------- pass A: forward recompute, delta to smem, checkpoints
+        for (int k = 0; k < cnt; k += 2) {
+          const int km = k + half;
+          const bool vm = km < cnt;
+          const float uu = lds_act(su + km * kDTile + dl);
+          const float sp = vm ? (kFast ? softplus_fast(lds_act(sr + km * kDTile + dl) + bias)
+                                       : softplus_f(lds_act(sr + km * kDTile + dl) + bias))
+                              : 0.f;
+          if (vm) dbuf[(tb + km) * kDTile + dl] = sp;
+          const float spu = sp * uu;
+          const float o_sp = __shfl_xor_sync(0xffffffffu, sp, 1);
+          const float o_spu = __shfl_xor_sync(0xffffffffu, spu, 1);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int kk = k + e;
+            if (kk < cnt) {
+              if (((tb + kk) % kSub) == 0) {
+                float2* ck = reinterpret_cast<float2*>(ckpt + (((tb + kk) / kSub) * kScanThreads + tid) * NG);
+#pragma unroll
+                for (int i = 0; i < NH; ++i) ck[i] = h[i];
+              }
+              const float dv = (e == half) ? sp : o_sp;
+              const float duv = (e == half) ? spu : o_spu;
+              const float2 dd = make_float2(dv, dv), uu2 = make_float2(duv, duv);
+              const float* Brow = Bt + kk * bst;
+#pragma unroll
+              for (int i = 0; i < NH; ++i) {
+                const float2 Bv = *reinterpret_cast<const float2*>(Brow + 2 * i);
+                h[i] = ffma2(decay2<kFast>(dd, A2[i]), h[i], fmul2(uu2, Bv));
+              }
+            }
+          }
+        }
+      } else {
+        // ---------- pass B: sub-chunks of this tile, last first
+        const Act* sz = tile_z(s);
+        const Act* sg = tile_g(s);
+        const int nsub = (cnt + kSub - 1) / kSub;
+        for (int sc = nsub - 1; sc >= 0; --sc) {
+          const int ks = sc * kSub;              // first step of the sub-chunk within the tile
+          const int cnt8 = min(kSub, cnt - ks);
+          float2 hstart[NH];
+          {
+            const float2* ck = reinterpret_cast<const float2*>(ckpt + (((tb + ks) / kSub) * kScanThreads + tid) * NG);
+#pragma unroll
+            for (int i = 0; i < NH; ++i) hstart[i] = ck[i];
+          }
+          float2 hs[kSub][NH];
+#pragma unroll
+          for (int k = 0; k < kSub; ++k) {
+            if (k < cnt8) {
+              const int kt = ks + k;
+              const float dv = dbuf[(tb + kt) * kDTile + dl];
+              const float duv = dv * lds_act(su + kt * kDTile + dl);
+              const float2 dd = make_float2(dv, dv), uu2 = make_float2(duv, duv);
+              const float* Brow = Bt + kt * bst;
+#pragma unroll
+              for (int i = 0; i < NH; ++i) {
+                const float2 Bv = *reinterpret_cast<const float2*>(Brow + 2 * i);
+                const float2 hp = k == 0 ? hstart[i] : hs[k > 0 ? k - 1 : 0][i];
+                hs[k][i] = ffma2(decay2<kFast>(dd, A2[i]), hp, fmul2(uu2, Bv));
+              }
+            }
+          }
+          // reverse, two steps at a time: (2m+1, 2m); lane `half` owns step 2m+half
+#pragma unroll
+          for (int m = kSub / 2 - 1; m >= 0; --m) {
+            if (2 * m < cnt8) {
+              const int kown = ks + 2 * m + half;  // tile row this lane owns
+              const bool vown = (2 * m + half) < cnt8;
+              // (t, d) work of the owned step
+              const float dv_o = dbuf[(tb + min(kown, cnt - 1)) * kDTile + dl];
+              const float u_o = lds_act(su + kown * kDTile + dl);
+              const float gout = lds_act(sg + kown * kDTile + dl);
+              float dy_o = gout, dzf_o = 0.f;
+              if (kGate) {
+                const float zz = lds_act(sz + kown * kDTile + dl);
+                const float sgz = kFast ? sigmoid_fast(zz) : sigmoid_f(zz);
+                dy_o = gout * zz * sgz;
+                dzf_o = gout * sgz * fmaf(zz, 1.f - sgz, 1.f);
+              }
+              if (!vown) dy_o = 0.f;
+              const float dy_x = __shfl_xor_sync(0xffffffffu, dy_o, 1);
+              float ysum[2], gbsum[2], apsum[2];
+#pragma unroll
+              for (int e = 1; e >= 0; --e) {
+                const int k = 2 * m + e;
+                ysum[e] = 0.f;
+                gbsum[e] = 0.f;
+                apsum[e] = 0.f;
+                if (k < cnt8) {
+                  const int kt = ks + k;
+                  const float dv = dbuf[(tb + kt) * kDTile + dl];
+                  const float duv = dv * lds_act(su + kt * kDTile + dl);
+                  const float dy = (e == half) ? dy_o : dy_x;
+                  const float2 dd = make_float2(dv, dv), uu2 = make_float2(duv, duv);
+                  const float2 dy2 = make_float2(dy, dy);
+                  const float* Brow = Bt + kt * bst;
+                  const float* Crow = Ct + kt * bst;
+                  float2 ya = make_float2(0.f, 0.f), gba = make_float2(0.f, 0.f), apa = make_float2(0.f, 0.f);
+                  float* rb = red + red_parity * kRedBuf;
+#pragma unroll
+                  for (int i = 0; i < NH; ++i) {
+                    const float2 Bv = *reinterpret_cast<const float2*>(Brow + 2 * i);
+                    const float2 Cv = *reinterpret_cast<const float2*>(Crow + 2 * i);
+                    const float2 a = decay2<kFast>(dd, A2[i]);
+                    const float2 hk = hs[k][i];
+                    const float2 hp = k == 0 ? hstart[i] : hs[k > 0 ? k - 1 : 0][i];
+                    const float2 g = ffma2(dy2, Cv, carry[i]);
+                    const float2 pv = fmul2(g, fmul2(a, hp));
+                    apa = ffma2(A2[i], pv, apa);
+                    accA[i] = ffma2(dd, pv, accA[i]);
+                    gba = ffma2(g, Bv, gba);
+                    ya = ffma2(Cv, hk, ya);
+                    const float2 tB = dvalid ? fmul2(g, uu2) : make_float2(0.f, 0.f);
+                    const float2 tC = dvalid ? fmul2(dy2, hk) : make_float2(0.f, 0.f);
+                    *reinterpret_cast<float2*>(rb + red_at(0, dl, half * NG + 2 * i)) = tB;
+                    *reinterpret_cast<float2*>(rb + red_at(1, dl, half * NG + 2 * i)) = tC;
+                    carry[i] = fmul2(a, g);
+                  }
+                  ysum[e] = ya.x + ya.y;
+                  gbsum[e] = gba.x + gba.y;
+                  apsum[e] = (apa.x + apa.y) * kAscale;
+                  // channel sum of this step's dBm / dCm terms, fixed order
+                  named_bar_sync(1, kScanThreads);
+                  float2 v = make_float2(0.f, 0.f);
+#pragma unroll
+                  for (int k2 = 0; k2 < 8; ++k2) {
+                    const float2 x = *reinterpret_cast<const float2*>(rb + red_at(red_q, red_r * 8 + k2, red_n));
+                    v = make_float2(v.x + x.x, v.y + x.y);
+                  }
+#pragma unroll
+                  for (int msk = 1; msk < 8; msk <<= 1) {
+                    const float ox = __shfl_xor_sync(0xffffffffu, v.x, msk);
+                    const float oy = __shfl_xor_sync(0xffffffffu, v.y, msk);
+                    v = make_float2(v.x + ox, v.y + oy);
+                  }
+                  if (red_store) {
+                    float* wp = p.ws_dbc + ((((size_t)blockIdx.x * p.B + b) * L + (t0 + tb + kt)) * 2 + red_q) * N2 + red_n;
+                    *reinterpret_cast<float2*>(wp) = v;
+                  }
+                  red_parity ^= 1;
+                }
+              }
+              // exchange the pair's partial sums: each lane keeps the full sums of its owned step
+              float ysum_f, gb_f, ap_f;
+              {
+                const float sy = half ? ysum[0] : ysum[1], ky = half ? ysum[1] : ysum[0];
+                const float sg2 = half ? gbsum[0] : gbsum[1], kg = half ? gbsum[1] : gbsum[0];
+                const float sa = half ? apsum[0] : apsum[1], ka = half ? apsum[1] : apsum[0];
+                ysum_f = ky + __shfl_xor_sync(0xffffffffu, sy, 1);
+                gb_f = kg + __shfl_xor_sync(0xffffffffu, sg2, 1);
+                ap_f = ka + __shfl_xor_sync(0xffffffffu, sa, 1);
+              }
+              if (vown && dvalid) {
+                const float y = fmaf(Dd, u_o, ysum_f);
+                const float dsp = kFast ? dsoftplus_fast(dv_o) : -expm1f(-dv_o);
+                const float dd_ = fmaf(u_o, gb_f, ap_f);
+                const float draw = dd_ * dsp;
+                const size_t o = (size_t)(t0 + tb + kown) * D;
+                st_act(dup + o, fmaf(Dd, dy_o, dv_o * gb_f));
+                st_act(drp + o, draw);
+                if (kGate) st_act(dzp + o, y * dzf_o);
+                accD = fmaf(dy_o, u_o, accD);
+                accBias += draw;
+              }
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    // chunk sums -> compensated running totals (per-lane private smem)
+#pragma unroll
+    for (int i = 0; i < NH; ++i) {
+      kahan_add(my_tot[2 * i], my_cmp[2 * i], accA[i].x);
+      kahan_add(my_tot[2 * i + 1], my_cmp[2 * i + 1], accA[i].y);
+    }
+    kahan_add(my_tot[NG], my_cmp[NG], accD);
+    kahan_add(my_tot[NG + 1], my_cmp[NG + 1], accBias);
+  }
+  // ---------------- per-batch parameter partials and dh0
+  {
+    const float tD = my_tot[NG] + __shfl_xor_sync(0xffffffffu, my_tot[NG], 1);
+    const float tB = my_tot[NG + 1] + __shfl_xor_sync(0xffffffffu, my_tot[NG + 1], 1);
+    if (dvalid) {
+      float* wp = p.ws_param + ((size_t)b * D + d) * (N2 + 2);
+#pragma unroll
+      for (int i = 0; i < NH; ++i) {
+        const int n = half * NG + 2 * i;
+        wp[n] = (A2[i].x * kAscale) * my_tot[2 * i];
+        wp[n + 1] = (A2[i].y * kAscale) * my_tot[2 * i + 1];
+        if (p.dh0) *reinterpret_cast<float2*>(p.dh0 + ((size_t)b * D + d) * N2 + n) = carry[i];
+      }
+      if (half == 0) {
+        wp[N2] = tD;
+        wp[N2 + 1] = tB;
+      }
+    }
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, int act, uint64_t rows, uint64_t cols, uint32_t box_rows,
+              uint32_t box_cols) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  const size_t e = act == SSM_BF16 ? 2 : 4;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * e};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, act == SSM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename Act>
+size_t bwd_smem_bytes(int NG) {
+  const bool bf = std::is_same<Act, __nv_bfloat16>::value;
+  size_t bytes = (size_t)kStages * (4 * kTT * kDTile + 2 * kTT * 2 * NG) * sizeof(Act);
+  bytes += (bf ? (size_t)kStages * kTT * 2 * 2 * NG : 0) * 4;  // bcf
+  bytes += (size_t)kChunk * kDTile * 4;                            // dbuf
+  bytes += (size_t)(kChunk / kSub) * kScanThreads * NG * 4;       // ckpt
+  bytes += (size_t)2 * kRedBuf * 4;                                // red
+  bytes += (size_t)2 * kScanThreads * (NG + 2) * 4;                // tot
+  bytes += 3 * kStages * 8;                                        // barriers
+  return bytes;
+}
+
+template <typename Act, int NG, bool kFast, bool kGate>
+cudaError_t launch_one(const BwdTmaParams& P, cudaStream_t stream) {
+  auto kern = s6_bwd_tma_kernel<Act, NG, kFast, kGate>;
+  const size_t smem = bwd_smem_bytes<Act>(NG);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((P.p.D + kDTile - 1) / kDTile, P.p.B);
+  kern<<<grid, kBwdWarps * 32, smem, stream>>>(P);
+  return cudaGetLastError();
+}
+
+template <typename Act, int NG, bool kFast>
+cudaError_t launch_ng(const BwdTmaParams& P, cudaStream_t stream) {
+  return P.p.z ? launch_one<Act, NG, kFast, true>(P, stream) : launch_one<Act, NG, kFast, false>(P, stream);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+// Same shape rules as the TMA forward: N in {4, 8, 16}, N*e and D*e
+// multiples of 16 bytes, 16-byte aligned tensors.
+bool bwd_tma_supported(const BwdParams& p, int act) {
+  const int e = act == SSM_BF16 ? 2 : 4;
+  if (!(p.N == 4 || p.N == 8 || p.N == 16)) return false;
+  if (act == SSM_BF16 && p.N == 4) return false;
+  if ((p.N * e) % 16 != 0 || (p.D * e) % 16 != 0) return false;
+  const void* ptrs[] = {p.u, p.delta_raw, p.Bm, p.Cm, p.dout, p.chunk_states};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return false;
+  if (p.z && !aligned16(p.z)) return false;
+  if (p.dh0 && !aligned16(p.dh0)) return false;
+  if (p.dh_last && (reinterpret_cast<uintptr_t>(p.dh_last) & 7)) return false;
+  return get_encode() != nullptr;
+}
+
+cudaError_t launch_bwd_tma(const BwdParams& p, int act, cudaStream_t stream) {
+  BwdTmaParams P;
+  memset(&P, 0, sizeof(P));
+  P.p = p;
+  const uint64_t rows = (uint64_t)p.B * p.L;
+  bool ok = make_map(&P.map_u, p.u, act, rows, p.D, kTT, kDTile) &&
+            make_map(&P.map_raw, p.delta_raw, act, rows, p.D, kTT, kDTile) &&
+            make_map(&P.map_dout, p.dout, act, rows, p.D, kTT, kDTile) &&
+            make_map(&P.map_B, p.Bm, act, rows, p.N, kTT, p.N) &&
+            make_map(&P.map_C, p.Cm, act, rows, p.N, kTT, p.N);
+  if (p.z) ok = ok && make_map(&P.map_z, p.z, act, rows, p.D, kTT, kDTile);
+  if (!ok) return cudaErrorInvalidValue;
+  const int NG = p.N / 2;
+  if (act == SSM_BF16) {
+    if (NG == 8) return launch_ng<__nv_bfloat16, 8, true>(P, stream);
+    if (NG == 4) return launch_ng<__nv_bfloat16, 4, true>(P, stream);
+    return cudaErrorInvalidValue;
+  }
+  if (NG == 8) return launch_ng<float, 8, false>(P, stream);
+  if (NG == 4) return launch_ng<float, 4, false>(P, stream);
+  if (NG == 2) return launch_ng<float, 2, false>(P, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace s6

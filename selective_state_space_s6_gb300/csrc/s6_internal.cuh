@@ -54,6 +54,7 @@ struct BwdParams {
   float* dh0;  // nullable
   float* ws_dbc;    // [ndt][B][L][2][N] per-CTA sums of the dBm / dCm terms
   float* ws_param;  // [B][D][N+2] per-batch sums: A*sum(...), dDp, d_delta_bias
+  unsigned int* status;  // device status word (bounded waits report here)
   int B, L, D, N, nchunks;
 };
 
@@ -66,6 +67,8 @@ cudaError_t launch_fwd_tma(const FwdParams& p, int act, cudaStream_t stream);
 // Device address of the library's status word on the current device (nullptr on error).
 unsigned int* device_status_word();
 cudaError_t launch_bwd(const BwdParams& p, int act, cudaStream_t stream);
+bool bwd_tma_supported(const BwdParams& p, int act);
+cudaError_t launch_bwd_tma(const BwdParams& p, int act, cudaStream_t stream);
 cudaError_t launch_reduce_dbc(const float* ws_dbc, int ndt, int B, int L, int N, void* dBm,
                               void* dCm, int act, cudaStream_t stream);
 cudaError_t launch_reduce_params(const float* ws_param, int B, int D, int N, float* dA_log,
