@@ -8,14 +8,19 @@
 //              cp.async.bulk.tensor (TMA), completion tracked by mbarriers;
 //   warp 5     converter (bf16 only): widens each stage's Bm/Cm tile to f32 once,
 //              for all 64 channels.
-// Per step a lane does, for its NG states, x = delta*A*log2(e), Abar = 2^x,
-// h = Abar*h + (delta*u)*B, y += C*h with packed f32x2 multiplies / FMAs, so
-// one instruction covers two states.  The softplus of a step is computed by
-// one lane of the pair (even steps: lane 0, odd steps: lane 1) and shared by
-// a shuffle; the two partial readouts are exchanged the same way, and each
-// lane of the pair then gates and stores the output of "its" step.  Every
-// SSM_CHUNK_LEN steps the state is stored as a chunk state (the activation
-// saves of the kernels.rs page's multi-step forward).
+// A consumer handles a 32-step tile in three phases, so that only the state
+// update is carried from step to step and everything else has independent
+// work to overlap:
+//   1. softplus: each lane of a pair computes (delta, delta*u) for the steps
+//      it owns (even steps: lane 0, odd: lane 1) into shared memory;
+//   2. recurrence: per step, for its NG states, x = delta*A*log2(e),
+//      Abar = 2^x, h = Abar*h + (delta*u)*B, y += C*h with packed f32x2
+//      multiplies / FMAs (one instruction covers two states); the lane's
+//      partial readout goes to shared memory;
+//   3. output: each lane adds its partner's partial for the steps it owns,
+//      adds Dp*u, gates with silu(z) and stores.
+// Every SSM_CHUNK_LEN steps the state is stored as a chunk state (the
+// activation saves of the kernels.rs page's multi-step forward).
 //
 // All pipeline waits are bounded (s6_tma.cuh); nothing else spins.
 #include <cudaTypedefs.h>
@@ -198,21 +203,8 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
   const float Dd = p.Dp[dc];
   Act* outp = static_cast<Act*>(p.out) + (size_t)b * L * D + d;
 
-  // one step over this lane's NG states; returns the partial readout
-  auto step = [&](float dlt, float dlu, const float* Brow, const float* Crow) -> float {
-    const float2 dd = make_float2(dlt, dlt);
-    const float2 uu = make_float2(dlu, dlu);
-    float2 yacc = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < NH; ++i) {
-      const float2 Bv = *reinterpret_cast<const float2*>(Brow + 2 * i);
-      const float2 Cv = *reinterpret_cast<const float2*>(Crow + 2 * i);
-      const float2 a = decay2<kFast>(dd, A2[i]);
-      h[i] = ffma2(a, h[i], fmul2(uu, Bv));
-      yacc = ffma2(Cv, h[i], yacc);
-    }
-    return yacc.x + yacc.y;
-  };
+  float2* prep = reinterpret_cast<float2*>(empty + S);   // [TT][64] (delta, delta*u)
+  float* ypart = reinterpret_cast<float*>(prep + kTT * kDTile);  // [TT][128] partial readouts
 
   for (int k = 0; k < ntiles; ++k) {
     const int s = k % S;
@@ -231,7 +223,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
     const Act* sz = tile_z(s);
     const float* Bt;
     const float* Ct;
-    int bstride, coff;
+    int bstride;
     if (kBf16) {
       Bt = bcf + (size_t)s * kTT * 2 * N2 + half * NG;
       Ct = Bt + N2;
@@ -241,28 +233,49 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
       Ct = reinterpret_cast<const float*>(tile_C(s)) + half * NG;
       bstride = N2;
     }
-    (void)coff;
-#pragma unroll 2
-    for (int j = 0; j < cnt; j += 2) {
-      const int tm = j + half;  // the step whose softplus / output this lane owns
-      const bool vm = tm < cnt;
-      const float uu = lds_act(su + tm * kDTile + dl);
-      const float sp = vm ? softplus_k<kFast>(lds_act(sr + tm * kDTile + dl) + bias) : 0.f;
-      const float spu = sp * uu;
-      const float o_sp = __shfl_xor_sync(0xffffffffu, sp, 1);
-      const float o_spu = __shfl_xor_sync(0xffffffffu, spu, 1);
-      const float dA = half ? o_sp : sp, duA = half ? o_spu : spu;
-      const float dB = half ? sp : o_sp, duB = half ? spu : o_spu;
-      const float yA = step(dA, duA, Bt + j * bstride, Ct + j * bstride);
-      float yB = 0.f;
-      if (j + 1 < cnt) yB = step(dB, duB, Bt + (j + 1) * bstride, Ct + (j + 1) * bstride);
-      const float send = half ? yA : yB;
-      const float keep = half ? yB : yA;
-      const float y = keep + __shfl_xor_sync(0xffffffffu, send, 1);
-      if (vm && dvalid) {
-        float o = fmaf(Dd, uu, y);
-        if (kGate) o *= silu_k<kFast>(lds_act(sz + tm * kDTile + dl));
-        st_act(outp + (size_t)(tbase + tm) * D, o);
+    // phase 1: (delta, delta*u) of the steps this lane owns (k = 2i + half),
+    // independent of each other; steps past the end get (0, 0), which leaves
+    // the state unchanged (Abar = 1, input 0)
+#pragma unroll
+    for (int i = 0; i < kTT / 2; ++i) {
+      const int km = 2 * i + half;
+      float2 v = make_float2(0.f, 0.f);
+      if (km < cnt) {
+        const float sp = softplus_k<kFast>(lds_act(sr + km * kDTile + dl) + bias);
+        v = make_float2(sp, sp * lds_act(su + km * kDTile + dl));
+      }
+      prep[km * kDTile + dl] = v;
+    }
+    __syncwarp();
+    // phase 2: the recurrence; only h is carried from step to step
+#pragma unroll 4
+    for (int kk = 0; kk < cnt; ++kk) {
+      const float2 dv = prep[kk * kDTile + dl];
+      const float2 dd = make_float2(dv.x, dv.x);
+      const float2 uu = make_float2(dv.y, dv.y);
+      const float* Brow = Bt + kk * bstride;
+      const float* Crow = Ct + kk * bstride;
+      float2 yacc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < NH; ++i) {
+        const float2 Bv = *reinterpret_cast<const float2*>(Brow + 2 * i);
+        const float2 Cv = *reinterpret_cast<const float2*>(Crow + 2 * i);
+        const float2 a = decay2<kFast>(dd, A2[i]);
+        h[i] = ffma2(a, h[i], fmul2(uu, Bv));
+        yacc = ffma2(Cv, h[i], yacc);
+      }
+      ypart[kk * kScanThreads + tid] = yacc.x + yacc.y;
+    }
+    __syncwarp();
+    // phase 3: each lane completes the readout of its owned steps, gates and stores
+#pragma unroll
+    for (int i = 0; i < kTT / 2; ++i) {
+      const int km = 2 * i + half;
+      if (km < cnt && dvalid) {
+        const float y = ypart[km * kScanThreads + tid] + ypart[km * kScanThreads + (tid ^ 1)];
+        float o = fmaf(Dd, lds_act(su + km * kDTile + dl), y);
+        if (kGate) o *= silu_k<kFast>(lds_act(sz + km * kDTile + dl));
+        st_act(outp + (size_t)(tbase + km) * D, o);
       }
     }
     __syncwarp();
@@ -312,7 +325,7 @@ template <typename Act>
 constexpr size_t fwd_smem_bytes(int NG) {
   return (size_t)FwdCfg<Act>::kStages * (3 * kTT * kDTile + 2 * kTT * 2 * NG) * sizeof(Act) +
          (std::is_same<Act, float>::value ? 0 : (size_t)FwdCfg<Act>::kStages * kTT * 2 * 2 * NG * 4) +
-         3 * FwdCfg<Act>::kStages * 8;
+         3 * FwdCfg<Act>::kStages * 8 + (size_t)kTT * kDTile * 8 + (size_t)kTT * kScanThreads * 4;
 }
 
 template <typename Act, int NG, bool kSave, bool kFast, bool kGate>
