@@ -44,17 +44,19 @@ namespace {
 constexpr int kTT = 32;           // steps per tile
 constexpr int kTilesPerChunk = kChunk / kTT;
 constexpr int kBwdWarps = 6;
-constexpr int kStages = 3;
+template <typename Act>
+struct BwdStages {
+  static constexpr int value = std::is_same<Act, float>::value ? 2 : 3;
+};
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-// Reduction scratch of one step: [q][state half][channel group][8 channels][8 states].
-// Groups of 8 channels are padded to 68 floats and state halves to 548, so
-// that 128-bit writes (a quarter-warp: 4 channels x 2 halves) and 64-bit
-// reads (a half-warp: 8 channel groups x 2 state pairs) hit distinct banks.
-constexpr int kRedGroup = 8 * 8 + 4;
-constexpr int kRedHalf = 8 * kRedGroup + 4;
-constexpr int kRedQ = 2 * kRedHalf;
-constexpr int kRedBuf = 2 * kRedQ;
+// Warp-local reduction scratch of one step: 4 blocks (q = dBm/dCm term x two
+// 4-state chunks of a lane's 8 states), each block holding one 16-byte chunk
+// per lane in lane order (conflict-free 128-bit writes), padded to 136 floats
+// so that the 64-bit reads of a half-warp (16 state pairs, one channel) hit
+// distinct banks.
+constexpr int kRedBlock = 32 * 4 + 8;
+constexpr int kRedWarpBuf = 4 * kRedBlock;
 
 struct BwdTmaParams {
   CUtensorMap map_u, map_raw, map_z, map_dout, map_B, map_C;
@@ -102,12 +104,13 @@ __device__ __forceinline__ void kahan_add(float& sum, float& comp, float x) {
   sum = t;
 }
 
-__device__ __forceinline__ int red_at(int q, int d, int n) {
-  return q * kRedQ + (n >> 3) * kRedHalf + (d >> 3) * kRedGroup + (d & 7) * 8 + (n & 7);
+// float offset of the value (q, lane-local state n) written by lane L in a warp buffer
+__device__ __forceinline__ int red_at(int q, int L, int n) {
+  return (q * 2 + ((n & 7) >> 2)) * kRedBlock + L * 4 + (n & 3);
 }
 
 template <typename Act, int NG, bool kFast, bool kGate>
-__global__ void __launch_bounds__(kBwdWarps * 32) s6_bwd_tma_kernel(const __grid_constant__ BwdTmaParams P) {
+__global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __grid_constant__ BwdTmaParams P) {
   constexpr int N2 = 2 * NG;
   constexpr int NH = NG / 2;
   constexpr int kTile = kTT * kDTile;
@@ -116,17 +119,21 @@ __global__ void __launch_bounds__(kBwdWarps * 32) s6_bwd_tma_kernel(const __grid
   constexpr int kStageElems = 4 * kTile + 2 * kBC;
   constexpr int kNSub = kChunk / kSub;  // checkpoints per chunk
 
+  constexpr int S = BwdStages<Act>::value;
   extern __shared__ __align__(1024) unsigned char smem[];
   Act* stages = reinterpret_cast<Act*>(smem);
-  float* fbase = reinterpret_cast<float*>(smem + (size_t)kStages * kStageElems * sizeof(Act));
-  float* bcf = fbase;                                           // [S][TT][2][N2] (bf16 only)
-  float* dbuf = bcf + (kBf16 ? kStages * kTT * 2 * N2 : 0);     // [kChunk][64] delta of the chunk
-  float* ckpt = dbuf + kChunk * kDTile;                         // [kNSub][128][NG]
-  float* red = ckpt + kNSub * kScanThreads * NG;                // [2][kRedBuf]
-  float* tot = red + 2 * kRedBuf;                               // [2 (sum, comp)][128][NG + 2]
+  float* fbase = reinterpret_cast<float*>(smem + (size_t)S * kStageElems * sizeof(Act));
+  float* bcf = fbase;                                              // [S][TT][2][N2] (bf16 only)
+  float2* dbuf = reinterpret_cast<float2*>(bcf + (kBf16 ? S * kTT * 2 * N2 : 0));  // [kChunk][64] (delta, delta*u)
+  float* ckpt = reinterpret_cast<float*>(dbuf + kChunk * kDTile);  // [kNSub][128][NG]
+  float* redw = ckpt + kNSub * kScanThreads * NG;                  // [4 warps][2][kRedWarpBuf]
+  float* wpart = redw + 4 * 2 * kRedWarpBuf;                       // [2][kSub][4 warps][32]
+  float4* part = reinterpret_cast<float4*>(wpart + 2 * kSub * 4 * 32);  // [kSub][128] (y, gB, Ap, -)
+  float2* bprep = reinterpret_cast<float2*>(part + kSub * kScanThreads);  // [kSub][64] (dy, dz factor)
+  float* tot = reinterpret_cast<float*>(bprep + kSub * kDTile);   // [2 (sum, comp)][128][NG + 2]
   uint64_t* full = reinterpret_cast<uint64_t*>(tot + 2 * kScanThreads * (NG + 2));
-  uint64_t* conv = full + kStages;
-  uint64_t* empty = conv + kStages;
+  uint64_t* conv = full + S;
+  uint64_t* empty = conv + S;
 
   const BwdParams& p = P.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -135,7 +142,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32) s6_bwd_tma_kernel(const __grid
   const int nchunks = p.nchunks;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&conv[s], 32);
       mbar_init(&empty[s], 4);
@@ -173,9 +180,9 @@ __global__ void __launch_bounds__(kBwdWarps * 32) s6_bwd_tma_kernel(const __grid
         for (int it = 0; it < 2 * ntl; ++it, ++item) {
           const bool passA = it < ntl;
           const int j = passA ? it : 2 * ntl - 1 - it;
-          const int s = item % kStages;
-          const uint32_t use = (uint32_t)(item / kStages);
-          if (item >= kStages && !mbar_wait(&empty[s], (use - 1) & 1, p.status)) {
+          const int s = item % S;
+          const uint32_t use = (uint32_t)(item / S);
+          if (item >= S && !mbar_wait(&empty[s], (use - 1) & 1, p.status)) {
             ok = false;
             break;
           }
@@ -192,9 +199,9 @@ __global__ void __launch_bounds__(kBwdWarps * 32) s6_bwd_tma_kernel(const __grid
         }
       }
       // never leave with copies in flight: wait for the last use of every stage
-      for (int s = 0; s < kStages && s < item; ++s) {
-        const int k_last = s + kStages * ((item - 1 - s) / kStages);
-        mbar_wait(&full[s], (uint32_t)(k_last / kStages) & 1, p.status);
+      for (int s = 0; s < S && s < item; ++s) {
+        const int k_last = s + S * ((item - 1 - s) / S);
+        mbar_wait(&full[s], (uint32_t)(k_last / S) & 1, p.status);
       }
     }
     return;
@@ -208,8 +215,8 @@ __global__ void __launch_bounds__(kBwdWarps * 32) s6_bwd_tma_kernel(const __grid
         const int ntl = chunk_tiles(c);
         for (int it = 0; it < 2 * ntl; ++it, ++item) {
           const bool passA = it < ntl;
-          const int s = item % kStages;
-          if (ok) ok = mbar_wait(&full[s], (uint32_t)(item / kStages) & 1, p.status);
+          const int s = item % S;
+          if (ok) ok = mbar_wait(&full[s], (uint32_t)(item / S) & 1, p.status);
           const Act* tb = tile_B(s);
           const Act* tc = tile_C(s);
           float* dst = bcf + (size_t)s * kTT * 2 * N2;
@@ -231,6 +238,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32) s6_bwd_tma_kernel(const __grid
   const int d = d0 + dl;
   const bool dvalid = d < D;
   const int dc = dvalid ? d : D - 1;
+  const int wl = warp;  // consumer warp 0..3
 
   // A2 = A*log2(e) on the fast path (2^x decays), A itself otherwise; sums
   // weighted by A are taken with A2 and scaled by kAscale = A / A2 at the end.
@@ -248,7 +256,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32) s6_bwd_tma_kernel(const __grid
   }
   const float bias = p.delta_bias[dc];
   const float Dd = p.Dp[dc];
-  float* my_tot = tot + tid * (NG + 2);                          // running totals
+  float* my_tot = tot + tid * (NG + 2);                            // running totals
   float* my_cmp = tot + kScanThreads * (NG + 2) + tid * (NG + 2);  // Kahan compensation
 #pragma unroll
   for (int i = 0; i < NG + 2; ++i) {
@@ -256,10 +264,11 @@ __global__ void __launch_bounds__(kBwdWarps * 32) s6_bwd_tma_kernel(const __grid
     my_cmp[i] = 0.f;
   }
 
-  // reducer role: output pair op (q = op >> 3, states 2*(op&7), +1), channel group r of 8
-  const int red_op = tid >> 3, red_r = tid & 7;
-  const int red_q = red_op >> 3, red_n = 2 * (red_op & 7);
-  const bool red_store = red_r == 0 && red_n < N2 && (red_n + 1) < N2 + 1;
+  // warp-local reducer role: output pair op = lane & 15 (q = op >> 3, states
+  // n = 2*(op & 7), n+1), channel half chh = lane >> 4 (8 channels each)
+  const int r_op = lane & 15, r_chh = lane >> 4;
+  const int r_q = r_op >> 3, r_n = 2 * (r_op & 7);
+  float* my_redw = redw + wl * 2 * kRedWarpBuf;
 
   Act* dup = static_cast<Act*>(p.du) + (size_t)b * L * D + d;
   Act* drp = static_cast<Act*>(p.d_delta_raw) + (size_t)b * L * D + d;
@@ -267,7 +276,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32) s6_bwd_tma_kernel(const __grid
 
   bool failed = false;
   int item = 0;
-  int red_parity = 0;
+  int sub_parity = 0;
   for (int c = nchunks - 1; c >= 0; --c) {
     const int t0 = c * kChunk;
     const int clen = min(kChunk, L - t0);
@@ -285,8 +294,8 @@ __global__ void __launch_bounds__(kBwdWarps * 32) s6_bwd_tma_kernel(const __grid
     for (int it = 0; it < 2 * ntl; ++it, ++item) {
       const bool passA = it < ntl;
       const int j = passA ? it : 2 * ntl - 1 - it;
-      const int s = item % kStages;
-      const uint32_t par = (uint32_t)(item / kStages) & 1;
+      const int s = item % S;
+      const uint32_t par = (uint32_t)(item / S) & 1;
       if (!failed) failed = !mbar_wait(&full[s], par, p.status);
       if (kBf16 && !failed) failed = !mbar_wait(&conv[s], par, p.status);
       __syncwarp();
@@ -307,174 +316,180 @@ __global__ void __launch_bounds__(kBwdWarps * 32) s6_bwd_tma_kernel(const __grid
         bst = N2;
       }
       if (passA) {
-        // ---------- pass A: forward recompute, delta to smem, checkpoints
-        for (int k = 0; k < cnt; k += 2) {
-          const int km = k + half;
-          const bool vm = km < cnt;
-          const float uu = lds_act(su + km * kDTile + dl);
-          const float sp = vm ? (kFast ? softplus_fast(lds_act(sr + km * kDTile + dl) + bias)
-                                       : softplus_f(lds_act(sr + km * kDTile + dl) + bias))
-                              : 0.f;
-          if (vm) dbuf[(tb + km) * kDTile + dl] = sp;
-          const float spu = sp * uu;
-          const float o_sp = __shfl_xor_sync(0xffffffffu, sp, 1);
-          const float o_spu = __shfl_xor_sync(0xffffffffu, spu, 1);
+        // ---------- pass A1: (delta, delta*u) of the owned steps into the chunk buffer
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int kk = k + e;
-            if (kk < cnt) {
-              if (((tb + kk) % kSub) == 0) {
-                float2* ck = reinterpret_cast<float2*>(ckpt + (((tb + kk) / kSub) * kScanThreads + tid) * NG);
+        for (int i = 0; i < kTT / 2; ++i) {
+          const int km = 2 * i + half;
+          if (km < cnt) {
+            const float sv = lds_act(sr + km * kDTile + dl) + bias;
+            const float sp = kFast ? softplus_fast(sv) : softplus_f(sv);
+            dbuf[(tb + km) * kDTile + dl] = make_float2(sp, sp * lds_act(su + km * kDTile + dl));
+          }
+        }
+        __syncwarp();
+        // ---------- pass A2: recompute h over the tile, checkpoint every kSub steps
+#pragma unroll 4
+        for (int kk = 0; kk < cnt; ++kk) {
+          if (((tb + kk) % kSub) == 0) {
+            float2* ck = reinterpret_cast<float2*>(ckpt + (((tb + kk) / kSub) * kScanThreads + tid) * NG);
 #pragma unroll
-                for (int i = 0; i < NH; ++i) ck[i] = h[i];
-              }
-              const float dv = (e == half) ? sp : o_sp;
-              const float duv = (e == half) ? spu : o_spu;
-              const float2 dd = make_float2(dv, dv), uu2 = make_float2(duv, duv);
-              const float* Brow = Bt + kk * bst;
+            for (int i = 0; i < NH; ++i) ck[i] = h[i];
+          }
+          const float2 dv = dbuf[(tb + kk) * kDTile + dl];
+          const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
+          const float* Brow = Bt + kk * bst;
 #pragma unroll
-              for (int i = 0; i < NH; ++i) {
-                const float2 Bv = *reinterpret_cast<const float2*>(Brow + 2 * i);
-                h[i] = ffma2(decay2<kFast>(dd, A2[i]), h[i], fmul2(uu2, Bv));
-              }
-            }
+          for (int i = 0; i < NH; ++i) {
+            const float2 Bv = *reinterpret_cast<const float2*>(Brow + 2 * i);
+            h[i] = ffma2(decay2<kFast>(dd, A2[i]), h[i], fmul2(uu2, Bv));
           }
         }
       } else {
-        // ---------- pass B: sub-chunks of this tile, last first
+        // ---------- pass B: 8-step sub-chunks of this tile, last first
         const Act* sz = tile_z(s);
         const Act* sg = tile_g(s);
         const int nsub = (cnt + kSub - 1) / kSub;
         for (int sc = nsub - 1; sc >= 0; --sc) {
-          const int ks = sc * kSub;              // first step of the sub-chunk within the tile
+          const int ks = sc * kSub;  // first step of the sub-chunk within the tile
           const int cnt8 = min(kSub, cnt - ks);
-          float2 hstart[NH];
-          {
-            const float2* ck = reinterpret_cast<const float2*>(ckpt + (((tb + ks) / kSub) * kScanThreads + tid) * NG);
-#pragma unroll
-            for (int i = 0; i < NH; ++i) hstart[i] = ck[i];
-          }
+          const int cstep = tb + ks;  // ... within the chunk
+          const float2* ckp = reinterpret_cast<const float2*>(ckpt + ((cstep / kSub) * kScanThreads + tid) * NG);
+          // B1: recompute the sub-chunk's states into registers
           float2 hs[kSub][NH];
 #pragma unroll
           for (int k = 0; k < kSub; ++k) {
             if (k < cnt8) {
-              const int kt = ks + k;
-              const float dv = dbuf[(tb + kt) * kDTile + dl];
-              const float duv = dv * lds_act(su + kt * kDTile + dl);
-              const float2 dd = make_float2(dv, dv), uu2 = make_float2(duv, duv);
-              const float* Brow = Bt + kt * bst;
+              const float2 dv = dbuf[(cstep + k) * kDTile + dl];
+              const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
+              const float* Brow = Bt + (ks + k) * bst;
 #pragma unroll
               for (int i = 0; i < NH; ++i) {
                 const float2 Bv = *reinterpret_cast<const float2*>(Brow + 2 * i);
-                const float2 hp = k == 0 ? hstart[i] : hs[k > 0 ? k - 1 : 0][i];
+                const float2 hp = k == 0 ? ckp[i] : hs[k > 0 ? k - 1 : 0][i];
                 hs[k][i] = ffma2(decay2<kFast>(dd, A2[i]), hp, fmul2(uu2, Bv));
               }
             }
           }
-          // reverse, two steps at a time: (2m+1, 2m); lane `half` owns step 2m+half
+          // B2: gate terms of the owned steps: dy = dout*silu(z), dz factor
 #pragma unroll
-          for (int m = kSub / 2 - 1; m >= 0; --m) {
-            if (2 * m < cnt8) {
-              const int kown = ks + 2 * m + half;  // tile row this lane owns
-              const bool vown = (2 * m + half) < cnt8;
-              // (t, d) work of the owned step
-              const float dv_o = dbuf[(tb + min(kown, cnt - 1)) * kDTile + dl];
-              const float u_o = lds_act(su + kown * kDTile + dl);
-              const float gout = lds_act(sg + kown * kDTile + dl);
-              float dy_o = gout, dzf_o = 0.f;
+          for (int i = 0; i < kSub / 2; ++i) {
+            const int km = 2 * i + half;
+            float2 v = make_float2(0.f, 0.f);
+            if (km < cnt8) {
+              const float gout = lds_act(sg + (ks + km) * kDTile + dl);
+              v.x = gout;
               if (kGate) {
-                const float zz = lds_act(sz + kown * kDTile + dl);
+                const float zz = lds_act(sz + (ks + km) * kDTile + dl);
                 const float sgz = kFast ? sigmoid_fast(zz) : sigmoid_f(zz);
-                dy_o = gout * zz * sgz;
-                dzf_o = gout * sgz * fmaf(zz, 1.f - sgz, 1.f);
-              }
-              if (!vown) dy_o = 0.f;
-              const float dy_x = __shfl_xor_sync(0xffffffffu, dy_o, 1);
-              float ysum[2], gbsum[2], apsum[2];
-#pragma unroll
-              for (int e = 1; e >= 0; --e) {
-                const int k = 2 * m + e;
-                ysum[e] = 0.f;
-                gbsum[e] = 0.f;
-                apsum[e] = 0.f;
-                if (k < cnt8) {
-                  const int kt = ks + k;
-                  const float dv = dbuf[(tb + kt) * kDTile + dl];
-                  const float duv = dv * lds_act(su + kt * kDTile + dl);
-                  const float dy = (e == half) ? dy_o : dy_x;
-                  const float2 dd = make_float2(dv, dv), uu2 = make_float2(duv, duv);
-                  const float2 dy2 = make_float2(dy, dy);
-                  const float* Brow = Bt + kt * bst;
-                  const float* Crow = Ct + kt * bst;
-                  float2 ya = make_float2(0.f, 0.f), gba = make_float2(0.f, 0.f), apa = make_float2(0.f, 0.f);
-                  float* rb = red + red_parity * kRedBuf;
-#pragma unroll
-                  for (int i = 0; i < NH; ++i) {
-                    const float2 Bv = *reinterpret_cast<const float2*>(Brow + 2 * i);
-                    const float2 Cv = *reinterpret_cast<const float2*>(Crow + 2 * i);
-                    const float2 a = decay2<kFast>(dd, A2[i]);
-                    const float2 hk = hs[k][i];
-                    const float2 hp = k == 0 ? hstart[i] : hs[k > 0 ? k - 1 : 0][i];
-                    const float2 g = ffma2(dy2, Cv, carry[i]);
-                    const float2 pv = fmul2(g, fmul2(a, hp));
-                    apa = ffma2(A2[i], pv, apa);
-                    accA[i] = ffma2(dd, pv, accA[i]);
-                    gba = ffma2(g, Bv, gba);
-                    ya = ffma2(Cv, hk, ya);
-                    const float2 tB = dvalid ? fmul2(g, uu2) : make_float2(0.f, 0.f);
-                    const float2 tC = dvalid ? fmul2(dy2, hk) : make_float2(0.f, 0.f);
-                    *reinterpret_cast<float2*>(rb + red_at(0, dl, half * NG + 2 * i)) = tB;
-                    *reinterpret_cast<float2*>(rb + red_at(1, dl, half * NG + 2 * i)) = tC;
-                    carry[i] = fmul2(a, g);
-                  }
-                  ysum[e] = ya.x + ya.y;
-                  gbsum[e] = gba.x + gba.y;
-                  apsum[e] = (apa.x + apa.y) * kAscale;
-                  // channel sum of this step's dBm / dCm terms, fixed order
-                  named_bar_sync(1, kScanThreads);
-                  float2 v = make_float2(0.f, 0.f);
-#pragma unroll
-                  for (int k2 = 0; k2 < 8; ++k2) {
-                    const float2 x = *reinterpret_cast<const float2*>(rb + red_at(red_q, red_r * 8 + k2, red_n));
-                    v = make_float2(v.x + x.x, v.y + x.y);
-                  }
-#pragma unroll
-                  for (int msk = 1; msk < 8; msk <<= 1) {
-                    const float ox = __shfl_xor_sync(0xffffffffu, v.x, msk);
-                    const float oy = __shfl_xor_sync(0xffffffffu, v.y, msk);
-                    v = make_float2(v.x + ox, v.y + oy);
-                  }
-                  if (red_store) {
-                    float* wp = p.ws_dbc + ((((size_t)blockIdx.x * p.B + b) * L + (t0 + tb + kt)) * 2 + red_q) * N2 + red_n;
-                    *reinterpret_cast<float2*>(wp) = v;
-                  }
-                  red_parity ^= 1;
-                }
-              }
-              // exchange the pair's partial sums: each lane keeps the full sums of its owned step
-              float ysum_f, gb_f, ap_f;
-              {
-                const float sy = half ? ysum[0] : ysum[1], ky = half ? ysum[1] : ysum[0];
-                const float sg2 = half ? gbsum[0] : gbsum[1], kg = half ? gbsum[1] : gbsum[0];
-                const float sa = half ? apsum[0] : apsum[1], ka = half ? apsum[1] : apsum[0];
-                ysum_f = ky + __shfl_xor_sync(0xffffffffu, sy, 1);
-                gb_f = kg + __shfl_xor_sync(0xffffffffu, sg2, 1);
-                ap_f = ka + __shfl_xor_sync(0xffffffffu, sa, 1);
-              }
-              if (vown && dvalid) {
-                const float y = fmaf(Dd, u_o, ysum_f);
-                const float dsp = kFast ? dsoftplus_fast(dv_o) : -expm1f(-dv_o);
-                const float dd_ = fmaf(u_o, gb_f, ap_f);
-                const float draw = dd_ * dsp;
-                const size_t o = (size_t)(t0 + tb + kown) * D;
-                st_act(dup + o, fmaf(Dd, dy_o, dv_o * gb_f));
-                st_act(drp + o, draw);
-                if (kGate) st_act(dzp + o, y * dzf_o);
-                accD = fmaf(dy_o, u_o, accD);
-                accBias += draw;
+                v.x = gout * zz * sgz;
+                v.y = gout * sgz * fmaf(zz, 1.f - sgz, 1.f);
               }
             }
+            bprep[km * kDTile + dl] = v;
           }
+          __syncwarp();
+          // B3: reverse steps; the adjoint carry is the only loop-carried value
+          float* wp_sub = wpart + sub_parity * (kSub * 4 * 32);
+#pragma unroll
+          for (int k = kSub - 1; k >= 0; --k) {
+            if (k < cnt8) {
+              const float2 dv = dbuf[(cstep + k) * kDTile + dl];
+              const float dy = bprep[k * kDTile + dl].x;
+              const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
+              const float2 dy2 = make_float2(dy, dy);
+              const float* Brow = Bt + (ks + k) * bst;
+              const float* Crow = Ct + (ks + k) * bst;
+              float2 ya = make_float2(0.f, 0.f), gba = make_float2(0.f, 0.f), apa = make_float2(0.f, 0.f);
+              float* rb = my_redw + (k & 1) * kRedWarpBuf;
+#pragma unroll
+              for (int i = 0; i < NH; i += 2) {
+                float2 tB[2], tC[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                  const int ii = i + u;
+                  if (ii < NH) {
+                    const float2 Bv = *reinterpret_cast<const float2*>(Brow + 2 * ii);
+                    const float2 Cv = *reinterpret_cast<const float2*>(Crow + 2 * ii);
+                    const float2 a = decay2<kFast>(dd, A2[ii]);
+                    const float2 hk = hs[k][ii];
+                    const float2 hp = k == 0 ? ckp[ii] : hs[k > 0 ? k - 1 : 0][ii];
+                    const float2 g = ffma2(dy2, Cv, carry[ii]);
+                    const float2 pv = fmul2(g, fmul2(a, hp));
+                    apa = ffma2(A2[ii], pv, apa);
+                    accA[ii] = ffma2(dd, pv, accA[ii]);
+                    gba = ffma2(g, Bv, gba);
+                    ya = ffma2(Cv, hk, ya);
+                    tB[u] = dvalid ? fmul2(g, uu2) : make_float2(0.f, 0.f);
+                    tC[u] = dvalid ? fmul2(dy2, hk) : make_float2(0.f, 0.f);
+                    carry[ii] = fmul2(a, g);
+                  }
+                }
+                if (NH >= 2) {
+                  *reinterpret_cast<float4*>(rb + red_at(0, lane, 2 * i)) =
+                      make_float4(tB[0].x, tB[0].y, tB[1].x, tB[1].y);
+                  *reinterpret_cast<float4*>(rb + red_at(1, lane, 2 * i)) =
+                      make_float4(tC[0].x, tC[0].y, tC[1].x, tC[1].y);
+                } else {
+                  *reinterpret_cast<float2*>(rb + red_at(0, lane, 2 * i)) = tB[0];
+                  *reinterpret_cast<float2*>(rb + red_at(1, lane, 2 * i)) = tC[0];
+                }
+              }
+              part[k * kScanThreads + tid] = make_float4(ya.x + ya.y, gba.x + gba.y, (apa.x + apa.y) * kAscale, 0.f);
+              // warp-local channel sum of this step's dBm/dCm terms (fixed order)
+              __syncwarp();
+              float2 v = make_float2(0.f, 0.f);
+              if (r_n < N2) {
+                const int rhalf = r_n / NG;
+#pragma unroll
+                for (int k2 = 0; k2 < 8; ++k2) {
+                  const int L2 = 2 * (r_chh * 8 + k2) + rhalf;
+                  const float2 x = *reinterpret_cast<const float2*>(rb + red_at(r_q, L2, r_n % NG));
+                  v = make_float2(v.x + x.x, v.y + x.y);
+                }
+              }
+              const float ox = __shfl_xor_sync(0xffffffffu, v.x, 16);
+              const float oy = __shfl_xor_sync(0xffffffffu, v.y, 16);
+              if (r_chh == 0)
+                *reinterpret_cast<float2*>(wp_sub + (k * 4 + wl) * 32 + r_q * 16 + r_n) = make_float2(v.x + ox, v.y + oy);
+            }
+          }
+          __syncwarp();
+          // B4: owned steps: combine the pair's partial sums, write du, d_delta_raw, dz
+#pragma unroll
+          for (int i = 0; i < kSub / 2; ++i) {
+            const int km = 2 * i + half;
+            if (km < cnt8 && dvalid) {
+              const float4 mine = part[km * kScanThreads + tid];
+              const float4 other = part[km * kScanThreads + (tid ^ 1)];
+              const float2 dv = dbuf[(cstep + km) * kDTile + dl];
+              const float2 bp = bprep[km * kDTile + dl];
+              const float uo = lds_act(su + (ks + km) * kDTile + dl);
+              const float ysum = mine.x + other.x, gb = mine.y + other.y, ap = mine.z + other.z;
+              const float dsp = kFast ? dsoftplus_fast(dv.x) : -expm1f(-dv.x);
+              const float draw = fmaf(uo, gb, ap) * dsp;
+              const size_t o = (size_t)(t0 + cstep + km) * D;
+              st_act(dup + o, fmaf(Dd, bp.x, dv.x * gb));
+              st_act(drp + o, draw);
+              if (kGate) st_act(dzp + o, fmaf(Dd, uo, ysum) * bp.y);
+              accD = fmaf(bp.x, uo, accD);
+              accBias += draw;
+            }
+          }
+          // B5: cross-warp sum of the sub-chunk's dBm/dCm partials (fixed warp order)
+          named_bar_sync(1, kScanThreads);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int idx = tid + e * kScanThreads;  // (step k, output o) = (idx / 32, idx % 32)
+            const int k = idx >> 5, o = idx & 31;
+            const int q = o >> 4, n = o & 15;
+            if (k < cnt8 && n < N2) {
+              const float* src = wp_sub + k * 4 * 32 + o;
+              const float v = ((src[0] + src[32]) + src[64]) + src[96];
+              p.ws_dbc[((((size_t)blockIdx.x * p.B + b) * L + (t0 + cstep + k)) * 2 + q) * N2 + n] = v;
+            }
+          }
+          sub_parity ^= 1;
+          __syncwarp();
         }
       }
       __syncwarp();
@@ -492,7 +507,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32) s6_bwd_tma_kernel(const __grid
   // ---------------- per-batch parameter partials and dh0
   {
     const float tD = my_tot[NG] + __shfl_xor_sync(0xffffffffu, my_tot[NG], 1);
-    const float tB = my_tot[NG + 1] + __shfl_xor_sync(0xffffffffu, my_tot[NG + 1], 1);
+    const float tBs = my_tot[NG + 1] + __shfl_xor_sync(0xffffffffu, my_tot[NG + 1], 1);
     if (dvalid) {
       float* wp = p.ws_param + ((size_t)b * D + d) * (N2 + 2);
 #pragma unroll
@@ -504,7 +519,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32) s6_bwd_tma_kernel(const __grid
       }
       if (half == 0) {
         wp[N2] = tD;
-        wp[N2 + 1] = tB;
+        wp[N2 + 1] = tBs;
       }
     }
   }
@@ -542,13 +557,17 @@ bool make_map(CUtensorMap* m, const void* base, int act, uint64_t rows, uint64_t
 template <typename Act>
 size_t bwd_smem_bytes(int NG) {
   const bool bf = std::is_same<Act, __nv_bfloat16>::value;
-  size_t bytes = (size_t)kStages * (4 * kTT * kDTile + 2 * kTT * 2 * NG) * sizeof(Act);
-  bytes += (bf ? (size_t)kStages * kTT * 2 * 2 * NG : 0) * 4;  // bcf
-  bytes += (size_t)kChunk * kDTile * 4;                            // dbuf
+  const int S = BwdStages<Act>::value;
+  size_t bytes = (size_t)S * (4 * kTT * kDTile + 2 * kTT * 2 * NG) * sizeof(Act);
+  bytes += (bf ? (size_t)S * kTT * 2 * 2 * NG : 0) * 4;          // bcf
+  bytes += (size_t)kChunk * kDTile * 8;                            // dbuf (float2)
   bytes += (size_t)(kChunk / kSub) * kScanThreads * NG * 4;       // ckpt
-  bytes += (size_t)2 * kRedBuf * 4;                                // red
+  bytes += (size_t)4 * 2 * kRedWarpBuf * 4;                        // redw
+  bytes += (size_t)2 * kSub * 4 * 32 * 4;                          // wpart
+  bytes += (size_t)kSub * kScanThreads * 16;                       // part (float4)
+  bytes += (size_t)kSub * kDTile * 8;                              // bprep
   bytes += (size_t)2 * kScanThreads * (NG + 2) * 4;                // tot
-  bytes += 3 * kStages * 8;                                        // barriers
+  bytes += 3 * S * 8;                                              // barriers
   return bytes;
 }
 

@@ -1,8 +1,9 @@
 // S6 forward, TMA-pipelined (sm_103a).
 //
-// CTA = (64-channel tile, batch); 6 warps:
-//   warps 0-3  consumers: lane pair (d, half) holds states half*NG .. half*NG+NG-1
-//              of channel d in registers and walks the sequence in order;
+// CTA = (channel tile, batch); 6 warps:
+//   warps 0-3  consumers: each channel's N states are split over TPC = N/4
+//              lanes, 4 states per lane in registers (the tile is 128/TPC
+//              channels); every lane walks the sequence in order;
 //   warp 4     producer: one lane streams [TT x 64] tiles of u, delta_raw, z and
 //              [TT x N] tiles of Bm, Cm into an S-stage shared-memory ring with
 //              cp.async.bulk.tensor (TMA), completion tracked by mbarriers;
@@ -11,14 +12,14 @@
 // A consumer handles a 32-step tile in three phases, so that only the state
 // update is carried from step to step and everything else has independent
 // work to overlap:
-//   1. softplus: each lane of a pair computes (delta, delta*u) for the steps
-//      it owns (even steps: lane 0, odd: lane 1) into shared memory;
-//   2. recurrence: per step, for its NG states, x = delta*A*log2(e),
+//   1. softplus: each lane computes (delta, delta*u) for the steps it owns
+//      (step k belongs to lane k mod TPC of the channel) into shared memory;
+//   2. recurrence: per step, for its 4 states, x = delta*A*log2(e),
 //      Abar = 2^x, h = Abar*h + (delta*u)*B, y += C*h with packed f32x2
 //      multiplies / FMAs (one instruction covers two states); the lane's
 //      partial readout goes to shared memory;
-//   3. output: each lane adds its partner's partial for the steps it owns,
-//      adds Dp*u, gates with silu(z) and stores.
+//   3. output: for its owned steps a lane adds the channel's TPC partial
+//      readouts in fixed order, adds Dp*u, gates with silu(z) and stores.
 // Every SSM_CHUNK_LEN steps the state is stored as a chunk state (the
 // activation saves of the kernels.rs page's multi-step forward).
 //
@@ -92,25 +93,32 @@ __device__ __forceinline__ float2 decay2(float2 dd, float2 A) {
   return make_float2(expf(x.x), expf(x.y));
 }
 
-template <typename Act, int NG, bool kSave, bool kFast, bool kGate>
+// TPC lanes per channel, 4 states per lane (N = 4 * TPC); 128 consumer lanes
+// cover kCh = 128 / TPC channels.
+template <typename Act, int TPC, bool kSave, bool kFast, bool kGate>
 __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid_constant__ FwdTmaParams P) {
-  constexpr int N2 = 2 * NG;  // == N on this path
+  constexpr int N = 4 * TPC;
+  constexpr int kCh = kScanThreads / TPC;  // channels per CTA
   constexpr int S = FwdCfg<Act>::kStages;
-  constexpr int kTile = kTT * kDTile;  // elements of a [TT x 64] tile
-  constexpr int kBC = kTT * N2;        // elements of a [TT x N] tile
+  constexpr int kTile = kTT * kCh;        // elements of a [TT x kCh] tile
+  constexpr int kBC = kTT * N;            // elements of a [TT x N] tile
   constexpr bool kBf16 = std::is_same<Act, __nv_bfloat16>::value;
   constexpr int kStageElems = 3 * kTile + 2 * kBC;
+  constexpr int kBst = kBf16 ? 2 * N : N;  // f32 row stride of B (and C) rows
+  constexpr int kOwn = kTT / TPC;          // steps whose (t, d) work a lane owns
 
   extern __shared__ __align__(1024) unsigned char smem[];
   Act* stages = reinterpret_cast<Act*>(smem);
-  float* bcf = reinterpret_cast<float*>(smem + (size_t)S * kStageElems * sizeof(Act));  // [S][TT][2][N2]
-  uint64_t* full = reinterpret_cast<uint64_t*>(bcf + (kBf16 ? S * kTT * 2 * N2 : 0));
+  float* bcf = reinterpret_cast<float*>(smem + (size_t)S * kStageElems * sizeof(Act));  // [S][TT][2][N]
+  float2* prep = reinterpret_cast<float2*>(bcf + (kBf16 ? S * kTT * 2 * N : 0));         // [TT][kCh]
+  float* ypart = reinterpret_cast<float*>(prep + kTT * kCh);                            // [TT][128]
+  uint64_t* full = reinterpret_cast<uint64_t*>(ypart + kTT * kScanThreads);
   uint64_t* conv = full + S;
   uint64_t* empty = conv + S;
 
   const FwdParams& p = P.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.y, d0 = blockIdx.x * kDTile;
+  const int b = blockIdx.y, d0 = blockIdx.x * kCh;
   const int L = p.L, D = p.D;
   const int ntiles = (L + kTT - 1) / kTT;
 
@@ -167,13 +175,14 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
       for (int k = 0; k < ntiles; ++k) {
         const int s = k % S;
         if (!mbar_wait(&full[s], (uint32_t)(k / S) & 1, p.status)) break;
-        const Act* tb = tile_B(s);
-        const Act* tc = tile_C(s);
-        float* dst = bcf + (size_t)s * kTT * 2 * N2;
-        for (int e = lane; e < kBC; e += 32) {
-          const int t = e / N2, n = e % N2;
-          dst[(t * 2 + 0) * N2 + n] = lds_act(tb + e);
-          dst[(t * 2 + 1) * N2 + n] = lds_act(tc + e);
+        const __nv_bfloat162* tb = reinterpret_cast<const __nv_bfloat162*>(tile_B(s));
+        const __nv_bfloat162* tc = reinterpret_cast<const __nv_bfloat162*>(tile_C(s));
+        float* dst = bcf + (size_t)s * kTT * 2 * N;
+#pragma unroll 4
+        for (int e = lane; e < kBC / 2; e += 32) {
+          const int t = (2 * e) / N, n = (2 * e) % N;
+          *reinterpret_cast<float2*>(dst + (t * 2 + 0) * N + n) = __bfloat1622float2(tb[e]);
+          *reinterpret_cast<float2*>(dst + (t * 2 + 1) * N + n) = __bfloat1622float2(tc[e]);
         }
         mbar_arrive(&conv[s]);
       }
@@ -182,29 +191,25 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
   }
 
   // ---------------- consumers
-  const int half = tid & 1;
-  const int dl = tid >> 1;
-  const int d = d0 + dl;
+  const int q = tid % TPC;    // state group: states 4q .. 4q+3
+  const int cl = tid / TPC;   // channel within the CTA
+  const int d = d0 + cl;
   const bool dvalid = d < D;
   const int dc = dvalid ? d : D - 1;
-  constexpr int NH = NG / 2;  // float2 pairs per lane
 
-  float2 A2[NH], h[NH];
+  float2 A2[2], h[2];
 #pragma unroll
-  for (int i = 0; i < NH; ++i) {
-    const int n = half * NG + 2 * i;
-    const float a0 = -expf(p.A_log[dc * N2 + n]);
-    const float a1 = -expf(p.A_log[dc * N2 + n + 1]);
+  for (int i = 0; i < 2; ++i) {
+    const int n = 4 * q + 2 * i;
+    const float a0 = -expf(p.A_log[dc * N + n]);
+    const float a1 = -expf(p.A_log[dc * N + n + 1]);
     A2[i] = kFast ? make_float2(a0 * kLog2e, a1 * kLog2e) : make_float2(a0, a1);
-    h[i] = p.h0 ? make_float2(p.h0[((size_t)b * D + dc) * N2 + n], p.h0[((size_t)b * D + dc) * N2 + n + 1])
+    h[i] = p.h0 ? make_float2(p.h0[((size_t)b * D + dc) * N + n], p.h0[((size_t)b * D + dc) * N + n + 1])
                 : make_float2(0.f, 0.f);
   }
   const float bias = p.delta_bias[dc];
   const float Dd = p.Dp[dc];
   Act* outp = static_cast<Act*>(p.out) + (size_t)b * L * D + d;
-
-  float2* prep = reinterpret_cast<float2*>(empty + S);   // [TT][64] (delta, delta*u)
-  float* ypart = reinterpret_cast<float*>(prep + kTT * kDTile);  // [TT][128] partial readouts
 
   for (int k = 0; k < ntiles; ++k) {
     const int s = k % S;
@@ -214,67 +219,61 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
     const int tbase = k * kTT;
     const int cnt = min(kTT, L - tbase);
     if (kSave && (tbase % kChunk) == 0 && dvalid) {
-      float* cs = p.chunk_states + (((size_t)b * p.nchunks + tbase / kChunk) * D + d) * N2 + half * NG;
-#pragma unroll
-      for (int i = 0; i < NH; ++i) reinterpret_cast<float2*>(cs)[i] = h[i];
+      float* cs = p.chunk_states + (((size_t)b * p.nchunks + tbase / kChunk) * D + d) * N + 4 * q;
+      *reinterpret_cast<float4*>(cs) = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
     }
     const Act* su = tile_u(s);
     const Act* sr = tile_raw(s);
     const Act* sz = tile_z(s);
-    const float* Bt;
-    const float* Ct;
-    int bstride;
-    if (kBf16) {
-      Bt = bcf + (size_t)s * kTT * 2 * N2 + half * NG;
-      Ct = Bt + N2;
-      bstride = 2 * N2;
-    } else {
-      Bt = reinterpret_cast<const float*>(tile_B(s)) + half * NG;
-      Ct = reinterpret_cast<const float*>(tile_C(s)) + half * NG;
-      bstride = N2;
-    }
-    // phase 1: (delta, delta*u) of the steps this lane owns (k = 2i + half),
-    // independent of each other; steps past the end get (0, 0), which leaves
-    // the state unchanged (Abar = 1, input 0)
+    const float* Bt = (kBf16 ? bcf + (size_t)s * kTT * 2 * N : reinterpret_cast<const float*>(tile_B(s))) + 4 * q;
+    const float* Ct = (kBf16 ? Bt + N : reinterpret_cast<const float*>(tile_C(s)) + 4 * q);
+
+    // phase 1: (delta, delta*u) of the owned steps (k % TPC == q); steps past
+    // the end get (0, 0), which leaves the state unchanged (Abar = 1, input 0)
 #pragma unroll
-    for (int i = 0; i < kTT / 2; ++i) {
-      const int km = 2 * i + half;
+    for (int i = 0; i < kOwn; ++i) {
+      const int km = i * TPC + q;
       float2 v = make_float2(0.f, 0.f);
       if (km < cnt) {
-        const float sp = softplus_k<kFast>(lds_act(sr + km * kDTile + dl) + bias);
-        v = make_float2(sp, sp * lds_act(su + km * kDTile + dl));
+        const float sp = softplus_k<kFast>(lds_act(sr + km * kCh + cl) + bias);
+        v = make_float2(sp, sp * lds_act(su + km * kCh + cl));
       }
-      prep[km * kDTile + dl] = v;
+      prep[km * kCh + cl] = v;
     }
     __syncwarp();
     // phase 2: the recurrence; only h is carried from step to step
-#pragma unroll 4
-    for (int kk = 0; kk < cnt; ++kk) {
-      const float2 dv = prep[kk * kDTile + dl];
+    auto step = [&](int kk) {
+      const float2 dv = prep[kk * kCh + cl];
       const float2 dd = make_float2(dv.x, dv.x);
       const float2 uu = make_float2(dv.y, dv.y);
-      const float* Brow = Bt + kk * bstride;
-      const float* Crow = Ct + kk * bstride;
-      float2 yacc = make_float2(0.f, 0.f);
+      const float4 Bv = *reinterpret_cast<const float4*>(Bt + kk * kBst);
+      const float4 Cv = *reinterpret_cast<const float4*>(Ct + kk * kBst);
+      const float2 a0 = decay2<kFast>(dd, A2[0]);
+      const float2 a1 = decay2<kFast>(dd, A2[1]);
+      h[0] = ffma2(a0, h[0], fmul2(uu, make_float2(Bv.x, Bv.y)));
+      h[1] = ffma2(a1, h[1], fmul2(uu, make_float2(Bv.z, Bv.w)));
+      const float2 y2 = ffma2(make_float2(Cv.z, Cv.w), h[1], fmul2(make_float2(Cv.x, Cv.y), h[0]));
+      ypart[kk * kScanThreads + tid] = y2.x + y2.y;
+    };
+    if (cnt == kTT) {
 #pragma unroll
-      for (int i = 0; i < NH; ++i) {
-        const float2 Bv = *reinterpret_cast<const float2*>(Brow + 2 * i);
-        const float2 Cv = *reinterpret_cast<const float2*>(Crow + 2 * i);
-        const float2 a = decay2<kFast>(dd, A2[i]);
-        h[i] = ffma2(a, h[i], fmul2(uu, Bv));
-        yacc = ffma2(Cv, h[i], yacc);
-      }
-      ypart[kk * kScanThreads + tid] = yacc.x + yacc.y;
+      for (int kk = 0; kk < kTT; ++kk) step(kk);
+    } else {
+      for (int kk = 0; kk < cnt; ++kk) step(kk);
     }
     __syncwarp();
-    // phase 3: each lane completes the readout of its owned steps, gates and stores
+    // phase 3: complete the readout of the owned steps (fixed order over the
+    // channel's TPC lanes), add Dp*u, gate with silu(z), store
 #pragma unroll
-    for (int i = 0; i < kTT / 2; ++i) {
-      const int km = 2 * i + half;
+    for (int i = 0; i < kOwn; ++i) {
+      const int km = i * TPC + q;
       if (km < cnt && dvalid) {
-        const float y = ypart[km * kScanThreads + tid] + ypart[km * kScanThreads + (tid ^ 1)];
-        float o = fmaf(Dd, lds_act(su + km * kDTile + dl), y);
-        if (kGate) o *= silu_k<kFast>(lds_act(sz + km * kDTile + dl));
+        const float* yp = ypart + km * kScanThreads + cl * TPC;
+        float y = yp[0];
+#pragma unroll
+        for (int r = 1; r < TPC; ++r) y += yp[r];
+        float o = fmaf(Dd, lds_act(su + km * kCh + cl), y);
+        if (kGate) o *= silu_k<kFast>(lds_act(sz + km * kCh + cl));
         st_act(outp + (size_t)(tbase + km) * D, o);
       }
     }
@@ -282,9 +281,8 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
     if (lane == 0) mbar_arrive(&empty[s]);
   }
   if (p.h_last && dvalid) {
-    float* hl = p.h_last + ((size_t)b * D + d) * N2 + half * NG;
-#pragma unroll
-    for (int i = 0; i < NH; ++i) reinterpret_cast<float2*>(hl)[i] = h[i];
+    float* hl = p.h_last + ((size_t)b * D + d) * N + 4 * q;
+    *reinterpret_cast<float4*>(hl) = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
   }
 }
 
@@ -321,30 +319,32 @@ bool make_map(CUtensorMap* m, const void* base, int act, uint64_t rows, uint64_t
   return r == CUDA_SUCCESS;
 }
 
-template <typename Act>
-constexpr size_t fwd_smem_bytes(int NG) {
-  return (size_t)FwdCfg<Act>::kStages * (3 * kTT * kDTile + 2 * kTT * 2 * NG) * sizeof(Act) +
-         (std::is_same<Act, float>::value ? 0 : (size_t)FwdCfg<Act>::kStages * kTT * 2 * 2 * NG * 4) +
-         3 * FwdCfg<Act>::kStages * 8 + (size_t)kTT * kDTile * 8 + (size_t)kTT * kScanThreads * 4;
+template <typename Act, int TPC>
+constexpr size_t fwd_smem_bytes() {
+  constexpr int N = 4 * TPC, kCh = kScanThreads / TPC, S = FwdCfg<Act>::kStages;
+  constexpr bool bf = std::is_same<Act, __nv_bfloat16>::value;
+  return (size_t)S * (3 * kTT * kCh + 2 * kTT * N) * sizeof(Act) + (bf ? (size_t)S * kTT * 2 * N * 4 : 0) +
+         (size_t)kTT * kCh * 8 + (size_t)kTT * kScanThreads * 4 + 3 * S * 8;
 }
 
-template <typename Act, int NG, bool kSave, bool kFast, bool kGate>
+template <typename Act, int TPC, bool kSave, bool kFast, bool kGate>
 cudaError_t launch_one(const FwdTmaParams& P, cudaStream_t stream) {
-  auto kern = s6_fwd_tma_kernel<Act, NG, kSave, kFast, kGate>;
-  const size_t smem = fwd_smem_bytes<Act>(NG);
+  auto kern = s6_fwd_tma_kernel<Act, TPC, kSave, kFast, kGate>;
+  constexpr size_t smem = fwd_smem_bytes<Act, TPC>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((P.p.D + kDTile - 1) / kDTile, P.p.B);
+  constexpr int kCh = kScanThreads / TPC;
+  const dim3 grid((P.p.D + kCh - 1) / kCh, P.p.B);
   kern<<<grid, kFwdWarps * 32, smem, stream>>>(P);
   return cudaGetLastError();
 }
 
-template <typename Act, int NG, bool kFast>
-cudaError_t launch_ng(const FwdTmaParams& P, cudaStream_t stream) {
+template <typename Act, int TPC, bool kFast>
+cudaError_t launch_tpc(const FwdTmaParams& P, cudaStream_t stream) {
   const bool save = P.p.chunk_states != nullptr, gate = P.p.z != nullptr;
   if (save)
-    return gate ? launch_one<Act, NG, true, kFast, true>(P, stream) : launch_one<Act, NG, true, kFast, false>(P, stream);
-  return gate ? launch_one<Act, NG, false, kFast, true>(P, stream) : launch_one<Act, NG, false, kFast, false>(P, stream);
+    return gate ? launch_one<Act, TPC, true, kFast, true>(P, stream) : launch_one<Act, TPC, true, kFast, false>(P, stream);
+  return gate ? launch_one<Act, TPC, false, kFast, true>(P, stream) : launch_one<Act, TPC, false, kFast, false>(P, stream);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -371,22 +371,23 @@ cudaError_t launch_fwd_tma(const FwdParams& p, int act, cudaStream_t stream) {
   FwdTmaParams P;
   memset(&P, 0, sizeof(P));
   P.p = p;
+  const int tpc = p.N / 4;
+  const uint32_t kch = (uint32_t)(kScanThreads / tpc);
   const uint64_t rows = (uint64_t)p.B * p.L;
-  bool ok = make_map(&P.map_u, p.u, act, rows, p.D, kTT, kDTile) &&
-            make_map(&P.map_raw, p.delta_raw, act, rows, p.D, kTT, kDTile) &&
+  bool ok = make_map(&P.map_u, p.u, act, rows, p.D, kTT, kch) &&
+            make_map(&P.map_raw, p.delta_raw, act, rows, p.D, kTT, kch) &&
             make_map(&P.map_B, p.Bm, act, rows, p.N, kTT, p.N) &&
             make_map(&P.map_C, p.Cm, act, rows, p.N, kTT, p.N);
-  if (p.z) ok = ok && make_map(&P.map_z, p.z, act, rows, p.D, kTT, kDTile);
+  if (p.z) ok = ok && make_map(&P.map_z, p.z, act, rows, p.D, kTT, kch);
   if (!ok) return cudaErrorInvalidValue;
-  const int NG = p.N / 2;
   if (act == SSM_BF16) {
-    if (NG == 8) return launch_ng<__nv_bfloat16, 8, true>(P, stream);
-    if (NG == 4) return launch_ng<__nv_bfloat16, 4, true>(P, stream);
+    if (tpc == 4) return launch_tpc<__nv_bfloat16, 4, true>(P, stream);
+    if (tpc == 2) return launch_tpc<__nv_bfloat16, 2, true>(P, stream);
     return cudaErrorInvalidValue;
   }
-  if (NG == 8) return launch_ng<float, 8, false>(P, stream);
-  if (NG == 4) return launch_ng<float, 4, false>(P, stream);
-  if (NG == 2) return launch_ng<float, 2, false>(P, stream);
+  if (tpc == 4) return launch_tpc<float, 4, false>(P, stream);
+  if (tpc == 2) return launch_tpc<float, 2, false>(P, stream);
+  if (tpc == 1) return launch_tpc<float, 1, false>(P, stream);
   return cudaErrorInvalidValue;
 }
 
