@@ -228,20 +228,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
     const float* Bt = (kBf16 ? bcf + (size_t)s * kTT * 2 * N : reinterpret_cast<const float*>(tile_B(s))) + 4 * q;
     const float* Ct = (kBf16 ? Bt + N : reinterpret_cast<const float*>(tile_C(s)) + 4 * q);
 
-    // phase 1: (delta, delta*u) of the owned steps (k % TPC == q); steps past
-    // the end get (0, 0), which leaves the state unchanged (Abar = 1, input 0)
-#pragma unroll
-    for (int i = 0; i < kOwn; ++i) {
-      const int km = i * TPC + q;
-      float2 v = make_float2(0.f, 0.f);
-      if (km < cnt) {
-        const float sp = softplus_k<kFast>(lds_act(sr + km * kCh + cl) + bias);
-        v = make_float2(sp, sp * lds_act(su + km * kCh + cl));
-      }
-      prep[km * kCh + cl] = v;
-    }
-    __syncwarp();
-    // phase 2: the recurrence; only h is carried from step to step
+    // one recurrence step for this lane's 4 states; the partial readout goes to ypart
     auto step = [&](int kk) {
       const float2 dv = prep[kk * kCh + cl];
       const float2 dd = make_float2(dv.x, dv.x);
@@ -255,28 +242,59 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
       const float2 y2 = ffma2(make_float2(Cv.z, Cv.w), h[1], fmul2(make_float2(Cv.x, Cv.y), h[0]));
       ypart[kk * kScanThreads + tid] = y2.x + y2.y;
     };
-    if (cnt == kTT) {
+    // One tile in three phases.  kFull (all kTT steps valid, the common case)
+    // has no data-dependent branches, so the independent iterations of each
+    // phase overlap; the last, partial tile takes the guarded version.
+    auto run_tile = [&](auto full_tag) {
+      constexpr bool kFull = decltype(full_tag)::value;
+      const int n_valid = kFull ? kTT : cnt;
+      // phase 1: (delta, delta*u) of the owned steps (k % TPC == q); steps past
+      // the end get (0, 0), which leaves the state unchanged (Abar = 1, input 0)
+      float2 pv[kOwn];
 #pragma unroll
-      for (int kk = 0; kk < kTT; ++kk) step(kk);
-    } else {
-      for (int kk = 0; kk < cnt; ++kk) step(kk);
-    }
-    __syncwarp();
-    // phase 3: complete the readout of the owned steps (fixed order over the
-    // channel's TPC lanes), add Dp*u, gate with silu(z), store
+      for (int i = 0; i < kOwn; ++i) {
+        const int km = i * TPC + q;
+        const int kr = kFull ? km : min(km, n_valid - 1);
+        const float sp = softplus_k<kFast>(lds_act(sr + kr * kCh + cl) + bias);
+        pv[i] = make_float2(sp, sp * lds_act(su + kr * kCh + cl));
+        if (!kFull && km >= n_valid) pv[i] = make_float2(0.f, 0.f);
+      }
 #pragma unroll
-    for (int i = 0; i < kOwn; ++i) {
-      const int km = i * TPC + q;
-      if (km < cnt && dvalid) {
-        const float* yp = ypart + km * kScanThreads + cl * TPC;
+      for (int i = 0; i < kOwn; ++i) prep[(i * TPC + q) * kCh + cl] = pv[i];
+      __syncwarp();
+      // phase 2: the recurrence; only h is carried from step to step
+      if (kFull) {
+#pragma unroll
+        for (int kk = 0; kk < kTT; ++kk) step(kk);
+      } else {
+        for (int kk = 0; kk < n_valid; ++kk) step(kk);
+      }
+      __syncwarp();
+      // phase 3: complete the readout of the owned steps (fixed order over the
+      // channel's TPC lanes), add Dp*u, gate with silu(z), store
+      float ov[kOwn];
+#pragma unroll
+      for (int i = 0; i < kOwn; ++i) {
+        const int km = i * TPC + q;
+        const int kr = kFull ? km : min(km, n_valid - 1);
+        const float* yp = ypart + kr * kScanThreads + cl * TPC;
         float y = yp[0];
 #pragma unroll
         for (int r = 1; r < TPC; ++r) y += yp[r];
-        float o = fmaf(Dd, lds_act(su + km * kCh + cl), y);
-        if (kGate) o *= silu_k<kFast>(lds_act(sz + km * kCh + cl));
-        st_act(outp + (size_t)(tbase + km) * D, o);
+        float o = fmaf(Dd, lds_act(su + kr * kCh + cl), y);
+        if (kGate) o *= silu_k<kFast>(lds_act(sz + kr * kCh + cl));
+        ov[i] = o;
       }
-    }
+#pragma unroll
+      for (int i = 0; i < kOwn; ++i) {
+        const int km = i * TPC + q;
+        if (dvalid && (kFull || km < n_valid)) st_act(outp + (size_t)(tbase + km) * D, ov[i]);
+      }
+    };
+    if (cnt == kTT)
+      run_tile(std::true_type{});
+    else
+      run_tile(std::false_type{});
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
