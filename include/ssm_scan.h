@@ -169,6 +169,35 @@ int ssm_scan_bwd_finalize(int64_t batch, int64_t seqlen, int64_t dim, int64_t ds
                           const void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * ssm_scan_bwd for callers that cannot allocate device memory.  (The pages
+ * have no counterpart of this entry point; it is a deployment convenience.)
+ * Same arguments and results as ssm_scan_bwd, minus ws/ws_bytes: the scratch
+ * for the partial sums is a fixed array of ssm_noalloc_scratch_bytes()
+ * (16 MiB) inside the library, reserved on every GPU that loads it until the
+ * process exits.  Meant for callers that must not call cudaMalloc: hosts whose
+ * framework owns the device allocator, plugin interfaces that pass only input
+ * and output pointers, loops that must not allocate or synchronise.
+ *   - Shapes needing more scratch than that (ssm_bwd_workspace_bytes() >
+ *     ssm_noalloc_scratch_bytes()) are rejected with SSM_ERR_UNSUPPORTED.
+ *   - The first call on a device looks the array's device address up with
+ *     cudaGetSymbolAddress (that device current); make it before any stream
+ *     capture.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents; calls whose GPU work may overlap race on it and must be
+ *     ordered by the caller (same stream, or events).
+ *   - Allocates and frees nothing.
+ */
+size_t ssm_noalloc_scratch_bytes(void);
+
+int ssm_scan_bwd_noalloc(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
+                         const void *u, const void *delta_raw, const void *z, const void *Bm,
+                         const void *Cm, const float *A_log, const float *Dp,
+                         const float *delta_bias, const float *h0, const float *chunk_states,
+                         const void *dout, const float *dh_last, void *du, void *d_delta_raw,
+                         void *dz, void *dBm, void *dCm, float *dA_log, float *dDp,
+                         float *d_delta_bias, float *dh0, void *stream);
+
+/*
  * One decode step, T = 1 (kernels.rs page: "Single-step SSM forward (T=1
  * inference)").  u, delta_raw, z [B][D] (z nullable), Bm, Cm [B][N], h
  * [B][D][N] f32 read and overwritten in place with the new state, out [B][D].

@@ -156,6 +156,20 @@ int fwd_common(int64_t B, int64_t L, int64_t D, int64_t N, int act, const void* 
 
 }  // namespace
 
+namespace s6 {
+
+// Records a message for ssm_last_error() and returns `code` (for entry points
+// defined in other translation units).
+int report_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+}  // namespace s6
+
 extern "C" {
 
 const char* ssm_status_string(int status) {

@@ -66,6 +66,8 @@ bool fwd_tma_supported(const FwdParams& p, int act);
 cudaError_t launch_fwd_tma(const FwdParams& p, int act, cudaStream_t stream);
 // Device address of the library's status word on the current device (nullptr on error).
 unsigned int* device_status_word();
+// Sets the calling thread's ssm_last_error() message; returns `code`.
+int report_error(int code, const char* fmt, ...);
 cudaError_t launch_bwd(const BwdParams& p, int act, cudaStream_t stream);
 bool bwd_tma_supported(const BwdParams& p, int act);
 cudaError_t launch_bwd_tma(const BwdParams& p, int act, cudaStream_t stream);
