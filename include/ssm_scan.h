@@ -104,6 +104,10 @@ int64_t ssm_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t dim, int6
  *            chunk_states [B][nc][D][N] = state before step c*SSM_CHUNK_LEN
  *            (chunk 0 holds h0); it is what ssm_scan_bwd reads.
  *   ws/ws_bytes: scratch of ssm_fwd_workspace_bytes() bytes (nullable when 0).
+ *     Long sequences over few channels are split into time segments that run
+ *     in parallel (a chunked parallel scan: per-segment decay products and
+ *     end states, composed in segment order); ws holds those aggregates.  The
+ *     plan is a function of the shape alone, so results are deterministic.
  */
 int ssm_scan_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
                  const void *u, const void *delta_raw, const void *z, const void *Bm,

@@ -95,6 +95,31 @@ int check_ws(const void* ws, size_t ws_bytes, int64_t total) {
   return SSM_OK;
 }
 
+// The segment plan of the forward is a function of the shape only (it
+// targets a 152-SM GB300), so workspace sizes never depend on the device.
+constexpr int kPlanSms = 152;
+
+struct FwdWorkspace {
+  int nseg, seg_len;
+  int64_t agg_off, start_off, total;
+};
+
+FwdWorkspace fwd_ws_layout(int64_t B, int64_t L, int64_t D, int64_t N) {
+  FwdWorkspace w;
+  w.nseg = s6::fwd_segments((int)B, (int)L, (int)D, (int)N, kPlanSms);
+  w.seg_len = (int)L;
+  w.agg_off = w.start_off = w.total = 0;
+  if (w.nseg > 1) {
+    w.seg_len = (int)(((L + w.nseg - 1) / w.nseg + SSM_CHUNK_LEN - 1) / SSM_CHUNK_LEN * SSM_CHUNK_LEN);
+    w.nseg = (int)((L + w.seg_len - 1) / w.seg_len);
+    const int64_t cells = B * w.nseg * D * N;
+    w.agg_off = 0;
+    w.start_off = align_up(cells * 2 * (int64_t)sizeof(float), 256);
+    w.total = align_up(w.start_off + cells * (int64_t)sizeof(float), 256);
+  }
+  return w;
+}
+
 struct BwdWorkspace {
   int64_t dbc_off, dbc_bytes, param_off, param_bytes, total;
 };
@@ -113,7 +138,8 @@ BwdWorkspace bwd_ws_layout(int64_t B, int64_t L, int64_t D, int64_t N) {
 int fwd_common(int64_t B, int64_t L, int64_t D, int64_t N, int act, const void* u,
                const void* delta_raw, const void* z, const void* Bm, const void* Cm,
                const float* A_log, const float* Dp, const float* delta_bias, const float* h0,
-               void* out, float* h_last, float* chunk_states, bool save, void* stream) {
+               void* out, float* h_last, float* chunk_states, bool save, void* ws,
+               size_t ws_bytes, void* stream) {
   S6_TRY(check_shape(B, L, D, N, act));
   const size_t e = act_size(act);
   const int64_t bld = B * L * D, bln = B * L * N, dn = D * N;
@@ -149,7 +175,19 @@ int fwd_common(int64_t B, int64_t L, int64_t D, int64_t N, int act, const void* 
   p.nchunks = (int)ssm_num_chunks(L);
   p.status = s6::device_status_word();
   if (!p.status) return fail(SSM_ERR_CUDA, "cannot locate the device status word");
-  cudaError_t ce = s6::fwd_tma_supported(p, act) ? s6::launch_fwd_tma(p, act, st) : s6::launch_fwd(p, act, st);
+  const FwdWorkspace w = fwd_ws_layout(B, L, D, N);
+  S6_TRY(check_ws(ws, ws_bytes, w.total));
+  p.nseg = 1;
+  p.seg_len = (int)L;
+  p.seg_agg = p.seg_start = nullptr;
+  const bool tma = s6::fwd_tma_supported(p, act);
+  if (tma && w.nseg > 1) {
+    p.nseg = w.nseg;
+    p.seg_len = w.seg_len;
+    p.seg_agg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.agg_off);
+    p.seg_start = reinterpret_cast<float*>(static_cast<char*>(ws) + w.start_off);
+  }
+  cudaError_t ce = tma ? s6::launch_fwd_tma(p, act, st) : s6::launch_fwd(p, act, st);
   if (ce != cudaSuccess) return cuda_fail(ce, "ssm_scan_fwd launch");
   return SSM_OK;
 }
@@ -209,7 +247,7 @@ int64_t ssm_num_chunks(int64_t seqlen) {
 
 int64_t ssm_fwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act) {
   if (check_shape(batch, seqlen, dim, dstate, act) != SSM_OK) return -1;
-  return 0;
+  return fwd_ws_layout(batch, seqlen, dim, dstate).total;
 }
 
 int64_t ssm_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act) {
@@ -222,9 +260,8 @@ int ssm_scan_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int
                  const void* Cm, const float* A_log, const float* Dp, const float* delta_bias,
                  const float* h0, void* out, float* h_last, float* chunk_states, void* ws,
                  size_t ws_bytes, void* stream) {
-  (void)ws; (void)ws_bytes;
   return fwd_common(batch, seqlen, dim, dstate, act, u, delta_raw, z, Bm, Cm, A_log, Dp,
-                    delta_bias, h0, out, h_last, chunk_states, true, stream);
+                    delta_bias, h0, out, h_last, chunk_states, true, ws, ws_bytes, stream);
 }
 
 int ssm_scan_fwd_nosave(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
@@ -232,9 +269,8 @@ int ssm_scan_fwd_nosave(int64_t batch, int64_t seqlen, int64_t dim, int64_t dsta
                         const void* Cm, const float* A_log, const float* Dp,
                         const float* delta_bias, const float* h0, void* out, float* h_last,
                         void* ws, size_t ws_bytes, void* stream) {
-  (void)ws; (void)ws_bytes;
   return fwd_common(batch, seqlen, dim, dstate, act, u, delta_raw, z, Bm, Cm, A_log, Dp,
-                    delta_bias, h0, out, h_last, nullptr, false, stream);
+                    delta_bias, h0, out, h_last, nullptr, false, ws, ws_bytes, stream);
 }
 
 int ssm_scan_bwd_partials(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
@@ -344,7 +380,7 @@ int ssm_step(int64_t batch, int64_t dim, int64_t dstate, int act, const void* u,
              void* stream) {
   S6_TRY(need(h, batch * dim * (dstate > 0 ? dstate : 0), 4, "h"));
   return fwd_common(batch, 1, dim, dstate, act, u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias,
-                    h, out, h, nullptr, false, stream);
+                    h, out, h, nullptr, false, nullptr, 0, stream);
 }
 
 }  // extern "C"

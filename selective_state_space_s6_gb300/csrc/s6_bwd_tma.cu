@@ -126,8 +126,8 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
   float* bcf = fbase;                                              // [S][TT][2][N2] (bf16 only)
   float2* dbuf = reinterpret_cast<float2*>(bcf + (kBf16 ? S * kTT * 2 * N2 : 0));  // [kChunk][64] (delta, delta*u)
   float* ckpt = reinterpret_cast<float*>(dbuf + kChunk * kDTile);  // [kNSub][128][NG]
-  float* redw = ckpt + kNSub * kScanThreads * NG;                  // [4 warps][2][kRedWarpBuf]
-  float* wpart = redw + 4 * 2 * kRedWarpBuf;                       // [2][kSub][4 warps][32]
+  float* redw = ckpt + kNSub * kScanThreads * NG;                  // [4 warps][4 slots][kRedWarpBuf]
+  float* wpart = redw + 4 * 4 * kRedWarpBuf;                       // [2][kSub][4 warps][32]
   float4* part = reinterpret_cast<float4*>(wpart + 2 * kSub * 4 * 32);  // [kSub][128] (y, gB, Ap, -)
   float2* bprep = reinterpret_cast<float2*>(part + kSub * kScanThreads);  // [kSub][64] (dy, dz factor)
   float* tot = reinterpret_cast<float*>(bprep + kSub * kDTile);   // [2 (sum, comp)][128][NG + 2]
@@ -268,14 +268,31 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
   // n = 2*(op & 7), n+1), channel half chh = lane >> 4 (8 channels each)
   const int r_op = lane & 15, r_chh = lane >> 4;
   const int r_q = r_op >> 3, r_n = 2 * (r_op & 7);
-  float* my_redw = redw + wl * 2 * kRedWarpBuf;
+  const int r_half = r_n / NG, r_nl = r_n % NG;
+  float* my_redw = redw + wl * 4 * kRedWarpBuf;  // 4 step slots
 
   Act* dup = static_cast<Act*>(p.du) + (size_t)b * L * D + d;
   Act* drp = static_cast<Act*>(p.d_delta_raw) + (size_t)b * L * D + d;
   Act* dzp = kGate ? static_cast<Act*>(p.dz) + (size_t)b * L * D + d : nullptr;
+  float* ws_dbc_b = p.ws_dbc + ((size_t)blockIdx.x * p.B + b) * (size_t)L * 2 * N2;
+
+  // the NH state pairs of this lane from a row of B or C (16-byte loads)
+  auto load_row = [&](const float* row, float2 (&v)[NH]) {
+    if constexpr (NH >= 2) {
+#pragma unroll
+      for (int i = 0; i < NH; i += 2) {
+        const float4 f = *reinterpret_cast<const float4*>(row + 2 * i);
+        v[i] = make_float2(f.x, f.y);
+        v[i + 1] = make_float2(f.z, f.w);
+      }
+    } else {
+      v[0] = *reinterpret_cast<const float2*>(row);
+    }
+  };
 
   bool failed = false;
-  int item = 0;
+  int s = 0;          // ring stage of the current item
+  uint32_t par = 0;   // its phase parity
   int sub_parity = 0;
   for (int c = nchunks - 1; c >= 0; --c) {
     const int t0 = c * kChunk;
@@ -288,14 +305,11 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
     float2 h[NH];
     {
       const float* cs = p.chunk_states + (((size_t)b * nchunks + c) * D + dc) * N2 + half * NG;
-#pragma unroll
-      for (int i = 0; i < NH; ++i) h[i] = *reinterpret_cast<const float2*>(cs + 2 * i);
+      load_row(cs, h);
     }
-    for (int it = 0; it < 2 * ntl; ++it, ++item) {
+    for (int it = 0; it < 2 * ntl; ++it) {
       const bool passA = it < ntl;
       const int j = passA ? it : 2 * ntl - 1 - it;
-      const int s = item % S;
-      const uint32_t par = (uint32_t)(item / S) & 1;
       if (!failed) failed = !mbar_wait(&full[s], par, p.status);
       if (kBf16 && !failed) failed = !mbar_wait(&conv[s], par, p.status);
       __syncwarp();
@@ -303,47 +317,49 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
       const int cnt = min(kTT, clen - tb);
       const Act* su = tile_u(s);
       const Act* sr = tile_raw(s);
-      const float* Bt;
-      const float* Ct;
-      int bst;
-      if (kBf16) {
-        Bt = bcf + (size_t)s * kTT * 2 * N2 + half * NG;
-        Ct = Bt + N2;
-        bst = 2 * N2;
-      } else {
-        Bt = reinterpret_cast<const float*>(tile_B(s)) + half * NG;
-        Ct = reinterpret_cast<const float*>(tile_C(s)) + half * NG;
-        bst = N2;
-      }
+      constexpr int kBst = kBf16 ? 2 * N2 : N2;
+      const float* Bt = (kBf16 ? bcf + (size_t)s * kTT * 2 * N2 : reinterpret_cast<const float*>(tile_B(s))) + half * NG;
+      const float* Ct = kBf16 ? Bt + N2 : reinterpret_cast<const float*>(tile_C(s)) + half * NG;
+      float2* dtile = dbuf + tb * kDTile;  // (delta, delta*u) rows of this tile
+
       if (passA) {
-        // ---------- pass A1: (delta, delta*u) of the owned steps into the chunk buffer
+        // ---------- pass A: (delta, delta*u) of the owned steps, then the recurrence
+        auto pass_a = [&](auto full_tag) {
+          constexpr bool kFull = decltype(full_tag)::value;
+          const int nv = kFull ? kTT : cnt;
 #pragma unroll
-        for (int i = 0; i < kTT / 2; ++i) {
-          const int km = 2 * i + half;
-          if (km < cnt) {
-            const float sv = lds_act(sr + km * kDTile + dl) + bias;
+          for (int i = 0; i < kTT / 2; ++i) {
+            const int km = 2 * i + half;
+            const int kr = kFull ? km : min(km, nv - 1);
+            const float sv = lds_act(sr + kr * kDTile + dl) + bias;
             const float sp = kFast ? softplus_fast(sv) : softplus_f(sv);
-            dbuf[(tb + km) * kDTile + dl] = make_float2(sp, sp * lds_act(su + km * kDTile + dl));
+            if (kFull || km < nv) dtile[km * kDTile + dl] = make_float2(sp, sp * lds_act(su + kr * kDTile + dl));
           }
-        }
-        __syncwarp();
-        // ---------- pass A2: recompute h over the tile, checkpoint every kSub steps
-#pragma unroll 4
-        for (int kk = 0; kk < cnt; ++kk) {
-          if (((tb + kk) % kSub) == 0) {
-            float2* ck = reinterpret_cast<float2*>(ckpt + (((tb + kk) / kSub) * kScanThreads + tid) * NG);
+          __syncwarp();
+          auto stepA = [&](int kk) {
+            if ((kk % kSub) == 0) {
+              float2* ck = reinterpret_cast<float2*>(ckpt + (((tb + kk) / kSub) * kScanThreads + tid) * NG);
 #pragma unroll
-            for (int i = 0; i < NH; ++i) ck[i] = h[i];
-          }
-          const float2 dv = dbuf[(tb + kk) * kDTile + dl];
-          const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
-          const float* Brow = Bt + kk * bst;
+              for (int i = 0; i < NH; ++i) ck[i] = h[i];
+            }
+            const float2 dv = dtile[kk * kDTile + dl];
+            const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
+            float2 Bv[NH];
+            load_row(Bt + kk * kBst, Bv);
 #pragma unroll
-          for (int i = 0; i < NH; ++i) {
-            const float2 Bv = *reinterpret_cast<const float2*>(Brow + 2 * i);
-            h[i] = ffma2(decay2<kFast>(dd, A2[i]), h[i], fmul2(uu2, Bv));
+            for (int i = 0; i < NH; ++i) h[i] = ffma2(decay2<kFast>(dd, A2[i]), h[i], fmul2(uu2, Bv[i]));
+          };
+          if (kFull) {
+#pragma unroll
+            for (int kk = 0; kk < kTT; ++kk) stepA(kk);
+          } else {
+            for (int kk = 0; kk < nv; ++kk) stepA(kk);
           }
-        }
+        };
+        if (cnt == kTT)
+          pass_a(std::true_type{});
+        else
+          pass_a(std::false_type{});
       } else {
         // ---------- pass B: 8-step sub-chunks of this tile, last first
         const Act* sz = tile_z(s);
@@ -354,127 +370,149 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
           const int cnt8 = min(kSub, cnt - ks);
           const int cstep = tb + ks;  // ... within the chunk
           const float2* ckp = reinterpret_cast<const float2*>(ckpt + ((cstep / kSub) * kScanThreads + tid) * NG);
-          // B1: recompute the sub-chunk's states into registers
-          float2 hs[kSub][NH];
+          const float2* dsub = dbuf + cstep * kDTile;
+          float* wp_sub = wpart + sub_parity * (kSub * 4 * 32);
+          auto sub = [&](auto full_tag) {
+            constexpr bool kFull = decltype(full_tag)::value;
+            const int nv = kFull ? kSub : cnt8;
+            // B1: recompute the sub-chunk's states into registers
+            float2 hs[kSub][NH];
 #pragma unroll
-          for (int k = 0; k < kSub; ++k) {
-            if (k < cnt8) {
-              const float2 dv = dbuf[(cstep + k) * kDTile + dl];
-              const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
-              const float* Brow = Bt + (ks + k) * bst;
+            for (int k = 0; k < kSub; ++k) {
+              if (kFull || k < nv) {
+                const float2 dv = dsub[k * kDTile + dl];
+                const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
+                float2 Bv[NH];
+                load_row(Bt + (ks + k) * kBst, Bv);
 #pragma unroll
-              for (int i = 0; i < NH; ++i) {
-                const float2 Bv = *reinterpret_cast<const float2*>(Brow + 2 * i);
-                const float2 hp = k == 0 ? ckp[i] : hs[k > 0 ? k - 1 : 0][i];
-                hs[k][i] = ffma2(decay2<kFast>(dd, A2[i]), hp, fmul2(uu2, Bv));
+                for (int i = 0; i < NH; ++i) {
+                  const float2 hp = k == 0 ? ckp[i] : hs[k > 0 ? k - 1 : 0][i];
+                  hs[k][i] = ffma2(decay2<kFast>(dd, A2[i]), hp, fmul2(uu2, Bv[i]));
+                }
               }
             }
-          }
-          // B2: gate terms of the owned steps: dy = dout*silu(z), dz factor
+            // B2: gate terms of the owned steps: dy = dout*silu(z), dz factor
 #pragma unroll
-          for (int i = 0; i < kSub / 2; ++i) {
-            const int km = 2 * i + half;
-            float2 v = make_float2(0.f, 0.f);
-            if (km < cnt8) {
-              const float gout = lds_act(sg + (ks + km) * kDTile + dl);
-              v.x = gout;
+            for (int i = 0; i < kSub / 2; ++i) {
+              const int km = 2 * i + half;
+              const int kr = ks + (kFull ? km : min(km, nv - 1));
+              const float gout = lds_act(sg + kr * kDTile + dl);
+              float2 v = make_float2(gout, 0.f);
               if (kGate) {
-                const float zz = lds_act(sz + (ks + km) * kDTile + dl);
+                const float zz = lds_act(sz + kr * kDTile + dl);
                 const float sgz = kFast ? sigmoid_fast(zz) : sigmoid_f(zz);
                 v.x = gout * zz * sgz;
                 v.y = gout * sgz * fmaf(zz, 1.f - sgz, 1.f);
               }
+              if (!kFull && km >= nv) v = make_float2(0.f, 0.f);
+              bprep[km * kDTile + dl] = v;
             }
-            bprep[km * kDTile + dl] = v;
-          }
-          __syncwarp();
-          // B3: reverse steps; the adjoint carry is the only loop-carried value
-          float* wp_sub = wpart + sub_parity * (kSub * 4 * 32);
+            __syncwarp();
+            // B3: reverse steps in two groups of four; the adjoint carry is the
+            // only loop-carried value.  Each step's dBm/dCm terms go to one of
+            // four warp-local slots, reduced over the warp's 16 channels after
+            // each group (fixed order) into the per-warp partial wp_sub.
 #pragma unroll
-          for (int k = kSub - 1; k >= 0; --k) {
-            if (k < cnt8) {
-              const float2 dv = dbuf[(cstep + k) * kDTile + dl];
-              const float dy = bprep[k * kDTile + dl].x;
-              const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
-              const float2 dy2 = make_float2(dy, dy);
-              const float* Brow = Bt + (ks + k) * bst;
-              const float* Crow = Ct + (ks + k) * bst;
-              float2 ya = make_float2(0.f, 0.f), gba = make_float2(0.f, 0.f), apa = make_float2(0.f, 0.f);
-              float* rb = my_redw + (k & 1) * kRedWarpBuf;
+            for (int gi = kSub / 4 - 1; gi >= 0; --gi) {
 #pragma unroll
-              for (int i = 0; i < NH; i += 2) {
-                float2 tB[2], tC[2];
+              for (int k = 4 * gi + 3; k >= 4 * gi; --k) {
+                if (kFull || k < nv) {
+                  const float2 dv = dsub[k * kDTile + dl];
+                  const float dy = bprep[k * kDTile + dl].x;
+                  const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
+                  const float2 dy2 = make_float2(dy, dy);
+                  float2 Bv[NH], Cv[NH];
+                  load_row(Bt + (ks + k) * kBst, Bv);
+                  load_row(Ct + (ks + k) * kBst, Cv);
+                  float2 ya = make_float2(0.f, 0.f), gba = make_float2(0.f, 0.f), apa = make_float2(0.f, 0.f);
+                  float2 tB[NH], tC[NH];
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                  const int ii = i + u;
-                  if (ii < NH) {
-                    const float2 Bv = *reinterpret_cast<const float2*>(Brow + 2 * ii);
-                    const float2 Cv = *reinterpret_cast<const float2*>(Crow + 2 * ii);
-                    const float2 a = decay2<kFast>(dd, A2[ii]);
-                    const float2 hk = hs[k][ii];
-                    const float2 hp = k == 0 ? ckp[ii] : hs[k > 0 ? k - 1 : 0][ii];
-                    const float2 g = ffma2(dy2, Cv, carry[ii]);
+                  for (int i = 0; i < NH; ++i) {
+                    const float2 a = decay2<kFast>(dd, A2[i]);
+                    const float2 hk = hs[k][i];
+                    const float2 hp = k == 0 ? ckp[i] : hs[k > 0 ? k - 1 : 0][i];
+                    const float2 g = ffma2(dy2, Cv[i], carry[i]);
                     const float2 pv = fmul2(g, fmul2(a, hp));
-                    apa = ffma2(A2[ii], pv, apa);
-                    accA[ii] = ffma2(dd, pv, accA[ii]);
-                    gba = ffma2(g, Bv, gba);
-                    ya = ffma2(Cv, hk, ya);
-                    tB[u] = dvalid ? fmul2(g, uu2) : make_float2(0.f, 0.f);
-                    tC[u] = dvalid ? fmul2(dy2, hk) : make_float2(0.f, 0.f);
-                    carry[ii] = fmul2(a, g);
+                    apa = ffma2(A2[i], pv, apa);
+                    accA[i] = ffma2(dd, pv, accA[i]);
+                    gba = ffma2(g, Bv[i], gba);
+                    ya = ffma2(Cv[i], hk, ya);
+                    tB[i] = fmul2(g, uu2);
+                    tC[i] = fmul2(dy2, hk);
+                    carry[i] = fmul2(a, g);
                   }
-                }
-                if (NH >= 2) {
-                  *reinterpret_cast<float4*>(rb + red_at(0, lane, 2 * i)) =
-                      make_float4(tB[0].x, tB[0].y, tB[1].x, tB[1].y);
-                  *reinterpret_cast<float4*>(rb + red_at(1, lane, 2 * i)) =
-                      make_float4(tC[0].x, tC[0].y, tC[1].x, tC[1].y);
-                } else {
-                  *reinterpret_cast<float2*>(rb + red_at(0, lane, 2 * i)) = tB[0];
-                  *reinterpret_cast<float2*>(rb + red_at(1, lane, 2 * i)) = tC[0];
+                  float* rb = my_redw + (k & 3) * kRedWarpBuf;
+                  if constexpr (NH >= 2) {
+#pragma unroll
+                    for (int i = 0; i < NH; i += 2) {
+                      *reinterpret_cast<float4*>(rb + red_at(0, lane, 2 * i)) =
+                          dvalid ? make_float4(tB[i].x, tB[i].y, tB[i + 1].x, tB[i + 1].y) : make_float4(0.f, 0.f, 0.f, 0.f);
+                      *reinterpret_cast<float4*>(rb + red_at(1, lane, 2 * i)) =
+                          dvalid ? make_float4(tC[i].x, tC[i].y, tC[i + 1].x, tC[i + 1].y) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                  } else {
+                    *reinterpret_cast<float2*>(rb + red_at(0, lane, 0)) = dvalid ? tB[0] : make_float2(0.f, 0.f);
+                    *reinterpret_cast<float2*>(rb + red_at(1, lane, 0)) = dvalid ? tC[0] : make_float2(0.f, 0.f);
+                  }
+                  part[k * kScanThreads + tid] =
+                      make_float4(ya.x + ya.y, gba.x + gba.y, (apa.x + apa.y) * kAscale, 0.f);
                 }
               }
-              part[k * kScanThreads + tid] = make_float4(ya.x + ya.y, gba.x + gba.y, (apa.x + apa.y) * kAscale, 0.f);
-              // warp-local channel sum of this step's dBm/dCm terms (fixed order)
               __syncwarp();
-              float2 v = make_float2(0.f, 0.f);
-              if (r_n < N2) {
-                const int rhalf = r_n / NG;
+              // channel sums of the group's four steps: 8 channels per lane, then the other half
 #pragma unroll
-                for (int k2 = 0; k2 < 8; ++k2) {
-                  const int L2 = 2 * (r_chh * 8 + k2) + rhalf;
-                  const float2 x = *reinterpret_cast<const float2*>(rb + red_at(r_q, L2, r_n % NG));
-                  v = make_float2(v.x + x.x, v.y + x.y);
+              for (int k = 4 * gi + 3; k >= 4 * gi; --k) {
+                if (kFull || k < nv) {
+                  const float* rb = my_redw + (k & 3) * kRedWarpBuf;
+                  float2 v = make_float2(0.f, 0.f);
+#pragma unroll
+                  for (int k2 = 0; k2 < 8; ++k2) {
+                    const int L2 = 2 * (r_chh * 8 + k2) + r_half;
+                    v = fadd2(v, *reinterpret_cast<const float2*>(rb + red_at(r_q, L2, r_nl)));
+                  }
+                  const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, v.x, 16), __shfl_xor_sync(0xffffffffu, v.y, 16));
+                  // both lanes of the pair hold the identical sum; both store it
+                  *reinterpret_cast<float2*>(wp_sub + (k * 4 + wl) * 32 + r_q * 16 + r_n) = fadd2(v, o);
                 }
               }
-              const float ox = __shfl_xor_sync(0xffffffffu, v.x, 16);
-              const float oy = __shfl_xor_sync(0xffffffffu, v.y, 16);
-              if (r_chh == 0)
-                *reinterpret_cast<float2*>(wp_sub + (k * 4 + wl) * 32 + r_q * 16 + r_n) = make_float2(v.x + ox, v.y + oy);
+              __syncwarp();
             }
-          }
-          __syncwarp();
-          // B4: owned steps: combine the pair's partial sums, write du, d_delta_raw, dz
+            // B4: owned steps: combine the pair's partial sums, write du, d_delta_raw, dz
+            float o_du[kSub / 2], o_dr[kSub / 2], o_dz[kSub / 2];
 #pragma unroll
-          for (int i = 0; i < kSub / 2; ++i) {
-            const int km = 2 * i + half;
-            if (km < cnt8 && dvalid) {
-              const float4 mine = part[km * kScanThreads + tid];
-              const float4 other = part[km * kScanThreads + (tid ^ 1)];
-              const float2 dv = dbuf[(cstep + km) * kDTile + dl];
-              const float2 bp = bprep[km * kDTile + dl];
-              const float uo = lds_act(su + (ks + km) * kDTile + dl);
+            for (int i = 0; i < kSub / 2; ++i) {
+              const int km = 2 * i + half;
+              const int kr = kFull ? km : min(km, nv - 1);
+              const float4 mine = part[kr * kScanThreads + tid];
+              const float4 other = part[kr * kScanThreads + (tid ^ 1)];
+              const float2 dv = dsub[kr * kDTile + dl];
+              const float2 bp = bprep[kr * kDTile + dl];
+              const float uo = lds_act(su + (ks + kr) * kDTile + dl);
               const float ysum = mine.x + other.x, gb = mine.y + other.y, ap = mine.z + other.z;
               const float dsp = kFast ? dsoftplus_fast(dv.x) : -expm1f(-dv.x);
               const float draw = fmaf(uo, gb, ap) * dsp;
-              const size_t o = (size_t)(t0 + cstep + km) * D;
-              st_act(dup + o, fmaf(Dd, bp.x, dv.x * gb));
-              st_act(drp + o, draw);
-              if (kGate) st_act(dzp + o, fmaf(Dd, uo, ysum) * bp.y);
-              accD = fmaf(bp.x, uo, accD);
-              accBias += draw;
+              o_du[i] = fmaf(Dd, bp.x, dv.x * gb);
+              o_dr[i] = draw;
+              o_dz[i] = fmaf(Dd, uo, ysum) * bp.y;
+              const bool ok = kFull || km < nv;
+              accD += ok ? bp.x * uo : 0.f;
+              accBias += ok ? draw : 0.f;
             }
-          }
+#pragma unroll
+            for (int i = 0; i < kSub / 2; ++i) {
+              const int km = 2 * i + half;
+              if (dvalid && (kFull || km < nv)) {
+                const size_t o = (size_t)(t0 + cstep + km) * D;
+                st_act(dup + o, o_du[i]);
+                st_act(drp + o, o_dr[i]);
+                if (kGate) st_act(dzp + o, o_dz[i]);
+              }
+            }
+          };
+          if (cnt8 == kSub)
+            sub(std::true_type{});
+          else
+            sub(std::false_type{});
           // B5: cross-warp sum of the sub-chunk's dBm/dCm partials (fixed warp order)
           named_bar_sync(1, kScanThreads);
 #pragma unroll
@@ -485,7 +523,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
             if (k < cnt8 && n < N2) {
               const float* src = wp_sub + k * 4 * 32 + o;
               const float v = ((src[0] + src[32]) + src[64]) + src[96];
-              p.ws_dbc[((((size_t)blockIdx.x * p.B + b) * L + (t0 + cstep + k)) * 2 + q) * N2 + n] = v;
+              ws_dbc_b[((size_t)(t0 + cstep + k) * 2 + q) * N2 + n] = v;
             }
           }
           sub_parity ^= 1;
@@ -494,6 +532,10 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
+      if (++s == S) {
+        s = 0;
+        par ^= 1;
+      }
     }
     // chunk sums -> compensated running totals (per-lane private smem)
 #pragma unroll
@@ -562,7 +604,7 @@ size_t bwd_smem_bytes(int NG) {
   bytes += (bf ? (size_t)S * kTT * 2 * 2 * NG : 0) * 4;          // bcf
   bytes += (size_t)kChunk * kDTile * 8;                            // dbuf (float2)
   bytes += (size_t)(kChunk / kSub) * kScanThreads * NG * 4;       // ckpt
-  bytes += (size_t)4 * 2 * kRedWarpBuf * 4;                        // redw
+  bytes += (size_t)4 * 4 * kRedWarpBuf * 4;                        // redw (4 step slots per warp)
   bytes += (size_t)2 * kSub * 4 * 32 * 4;                          // wpart
   bytes += (size_t)kSub * kScanThreads * 16;                       // part (float4)
   bytes += (size_t)kSub * kDTile * 8;                              // bprep

@@ -26,6 +26,7 @@
 // All pipeline waits are bounded (s6_tma.cuh); nothing else spins.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <type_traits>
@@ -94,8 +95,11 @@ __device__ __forceinline__ float2 decay2(float2 dd, float2 A) {
 }
 
 // TPC lanes per channel, 4 states per lane (N = 4 * TPC); 128 consumer lanes
-// cover kCh = 128 / TPC channels.
-template <typename Act, int TPC, bool kSave, bool kFast, bool kGate>
+// cover kCh = 128 / TPC channels.  grid.z = time segment.  kAgg: the
+// aggregate pass of the chunked parallel scan -- from a zero state, run the
+// segment and store its end state and its decay product exp(A * sum(delta))
+// (no readout, no output; z and Cm are not loaded).
+template <typename Act, int TPC, bool kSave, bool kFast, bool kGate, bool kAgg = false>
 __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid_constant__ FwdTmaParams P) {
   constexpr int N = 4 * TPC;
   constexpr int kCh = kScanThreads / TPC;  // channels per CTA
@@ -118,9 +122,11 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
 
   const FwdParams& p = P.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.y, d0 = blockIdx.x * kCh;
+  const int b = blockIdx.y, d0 = blockIdx.x * kCh, seg = blockIdx.z;
   const int L = p.L, D = p.D;
-  const int ntiles = (L + kTT - 1) / kTT;
+  const int t_begin = seg * p.seg_len;                  // first step of this segment
+  const int t_end = min(L, t_begin + p.seg_len);
+  const int ntiles = (t_end - t_begin + kTT - 1) / kTT;
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -146,19 +152,20 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
       if (kGate) tma_prefetch_desc(&P.map_z);
       tma_prefetch_desc(&P.map_B);
       tma_prefetch_desc(&P.map_C);
-      const uint32_t bytes = (uint32_t)(((kGate ? 3 : 2) * kTile + 2 * kBC) * sizeof(Act));
+      constexpr bool kZ = kGate && !kAgg;
+      const uint32_t bytes = (uint32_t)(((kZ ? 3 : 2) * kTile + (kAgg ? 1 : 2) * kBC) * sizeof(Act));
       int issued = 0;
       for (int k = 0; k < ntiles; ++k) {
         const int s = k % S;
         const uint32_t use = (uint32_t)(k / S);
         if (k >= S && !mbar_wait(&empty[s], (use - 1) & 1, p.status)) break;
         mbar_arrive_expect_tx(&full[s], bytes);
-        const int row = b * L + k * kTT;
+        const int row = b * L + t_begin + k * kTT;
         tma_load_2d(tile_u(s), &P.map_u, &full[s], d0, row);
         tma_load_2d(tile_raw(s), &P.map_raw, &full[s], d0, row);
-        if (kGate) tma_load_2d(tile_z(s), &P.map_z, &full[s], d0, row);
+        if (kZ) tma_load_2d(tile_z(s), &P.map_z, &full[s], d0, row);
         tma_load_2d(tile_B(s), &P.map_B, &full[s], 0, row);
-        tma_load_2d(tile_C(s), &P.map_C, &full[s], 0, row);
+        if (!kAgg) tma_load_2d(tile_C(s), &P.map_C, &full[s], 0, row);
         issued = k + 1;
       }
       // never leave with copies in flight: wait for the last use of every stage
@@ -182,7 +189,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
         for (int e = lane; e < kBC / 2; e += 32) {
           const int t = (2 * e) / N, n = (2 * e) % N;
           *reinterpret_cast<float2*>(dst + (t * 2 + 0) * N + n) = __bfloat1622float2(tb[e]);
-          *reinterpret_cast<float2*>(dst + (t * 2 + 1) * N + n) = __bfloat1622float2(tc[e]);
+          if (!kAgg) *reinterpret_cast<float2*>(dst + (t * 2 + 1) * N + n) = __bfloat1622float2(tc[e]);
         }
         mbar_arrive(&conv[s]);
       }
@@ -204,21 +211,24 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
     const float a0 = -expf(p.A_log[dc * N + n]);
     const float a1 = -expf(p.A_log[dc * N + n + 1]);
     A2[i] = kFast ? make_float2(a0 * kLog2e, a1 * kLog2e) : make_float2(a0, a1);
-    h[i] = p.h0 ? make_float2(p.h0[((size_t)b * D + dc) * N + n], p.h0[((size_t)b * D + dc) * N + n + 1])
-                : make_float2(0.f, 0.f);
+    // initial state: zero (aggregate pass), the composed segment start, or h0
+    const float* hin = kAgg ? nullptr
+                            : (p.nseg > 1 ? p.seg_start + (((size_t)b * p.nseg + seg) * D + dc) * N : (p.h0 ? p.h0 + ((size_t)b * D + dc) * N : nullptr));
+    h[i] = hin ? make_float2(hin[n], hin[n + 1]) : make_float2(0.f, 0.f);
   }
   const float bias = p.delta_bias[dc];
   const float Dd = p.Dp[dc];
   Act* outp = static_cast<Act*>(p.out) + (size_t)b * L * D + d;
+  float dsum = 0.f;  // aggregate pass: sum of delta over the segment (per-tile partials added)
 
   for (int k = 0; k < ntiles; ++k) {
     const int s = k % S;
     const uint32_t par = (uint32_t)(k / S) & 1;
     if (!mbar_wait(&full[s], par, p.status)) break;
     if (kBf16 && !mbar_wait(&conv[s], par, p.status)) break;
-    const int tbase = k * kTT;
-    const int cnt = min(kTT, L - tbase);
-    if (kSave && (tbase % kChunk) == 0 && dvalid) {
+    const int tbase = t_begin + k * kTT;
+    const int cnt = min(kTT, t_end - tbase);
+    if (kSave && !kAgg && (tbase % kChunk) == 0 && dvalid) {
       float* cs = p.chunk_states + (((size_t)b * p.nchunks + tbase / kChunk) * D + d) * N + 4 * q;
       *reinterpret_cast<float4*>(cs) = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
     }
@@ -229,18 +239,23 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
     const float* Ct = (kBf16 ? Bt + N : reinterpret_cast<const float*>(tile_C(s)) + 4 * q);
 
     // one recurrence step for this lane's 4 states; the partial readout goes to ypart
+    float tsum = 0.f;
     auto step = [&](int kk) {
       const float2 dv = prep[kk * kCh + cl];
       const float2 dd = make_float2(dv.x, dv.x);
       const float2 uu = make_float2(dv.y, dv.y);
       const float4 Bv = *reinterpret_cast<const float4*>(Bt + kk * kBst);
-      const float4 Cv = *reinterpret_cast<const float4*>(Ct + kk * kBst);
       const float2 a0 = decay2<kFast>(dd, A2[0]);
       const float2 a1 = decay2<kFast>(dd, A2[1]);
       h[0] = ffma2(a0, h[0], fmul2(uu, make_float2(Bv.x, Bv.y)));
       h[1] = ffma2(a1, h[1], fmul2(uu, make_float2(Bv.z, Bv.w)));
-      const float2 y2 = ffma2(make_float2(Cv.z, Cv.w), h[1], fmul2(make_float2(Cv.x, Cv.y), h[0]));
-      ypart[kk * kScanThreads + tid] = y2.x + y2.y;
+      if (kAgg) {
+        tsum += dv.x;
+      } else {
+        const float4 Cv = *reinterpret_cast<const float4*>(Ct + kk * kBst);
+        const float2 y2 = ffma2(make_float2(Cv.z, Cv.w), h[1], fmul2(make_float2(Cv.x, Cv.y), h[0]));
+        ypart[kk * kScanThreads + tid] = y2.x + y2.y;
+      }
     };
     // One tile in three phases.  kFull (all kTT steps valid, the common case)
     // has no data-dependent branches, so the independent iterations of each
@@ -269,6 +284,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
       } else {
         for (int kk = 0; kk < n_valid; ++kk) step(kk);
       }
+      if (kAgg) return;
       __syncwarp();
       // phase 3: complete the readout of the owned steps (fixed order over the
       // channel's TPC lanes), add Dp*u, gate with silu(z), store
@@ -295,12 +311,41 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
       run_tile(std::true_type{});
     else
       run_tile(std::false_type{});
+    dsum += tsum;
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
-  if (p.h_last && dvalid) {
+  if (kAgg) {
+    if (dvalid) {
+      // decay product over the segment, exp(A * sum(delta)), and the end state from zero
+      float* ag = p.seg_agg + ((((size_t)b * p.nseg + seg) * D + d) * N + 4 * q) * 2;
+      const float2 x0 = fmul2(make_float2(dsum, dsum), A2[0]);
+      const float2 x1 = fmul2(make_float2(dsum, dsum), A2[1]);
+      const float P0 = kFast ? ex2_approx(x0.x) : expf(x0.x), P1 = kFast ? ex2_approx(x0.y) : expf(x0.y);
+      const float P2 = kFast ? ex2_approx(x1.x) : expf(x1.x), P3 = kFast ? ex2_approx(x1.y) : expf(x1.y);
+      reinterpret_cast<float4*>(ag)[0] = make_float4(P0, h[0].x, P1, h[0].y);
+      reinterpret_cast<float4*>(ag)[1] = make_float4(P2, h[1].x, P3, h[1].y);
+    }
+  } else if (p.h_last && dvalid && seg == (int)gridDim.z - 1) {
     float* hl = p.h_last + ((size_t)b * D + d) * N + 4 * q;
     *reinterpret_cast<float4*>(hl) = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+  }
+}
+
+// Carry pass of the chunked parallel scan: per (b, d, n), in segment order,
+// seg_start[s] = state before segment s, seg_start[s+1] = P_s * seg_start[s] + hloc_s.
+__global__ void s6_fwd_seg_carry_kernel(const FwdParams p) {
+  const size_t per = (size_t)p.D * p.N;
+  const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int b = blockIdx.y;
+  if (e >= per) return;
+  float h = p.h0 ? p.h0[(size_t)b * per + e] : 0.f;
+  for (int sg = 0; sg < p.nseg; ++sg) {
+    p.seg_start[((size_t)b * p.nseg + sg) * per + e] = h;
+    if (sg + 1 < p.nseg) {
+      const float* ag = p.seg_agg + (((size_t)b * p.nseg + sg) * per + e) * 2;
+      h = fmaf(ag[0], h, ag[1]);
+    }
   }
 }
 
@@ -345,16 +390,30 @@ constexpr size_t fwd_smem_bytes() {
          (size_t)kTT * kCh * 8 + (size_t)kTT * kScanThreads * 4 + 3 * S * 8;
 }
 
-template <typename Act, int TPC, bool kSave, bool kFast, bool kGate>
-cudaError_t launch_one(const FwdTmaParams& P, cudaStream_t stream) {
-  auto kern = s6_fwd_tma_kernel<Act, TPC, kSave, kFast, kGate>;
+template <typename Act, int TPC, bool kSave, bool kFast, bool kGate, bool kAgg>
+cudaError_t launch_kernel(const FwdTmaParams& P, int nz, cudaStream_t stream) {
+  auto kern = s6_fwd_tma_kernel<Act, TPC, kSave, kFast, kGate, kAgg>;
   constexpr size_t smem = fwd_smem_bytes<Act, TPC>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   constexpr int kCh = kScanThreads / TPC;
-  const dim3 grid((P.p.D + kCh - 1) / kCh, P.p.B);
+  const dim3 grid((P.p.D + kCh - 1) / kCh, P.p.B, nz);
   kern<<<grid, kFwdWarps * 32, smem, stream>>>(P);
   return cudaGetLastError();
+}
+
+template <typename Act, int TPC, bool kSave, bool kFast, bool kGate>
+cudaError_t launch_one(const FwdTmaParams& P, cudaStream_t stream) {
+  if (P.p.nseg > 1) {
+    // chunked parallel scan: segment aggregates -> carries -> all segments at once
+    cudaError_t e = launch_kernel<Act, TPC, false, kFast, kGate, true>(P, P.p.nseg - 1, stream);
+    if (e != cudaSuccess) return e;
+    const dim3 cgrid((unsigned)(((size_t)P.p.D * P.p.N + 255) / 256), P.p.B);
+    s6_fwd_seg_carry_kernel<<<cgrid, 256, 0, stream>>>(P.p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return launch_kernel<Act, TPC, kSave, kFast, kGate, false>(P, P.p.nseg, stream);
 }
 
 template <typename Act, int TPC, bool kFast>
@@ -368,6 +427,22 @@ cudaError_t launch_tpc(const FwdTmaParams& P, cudaStream_t stream) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
+
+// Segments are used when the (batch x channel-tile) grid alone would leave
+// most SMs idle: enough segments for about three CTAs per SM, each at least
+// 512 steps long (a multiple of the chunk length).
+int fwd_segments(int B, int L, int D, int N, int sms) {
+  if (!(N == 4 || N == 8 || N == 16) || L < 1024 || B <= 0 || D <= 0) return 1;
+  const int kch = kScanThreads / (N / 4);
+  const long ctas = (long)B * ((D + kch - 1) / kch);
+  const long want = 3L * sms;
+  if (ctas * 2 >= want) return 1;
+  long nseg = (want + ctas - 1) / ctas;
+  nseg = std::min<long>(nseg, L / 512);
+  if (nseg < 2) return 1;
+  const int seg_len = (int)((((long)L + nseg - 1) / nseg + kChunk - 1) / kChunk * kChunk);
+  return (L + seg_len - 1) / seg_len;
+}
 
 // The TMA path covers N in {4, 8, 16} with N*e and D*e multiples of 16 bytes
 // and 16-byte aligned activation pointers; everything else takes the generic

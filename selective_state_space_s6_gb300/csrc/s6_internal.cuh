@@ -33,6 +33,14 @@ struct FwdParams {
   float* h_last;        // nullable (may alias h0 for the decode step)
   float* chunk_states;  // nullable (nosave)
   unsigned int* status;  // device status word (bounded waits report here)
+  // Time segments (long sequences): the steps are split into nseg segments
+  // of seg_len steps (a multiple of kChunk), run in parallel.  seg_agg
+  // ([B][nseg][D][N][2] f32: decay product and zero-start end state of each
+  // segment) is written by the aggregate pass, seg_start ([B][nseg][D][N]
+  // f32: state before each segment's first step) by the carry kernel.
+  int seg_len, nseg;
+  float* seg_agg;
+  float* seg_start;
   int B, L, D, N, nchunks;
 };
 
@@ -64,6 +72,8 @@ struct BwdParams {
 cudaError_t launch_fwd(const FwdParams& p, int act, cudaStream_t stream);
 bool fwd_tma_supported(const FwdParams& p, int act);
 cudaError_t launch_fwd_tma(const FwdParams& p, int act, cudaStream_t stream);
+// Segment count the TMA forward uses for this shape on a GPU with `sms` SMs (1 = none).
+int fwd_segments(int B, int L, int D, int N, int sms);
 // Device address of the library's status word on the current device (nullptr on error).
 unsigned int* device_status_word();
 // Sets the calling thread's ssm_last_error() message; returns `code`.

@@ -44,6 +44,11 @@ SMALL = [
     (1, 1, 64, 16, "bf16"),     # one step
     (2, 31, 24, 4, "f32"),
     (2, 160, 64, 8, "f32"),
+    # long and narrow: the forward splits time into segments (chunked parallel scan)
+    (1, 1100, 64, 16, "f32"),   # 2 segments, ragged last one
+    (1, 4096, 32, 16, "bf16"),  # 8 segments of 512 steps
+    (2, 3000, 100, 4, "f32"),   # 128 channels per tile, 5 segments
+    (1, 2500, 72, 8, "bf16"),
 ]
 
 
