@@ -121,17 +121,27 @@ FwdWorkspace fwd_ws_layout(int64_t B, int64_t L, int64_t D, int64_t N) {
 }
 
 struct BwdWorkspace {
-  int64_t dbc_off, dbc_bytes, param_off, param_bytes, total;
+  int nseg, seg_len;
+  int64_t dbc_off, dbc_bytes, param_off, param_bytes, agg_off, carry_off, total;
 };
 
 BwdWorkspace bwd_ws_layout(int64_t B, int64_t L, int64_t D, int64_t N) {
   BwdWorkspace w;
+  w.nseg = s6::bwd_segments((int)B, (int)L, (int)D, (int)N, kPlanSms);
+  w.seg_len = (int)(L > 0 ? ssm_num_chunks(L) * SSM_CHUNK_LEN : 0);
+  if (w.nseg > 1) {
+    w.seg_len = (int)(((L + w.nseg - 1) / w.nseg + SSM_CHUNK_LEN - 1) / SSM_CHUNK_LEN * SSM_CHUNK_LEN);
+    w.nseg = (int)((L + w.seg_len - 1) / w.seg_len);
+  }
   const int64_t ndt = (D + s6::kDTile - 1) / s6::kDTile;
   w.dbc_off = 0;
   w.dbc_bytes = ndt * B * L * 2 * N * (int64_t)sizeof(float);
   w.param_off = align_up(w.dbc_bytes, 256);
-  w.param_bytes = B * D * (N + 2) * (int64_t)sizeof(float);
-  w.total = align_up(w.param_off + w.param_bytes, 256);
+  w.param_bytes = B * w.nseg * D * (N + 2) * (int64_t)sizeof(float);
+  w.agg_off = align_up(w.param_off + w.param_bytes, 256);
+  const int64_t cells = w.nseg > 1 ? B * w.nseg * D * N : 0;
+  w.carry_off = align_up(w.agg_off + cells * 2 * (int64_t)sizeof(float), 256);
+  w.total = align_up(w.carry_off + cells * (int64_t)sizeof(float), 256);
   return w;
 }
 
@@ -313,9 +323,23 @@ int ssm_scan_bwd_partials(int64_t batch, int64_t seqlen, int64_t dim, int64_t ds
   p.nchunks = (int)ssm_num_chunks(L);
   p.status = s6::device_status_word();
   if (!p.status) return fail(SSM_ERR_CUDA, "cannot locate the device status word");
-  const cudaError_t ce = (L > 0 && s6::bwd_tma_supported(p, act))
-                             ? s6::launch_bwd_tma(p, act, static_cast<cudaStream_t>(stream))
-                             : s6::launch_bwd(p, act, static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  p.nseg = w.nseg;
+  p.seg_len = w.seg_len;
+  p.seg_agg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.agg_off);
+  p.seg_carry = reinterpret_cast<float*>(static_cast<char*>(ws) + w.carry_off);
+  cudaError_t ce;
+  if (L > 0 && s6::bwd_tma_supported(p, act)) {
+    ce = s6::launch_bwd_tma(p, act, st);
+  } else {
+    // the generic kernel does not split time: it fills segment row 0 of the
+    // parameter partials; the other rows of the plan's layout are zeroed
+    if (w.nseg > 1) {
+      ce = cudaMemsetAsync(p.ws_param, 0, (size_t)w.param_bytes, st);
+      if (ce != cudaSuccess) return cuda_fail(ce, "ssm_scan_bwd_partials");
+    }
+    ce = s6::launch_bwd(p, act, st);
+  }
   if (ce != cudaSuccess) return cuda_fail(ce, "ssm_scan_bwd_partials launch");
   return SSM_OK;
 }
@@ -344,7 +368,7 @@ int ssm_scan_bwd_finalize(int64_t batch, int64_t seqlen, int64_t dim, int64_t ds
     ce = s6::launch_reduce_dbc(ws_dbc, ndt, (int)B, (int)L, (int)N, dBm, dCm, act, st);
     if (ce != cudaSuccess) return cuda_fail(ce, "ssm_scan_bwd_finalize dBm/dCm reduction");
   }
-  ce = s6::launch_reduce_params(ws_param, (int)B, (int)D, (int)N, dA_log, dDp, d_delta_bias, st);
+  ce = s6::launch_reduce_params(ws_param, (int)(B * w.nseg), (int)D, (int)N, dA_log, dDp, d_delta_bias, st);
   if (ce != cudaSuccess) return cuda_fail(ce, "ssm_scan_bwd_finalize parameter reduction");
   return SSM_OK;
 }

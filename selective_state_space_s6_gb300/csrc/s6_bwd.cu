@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kScanThreads)
   }
   // ---- per-batch parameter-gradient partials and dh0
   if (dvalid) {
-    float* wp = p.ws_param + ((size_t)b * D + d) * (N + 2);
+    float* wp = p.ws_param + ((size_t)b * p.nseg * D + d) * (N + 2);  // segment row 0
 #pragma unroll
     for (int i = 0; i < NG; ++i) {
       const int n = half * NG + i;

@@ -30,6 +30,7 @@
 // (even steps: lane 0, odd steps: lane 1) and shared with a shuffle.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <type_traits>
@@ -140,6 +141,11 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
   const int b = blockIdx.y, d0 = blockIdx.x * kDTile;
   const int L = p.L, D = p.D;
   const int nchunks = p.nchunks;
+  // this CTA's time segment: chunks [c_lo, c_hi)
+  const int seg = blockIdx.z;
+  const int cps = p.seg_len / kChunk;
+  const int c_lo = seg * cps;
+  const int c_hi = min(nchunks, c_lo + cps);
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -175,7 +181,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
       const uint32_t bytesB = (uint32_t)(((kGate ? 4 : 3) * kTile + 2 * kBC) * sizeof(Act));
       int item = 0;
       bool ok = true;
-      for (int c = nchunks - 1; c >= 0 && ok; --c) {
+      for (int c = c_hi - 1; c >= c_lo && ok; --c) {
         const int ntl = chunk_tiles(c);
         for (int it = 0; it < 2 * ntl; ++it, ++item) {
           const bool passA = it < ntl;
@@ -211,7 +217,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
     if (kBf16) {
       int item = 0;
       bool ok = true;
-      for (int c = nchunks - 1; c >= 0; --c) {
+      for (int c = c_hi - 1; c >= c_lo; --c) {
         const int ntl = chunk_tiles(c);
         for (int it = 0; it < 2 * ntl; ++it, ++item) {
           const bool passA = it < ntl;
@@ -250,9 +256,11 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
     const float a0 = -expf(p.A_log[dc * N2 + n]);
     const float a1 = -expf(p.A_log[dc * N2 + n + 1]);
     A2[i] = kFast ? make_float2(a0 * kLog2e, a1 * kLog2e) : make_float2(a0, a1);
-    carry[i] = (p.dh_last && dvalid)
-                   ? make_float2(p.dh_last[((size_t)b * D + d) * N2 + n], p.dh_last[((size_t)b * D + d) * N2 + n + 1])
-                   : make_float2(0.f, 0.f);
+    // adjoint carry entering this segment's last step: dh_last for the last
+    // segment, the composed carry of the segments to the right otherwise
+    const float* cin = p.nseg > 1 ? p.seg_carry + (((size_t)b * p.nseg + seg) * D + dc) * N2
+                                  : (p.dh_last ? p.dh_last + ((size_t)b * D + dc) * N2 : nullptr);
+    carry[i] = (cin && dvalid) ? make_float2(cin[n], cin[n + 1]) : make_float2(0.f, 0.f);
   }
   const float bias = p.delta_bias[dc];
   const float Dd = p.Dp[dc];
@@ -294,7 +302,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
   int s = 0;          // ring stage of the current item
   uint32_t par = 0;   // its phase parity
   int sub_parity = 0;
-  for (int c = nchunks - 1; c >= 0; --c) {
+  for (int c = c_hi - 1; c >= c_lo; --c) {
     const int t0 = c * kChunk;
     const int clen = min(kChunk, L - t0);
     const int ntl = (clen + kTT - 1) / kTT;
@@ -551,13 +559,13 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
     const float tD = my_tot[NG] + __shfl_xor_sync(0xffffffffu, my_tot[NG], 1);
     const float tBs = my_tot[NG + 1] + __shfl_xor_sync(0xffffffffu, my_tot[NG + 1], 1);
     if (dvalid) {
-      float* wp = p.ws_param + ((size_t)b * D + d) * (N2 + 2);
+      float* wp = p.ws_param + (((size_t)b * p.nseg + seg) * D + d) * (N2 + 2);
 #pragma unroll
       for (int i = 0; i < NH; ++i) {
         const int n = half * NG + 2 * i;
         wp[n] = (A2[i].x * kAscale) * my_tot[2 * i];
         wp[n + 1] = (A2[i].y * kAscale) * my_tot[2 * i + 1];
-        if (p.dh0) *reinterpret_cast<float2*>(p.dh0 + ((size_t)b * D + d) * N2 + n) = carry[i];
+        if (p.dh0 && seg == 0) *reinterpret_cast<float2*>(p.dh0 + ((size_t)b * D + d) * N2 + n) = carry[i];
       }
       if (half == 0) {
         wp[N2] = tD;
@@ -565,6 +573,203 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
       }
     }
   }
+}
+
+// ---------------------------------------------------------------- segment aggregates
+// Aggregate pass of the backward's chunked parallel scan.  For segment s >= 1
+// (grid.z + 1), from a zero carry, run the adjoint recurrence
+//   g_t = dy_t * C_t + carry,  carry = Abar_t * g_t
+// from the segment's last step down to its first, and store per state the
+// segment's decay product exp(A * sum(delta)) and the final carry.  Same warp
+// roles and lane layout as the forward (TPC lanes per channel, 4 states each);
+// tiles are streamed last first.
+template <typename Act, int TPC, bool kFast, bool kGate>
+__global__ void __launch_bounds__(kBwdWarps * 32) s6_bwd_agg_kernel(const __grid_constant__ BwdTmaParams P) {
+  constexpr int N = 4 * TPC;
+  constexpr int kCh = kScanThreads / TPC;
+  constexpr int S = 3;
+  constexpr int kTile = kTT * kCh;
+  constexpr int kBC = kTT * N;
+  constexpr bool kBf16 = std::is_same<Act, __nv_bfloat16>::value;
+  constexpr int kStageElems = 3 * kTile + kBC;
+  constexpr int kOwn = kTT / TPC;
+
+  extern __shared__ __align__(1024) unsigned char smem[];
+  Act* stages = reinterpret_cast<Act*>(smem);
+  float* cf = reinterpret_cast<float*>(smem + (size_t)S * kStageElems * sizeof(Act));  // [S][TT][N] (bf16)
+  float2* prep = reinterpret_cast<float2*>(cf + (kBf16 ? S * kTT * N : 0));              // [TT][kCh] (delta, dy)
+  uint64_t* full = reinterpret_cast<uint64_t*>(prep + kTT * kCh);
+  uint64_t* conv = full + S;
+  uint64_t* empty = conv + S;
+
+  const BwdParams& p = P.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.y, d0 = blockIdx.x * kCh, seg = blockIdx.z + 1;
+  const int L = p.L, D = p.D;
+  const int t_lo = seg * p.seg_len, t_hi = min(L, t_lo + p.seg_len);
+  const int ntiles = (t_hi - t_lo + kTT - 1) / kTT;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&conv[s], 32);
+      mbar_init(&empty[s], 4);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto tile_raw = [&](int s) { return stages + (size_t)s * kStageElems; };
+  auto tile_z = [&](int s) { return stages + (size_t)s * kStageElems + kTile; };
+  auto tile_g = [&](int s) { return stages + (size_t)s * kStageElems + 2 * kTile; };
+  auto tile_C = [&](int s) { return stages + (size_t)s * kStageElems + 3 * kTile; };
+
+  if (warp == 4) {
+    if (lane == 0) {
+      const uint32_t bytes = (uint32_t)(((kGate ? 3 : 2) * kTile + kBC) * sizeof(Act));
+      int issued = 0;
+      for (int k = 0; k < ntiles; ++k) {  // k-th tile from the end
+        const int s = k % S;
+        if (k >= S && !mbar_wait(&empty[s], (uint32_t)(k / S - 1) & 1, p.status)) break;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        const int row = b * L + t_lo + (ntiles - 1 - k) * kTT;
+        tma_load_2d(tile_raw(s), &P.map_raw, &full[s], d0, row);
+        if (kGate) tma_load_2d(tile_z(s), &P.map_z, &full[s], d0, row);
+        tma_load_2d(tile_g(s), &P.map_dout, &full[s], d0, row);
+        tma_load_2d(tile_C(s), &P.map_C, &full[s], 0, row);
+        issued = k + 1;
+      }
+      for (int s = 0; s < S && s < issued; ++s) {
+        const int k_last = s + S * ((issued - 1 - s) / S);
+        mbar_wait(&full[s], (uint32_t)(k_last / S) & 1, p.status);
+      }
+    }
+    return;
+  }
+  if (warp == 5) {
+    if (kBf16) {
+      for (int k = 0; k < ntiles; ++k) {
+        const int s = k % S;
+        if (!mbar_wait(&full[s], (uint32_t)(k / S) & 1, p.status)) break;
+        const __nv_bfloat162* tc = reinterpret_cast<const __nv_bfloat162*>(tile_C(s));
+        float* dst = cf + (size_t)s * kTT * N;
+        for (int e = lane; e < kBC / 2; e += 32)
+          *reinterpret_cast<float2*>(dst + 2 * e) = __bfloat1622float2(tc[e]);
+        mbar_arrive(&conv[s]);
+      }
+    }
+    return;
+  }
+
+  const int q = tid % TPC, cl = tid / TPC;
+  const int d = d0 + cl;
+  const bool dvalid = d < D;
+  const int dc = dvalid ? d : D - 1;
+  float2 A2[2], carry[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int n = 4 * q + 2 * i;
+    const float a0 = -expf(p.A_log[dc * N + n]);
+    const float a1 = -expf(p.A_log[dc * N + n + 1]);
+    A2[i] = kFast ? make_float2(a0 * kLog2e, a1 * kLog2e) : make_float2(a0, a1);
+    carry[i] = make_float2(0.f, 0.f);
+  }
+  const float bias = p.delta_bias[dc];
+  float dsum = 0.f;
+  for (int k = 0; k < ntiles; ++k) {
+    const int s = k % S;
+    const uint32_t par = (uint32_t)(k / S) & 1;
+    if (!mbar_wait(&full[s], par, p.status)) break;
+    if (kBf16 && !mbar_wait(&conv[s], par, p.status)) break;
+    const int tbase = t_lo + (ntiles - 1 - k) * kTT;
+    const int cnt = min(kTT, t_hi - tbase);
+    const Act* sr = tile_raw(s);
+    const Act* sz = tile_z(s);
+    const Act* sg = tile_g(s);
+    const float* Ct = (kBf16 ? cf + (size_t)s * kTT * N : reinterpret_cast<const float*>(tile_C(s))) + 4 * q;
+    // phase 1: (delta, dy) of the owned steps; steps past the end get (0, 0)
+#pragma unroll
+    for (int i = 0; i < kOwn; ++i) {
+      const int km = i * TPC + q;
+      const int kr = min(km, cnt - 1);
+      const float sp = kFast ? softplus_fast(lds_act(sr + kr * kCh + cl) + bias)
+                             : softplus_f(lds_act(sr + kr * kCh + cl) + bias);
+      float dy = lds_act(sg + kr * kCh + cl);
+      if (kGate) {
+        const float zz = lds_act(sz + kr * kCh + cl);
+        dy *= zz * (kFast ? sigmoid_fast(zz) : sigmoid_f(zz));
+      }
+      prep[km * kCh + cl] = km < cnt ? make_float2(sp, dy) : make_float2(0.f, 0.f);
+    }
+    __syncwarp();
+    // phase 2: the adjoint recurrence, last step first; only the carry is carried
+    float tsum = 0.f;
+    auto rstep = [&](int kk) {
+      const float2 v = prep[kk * kCh + cl];
+      const float2 dd = make_float2(v.x, v.x), dy2 = make_float2(v.y, v.y);
+      const float4 Cv = *reinterpret_cast<const float4*>(Ct + kk * N);
+      const float2 g0 = ffma2(dy2, make_float2(Cv.x, Cv.y), carry[0]);
+      const float2 g1 = ffma2(dy2, make_float2(Cv.z, Cv.w), carry[1]);
+      carry[0] = fmul2(decay2<kFast>(dd, A2[0]), g0);
+      carry[1] = fmul2(decay2<kFast>(dd, A2[1]), g1);
+      tsum += v.x;
+    };
+    if (cnt == kTT) {
+#pragma unroll
+      for (int kk = kTT - 1; kk >= 0; --kk) rstep(kk);
+    } else {
+      for (int kk = cnt - 1; kk >= 0; --kk) rstep(kk);
+    }
+    dsum += tsum;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+  if (dvalid) {
+    float* ag = p.seg_agg + ((((size_t)b * p.nseg + seg) * D + d) * N + 4 * q) * 2;
+    const float2 x0 = fmul2(make_float2(dsum, dsum), A2[0]);
+    const float2 x1 = fmul2(make_float2(dsum, dsum), A2[1]);
+    const float P0 = kFast ? ex2_approx(x0.x) : expf(x0.x), P1 = kFast ? ex2_approx(x0.y) : expf(x0.y);
+    const float P2 = kFast ? ex2_approx(x1.x) : expf(x1.x), P3 = kFast ? ex2_approx(x1.y) : expf(x1.y);
+    reinterpret_cast<float4*>(ag)[0] = make_float4(P0, carry[0].x, P1, carry[0].y);
+    reinterpret_cast<float4*>(ag)[1] = make_float4(P2, carry[1].x, P3, carry[1].y);
+  }
+}
+
+// Carry pass: per (b, d, n), from the last segment to the first,
+// seg_carry[s] = adjoint carry entering segment s's last step;
+// seg_carry[s-1] = carry_out_s + P_s * seg_carry[s].
+__global__ void s6_bwd_seg_carry_kernel(const BwdParams p) {
+  const size_t per = (size_t)p.D * p.N;
+  const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int b = blockIdx.y;
+  if (e >= per) return;
+  float chi = p.dh_last ? p.dh_last[(size_t)b * per + e] : 0.f;
+  for (int sg = p.nseg - 1; sg >= 0; --sg) {
+    p.seg_carry[((size_t)b * p.nseg + sg) * per + e] = chi;
+    if (sg > 0) {
+      const float* ag = p.seg_agg + (((size_t)b * p.nseg + sg) * per + e) * 2;
+      chi = fmaf(ag[0], chi, ag[1]);
+    }
+  }
+}
+
+template <typename Act, int TPC>
+size_t bwd_agg_smem_bytes() {
+  constexpr int N = 4 * TPC, kCh = kScanThreads / TPC, S = 3;
+  constexpr bool bf = std::is_same<Act, __nv_bfloat16>::value;
+  return (size_t)S * (3 * kTT * kCh + kTT * N) * sizeof(Act) + (bf ? (size_t)S * kTT * N * 4 : 0) +
+         (size_t)kTT * kCh * 8 + 3 * S * 8;
+}
+
+template <typename Act, int TPC, bool kFast, bool kGate>
+cudaError_t launch_agg(const BwdTmaParams& P, cudaStream_t stream) {
+  auto kern = s6_bwd_agg_kernel<Act, TPC, kFast, kGate>;
+  const size_t smem = bwd_agg_smem_bytes<Act, TPC>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  constexpr int kCh = kScanThreads / TPC;
+  const dim3 grid((P.p.D + kCh - 1) / kCh, P.p.B, P.p.nseg - 1);
+  kern<<<grid, kBwdWarps * 32, smem, stream>>>(P);
+  return cudaGetLastError();
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -619,19 +824,45 @@ cudaError_t launch_one(const BwdTmaParams& P, cudaStream_t stream) {
   const size_t smem = bwd_smem_bytes<Act>(NG);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((P.p.D + kDTile - 1) / kDTile, P.p.B);
+  const dim3 grid((P.p.D + kDTile - 1) / kDTile, P.p.B, P.p.nseg);
   kern<<<grid, kBwdWarps * 32, smem, stream>>>(P);
   return cudaGetLastError();
 }
 
 template <typename Act, int NG, bool kFast>
-cudaError_t launch_ng(const BwdTmaParams& P, cudaStream_t stream) {
+cudaError_t launch_ng(const BwdTmaParams& P, const BwdTmaParams& Pagg, cudaStream_t stream) {
+  if (P.p.nseg > 1) {
+    // chunked parallel scan: adjoint segment aggregates -> carries -> all segments at once
+    // (Pagg's tensor maps have the aggregate pass's 128/TPC-channel boxes)
+    constexpr int TPC = NG / 2;  // aggregate pass: 4 states per lane
+    cudaError_t e = P.p.z ? launch_agg<Act, TPC, kFast, true>(Pagg, stream) : launch_agg<Act, TPC, kFast, false>(Pagg, stream);
+    if (e != cudaSuccess) return e;
+    const dim3 cgrid((unsigned)(((size_t)P.p.D * P.p.N + 255) / 256), P.p.B);
+    s6_bwd_seg_carry_kernel<<<cgrid, 256, 0, stream>>>(P.p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   return P.p.z ? launch_one<Act, NG, kFast, true>(P, stream) : launch_one<Act, NG, kFast, false>(P, stream);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
+
+// Segments are used when the (batch x 64-channel tile) grid would leave SMs
+// idle (one CTA fits per SM): enough segments for about two CTAs per SM, each
+// at least four chunks long.
+int bwd_segments(int B, int L, int D, int N, int sms) {
+  if (!(N == 4 || N == 8 || N == 16) || L < 1024 || B <= 0 || D <= 0) return 1;
+  const long ctas = (long)B * ((D + kDTile - 1) / kDTile);
+  const long want = 2L * sms;
+  if (ctas * 2 >= want) return 1;
+  long nseg = (want + ctas - 1) / ctas;
+  nseg = std::min<long>(nseg, L / (4 * kChunk));
+  if (nseg < 2) return 1;
+  const int seg_len = (int)((((long)L + nseg - 1) / nseg + kChunk - 1) / kChunk * kChunk);
+  return (L + seg_len - 1) / seg_len;
+}
 
 // Same shape rules as the TMA forward: N in {4, 8, 16}, N*e and D*e
 // multiples of 16 bytes, 16-byte aligned tensors.
@@ -661,15 +892,23 @@ cudaError_t launch_bwd_tma(const BwdParams& p, int act, cudaStream_t stream) {
             make_map(&P.map_C, p.Cm, act, rows, p.N, kTT, p.N);
   if (p.z) ok = ok && make_map(&P.map_z, p.z, act, rows, p.D, kTT, kDTile);
   if (!ok) return cudaErrorInvalidValue;
+  BwdTmaParams Pagg = P;
+  if (p.nseg > 1) {
+    const uint32_t kch = (uint32_t)(kScanThreads / (p.N / 4));
+    ok = make_map(&Pagg.map_raw, p.delta_raw, act, rows, p.D, kTT, kch) &&
+         make_map(&Pagg.map_dout, p.dout, act, rows, p.D, kTT, kch);
+    if (p.z) ok = ok && make_map(&Pagg.map_z, p.z, act, rows, p.D, kTT, kch);
+    if (!ok) return cudaErrorInvalidValue;
+  }
   const int NG = p.N / 2;
   if (act == SSM_BF16) {
-    if (NG == 8) return launch_ng<__nv_bfloat16, 8, true>(P, stream);
-    if (NG == 4) return launch_ng<__nv_bfloat16, 4, true>(P, stream);
+    if (NG == 8) return launch_ng<__nv_bfloat16, 8, true>(P, Pagg, stream);
+    if (NG == 4) return launch_ng<__nv_bfloat16, 4, true>(P, Pagg, stream);
     return cudaErrorInvalidValue;
   }
-  if (NG == 8) return launch_ng<float, 8, false>(P, stream);
-  if (NG == 4) return launch_ng<float, 4, false>(P, stream);
-  if (NG == 2) return launch_ng<float, 2, false>(P, stream);
+  if (NG == 8) return launch_ng<float, 8, false>(P, Pagg, stream);
+  if (NG == 4) return launch_ng<float, 4, false>(P, Pagg, stream);
+  if (NG == 2) return launch_ng<float, 2, false>(P, Pagg, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -61,8 +61,15 @@ struct BwdParams {
   void* dz;    // non-null iff z non-null
   float* dh0;  // nullable
   float* ws_dbc;    // [ndt][B][L][2][N] per-CTA sums of the dBm / dCm terms
-  float* ws_param;  // [B][D][N+2] per-batch sums: A*sum(...), dDp, d_delta_bias
+  float* ws_param;  // [B][nseg][D][N+2] per-(batch, segment) sums: A*sum(...), dDp, d_delta_bias
   unsigned int* status;  // device status word (bounded waits report here)
+  // Time segments (chunked parallel scan, as in FwdParams): seg_len steps
+  // (a multiple of kChunk) each; seg_agg [B][nseg][D][N][2] holds each
+  // segment's decay product and zero-carry adjoint carry-out, seg_carry
+  // [B][nseg][D][N] the adjoint carry entering each segment's last step.
+  int seg_len, nseg;
+  float* seg_agg;
+  float* seg_carry;
   int B, L, D, N, nchunks;
 };
 
@@ -81,10 +88,13 @@ int report_error(int code, const char* fmt, ...);
 cudaError_t launch_bwd(const BwdParams& p, int act, cudaStream_t stream);
 bool bwd_tma_supported(const BwdParams& p, int act);
 cudaError_t launch_bwd_tma(const BwdParams& p, int act, cudaStream_t stream);
+// Segment count the TMA backward uses for this shape on a GPU with `sms` SMs (1 = none).
+int bwd_segments(int B, int L, int D, int N, int sms);
 cudaError_t launch_reduce_dbc(const float* ws_dbc, int ndt, int B, int L, int N, void* dBm,
                               void* dCm, int act, cudaStream_t stream);
 cudaError_t launch_reduce_params(const float* ws_param, int B, int D, int N, float* dA_log,
                                  float* dDp, float* d_delta_bias, cudaStream_t stream);
+// (B here is the number of partial rows: batches x segments.)
 
 // ---------------------------------------------------------------- device helpers
 
