@@ -58,8 +58,8 @@ typedef enum {
   SSM_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. N > 16) */
   SSM_ERR_WORKSPACE = 3,   /* ws NULL or ws_bytes below the required size */
   SSM_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
-  SSM_ERR_TIMEOUT = 5,     /* reserved: a bounded device-side wait gave up */
-  SSM_ERR_INTERNAL = 6     /* reserved: a device-side consistency check failed */
+  SSM_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up */
+  SSM_ERR_INTERNAL = 6     /* a device-side consistency check failed */
 } ssm_status;
 
 typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
@@ -81,7 +81,9 @@ int ssm_version(void);
 /* Synchronises `stream`, then reads and clears the library's device status
  * word on the current device.  Returns SSM_ERR_TIMEOUT if a kernel's bounded
  * pipeline wait gave up since the last check (its outputs are then invalid),
- * SSM_ERR_CUDA if the stream reports an error, else SSM_OK. */
+ * SSM_ERR_INTERNAL if a kernel found its shared-memory layout unusable and
+ * skipped its work (outputs invalid), SSM_ERR_CUDA if the stream reports an
+ * error, else SSM_OK. */
 int ssm_check_device_status(void *stream);
 
 /* Number of saved chunk states: ceil(seqlen / SSM_CHUNK_LEN); 0 for seqlen <= 0. */

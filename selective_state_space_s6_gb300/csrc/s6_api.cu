@@ -248,6 +248,8 @@ int ssm_check_device_status(void* stream) {
   if (ce == cudaSuccess) ce = cudaStreamSynchronize(st);
   if (ce != cudaSuccess) return cuda_fail(ce, "ssm_check_device_status");
   if (v & s6::kStatusWaitTimeoutBit) return fail(SSM_ERR_TIMEOUT, "a device-side wait gave up (status 0x%x)", v);
+  if (v & s6::kStatusLayoutBit)
+    return fail(SSM_ERR_INTERNAL, "a kernel found its shared memory misaligned for swizzled tiles (status 0x%x)", v);
   return SSM_OK;
 }
 

@@ -1,8 +1,9 @@
 // S6 backward, TMA-pipelined (sm_103a).
 //
-// CTA = (64-channel tile, batch), 6 warps: 4 consumer warps (lane pair =
-// channel, NG states per lane, as in the forward), a TMA producer warp and a
-// converter warp (bf16: Bm/Cm tiles widened to f32 once per tile).
+// CTA = (64-channel tile, batch, time segment), 2*TPC + 2 warps: 2*TPC
+// consumer warps (TPC = N/4 lanes per channel, 4 states per lane), a TMA
+// producer warp and a converter warp (bf16: Bm/Cm tiles widened to f32 once
+// per tile).
 //
 // Each lane walks its chunks (SSM_CHUNK_LEN = 64 steps, restarted from the
 // forward's chunk states) from last to first.  The producer streams each
@@ -17,17 +18,18 @@
 // (The second read of a chunk's tiles comes from L2.)
 //
 // Per step, the channel sums of the dBm and dCm terms over the CTA's 64
-// channels are taken in shared memory in a fixed order (8 channels per
-// thread with packed adds, then a 3-level xor butterfly) and stored as one
-// partial per CTA; the sums over t of the parameter terms stay in registers
-// per chunk and are added into per-lane totals with a compensated (Kahan)
-// add.  A small kernel adds the partials in ascending tile / batch order
-// (s6_bwd.cu).  No floating-point atomics: results are bit-identical from run
-// to run (the single-writer, fixed-order policy of deterministic_backward.py).
+// channels are taken in shared memory in a fixed order (within a warp: 4
+// channels per lane with packed adds, then an xor butterfly over the lane
+// groups; then the warps in ascending order) and stored as one partial per
+// CTA; the sums over t of the parameter terms stay in registers per chunk
+// and are added into per-lane totals with a compensated (Kahan) add.  A small
+// kernel adds the partials in ascending tile / batch order (s6_bwd.cu).  No
+// floating-point atomics: results are bit-identical from run to run (the
+// single-writer, fixed-order policy of deterministic_backward.py).
 //
-// Work that depends only on (t, d) -- softplus, the gate's sigmoid, dy,
-// the softplus derivative -- is done once per step by one lane of the pair
-// (even steps: lane 0, odd steps: lane 1) and shared with a shuffle.
+// Work that depends only on (t, d) -- softplus, the gate's sigmoid, dy, the
+// softplus derivative, the outputs du / d_delta_raw / dz -- is done for step
+// k by lane k % TPC of the channel and shared through shared memory.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -44,20 +46,20 @@ namespace {
 
 constexpr int kTT = 32;           // steps per tile
 constexpr int kTilesPerChunk = kChunk / kTT;
-constexpr int kBwdWarps = 6;
+constexpr int kAggWarps = 6;  // aggregate pass: 4 consumer warps + producer + converter
 template <typename Act>
 struct BwdStages {
   static constexpr int value = std::is_same<Act, float>::value ? 2 : 3;
 };
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-// Warp-local reduction scratch of one step: 4 blocks (q = dBm/dCm term x two
-// 4-state chunks of a lane's 8 states), each block holding one 16-byte chunk
-// per lane in lane order (conflict-free 128-bit writes), padded to 136 floats
-// so that the 64-bit reads of a half-warp (16 state pairs, one channel) hit
-// distinct banks.
-constexpr int kRedBlock = 32 * 4 + 8;
-constexpr int kRedWarpBuf = 4 * kRedBlock;
+// Warp-local reduction scratch of one step: two blocks (dBm terms, dCm terms),
+// each holding one 16-byte chunk (a lane's 4 states) per lane in lane order,
+// padded to 144 floats so that the 64-bit reads of a half-warp hit distinct
+// banks.  Two step slots per warp.
+constexpr int kRedBlock = 32 * 4 + 16;
+constexpr int kRedSlot = 2 * kRedBlock;
+constexpr int kRedSlots = 2;
 
 struct BwdTmaParams {
   CUtensorMap map_u, map_raw, map_z, map_dout, map_B, map_C;
@@ -105,38 +107,70 @@ __device__ __forceinline__ void kahan_add(float& sum, float& comp, float x) {
   sum = t;
 }
 
-// float offset of the value (q, lane-local state n) written by lane L in a warp buffer
-__device__ __forceinline__ int red_at(int q, int L, int n) {
-  return (q * 2 + ((n & 7) >> 2)) * kRedBlock + L * 4 + (n & 3);
+// Row stride (float2) of the per-step channel arrays dbuf / bprep: 64 + 4, so
+// that consecutive rows (read at once by the lanes of a channel, which own
+// consecutive steps) start 32 bytes apart in the banks: a half-warp's 64-bit
+// accesses (4 channels x 4 rows) then fill the 32 banks once.
+constexpr int kRow = kDTile + 4;
+
+// Activation tiles (u, delta_raw, z, dout) land in shared memory with the TMA
+// 128-byte swizzle: rows of 128 bytes (bf16: one row of 64 channels; f32: two
+// half tiles of 32 channels), and within each row the 16-byte unit j is
+// stored at j ^ (row % 8).  Byte offset of (row, channel):
+template <typename Act>
+__host__ __device__ constexpr int swz_col(int row7, int cl) {
+  // row7 = row % 8; the row's own 128-byte offset is added by the caller
+  return std::is_same<Act, float>::value
+             ? (cl >> 5) * (kTT * 128) + ((((cl & 31) >> 2) ^ row7) << 4) + ((cl & 3) << 2)
+             : ((((cl >> 3)) ^ row7) << 4) + ((cl & 7) << 1);
+}
+template <typename Act>
+__device__ __forceinline__ float lds_swz(const Act* tile, int row, int col_off) {
+  const unsigned char* base = reinterpret_cast<const unsigned char*>(tile) + row * 128 + col_off;
+  return lds_act(reinterpret_cast<const Act*>(base));
 }
 
-template <typename Act, int NG, bool kFast, bool kGate>
-__global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __grid_constant__ BwdTmaParams P) {
-  constexpr int N2 = 2 * NG;
-  constexpr int NH = NG / 2;
+// TPC lanes per channel, 4 states per lane (N = 4 * TPC); a CTA covers 64
+// channels with 64 * TPC consumer threads (2 * TPC warps), plus a producer
+// and a converter warp.
+template <typename Act, int TPC, bool kFast, bool kGate>
+__global__ void __launch_bounds__((2 * TPC + 2) * 32, 1) s6_bwd_tma_kernel(const __grid_constant__ BwdTmaParams P) {
+  constexpr int N = 4 * TPC;
+  constexpr int kLanes = kDTile * TPC;  // consumer threads
+  constexpr int kCW = kLanes / 32;      // consumer warps
   constexpr int kTile = kTT * kDTile;
-  constexpr int kBC = kTT * N2;
+  constexpr int kBC = kTT * N;
   constexpr bool kBf16 = std::is_same<Act, __nv_bfloat16>::value;
   constexpr int kStageElems = 4 * kTile + 2 * kBC;
   constexpr int kNSub = kChunk / kSub;  // checkpoints per chunk
-
   constexpr int S = BwdStages<Act>::value;
+  constexpr int kBst = kBf16 ? 2 * N : N;  // f32 row stride of the B (and C) rows
+  constexpr int kOwnA = kTT / TPC;         // pass-A steps a lane owns per tile
+  constexpr int kOwnB = kSub / TPC;        // pass-B steps a lane owns per sub-chunk
+  // per-step rows of the lanes' partial sums, one float4 of padding: the TPC
+  // lanes of a channel read rows k, k+1, .. at once, 16 bytes apart in the banks
+  constexpr int kPartRow = kLanes + 1;
+
   extern __shared__ __align__(1024) unsigned char smem[];
   Act* stages = reinterpret_cast<Act*>(smem);
-  float* fbase = reinterpret_cast<float*>(smem + (size_t)S * kStageElems * sizeof(Act));
-  float* bcf = fbase;                                              // [S][TT][2][N2] (bf16 only)
-  float2* dbuf = reinterpret_cast<float2*>(bcf + (kBf16 ? S * kTT * 2 * N2 : 0));  // [kChunk][64] (delta, delta*u)
-  float* ckpt = reinterpret_cast<float*>(dbuf + kChunk * kDTile);  // [kNSub][128][NG]
-  float* redw = ckpt + kNSub * kScanThreads * NG;                  // [4 warps][4 slots][kRedWarpBuf]
-  float* wpart = redw + 4 * 4 * kRedWarpBuf;                       // [2][kSub][4 warps][32]
-  float4* part = reinterpret_cast<float4*>(wpart + 2 * kSub * 4 * 32);  // [kSub][128] (y, gB, Ap, -)
-  float2* bprep = reinterpret_cast<float2*>(part + kSub * kScanThreads);  // [kSub][64] (dy, dz factor)
-  float* tot = reinterpret_cast<float*>(bprep + kSub * kDTile);   // [2 (sum, comp)][128][NG + 2]
-  uint64_t* full = reinterpret_cast<uint64_t*>(tot + 2 * kScanThreads * (NG + 2));
+  float* bcf = reinterpret_cast<float*>(smem + (size_t)S * kStageElems * sizeof(Act));  // [S][TT][2][N] (bf16)
+  float2* dbuf = reinterpret_cast<float2*>(bcf + (kBf16 ? S * kTT * 2 * N : 0));       // [kChunk][kRow] (delta, delta*u)
+  float* ckpt = reinterpret_cast<float*>(dbuf + kChunk * kRow);    // [kNSub][kLanes][4]
+  float* redw = ckpt + kNSub * kLanes * 4;                         // [kCW][kRedSlots][kRedSlot]
+  float* wpart = redw + kCW * kRedSlots * kRedSlot;                // [2][kSub][kCW][32]
+  float4* part = reinterpret_cast<float4*>(wpart + 2 * kSub * kCW * 32);  // [kSub][kPartRow] (y, gB, Ap, -)
+  float2* bprep = reinterpret_cast<float2*>(part + kSub * kPartRow);      // [kSub][kRow] (dy, dz factor)
+  float* tot = reinterpret_cast<float*>(bprep + kSub * kRow);             // [2 (sum, comp)][kLanes][6]
+  uint64_t* full = reinterpret_cast<uint64_t*>(tot + 2 * kLanes * 6);
   uint64_t* conv = full + S;
   uint64_t* empty = conv + S;
 
   const BwdParams& p = P.p;
+  // the swizzled tiles need 1024-byte aligned stages (uniform: the whole CTA leaves)
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusLayout);
+    return;
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.y, d0 = blockIdx.x * kDTile;
   const int L = p.L, D = p.D;
@@ -151,7 +185,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&conv[s], 32);
-      mbar_init(&empty[s], 4);
+      mbar_init(&empty[s], kCW);
     }
     fence_mbar_init();
   }
@@ -164,11 +198,17 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
   auto tile_B = [&](int s) { return stages + (size_t)s * kStageElems + 4 * kTile; };
   auto tile_C = [&](int s) { return stages + (size_t)s * kStageElems + 4 * kTile + kBC; };
 
-  // The item sequence every role walks: for chunk c = last..0 with ntl tiles:
-  // pass A tiles 0..ntl-1, then pass B tiles ntl-1..0.
+  // activation tile: one 64-channel box (bf16), two 32-channel half boxes (f32)
+  auto load_act = [&](Act* dst, const CUtensorMap* m, uint64_t* bar, int row) {
+    tma_load_2d(dst, m, bar, d0, row);
+    if (!kBf16) tma_load_2d(reinterpret_cast<unsigned char*>(dst) + kTT * 128, m, bar, d0 + 32, row);
+  };
+
+  // The item sequence every role walks: for chunk c = last..first of the
+  // segment, with ntl tiles: pass A tiles 0..ntl-1, then pass B tiles ntl-1..0.
   auto chunk_tiles = [&](int c) { return (min(kChunk, L - c * kChunk) + kTT - 1) / kTT; };
 
-  if (warp == 4) {
+  if (warp == kCW) {
     // ---------------- producer
     if (lane == 0) {
       tma_prefetch_desc(&P.map_u);
@@ -194,12 +234,12 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
           }
           const int row = b * L + c * kChunk + j * kTT;
           mbar_arrive_expect_tx(&full[s], passA ? bytesA : bytesB);
-          tma_load_2d(tile_u(s), &P.map_u, &full[s], d0, row);
-          tma_load_2d(tile_raw(s), &P.map_raw, &full[s], d0, row);
+          load_act(tile_u(s), &P.map_u, &full[s], row);
+          load_act(tile_raw(s), &P.map_raw, &full[s], row);
           tma_load_2d(tile_B(s), &P.map_B, &full[s], 0, row);
           if (!passA) {
-            if (kGate) tma_load_2d(tile_z(s), &P.map_z, &full[s], d0, row);
-            tma_load_2d(tile_g(s), &P.map_dout, &full[s], d0, row);
+            if (kGate) load_act(tile_z(s), &P.map_z, &full[s], row);
+            load_act(tile_g(s), &P.map_dout, &full[s], row);
             tma_load_2d(tile_C(s), &P.map_C, &full[s], 0, row);
           }
         }
@@ -212,7 +252,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
     }
     return;
   }
-  if (warp == 5) {
+  if (warp == kCW + 1) {
     // ---------------- converter (bf16): Bm (and Cm in pass B) -> f32
     if (kBf16) {
       int item = 0;
@@ -223,13 +263,13 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
           const bool passA = it < ntl;
           const int s = item % S;
           if (ok) ok = mbar_wait(&full[s], (uint32_t)(item / S) & 1, p.status);
-          const Act* tb = tile_B(s);
-          const Act* tc = tile_C(s);
-          float* dst = bcf + (size_t)s * kTT * 2 * N2;
-          for (int e = lane; e < kBC; e += 32) {
-            const int t = e / N2, n = e % N2;
-            dst[(t * 2 + 0) * N2 + n] = lds_act(tb + e);
-            if (!passA) dst[(t * 2 + 1) * N2 + n] = lds_act(tc + e);
+          const __nv_bfloat162* tb = reinterpret_cast<const __nv_bfloat162*>(tile_B(s));
+          const __nv_bfloat162* tc = reinterpret_cast<const __nv_bfloat162*>(tile_C(s));
+          float* dst = bcf + (size_t)s * kTT * 2 * N;
+          for (int e = lane; e < kBC / 2; e += 32) {
+            const int t = (2 * e) / N, n = (2 * e) % N;
+            *reinterpret_cast<float2*>(dst + (t * 2 + 0) * N + n) = __bfloat1622float2(tb[e]);
+            if (!passA) *reinterpret_cast<float2*>(dst + (t * 2 + 1) * N + n) = __bfloat1622float2(tc[e]);
           }
           mbar_arrive(&conv[s]);
         }
@@ -239,81 +279,73 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
   }
 
   // ---------------- consumers
-  const int half = tid & 1;
-  const int dl = tid >> 1;
-  const int d = d0 + dl;
+  const int q = tid % TPC;   // state group: states 4q .. 4q+3
+  const int cl = tid / TPC;  // channel within the CTA
+  const int d = d0 + cl;
   const bool dvalid = d < D;
   const int dc = dvalid ? d : D - 1;
-  const int wl = warp;  // consumer warp 0..3
+  // Lane q owns the steps k with k % TPC == q (row % 8 of owned step i of an
+  // 8-step group is i*TPC + q): byte offsets of this lane's channel in those
+  // rows of a swizzled tile.
+  int colo[kOwnB];
+#pragma unroll
+  for (int i = 0; i < kOwnB; ++i) colo[i] = swz_col<Act>(i * TPC + q, cl);
 
   // A2 = A*log2(e) on the fast path (2^x decays), A itself otherwise; sums
   // weighted by A are taken with A2 and scaled by kAscale = A / A2 at the end.
   constexpr float kAscale = kFast ? kLn2 : 1.f;
-  float2 A2[NH], carry[NH];
+  float2 A2[2], carry[2];
+  {
+    const float* cin = p.nseg > 1 ? p.seg_carry + (((size_t)b * p.nseg + seg) * D + dc) * N
+                                  : (p.dh_last ? p.dh_last + ((size_t)b * D + dc) * N : nullptr);
 #pragma unroll
-  for (int i = 0; i < NH; ++i) {
-    const int n = half * NG + 2 * i;
-    const float a0 = -expf(p.A_log[dc * N2 + n]);
-    const float a1 = -expf(p.A_log[dc * N2 + n + 1]);
-    A2[i] = kFast ? make_float2(a0 * kLog2e, a1 * kLog2e) : make_float2(a0, a1);
-    // adjoint carry entering this segment's last step: dh_last for the last
-    // segment, the composed carry of the segments to the right otherwise
-    const float* cin = p.nseg > 1 ? p.seg_carry + (((size_t)b * p.nseg + seg) * D + dc) * N2
-                                  : (p.dh_last ? p.dh_last + ((size_t)b * D + dc) * N2 : nullptr);
-    carry[i] = (cin && dvalid) ? make_float2(cin[n], cin[n + 1]) : make_float2(0.f, 0.f);
+    for (int i = 0; i < 2; ++i) {
+      const int n = 4 * q + 2 * i;
+      const float a0 = -expf(p.A_log[dc * N + n]);
+      const float a1 = -expf(p.A_log[dc * N + n + 1]);
+      A2[i] = kFast ? make_float2(a0 * kLog2e, a1 * kLog2e) : make_float2(a0, a1);
+      // adjoint carry entering this segment's last step: dh_last for the last
+      // segment, the composed carry of the segments to the right otherwise
+      carry[i] = (cin && dvalid) ? make_float2(cin[n], cin[n + 1]) : make_float2(0.f, 0.f);
+    }
   }
   const float bias = p.delta_bias[dc];
   const float Dd = p.Dp[dc];
-  float* my_tot = tot + tid * (NG + 2);                            // running totals
-  float* my_cmp = tot + kScanThreads * (NG + 2) + tid * (NG + 2);  // Kahan compensation
+  float* my_tot = tot + tid * 6;               // running totals: 4 states, dDp, d_delta_bias
+  float* my_cmp = tot + kLanes * 6 + tid * 6;  // Kahan compensation
 #pragma unroll
-  for (int i = 0; i < NG + 2; ++i) {
+  for (int i = 0; i < 6; ++i) {
     my_tot[i] = 0.f;
     my_cmp[i] = 0.f;
   }
 
-  // warp-local reducer role: output pair op = lane & 15 (q = op >> 3, states
-  // n = 2*(op & 7), n+1), channel half chh = lane >> 4 (8 channels each)
-  const int r_op = lane & 15, r_chh = lane >> 4;
-  const int r_q = r_op >> 3, r_n = 2 * (r_op & 7);
-  const int r_half = r_n / NG, r_nl = r_n % NG;
-  float* my_redw = redw + wl * 4 * kRedWarpBuf;  // 4 step slots
+  // warp-local reducer role: output pair op = lane % N (term r_q, states r_n,
+  // r_n + 1 of the channel), group r_g = lane / N of 4 channels
+  const int r_op = lane % N, r_g = lane / N;
+  const int r_q = r_op / (N / 2), r_n = 2 * (r_op % (N / 2));
+  const int r_src = r_n / 4, r_j = r_n % 4;  // owning lane-in-channel and index in its chunk
+  float* my_redw = redw + warp * kRedSlots * kRedSlot;
 
   Act* dup = static_cast<Act*>(p.du) + (size_t)b * L * D + d;
   Act* drp = static_cast<Act*>(p.d_delta_raw) + (size_t)b * L * D + d;
   Act* dzp = kGate ? static_cast<Act*>(p.dz) + (size_t)b * L * D + d : nullptr;
-  float* ws_dbc_b = p.ws_dbc + ((size_t)blockIdx.x * p.B + b) * (size_t)L * 2 * N2;
-
-  // the NH state pairs of this lane from a row of B or C (16-byte loads)
-  auto load_row = [&](const float* row, float2 (&v)[NH]) {
-    if constexpr (NH >= 2) {
-#pragma unroll
-      for (int i = 0; i < NH; i += 2) {
-        const float4 f = *reinterpret_cast<const float4*>(row + 2 * i);
-        v[i] = make_float2(f.x, f.y);
-        v[i + 1] = make_float2(f.z, f.w);
-      }
-    } else {
-      v[0] = *reinterpret_cast<const float2*>(row);
-    }
-  };
+  float* ws_dbc_b = p.ws_dbc + ((size_t)blockIdx.x * p.B + b) * (size_t)L * 2 * N;
 
   bool failed = false;
-  int s = 0;          // ring stage of the current item
-  uint32_t par = 0;   // its phase parity
+  int s = 0;         // ring stage of the current item
+  uint32_t par = 0;  // its phase parity
   int sub_parity = 0;
   for (int c = c_hi - 1; c >= c_lo; --c) {
     const int t0 = c * kChunk;
     const int clen = min(kChunk, L - t0);
     const int ntl = (clen + kTT - 1) / kTT;
-    float2 accA[NH];
+    float2 accA[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     float accD = 0.f, accBias = 0.f;
-#pragma unroll
-    for (int i = 0; i < NH; ++i) accA[i] = make_float2(0.f, 0.f);
-    float2 h[NH];
+    float2 h[2];
     {
-      const float* cs = p.chunk_states + (((size_t)b * nchunks + c) * D + dc) * N2 + half * NG;
-      load_row(cs, h);
+      const float4 cs = *reinterpret_cast<const float4*>(p.chunk_states + (((size_t)b * nchunks + c) * D + dc) * N + 4 * q);
+      h[0] = make_float2(cs.x, cs.y);
+      h[1] = make_float2(cs.z, cs.w);
     }
     for (int it = 0; it < 2 * ntl; ++it) {
       const bool passA = it < ntl;
@@ -325,10 +357,9 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
       const int cnt = min(kTT, clen - tb);
       const Act* su = tile_u(s);
       const Act* sr = tile_raw(s);
-      constexpr int kBst = kBf16 ? 2 * N2 : N2;
-      const float* Bt = (kBf16 ? bcf + (size_t)s * kTT * 2 * N2 : reinterpret_cast<const float*>(tile_B(s))) + half * NG;
-      const float* Ct = kBf16 ? Bt + N2 : reinterpret_cast<const float*>(tile_C(s)) + half * NG;
-      float2* dtile = dbuf + tb * kDTile;  // (delta, delta*u) rows of this tile
+      const float* Bt = (kBf16 ? bcf + (size_t)s * kTT * 2 * N : reinterpret_cast<const float*>(tile_B(s))) + 4 * q;
+      const float* Ct = kBf16 ? Bt + N : reinterpret_cast<const float*>(tile_C(s)) + 4 * q;
+      float2* dtile = dbuf + tb * kRow;  // (delta, delta*u) rows of this tile
 
       if (passA) {
         // ---------- pass A: (delta, delta*u) of the owned steps, then the recurrence
@@ -336,26 +367,24 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
           constexpr bool kFull = decltype(full_tag)::value;
           const int nv = kFull ? kTT : cnt;
 #pragma unroll
-          for (int i = 0; i < kTT / 2; ++i) {
-            const int km = 2 * i + half;
+          for (int i = 0; i < kOwnA; ++i) {
+            const int km = i * TPC + q;
             const int kr = kFull ? km : min(km, nv - 1);
-            const float sv = lds_act(sr + kr * kDTile + dl) + bias;
+            const int co = kFull ? colo[i % kOwnB] : swz_col<Act>(kr & 7, cl);
+            const float sv = lds_swz(sr, kr, co) + bias;
             const float sp = kFast ? softplus_fast(sv) : softplus_f(sv);
-            if (kFull || km < nv) dtile[km * kDTile + dl] = make_float2(sp, sp * lds_act(su + kr * kDTile + dl));
+            if (kFull || km < nv) dtile[km * kRow + cl] = make_float2(sp, sp * lds_swz(su, kr, co));
           }
           __syncwarp();
           auto stepA = [&](int kk) {
-            if ((kk % kSub) == 0) {
-              float2* ck = reinterpret_cast<float2*>(ckpt + (((tb + kk) / kSub) * kScanThreads + tid) * NG);
-#pragma unroll
-              for (int i = 0; i < NH; ++i) ck[i] = h[i];
-            }
-            const float2 dv = dtile[kk * kDTile + dl];
+            if ((kk % kSub) == 0)
+              *reinterpret_cast<float4*>(ckpt + (((tb + kk) / kSub) * kLanes + tid) * 4) =
+                  make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+            const float2 dv = dtile[kk * kRow + cl];
             const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
-            float2 Bv[NH];
-            load_row(Bt + kk * kBst, Bv);
-#pragma unroll
-            for (int i = 0; i < NH; ++i) h[i] = ffma2(decay2<kFast>(dd, A2[i]), h[i], fmul2(uu2, Bv[i]));
+            const float4 Bv = *reinterpret_cast<const float4*>(Bt + kk * kBst);
+            h[0] = ffma2(decay2<kFast>(dd, A2[0]), h[0], fmul2(uu2, make_float2(Bv.x, Bv.y)));
+            h[1] = ffma2(decay2<kFast>(dd, A2[1]), h[1], fmul2(uu2, make_float2(Bv.z, Bv.w)));
           };
           if (kFull) {
 #pragma unroll
@@ -377,68 +406,69 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
           const int ks = sc * kSub;  // first step of the sub-chunk within the tile
           const int cnt8 = min(kSub, cnt - ks);
           const int cstep = tb + ks;  // ... within the chunk
-          const float2* ckp = reinterpret_cast<const float2*>(ckpt + ((cstep / kSub) * kScanThreads + tid) * NG);
-          const float2* dsub = dbuf + cstep * kDTile;
-          float* wp_sub = wpart + sub_parity * (kSub * 4 * 32);
+          const float4 ck = *reinterpret_cast<const float4*>(ckpt + ((cstep / kSub) * kLanes + tid) * 4);
+          const float2 hstart[2] = {make_float2(ck.x, ck.y), make_float2(ck.z, ck.w)};
+          const float2* dsub = dbuf + cstep * kRow;
+          float* wp_sub = wpart + sub_parity * (kSub * kCW * 32);
           auto sub = [&](auto full_tag) {
             constexpr bool kFull = decltype(full_tag)::value;
             const int nv = kFull ? kSub : cnt8;
             // B1: recompute the sub-chunk's states into registers
-            float2 hs[kSub][NH];
+            float2 hs[kSub][2];
 #pragma unroll
             for (int k = 0; k < kSub; ++k) {
               if (kFull || k < nv) {
-                const float2 dv = dsub[k * kDTile + dl];
+                const float2 dv = dsub[k * kRow + cl];
                 const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
-                float2 Bv[NH];
-                load_row(Bt + (ks + k) * kBst, Bv);
-#pragma unroll
-                for (int i = 0; i < NH; ++i) {
-                  const float2 hp = k == 0 ? ckp[i] : hs[k > 0 ? k - 1 : 0][i];
-                  hs[k][i] = ffma2(decay2<kFast>(dd, A2[i]), hp, fmul2(uu2, Bv[i]));
-                }
+                const float4 Bv = *reinterpret_cast<const float4*>(Bt + (ks + k) * kBst);
+                const float2 hp0 = k == 0 ? hstart[0] : hs[k > 0 ? k - 1 : 0][0];
+                const float2 hp1 = k == 0 ? hstart[1] : hs[k > 0 ? k - 1 : 0][1];
+                hs[k][0] = ffma2(decay2<kFast>(dd, A2[0]), hp0, fmul2(uu2, make_float2(Bv.x, Bv.y)));
+                hs[k][1] = ffma2(decay2<kFast>(dd, A2[1]), hp1, fmul2(uu2, make_float2(Bv.z, Bv.w)));
               }
             }
             // B2: gate terms of the owned steps: dy = dout*silu(z), dz factor
 #pragma unroll
-            for (int i = 0; i < kSub / 2; ++i) {
-              const int km = 2 * i + half;
+            for (int i = 0; i < kOwnB; ++i) {
+              const int km = i * TPC + q;
               const int kr = ks + (kFull ? km : min(km, nv - 1));
-              const float gout = lds_act(sg + kr * kDTile + dl);
+              const int co = kFull ? colo[i] : swz_col<Act>(kr & 7, cl);
+              const float gout = lds_swz(sg, kr, co);
               float2 v = make_float2(gout, 0.f);
               if (kGate) {
-                const float zz = lds_act(sz + kr * kDTile + dl);
+                const float zz = lds_swz(sz, kr, co);
                 const float sgz = kFast ? sigmoid_fast(zz) : sigmoid_f(zz);
                 v.x = gout * zz * sgz;
                 v.y = gout * sgz * fmaf(zz, 1.f - sgz, 1.f);
               }
               if (!kFull && km >= nv) v = make_float2(0.f, 0.f);
-              bprep[km * kDTile + dl] = v;
+              bprep[km * kRow + cl] = v;
             }
             __syncwarp();
-            // B3: reverse steps in two groups of four; the adjoint carry is the
-            // only loop-carried value.  Each step's dBm/dCm terms go to one of
-            // four warp-local slots, reduced over the warp's 16 channels after
-            // each group (fixed order) into the per-warp partial wp_sub.
+            // B3: reverse steps in pairs; the adjoint carry is the only
+            // loop-carried value.  Each step's dBm/dCm terms go to one of two
+            // warp-local slots and are summed over the warp's channels after
+            // each pair (fixed order) into the per-warp partial wp_sub.
 #pragma unroll
-            for (int gi = kSub / 4 - 1; gi >= 0; --gi) {
+            for (int gi = kSub / 2 - 1; gi >= 0; --gi) {
 #pragma unroll
-              for (int k = 4 * gi + 3; k >= 4 * gi; --k) {
+              for (int k = 2 * gi + 1; k >= 2 * gi; --k) {
                 if (kFull || k < nv) {
-                  const float2 dv = dsub[k * kDTile + dl];
-                  const float dy = bprep[k * kDTile + dl].x;
+                  const float2 dv = dsub[k * kRow + cl];
+                  const float dy = bprep[k * kRow + cl].x;
                   const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
                   const float2 dy2 = make_float2(dy, dy);
-                  float2 Bv[NH], Cv[NH];
-                  load_row(Bt + (ks + k) * kBst, Bv);
-                  load_row(Ct + (ks + k) * kBst, Cv);
+                  const float4 Bv4 = *reinterpret_cast<const float4*>(Bt + (ks + k) * kBst);
+                  const float4 Cv4 = *reinterpret_cast<const float4*>(Ct + (ks + k) * kBst);
+                  const float2 Bv[2] = {make_float2(Bv4.x, Bv4.y), make_float2(Bv4.z, Bv4.w)};
+                  const float2 Cv[2] = {make_float2(Cv4.x, Cv4.y), make_float2(Cv4.z, Cv4.w)};
                   float2 ya = make_float2(0.f, 0.f), gba = make_float2(0.f, 0.f), apa = make_float2(0.f, 0.f);
-                  float2 tB[NH], tC[NH];
+                  float2 tB[2], tC[2];
 #pragma unroll
-                  for (int i = 0; i < NH; ++i) {
+                  for (int i = 0; i < 2; ++i) {
                     const float2 a = decay2<kFast>(dd, A2[i]);
                     const float2 hk = hs[k][i];
-                    const float2 hp = k == 0 ? ckp[i] : hs[k > 0 ? k - 1 : 0][i];
+                    const float2 hp = k == 0 ? hstart[i] : hs[k > 0 ? k - 1 : 0][i];
                     const float2 g = ffma2(dy2, Cv[i], carry[i]);
                     const float2 pv = fmul2(g, fmul2(a, hp));
                     apa = ffma2(A2[i], pv, apa);
@@ -449,66 +479,63 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
                     tC[i] = fmul2(dy2, hk);
                     carry[i] = fmul2(a, g);
                   }
-                  float* rb = my_redw + (k & 3) * kRedWarpBuf;
-                  if constexpr (NH >= 2) {
-#pragma unroll
-                    for (int i = 0; i < NH; i += 2) {
-                      *reinterpret_cast<float4*>(rb + red_at(0, lane, 2 * i)) =
-                          dvalid ? make_float4(tB[i].x, tB[i].y, tB[i + 1].x, tB[i + 1].y) : make_float4(0.f, 0.f, 0.f, 0.f);
-                      *reinterpret_cast<float4*>(rb + red_at(1, lane, 2 * i)) =
-                          dvalid ? make_float4(tC[i].x, tC[i].y, tC[i + 1].x, tC[i + 1].y) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                  } else {
-                    *reinterpret_cast<float2*>(rb + red_at(0, lane, 0)) = dvalid ? tB[0] : make_float2(0.f, 0.f);
-                    *reinterpret_cast<float2*>(rb + red_at(1, lane, 0)) = dvalid ? tC[0] : make_float2(0.f, 0.f);
-                  }
-                  part[k * kScanThreads + tid] =
-                      make_float4(ya.x + ya.y, gba.x + gba.y, (apa.x + apa.y) * kAscale, 0.f);
+                  float* rb = my_redw + (k & 1) * kRedSlot;
+                  *reinterpret_cast<float4*>(rb + lane * 4) =
+                      dvalid ? make_float4(tB[0].x, tB[0].y, tB[1].x, tB[1].y) : make_float4(0.f, 0.f, 0.f, 0.f);
+                  *reinterpret_cast<float4*>(rb + kRedBlock + lane * 4) =
+                      dvalid ? make_float4(tC[0].x, tC[0].y, tC[1].x, tC[1].y) : make_float4(0.f, 0.f, 0.f, 0.f);
+                  part[k * kPartRow + tid] = make_float4(ya.x + ya.y, gba.x + gba.y, (apa.x + apa.y) * kAscale, 0.f);
                 }
               }
               __syncwarp();
-              // channel sums of the group's four steps: 8 channels per lane, then the other half
+              // channel sums of the pair's steps: 4 channels per lane, then across groups
 #pragma unroll
-              for (int k = 4 * gi + 3; k >= 4 * gi; --k) {
+              for (int k = 2 * gi + 1; k >= 2 * gi; --k) {
                 if (kFull || k < nv) {
-                  const float* rb = my_redw + (k & 3) * kRedWarpBuf;
+                  const float* rb = my_redw + (k & 1) * kRedSlot + r_q * kRedBlock;
                   float2 v = make_float2(0.f, 0.f);
 #pragma unroll
-                  for (int k2 = 0; k2 < 8; ++k2) {
-                    const int L2 = 2 * (r_chh * 8 + k2) + r_half;
-                    v = fadd2(v, *reinterpret_cast<const float2*>(rb + red_at(r_q, L2, r_nl)));
+                  for (int k2 = 0; k2 < 4; ++k2) {
+                    const int L2 = (r_g * 4 + k2) * TPC + r_src;
+                    v = fadd2(v, *reinterpret_cast<const float2*>(rb + L2 * 4 + r_j));
                   }
-                  const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, v.x, 16), __shfl_xor_sync(0xffffffffu, v.y, 16));
-                  // both lanes of the pair hold the identical sum; both store it
-                  *reinterpret_cast<float2*>(wp_sub + (k * 4 + wl) * 32 + r_q * 16 + r_n) = fadd2(v, o);
+#pragma unroll
+                  for (int m = N; m < 32; m <<= 1)
+                    v = fadd2(v, make_float2(__shfl_xor_sync(0xffffffffu, v.x, m), __shfl_xor_sync(0xffffffffu, v.y, m)));
+                  // every group holds the identical sum; all store it
+                  *reinterpret_cast<float2*>(wp_sub + (k * kCW + warp) * 32 + r_q * N + r_n) = v;
                 }
               }
               __syncwarp();
             }
-            // B4: owned steps: combine the pair's partial sums, write du, d_delta_raw, dz
-            float o_du[kSub / 2], o_dr[kSub / 2], o_dz[kSub / 2];
+            // B4: owned steps: combine the channel's partial sums (fixed lane
+            // order), write du, d_delta_raw, dz
+            float o_du[kOwnB], o_dr[kOwnB], o_dz[kOwnB];
 #pragma unroll
-            for (int i = 0; i < kSub / 2; ++i) {
-              const int km = 2 * i + half;
+            for (int i = 0; i < kOwnB; ++i) {
+              const int km = i * TPC + q;
               const int kr = kFull ? km : min(km, nv - 1);
-              const float4 mine = part[kr * kScanThreads + tid];
-              const float4 other = part[kr * kScanThreads + (tid ^ 1)];
-              const float2 dv = dsub[kr * kDTile + dl];
-              const float2 bp = bprep[kr * kDTile + dl];
-              const float uo = lds_act(su + (ks + kr) * kDTile + dl);
-              const float ysum = mine.x + other.x, gb = mine.y + other.y, ap = mine.z + other.z;
+              float4 acc = part[kr * kPartRow + cl * TPC];
+#pragma unroll
+              for (int r = 1; r < TPC; ++r) {
+                const float4 o = part[kr * kPartRow + cl * TPC + r];
+                acc = make_float4(acc.x + o.x, acc.y + o.y, acc.z + o.z, 0.f);
+              }
+              const float2 dv = dsub[kr * kRow + cl];
+              const float2 bp = bprep[kr * kRow + cl];
+              const float uo = lds_swz(su, ks + kr, kFull ? colo[i] : swz_col<Act>(kr & 7, cl));
               const float dsp = kFast ? dsoftplus_fast(dv.x) : -expm1f(-dv.x);
-              const float draw = fmaf(uo, gb, ap) * dsp;
-              o_du[i] = fmaf(Dd, bp.x, dv.x * gb);
+              const float draw = fmaf(uo, acc.y, acc.z) * dsp;
+              o_du[i] = fmaf(Dd, bp.x, dv.x * acc.y);
               o_dr[i] = draw;
-              o_dz[i] = fmaf(Dd, uo, ysum) * bp.y;
+              o_dz[i] = fmaf(Dd, uo, acc.x) * bp.y;
               const bool ok = kFull || km < nv;
               accD += ok ? bp.x * uo : 0.f;
               accBias += ok ? draw : 0.f;
             }
 #pragma unroll
-            for (int i = 0; i < kSub / 2; ++i) {
-              const int km = 2 * i + half;
+            for (int i = 0; i < kOwnB; ++i) {
+              const int km = i * TPC + q;
               if (dvalid && (kFull || km < nv)) {
                 const size_t o = (size_t)(t0 + cstep + km) * D;
                 st_act(dup + o, o_du[i]);
@@ -522,16 +549,15 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
           else
             sub(std::false_type{});
           // B5: cross-warp sum of the sub-chunk's dBm/dCm partials (fixed warp order)
-          named_bar_sync(1, kScanThreads);
+          named_bar_sync(1, kLanes);
+          for (int idx = tid; idx < kSub * 2 * N; idx += kLanes) {
+            const int k = idx / (2 * N), o = idx % (2 * N);
+            if (k < cnt8) {
+              const float* src = wp_sub + k * kCW * 32 + o;
+              float v = src[0];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int idx = tid + e * kScanThreads;  // (step k, output o) = (idx / 32, idx % 32)
-            const int k = idx >> 5, o = idx & 31;
-            const int q = o >> 4, n = o & 15;
-            if (k < cnt8 && n < N2) {
-              const float* src = wp_sub + k * 4 * 32 + o;
-              const float v = ((src[0] + src[32]) + src[64]) + src[96];
-              ws_dbc_b[((size_t)(t0 + cstep + k) * 2 + q) * N2 + n] = v;
+              for (int w = 1; w < kCW; ++w) v += src[w * 32];
+              ws_dbc_b[(size_t)(t0 + cstep + k) * 2 * N + o] = v;
             }
           }
           sub_parity ^= 1;
@@ -546,30 +572,34 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
       }
     }
     // chunk sums -> compensated running totals (per-lane private smem)
-#pragma unroll
-    for (int i = 0; i < NH; ++i) {
-      kahan_add(my_tot[2 * i], my_cmp[2 * i], accA[i].x);
-      kahan_add(my_tot[2 * i + 1], my_cmp[2 * i + 1], accA[i].y);
-    }
-    kahan_add(my_tot[NG], my_cmp[NG], accD);
-    kahan_add(my_tot[NG + 1], my_cmp[NG + 1], accBias);
+    kahan_add(my_tot[0], my_cmp[0], accA[0].x);
+    kahan_add(my_tot[1], my_cmp[1], accA[0].y);
+    kahan_add(my_tot[2], my_cmp[2], accA[1].x);
+    kahan_add(my_tot[3], my_cmp[3], accA[1].y);
+    kahan_add(my_tot[4], my_cmp[4], accD);
+    kahan_add(my_tot[5], my_cmp[5], accBias);
   }
-  // ---------------- per-batch parameter partials and dh0
+  // ---------------- per-(batch, segment) parameter partials and dh0
   {
-    const float tD = my_tot[NG] + __shfl_xor_sync(0xffffffffu, my_tot[NG], 1);
-    const float tBs = my_tot[NG + 1] + __shfl_xor_sync(0xffffffffu, my_tot[NG + 1], 1);
-    if (dvalid) {
-      float* wp = p.ws_param + (((size_t)b * p.nseg + seg) * D + d) * (N2 + 2);
+    // dDp and d_delta_bias: each lane summed its owned steps; add the channel's TPC lanes
+    float tD = my_tot[4], tBs = my_tot[5];
 #pragma unroll
-      for (int i = 0; i < NH; ++i) {
-        const int n = half * NG + 2 * i;
+    for (int m = 1; m < TPC; m <<= 1) {
+      tD += __shfl_xor_sync(0xffffffffu, tD, m);
+      tBs += __shfl_xor_sync(0xffffffffu, tBs, m);
+    }
+    if (dvalid) {
+      float* wp = p.ws_param + (((size_t)b * p.nseg + seg) * D + d) * (N + 2);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int n = 4 * q + 2 * i;
         wp[n] = (A2[i].x * kAscale) * my_tot[2 * i];
         wp[n + 1] = (A2[i].y * kAscale) * my_tot[2 * i + 1];
-        if (p.dh0 && seg == 0) *reinterpret_cast<float2*>(p.dh0 + ((size_t)b * D + d) * N2 + n) = carry[i];
+        if (p.dh0 && seg == 0) *reinterpret_cast<float2*>(p.dh0 + ((size_t)b * D + d) * N + n) = carry[i];
       }
-      if (half == 0) {
-        wp[N2] = tD;
-        wp[N2 + 1] = tBs;
+      if (q == 0) {
+        wp[N] = tD;
+        wp[N + 1] = tBs;
       }
     }
   }
@@ -584,7 +614,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) s6_bwd_tma_kernel(const __g
 // roles and lane layout as the forward (TPC lanes per channel, 4 states each);
 // tiles are streamed last first.
 template <typename Act, int TPC, bool kFast, bool kGate>
-__global__ void __launch_bounds__(kBwdWarps * 32) s6_bwd_agg_kernel(const __grid_constant__ BwdTmaParams P) {
+__global__ void __launch_bounds__(kAggWarps * 32) s6_bwd_agg_kernel(const __grid_constant__ BwdTmaParams P) {
   constexpr int N = 4 * TPC;
   constexpr int kCh = kScanThreads / TPC;
   constexpr int S = 3;
@@ -768,7 +798,7 @@ cudaError_t launch_agg(const BwdTmaParams& P, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   constexpr int kCh = kScanThreads / TPC;
   const dim3 grid((P.p.D + kCh - 1) / kCh, P.p.B, P.p.nseg - 1);
-  kern<<<grid, kBwdWarps * 32, smem, stream>>>(P);
+  kern<<<grid, kAggWarps * 32, smem, stream>>>(P);
   return cudaGetLastError();
 }
 
@@ -787,7 +817,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 bool make_map(CUtensorMap* m, const void* base, int act, uint64_t rows, uint64_t cols, uint32_t box_rows,
-              uint32_t box_cols) {
+              uint32_t box_cols, bool swizzle128 = false) {
   auto enc = get_encode();
   if (!enc) return false;
   const size_t e = act == SSM_BF16 ? 2 : 4;
@@ -797,44 +827,45 @@ bool make_map(CUtensorMap* m, const void* base, int act, uint64_t rows, uint64_t
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, act == SSM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename Act>
-size_t bwd_smem_bytes(int NG) {
+template <typename Act, int TPC>
+size_t bwd_smem_bytes() {
   const bool bf = std::is_same<Act, __nv_bfloat16>::value;
   const int S = BwdStages<Act>::value;
-  size_t bytes = (size_t)S * (4 * kTT * kDTile + 2 * kTT * 2 * NG) * sizeof(Act);
-  bytes += (bf ? (size_t)S * kTT * 2 * 2 * NG : 0) * 4;          // bcf
-  bytes += (size_t)kChunk * kDTile * 8;                            // dbuf (float2)
-  bytes += (size_t)(kChunk / kSub) * kScanThreads * NG * 4;       // ckpt
-  bytes += (size_t)4 * 4 * kRedWarpBuf * 4;                        // redw (4 step slots per warp)
-  bytes += (size_t)2 * kSub * 4 * 32 * 4;                          // wpart
-  bytes += (size_t)kSub * kScanThreads * 16;                       // part (float4)
-  bytes += (size_t)kSub * kDTile * 8;                              // bprep
-  bytes += (size_t)2 * kScanThreads * (NG + 2) * 4;                // tot
-  bytes += 3 * S * 8;                                              // barriers
+  const int N = 4 * TPC, lanes = kDTile * TPC, cw = lanes / 32;
+  size_t bytes = (size_t)S * (4 * kTT * kDTile + 2 * kTT * N) * sizeof(Act);
+  bytes += (bf ? (size_t)S * kTT * 2 * N : 0) * 4;      // bcf
+  bytes += (size_t)kChunk * kRow * 8;                    // dbuf (float2)
+  bytes += (size_t)(kChunk / kSub) * lanes * 4 * 4;      // ckpt
+  bytes += (size_t)cw * kRedSlots * kRedSlot * 4;        // redw
+  bytes += (size_t)2 * kSub * cw * 32 * 4;               // wpart
+  bytes += (size_t)kSub * (lanes + 1) * 16;              // part (float4)
+  bytes += (size_t)kSub * kRow * 8;                      // bprep
+  bytes += (size_t)2 * lanes * 6 * 4;                    // tot
+  bytes += 3 * S * 8;                                    // barriers
   return bytes;
 }
 
-template <typename Act, int NG, bool kFast, bool kGate>
+template <typename Act, int TPC, bool kFast, bool kGate>
 cudaError_t launch_one(const BwdTmaParams& P, cudaStream_t stream) {
-  auto kern = s6_bwd_tma_kernel<Act, NG, kFast, kGate>;
-  const size_t smem = bwd_smem_bytes<Act>(NG);
+  auto kern = s6_bwd_tma_kernel<Act, TPC, kFast, kGate>;
+  const size_t smem = bwd_smem_bytes<Act, TPC>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((P.p.D + kDTile - 1) / kDTile, P.p.B, P.p.nseg);
-  kern<<<grid, kBwdWarps * 32, smem, stream>>>(P);
+  kern<<<grid, (2 * TPC + 2) * 32, smem, stream>>>(P);
   return cudaGetLastError();
 }
 
-template <typename Act, int NG, bool kFast>
-cudaError_t launch_ng(const BwdTmaParams& P, const BwdTmaParams& Pagg, cudaStream_t stream) {
+// TPC lanes per channel: 4 states per lane in both the main and the aggregate pass
+template <typename Act, int TPC, bool kFast>
+cudaError_t launch_tpc(const BwdTmaParams& P, const BwdTmaParams& Pagg, cudaStream_t stream) {
   if (P.p.nseg > 1) {
     // chunked parallel scan: adjoint segment aggregates -> carries -> all segments at once
     // (Pagg's tensor maps have the aggregate pass's 128/TPC-channel boxes)
-    constexpr int TPC = NG / 2;  // aggregate pass: 4 states per lane
     cudaError_t e = P.p.z ? launch_agg<Act, TPC, kFast, true>(Pagg, stream) : launch_agg<Act, TPC, kFast, false>(Pagg, stream);
     if (e != cudaSuccess) return e;
     const dim3 cgrid((unsigned)(((size_t)P.p.D * P.p.N + 255) / 256), P.p.B);
@@ -842,7 +873,7 @@ cudaError_t launch_ng(const BwdTmaParams& P, const BwdTmaParams& Pagg, cudaStrea
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  return P.p.z ? launch_one<Act, NG, kFast, true>(P, stream) : launch_one<Act, NG, kFast, false>(P, stream);
+  return P.p.z ? launch_one<Act, TPC, kFast, true>(P, stream) : launch_one<Act, TPC, kFast, false>(P, stream);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -885,12 +916,14 @@ cudaError_t launch_bwd_tma(const BwdParams& p, int act, cudaStream_t stream) {
   memset(&P, 0, sizeof(P));
   P.p = p;
   const uint64_t rows = (uint64_t)p.B * p.L;
-  bool ok = make_map(&P.map_u, p.u, act, rows, p.D, kTT, kDTile) &&
-            make_map(&P.map_raw, p.delta_raw, act, rows, p.D, kTT, kDTile) &&
-            make_map(&P.map_dout, p.dout, act, rows, p.D, kTT, kDTile) &&
+  // activation tiles: 128-byte swizzled boxes of 128-byte rows (64 bf16 / 32 f32 channels)
+  const uint32_t abox = act == SSM_BF16 ? kDTile : kDTile / 2;
+  bool ok = make_map(&P.map_u, p.u, act, rows, p.D, kTT, abox, true) &&
+            make_map(&P.map_raw, p.delta_raw, act, rows, p.D, kTT, abox, true) &&
+            make_map(&P.map_dout, p.dout, act, rows, p.D, kTT, abox, true) &&
             make_map(&P.map_B, p.Bm, act, rows, p.N, kTT, p.N) &&
             make_map(&P.map_C, p.Cm, act, rows, p.N, kTT, p.N);
-  if (p.z) ok = ok && make_map(&P.map_z, p.z, act, rows, p.D, kTT, kDTile);
+  if (p.z) ok = ok && make_map(&P.map_z, p.z, act, rows, p.D, kTT, abox, true);
   if (!ok) return cudaErrorInvalidValue;
   BwdTmaParams Pagg = P;
   if (p.nseg > 1) {
@@ -900,15 +933,15 @@ cudaError_t launch_bwd_tma(const BwdParams& p, int act, cudaStream_t stream) {
     if (p.z) ok = ok && make_map(&Pagg.map_z, p.z, act, rows, p.D, kTT, kch);
     if (!ok) return cudaErrorInvalidValue;
   }
-  const int NG = p.N / 2;
+  const int TPC = p.N / 4;
   if (act == SSM_BF16) {
-    if (NG == 8) return launch_ng<__nv_bfloat16, 8, true>(P, Pagg, stream);
-    if (NG == 4) return launch_ng<__nv_bfloat16, 4, true>(P, Pagg, stream);
+    if (TPC == 4) return launch_tpc<__nv_bfloat16, 4, true>(P, Pagg, stream);
+    if (TPC == 2) return launch_tpc<__nv_bfloat16, 2, true>(P, Pagg, stream);
     return cudaErrorInvalidValue;
   }
-  if (NG == 8) return launch_ng<float, 8, false>(P, Pagg, stream);
-  if (NG == 4) return launch_ng<float, 4, false>(P, Pagg, stream);
-  if (NG == 2) return launch_ng<float, 2, false>(P, Pagg, stream);
+  if (TPC == 4) return launch_tpc<float, 4, false>(P, Pagg, stream);
+  if (TPC == 2) return launch_tpc<float, 2, false>(P, Pagg, stream);
+  if (TPC == 1) return launch_tpc<float, 1, false>(P, Pagg, stream);
   return cudaErrorInvalidValue;
 }
 

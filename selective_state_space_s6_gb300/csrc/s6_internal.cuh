@@ -16,6 +16,7 @@ constexpr int kThreadsPerChannel = 2;  // each channel's N states are split over
 constexpr int kScanThreads = kDTile * kThreadsPerChannel;
 constexpr int kSub = 8;                // backward: steps kept in registers per sub-chunk
 constexpr unsigned int kStatusWaitTimeoutBit = 1u;  // same bit as kStatusWaitTimeout
+constexpr unsigned int kStatusLayoutBit = 2u;       // same bit as kStatusLayout
 
 // ---------------------------------------------------------------- params
 

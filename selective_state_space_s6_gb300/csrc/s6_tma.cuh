@@ -12,6 +12,9 @@ namespace s6 {
 // Bits of the library's device status word (see ssm_check_device_status);
 // kernels receive the word's address as a parameter.
 constexpr unsigned int kStatusWaitTimeout = 1u;
+// a kernel found its shared-memory layout unusable (a swizzled TMA tile not
+// on a 1024-byte boundary) and did no work
+constexpr unsigned int kStatusLayout = 2u;
 // about 2 s at 2 GHz; a healthy pipeline waits microseconds
 constexpr long long kWaitCycles = 4000000000LL;
 
