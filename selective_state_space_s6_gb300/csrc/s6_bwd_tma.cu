@@ -1,9 +1,9 @@
 // S6 backward, TMA-pipelined (sm_103a).
 //
-// CTA = (64-channel tile, batch, time segment), 2*TPC + 2 warps: 2*TPC
+// CTA = (64-channel tile, batch, time segment), 2*TPC + 3 warps: 2*TPC
 // consumer warps (TPC = N/4 lanes per channel, 4 states per lane), a TMA
-// producer warp and a converter warp (bf16: Bm/Cm tiles widened to f32 once
-// per tile).
+// producer warp, a converter warp (bf16: Bm/Cm tiles widened to f32 once per
+// tile) and a reducer warp (cross-warp sums of the dBm/dCm terms).
 //
 // Each lane walks its chunks (SSM_CHUNK_LEN = 64 steps, restarted from the
 // forward's chunk states) from last to first.  The producer streams each
@@ -134,7 +134,7 @@ __device__ __forceinline__ float lds_swz(const Act* tile, int row, int col_off) 
 // channels with 64 * TPC consumer threads (2 * TPC warps), plus a producer
 // and a converter warp.
 template <typename Act, int TPC, bool kFast, bool kGate>
-__global__ void __launch_bounds__((2 * TPC + 2) * 32, 1) s6_bwd_tma_kernel(const __grid_constant__ BwdTmaParams P) {
+__global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const __grid_constant__ BwdTmaParams P) {
   constexpr int N = 4 * TPC;
   constexpr int kLanes = kDTile * TPC;  // consumer threads
   constexpr int kCW = kLanes / 32;      // consumer warps
@@ -164,6 +164,8 @@ __global__ void __launch_bounds__((2 * TPC + 2) * 32, 1) s6_bwd_tma_kernel(const
   uint64_t* full = reinterpret_cast<uint64_t*>(tot + 2 * kLanes * 6);
   uint64_t* conv = full + S;
   uint64_t* empty = conv + S;
+  uint64_t* wfull = empty + S;  // [2] wpart slot written by every consumer warp
+  uint64_t* wempty = wfull + 2; // [2] wpart slot summed by the reducer warp
 
   const BwdParams& p = P.p;
   // the swizzled tiles need 1024-byte aligned stages (uniform: the whole CTA leaves)
@@ -186,6 +188,10 @@ __global__ void __launch_bounds__((2 * TPC + 2) * 32, 1) s6_bwd_tma_kernel(const
       mbar_init(&full[s], 1);
       mbar_init(&conv[s], 32);
       mbar_init(&empty[s], kCW);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&wfull[i], kCW);
+      mbar_init(&wempty[i], 1);
     }
     fence_mbar_init();
   }
@@ -278,6 +284,38 @@ __global__ void __launch_bounds__((2 * TPC + 2) * 32, 1) s6_bwd_tma_kernel(const
     return;
   }
 
+  if (warp == kCW + 2) {
+    // ---------------- reducer: cross-warp sums of each sub-chunk's dBm/dCm
+    // partials (fixed warp order) -> this CTA's partial row in ws_dbc
+    float* ws_dbc_r = p.ws_dbc + ((size_t)blockIdx.x * p.B + b) * (size_t)L * 2 * N;
+    int n = 0;
+    bool ok = true;
+    for (int c = c_hi - 1; c >= c_lo; --c) {
+      const int clen = min(kChunk, L - c * kChunk);
+      for (int j = chunk_tiles(c) - 1; j >= 0; --j) {
+        const int cnt = min(kTT, clen - j * kTT);
+        for (int sc = (cnt + kSub - 1) / kSub - 1; sc >= 0; --sc, ++n) {
+          const int cnt8 = min(kSub, cnt - sc * kSub);
+          const int slot = n & 1;
+          if (ok) ok = mbar_wait(&wfull[slot], (uint32_t)(n >> 1) & 1, p.status);
+          const float* wp = wpart + slot * (kSub * kCW * 32);
+          float* dst = ws_dbc_r + (size_t)(c * kChunk + j * kTT + sc * kSub) * 2 * N;
+          for (int idx = lane; idx < cnt8 * 2 * N; idx += 32) {
+            const int k = idx / (2 * N), o = idx % (2 * N);
+            const float* src = wp + k * kCW * 32 + o;
+            float v = src[0];
+#pragma unroll
+            for (int w = 1; w < kCW; ++w) v += src[w * 32];
+            dst[idx] = v;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&wempty[slot]);
+        }
+      }
+    }
+    return;
+  }
+
   // ---------------- consumers
   const int q = tid % TPC;   // state group: states 4q .. 4q+3
   const int cl = tid / TPC;  // channel within the CTA
@@ -329,12 +367,11 @@ __global__ void __launch_bounds__((2 * TPC + 2) * 32, 1) s6_bwd_tma_kernel(const
   Act* dup = static_cast<Act*>(p.du) + (size_t)b * L * D + d;
   Act* drp = static_cast<Act*>(p.d_delta_raw) + (size_t)b * L * D + d;
   Act* dzp = kGate ? static_cast<Act*>(p.dz) + (size_t)b * L * D + d : nullptr;
-  float* ws_dbc_b = p.ws_dbc + ((size_t)blockIdx.x * p.B + b) * (size_t)L * 2 * N;
 
   bool failed = false;
   int s = 0;         // ring stage of the current item
   uint32_t par = 0;  // its phase parity
-  int sub_parity = 0;
+  int nsub_done = 0;  // sub-chunks handed to the reducer so far
   for (int c = c_hi - 1; c >= c_lo; --c) {
     const int t0 = c * kChunk;
     const int clen = min(kChunk, L - t0);
@@ -409,7 +446,10 @@ __global__ void __launch_bounds__((2 * TPC + 2) * 32, 1) s6_bwd_tma_kernel(const
           const float4 ck = *reinterpret_cast<const float4*>(ckpt + ((cstep / kSub) * kLanes + tid) * 4);
           const float2 hstart[2] = {make_float2(ck.x, ck.y), make_float2(ck.z, ck.w)};
           const float2* dsub = dbuf + cstep * kRow;
-          float* wp_sub = wpart + sub_parity * (kSub * kCW * 32);
+          // wpart slot of this sub-chunk: wait until the reducer has summed its previous use
+          const int slot = nsub_done & 1;
+          if (nsub_done >= 2 && !failed) failed = !mbar_wait(&wempty[slot], (uint32_t)((nsub_done >> 1) - 1) & 1, p.status);
+          float* wp_sub = wpart + slot * (kSub * kCW * 32);
           auto sub = [&](auto full_tag) {
             constexpr bool kFull = decltype(full_tag)::value;
             const int nv = kFull ? kSub : cnt8;
@@ -480,10 +520,10 @@ __global__ void __launch_bounds__((2 * TPC + 2) * 32, 1) s6_bwd_tma_kernel(const
                     carry[i] = fmul2(a, g);
                   }
                   float* rb = my_redw + (k & 1) * kRedSlot;
-                  *reinterpret_cast<float4*>(rb + lane * 4) =
-                      dvalid ? make_float4(tB[0].x, tB[0].y, tB[1].x, tB[1].y) : make_float4(0.f, 0.f, 0.f, 0.f);
-                  *reinterpret_cast<float4*>(rb + kRedBlock + lane * 4) =
-                      dvalid ? make_float4(tC[0].x, tC[0].y, tC[1].x, tC[1].y) : make_float4(0.f, 0.f, 0.f, 0.f);
+                  // (channels past D: the tiles' zero fill makes dout and u,
+                  // hence dy, g and both terms, exactly 0)
+                  *reinterpret_cast<float4*>(rb + lane * 4) = make_float4(tB[0].x, tB[0].y, tB[1].x, tB[1].y);
+                  *reinterpret_cast<float4*>(rb + kRedBlock + lane * 4) = make_float4(tC[0].x, tC[0].y, tC[1].x, tC[1].y);
                   part[k * kPartRow + tid] = make_float4(ya.x + ya.y, gba.x + gba.y, (apa.x + apa.y) * kAscale, 0.f);
                 }
               }
@@ -548,20 +588,10 @@ __global__ void __launch_bounds__((2 * TPC + 2) * 32, 1) s6_bwd_tma_kernel(const
             sub(std::true_type{});
           else
             sub(std::false_type{});
-          // B5: cross-warp sum of the sub-chunk's dBm/dCm partials (fixed warp order)
-          named_bar_sync(1, kLanes);
-          for (int idx = tid; idx < kSub * 2 * N; idx += kLanes) {
-            const int k = idx / (2 * N), o = idx % (2 * N);
-            if (k < cnt8) {
-              const float* src = wp_sub + k * kCW * 32 + o;
-              float v = src[0];
-#pragma unroll
-              for (int w = 1; w < kCW; ++w) v += src[w * 32];
-              ws_dbc_b[(size_t)(t0 + cstep + k) * 2 * N + o] = v;
-            }
-          }
-          sub_parity ^= 1;
+          // B5: hand the sub-chunk's per-warp partials to the reducer warp
           __syncwarp();
+          if (lane == 0) mbar_arrive(&wfull[slot]);
+          ++nsub_done;
         }
       }
       __syncwarp();
@@ -845,7 +875,7 @@ size_t bwd_smem_bytes() {
   bytes += (size_t)kSub * (lanes + 1) * 16;              // part (float4)
   bytes += (size_t)kSub * kRow * 8;                      // bprep
   bytes += (size_t)2 * lanes * 6 * 4;                    // tot
-  bytes += 3 * S * 8;                                    // barriers
+  bytes += (3 * S + 4) * 8;                              // barriers
   return bytes;
 }
 
@@ -856,7 +886,7 @@ cudaError_t launch_one(const BwdTmaParams& P, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((P.p.D + kDTile - 1) / kDTile, P.p.B, P.p.nseg);
-  kern<<<grid, (2 * TPC + 2) * 32, smem, stream>>>(P);
+  kern<<<grid, (2 * TPC + 3) * 32, smem, stream>>>(P);
   return cudaGetLastError();
 }
 
