@@ -510,14 +510,15 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
                     const float2 hk = hs[k][i];
                     const float2 hp = k == 0 ? hstart[i] : hs[k > 0 ? k - 1 : 0][i];
                     const float2 g = ffma2(dy2, Cv[i], carry[i]);
-                    const float2 pv = fmul2(g, fmul2(a, hp));
+                    const float2 ag = fmul2(a, g);   // adjoint carried to step k-1
+                    const float2 pv = fmul2(ag, hp); // g * a * h_{k-1}
                     apa = ffma2(A2[i], pv, apa);
                     accA[i] = ffma2(dd, pv, accA[i]);
                     gba = ffma2(g, Bv[i], gba);
                     ya = ffma2(Cv[i], hk, ya);
                     tB[i] = fmul2(g, uu2);
                     tC[i] = fmul2(dy2, hk);
-                    carry[i] = fmul2(a, g);
+                    carry[i] = ag;
                   }
                   float* rb = my_redw + (k & 1) * kRedSlot;
                   // (channels past D: the tiles' zero fill makes dout and u,

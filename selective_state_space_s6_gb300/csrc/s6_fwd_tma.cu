@@ -46,6 +46,13 @@ constexpr float kLn2 = 0.6931471805599453f;
 template <typename Act>
 struct FwdCfg {
   static constexpr int kStages = std::is_same<Act, float>::value ? 3 : 4;
+  // one stage: u, delta_raw, z tiles [kTT][128/TPC] and Bm, Cm tiles [kTT][N],
+  // rounded up to 1024 bytes so that every stage's tiles start on the
+  // swizzle's alignment
+  template <int TPC>
+  static constexpr int stage_bytes() {
+    return ((3 * kTT * (kScanThreads / TPC) + 2 * kTT * 4 * TPC) * (int)sizeof(Act) + 1023) / 1024 * 1024;
+  }
 };
 
 struct FwdTmaParams {
@@ -94,6 +101,29 @@ __device__ __forceinline__ float2 decay2(float2 dd, float2 A) {
   return make_float2(expf(x.x), expf(x.y));
 }
 
+// Activation tiles [kTT rows][kCh channels] (u, delta_raw, z) arrive through
+// TMA boxes of at most 128 bytes per row (kNBox boxes side by side, each
+// [kTT][kChBox]) with the matching TMA swizzle (128, 64 or 32 bytes): within
+// every 8 rows, the 16-byte units of a row are permuted by an XOR with a
+// function of the row, so that the lanes of a channel, which read different
+// rows at the same time, hit different banks.  off() is the byte offset of
+// (row, channel) in the tile.
+template <typename Act, int kCh>
+struct ActTile {
+  static constexpr int kE = (int)sizeof(Act);
+  static constexpr int kRowB = kCh * kE < 128 ? kCh * kE : 128;  // bytes per box row
+  static constexpr int kChBox = kRowB / kE;                       // channels per box
+  static constexpr int kNBox = kCh / kChBox;
+  static constexpr int kMask = kRowB / 16 - 1;  // XOR mask: 7 (128 B), 3 (64 B), 1 (32 B)
+  static_assert(kRowB >= 32, "swizzled rows need at least 32 bytes");
+  __host__ __device__ static constexpr int off(int row, int ch) {
+    return swz((ch / kChBox) * (kTT * kRowB) + row * kRowB + (ch % kChBox) * kE);
+  }
+  // TMA swizzle of a byte offset within a box aligned to 8 rows: the 16-byte
+  // unit index (bits 4..) is XORed with the 128-byte line index (bits 7..)
+  __host__ __device__ static constexpr int swz(int o) { return o ^ (((o >> 7) & kMask) << 4); }
+};
+
 // TPC lanes per channel, 4 states per lane (N = 4 * TPC); 128 consumer lanes
 // cover kCh = 128 / TPC channels.  grid.z = time segment.  kAgg: the
 // aggregate pass of the chunked parallel scan -- from a zero state, run the
@@ -107,20 +137,33 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
   constexpr int kTile = kTT * kCh;        // elements of a [TT x kCh] tile
   constexpr int kBC = kTT * N;            // elements of a [TT x N] tile
   constexpr bool kBf16 = std::is_same<Act, __nv_bfloat16>::value;
-  constexpr int kStageElems = 3 * kTile + 2 * kBC;
+  constexpr int kStageBytes = FwdCfg<Act>::template stage_bytes<TPC>();
   constexpr int kBst = kBf16 ? 2 * N : N;  // f32 row stride of B (and C) rows
   constexpr int kOwn = kTT / TPC;          // steps whose (t, d) work a lane owns
+  constexpr int kPer = 8 / TPC;            // owned steps per 8 rows (the swizzle period)
+  constexpr int kPrepRow = kCh + 4;        // float2 row stride of prep (see below)
+  constexpr int kYRow = kScanThreads + 1;  // float row stride of ypart (see below)
+  using AT = ActTile<Act, kCh>;
 
   extern __shared__ __align__(1024) unsigned char smem[];
-  Act* stages = reinterpret_cast<Act*>(smem);
-  float* bcf = reinterpret_cast<float*>(smem + (size_t)S * kStageElems * sizeof(Act));  // [S][TT][2][N]
-  float2* prep = reinterpret_cast<float2*>(bcf + (kBf16 ? S * kTT * 2 * N : 0));         // [TT][kCh]
-  float* ypart = reinterpret_cast<float*>(prep + kTT * kCh);                            // [TT][128]
-  uint64_t* full = reinterpret_cast<uint64_t*>(ypart + kTT * kScanThreads);
+  unsigned char* stages = smem;
+  float* bcf = reinterpret_cast<float*>(smem + (size_t)S * kStageBytes);  // [S][TT][2][N]
+  // (delta, delta*u) per (step, channel); rows padded by 32 bytes so that the
+  // 64-bit accesses of a half-warp (4 rows x 4 channels) fill the banks once
+  float2* prep = reinterpret_cast<float2*>(bcf + (kBf16 ? S * kTT * 2 * N : 0));  // [TT][kPrepRow]
+  // per-lane partial readouts; rows padded by one float so that the TPC lanes
+  // of a channel, reading rows k, k+1, .. at once, hit different banks
+  float* ypart = reinterpret_cast<float*>(prep + kTT * kPrepRow);  // [TT][kYRow]
+  uint64_t* full = reinterpret_cast<uint64_t*>(ypart + kTT * kYRow);
   uint64_t* conv = full + S;
   uint64_t* empty = conv + S;
 
   const FwdParams& p = P.p;
+  // the swizzled tiles need 1024-byte aligned stages (uniform: the whole CTA leaves)
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusLayout);
+    return;
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.y, d0 = blockIdx.x * kCh, seg = blockIdx.z;
   const int L = p.L, D = p.D;
@@ -138,11 +181,17 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
   }
   __syncthreads();
 
-  auto tile_u = [&](int s) { return stages + (size_t)s * kStageElems; };
-  auto tile_raw = [&](int s) { return stages + (size_t)s * kStageElems + kTile; };
-  auto tile_z = [&](int s) { return stages + (size_t)s * kStageElems + 2 * kTile; };
-  auto tile_B = [&](int s) { return stages + (size_t)s * kStageElems + 3 * kTile; };
-  auto tile_C = [&](int s) { return stages + (size_t)s * kStageElems + 3 * kTile + kBC; };
+  auto tile_u = [&](int s) { return reinterpret_cast<Act*>(stages + (size_t)s * kStageBytes); };
+  auto tile_raw = [&](int s) { return tile_u(s) + kTile; };
+  auto tile_z = [&](int s) { return tile_u(s) + 2 * kTile; };
+  auto tile_B = [&](int s) { return tile_u(s) + 3 * kTile; };
+  auto tile_C = [&](int s) { return tile_u(s) + 3 * kTile + kBC; };
+  // activation tile: kNBox boxes of kChBox channels side by side
+  auto load_act = [&](Act* dst, const CUtensorMap* m, uint64_t* bar, int row) {
+#pragma unroll
+    for (int bx = 0; bx < AT::kNBox; ++bx)
+      tma_load_2d(reinterpret_cast<unsigned char*>(dst) + bx * (kTT * AT::kRowB), m, bar, d0 + bx * AT::kChBox, row);
+  };
 
   if (warp == 4) {
     // ---------------- producer
@@ -161,9 +210,9 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
         if (k >= S && !mbar_wait(&empty[s], (use - 1) & 1, p.status)) break;
         mbar_arrive_expect_tx(&full[s], bytes);
         const int row = b * L + t_begin + k * kTT;
-        tma_load_2d(tile_u(s), &P.map_u, &full[s], d0, row);
-        tma_load_2d(tile_raw(s), &P.map_raw, &full[s], d0, row);
-        if (kZ) tma_load_2d(tile_z(s), &P.map_z, &full[s], d0, row);
+        load_act(tile_u(s), &P.map_u, &full[s], row);
+        load_act(tile_raw(s), &P.map_raw, &full[s], row);
+        if (kZ) load_act(tile_z(s), &P.map_z, &full[s], row);
         tma_load_2d(tile_B(s), &P.map_B, &full[s], 0, row);
         if (!kAgg) tma_load_2d(tile_C(s), &P.map_C, &full[s], 0, row);
         issued = k + 1;
@@ -203,6 +252,11 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
   const int d = d0 + cl;
   const bool dvalid = d < D;
   const int dc = dvalid ? d : D - 1;
+  // swizzled offsets of this lane's channel in the rows of its owned steps
+  // (minus the row's own offset; the pattern repeats every 8 rows)
+  int colo[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) colo[j] = AT::off(j * TPC + q, cl) - (j * TPC + q) * AT::kRowB;
 
   float2 A2[2], h[2];
 #pragma unroll
@@ -232,16 +286,21 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
       float* cs = p.chunk_states + (((size_t)b * p.nchunks + tbase / kChunk) * D + d) * N + 4 * q;
       *reinterpret_cast<float4*>(cs) = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
     }
-    const Act* su = tile_u(s);
-    const Act* sr = tile_raw(s);
-    const Act* sz = tile_z(s);
+    const unsigned char* su = reinterpret_cast<const unsigned char*>(tile_u(s));
+    const unsigned char* sr = reinterpret_cast<const unsigned char*>(tile_raw(s));
+    const unsigned char* sz = reinterpret_cast<const unsigned char*>(tile_z(s));
+    // activation at (tile row kr, this lane's channel); i = owned-step index when kr is that step
+    auto act_at = [&](const unsigned char* t, int kr, int i, bool exact) {
+      const int o = exact ? kr * AT::kRowB + colo[i % kPer] : AT::off(kr, cl);
+      return lds_act(reinterpret_cast<const Act*>(t + o));
+    };
     const float* Bt = (kBf16 ? bcf + (size_t)s * kTT * 2 * N : reinterpret_cast<const float*>(tile_B(s))) + 4 * q;
     const float* Ct = (kBf16 ? Bt + N : reinterpret_cast<const float*>(tile_C(s)) + 4 * q);
 
     // one recurrence step for this lane's 4 states; the partial readout goes to ypart
     float tsum = 0.f;
     auto step = [&](int kk) {
-      const float2 dv = prep[kk * kCh + cl];
+      const float2 dv = prep[kk * kPrepRow + cl];
       const float2 dd = make_float2(dv.x, dv.x);
       const float2 uu = make_float2(dv.y, dv.y);
       const float4 Bv = *reinterpret_cast<const float4*>(Bt + kk * kBst);
@@ -254,7 +313,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
       } else {
         const float4 Cv = *reinterpret_cast<const float4*>(Ct + kk * kBst);
         const float2 y2 = ffma2(make_float2(Cv.z, Cv.w), h[1], fmul2(make_float2(Cv.x, Cv.y), h[0]));
-        ypart[kk * kScanThreads + tid] = y2.x + y2.y;
+        ypart[kk * kYRow + tid] = y2.x + y2.y;
       }
     };
     // One tile in three phases.  kFull (all kTT steps valid, the common case)
@@ -270,12 +329,12 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
       for (int i = 0; i < kOwn; ++i) {
         const int km = i * TPC + q;
         const int kr = kFull ? km : min(km, n_valid - 1);
-        const float sp = softplus_k<kFast>(lds_act(sr + kr * kCh + cl) + bias);
-        pv[i] = make_float2(sp, sp * lds_act(su + kr * kCh + cl));
+        const float sp = softplus_k<kFast>(act_at(sr, kr, i, kFull) + bias);
+        pv[i] = make_float2(sp, sp * act_at(su, kr, i, kFull));
         if (!kFull && km >= n_valid) pv[i] = make_float2(0.f, 0.f);
       }
 #pragma unroll
-      for (int i = 0; i < kOwn; ++i) prep[(i * TPC + q) * kCh + cl] = pv[i];
+      for (int i = 0; i < kOwn; ++i) prep[(i * TPC + q) * kPrepRow + cl] = pv[i];
       __syncwarp();
       // phase 2: the recurrence; only h is carried from step to step
       if (kFull) {
@@ -293,12 +352,12 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
       for (int i = 0; i < kOwn; ++i) {
         const int km = i * TPC + q;
         const int kr = kFull ? km : min(km, n_valid - 1);
-        const float* yp = ypart + kr * kScanThreads + cl * TPC;
+        const float* yp = ypart + kr * kYRow + cl * TPC;
         float y = yp[0];
 #pragma unroll
         for (int r = 1; r < TPC; ++r) y += yp[r];
-        float o = fmaf(Dd, lds_act(su + kr * kCh + cl), y);
-        if (kGate) o *= silu_k<kFast>(lds_act(sz + kr * kCh + cl));
+        float o = fmaf(Dd, act_at(su, kr, i, kFull), y);
+        if (kGate) o *= silu_k<kFast>(act_at(sz, kr, i, kFull));
         ov[i] = o;
       }
 #pragma unroll
@@ -367,7 +426,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 // 2D map over a row-major [rows][cols] tensor, box [box_rows][box_cols].
 bool make_map(CUtensorMap* m, const void* base, int act, uint64_t rows, uint64_t cols, uint32_t box_rows,
-              uint32_t box_cols) {
+              uint32_t box_cols, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
   auto enc = get_encode();
   if (!enc) return false;
   const size_t e = act == SSM_BF16 ? 2 : 4;
@@ -377,7 +436,7 @@ bool make_map(CUtensorMap* m, const void* base, int act, uint64_t rows, uint64_t
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(m, act == SSM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -386,8 +445,8 @@ template <typename Act, int TPC>
 constexpr size_t fwd_smem_bytes() {
   constexpr int N = 4 * TPC, kCh = kScanThreads / TPC, S = FwdCfg<Act>::kStages;
   constexpr bool bf = std::is_same<Act, __nv_bfloat16>::value;
-  return (size_t)S * (3 * kTT * kCh + 2 * kTT * N) * sizeof(Act) + (bf ? (size_t)S * kTT * 2 * N * 4 : 0) +
-         (size_t)kTT * kCh * 8 + (size_t)kTT * kScanThreads * 4 + 3 * S * 8;
+  return (size_t)S * FwdCfg<Act>::template stage_bytes<TPC>() + (bf ? (size_t)S * kTT * 2 * N * 4 : 0) +
+         (size_t)kTT * (kCh + 4) * 8 + (size_t)kTT * (kScanThreads + 1) * 4 + 3 * S * 8;
 }
 
 template <typename Act, int TPC, bool kSave, bool kFast, bool kGate, bool kAgg>
@@ -467,11 +526,18 @@ cudaError_t launch_fwd_tma(const FwdParams& p, int act, cudaStream_t stream) {
   const int tpc = p.N / 4;
   const uint32_t kch = (uint32_t)(kScanThreads / tpc);
   const uint64_t rows = (uint64_t)p.B * p.L;
-  bool ok = make_map(&P.map_u, p.u, act, rows, p.D, kTT, kch) &&
-            make_map(&P.map_raw, p.delta_raw, act, rows, p.D, kTT, kch) &&
+  // activation boxes: rows of min(kch * e, 128) bytes with the swizzle of that width
+  const uint32_t e = act == SSM_BF16 ? 2 : 4;
+  const uint32_t row_b = std::min<uint32_t>(kch * e, 128);
+  const uint32_t abox = row_b / e;
+  const CUtensorMapSwizzle sw = row_b == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : row_b == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_32B;
+  bool ok = make_map(&P.map_u, p.u, act, rows, p.D, kTT, abox, sw) &&
+            make_map(&P.map_raw, p.delta_raw, act, rows, p.D, kTT, abox, sw) &&
             make_map(&P.map_B, p.Bm, act, rows, p.N, kTT, p.N) &&
             make_map(&P.map_C, p.Cm, act, rows, p.N, kTT, p.N);
-  if (p.z) ok = ok && make_map(&P.map_z, p.z, act, rows, p.D, kTT, kch);
+  if (p.z) ok = ok && make_map(&P.map_z, p.z, act, rows, p.D, kTT, abox, sw);
   if (!ok) return cudaErrorInvalidValue;
   if (act == SSM_BF16) {
     if (tpc == 4) return launch_tpc<__nv_bfloat16, 4, true>(P, stream);
