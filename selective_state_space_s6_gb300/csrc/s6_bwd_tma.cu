@@ -113,21 +113,10 @@ __device__ __forceinline__ void kahan_add(float& sum, float& comp, float x) {
 // accesses (4 channels x 4 rows) then fill the 32 banks once.
 constexpr int kRow = kDTile + 4;
 
-// Activation tiles (u, delta_raw, z, dout) land in shared memory with the TMA
-// 128-byte swizzle: rows of 128 bytes (bf16: one row of 64 channels; f32: two
-// half tiles of 32 channels), and within each row the 16-byte unit j is
-// stored at j ^ (row % 8).  Byte offset of (row, channel):
+// activation at a byte offset of a (swizzled) tile
 template <typename Act>
-__host__ __device__ constexpr int swz_col(int row7, int cl) {
-  // row7 = row % 8; the row's own 128-byte offset is added by the caller
-  return std::is_same<Act, float>::value
-             ? (cl >> 5) * (kTT * 128) + ((((cl & 31) >> 2) ^ row7) << 4) + ((cl & 3) << 2)
-             : ((((cl >> 3)) ^ row7) << 4) + ((cl & 7) << 1);
-}
-template <typename Act>
-__device__ __forceinline__ float lds_swz(const Act* tile, int row, int col_off) {
-  const unsigned char* base = reinterpret_cast<const unsigned char*>(tile) + row * 128 + col_off;
-  return lds_act(reinterpret_cast<const Act*>(base));
+__device__ __forceinline__ float lds_at(const Act* tile, int byte_off) {
+  return lds_act(reinterpret_cast<const Act*>(reinterpret_cast<const unsigned char*>(tile) + byte_off));
 }
 
 // TPC lanes per channel, 4 states per lane (N = 4 * TPC); a CTA covers 64
@@ -150,6 +139,8 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   // per-step rows of the lanes' partial sums, one float4 of padding: the TPC
   // lanes of a channel read rows k, k+1, .. at once, 16 bytes apart in the banks
   constexpr int kPartRow = kLanes + 1;
+  using AT = SwzTile<Act, kDTile, kTT>;  // u, delta_raw, z, dout tiles (128-byte rows)
+  constexpr int kRB = AT::kRowB;
 
   extern __shared__ __align__(1024) unsigned char smem[];
   Act* stages = reinterpret_cast<Act*>(smem);
@@ -204,10 +195,11 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   auto tile_B = [&](int s) { return stages + (size_t)s * kStageElems + 4 * kTile; };
   auto tile_C = [&](int s) { return stages + (size_t)s * kStageElems + 4 * kTile + kBC; };
 
-  // activation tile: one 64-channel box (bf16), two 32-channel half boxes (f32)
+  // activation tile: AT::kNBox boxes of AT::kChBox channels side by side
   auto load_act = [&](Act* dst, const CUtensorMap* m, uint64_t* bar, int row) {
-    tma_load_2d(dst, m, bar, d0, row);
-    if (!kBf16) tma_load_2d(reinterpret_cast<unsigned char*>(dst) + kTT * 128, m, bar, d0 + 32, row);
+#pragma unroll
+    for (int bx = 0; bx < AT::kNBox; ++bx)
+      tma_load_2d(reinterpret_cast<unsigned char*>(dst) + bx * AT::kBoxBytes, m, bar, d0 + bx * AT::kChBox, row);
   };
 
   // The item sequence every role walks: for chunk c = last..first of the
@@ -327,7 +319,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   // rows of a swizzled tile.
   int colo[kOwnB];
 #pragma unroll
-  for (int i = 0; i < kOwnB; ++i) colo[i] = swz_col<Act>(i * TPC + q, cl);
+  for (int i = 0; i < kOwnB; ++i) colo[i] = AT::col(i * TPC + q, cl);
 
   // A2 = A*log2(e) on the fast path (2^x decays), A itself otherwise; sums
   // weighted by A are taken with A2 and scaled by kAscale = A / A2 at the end.
@@ -407,10 +399,10 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
           for (int i = 0; i < kOwnA; ++i) {
             const int km = i * TPC + q;
             const int kr = kFull ? km : min(km, nv - 1);
-            const int co = kFull ? colo[i % kOwnB] : swz_col<Act>(kr & 7, cl);
-            const float sv = lds_swz(sr, kr, co) + bias;
+            const int o = kr * kRB + (kFull ? colo[i % kOwnB] : AT::col(kr, cl));
+            const float sv = lds_at(sr, o) + bias;
             const float sp = kFast ? softplus_fast(sv) : softplus_f(sv);
-            if (kFull || km < nv) dtile[km * kRow + cl] = make_float2(sp, sp * lds_swz(su, kr, co));
+            if (kFull || km < nv) dtile[km * kRow + cl] = make_float2(sp, sp * lds_at(su, o));
           }
           __syncwarp();
           auto stepA = [&](int kk) {
@@ -472,11 +464,11 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
             for (int i = 0; i < kOwnB; ++i) {
               const int km = i * TPC + q;
               const int kr = ks + (kFull ? km : min(km, nv - 1));
-              const int co = kFull ? colo[i] : swz_col<Act>(kr & 7, cl);
-              const float gout = lds_swz(sg, kr, co);
+              const int o = kr * kRB + (kFull ? colo[i] : AT::col(kr, cl));
+              const float gout = lds_at(sg, o);
               float2 v = make_float2(gout, 0.f);
               if (kGate) {
-                const float zz = lds_swz(sz, kr, co);
+                const float zz = lds_at(sz, o);
                 const float sgz = kFast ? sigmoid_fast(zz) : sigmoid_f(zz);
                 v.x = gout * zz * sgz;
                 v.y = gout * sgz * fmaf(zz, 1.f - sgz, 1.f);
@@ -564,7 +556,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
               }
               const float2 dv = dsub[kr * kRow + cl];
               const float2 bp = bprep[kr * kRow + cl];
-              const float uo = lds_swz(su, ks + kr, kFull ? colo[i] : swz_col<Act>(kr & 7, cl));
+              const float uo = lds_at(su, (ks + kr) * kRB + (kFull ? colo[i] : AT::col(kr, cl)));
               const float dsp = kFast ? dsoftplus_fast(dv.x) : -expm1f(-dv.x);
               const float draw = fmaf(uo, acc.y, acc.z) * dsp;
               o_du[i] = fmaf(Dd, bp.x, dv.x * acc.y);
@@ -644,6 +636,13 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
 // segment's decay product exp(A * sum(delta)) and the final carry.  Same warp
 // roles and lane layout as the forward (TPC lanes per channel, 4 states each);
 // tiles are streamed last first.
+// one aggregate-pass stage: delta_raw, z, dout tiles [kTT][128/TPC] and a Cm
+// tile [kTT][N], rounded up to 1024 bytes (the swizzled tiles' alignment)
+template <typename Act, int TPC>
+constexpr int agg_stage_bytes() {
+  return ((3 * kTT * (kScanThreads / TPC) + kTT * 4 * TPC) * (int)sizeof(Act) + 1023) / 1024 * 1024;
+}
+
 template <typename Act, int TPC, bool kFast, bool kGate>
 __global__ void __launch_bounds__(kAggWarps * 32) s6_bwd_agg_kernel(const __grid_constant__ BwdTmaParams P) {
   constexpr int N = 4 * TPC;
@@ -652,18 +651,25 @@ __global__ void __launch_bounds__(kAggWarps * 32) s6_bwd_agg_kernel(const __grid
   constexpr int kTile = kTT * kCh;
   constexpr int kBC = kTT * N;
   constexpr bool kBf16 = std::is_same<Act, __nv_bfloat16>::value;
-  constexpr int kStageElems = 3 * kTile + kBC;
+  constexpr int kStageBytes = agg_stage_bytes<Act, TPC>();
   constexpr int kOwn = kTT / TPC;
+  constexpr int kPer = 8 / TPC;      // owned steps per 8 rows (the swizzle period)
+  constexpr int kPrepRow = kCh + 4;  // float2 row stride of prep: rows 32 bytes apart in the banks
+  using AT = SwzTile<Act, kCh, kTT>;  // delta_raw, z, dout tiles
 
   extern __shared__ __align__(1024) unsigned char smem[];
-  Act* stages = reinterpret_cast<Act*>(smem);
-  float* cf = reinterpret_cast<float*>(smem + (size_t)S * kStageElems * sizeof(Act));  // [S][TT][N] (bf16)
-  float2* prep = reinterpret_cast<float2*>(cf + (kBf16 ? S * kTT * N : 0));              // [TT][kCh] (delta, dy)
-  uint64_t* full = reinterpret_cast<uint64_t*>(prep + kTT * kCh);
+  unsigned char* stages = smem;
+  float* cf = reinterpret_cast<float*>(smem + (size_t)S * kStageBytes);  // [S][TT][N] (bf16)
+  float2* prep = reinterpret_cast<float2*>(cf + (kBf16 ? S * kTT * N : 0));  // [TT][kPrepRow] (delta, dy)
+  uint64_t* full = reinterpret_cast<uint64_t*>(prep + kTT * kPrepRow);
   uint64_t* conv = full + S;
   uint64_t* empty = conv + S;
 
   const BwdParams& p = P.p;
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusLayout);
+    return;
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.y, d0 = blockIdx.x * kCh, seg = blockIdx.z + 1;
   const int L = p.L, D = p.D;
@@ -679,10 +685,15 @@ __global__ void __launch_bounds__(kAggWarps * 32) s6_bwd_agg_kernel(const __grid
     fence_mbar_init();
   }
   __syncthreads();
-  auto tile_raw = [&](int s) { return stages + (size_t)s * kStageElems; };
-  auto tile_z = [&](int s) { return stages + (size_t)s * kStageElems + kTile; };
-  auto tile_g = [&](int s) { return stages + (size_t)s * kStageElems + 2 * kTile; };
-  auto tile_C = [&](int s) { return stages + (size_t)s * kStageElems + 3 * kTile; };
+  auto tile_raw = [&](int s) { return reinterpret_cast<Act*>(stages + (size_t)s * kStageBytes); };
+  auto tile_z = [&](int s) { return tile_raw(s) + kTile; };
+  auto tile_g = [&](int s) { return tile_raw(s) + 2 * kTile; };
+  auto tile_C = [&](int s) { return tile_raw(s) + 3 * kTile; };
+  auto load_act = [&](Act* dst, const CUtensorMap* m, uint64_t* bar, int row) {
+#pragma unroll
+    for (int bx = 0; bx < AT::kNBox; ++bx)
+      tma_load_2d(reinterpret_cast<unsigned char*>(dst) + bx * AT::kBoxBytes, m, bar, d0 + bx * AT::kChBox, row);
+  };
 
   if (warp == 4) {
     if (lane == 0) {
@@ -693,9 +704,9 @@ __global__ void __launch_bounds__(kAggWarps * 32) s6_bwd_agg_kernel(const __grid
         if (k >= S && !mbar_wait(&empty[s], (uint32_t)(k / S - 1) & 1, p.status)) break;
         mbar_arrive_expect_tx(&full[s], bytes);
         const int row = b * L + t_lo + (ntiles - 1 - k) * kTT;
-        tma_load_2d(tile_raw(s), &P.map_raw, &full[s], d0, row);
-        if (kGate) tma_load_2d(tile_z(s), &P.map_z, &full[s], d0, row);
-        tma_load_2d(tile_g(s), &P.map_dout, &full[s], d0, row);
+        load_act(tile_raw(s), &P.map_raw, &full[s], row);
+        if (kGate) load_act(tile_z(s), &P.map_z, &full[s], row);
+        load_act(tile_g(s), &P.map_dout, &full[s], row);
         tma_load_2d(tile_C(s), &P.map_C, &full[s], 0, row);
         issued = k + 1;
       }
@@ -735,6 +746,9 @@ __global__ void __launch_bounds__(kAggWarps * 32) s6_bwd_agg_kernel(const __grid
     carry[i] = make_float2(0.f, 0.f);
   }
   const float bias = p.delta_bias[dc];
+  int colo[kPer];  // swizzled offsets of this channel in the rows of the owned steps
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) colo[j] = AT::col(j * TPC + q, cl);
   float dsum = 0.f;
   for (int k = 0; k < ntiles; ++k) {
     const int s = k % S;
@@ -748,24 +762,25 @@ __global__ void __launch_bounds__(kAggWarps * 32) s6_bwd_agg_kernel(const __grid
     const Act* sg = tile_g(s);
     const float* Ct = (kBf16 ? cf + (size_t)s * kTT * N : reinterpret_cast<const float*>(tile_C(s))) + 4 * q;
     // phase 1: (delta, dy) of the owned steps; steps past the end get (0, 0)
+    const bool full_tile = cnt == kTT;
 #pragma unroll
     for (int i = 0; i < kOwn; ++i) {
       const int km = i * TPC + q;
       const int kr = min(km, cnt - 1);
-      const float sp = kFast ? softplus_fast(lds_act(sr + kr * kCh + cl) + bias)
-                             : softplus_f(lds_act(sr + kr * kCh + cl) + bias);
-      float dy = lds_act(sg + kr * kCh + cl);
+      const int o = full_tile ? km * AT::kRowB + colo[i % kPer] : AT::off(kr, cl);
+      const float sp = kFast ? softplus_fast(lds_at(sr, o) + bias) : softplus_f(lds_at(sr, o) + bias);
+      float dy = lds_at(sg, o);
       if (kGate) {
-        const float zz = lds_act(sz + kr * kCh + cl);
+        const float zz = lds_at(sz, o);
         dy *= zz * (kFast ? sigmoid_fast(zz) : sigmoid_f(zz));
       }
-      prep[km * kCh + cl] = km < cnt ? make_float2(sp, dy) : make_float2(0.f, 0.f);
+      prep[km * kPrepRow + cl] = km < cnt ? make_float2(sp, dy) : make_float2(0.f, 0.f);
     }
     __syncwarp();
     // phase 2: the adjoint recurrence, last step first; only the carry is carried
     float tsum = 0.f;
     auto rstep = [&](int kk) {
-      const float2 v = prep[kk * kCh + cl];
+      const float2 v = prep[kk * kPrepRow + cl];
       const float2 dd = make_float2(v.x, v.x), dy2 = make_float2(v.y, v.y);
       const float4 Cv = *reinterpret_cast<const float4*>(Ct + kk * N);
       const float2 g0 = ffma2(dy2, make_float2(Cv.x, Cv.y), carry[0]);
@@ -817,8 +832,8 @@ template <typename Act, int TPC>
 size_t bwd_agg_smem_bytes() {
   constexpr int N = 4 * TPC, kCh = kScanThreads / TPC, S = 3;
   constexpr bool bf = std::is_same<Act, __nv_bfloat16>::value;
-  return (size_t)S * (3 * kTT * kCh + kTT * N) * sizeof(Act) + (bf ? (size_t)S * kTT * N * 4 : 0) +
-         (size_t)kTT * kCh * 8 + 3 * S * 8;
+  return (size_t)S * agg_stage_bytes<Act, TPC>() + (bf ? (size_t)S * kTT * N * 4 : 0) +
+         (size_t)kTT * (kCh + 4) * 8 + 3 * S * 8;
 }
 
 template <typename Act, int TPC, bool kFast, bool kGate>
@@ -848,7 +863,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 bool make_map(CUtensorMap* m, const void* base, int act, uint64_t rows, uint64_t cols, uint32_t box_rows,
-              uint32_t box_cols, bool swizzle128 = false) {
+              uint32_t box_cols, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
   auto enc = get_encode();
   if (!enc) return false;
   const size_t e = act == SSM_BF16 ? 2 : 4;
@@ -858,7 +873,7 @@ bool make_map(CUtensorMap* m, const void* base, int act, uint64_t rows, uint64_t
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, act == SSM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -911,19 +926,35 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 }  // namespace
 
-// Segments are used when the (batch x 64-channel tile) grid would leave SMs
-// idle (one CTA fits per SM): enough segments for about two CTAs per SM, each
-// at least four chunks long.
+// Time segments (chunked parallel scan) split each (batch, 64-channel tile)
+// into nseg CTAs over consecutive ranges of chunks.  One CTA fits per SM, so
+// the grid runs in waves of `sms` CTAs; the plan minimises a model of the run
+// time in units of one CTA's full-length run:
+//   ceil(ctas * nseg / sms) * (longest segment / sequence)      (main pass)
+//   + kAggCost * (nseg - 1) / nseg * ctas / sms                  (aggregates)
+// where kAggCost is the aggregate pass's cost per step relative to the main
+// pass.  Segments are at least four chunks long; a plan must beat one
+// segment by 3% to be taken.
 int bwd_segments(int B, int L, int D, int N, int sms) {
-  if (!(N == 4 || N == 8 || N == 16) || L < 1024 || B <= 0 || D <= 0) return 1;
+  if (!(N == 4 || N == 8 || N == 16) || L < 1024 || B <= 0 || D <= 0 || sms <= 0) return 1;
+  constexpr double kAggCost = 0.12;
   const long ctas = (long)B * ((D + kDTile - 1) / kDTile);
-  const long want = 2L * sms;
-  if (ctas * 2 >= want) return 1;
-  long nseg = (want + ctas - 1) / ctas;
-  nseg = std::min<long>(nseg, L / (4 * kChunk));
-  if (nseg < 2) return 1;
-  const int seg_len = (int)((((long)L + nseg - 1) / nseg + kChunk - 1) / kChunk * kChunk);
-  return (L + seg_len - 1) / seg_len;
+  const long nch = ((long)L + kChunk - 1) / kChunk;
+  auto waves = [&](long n) { return (double)((ctas * n + sms - 1) / sms); };
+  double best = waves(1);
+  int best_n = 1;
+  for (long n = 2; n <= 64 && nch / n >= 4; ++n) {
+    const long seg_ch = (nch + n - 1) / n;        // chunks per segment (the last may be shorter)
+    const long nseg = (nch + seg_ch - 1) / seg_ch;
+    if (nseg != n) continue;
+    const double t = waves(nseg) * (double)seg_ch / (double)nch +
+                     kAggCost * (double)(nseg - 1) / (double)nseg * (double)ctas / (double)sms;
+    if (t < 0.97 * best && t < 0.97 * waves(1)) {
+      best = t;
+      best_n = (int)nseg;
+    }
+  }
+  return best_n;
 }
 
 // Same shape rules as the TMA forward: N in {4, 8, 16}, N*e and D*e
@@ -949,19 +980,23 @@ cudaError_t launch_bwd_tma(const BwdParams& p, int act, cudaStream_t stream) {
   const uint64_t rows = (uint64_t)p.B * p.L;
   // activation tiles: 128-byte swizzled boxes of 128-byte rows (64 bf16 / 32 f32 channels)
   const uint32_t abox = act == SSM_BF16 ? kDTile : kDTile / 2;
-  bool ok = make_map(&P.map_u, p.u, act, rows, p.D, kTT, abox, true) &&
-            make_map(&P.map_raw, p.delta_raw, act, rows, p.D, kTT, abox, true) &&
-            make_map(&P.map_dout, p.dout, act, rows, p.D, kTT, abox, true) &&
+  bool ok = make_map(&P.map_u, p.u, act, rows, p.D, kTT, abox, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_map(&P.map_raw, p.delta_raw, act, rows, p.D, kTT, abox, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_map(&P.map_dout, p.dout, act, rows, p.D, kTT, abox, CU_TENSOR_MAP_SWIZZLE_128B) &&
             make_map(&P.map_B, p.Bm, act, rows, p.N, kTT, p.N) &&
             make_map(&P.map_C, p.Cm, act, rows, p.N, kTT, p.N);
-  if (p.z) ok = ok && make_map(&P.map_z, p.z, act, rows, p.D, kTT, abox, true);
+  if (p.z) ok = ok && make_map(&P.map_z, p.z, act, rows, p.D, kTT, abox, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
   BwdTmaParams Pagg = P;
   if (p.nseg > 1) {
+    // the aggregate pass's tiles: 128/TPC channels in boxes of <= 128-byte rows, swizzled
     const uint32_t kch = (uint32_t)(kScanThreads / (p.N / 4));
-    ok = make_map(&Pagg.map_raw, p.delta_raw, act, rows, p.D, kTT, kch) &&
-         make_map(&Pagg.map_dout, p.dout, act, rows, p.D, kTT, kch);
-    if (p.z) ok = ok && make_map(&Pagg.map_z, p.z, act, rows, p.D, kTT, kch);
+    const uint32_t e = act == SSM_BF16 ? 2 : 4;
+    const uint32_t row_b = std::min<uint32_t>(kch * e, 128);
+    const CUtensorMapSwizzle sw = swizzle_for_row_bytes((int)row_b);
+    ok = make_map(&Pagg.map_raw, p.delta_raw, act, rows, p.D, kTT, row_b / e, sw) &&
+         make_map(&Pagg.map_dout, p.dout, act, rows, p.D, kTT, row_b / e, sw);
+    if (p.z) ok = ok && make_map(&Pagg.map_z, p.z, act, rows, p.D, kTT, row_b / e, sw);
     if (!ok) return cudaErrorInvalidValue;
   }
   const int TPC = p.N / 4;

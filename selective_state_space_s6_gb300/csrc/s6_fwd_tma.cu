@@ -45,7 +45,9 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 template <typename Act>
 struct FwdCfg {
-  static constexpr int kStages = std::is_same<Act, float>::value ? 3 : 4;
+  // bf16: two stages keep a CTA at ~50 KB of shared memory, four CTAs per SM
+  // (a tile takes microseconds of compute, well above the copy latency)
+  static constexpr int kStages = std::is_same<Act, float>::value ? 3 : 2;
   // one stage: u, delta_raw, z tiles [kTT][128/TPC] and Bm, Cm tiles [kTT][N],
   // rounded up to 1024 bytes so that every stage's tiles start on the
   // swizzle's alignment
@@ -101,29 +103,6 @@ __device__ __forceinline__ float2 decay2(float2 dd, float2 A) {
   return make_float2(expf(x.x), expf(x.y));
 }
 
-// Activation tiles [kTT rows][kCh channels] (u, delta_raw, z) arrive through
-// TMA boxes of at most 128 bytes per row (kNBox boxes side by side, each
-// [kTT][kChBox]) with the matching TMA swizzle (128, 64 or 32 bytes): within
-// every 8 rows, the 16-byte units of a row are permuted by an XOR with a
-// function of the row, so that the lanes of a channel, which read different
-// rows at the same time, hit different banks.  off() is the byte offset of
-// (row, channel) in the tile.
-template <typename Act, int kCh>
-struct ActTile {
-  static constexpr int kE = (int)sizeof(Act);
-  static constexpr int kRowB = kCh * kE < 128 ? kCh * kE : 128;  // bytes per box row
-  static constexpr int kChBox = kRowB / kE;                       // channels per box
-  static constexpr int kNBox = kCh / kChBox;
-  static constexpr int kMask = kRowB / 16 - 1;  // XOR mask: 7 (128 B), 3 (64 B), 1 (32 B)
-  static_assert(kRowB >= 32, "swizzled rows need at least 32 bytes");
-  __host__ __device__ static constexpr int off(int row, int ch) {
-    return swz((ch / kChBox) * (kTT * kRowB) + row * kRowB + (ch % kChBox) * kE);
-  }
-  // TMA swizzle of a byte offset within a box aligned to 8 rows: the 16-byte
-  // unit index (bits 4..) is XORed with the 128-byte line index (bits 7..)
-  __host__ __device__ static constexpr int swz(int o) { return o ^ (((o >> 7) & kMask) << 4); }
-};
-
 // TPC lanes per channel, 4 states per lane (N = 4 * TPC); 128 consumer lanes
 // cover kCh = 128 / TPC channels.  grid.z = time segment.  kAgg: the
 // aggregate pass of the chunked parallel scan -- from a zero state, run the
@@ -143,7 +122,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
   constexpr int kPer = 8 / TPC;            // owned steps per 8 rows (the swizzle period)
   constexpr int kPrepRow = kCh + 4;        // float2 row stride of prep (see below)
   constexpr int kYRow = kScanThreads + 1;  // float row stride of ypart (see below)
-  using AT = ActTile<Act, kCh>;
+  using AT = SwzTile<Act, kCh, kTT>;  // u, delta_raw, z tiles
 
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* stages = smem;
@@ -256,7 +235,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
   // (minus the row's own offset; the pattern repeats every 8 rows)
   int colo[kPer];
 #pragma unroll
-  for (int j = 0; j < kPer; ++j) colo[j] = AT::off(j * TPC + q, cl) - (j * TPC + q) * AT::kRowB;
+  for (int j = 0; j < kPer; ++j) colo[j] = AT::col(j * TPC + q, cl);
 
   float2 A2[2], h[2];
 #pragma unroll
@@ -530,9 +509,7 @@ cudaError_t launch_fwd_tma(const FwdParams& p, int act, cudaStream_t stream) {
   const uint32_t e = act == SSM_BF16 ? 2 : 4;
   const uint32_t row_b = std::min<uint32_t>(kch * e, 128);
   const uint32_t abox = row_b / e;
-  const CUtensorMapSwizzle sw = row_b == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
-                                : row_b == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                              : CU_TENSOR_MAP_SWIZZLE_32B;
+  const CUtensorMapSwizzle sw = swizzle_for_row_bytes((int)row_b);
   bool ok = make_map(&P.map_u, p.u, act, rows, p.D, kTT, abox, sw) &&
             make_map(&P.map_raw, p.delta_raw, act, rows, p.D, kTT, abox, sw) &&
             make_map(&P.map_B, p.Bm, act, rows, p.N, kTT, p.N) &&

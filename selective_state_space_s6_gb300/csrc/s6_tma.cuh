@@ -139,4 +139,36 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 
+// Shared-memory image of a [kRows][kCh] activation tile delivered by TMA
+// boxes of at most 128 bytes per row (kNBox boxes of kChBox channels side by
+// side) with the swizzle of the box row width (128, 64 or 32 bytes): in each
+// byte offset the 16-byte unit index (bits 4..) is XORed with the 128-byte
+// line index (bits 7..), masked to the row width.  The lanes of a channel
+// read different rows at once; the XOR spreads those rows over the banks.
+// Tiles start on a 1024-byte boundary.
+template <typename Act, int kCh, int kRows>
+struct SwzTile {
+  static constexpr int kE = (int)sizeof(Act);
+  static constexpr int kRowB = kCh * kE < 128 ? kCh * kE : 128;  // bytes per box row
+  static constexpr int kChBox = kRowB / kE;                       // channels per box
+  static constexpr int kNBox = kCh / kChBox;
+  static constexpr int kBoxBytes = kRows * kRowB;
+  static constexpr int kMask = kRowB / 16 - 1;  // 7 (128 B), 3 (64 B), 1 (32 B)
+  static_assert(kRowB >= 32 && kCh % kChBox == 0 && kBoxBytes % 1024 == 0, "unsupported swizzled tile");
+  __host__ __device__ static constexpr int swz(int o) { return o ^ (((o >> 7) & kMask) << 4); }
+  // byte offset of (row, channel)
+  __host__ __device__ static constexpr int off(int row, int ch) {
+    return swz((ch / kChBox) * kBoxBytes + row * kRowB + (ch % kChBox) * kE);
+  }
+  // off(row, ch) - row * kRowB, which depends on row % 8 only
+  __host__ __device__ static constexpr int col(int row, int ch) { return off(row & 7, ch) - (row & 7) * kRowB; }
+};
+
+// tensor-map swizzle mode matching SwzTile's box row width
+inline CUtensorMapSwizzle swizzle_for_row_bytes(int row_bytes) {
+  return row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+         : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                           : CU_TENSOR_MAP_SWIZZLE_32B;
+}
+
 }  // namespace s6
