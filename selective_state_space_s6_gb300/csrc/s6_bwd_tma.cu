@@ -9,11 +9,12 @@
 // forward's chunk states) from last to first.  The producer streams each
 // chunk twice through an S-stage ring of 32-step tiles:
 //   pass A (tiles in forward order; delta_raw, u, Bm): recompute h from the
-//     chunk state, store delta = softplus(.) in shared memory for the chunk,
-//     and keep the state at every 8th step (checkpoints, shared memory);
+//     chunk state, store (delta, delta*u) in shared memory for the chunk and
+//     every state of the chunk in tensor memory (TMEM: 64 steps x 4 states
+//     per lane, 8 steps per 32-column store);
 //   pass B (tiles in reverse order; all inputs): for each 8-step sub-chunk,
-//     last first, recompute its 8 states into registers, then step backward
-//     with the adjoint g_t = dy_t*C_t + Abar_{t+1}*g_{t+1}, producing
+//     last first, load its 8 states from TMEM into registers, then step
+//     backward with the adjoint g_t = dy_t*C_t + Abar_{t+1}*g_{t+1}, producing
 //     du, d_delta_raw, dz and the dBm/dCm/dA_log/dDp/d_delta_bias terms.
 // (The second read of a chunk's tiles comes from L2.)
 //
@@ -131,7 +132,6 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   constexpr int kBC = kTT * N;
   constexpr bool kBf16 = std::is_same<Act, __nv_bfloat16>::value;
   constexpr int kStageElems = 4 * kTile + 2 * kBC;
-  constexpr int kNSub = kChunk / kSub;  // checkpoints per chunk
   constexpr int S = BwdStages<Act>::value;
   constexpr int kBst = kBf16 ? 2 * N : N;  // f32 row stride of the B (and C) rows
   constexpr int kOwnA = kTT / TPC;         // pass-A steps a lane owns per tile
@@ -139,6 +139,8 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   // per-step rows of the lanes' partial sums, one float4 of padding: the TPC
   // lanes of a channel read rows k, k+1, .. at once, 16 bytes apart in the banks
   constexpr int kPartRow = kLanes + 1;
+  constexpr uint32_t kTmemCols = 512;
+  static_assert(kCW <= 8, "two consumer warps per TMEM lane quarter at most");
   using AT = SwzTile<Act, kDTile, kTT>;  // u, delta_raw, z, dout tiles (128-byte rows)
   constexpr int kRB = AT::kRowB;
 
@@ -146,8 +148,8 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   Act* stages = reinterpret_cast<Act*>(smem);
   float* bcf = reinterpret_cast<float*>(smem + (size_t)S * kStageElems * sizeof(Act));  // [S][TT][2][N] (bf16)
   float2* dbuf = reinterpret_cast<float2*>(bcf + (kBf16 ? S * kTT * 2 * N : 0));       // [kChunk][kRow] (delta, delta*u)
-  float* ckpt = reinterpret_cast<float*>(dbuf + kChunk * kRow);    // [kNSub][kLanes][4]
-  float* redw = ckpt + kNSub * kLanes * 4;                         // [kCW][kRedSlots][kRedSlot]
+  float4* hc0 = reinterpret_cast<float4*>(dbuf + kChunk * kRow);   // [kLanes] state at the chunk start
+  float* redw = reinterpret_cast<float*>(hc0 + kLanes);            // [kCW][kRedSlots][kRedSlot]
   float* wpart = redw + kCW * kRedSlots * kRedSlot;                // [2][kSub][kCW][32]
   float4* part = reinterpret_cast<float4*>(wpart + 2 * kSub * kCW * 32);  // [kSub][kPartRow] (y, gB, Ap, -)
   float2* bprep = reinterpret_cast<float2*>(part + kSub * kPartRow);      // [kSub][kRow] (dy, dz factor)
@@ -157,6 +159,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   uint64_t* empty = conv + S;
   uint64_t* wfull = empty + S;  // [2] wpart slot written by every consumer warp
   uint64_t* wempty = wfull + 2; // [2] wpart slot summed by the reducer warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wempty + 2);
 
   const BwdParams& p = P.p;
   // the swizzled tiles need 1024-byte aligned stages (uniform: the whole CTA leaves)
@@ -186,7 +189,13 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
     }
     fence_mbar_init();
   }
+  // TMEM holds every state of the chunk being processed: per consumer warp
+  // 256 columns (64 steps x 4 states) of its 32 lanes; warps w and w + 4
+  // share a lane quarter and take columns 0..255 / 256..511
+  if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
+  tmem_fence_before_sync();
   __syncthreads();
+  tmem_fence_after_sync();
 
   auto tile_u = [&](int s) { return stages + (size_t)s * kStageElems; };
   auto tile_raw = [&](int s) { return stages + (size_t)s * kStageElems + kTile; };
@@ -341,6 +350,8 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   }
   const float bias = p.delta_bias[dc];
   const float Dd = p.Dp[dc];
+  // this warp's TMEM region: column 32*j + 4*k + i = state i of step 8*j + k of the chunk
+  const uint32_t tm = *tmem_slot + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((warp >> 2) * 256);
   float* my_tot = tot + tid * 6;               // running totals: 4 states, dDp, d_delta_bias
   float* my_cmp = tot + kLanes * 6 + tid * 6;  // Kahan compensation
 #pragma unroll
@@ -405,21 +416,26 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
             if (kFull || km < nv) dtile[km * kRow + cl] = make_float2(sp, sp * lds_at(su, o));
           }
           __syncwarp();
+          if (tb == 0) hc0[tid] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+          // states after each step, 8 steps at a time, then to TMEM
+          float hb[4 * kSub];
           auto stepA = [&](int kk) {
-            if ((kk % kSub) == 0)
-              *reinterpret_cast<float4*>(ckpt + (((tb + kk) / kSub) * kLanes + tid) * 4) =
-                  make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
             const float2 dv = dtile[kk * kRow + cl];
             const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
             const float4 Bv = *reinterpret_cast<const float4*>(Bt + kk * kBst);
             h[0] = ffma2(decay2<kFast>(dd, A2[0]), h[0], fmul2(uu2, make_float2(Bv.x, Bv.y)));
             h[1] = ffma2(decay2<kFast>(dd, A2[1]), h[1], fmul2(uu2, make_float2(Bv.z, Bv.w)));
+            const int r = 4 * (kk % kSub);
+            hb[r] = h[0].x;
+            hb[r + 1] = h[0].y;
+            hb[r + 2] = h[1].x;
+            hb[r + 3] = h[1].y;
           };
-          if (kFull) {
 #pragma unroll
-            for (int kk = 0; kk < kTT; ++kk) stepA(kk);
-          } else {
-            for (int kk = 0; kk < nv; ++kk) stepA(kk);
+          for (int kk = 0; kk < kTT; ++kk) {
+            if (kFull || kk < nv) stepA(kk);
+            // a block with at least one valid step goes out (warp-uniform)
+            if ((kk % kSub) == kSub - 1 && (kFull || kk - (kSub - 1) < nv)) tmem_st32(tm + (uint32_t)(4 * (tb + kk - (kSub - 1))), hb);
           }
         };
         if (cnt == kTT)
@@ -431,12 +447,20 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
         const Act* sz = tile_z(s);
         const Act* sg = tile_g(s);
         const int nsub = (cnt + kSub - 1) / kSub;
+        if (it == ntl) tmem_wait_st();  // the chunk's states (pass A) are in TMEM
         for (int sc = nsub - 1; sc >= 0; --sc) {
           const int ks = sc * kSub;  // first step of the sub-chunk within the tile
           const int cnt8 = min(kSub, cnt - ks);
           const int cstep = tb + ks;  // ... within the chunk
-          const float4 ck = *reinterpret_cast<const float4*>(ckpt + ((cstep / kSub) * kLanes + tid) * 4);
-          const float2 hstart[2] = {make_float2(ck.x, ck.y), make_float2(ck.z, ck.w)};
+          // the state before the sub-chunk: last state of the previous block, or the chunk start
+          float hq[4];
+          if (cstep > 0) {
+            tmem_ld4(tm + (uint32_t)(4 * cstep - 4), hq);
+          } else {
+            const float4 c0 = hc0[tid];
+            hq[0] = c0.x, hq[1] = c0.y, hq[2] = c0.z, hq[3] = c0.w;
+          }
+          const float2 hstart[2] = {make_float2(hq[0], hq[1]), make_float2(hq[2], hq[3])};
           const float2* dsub = dbuf + cstep * kRow;
           // wpart slot of this sub-chunk: wait until the reducer has summed its previous use
           const int slot = nsub_done & 1;
@@ -445,19 +469,14 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
           auto sub = [&](auto full_tag) {
             constexpr bool kFull = decltype(full_tag)::value;
             const int nv = kFull ? kSub : cnt8;
-            // B1: recompute the sub-chunk's states into registers
+            // B1: the sub-chunk's states from TMEM (written by pass A)
+            float hv[4 * kSub];
+            tmem_ld32(tm + (uint32_t)(4 * cstep), hv);
             float2 hs[kSub][2];
 #pragma unroll
             for (int k = 0; k < kSub; ++k) {
-              if (kFull || k < nv) {
-                const float2 dv = dsub[k * kRow + cl];
-                const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
-                const float4 Bv = *reinterpret_cast<const float4*>(Bt + (ks + k) * kBst);
-                const float2 hp0 = k == 0 ? hstart[0] : hs[k > 0 ? k - 1 : 0][0];
-                const float2 hp1 = k == 0 ? hstart[1] : hs[k > 0 ? k - 1 : 0][1];
-                hs[k][0] = ffma2(decay2<kFast>(dd, A2[0]), hp0, fmul2(uu2, make_float2(Bv.x, Bv.y)));
-                hs[k][1] = ffma2(decay2<kFast>(dd, A2[1]), hp1, fmul2(uu2, make_float2(Bv.z, Bv.w)));
-              }
+              hs[k][0] = make_float2(hv[4 * k], hv[4 * k + 1]);
+              hs[k][1] = make_float2(hv[4 * k + 2], hv[4 * k + 3]);
             }
             // B2: gate terms of the owned steps: dy = dout*silu(z), dz factor
 #pragma unroll
@@ -625,6 +644,14 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
         wp[N + 1] = tBs;
       }
     }
+  }
+  // every consumer is done with TMEM (loads waited for inline, stores before
+  // the loads of the same chunk): free it
+  tmem_fence_before_sync();
+  named_bar_sync(1, kLanes);
+  if (warp == 0) {
+    tmem_fence_after_sync();
+    tmem_dealloc(*tmem_slot, kTmemCols);
   }
 }
 
@@ -885,13 +912,13 @@ size_t bwd_smem_bytes() {
   size_t bytes = (size_t)S * (4 * kTT * kDTile + 2 * kTT * N) * sizeof(Act);
   bytes += (bf ? (size_t)S * kTT * 2 * N : 0) * 4;      // bcf
   bytes += (size_t)kChunk * kRow * 8;                    // dbuf (float2)
-  bytes += (size_t)(kChunk / kSub) * lanes * 4 * 4;      // ckpt
+  bytes += (size_t)lanes * 16;                           // hc0
   bytes += (size_t)cw * kRedSlots * kRedSlot * 4;        // redw
   bytes += (size_t)2 * kSub * cw * 32 * 4;               // wpart
   bytes += (size_t)kSub * (lanes + 1) * 16;              // part (float4)
   bytes += (size_t)kSub * kRow * 8;                      // bprep
   bytes += (size_t)2 * lanes * 6 * 4;                    // tot
-  bytes += (3 * S + 4) * 8;                              // barriers
+  bytes += (3 * S + 4) * 8 + 16;                         // barriers, TMEM address
   return bytes;
 }
 
