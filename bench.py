@@ -42,7 +42,23 @@ WORKLOAD = "mamba1p4b"
 METRIC = "fwd+bwd selective-scan G(B*L*D*N)/s"
 UNIT = "G(B*L*D*N)/s"
 ARGS = ("u", "delta_raw", "z", "Bm", "Cm", "A_log", "Dp", "delta_bias")
-KERNELS_PER_STEP = 4  # s6_fwd_kernel, s6_bwd_kernel, s6_reduce_dbc_kernel, s6_reduce_params_kernel
+# FP32 pipe: 152 SMs x 128 lanes x 2 flops (FMA) x 2.07 GHz (maximum SM clock)
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+# Algorithmic f32 flops per cell (b, t, d, n) of the method as the oracle
+# computes it (FMA = 2, exp on the special-function unit not counted):
+#   fwd: delta*A, (delta*u)*B, h = Abar*h + b, y += C*h                      -> 6
+#   bwd: the forward recurrence again (4) + g = dy*C + carry (2), a*g (1),
+#        (a*g)*h_prev (1), sum_n A*p (2), sum_t delta*p (2), sum_n g*B (2),
+#        sum_n C*h (2), dBm term g*delta*u and its sum over d (2), dCm term
+#        dy*h and its sum over d (2)                                          -> 20
+FLOPS_PER_CELL = {"fwd": 6, "bwd": 20}
+
+
+def launches_per_step(fwd_segments, bwd_segments):
+    """Kernels one step launches: the forward scan (or segment aggregates,
+    carries and the segmented scan), the backward scan (likewise), then the
+    two fixed-order reduction kernels of the finalize."""
+    return (1 if fwd_segments == 1 else 3) + (1 if bwd_segments == 1 else 3) + 2
 
 
 def load_peaks():
@@ -310,27 +326,38 @@ def run_ours(args, world, rank, local):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / ke, world)
     e2e_value = world * cells / (e2e_ms * 1e-3) / 1e9
 
-    # ---- roofline of the dominant kernel (the backward scan), live event timing
+    # ---- roofline of the dominant kernel (the backward scan), live event timing.
+    # The scans are bound by instruction issue on the FP32/SFU pipes, not by
+    # HBM: the roofline is the FP32 one (algorithmic flops / event time), with
+    # the HBM figures beside it.
     peak, peak_kind = load_peaks()
     fwd_bytes, bwd_bytes = algorithmic_bytes(B, L, D, N, e, s6.CHUNK_LEN)
     kern = {
-        "s6_fwd_kernel": {"ms": t_fwd, "bytes": fwd_bytes},
-        "s6_bwd_kernel": {"ms": t_bwd, "bytes": bwd_bytes},
-        "s6_reduce (finalize)": {"ms": t_fin, "bytes": None},
+        "s6_fwd": {"ms": t_fwd, "bytes": fwd_bytes, "flops": FLOPS_PER_CELL["fwd"] * cells},
+        "s6_bwd": {"ms": t_bwd, "bytes": bwd_bytes, "flops": FLOPS_PER_CELL["bwd"] * cells},
     }
-    dom = max(("s6_fwd_kernel", "s6_bwd_kernel"), key=lambda k: kern[k]["ms"])
-    achieved = kern[dom]["bytes"] / (kern[dom]["ms"] * 1e-3) / 1e9
-    traffic = load_traffic(dom)
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
-                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
-                "algorithmic_bytes_per_launch": kern[dom]["bytes"]}
+    dom = max(kern, key=lambda k: kern[k]["ms"])
+    secs = kern[dom]["ms"] * 1e-3
+    tflops = kern[dom]["flops"] / secs / 1e12
+    gbs_dom = kern[dom]["bytes"] / secs / 1e9
+    roofline = {"bound": "alu", "kernel": dom + " (segment aggregates + carries + scan)",
+                "achieved": round(tflops, 2), "peak": round(FP32_PEAK_TFLOPS, 2), "unit": "TFLOP/s",
+                "frac": round(tflops / FP32_PEAK_TFLOPS, 4), "traffic": load_traffic(dom),
+                "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 (FMA) x 2.07 GHz",
+                "algorithmic_flops_per_launch": kern[dom]["flops"],
+                "hbm": {"achieved": round(gbs_dom, 1), "peak": peak, "unit": "GB/s",
+                        "frac": round(gbs_dom / peak, 4), "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
+                        "algorithmic_bytes_per_launch": kern[dom]["bytes"]}}
     per_kernel = {}
-    for k in ("s6_fwd_kernel", "s6_bwd_kernel"):
-        gbs = kern[k]["bytes"] / (kern[k]["ms"] * 1e-3) / 1e9
-        per_kernel[k] = {"ms": round(kern[k]["ms"], 4), "gcells_s": round(cells / (kern[k]["ms"] * 1e-3) / 1e9, 1),
+    for k in kern:
+        s_k = kern[k]["ms"] * 1e-3
+        gbs = kern[k]["bytes"] / s_k / 1e9
+        per_kernel[k] = {"ms": round(kern[k]["ms"], 4), "gcells_s": round(cells / s_k / 1e9, 1),
+                         "tflops": round(kern[k]["flops"] / s_k / 1e12, 2),
+                         "fp32_frac": round(kern[k]["flops"] / s_k / 1e12 / FP32_PEAK_TFLOPS, 4),
                          "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4)}
-    per_kernel["s6_reduce_dbc+params (finalize)"] = {"ms": round(t_fin, 4)}
+    per_kernel["s6_bwd_finalize (reduce_dbc + reduce_params)"] = {"ms": round(t_fin, 4)}
+    fwd_seg, bwd_seg = s6.plan_segments(B, L, D, N, act)
 
     cpu_base = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -350,7 +377,8 @@ def run_ours(args, world, rank, local):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": KERNELS_PER_STEP * K,
+        "gpu_launches": launches_per_step(fwd_seg, bwd_seg) * K,
+        "segments": {"fwd": fwd_seg, "bwd": bwd_seg},
         "roofline": roofline,
         "kernels": per_kernel,
         "cpu_baseline": cpu_base,

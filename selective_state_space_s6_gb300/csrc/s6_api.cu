@@ -267,6 +267,15 @@ int64_t ssm_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t dim, int6
   return bwd_ws_layout(batch, seqlen, dim, dstate).total;
 }
 
+int ssm_plan_segments(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
+                      int* fwd_segments, int* bwd_segments) {
+  const int rc = check_shape(batch, seqlen, dim, dstate, act);
+  if (rc != SSM_OK) return rc;
+  if (fwd_segments) *fwd_segments = fwd_ws_layout(batch, seqlen, dim, dstate).nseg;
+  if (bwd_segments) *bwd_segments = bwd_ws_layout(batch, seqlen, dim, dstate).nseg;
+  return SSM_OK;
+}
+
 int ssm_scan_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
                  const void* u, const void* delta_raw, const void* z, const void* Bm,
                  const void* Cm, const float* A_log, const float* Dp, const float* delta_bias,

@@ -71,6 +71,8 @@ def load_library():
         lib.ssm_scan_bwd_finalize.restype = ci
         lib.ssm_step.argtypes = [i64] * 3 + [ci] + [vp] * 10 + [vp]
         lib.ssm_step.restype = ci
+        lib.ssm_plan_segments.argtypes = [i64] * 4 + [ci, ctypes.POINTER(ci), ctypes.POINTER(ci)]
+        lib.ssm_plan_segments.restype = ci
         _lib = lib
         return lib
 
@@ -115,6 +117,14 @@ def fwd_workspace_bytes(batch, seqlen, dim, dstate, act) -> int:
 
 def bwd_workspace_bytes(batch, seqlen, dim, dstate, act) -> int:
     return int(load_library().ssm_bwd_workspace_bytes(batch, seqlen, dim, dstate, act))
+
+
+def plan_segments(batch, seqlen, dim, dstate, act):
+    """(forward, backward) time-segment counts of the chunked parallel scan for this shape."""
+    f, b = ctypes.c_int(0), ctypes.c_int(0)
+    _check("ssm_plan_segments", load_library().ssm_plan_segments(batch, seqlen, dim, dstate, act,
+                                                                  ctypes.byref(f), ctypes.byref(b)))
+    return f.value, b.value
 
 
 def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]):

@@ -93,3 +93,28 @@ def test_step_validation(lib):
     args[8] = None  # h
     assert lib.ssm_step(2, 8, 4, 0, *args, None) == 1
     assert b"h must not be NULL" in lib.ssm_last_error()
+
+
+def test_segment_plan(lib):
+    """The time-segment plan is a function of the shape: one pass where the
+    (batch x channel-tile) grid fills the GPU in whole waves, several segments
+    for long sequences over few channels, never segments shorter than four
+    64-step chunks, and the workspace grows with the segment count."""
+    bf16 = s6.SSM_BF16
+    f, b = s6.plan_segments(4, 4096, 4096, 16, bf16)
+    assert f == 1 and b >= 1
+    f, b = s6.plan_segments(1, 65536, 2048, 16, s6.SSM_F32)
+    assert f > 1 and b > 1
+    for shape in [(1, 64, 16, 4), (2, 1023, 64, 16), (1, 1100, 64, 16), (3, 5000, 200, 8), (1, 4096, 32, 16)]:
+        f, b = s6.plan_segments(*shape, s6.SSM_F32)
+        L = shape[1]
+        for n in (f, b):
+            assert n >= 1
+            if n > 1:
+                seg = -(-L // n)
+                assert -(-seg // 64) >= 4 or L < 1024
+        assert s6.plan_segments(*shape, s6.SSM_F32) == (f, b)
+    # short sequences are never split
+    assert s6.plan_segments(1, 1000, 64, 16, s6.SSM_F32) == (1, 1)
+    with pytest.raises(s6.SSMError):
+        s6.plan_segments(1, 10, 16, 32, s6.SSM_F32)  # dstate above 16
