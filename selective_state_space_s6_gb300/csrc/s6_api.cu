@@ -149,7 +149,7 @@ int fwd_common(int64_t B, int64_t L, int64_t D, int64_t N, int act, const void* 
                const void* delta_raw, const void* z, const void* Bm, const void* Cm,
                const float* A_log, const float* Dp, const float* delta_bias, const float* h0,
                void* out, float* h_last, float* chunk_states, bool save, void* ws,
-               size_t ws_bytes, void* stream) {
+               size_t ws_bytes, void* stream, bool step = false) {
   S6_TRY(check_shape(B, L, D, N, act));
   const size_t e = act_size(act);
   const int64_t bld = B * L * D, bln = B * L * N, dn = D * N;
@@ -197,7 +197,11 @@ int fwd_common(int64_t B, int64_t L, int64_t D, int64_t N, int act, const void* 
     p.seg_agg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.agg_off);
     p.seg_start = reinterpret_cast<float*>(static_cast<char*>(ws) + w.start_off);
   }
-  cudaError_t ce = tma ? s6::launch_fwd_tma(p, act, st) : s6::launch_fwd(p, act, st);
+  cudaError_t ce;
+  if (step && L == 1 && s6::step_supported(p, act))
+    ce = s6::launch_step(p, act, st);
+  else
+    ce = tma ? s6::launch_fwd_tma(p, act, st) : s6::launch_fwd(p, act, st);
   if (ce != cudaSuccess) return cuda_fail(ce, "ssm_scan_fwd launch");
   return SSM_OK;
 }
@@ -415,7 +419,7 @@ int ssm_step(int64_t batch, int64_t dim, int64_t dstate, int act, const void* u,
              void* stream) {
   S6_TRY(need(h, batch * dim * (dstate > 0 ? dstate : 0), 4, "h"));
   return fwd_common(batch, 1, dim, dstate, act, u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias,
-                    h, out, h, nullptr, false, nullptr, 0, stream);
+                    h, out, h, nullptr, false, nullptr, 0, stream, /*step=*/true);
 }
 
 }  // extern "C"

@@ -370,6 +370,72 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
   }
 }
 
+// One decode step (T = 1).  TPC = N/4 lanes per channel, 4 states per lane,
+// with the arithmetic of the scan kernel above in the same order (softplus,
+// decays, state update, per-lane readout, the channel's lanes added in lane
+// order, skip, gate), so that L steps equal one L-step scan bit for bit.
+// Bound by HBM: each lane reads and writes its 16 bytes of state once; u,
+// delta_raw, z and Bm, Cm are shared by the lanes of a channel / a batch row.
+template <typename Act, int TPC, bool kFast, bool kGate>
+__global__ void __launch_bounds__(256) s6_step_kernel(const FwdParams p) {
+  constexpr int N = 4 * TPC;
+  const long long total = (long long)p.B * p.D * TPC;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const bool active = idx < total;
+  const long long i = active ? idx : total - 1;  // idle lanes still take part in the shuffles
+  const int q = (int)(i % TPC);
+  const long long bd = i / TPC;  // b * D + d
+  const int d = (int)(bd % p.D);
+  const long long b = bd / p.D;
+  const int lane = threadIdx.x & 31;
+
+  const Act* u_p = static_cast<const Act*>(p.u);
+  const float u = ld_act(u_p + bd);
+  const float raw = ld_act(static_cast<const Act*>(p.delta_raw) + bd);
+  const float4 al = __ldg(reinterpret_cast<const float4*>(p.A_log + (size_t)d * N + 4 * q));
+  float2 A2[2];
+  {
+    const float a0 = -expf(al.x), a1 = -expf(al.y), a2 = -expf(al.z), a3 = -expf(al.w);
+    A2[0] = kFast ? make_float2(a0 * kLog2e, a1 * kLog2e) : make_float2(a0, a1);
+    A2[1] = kFast ? make_float2(a2 * kLog2e, a3 * kLog2e) : make_float2(a2, a3);
+  }
+  float2 Bv[2], Cv[2];
+  if constexpr (std::is_same<Act, float>::value) {
+    const float4 bb = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.Bm) + b * N + 4 * q));
+    const float4 cc = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.Cm) + b * N + 4 * q));
+    Bv[0] = make_float2(bb.x, bb.y), Bv[1] = make_float2(bb.z, bb.w);
+    Cv[0] = make_float2(cc.x, cc.y), Cv[1] = make_float2(cc.z, cc.w);
+  } else {
+    const __nv_bfloat162* bb = reinterpret_cast<const __nv_bfloat162*>(static_cast<const Act*>(p.Bm) + b * N + 4 * q);
+    const __nv_bfloat162* cc = reinterpret_cast<const __nv_bfloat162*>(static_cast<const Act*>(p.Cm) + b * N + 4 * q);
+    Bv[0] = __bfloat1622float2(bb[0]), Bv[1] = __bfloat1622float2(bb[1]);
+    Cv[0] = __bfloat1622float2(cc[0]), Cv[1] = __bfloat1622float2(cc[1]);
+  }
+  const float4 hv = *reinterpret_cast<const float4*>(p.h0 + bd * N + 4 * q);
+  float2 h[2] = {make_float2(hv.x, hv.y), make_float2(hv.z, hv.w)};
+
+  const float sp = softplus_k<kFast>(raw + p.delta_bias[d]);
+  const float du = sp * u;
+  const float2 dd = make_float2(sp, sp), uu = make_float2(du, du);
+  const float2 a0 = decay2<kFast>(dd, A2[0]);
+  const float2 a1 = decay2<kFast>(dd, A2[1]);
+  h[0] = ffma2(a0, h[0], fmul2(uu, Bv[0]));
+  h[1] = ffma2(a1, h[1], fmul2(uu, Bv[1]));
+  const float2 y2 = ffma2(Cv[1], h[1], fmul2(Cv[0], h[0]));
+  const float part = y2.x + y2.y;
+  // the channel's lanes are consecutive: add their partial readouts in lane order
+  float y = __shfl_sync(0xffffffffu, part, lane - q);
+#pragma unroll
+  for (int r = 1; r < TPC; ++r) y += __shfl_sync(0xffffffffu, part, lane - q + r);
+  if (!active) return;
+  *reinterpret_cast<float4*>(p.h_last + bd * N + 4 * q) = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+  if (q == 0) {
+    float o = fmaf(p.Dp[d], u, y);
+    if (kGate) o *= silu_k<kFast>(ld_act(static_cast<const Act*>(p.z) + bd));
+    st_act(static_cast<Act*>(p.out) + bd, o);
+  }
+}
+
 // Carry pass of the chunked parallel scan: per (b, d, n), in segment order,
 // seg_start[s] = state before segment s, seg_start[s+1] = P_s * seg_start[s] + hloc_s.
 __global__ void s6_fwd_seg_carry_kernel(const FwdParams p) {
@@ -464,7 +530,45 @@ cudaError_t launch_tpc(const FwdTmaParams& P, cudaStream_t stream) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+template <typename Act, int TPC, bool kFast>
+cudaError_t launch_step_tpc(const FwdParams& p, cudaStream_t stream) {
+  const long long threads = (long long)p.B * p.D * TPC;
+  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  if (p.z)
+    s6_step_kernel<Act, TPC, kFast, true><<<blocks, 256, 0, stream>>>(p);
+  else
+    s6_step_kernel<Act, TPC, kFast, false><<<blocks, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+// The step kernel takes N in {4, 8, 16} with 16-byte aligned h and A_log and
+// Bm/Cm rows aligned to their 4-element loads (the same N as the TMA scan,
+// whose arithmetic it repeats); other shapes take one step of the generic scan.
+bool step_supported(const FwdParams& p, int act) {
+  if (!(p.N == 4 || p.N == 8 || p.N == 16)) return false;
+  if (act == SSM_BF16 && p.N == 4) return false;  // the TMA scan's rule for bf16
+  const uintptr_t bc_align = act == SSM_BF16 ? 7 : 15;
+  if ((reinterpret_cast<uintptr_t>(p.Bm) & bc_align) || (reinterpret_cast<uintptr_t>(p.Cm) & bc_align)) return false;
+  if (!aligned16(p.A_log) || !aligned16(p.h0) || !aligned16(p.h_last)) return false;
+  if ((long long)p.B * p.D * (p.N / 4) >= (1LL << 40)) return false;
+  // bit-identity with the scan needs the scan of the same shape to take the TMA path
+  return fwd_tma_supported(p, act);
+}
+
+cudaError_t launch_step(const FwdParams& p, int act, cudaStream_t stream) {
+  const int tpc = p.N / 4;
+  if (act == SSM_BF16) {
+    if (tpc == 4) return launch_step_tpc<__nv_bfloat16, 4, true>(p, stream);
+    if (tpc == 2) return launch_step_tpc<__nv_bfloat16, 2, true>(p, stream);
+    return cudaErrorInvalidValue;
+  }
+  if (tpc == 4) return launch_step_tpc<float, 4, false>(p, stream);
+  if (tpc == 2) return launch_step_tpc<float, 2, false>(p, stream);
+  if (tpc == 1) return launch_step_tpc<float, 1, false>(p, stream);
+  return cudaErrorInvalidValue;
+}
 
 // Segments are used when the (batch x channel-tile) grid alone would leave
 // most SMs idle: enough segments for about three CTAs per SM, each at least

@@ -80,6 +80,8 @@ struct BwdParams {
 cudaError_t launch_fwd(const FwdParams& p, int act, cudaStream_t stream);
 bool fwd_tma_supported(const FwdParams& p, int act);
 cudaError_t launch_fwd_tma(const FwdParams& p, int act, cudaStream_t stream);
+bool step_supported(const FwdParams& p, int act);
+cudaError_t launch_step(const FwdParams& p, int act, cudaStream_t stream);
 // Segment count the TMA forward uses for this shape on a GPU with `sms` SMs (1 = none).
 int fwd_segments(int B, int L, int D, int N, int sms);
 // Device address of the library's status word on the current device (nullptr on error).

@@ -88,16 +88,28 @@ def test_nosave_matches_save():
     assert torch.equal(o1, o2) and torch.equal(h1, h2)
 
 
-@pytest.mark.parametrize("act", ["f32", "bf16"])
-def test_step_chain_equals_scan(act):
-    B, L, D, N = 3, 40, 70, 16
-    x = _inputs(B, L, D, N, act, seed=11)
+STEP_SHAPES = [
+    # B, L, D, N, act, gate
+    (3, 40, 70, 16, "f32", True),    # D*4 not a multiple of 16: generic scan and step
+    (3, 40, 70, 16, "bf16", True),
+    (2, 45, 64, 16, "f32", True),    # TMA scan and the dedicated step kernel
+    (3, 33, 200, 16, "bf16", True),  # ragged channel tile
+    (2, 37, 32, 8, "f32", False),    # two lanes per channel, no gate
+    (2, 30, 64, 8, "bf16", True),
+    (3, 29, 24, 4, "f32", True),     # one lane per channel
+]
+
+
+@pytest.mark.parametrize("B,L,D,N,act,gate", STEP_SHAPES)
+def test_step_chain_equals_scan(B, L, D, N, act, gate):
+    x = _inputs(B, L, D, N, act, seed=11, z=gate)
     xd = to_dev(x)
     out_scan, h_scan, _ = s6.ssm_scan_fwd(*[xd[k] for k in ARGS], xd["h0"])
     h = xd["h0"].clone()
     outs = []
     for t in range(L):
-        sl = {k: xd[k][:, t].contiguous() for k in ("u", "delta_raw", "z", "Bm", "Cm")}
+        sl = {k: (xd[k][:, t].contiguous() if xd[k] is not None else None)
+              for k in ("u", "delta_raw", "z", "Bm", "Cm")}
         outs.append(s6.ssm_step(sl["u"], sl["delta_raw"], sl["z"], sl["Bm"], sl["Cm"],
                                 xd["A_log"], xd["Dp"], xd["delta_bias"], h))
     out_step = torch.stack(outs, dim=1)
