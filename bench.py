@@ -88,6 +88,75 @@ def algorithmic_bytes(B, L, D, N, e, chunk):
     return fwd, bwd
 
 
+def time_step(dev, reps=50, rounds=5):
+    """The decode step (ssm_step) on the decode workload's shape (B=256,
+    D=1536, N=16, f32), each step on a cold L2: CUDA graphs of `reps` x
+    (256 MB write + step) and of `reps` x (256 MB write) are replayed and the
+    step time is their difference.  Also the L2-resident time (graph of
+    chained steps only; h is 25 MB, smaller than L2)."""
+    from selective_state_space_s6_gb300 import s6
+
+    w = inputs.WORKLOADS["decode"]
+    B, D, N = w.batch, w.dim, w.dstate
+    e = 2 if w.act == "bf16" else 4
+    x = inputs.make_inputs(B, 1, D, N, w.act, seed=0, h0_std=0.5)
+    x = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    sl = {k: x[k][:, 0].contiguous() for k in ("u", "delta_raw", "z", "Bm", "Cm")}
+    h = x["h0"].clone()
+    out = torch.empty_like(sl["u"])
+    scratch = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        s6.ssm_step(sl["u"], sl["delta_raw"], sl["z"], sl["Bm"], sl["Cm"], x["A_log"], x["Dp"],
+                    x["delta_bias"], h, out=out)
+
+    def flush():
+        scratch.fill_(1)
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            flush()
+            step()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+
+    def capture(body):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                body()
+        return g
+
+    g_fs = capture(lambda: (flush(), step()))
+    g_f = capture(flush)
+    g_s = capture(step)
+
+    def replay_ms(g):
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(rounds):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / (rounds * reps)
+
+    t_fs, t_f, t_s = replay_ms(g_fs), replay_ms(g_f), replay_ms(g_s)
+    us_cold = (t_fs - t_f) * 1e3
+    nbytes = B * D * N * 4 * 2 + 4 * B * D * e + 2 * B * N * e + D * N * 4 + 2 * D * 4
+    peak, kind = load_peaks()
+    gbs = nbytes / (us_cold * 1e-6) / 1e9
+    return {"workload": f"decode: {w.description}", "us_per_step": round(us_cold, 2),
+            "us_per_step_l2_resident": round(t_s * 1e3, 2), "algorithmic_bytes": nbytes,
+            "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),
+            "timing": f"CUDA graphs of {reps} steps; cold L2 = (write 256 MB + step) - (write 256 MB)"}
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -182,20 +251,23 @@ def max_over_ranks(x: float, world: int) -> float:
 
 # ------------------------------------------------------------------ oracle (CPU baseline)
 
-def oracle_sample(w, seqlen, rank=0, threads=None):
-    """A bounded sample of the workload for the oracle: batch 0, the first
-    64*threads channels, the first ``seqlen``
-    steps; same distributions as the full workload."""
+def oracle_sample(w, cells_target, rank=0, threads=None):
+    """A bounded sample of the workload for the oracle, about ``cells_target``
+    cells: whole sequences first, then more channels, then more batch rows
+    (the full workload if that is smaller); same distributions as the full
+    workload."""
     import oracle
     threads = threads or oracle.default_threads()
-    channels = min(w.dim, 64 * threads)
-    seqlen = max(1, min(seqlen, w.seqlen))
-    x = inputs.make_inputs(1, seqlen, channels, w.dstate, w.act, seed=rank,
-                           delta_lo=w.delta_lo, delta_hi=w.delta_hi)
+    B, L, D, N = w.batch, w.seqlen, w.dim, w.dstate
+    ch0 = min(D, 64 * threads)  # at least one 64-channel block per thread
+    nl = max(1, min(L, cells_target // (ch0 * N)))
+    nd = max(ch0, min(D, cells_target // (nl * N)))
+    nb = max(1, min(B, cells_target // (nl * nd * N)))
+    x = inputs.make_inputs(nb, nl, nd, N, w.act, seed=rank, delta_lo=w.delta_lo, delta_hi=w.delta_hi)
     x64 = {k: (oracle._f64(v) if v is not None else None) for k, v in x.items()}
-    cells = seqlen * channels * w.dstate
-    desc = (f"batch 0 of {w.batch}, channels 0..{channels - 1} of {w.dim}, "
-            f"steps 0..{seqlen - 1} of {w.seqlen}")
+    cells = nb * nl * nd * N
+    desc = (f"batch rows 0..{nb - 1} of {B}, channels 0..{nd - 1} of {D}, "
+            f"steps 0..{nl - 1} of {L}")
     return x64, cells, desc, threads
 
 
@@ -205,22 +277,24 @@ def oracle_step(x64, threads):
     oracle.bwd(*[x64[k] for k in ARGS], None, x64["dout"], None, threads=threads)
 
 
-def time_oracle(w, steps, warmup, target_s, rank=0):
+def time_oracle(w, steps, warmup, target_s, rank=0, min_total_s=0.0):
     """Oracle fwd+bwd throughput on a sample sized so that one step takes about
-    ``target_s`` seconds (calibrated on a 128-step sample first)."""
-    x64, cells, _, threads = oracle_sample(w, 128, rank)
+    ``target_s`` seconds (calibrated on a small sample first); with
+    ``min_total_s``, enough steps are timed to cover at least that much work."""
+    x64, cells, _, threads = oracle_sample(w, 64 * 128 * w.dstate * 16, rank)
     t0 = time.perf_counter()
     oracle_step(x64, threads)
-    per_step = (time.perf_counter() - t0) / 128
-    seqlen = int(max(128, min(w.seqlen, target_s / max(per_step, 1e-9))))
-    x64, cells, desc, threads = oracle_sample(w, seqlen, rank, threads)
+    per_cell = (time.perf_counter() - t0) / cells
+    x64, cells, desc, threads = oracle_sample(w, int(target_s / max(per_cell, 1e-15)), rank, threads)
     for _ in range(warmup):
         oracle_step(x64, threads)
+    est = cells * per_cell
+    steps = max(steps, int(-(-min_total_s // max(est, 1e-9))))
     t0 = time.perf_counter()
     for _ in range(steps):
         oracle_step(x64, threads)
     dt = (time.perf_counter() - t0) / max(steps, 1)
-    return cells / dt / 1e9, desc, threads, dt
+    return cells / dt / 1e9, desc, threads, dt, steps
 
 
 # ------------------------------------------------------------------ our arm
@@ -359,11 +433,13 @@ def run_ours(args, world, rank, local):
     per_kernel["s6_bwd_finalize (reduce_dbc + reduce_params)"] = {"ms": round(t_fin, 4)}
     fwd_seg, bwd_seg = s6.plan_segments(B, L, D, N, act)
 
+    step_line = time_step(dev) if not args.no_step else None
+
     cpu_base = None
     if rank == 0 and not args.no_cpu_baseline:
-        v, desc, threads, dt = time_oracle(w, steps=1, warmup=0, target_s=15.0)
+        v, desc, threads, dt, n = time_oracle(w, steps=1, warmup=0, target_s=15.0, min_total_s=10.0)
         cpu_base = {"value": round(v, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
-                    "sample": desc + f" ({dt:.1f} s per fwd+bwd)"}
+                    "sample": desc + f" ({dt:.1f} s per fwd+bwd, {n} timed)"}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -381,6 +457,7 @@ def run_ours(args, world, rank, local):
         "segments": {"fwd": fwd_seg, "bwd": bwd_seg},
         "roofline": roofline,
         "kernels": per_kernel,
+        "step": step_line,
         "cpu_baseline": cpu_base,
         "clocks": clk,
     }
@@ -416,7 +493,7 @@ def run_reference(args, world, rank):
     w = inputs.WORKLOADS[args.workload]
     # whole run within a few minutes: about 150 s of oracle work over all steps
     target = max(0.5, 150.0 / max(1, args.steps + args.warmup))
-    v, desc, threads, dt = time_oracle(w, steps=args.steps, warmup=args.warmup, target_s=target)
+    v, desc, threads, dt, _ = time_oracle(w, steps=args.steps, warmup=args.warmup, target_s=target)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -443,6 +520,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-step", action="store_true", help="skip the decode-step measurement")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     world, rank, local = dist_setup()
