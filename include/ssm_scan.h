@@ -86,6 +86,14 @@ int ssm_version(void);
  * error, else SSM_OK. */
 int ssm_check_device_status(void *stream);
 
+/* Self-test of the give-up path (no counterpart on the pages): enqueues on
+ * `stream` one tiny kernel whose single thread waits on an mbarrier that
+ * nothing arrives at; the bounded wait gives up after about 2 s and sets the
+ * timeout bit, so the next ssm_check_device_status() returns SSM_ERR_TIMEOUT
+ * (and clears it).  Nothing faults and the context stays usable.  Returns
+ * SSM_OK, or SSM_ERR_CUDA if the launch fails. */
+int ssm_selftest_wait_timeout(void *stream);
+
 /* Number of saved chunk states: ceil(seqlen / SSM_CHUNK_LEN); 0 for seqlen <= 0. */
 int64_t ssm_num_chunks(int64_t seqlen);
 

@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "s6_internal.cuh"
+#include "s6_tma.cuh"
 
 namespace s6 {
 
@@ -222,6 +223,19 @@ int report_error(int code, const char* fmt, ...) {
 
 }  // namespace s6
 
+// One thread waits on an mbarrier phase that nothing completes: the bounded
+// wait gives up after kWaitCycles and sets the timeout bit (self-test of the
+// give-up path used by every pipeline wait).
+__global__ void s6_selftest_wait_kernel(unsigned int* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    s6::mbar_init(&bar, 1);
+    s6::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) s6::mbar_wait(&bar, 0, status);
+}
+
 extern "C" {
 
 const char* ssm_status_string(int status) {
@@ -255,6 +269,14 @@ int ssm_check_device_status(void* stream) {
   if (v & s6::kStatusLayoutBit)
     return fail(SSM_ERR_INTERNAL, "a kernel found its shared memory misaligned for swizzled tiles (status 0x%x)", v);
   return SSM_OK;
+}
+
+int ssm_selftest_wait_timeout(void* stream) {
+  unsigned int* w = s6::device_status_word();
+  if (!w) return fail(SSM_ERR_CUDA, "cannot locate the device status word");
+  s6_selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(w);
+  const cudaError_t ce = cudaGetLastError();
+  return ce == cudaSuccess ? SSM_OK : cuda_fail(ce, "ssm_selftest_wait_timeout");
 }
 
 int64_t ssm_num_chunks(int64_t seqlen) {

@@ -71,6 +71,8 @@ def load_library():
         lib.ssm_scan_bwd_finalize.restype = ci
         lib.ssm_step.argtypes = [i64] * 3 + [ci] + [vp] * 10 + [vp]
         lib.ssm_step.restype = ci
+        lib.ssm_selftest_wait_timeout.argtypes = [vp]
+        lib.ssm_selftest_wait_timeout.restype = ci
         lib.ssm_plan_segments.argtypes = [i64] * 4 + [ci, ctypes.POINTER(ci), ctypes.POINTER(ci)]
         lib.ssm_plan_segments.restype = ci
         _lib = lib
@@ -243,6 +245,12 @@ def ssm_step(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h, *, out=None, str
                                  _stream(stream))
     _check("ssm_step", rc)
     return out
+
+
+def selftest_wait_timeout(stream=None):
+    """Enqueue the library's give-up self-test (a bounded wait that runs out
+    after ~2 s); the next check_device_status() raises with SSM_ERR_TIMEOUT."""
+    _check("ssm_selftest_wait_timeout", load_library().ssm_selftest_wait_timeout(_stream(stream)))
 
 
 def check_device_status(stream=None):
