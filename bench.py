@@ -368,37 +368,100 @@ def run_ours(args, world, rank, local):
     cells = w.cells
     value = world * cells / (ms_step * 1e-3) / 1e9
 
-    # ---- e2e: pinned host inputs -> device -> fwd + bwd -> results back to pinned host
+    # ---- e2e: pinned host inputs -> device -> fwd + bwd -> results back to pinned host,
+    # every step.  Serial: one stream, copy in, compute, copy out.  Pipelined:
+    # three streams and two device buffer sets, so that the copy-in of step k+1
+    # and the copy-out of step k-1 run on the copy engines while step k computes.
     in_keys = ["u", "delta_raw", "z", "Bm", "Cm", "A_log", "Dp", "delta_bias", "dout"]
-    h_in = {k: x_cpu[k].pin_memory() for k in in_keys}
     out_keys = ["du", "d_delta_raw", "dz", "dBm", "dCm", "dA_log", "dD", "d_delta_bias"]
-    h_out = {k: torch.empty(g[k].shape, dtype=g[k].dtype, pin_memory=True) for k in out_keys}
-    h_out["out"] = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h_in = {k: x_cpu[k].pin_memory() for k in in_keys}
+
+    def host_outputs():
+        h = {k: torch.empty(g[k].shape, dtype=g[k].dtype, pin_memory=True) for k in out_keys}
+        h["out"] = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        return h
+
+    h_out = [host_outputs(), host_outputs()]
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0].values())
 
-    def e2e_step():
+    def device_set(first):
+        if first:
+            return {"x": x, "g": g, "out": out, "cs": cs, "ws": ws, "h_last": h_last}
+        return {"x": {k: (torch.empty_like(v) if isinstance(v, torch.Tensor) else v) for k, v in x.items()},
+                "g": {k: (torch.empty_like(v) if isinstance(v, torch.Tensor) else v) for k, v in g.items()},
+                "out": torch.empty_like(out), "cs": torch.empty_like(cs), "ws": torch.empty_like(ws),
+                "h_last": torch.empty_like(h_last)}
+
+    sets = [device_set(True), device_set(False)]
+
+    def compute(S, st):
+        xs = S["x"]
+        s6.ssm_scan_fwd(*[xs[k] for k in ARGS], None, out=S["out"], h_last=S["h_last"],
+                        chunk_states=S["cs"], ws=S["ws"], stream=st)
+        s6.bwd_partials(*[xs[k] for k in ARGS], S["cs"], xs["dout"], None, S["g"], S["ws"], st)
+        s6.bwd_finalize(B, L, D, N, act, S["g"], S["ws"], st)
+
+    def copy_in(S):
         for k in in_keys:
-            x[k].copy_(h_in[k], non_blocking=True)
-        fwd(); bwd_partials(); bwd_finalize()
-        h_out["out"].copy_(out, non_blocking=True)
-        for k in out_keys:
-            h_out[k].copy_(g[k], non_blocking=True)
+            S["x"][k].copy_(h_in[k], non_blocking=True)
 
-    for _ in range(max(1, min(args.warmup, 2))):
-        e2e_step()
+    def copy_out(S, H):
+        H["out"].copy_(S["out"], non_blocking=True)
+        for k in out_keys:
+            H[k].copy_(S["g"][k], non_blocking=True)
+
+    def serial_step():
+        copy_in(sets[0])
+        compute(sets[0], stream)
+        copy_out(sets[0], h_out[0])
+
+    s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev_in, ev_cmp, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+
+    def pipelined_step(k):
+        i = k % 2
+        S = sets[i]
+        with torch.cuda.stream(s_in):
+            if k >= 2:
+                s_in.wait_event(ev_cmp[i])  # step k-2 has finished reading set i
+            copy_in(S)
+            ev_in[i].record(s_in)
+        s_cmp.wait_event(ev_in[i])
+        if k >= 2:
+            s_cmp.wait_event(ev_out[i])  # step k-2's results have left set i
+        compute(S, s_cmp)
+        ev_cmp[i].record(s_cmp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_cmp[i])
+            copy_out(S, h_out[i])
+            ev_out[i].record(s_out)
+
+    def timed(run, nsteps, first_stream, last_stream):
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(first_stream)
+        for k in range(nsteps):
+            run(k)
+        e1.record(last_stream)
+        torch.cuda.synchronize(dev)
+        return max_over_ranks(e0.elapsed_time(e1) / nsteps, world)
+
+    for k in range(max(2, min(args.warmup, 4))):
+        serial_step()
     torch.cuda.synchronize(dev)
-    ke = max(1, min(K, args.e2e_steps))
-    barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(ke):
-        e2e_step()
-    e1.record(stream)
+    s_in.wait_stream(stream)
+    for k in range(max(2, min(args.warmup, 4))):
+        pipelined_step(k)
     torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / ke, world)
+    ke = max(2, args.e2e_steps)
+    serial_ms = timed(lambda k: serial_step(), ke, stream, stream)
+    s_in.wait_stream(stream)
+    e2e_ms = timed(pipelined_step, ke, s_in, s_out)
     e2e_value = world * cells / (e2e_ms * 1e-3) / 1e9
+    serial_value = world * cells / (serial_ms * 1e-3) / 1e9
 
     # ---- roofline of the dominant kernel (the backward scan), live event timing.
     # The scans are bound by instruction issue on the FP32/SFU pipes, not by
@@ -452,7 +515,10 @@ def run_ours(args, world, rank, local):
                          f"[B,L,D] inputs, larger than the 129 MB L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "steps": ke,
+                "overlap": "copy-in of step k+1 and copy-out of step k-1 overlap step k "
+                           "(three streams, two device buffer sets)",
+                "serial": {"value": round(serial_value, 2), "ms_per_step": round(serial_ms, 4)}},
         "gpu_launches": launches_per_step(fwd_seg, bwd_seg) * K,
         "segments": {"fwd": fwd_seg, "bwd": bwd_seg},
         "roofline": roofline,
@@ -518,7 +584,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(inputs.WORKLOADS))
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-step", action="store_true", help="skip the decode-step measurement")
     args = ap.parse_args(argv)
