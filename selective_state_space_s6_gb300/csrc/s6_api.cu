@@ -96,8 +96,9 @@ int check_ws(const void* ws, size_t ws_bytes, int64_t total) {
   return SSM_OK;
 }
 
-// The segment plan of the forward is a function of the shape only (it
-// targets a 152-SM GB300), so workspace sizes never depend on the device.
+// The forward's segment plan and the backward's work plan are functions of
+// the shape only (they target a 152-SM GB300), so workspace sizes and results
+// never depend on the device.
 constexpr int kPlanSms = 152;
 
 struct FwdWorkspace {
@@ -122,18 +123,15 @@ FwdWorkspace fwd_ws_layout(int64_t B, int64_t L, int64_t D, int64_t N) {
 }
 
 struct BwdWorkspace {
-  int nseg, seg_len;
-  int64_t dbc_off, dbc_bytes, param_off, param_bytes, agg_off, carry_off, total;
+  s6::BwdPlan plan;
+  int nseg;
+  int64_t dbc_off, dbc_bytes, param_off, param_bytes, agg_off, carry_off, flag_off, total;
 };
 
 BwdWorkspace bwd_ws_layout(int64_t B, int64_t L, int64_t D, int64_t N) {
   BwdWorkspace w;
-  w.nseg = s6::bwd_segments((int)B, (int)L, (int)D, (int)N, kPlanSms);
-  w.seg_len = (int)(L > 0 ? ssm_num_chunks(L) * SSM_CHUNK_LEN : 0);
-  if (w.nseg > 1) {
-    w.seg_len = (int)(((L + w.nseg - 1) / w.nseg + SSM_CHUNK_LEN - 1) / SSM_CHUNK_LEN * SSM_CHUNK_LEN);
-    w.nseg = (int)((L + w.seg_len - 1) / w.seg_len);
-  }
+  w.plan = s6::bwd_plan((int)B, (int)L, (int)D, (int)N, kPlanSms);
+  w.nseg = w.plan.maxp;
   const int64_t ndt = (D + s6::kDTile - 1) / s6::kDTile;
   w.dbc_off = 0;
   w.dbc_bytes = ndt * B * L * 2 * N * (int64_t)sizeof(float);
@@ -142,7 +140,10 @@ BwdWorkspace bwd_ws_layout(int64_t B, int64_t L, int64_t D, int64_t N) {
   w.agg_off = align_up(w.param_off + w.param_bytes, 256);
   const int64_t cells = w.nseg > 1 ? B * w.nseg * D * N : 0;
   w.carry_off = align_up(w.agg_off + cells * 2 * (int64_t)sizeof(float), 256);
-  w.total = align_up(w.carry_off + cells * (int64_t)sizeof(float), 256);
+  // one hand-over flag per (batch, channel tile) sequence
+  const int64_t nseq = w.nseg > 1 ? B * (int64_t)w.plan.ndt : 0;
+  w.flag_off = align_up(w.carry_off + cells * (int64_t)sizeof(float), 256);
+  w.total = align_up(w.flag_off + nseq * (int64_t)sizeof(int), 256);
   return w;
 }
 
@@ -361,10 +362,11 @@ int ssm_scan_bwd_partials(int64_t batch, int64_t seqlen, int64_t dim, int64_t ds
   p.status = s6::device_status_word();
   if (!p.status) return fail(SSM_ERR_CUDA, "cannot locate the device status word");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  p.plan = w.plan;
   p.nseg = w.nseg;
-  p.seg_len = w.seg_len;
   p.seg_agg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.agg_off);
   p.seg_carry = reinterpret_cast<float*>(static_cast<char*>(ws) + w.carry_off);
+  p.seq_flag = w.nseg > 1 ? reinterpret_cast<int*>(static_cast<char*>(ws) + w.flag_off) : nullptr;
   cudaError_t ce;
   if (L > 0 && s6::bwd_tma_supported(p, act)) {
     ce = s6::launch_bwd_tma(p, act, st);

@@ -168,14 +168,13 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
     return;
   }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.y, d0 = blockIdx.x * kDTile;
   const int L = p.L, D = p.D;
   const int nchunks = p.nchunks;
-  // this CTA's time segment: chunks [c_lo, c_hi)
-  const int seg = blockIdx.z;
-  const int cps = p.seg_len / kChunk;
-  const int c_lo = seg * cps;
-  const int c_hi = min(nchunks, c_lo + cps);
+  // this CTA's range of chunk units; every role walks its pieces in unit
+  // order: piece = sequence sq (batch sq / ndt, channel tile sq % ndt),
+  // chunks [c_lo, c_hi)
+  const BwdPlan& pl = p.plan;
+  const long long u_begin = plan_bound(pl, blockIdx.x), u_end = plan_bound(pl, blockIdx.x + 1);
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -205,15 +204,24 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   auto tile_C = [&](int s) { return stages + (size_t)s * kStageElems + 4 * kTile + kBC; };
 
   // activation tile: AT::kNBox boxes of AT::kChBox channels side by side
-  auto load_act = [&](Act* dst, const CUtensorMap* m, uint64_t* bar, int row) {
+  auto load_act = [&](Act* dst, const CUtensorMap* m, uint64_t* bar, int d0, int row) {
 #pragma unroll
     for (int bx = 0; bx < AT::kNBox; ++bx)
       tma_load_2d(reinterpret_cast<unsigned char*>(dst) + bx * AT::kBoxBytes, m, bar, d0 + bx * AT::kChBox, row);
   };
 
-  // The item sequence every role walks: for chunk c = last..first of the
-  // segment, with ntl tiles: pass A tiles 0..ntl-1, then pass B tiles ntl-1..0.
+  // The item sequence every role walks: for each piece, for chunk c =
+  // last..first of the piece, with ntl tiles: pass A tiles 0..ntl-1, then
+  // pass B tiles ntl-1..0.
   auto chunk_tiles = [&](int c) { return (min(kChunk, L - c * kChunk) + kTT - 1) / kTT; };
+  auto piece_at = [&](long long u, int& b, int& d0, int& c_lo, int& c_hi, long long& next) {
+    const long long sq = u / pl.nch, S0 = sq * pl.nch;
+    next = min(S0 + pl.nch, u_end);
+    b = (int)(sq / pl.ndt);
+    d0 = (int)(sq % pl.ndt) * kDTile;
+    c_lo = (int)(u - S0);
+    c_hi = (int)(next - S0);
+  };
 
   if (warp == kCW) {
     // ---------------- producer
@@ -228,26 +236,30 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
       const uint32_t bytesB = (uint32_t)(((kGate ? 4 : 3) * kTile + 2 * kBC) * sizeof(Act));
       int item = 0;
       bool ok = true;
-      for (int c = c_hi - 1; c >= c_lo && ok; --c) {
-        const int ntl = chunk_tiles(c);
-        for (int it = 0; it < 2 * ntl; ++it, ++item) {
-          const bool passA = it < ntl;
-          const int j = passA ? it : 2 * ntl - 1 - it;
-          const int s = item % S;
-          const uint32_t use = (uint32_t)(item / S);
-          if (item >= S && !mbar_wait(&empty[s], (use - 1) & 1, p.status)) {
-            ok = false;
-            break;
-          }
-          const int row = b * L + c * kChunk + j * kTT;
-          mbar_arrive_expect_tx(&full[s], passA ? bytesA : bytesB);
-          load_act(tile_u(s), &P.map_u, &full[s], row);
-          load_act(tile_raw(s), &P.map_raw, &full[s], row);
-          tma_load_2d(tile_B(s), &P.map_B, &full[s], 0, row);
-          if (!passA) {
-            if (kGate) load_act(tile_z(s), &P.map_z, &full[s], row);
-            load_act(tile_g(s), &P.map_dout, &full[s], row);
-            tma_load_2d(tile_C(s), &P.map_C, &full[s], 0, row);
+      for (long long u = u_begin, next; u < u_end && ok; u = next) {
+        int b, d0, c_lo, c_hi;
+        piece_at(u, b, d0, c_lo, c_hi, next);
+        for (int c = c_hi - 1; c >= c_lo && ok; --c) {
+          const int ntl = chunk_tiles(c);
+          for (int it = 0; it < 2 * ntl; ++it, ++item) {
+            const bool passA = it < ntl;
+            const int j = passA ? it : 2 * ntl - 1 - it;
+            const int s = item % S;
+            const uint32_t use = (uint32_t)(item / S);
+            if (item >= S && !mbar_wait(&empty[s], (use - 1) & 1, p.status)) {
+              ok = false;
+              break;
+            }
+            const int row = b * L + c * kChunk + j * kTT;
+            mbar_arrive_expect_tx(&full[s], passA ? bytesA : bytesB);
+            load_act(tile_u(s), &P.map_u, &full[s], d0, row);
+            load_act(tile_raw(s), &P.map_raw, &full[s], d0, row);
+            tma_load_2d(tile_B(s), &P.map_B, &full[s], 0, row);
+            if (!passA) {
+              if (kGate) load_act(tile_z(s), &P.map_z, &full[s], d0, row);
+              load_act(tile_g(s), &P.map_dout, &full[s], d0, row);
+              tma_load_2d(tile_C(s), &P.map_C, &full[s], 0, row);
+            }
           }
         }
       }
@@ -264,21 +276,25 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
     if (kBf16) {
       int item = 0;
       bool ok = true;
-      for (int c = c_hi - 1; c >= c_lo; --c) {
-        const int ntl = chunk_tiles(c);
-        for (int it = 0; it < 2 * ntl; ++it, ++item) {
-          const bool passA = it < ntl;
-          const int s = item % S;
-          if (ok) ok = mbar_wait(&full[s], (uint32_t)(item / S) & 1, p.status);
-          const __nv_bfloat162* tb = reinterpret_cast<const __nv_bfloat162*>(tile_B(s));
-          const __nv_bfloat162* tc = reinterpret_cast<const __nv_bfloat162*>(tile_C(s));
-          float* dst = bcf + (size_t)s * kTT * 2 * N;
-          for (int e = lane; e < kBC / 2; e += 32) {
-            const int t = (2 * e) / N, n = (2 * e) % N;
-            *reinterpret_cast<float2*>(dst + (t * 2 + 0) * N + n) = __bfloat1622float2(tb[e]);
-            if (!passA) *reinterpret_cast<float2*>(dst + (t * 2 + 1) * N + n) = __bfloat1622float2(tc[e]);
+      for (long long u = u_begin, next; u < u_end; u = next) {
+        int b, d0, c_lo, c_hi;
+        piece_at(u, b, d0, c_lo, c_hi, next);
+        for (int c = c_hi - 1; c >= c_lo; --c) {
+          const int ntl = chunk_tiles(c);
+          for (int it = 0; it < 2 * ntl; ++it, ++item) {
+            const bool passA = it < ntl;
+            const int s = item % S;
+            if (ok) ok = mbar_wait(&full[s], (uint32_t)(item / S) & 1, p.status);
+            const __nv_bfloat162* tb = reinterpret_cast<const __nv_bfloat162*>(tile_B(s));
+            const __nv_bfloat162* tc = reinterpret_cast<const __nv_bfloat162*>(tile_C(s));
+            float* dst = bcf + (size_t)s * kTT * 2 * N;
+            for (int e = lane; e < kBC / 2; e += 32) {
+              const int t = (2 * e) / N, n = (2 * e) % N;
+              *reinterpret_cast<float2*>(dst + (t * 2 + 0) * N + n) = __bfloat1622float2(tb[e]);
+              if (!passA) *reinterpret_cast<float2*>(dst + (t * 2 + 1) * N + n) = __bfloat1622float2(tc[e]);
+            }
+            mbar_arrive(&conv[s]);
           }
-          mbar_arrive(&conv[s]);
         }
       }
     }
@@ -288,29 +304,33 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   if (warp == kCW + 2) {
     // ---------------- reducer: cross-warp sums of each sub-chunk's dBm/dCm
     // partials (fixed warp order) -> this CTA's partial row in ws_dbc
-    float* ws_dbc_r = p.ws_dbc + ((size_t)blockIdx.x * p.B + b) * (size_t)L * 2 * N;
     int n = 0;
     bool ok = true;
-    for (int c = c_hi - 1; c >= c_lo; --c) {
-      const int clen = min(kChunk, L - c * kChunk);
-      for (int j = chunk_tiles(c) - 1; j >= 0; --j) {
-        const int cnt = min(kTT, clen - j * kTT);
-        for (int sc = (cnt + kSub - 1) / kSub - 1; sc >= 0; --sc, ++n) {
-          const int cnt8 = min(kSub, cnt - sc * kSub);
-          const int slot = n & 1;
-          if (ok) ok = mbar_wait(&wfull[slot], (uint32_t)(n >> 1) & 1, p.status);
-          const float* wp = wpart + slot * (kSub * kCW * 32);
-          float* dst = ws_dbc_r + (size_t)(c * kChunk + j * kTT + sc * kSub) * 2 * N;
-          for (int idx = lane; idx < cnt8 * 2 * N; idx += 32) {
-            const int k = idx / (2 * N), o = idx % (2 * N);
-            const float* src = wp + k * kCW * 32 + o;
-            float v = src[0];
+    for (long long u = u_begin, next; u < u_end; u = next) {
+      int b, d0, c_lo, c_hi;
+      piece_at(u, b, d0, c_lo, c_hi, next);
+      float* ws_dbc_r = p.ws_dbc + ((size_t)(d0 / kDTile) * p.B + b) * (size_t)L * 2 * N;
+      for (int c = c_hi - 1; c >= c_lo; --c) {
+        const int clen = min(kChunk, L - c * kChunk);
+        for (int j = chunk_tiles(c) - 1; j >= 0; --j) {
+          const int cnt = min(kTT, clen - j * kTT);
+          for (int sc = (cnt + kSub - 1) / kSub - 1; sc >= 0; --sc, ++n) {
+            const int cnt8 = min(kSub, cnt - sc * kSub);
+            const int slot = n & 1;
+            if (ok) ok = mbar_wait(&wfull[slot], (uint32_t)(n >> 1) & 1, p.status);
+            const float* wp = wpart + slot * (kSub * kCW * 32);
+            float* dst = ws_dbc_r + (size_t)(c * kChunk + j * kTT + sc * kSub) * 2 * N;
+            for (int idx = lane; idx < cnt8 * 2 * N; idx += 32) {
+              const int k = idx / (2 * N), o = idx % (2 * N);
+              const float* src = wp + k * kCW * 32 + o;
+              float v = src[0];
 #pragma unroll
-            for (int w = 1; w < kCW; ++w) v += src[w * 32];
-            dst[idx] = v;
+              for (int w = 1; w < kCW; ++w) v += src[w * 32];
+              dst[idx] = v;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&wempty[slot]);
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&wempty[slot]);
         }
       }
     }
@@ -319,10 +339,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
 
   // ---------------- consumers
   const int q = tid % TPC;   // state group: states 4q .. 4q+3
-  const int cl = tid / TPC;  // channel within the CTA
-  const int d = d0 + cl;
-  const bool dvalid = d < D;
-  const int dc = dvalid ? d : D - 1;
+  const int cl = tid / TPC;  // channel within the tile
   // Lane q owns the steps k with k % TPC == q (row % 8 of owned step i of an
   // 8-step group is i*TPC + q): byte offsets of this lane's channel in those
   // rows of a swizzled tile.
@@ -333,32 +350,10 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   // A2 = A*log2(e) on the fast path (2^x decays), A itself otherwise; sums
   // weighted by A are taken with A2 and scaled by kAscale = A / A2 at the end.
   constexpr float kAscale = kFast ? kLn2 : 1.f;
-  float2 A2[2], carry[2];
-  {
-    const float* cin = p.nseg > 1 ? p.seg_carry + (((size_t)b * p.nseg + seg) * D + dc) * N
-                                  : (p.dh_last ? p.dh_last + ((size_t)b * D + dc) * N : nullptr);
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int n = 4 * q + 2 * i;
-      const float a0 = -expf(p.A_log[dc * N + n]);
-      const float a1 = -expf(p.A_log[dc * N + n + 1]);
-      A2[i] = kFast ? make_float2(a0 * kLog2e, a1 * kLog2e) : make_float2(a0, a1);
-      // adjoint carry entering this segment's last step: dh_last for the last
-      // segment, the composed carry of the segments to the right otherwise
-      carry[i] = (cin && dvalid) ? make_float2(cin[n], cin[n + 1]) : make_float2(0.f, 0.f);
-    }
-  }
-  const float bias = p.delta_bias[dc];
-  const float Dd = p.Dp[dc];
   // this warp's TMEM region: column 32*j + 4*k + i = state i of step 8*j + k of the chunk
   const uint32_t tm = *tmem_slot + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((warp >> 2) * 256);
   float* my_tot = tot + tid * 6;               // running totals: 4 states, dDp, d_delta_bias
   float* my_cmp = tot + kLanes * 6 + tid * 6;  // Kahan compensation
-#pragma unroll
-  for (int i = 0; i < 6; ++i) {
-    my_tot[i] = 0.f;
-    my_cmp[i] = 0.f;
-  }
 
   // warp-local reducer role: output pair op = lane % N (term r_q, states r_n,
   // r_n + 1 of the channel), group r_g = lane / N of 4 channels
@@ -367,14 +362,51 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   const int r_src = r_n / 4, r_j = r_n % 4;  // owning lane-in-channel and index in its chunk
   float* my_redw = redw + warp * kRedSlots * kRedSlot;
 
-  Act* dup = static_cast<Act*>(p.du) + (size_t)b * L * D + d;
-  Act* drp = static_cast<Act*>(p.d_delta_raw) + (size_t)b * L * D + d;
-  Act* dzp = kGate ? static_cast<Act*>(p.dz) + (size_t)b * L * D + d : nullptr;
-
   bool failed = false;
   int s = 0;         // ring stage of the current item
   uint32_t par = 0;  // its phase parity
   int nsub_done = 0;  // sub-chunks handed to the reducer so far
+  for (long long u = u_begin, next; u < u_end; u = next) {
+  int b, d0, c_lo, c_hi;
+  piece_at(u, b, d0, c_lo, c_hi, next);
+  // piece index in time order within its sequence, and whether it ends the sequence
+  const int kp = c_lo == 0 ? 0 : (int)(plan_count_le(pl, u) - plan_count_le(pl, u - c_lo));
+  const bool last_piece = c_hi == pl.nch;
+  const int d = d0 + cl;
+  const bool dvalid = d < D;
+  const int dc = dvalid ? d : D - 1;
+  const long long sq = (u - c_lo) / pl.nch;  // sequence index
+  if (!last_piece && p.seq_flag) {
+    // hand-over mode: the carry comes from the CTA walking the sequence's last piece
+    if (lane == 0 && !failed) failed = !flag_wait(p.seq_flag + sq, p.status);
+    failed = __shfl_sync(0xffffffffu, failed, 0);
+    __syncwarp();
+  }
+  float2 A2[2], carry[2];
+  {
+    const float* cin = !last_piece ? p.seg_carry + (((size_t)b * p.nseg + kp) * D + dc) * N
+                                   : (p.dh_last ? p.dh_last + ((size_t)b * D + dc) * N : nullptr);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int n = 4 * q + 2 * i;
+      const float a0 = -expf(p.A_log[dc * N + n]);
+      const float a1 = -expf(p.A_log[dc * N + n + 1]);
+      A2[i] = kFast ? make_float2(a0 * kLog2e, a1 * kLog2e) : make_float2(a0, a1);
+      // adjoint carry entering the piece's last step: dh_last for the last
+      // piece of the sequence, the composed carry of the pieces after it otherwise
+      carry[i] = (cin && dvalid) ? make_float2(__ldcg(cin + n), __ldcg(cin + n + 1)) : make_float2(0.f, 0.f);
+    }
+  }
+  const float bias = p.delta_bias[dc];
+  const float Dd = p.Dp[dc];
+#pragma unroll
+  for (int i = 0; i < 6; ++i) {
+    my_tot[i] = 0.f;
+    my_cmp[i] = 0.f;
+  }
+  Act* dup = static_cast<Act*>(p.du) + (size_t)b * L * D + d;
+  Act* drp = static_cast<Act*>(p.d_delta_raw) + (size_t)b * L * D + d;
+  Act* dzp = kGate ? static_cast<Act*>(p.dz) + (size_t)b * L * D + d : nullptr;
   for (int c = c_hi - 1; c >= c_lo; --c) {
     const int t0 = c * kChunk;
     const int clen = min(kChunk, L - t0);
@@ -621,7 +653,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
     kahan_add(my_tot[4], my_cmp[4], accD);
     kahan_add(my_tot[5], my_cmp[5], accBias);
   }
-  // ---------------- per-(batch, segment) parameter partials and dh0
+  // ---------------- the piece's parameter partials (row b * nseg + kp) and dh0
   {
     // dDp and d_delta_bias: each lane summed its owned steps; add the channel's TPC lanes
     float tD = my_tot[4], tBs = my_tot[5];
@@ -631,20 +663,43 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
       tBs += __shfl_xor_sync(0xffffffffu, tBs, m);
     }
     if (dvalid) {
-      float* wp = p.ws_param + (((size_t)b * p.nseg + seg) * D + d) * (N + 2);
+      float* wp = p.ws_param + (((size_t)b * p.nseg + kp) * D + d) * (N + 2);
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int n = 4 * q + 2 * i;
         wp[n] = (A2[i].x * kAscale) * my_tot[2 * i];
         wp[n + 1] = (A2[i].y * kAscale) * my_tot[2 * i + 1];
-        if (p.dh0 && seg == 0) *reinterpret_cast<float2*>(p.dh0 + ((size_t)b * D + d) * N + n) = carry[i];
+        if (p.dh0 && c_lo == 0) *reinterpret_cast<float2*>(p.dh0 + ((size_t)b * D + d) * N + n) = carry[i];
       }
       if (q == 0) {
         wp[N] = tD;
         wp[N + 1] = tBs;
       }
+      if (p.seq_flag) {
+        // rows of pieces this sequence does not have stay zero for the finalize
+        for (int k2 = plan_pieces(pl, sq); k2 < p.nseg; ++k2) {
+          float* wz = p.ws_param + (((size_t)b * p.nseg + k2) * D + d) * (N + 2);
+          wz[4 * q] = wz[4 * q + 1] = wz[4 * q + 2] = wz[4 * q + 3] = 0.f;
+          if (q == 0) wz[N] = wz[N + 1] = 0.f;
+        }
+      }
+    }
+    if (p.seq_flag && kp > 0) {
+      // hand-over mode, the sequence's last piece: its final carry enters the
+      // first piece's last step; publish it and raise the flag
+      if (dvalid) {
+        float* co = p.seg_carry + (((size_t)b * p.nseg + kp - 1) * D + d) * N + 4 * q;
+        __stcg(co, carry[0].x);
+        __stcg(co + 1, carry[0].y);
+        __stcg(co + 2, carry[1].x);
+        __stcg(co + 3, carry[1].y);
+      }
+      __threadfence();
+      named_bar_sync(2, kLanes);
+      if (tid == 0) st_release_gpu(p.seq_flag + sq, 1);
     }
   }
+  }  // pieces
   // every consumer is done with TMEM (loads waited for inline, stores before
   // the loads of the same chunk): free it
   tmem_fence_before_sync();
@@ -698,9 +753,17 @@ __global__ void __launch_bounds__(kAggWarps * 32) s6_bwd_agg_kernel(const __grid
     return;
   }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.y, d0 = blockIdx.x * kCh, seg = blockIdx.z + 1;
+  // channels [d0, d0 + kValid) of the 64-channel tile d0 / kDTile (for
+  // TPC = 1 the CTA's 128 lanes cover the tile and the next one, whose
+  // lanes only load); piece seg >= 1 of the sequence (b, tile), if it has one
+  constexpr int kValid = kCh < kDTile ? kCh : kDTile;
+  const int b = blockIdx.y, d0 = blockIdx.x * kValid, seg = blockIdx.z + 1;
   const int L = p.L, D = p.D;
-  const int t_lo = seg * p.seg_len, t_hi = min(L, t_lo + p.seg_len);
+  const long long sq = (long long)b * p.plan.ndt + d0 / kDTile;
+  if (seg >= plan_pieces(p.plan, sq)) return;  // the whole CTA, before any barrier or copy
+  int c_lo, c_hi;
+  plan_piece_range(p.plan, sq, seg, c_lo, c_hi);
+  const int t_lo = c_lo * kChunk, t_hi = min(L, c_hi * kChunk);
   const int ntiles = (t_hi - t_lo + kTT - 1) / kTT;
 
   if (tid == 0) {
@@ -761,7 +824,7 @@ __global__ void __launch_bounds__(kAggWarps * 32) s6_bwd_agg_kernel(const __grid
 
   const int q = tid % TPC, cl = tid / TPC;
   const int d = d0 + cl;
-  const bool dvalid = d < D;
+  const bool dvalid = d < D && cl < kValid;
   const int dc = dvalid ? d : D - 1;
   float2 A2[2], carry[2];
 #pragma unroll
@@ -837,21 +900,30 @@ __global__ void __launch_bounds__(kAggWarps * 32) s6_bwd_agg_kernel(const __grid
   }
 }
 
-// Carry pass: per (b, d, n), from the last segment to the first,
-// seg_carry[s] = adjoint carry entering segment s's last step;
-// seg_carry[s-1] = carry_out_s + P_s * seg_carry[s].
+// Carry pass: per (b, d, n), over the K pieces of the sequence (b, d / 64)
+// from the last to the first: seg_carry[k] = adjoint carry entering piece
+// k's last step (dh_last, or 0, for the last piece); seg_carry[k - 1] =
+// carry_out_k + P_k * seg_carry[k].  Also zeroes the parameter-partial rows
+// k >= K of (b, d), which no piece writes.
 __global__ void s6_bwd_seg_carry_kernel(const BwdParams p) {
   const size_t per = (size_t)p.D * p.N;
   const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int b = blockIdx.y;
   if (e >= per) return;
+  const int d = (int)(e / p.N), n = (int)(e % p.N);
+  const int K = plan_pieces(p.plan, (long long)b * p.plan.ndt + d / kDTile);
   float chi = p.dh_last ? p.dh_last[(size_t)b * per + e] : 0.f;
-  for (int sg = p.nseg - 1; sg >= 0; --sg) {
-    p.seg_carry[((size_t)b * p.nseg + sg) * per + e] = chi;
-    if (sg > 0) {
-      const float* ag = p.seg_agg + (((size_t)b * p.nseg + sg) * per + e) * 2;
+  for (int k = K - 1; k >= 0; --k) {
+    p.seg_carry[((size_t)b * p.nseg + k) * per + e] = chi;
+    if (k > 0) {
+      const float* ag = p.seg_agg + (((size_t)b * p.nseg + k) * per + e) * 2;
       chi = fmaf(ag[0], chi, ag[1]);
     }
+  }
+  for (int k = K; k < p.nseg; ++k) {
+    float* wp = p.ws_param + (((size_t)b * p.nseg + k) * p.D + d) * (p.N + 2);
+    wp[n] = 0.f;
+    if (n < 2) wp[p.N + n] = 0.f;
   }
 }
 
@@ -870,7 +942,8 @@ cudaError_t launch_agg(const BwdTmaParams& P, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   constexpr int kCh = kScanThreads / TPC;
-  const dim3 grid((P.p.D + kCh - 1) / kCh, P.p.B, P.p.nseg - 1);
+  constexpr int kValid = kCh < kDTile ? kCh : kDTile;
+  const dim3 grid((P.p.D + kValid - 1) / kValid, P.p.B, P.p.nseg - 1);
   kern<<<grid, kAggWarps * 32, smem, stream>>>(P);
   return cudaGetLastError();
 }
@@ -923,21 +996,48 @@ size_t bwd_smem_bytes() {
 }
 
 template <typename Act, int TPC, bool kFast, bool kGate>
-cudaError_t launch_one(const BwdTmaParams& P, cudaStream_t stream) {
+cudaError_t launch_one(const BwdTmaParams& P, cudaStream_t stream, bool cooperative) {
   auto kern = s6_bwd_tma_kernel<Act, TPC, kFast, kGate>;
   const size_t smem = bwd_smem_bytes<Act, TPC>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((P.p.D + kDTile - 1) / kDTile, P.p.B, P.p.nseg);
-  kern<<<grid, (2 * TPC + 3) * 32, smem, stream>>>(P);
-  return cudaGetLastError();
+  // persistent: one CTA per range of the plan
+  if (!cooperative) {
+    kern<<<P.p.plan.P, (2 * TPC + 3) * 32, smem, stream>>>(P);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)P.p.plan.P);
+  cfg.blockDim = dim3((2 * TPC + 3) * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
 // TPC lanes per channel: 4 states per lane in both the main and the aggregate pass
 template <typename Act, int TPC, bool kFast>
-cudaError_t launch_tpc(const BwdTmaParams& P, const BwdTmaParams& Pagg, cudaStream_t stream) {
+cudaError_t launch_tpc(BwdTmaParams& P, BwdTmaParams& Pagg, cudaStream_t stream) {
+  const BwdPlan& pl = P.p.plan;
+  if (P.p.nseg > 1 && P.p.seq_flag && P.p.nseg == 2 && (long long)pl.nch <= pl.U / pl.P) {
+    // hand-over mode: every sequence in at most two pieces and no range
+    // shorter than a sequence, so the CTA holding a last piece (walked
+    // first) is done with it before the CTA holding the first piece (walked
+    // last) gets there; a cooperative launch keeps every CTA resident
+    cudaError_t e = cudaMemsetAsync(P.p.seq_flag, 0, sizeof(int) * (size_t)P.p.B * pl.ndt, stream);
+    if (e != cudaSuccess) return e;
+    e = P.p.z ? launch_one<Act, TPC, kFast, true>(P, stream, true) : launch_one<Act, TPC, kFast, false>(P, stream, true);
+    if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+    (void)cudaGetLastError();  // not resident at once on this GPU: aggregate mode
+  }
+  P.p.seq_flag = nullptr;
+  Pagg.p.seq_flag = nullptr;
   if (P.p.nseg > 1) {
-    // chunked parallel scan: adjoint segment aggregates -> carries -> all segments at once
+    // chunked parallel scan: adjoint piece aggregates -> carries -> all pieces at once
     // (Pagg's tensor maps have the aggregate pass's 128/TPC-channel boxes)
     cudaError_t e = P.p.z ? launch_agg<Act, TPC, kFast, true>(Pagg, stream) : launch_agg<Act, TPC, kFast, false>(Pagg, stream);
     if (e != cudaSuccess) return e;
@@ -946,42 +1046,32 @@ cudaError_t launch_tpc(const BwdTmaParams& P, const BwdTmaParams& Pagg, cudaStre
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  return P.p.z ? launch_one<Act, TPC, kFast, true>(P, stream) : launch_one<Act, TPC, kFast, false>(P, stream);
+  return P.p.z ? launch_one<Act, TPC, kFast, true>(P, stream, false) : launch_one<Act, TPC, kFast, false>(P, stream, false);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
 
-// Time segments (chunked parallel scan) split each (batch, 64-channel tile)
-// into nseg CTAs over consecutive ranges of chunks.  One CTA fits per SM, so
-// the grid runs in waves of `sms` CTAs; the plan minimises a model of the run
-// time in units of one CTA's full-length run:
-//   ceil(ctas * nseg / sms) * (longest segment / sequence)      (main pass)
-//   + kAggCost * (nseg - 1) / nseg * ctas / sms                  (aggregates)
-// where kAggCost is the aggregate pass's cost per step relative to the main
-// pass.  Segments are at least four chunks long; a plan must beat one
-// segment by 3% to be taken.
-int bwd_segments(int B, int L, int D, int N, int sms) {
-  if (!(N == 4 || N == 8 || N == 16) || L < 1024 || B <= 0 || D <= 0 || sms <= 0) return 1;
-  constexpr double kAggCost = 0.12;
-  const long ctas = (long)B * ((D + kDTile - 1) / kDTile);
-  const long nch = ((long)L + kChunk - 1) / kChunk;
-  auto waves = [&](long n) { return (double)((ctas * n + sms - 1) / sms); };
-  double best = waves(1);
-  int best_n = 1;
-  for (long n = 2; n <= 64 && nch / n >= 4; ++n) {
-    const long seg_ch = (nch + n - 1) / n;        // chunks per segment (the last may be shorter)
-    const long nseg = (nch + seg_ch - 1) / seg_ch;
-    if (nseg != n) continue;
-    const double t = waves(nseg) * (double)seg_ch / (double)nch +
-                     kAggCost * (double)(nseg - 1) / (double)nseg * (double)ctas / (double)sms;
-    if (t < 0.97 * best && t < 0.97 * waves(1)) {
-      best = t;
-      best_n = (int)nseg;
-    }
+// The work plan: sms ranges of equal length over all chunk units (one
+// persistent CTA per SM, no tail wave); sequences cut by a range boundary
+// get aggregates for their later pieces.  N outside {4, 8, 16} never takes
+// the TMA path: one piece per sequence.
+BwdPlan bwd_plan(int B, int L, int D, int N, int sms) {
+  BwdPlan pl;
+  pl.nch = L > 0 ? (L + kChunk - 1) / kChunk : 0;
+  pl.ndt = D > 0 ? (D + kDTile - 1) / kDTile : 0;
+  pl.U = (long long)(B > 0 ? B : 0) * pl.ndt * pl.nch;
+  pl.P = (int)std::max<long long>(1, std::min<long long>(std::max(sms, 1), pl.U));
+  pl.maxp = 1;
+  if (pl.U == 0 || !(N == 4 || N == 8 || N == 16)) {
+    pl.U = std::max<long long>(pl.U, 1);
+    pl.P = 1;
+    return pl;
   }
-  return best_n;
+  const long long nseq = (long long)B * pl.ndt;
+  for (long long sq = 0; sq < nseq; ++sq) pl.maxp = std::max(pl.maxp, plan_pieces(pl, sq));
+  return pl;
 }
 
 // Same shape rules as the TMA forward: N in {4, 8, 16}, N*e and D*e

@@ -45,6 +45,42 @@ struct FwdParams {
   int B, L, D, N, nchunks;
 };
 
+// Work plan of the TMA backward: the (batch, 64-channel tile) sequences,
+// each of nch chunks, are laid end to end as U = nseq * nch chunk units
+// (sequence s = b * ndt + j, unit s * nch + c) and cut into P equal ranges,
+// one per persistent CTA (range w = [bound(w), bound(w + 1)), bound(w) =
+// floor(w * U / P)).  A range covers pieces of one or more sequences; a
+// sequence cut by range boundaries has K > 1 pieces, numbered in time order.
+// Piece k > 0 needs the adjoint aggregate of the pieces after it (the chunked
+// parallel scan); piece k of sequence (b, j) owns row b * maxp + k of the
+// parameter partials.  The plan is a function of the shape only.
+struct BwdPlan {
+  long long U;  // chunk units
+  int P;        // worker CTAs (ranges), 1 <= P <= U
+  int nch;      // chunks per sequence
+  int ndt;      // 64-channel tiles
+  int maxp;     // most pieces any sequence has
+};
+
+__host__ __device__ inline long long plan_bound(const BwdPlan& pl, long long w) { return w * pl.U / pl.P; }
+// number of w in [0, P] with plan_bound(w) <= X, for 0 <= X < U
+__host__ __device__ inline long long plan_count_le(const BwdPlan& pl, long long X) {
+  return ((X + 1) * pl.P + pl.U - 1) / pl.U;
+}
+// pieces of sequence s
+__host__ __device__ inline int plan_pieces(const BwdPlan& pl, long long s) {
+  const long long S0 = s * pl.nch, S1 = S0 + pl.nch;
+  return (int)(plan_count_le(pl, S1 - 1) - plan_count_le(pl, S0)) + 1;
+}
+// chunk range [c_lo, c_hi) of piece k of sequence s
+__host__ __device__ inline void plan_piece_range(const BwdPlan& pl, long long s, int k, int& c_lo, int& c_hi) {
+  const long long S0 = s * pl.nch;
+  const long long wa = plan_count_le(pl, S0);  // first range boundary after the sequence start
+  const int K = plan_pieces(pl, s);
+  c_lo = k == 0 ? 0 : (int)(plan_bound(pl, wa + k - 1) - S0);
+  c_hi = k == K - 1 ? pl.nch : (int)(plan_bound(pl, wa + k) - S0);
+}
+
 struct BwdParams {
   const void* u;
   const void* delta_raw;
@@ -64,13 +100,20 @@ struct BwdParams {
   float* ws_dbc;    // [ndt][B][L][2][N] per-CTA sums of the dBm / dCm terms
   float* ws_param;  // [B][nseg][D][N+2] per-(batch, segment) sums: A*sum(...), dDp, d_delta_bias
   unsigned int* status;  // device status word (bounded waits report here)
-  // Time segments (chunked parallel scan, as in FwdParams): seg_len steps
-  // (a multiple of kChunk) each; seg_agg [B][nseg][D][N][2] holds each
-  // segment's decay product and zero-carry adjoint carry-out, seg_carry
-  // [B][nseg][D][N] the adjoint carry entering each segment's last step.
-  int seg_len, nseg;
+  // Pieces (chunked parallel scan): nseg = plan.maxp rows per batch;
+  // seg_agg [B][nseg][D][N][2] holds each piece's decay product and
+  // zero-carry adjoint carry-out, seg_carry [B][nseg][D][N] the adjoint carry
+  // entering each piece's last step.  The generic kernel uses row 0 only.
+  BwdPlan plan;
+  int nseg;
   float* seg_agg;
   float* seg_carry;
+  // Hand-over mode (cooperative launch, every sequence in at most two
+  // pieces): instead of aggregates, the CTA holding a sequence's last piece
+  // walks it first, writes the carry it ends with to seg_carry row 0 and
+  // raises seq_flag[sequence]; the CTA holding the first piece, which it
+  // walks last, waits for the flag.  nullptr = aggregate mode.
+  int* seq_flag;
   int B, L, D, N, nchunks;
 };
 
@@ -91,8 +134,8 @@ int report_error(int code, const char* fmt, ...);
 cudaError_t launch_bwd(const BwdParams& p, int act, cudaStream_t stream);
 bool bwd_tma_supported(const BwdParams& p, int act);
 cudaError_t launch_bwd_tma(const BwdParams& p, int act, cudaStream_t stream);
-// Segment count the TMA backward uses for this shape on a GPU with `sms` SMs (1 = none).
-int bwd_segments(int B, int L, int D, int N, int sms);
+// The TMA backward's work plan for this shape with `sms` worker CTAs.
+BwdPlan bwd_plan(int B, int L, int D, int N, int sms);
 cudaError_t launch_reduce_dbc(const float* ws_dbc, int ndt, int B, int L, int N, void* dBm,
                               void* dCm, int act, cudaStream_t stream);
 cudaError_t launch_reduce_params(const float* ws_param, int B, int D, int N, float* dA_log,

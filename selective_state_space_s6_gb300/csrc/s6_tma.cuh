@@ -139,6 +139,29 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 
+// ---- flags between CTAs of one (cooperative) launch
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Wait until *flag != 0; after ~2 s give up, set kStatusWaitTimeout and return false.
+__device__ __forceinline__ bool flag_wait(const int* flag, unsigned int* status) {
+  if (ld_acquire_gpu(flag)) return true;
+  const long long t0 = clock64();
+  while (!ld_acquire_gpu(flag)) {
+    __nanosleep(128);
+    if (clock64() - t0 > kWaitCycles) {
+      atomicOr(status, kStatusWaitTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
 // ---- tensor memory (TMEM) as per-lane scratch: a warp reaches the 32 TMEM
 // lanes 32*(warp % 4) .. +31 (thread i -> lane 32*(warp % 4) + i); an address
 // is (lane << 16) | column, one 32-bit value per (lane, column).

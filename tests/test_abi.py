@@ -96,25 +96,29 @@ def test_step_validation(lib):
 
 
 def test_segment_plan(lib):
-    """The time-segment plan is a function of the shape: one pass where the
-    (batch x channel-tile) grid fills the GPU in whole waves, several segments
-    for long sequences over few channels, never segments shorter than four
-    64-step chunks, and the workspace grows with the segment count."""
-    bf16 = s6.SSM_BF16
-    f, b = s6.plan_segments(4, 4096, 4096, 16, bf16)
-    assert f == 1 and b >= 1
-    f, b = s6.plan_segments(1, 65536, 2048, 16, s6.SSM_F32)
+    """The plans are functions of the shape.  Forward: one pass where the grid
+    fills the GPU, time segments of at least 512 steps for long sequences over
+    few channels.  Backward: the (batch x 64-channel tile) sequences are cut
+    into 152 equal ranges of 64-step chunks, so it reports the most pieces any
+    sequence has (1 = no cut)."""
+    bf16, f32 = s6.SSM_BF16, s6.SSM_F32
+    # 4 x 64 sequences of 64 chunks over 152 ranges of ~108 chunks: at most one cut each
+    assert s6.plan_segments(4, 4096, 4096, 16, bf16) == (1, 2)
+    # 152 sequences: one range each, no cut
+    assert s6.plan_segments(2, 4096, 76 * 64, 16, bf16)[1] == 1
+    # one sequence of 18 chunks: 18 ranges of one chunk
+    assert s6.plan_segments(1, 1100, 64, 16, f32)[1] == 18
+    f, b = s6.plan_segments(1, 65536, 2048, 16, f32)
     assert f > 1 and b > 1
-    for shape in [(1, 64, 16, 4), (2, 1023, 64, 16), (1, 1100, 64, 16), (3, 5000, 200, 8), (1, 4096, 32, 16)]:
-        f, b = s6.plan_segments(*shape, s6.SSM_F32)
-        L = shape[1]
-        for n in (f, b):
-            assert n >= 1
-            if n > 1:
-                seg = -(-L // n)
-                assert -(-seg // 64) >= 4 or L < 1024
-        assert s6.plan_segments(*shape, s6.SSM_F32) == (f, b)
-    # short sequences are never split
-    assert s6.plan_segments(1, 1000, 64, 16, s6.SSM_F32) == (1, 1)
+    for shape in [(1, 64, 16, 4), (2, 1023, 64, 16), (3, 5000, 200, 8), (1, 4096, 32, 16)]:
+        f, b = s6.plan_segments(*shape, f32)
+        assert f >= 1 and b >= 1
+        if f > 1:
+            assert -(-shape[1] // f) >= 512
+        assert s6.plan_segments(*shape, f32) == (f, b)
+    # dstate outside {4, 8, 16} never cuts sequences (generic kernels)
+    assert s6.plan_segments(3, 5000, 200, 5, f32)[1] == 1
+    # short sequences are never split in time by the forward
+    assert s6.plan_segments(1, 1000, 64, 16, f32)[0] == 1
     with pytest.raises(s6.SSMError):
-        s6.plan_segments(1, 10, 16, 32, s6.SSM_F32)  # dstate above 16
+        s6.plan_segments(1, 10, 16, 32, f32)  # dstate above 16

@@ -285,3 +285,21 @@ def test_decode_1000_chained_steps():
         errs.append(rel_err(np64(out_steps[:, :, d0:d1]), ref_out))
         errs.append(rel_err(np64(h[:, d0:d1]), ref_h))
     assert max(errs) <= TOL["f32"], errs
+
+
+@pytest.mark.parametrize("B,L,D,N,act", [(4, 256, 2560, 16, "bf16"), (3, 192, 4096, 16, "f32")])
+def test_handover_mode(B, L, D, N, act):
+    """Shapes whose backward cuts every (batch, channel tile) sequence at most
+    once, with ranges longer than a sequence: the carry is handed from the CTA
+    walking a sequence's last piece to the one walking its first piece.  Every
+    output against the oracle, and bit-identical over two runs."""
+    assert s6.plan_segments(B, L, D, N, s6.SSM_BF16 if act == "bf16" else s6.SSM_F32)[1] == 2
+    x = _inputs(B, L, D, N, act, seed=21)
+    xd = to_dev(x)
+    got = gpu_fwd_bwd(xd, dh_last=xd["dh_last"])
+    again = gpu_fwd_bwd(xd, dh_last=xd["dh_last"])
+    for k in GRAD_KEYS:
+        if got.get(k) is not None:
+            assert torch.equal(got[k], again[k]), k
+    ref = oracle_fwd_bwd(x, dh_last=x["dh_last"])
+    compare_all(got, ref, TOL[act])
