@@ -105,13 +105,19 @@ int64_t ssm_fwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t dim, int6
  * and per-batch partial sums of the parameter gradients); -1 if invalid. */
 int64_t ssm_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act);
 
-/* The time-segment plan of the forward and the backward scan for this shape
+/* The time-segment plans of the forward and the backward scan for this shape
  * (the chunked parallel scan of the kernels.rs page's "parallel scan" entry
- * point): 1 = one sequential pass per channel; n > 1 = per-segment
- * aggregates, a carry pass, then the n segments at once.  Used on the TMA
- * path (dstate 4, 8 or 16; 16-byte aligned tensors).  A function of the
- * shape only.  Writes *fwd_segments and *bwd_segments (each nullable);
- * returns SSM_OK, or SSM_ERR_INVALID_ARG for an invalid shape. */
+ * point), on the TMA path (dstate 4, 8 or 16; 16-byte aligned tensors); a
+ * function of the shape only.
+ *   *fwd_segments: 1 = one sequential pass per channel; n > 1 = per-segment
+ *     aggregates, a carry pass, then the n segments at once.
+ *   *bwd_segments: the backward splits the (batch, 64-channel tile)
+ *     sequences over 152 equal ranges of 64-step chunks, one CTA each.  1 =
+ *     no aggregate pass (no sequence cut, or every cut sequence hands its
+ *     carry from CTA to CTA within the launch); n > 1 = up to n pieces per
+ *     sequence, with piece aggregates and a carry pass first.
+ * Each pointer nullable; returns SSM_OK, or SSM_ERR_INVALID_ARG for an invalid
+ * shape. */
 int ssm_plan_segments(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
                       int *fwd_segments, int *bwd_segments);
 

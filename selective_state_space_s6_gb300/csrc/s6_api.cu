@@ -299,7 +299,10 @@ int ssm_plan_segments(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
   const int rc = check_shape(batch, seqlen, dim, dstate, act);
   if (rc != SSM_OK) return rc;
   if (fwd_segments) *fwd_segments = fwd_ws_layout(batch, seqlen, dim, dstate).nseg;
-  if (bwd_segments) *bwd_segments = bwd_ws_layout(batch, seqlen, dim, dstate).nseg;
+  if (bwd_segments) {
+    const BwdWorkspace w = bwd_ws_layout(batch, seqlen, dim, dstate);
+    *bwd_segments = w.plan.handover ? 1 : w.nseg;
+  }
   return SSM_OK;
 }
 

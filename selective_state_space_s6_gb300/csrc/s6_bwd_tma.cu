@@ -1023,7 +1023,7 @@ cudaError_t launch_one(const BwdTmaParams& P, cudaStream_t stream, bool cooperat
 template <typename Act, int TPC, bool kFast>
 cudaError_t launch_tpc(BwdTmaParams& P, BwdTmaParams& Pagg, cudaStream_t stream) {
   const BwdPlan& pl = P.p.plan;
-  if (P.p.nseg > 1 && P.p.seq_flag && P.p.nseg == 2 && (long long)pl.nch <= pl.U / pl.P) {
+  if (pl.handover && P.p.seq_flag) {
     // hand-over mode: every sequence in at most two pieces and no range
     // shorter than a sequence, so the CTA holding a last piece (walked
     // first) is done with it before the CTA holding the first piece (walked
@@ -1064,6 +1064,7 @@ BwdPlan bwd_plan(int B, int L, int D, int N, int sms) {
   pl.U = (long long)(B > 0 ? B : 0) * pl.ndt * pl.nch;
   pl.P = (int)std::max<long long>(1, std::min<long long>(std::max(sms, 1), pl.U));
   pl.maxp = 1;
+  pl.handover = false;
   if (pl.U == 0 || !(N == 4 || N == 8 || N == 16)) {
     pl.U = std::max<long long>(pl.U, 1);
     pl.P = 1;
@@ -1071,6 +1072,7 @@ BwdPlan bwd_plan(int B, int L, int D, int N, int sms) {
   }
   const long long nseq = (long long)B * pl.ndt;
   for (long long sq = 0; sq < nseq; ++sq) pl.maxp = std::max(pl.maxp, plan_pieces(pl, sq));
+  pl.handover = pl.maxp == 2 && (long long)pl.nch <= pl.U / pl.P;
   return pl;
 }
 

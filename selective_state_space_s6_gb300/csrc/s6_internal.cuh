@@ -60,6 +60,9 @@ struct BwdPlan {
   int nch;      // chunks per sequence
   int ndt;      // 64-channel tiles
   int maxp;     // most pieces any sequence has
+  // carries handed from CTA to CTA (no aggregate pass): every sequence in at
+  // most two pieces and no range shorter than a sequence
+  bool handover;
 };
 
 __host__ __device__ inline long long plan_bound(const BwdPlan& pl, long long w) { return w * pl.U / pl.P; }

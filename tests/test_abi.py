@@ -99,11 +99,13 @@ def test_segment_plan(lib):
     """The plans are functions of the shape.  Forward: one pass where the grid
     fills the GPU, time segments of at least 512 steps for long sequences over
     few channels.  Backward: the (batch x 64-channel tile) sequences are cut
-    into 152 equal ranges of 64-step chunks, so it reports the most pieces any
-    sequence has (1 = no cut)."""
+    into 152 equal ranges of 64-step chunks; it reports 1 when no aggregate
+    pass is needed (no cut, or cut sequences hand their carry over), else the
+    most pieces any sequence has."""
     bf16, f32 = s6.SSM_BF16, s6.SSM_F32
-    # 4 x 64 sequences of 64 chunks over 152 ranges of ~108 chunks: at most one cut each
-    assert s6.plan_segments(4, 4096, 4096, 16, bf16) == (1, 2)
+    # 4 x 64 sequences of 64 chunks over 152 ranges of ~108 chunks: at most one
+    # cut each, ranges longer than a sequence: carries handed over
+    assert s6.plan_segments(4, 4096, 4096, 16, bf16) == (1, 1)
     # 152 sequences: one range each, no cut
     assert s6.plan_segments(2, 4096, 76 * 64, 16, bf16)[1] == 1
     # one sequence of 18 chunks: 18 ranges of one chunk

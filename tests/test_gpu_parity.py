@@ -293,7 +293,7 @@ def test_handover_mode(B, L, D, N, act):
     once, with ranges longer than a sequence: the carry is handed from the CTA
     walking a sequence's last piece to the one walking its first piece.  Every
     output against the oracle, and bit-identical over two runs."""
-    assert s6.plan_segments(B, L, D, N, s6.SSM_BF16 if act == "bf16" else s6.SSM_F32)[1] == 2
+    assert s6.plan_segments(B, L, D, N, s6.SSM_BF16 if act == "bf16" else s6.SSM_F32)[1] == 1
     x = _inputs(B, L, D, N, act, seed=21)
     xd = to_dev(x)
     got = gpu_fwd_bwd(xd, dh_last=xd["dh_last"])
