@@ -174,7 +174,8 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   // order: piece = sequence sq (batch sq / ndt, channel tile sq % ndt),
   // chunks [c_lo, c_hi)
   const BwdPlan& pl = p.plan;
-  const long long u_begin = plan_bound(pl, blockIdx.x), u_end = plan_bound(pl, blockIdx.x + 1);
+  // (the plan keeps U below 2^31, so unit indices fit an int)
+  const int u_begin = (int)plan_bound(pl, blockIdx.x), u_end = (int)plan_bound(pl, blockIdx.x + 1);
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -214,13 +215,13 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   // last..first of the piece, with ntl tiles: pass A tiles 0..ntl-1, then
   // pass B tiles ntl-1..0.
   auto chunk_tiles = [&](int c) { return (min(kChunk, L - c * kChunk) + kTT - 1) / kTT; };
-  auto piece_at = [&](long long u, int& b, int& d0, int& c_lo, int& c_hi, long long& next) {
-    const long long sq = u / pl.nch, S0 = sq * pl.nch;
+  auto piece_at = [&](int u, int& b, int& d0, int& c_lo, int& c_hi, int& next) {
+    const int sq = u / pl.nch, S0 = sq * pl.nch;
     next = min(S0 + pl.nch, u_end);
-    b = (int)(sq / pl.ndt);
-    d0 = (int)(sq % pl.ndt) * kDTile;
-    c_lo = (int)(u - S0);
-    c_hi = (int)(next - S0);
+    b = sq / pl.ndt;
+    d0 = (sq % pl.ndt) * kDTile;
+    c_lo = u - S0;
+    c_hi = next - S0;
   };
 
   if (warp == kCW) {
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
       const uint32_t bytesB = (uint32_t)(((kGate ? 4 : 3) * kTile + 2 * kBC) * sizeof(Act));
       int item = 0;
       bool ok = true;
-      for (long long u = u_begin, next; u < u_end && ok; u = next) {
+      for (int u = u_begin, next; u < u_end && ok; u = next) {
         int b, d0, c_lo, c_hi;
         piece_at(u, b, d0, c_lo, c_hi, next);
         for (int c = c_hi - 1; c >= c_lo && ok; --c) {
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
     if (kBf16) {
       int item = 0;
       bool ok = true;
-      for (long long u = u_begin, next; u < u_end; u = next) {
+      for (int u = u_begin, next; u < u_end; u = next) {
         int b, d0, c_lo, c_hi;
         piece_at(u, b, d0, c_lo, c_hi, next);
         for (int c = c_hi - 1; c >= c_lo; --c) {
@@ -306,7 +307,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
     // partials (fixed warp order) -> this CTA's partial row in ws_dbc
     int n = 0;
     bool ok = true;
-    for (long long u = u_begin, next; u < u_end; u = next) {
+    for (int u = u_begin, next; u < u_end; u = next) {
       int b, d0, c_lo, c_hi;
       piece_at(u, b, d0, c_lo, c_hi, next);
       float* ws_dbc_r = p.ws_dbc + ((size_t)(d0 / kDTile) * p.B + b) * (size_t)L * 2 * N;
@@ -366,7 +367,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   int s = 0;         // ring stage of the current item
   uint32_t par = 0;  // its phase parity
   int nsub_done = 0;  // sub-chunks handed to the reducer so far
-  for (long long u = u_begin, next; u < u_end; u = next) {
+  for (int u = u_begin, next; u < u_end; u = next) {
   int b, d0, c_lo, c_hi;
   piece_at(u, b, d0, c_lo, c_hi, next);
   // piece index in time order within its sequence, and whether it ends the sequence
@@ -375,7 +376,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   const int d = d0 + cl;
   const bool dvalid = d < D;
   const int dc = dvalid ? d : D - 1;
-  const long long sq = (u - c_lo) / pl.nch;  // sequence index
+  const int sq = (u - c_lo) / pl.nch;  // sequence index
   if (!last_piece && p.seq_flag) {
     // hand-over mode: the carry comes from the CTA walking the sequence's last piece
     if (lane == 0 && !failed) failed = !flag_wait(p.seq_flag + sq, p.status);
@@ -404,9 +405,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
     my_tot[i] = 0.f;
     my_cmp[i] = 0.f;
   }
-  Act* dup = static_cast<Act*>(p.du) + (size_t)b * L * D + d;
-  Act* drp = static_cast<Act*>(p.d_delta_raw) + (size_t)b * L * D + d;
-  Act* dzp = kGate ? static_cast<Act*>(p.dz) + (size_t)b * L * D + d : nullptr;
+  const size_t bd_off = (size_t)b * L * D + d;  // du / d_delta_raw / dz of (b, t = 0, d)
   for (int c = c_hi - 1; c >= c_lo; --c) {
     const int t0 = c * kChunk;
     const int clen = min(kChunk, L - t0);
@@ -622,9 +621,9 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
               const int km = i * TPC + q;
               if (dvalid && (kFull || km < nv)) {
                 const size_t o = (size_t)(t0 + cstep + km) * D;
-                st_act(dup + o, o_du[i]);
-                st_act(drp + o, o_dr[i]);
-                if (kGate) st_act(dzp + o, o_dz[i]);
+                st_act(static_cast<Act*>(p.du) + bd_off + o, o_du[i]);
+                st_act(static_cast<Act*>(p.d_delta_raw) + bd_off + o, o_dr[i]);
+                if (kGate) st_act(static_cast<Act*>(p.dz) + bd_off + o, o_dz[i]);
               }
             }
           };
@@ -1083,6 +1082,7 @@ bool bwd_tma_supported(const BwdParams& p, int act) {
   if (!(p.N == 4 || p.N == 8 || p.N == 16)) return false;
   if (act == SSM_BF16 && p.N == 4) return false;
   if ((p.N * e) % 16 != 0 || (p.D * e) % 16 != 0) return false;
+  if (p.plan.U >= (1LL << 31)) return false;  // unit indices are ints in the kernel
   const void* ptrs[] = {p.u, p.delta_raw, p.Bm, p.Cm, p.dout, p.chunk_states};
   for (const void* q : ptrs)
     if (!aligned16(q)) return false;
