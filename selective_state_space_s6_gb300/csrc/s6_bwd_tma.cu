@@ -368,336 +368,336 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   uint32_t par = 0;  // its phase parity
   int nsub_done = 0;  // sub-chunks handed to the reducer so far
   for (int u = u_begin, next; u < u_end; u = next) {
-  int b, d0, c_lo, c_hi;
-  piece_at(u, b, d0, c_lo, c_hi, next);
-  // piece index in time order within its sequence, and whether it ends the sequence
-  const int kp = c_lo == 0 ? 0 : (int)(plan_count_le(pl, u) - plan_count_le(pl, u - c_lo));
-  const bool last_piece = c_hi == pl.nch;
-  const int d = d0 + cl;
-  const bool dvalid = d < D;
-  const int dc = dvalid ? d : D - 1;
-  const int sq = (u - c_lo) / pl.nch;  // sequence index
-  if (!last_piece && p.seq_flag) {
-    // hand-over mode: the carry comes from the CTA walking the sequence's last piece
-    if (lane == 0 && !failed) failed = !flag_wait(p.seq_flag + sq, p.status);
-    failed = __shfl_sync(0xffffffffu, failed, 0);
-    __syncwarp();
-  }
-  float2 A2[2], carry[2];
-  {
-    const float* cin = !last_piece ? p.seg_carry + (((size_t)b * p.nseg + kp) * D + dc) * N
-                                   : (p.dh_last ? p.dh_last + ((size_t)b * D + dc) * N : nullptr);
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int n = 4 * q + 2 * i;
-      const float a0 = -expf(p.A_log[dc * N + n]);
-      const float a1 = -expf(p.A_log[dc * N + n + 1]);
-      A2[i] = kFast ? make_float2(a0 * kLog2e, a1 * kLog2e) : make_float2(a0, a1);
-      // adjoint carry entering the piece's last step: dh_last for the last
-      // piece of the sequence, the composed carry of the pieces after it otherwise
-      carry[i] = (cin && dvalid) ? make_float2(__ldcg(cin + n), __ldcg(cin + n + 1)) : make_float2(0.f, 0.f);
+    int b, d0, c_lo, c_hi;
+    piece_at(u, b, d0, c_lo, c_hi, next);
+    // piece index in time order within its sequence, and whether it ends the sequence
+    const int kp = c_lo == 0 ? 0 : (int)(plan_count_le(pl, u) - plan_count_le(pl, u - c_lo));
+    const bool last_piece = c_hi == pl.nch;
+    const int d = d0 + cl;
+    const bool dvalid = d < D;
+    const int dc = dvalid ? d : D - 1;
+    const int sq = (u - c_lo) / pl.nch;  // sequence index
+    if (!last_piece && p.seq_flag) {
+      // hand-over mode: the carry comes from the CTA walking the sequence's last piece
+      if (lane == 0 && !failed) failed = !flag_wait(p.seq_flag + sq, p.status);
+      failed = __shfl_sync(0xffffffffu, failed, 0);
+      __syncwarp();
     }
-  }
-  const float bias = p.delta_bias[dc];
-  const float Dd = p.Dp[dc];
-#pragma unroll
-  for (int i = 0; i < 6; ++i) {
-    my_tot[i] = 0.f;
-    my_cmp[i] = 0.f;
-  }
-  const size_t bd_off = (size_t)b * L * D + d;  // du / d_delta_raw / dz of (b, t = 0, d)
-  for (int c = c_hi - 1; c >= c_lo; --c) {
-    const int t0 = c * kChunk;
-    const int clen = min(kChunk, L - t0);
-    const int ntl = (clen + kTT - 1) / kTT;
-    float2 accA[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-    float accD = 0.f, accBias = 0.f;
-    float2 h[2];
+    float2 A2[2], carry[2];
     {
-      const float4 cs = *reinterpret_cast<const float4*>(p.chunk_states + (((size_t)b * nchunks + c) * D + dc) * N + 4 * q);
-      h[0] = make_float2(cs.x, cs.y);
-      h[1] = make_float2(cs.z, cs.w);
-    }
-    for (int it = 0; it < 2 * ntl; ++it) {
-      const bool passA = it < ntl;
-      const int j = passA ? it : 2 * ntl - 1 - it;
-      if (!failed) failed = !mbar_wait(&full[s], par, p.status);
-      if (kBf16 && !failed) failed = !mbar_wait(&conv[s], par, p.status);
-      __syncwarp();
-      const int tb = j * kTT;  // first step of the tile within the chunk
-      const int cnt = min(kTT, clen - tb);
-      const Act* su = tile_u(s);
-      const Act* sr = tile_raw(s);
-      const float* Bt = (kBf16 ? bcf + (size_t)s * kTT * 2 * N : reinterpret_cast<const float*>(tile_B(s))) + 4 * q;
-      const float* Ct = kBf16 ? Bt + N : reinterpret_cast<const float*>(tile_C(s)) + 4 * q;
-      float2* dtile = dbuf + tb * kRow;  // (delta, delta*u) rows of this tile
-
-      if (passA) {
-        // ---------- pass A: (delta, delta*u) of the owned steps, then the recurrence
-        auto pass_a = [&](auto full_tag) {
-          constexpr bool kFull = decltype(full_tag)::value;
-          const int nv = kFull ? kTT : cnt;
-#pragma unroll
-          for (int i = 0; i < kOwnA; ++i) {
-            const int km = i * TPC + q;
-            const int kr = kFull ? km : min(km, nv - 1);
-            const int o = kr * kRB + (kFull ? colo[i % kOwnB] : AT::col(kr, cl));
-            const float sv = lds_at(sr, o) + bias;
-            const float sp = kFast ? softplus_fast(sv) : softplus_f(sv);
-            if (kFull || km < nv) dtile[km * kRow + cl] = make_float2(sp, sp * lds_at(su, o));
-          }
-          __syncwarp();
-          if (tb == 0) hc0[tid] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
-          // states after each step, 8 steps at a time, then to TMEM
-          float hb[4 * kSub];
-          auto stepA = [&](int kk) {
-            const float2 dv = dtile[kk * kRow + cl];
-            const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
-            const float4 Bv = *reinterpret_cast<const float4*>(Bt + kk * kBst);
-            h[0] = ffma2(decay2<kFast>(dd, A2[0]), h[0], fmul2(uu2, make_float2(Bv.x, Bv.y)));
-            h[1] = ffma2(decay2<kFast>(dd, A2[1]), h[1], fmul2(uu2, make_float2(Bv.z, Bv.w)));
-            const int r = 4 * (kk % kSub);
-            hb[r] = h[0].x;
-            hb[r + 1] = h[0].y;
-            hb[r + 2] = h[1].x;
-            hb[r + 3] = h[1].y;
-          };
-#pragma unroll
-          for (int kk = 0; kk < kTT; ++kk) {
-            if (kFull || kk < nv) stepA(kk);
-            // a block with at least one valid step goes out (warp-uniform)
-            if ((kk % kSub) == kSub - 1 && (kFull || kk - (kSub - 1) < nv)) tmem_st32(tm + (uint32_t)(4 * (tb + kk - (kSub - 1))), hb);
-          }
-        };
-        if (cnt == kTT)
-          pass_a(std::true_type{});
-        else
-          pass_a(std::false_type{});
-      } else {
-        // ---------- pass B: 8-step sub-chunks of this tile, last first
-        const Act* sz = tile_z(s);
-        const Act* sg = tile_g(s);
-        const int nsub = (cnt + kSub - 1) / kSub;
-        if (it == ntl) tmem_wait_st();  // the chunk's states (pass A) are in TMEM
-        for (int sc = nsub - 1; sc >= 0; --sc) {
-          const int ks = sc * kSub;  // first step of the sub-chunk within the tile
-          const int cnt8 = min(kSub, cnt - ks);
-          const int cstep = tb + ks;  // ... within the chunk
-          // the state before the sub-chunk: last state of the previous block, or the chunk start
-          float hq[4];
-          if (cstep > 0) {
-            tmem_ld4(tm + (uint32_t)(4 * cstep - 4), hq);
-          } else {
-            const float4 c0 = hc0[tid];
-            hq[0] = c0.x, hq[1] = c0.y, hq[2] = c0.z, hq[3] = c0.w;
-          }
-          const float2 hstart[2] = {make_float2(hq[0], hq[1]), make_float2(hq[2], hq[3])};
-          const float2* dsub = dbuf + cstep * kRow;
-          // wpart slot of this sub-chunk: wait until the reducer has summed its previous use
-          const int slot = nsub_done & 1;
-          if (nsub_done >= 2 && !failed) failed = !mbar_wait(&wempty[slot], (uint32_t)((nsub_done >> 1) - 1) & 1, p.status);
-          float* wp_sub = wpart + slot * (kSub * kCW * 32);
-          auto sub = [&](auto full_tag) {
-            constexpr bool kFull = decltype(full_tag)::value;
-            const int nv = kFull ? kSub : cnt8;
-            // B1: the sub-chunk's states from TMEM (written by pass A)
-            float hv[4 * kSub];
-            tmem_ld32(tm + (uint32_t)(4 * cstep), hv);
-            float2 hs[kSub][2];
-#pragma unroll
-            for (int k = 0; k < kSub; ++k) {
-              hs[k][0] = make_float2(hv[4 * k], hv[4 * k + 1]);
-              hs[k][1] = make_float2(hv[4 * k + 2], hv[4 * k + 3]);
-            }
-            // B2: gate terms of the owned steps: dy = dout*silu(z), dz factor
-#pragma unroll
-            for (int i = 0; i < kOwnB; ++i) {
-              const int km = i * TPC + q;
-              const int kr = ks + (kFull ? km : min(km, nv - 1));
-              const int o = kr * kRB + (kFull ? colo[i] : AT::col(kr, cl));
-              const float gout = lds_at(sg, o);
-              float2 v = make_float2(gout, 0.f);
-              if (kGate) {
-                const float zz = lds_at(sz, o);
-                const float sgz = kFast ? sigmoid_fast(zz) : sigmoid_f(zz);
-                v.x = gout * zz * sgz;
-                v.y = gout * sgz * fmaf(zz, 1.f - sgz, 1.f);
-              }
-              if (!kFull && km >= nv) v = make_float2(0.f, 0.f);
-              bprep[km * kRow + cl] = v;
-            }
-            __syncwarp();
-            // B3: reverse steps in pairs; the adjoint carry is the only
-            // loop-carried value.  Each step's dBm/dCm terms go to one of two
-            // warp-local slots and are summed over the warp's channels after
-            // each pair (fixed order) into the per-warp partial wp_sub.
-#pragma unroll
-            for (int gi = kSub / 2 - 1; gi >= 0; --gi) {
-#pragma unroll
-              for (int k = 2 * gi + 1; k >= 2 * gi; --k) {
-                if (kFull || k < nv) {
-                  const float2 dv = dsub[k * kRow + cl];
-                  const float dy = bprep[k * kRow + cl].x;
-                  const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
-                  const float2 dy2 = make_float2(dy, dy);
-                  const float4 Bv4 = *reinterpret_cast<const float4*>(Bt + (ks + k) * kBst);
-                  const float4 Cv4 = *reinterpret_cast<const float4*>(Ct + (ks + k) * kBst);
-                  const float2 Bv[2] = {make_float2(Bv4.x, Bv4.y), make_float2(Bv4.z, Bv4.w)};
-                  const float2 Cv[2] = {make_float2(Cv4.x, Cv4.y), make_float2(Cv4.z, Cv4.w)};
-                  float2 ya = make_float2(0.f, 0.f), gba = make_float2(0.f, 0.f), apa = make_float2(0.f, 0.f);
-                  float2 tB[2], tC[2];
-#pragma unroll
-                  for (int i = 0; i < 2; ++i) {
-                    const float2 a = decay2<kFast>(dd, A2[i]);
-                    const float2 hk = hs[k][i];
-                    const float2 hp = k == 0 ? hstart[i] : hs[k > 0 ? k - 1 : 0][i];
-                    const float2 g = ffma2(dy2, Cv[i], carry[i]);
-                    const float2 ag = fmul2(a, g);   // adjoint carried to step k-1
-                    const float2 pv = fmul2(ag, hp); // g * a * h_{k-1}
-                    apa = ffma2(A2[i], pv, apa);
-                    accA[i] = ffma2(dd, pv, accA[i]);
-                    gba = ffma2(g, Bv[i], gba);
-                    ya = ffma2(Cv[i], hk, ya);
-                    tB[i] = fmul2(g, uu2);
-                    tC[i] = fmul2(dy2, hk);
-                    carry[i] = ag;
-                  }
-                  float* rb = my_redw + (k & 1) * kRedSlot;
-                  // (channels past D: the tiles' zero fill makes dout and u,
-                  // hence dy, g and both terms, exactly 0)
-                  *reinterpret_cast<float4*>(rb + lane * 4) = make_float4(tB[0].x, tB[0].y, tB[1].x, tB[1].y);
-                  *reinterpret_cast<float4*>(rb + kRedBlock + lane * 4) = make_float4(tC[0].x, tC[0].y, tC[1].x, tC[1].y);
-                  part[k * kPartRow + tid] = make_float4(ya.x + ya.y, gba.x + gba.y, (apa.x + apa.y) * kAscale, 0.f);
-                }
-              }
-              __syncwarp();
-              // channel sums of the pair's steps: 4 channels per lane, then across groups
-#pragma unroll
-              for (int k = 2 * gi + 1; k >= 2 * gi; --k) {
-                if (kFull || k < nv) {
-                  const float* rb = my_redw + (k & 1) * kRedSlot + r_q * kRedBlock;
-                  float2 v = make_float2(0.f, 0.f);
-#pragma unroll
-                  for (int k2 = 0; k2 < 4; ++k2) {
-                    const int L2 = (r_g * 4 + k2) * TPC + r_src;
-                    v = fadd2(v, *reinterpret_cast<const float2*>(rb + L2 * 4 + r_j));
-                  }
-#pragma unroll
-                  for (int m = N; m < 32; m <<= 1)
-                    v = fadd2(v, make_float2(__shfl_xor_sync(0xffffffffu, v.x, m), __shfl_xor_sync(0xffffffffu, v.y, m)));
-                  // every group holds the identical sum; all store it
-                  *reinterpret_cast<float2*>(wp_sub + (k * kCW + warp) * 32 + r_q * N + r_n) = v;
-                }
-              }
-              __syncwarp();
-            }
-            // B4: owned steps: combine the channel's partial sums (fixed lane
-            // order), write du, d_delta_raw, dz
-            float o_du[kOwnB], o_dr[kOwnB], o_dz[kOwnB];
-#pragma unroll
-            for (int i = 0; i < kOwnB; ++i) {
-              const int km = i * TPC + q;
-              const int kr = kFull ? km : min(km, nv - 1);
-              float4 acc = part[kr * kPartRow + cl * TPC];
-#pragma unroll
-              for (int r = 1; r < TPC; ++r) {
-                const float4 o = part[kr * kPartRow + cl * TPC + r];
-                acc = make_float4(acc.x + o.x, acc.y + o.y, acc.z + o.z, 0.f);
-              }
-              const float2 dv = dsub[kr * kRow + cl];
-              const float2 bp = bprep[kr * kRow + cl];
-              const float uo = lds_at(su, (ks + kr) * kRB + (kFull ? colo[i] : AT::col(kr, cl)));
-              const float dsp = kFast ? dsoftplus_fast(dv.x) : -expm1f(-dv.x);
-              const float draw = fmaf(uo, acc.y, acc.z) * dsp;
-              o_du[i] = fmaf(Dd, bp.x, dv.x * acc.y);
-              o_dr[i] = draw;
-              o_dz[i] = fmaf(Dd, uo, acc.x) * bp.y;
-              const bool ok = kFull || km < nv;
-              accD += ok ? bp.x * uo : 0.f;
-              accBias += ok ? draw : 0.f;
-            }
-#pragma unroll
-            for (int i = 0; i < kOwnB; ++i) {
-              const int km = i * TPC + q;
-              if (dvalid && (kFull || km < nv)) {
-                const size_t o = (size_t)(t0 + cstep + km) * D;
-                st_act(static_cast<Act*>(p.du) + bd_off + o, o_du[i]);
-                st_act(static_cast<Act*>(p.d_delta_raw) + bd_off + o, o_dr[i]);
-                if (kGate) st_act(static_cast<Act*>(p.dz) + bd_off + o, o_dz[i]);
-              }
-            }
-          };
-          if (cnt8 == kSub)
-            sub(std::true_type{});
-          else
-            sub(std::false_type{});
-          // B5: hand the sub-chunk's per-warp partials to the reducer warp
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&wfull[slot]);
-          ++nsub_done;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-      if (++s == S) {
-        s = 0;
-        par ^= 1;
-      }
-    }
-    // chunk sums -> compensated running totals (per-lane private smem)
-    kahan_add(my_tot[0], my_cmp[0], accA[0].x);
-    kahan_add(my_tot[1], my_cmp[1], accA[0].y);
-    kahan_add(my_tot[2], my_cmp[2], accA[1].x);
-    kahan_add(my_tot[3], my_cmp[3], accA[1].y);
-    kahan_add(my_tot[4], my_cmp[4], accD);
-    kahan_add(my_tot[5], my_cmp[5], accBias);
-  }
-  // ---------------- the piece's parameter partials (row b * nseg + kp) and dh0
-  {
-    // dDp and d_delta_bias: each lane summed its owned steps; add the channel's TPC lanes
-    float tD = my_tot[4], tBs = my_tot[5];
-#pragma unroll
-    for (int m = 1; m < TPC; m <<= 1) {
-      tD += __shfl_xor_sync(0xffffffffu, tD, m);
-      tBs += __shfl_xor_sync(0xffffffffu, tBs, m);
-    }
-    if (dvalid) {
-      float* wp = p.ws_param + (((size_t)b * p.nseg + kp) * D + d) * (N + 2);
+      const float* cin = !last_piece ? p.seg_carry + (((size_t)b * p.nseg + kp) * D + dc) * N
+                                     : (p.dh_last ? p.dh_last + ((size_t)b * D + dc) * N : nullptr);
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int n = 4 * q + 2 * i;
-        wp[n] = (A2[i].x * kAscale) * my_tot[2 * i];
-        wp[n + 1] = (A2[i].y * kAscale) * my_tot[2 * i + 1];
-        if (p.dh0 && c_lo == 0) *reinterpret_cast<float2*>(p.dh0 + ((size_t)b * D + d) * N + n) = carry[i];
+        const float a0 = -expf(p.A_log[dc * N + n]);
+        const float a1 = -expf(p.A_log[dc * N + n + 1]);
+        A2[i] = kFast ? make_float2(a0 * kLog2e, a1 * kLog2e) : make_float2(a0, a1);
+        // adjoint carry entering the piece's last step: dh_last for the last
+        // piece of the sequence, the composed carry of the pieces after it otherwise
+        carry[i] = (cin && dvalid) ? make_float2(__ldcg(cin + n), __ldcg(cin + n + 1)) : make_float2(0.f, 0.f);
       }
-      if (q == 0) {
-        wp[N] = tD;
-        wp[N + 1] = tBs;
+    }
+    const float bias = p.delta_bias[dc];
+    const float Dd = p.Dp[dc];
+#pragma unroll
+    for (int i = 0; i < 6; ++i) {
+      my_tot[i] = 0.f;
+      my_cmp[i] = 0.f;
+    }
+    const size_t bd_off = (size_t)b * L * D + d;  // du / d_delta_raw / dz of (b, t = 0, d)
+    for (int c = c_hi - 1; c >= c_lo; --c) {
+      const int t0 = c * kChunk;
+      const int clen = min(kChunk, L - t0);
+      const int ntl = (clen + kTT - 1) / kTT;
+      float2 accA[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      float accD = 0.f, accBias = 0.f;
+      float2 h[2];
+      {
+        const float4 cs = *reinterpret_cast<const float4*>(p.chunk_states + (((size_t)b * nchunks + c) * D + dc) * N + 4 * q);
+        h[0] = make_float2(cs.x, cs.y);
+        h[1] = make_float2(cs.z, cs.w);
       }
-      if (p.seq_flag) {
-        // rows of pieces this sequence does not have stay zero for the finalize
-        for (int k2 = plan_pieces(pl, sq); k2 < p.nseg; ++k2) {
-          float* wz = p.ws_param + (((size_t)b * p.nseg + k2) * D + d) * (N + 2);
-          wz[4 * q] = wz[4 * q + 1] = wz[4 * q + 2] = wz[4 * q + 3] = 0.f;
-          if (q == 0) wz[N] = wz[N + 1] = 0.f;
+      for (int it = 0; it < 2 * ntl; ++it) {
+        const bool passA = it < ntl;
+        const int j = passA ? it : 2 * ntl - 1 - it;
+        if (!failed) failed = !mbar_wait(&full[s], par, p.status);
+        if (kBf16 && !failed) failed = !mbar_wait(&conv[s], par, p.status);
+        __syncwarp();
+        const int tb = j * kTT;  // first step of the tile within the chunk
+        const int cnt = min(kTT, clen - tb);
+        const Act* su = tile_u(s);
+        const Act* sr = tile_raw(s);
+        const float* Bt = (kBf16 ? bcf + (size_t)s * kTT * 2 * N : reinterpret_cast<const float*>(tile_B(s))) + 4 * q;
+        const float* Ct = kBf16 ? Bt + N : reinterpret_cast<const float*>(tile_C(s)) + 4 * q;
+        float2* dtile = dbuf + tb * kRow;  // (delta, delta*u) rows of this tile
+
+        if (passA) {
+          // ---------- pass A: (delta, delta*u) of the owned steps, then the recurrence
+          auto pass_a = [&](auto full_tag) {
+            constexpr bool kFull = decltype(full_tag)::value;
+            const int nv = kFull ? kTT : cnt;
+#pragma unroll
+            for (int i = 0; i < kOwnA; ++i) {
+              const int km = i * TPC + q;
+              const int kr = kFull ? km : min(km, nv - 1);
+              const int o = kr * kRB + (kFull ? colo[i % kOwnB] : AT::col(kr, cl));
+              const float sv = lds_at(sr, o) + bias;
+              const float sp = kFast ? softplus_fast(sv) : softplus_f(sv);
+              if (kFull || km < nv) dtile[km * kRow + cl] = make_float2(sp, sp * lds_at(su, o));
+            }
+            __syncwarp();
+            if (tb == 0) hc0[tid] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+            // states after each step, 8 steps at a time, then to TMEM
+            float hb[4 * kSub];
+            auto stepA = [&](int kk) {
+              const float2 dv = dtile[kk * kRow + cl];
+              const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
+              const float4 Bv = *reinterpret_cast<const float4*>(Bt + kk * kBst);
+              h[0] = ffma2(decay2<kFast>(dd, A2[0]), h[0], fmul2(uu2, make_float2(Bv.x, Bv.y)));
+              h[1] = ffma2(decay2<kFast>(dd, A2[1]), h[1], fmul2(uu2, make_float2(Bv.z, Bv.w)));
+              const int r = 4 * (kk % kSub);
+              hb[r] = h[0].x;
+              hb[r + 1] = h[0].y;
+              hb[r + 2] = h[1].x;
+              hb[r + 3] = h[1].y;
+            };
+#pragma unroll
+            for (int kk = 0; kk < kTT; ++kk) {
+              if (kFull || kk < nv) stepA(kk);
+              // a block with at least one valid step goes out (warp-uniform)
+              if ((kk % kSub) == kSub - 1 && (kFull || kk - (kSub - 1) < nv)) tmem_st32(tm + (uint32_t)(4 * (tb + kk - (kSub - 1))), hb);
+            }
+          };
+          if (cnt == kTT)
+            pass_a(std::true_type{});
+          else
+            pass_a(std::false_type{});
+        } else {
+          // ---------- pass B: 8-step sub-chunks of this tile, last first
+          const Act* sz = tile_z(s);
+          const Act* sg = tile_g(s);
+          const int nsub = (cnt + kSub - 1) / kSub;
+          if (it == ntl) tmem_wait_st();  // the chunk's states (pass A) are in TMEM
+          for (int sc = nsub - 1; sc >= 0; --sc) {
+            const int ks = sc * kSub;  // first step of the sub-chunk within the tile
+            const int cnt8 = min(kSub, cnt - ks);
+            const int cstep = tb + ks;  // ... within the chunk
+            // the state before the sub-chunk: last state of the previous block, or the chunk start
+            float hq[4];
+            if (cstep > 0) {
+              tmem_ld4(tm + (uint32_t)(4 * cstep - 4), hq);
+            } else {
+              const float4 c0 = hc0[tid];
+              hq[0] = c0.x, hq[1] = c0.y, hq[2] = c0.z, hq[3] = c0.w;
+            }
+            const float2 hstart[2] = {make_float2(hq[0], hq[1]), make_float2(hq[2], hq[3])};
+            const float2* dsub = dbuf + cstep * kRow;
+            // wpart slot of this sub-chunk: wait until the reducer has summed its previous use
+            const int slot = nsub_done & 1;
+            if (nsub_done >= 2 && !failed) failed = !mbar_wait(&wempty[slot], (uint32_t)((nsub_done >> 1) - 1) & 1, p.status);
+            float* wp_sub = wpart + slot * (kSub * kCW * 32);
+            auto sub = [&](auto full_tag) {
+              constexpr bool kFull = decltype(full_tag)::value;
+              const int nv = kFull ? kSub : cnt8;
+              // B1: the sub-chunk's states from TMEM (written by pass A)
+              float hv[4 * kSub];
+              tmem_ld32(tm + (uint32_t)(4 * cstep), hv);
+              float2 hs[kSub][2];
+#pragma unroll
+              for (int k = 0; k < kSub; ++k) {
+                hs[k][0] = make_float2(hv[4 * k], hv[4 * k + 1]);
+                hs[k][1] = make_float2(hv[4 * k + 2], hv[4 * k + 3]);
+              }
+              // B2: gate terms of the owned steps: dy = dout*silu(z), dz factor
+#pragma unroll
+              for (int i = 0; i < kOwnB; ++i) {
+                const int km = i * TPC + q;
+                const int kr = ks + (kFull ? km : min(km, nv - 1));
+                const int o = kr * kRB + (kFull ? colo[i] : AT::col(kr, cl));
+                const float gout = lds_at(sg, o);
+                float2 v = make_float2(gout, 0.f);
+                if (kGate) {
+                  const float zz = lds_at(sz, o);
+                  const float sgz = kFast ? sigmoid_fast(zz) : sigmoid_f(zz);
+                  v.x = gout * zz * sgz;
+                  v.y = gout * sgz * fmaf(zz, 1.f - sgz, 1.f);
+                }
+                if (!kFull && km >= nv) v = make_float2(0.f, 0.f);
+                bprep[km * kRow + cl] = v;
+              }
+              __syncwarp();
+              // B3: reverse steps in pairs; the adjoint carry is the only
+              // loop-carried value.  Each step's dBm/dCm terms go to one of two
+              // warp-local slots and are summed over the warp's channels after
+              // each pair (fixed order) into the per-warp partial wp_sub.
+#pragma unroll
+              for (int gi = kSub / 2 - 1; gi >= 0; --gi) {
+#pragma unroll
+                for (int k = 2 * gi + 1; k >= 2 * gi; --k) {
+                  if (kFull || k < nv) {
+                    const float2 dv = dsub[k * kRow + cl];
+                    const float dy = bprep[k * kRow + cl].x;
+                    const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
+                    const float2 dy2 = make_float2(dy, dy);
+                    const float4 Bv4 = *reinterpret_cast<const float4*>(Bt + (ks + k) * kBst);
+                    const float4 Cv4 = *reinterpret_cast<const float4*>(Ct + (ks + k) * kBst);
+                    const float2 Bv[2] = {make_float2(Bv4.x, Bv4.y), make_float2(Bv4.z, Bv4.w)};
+                    const float2 Cv[2] = {make_float2(Cv4.x, Cv4.y), make_float2(Cv4.z, Cv4.w)};
+                    float2 ya = make_float2(0.f, 0.f), gba = make_float2(0.f, 0.f), apa = make_float2(0.f, 0.f);
+                    float2 tB[2], tC[2];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                      const float2 a = decay2<kFast>(dd, A2[i]);
+                      const float2 hk = hs[k][i];
+                      const float2 hp = k == 0 ? hstart[i] : hs[k > 0 ? k - 1 : 0][i];
+                      const float2 g = ffma2(dy2, Cv[i], carry[i]);
+                      const float2 ag = fmul2(a, g);   // adjoint carried to step k-1
+                      const float2 pv = fmul2(ag, hp); // g * a * h_{k-1}
+                      apa = ffma2(A2[i], pv, apa);
+                      accA[i] = ffma2(dd, pv, accA[i]);
+                      gba = ffma2(g, Bv[i], gba);
+                      ya = ffma2(Cv[i], hk, ya);
+                      tB[i] = fmul2(g, uu2);
+                      tC[i] = fmul2(dy2, hk);
+                      carry[i] = ag;
+                    }
+                    float* rb = my_redw + (k & 1) * kRedSlot;
+                    // (channels past D: the tiles' zero fill makes dout and u,
+                    // hence dy, g and both terms, exactly 0)
+                    *reinterpret_cast<float4*>(rb + lane * 4) = make_float4(tB[0].x, tB[0].y, tB[1].x, tB[1].y);
+                    *reinterpret_cast<float4*>(rb + kRedBlock + lane * 4) = make_float4(tC[0].x, tC[0].y, tC[1].x, tC[1].y);
+                    part[k * kPartRow + tid] = make_float4(ya.x + ya.y, gba.x + gba.y, (apa.x + apa.y) * kAscale, 0.f);
+                  }
+                }
+                __syncwarp();
+                // channel sums of the pair's steps: 4 channels per lane, then across groups
+#pragma unroll
+                for (int k = 2 * gi + 1; k >= 2 * gi; --k) {
+                  if (kFull || k < nv) {
+                    const float* rb = my_redw + (k & 1) * kRedSlot + r_q * kRedBlock;
+                    float2 v = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int k2 = 0; k2 < 4; ++k2) {
+                      const int L2 = (r_g * 4 + k2) * TPC + r_src;
+                      v = fadd2(v, *reinterpret_cast<const float2*>(rb + L2 * 4 + r_j));
+                    }
+#pragma unroll
+                    for (int m = N; m < 32; m <<= 1)
+                      v = fadd2(v, make_float2(__shfl_xor_sync(0xffffffffu, v.x, m), __shfl_xor_sync(0xffffffffu, v.y, m)));
+                    // every group holds the identical sum; all store it
+                    *reinterpret_cast<float2*>(wp_sub + (k * kCW + warp) * 32 + r_q * N + r_n) = v;
+                  }
+                }
+                __syncwarp();
+              }
+              // B4: owned steps: combine the channel's partial sums (fixed lane
+              // order), write du, d_delta_raw, dz
+              float o_du[kOwnB], o_dr[kOwnB], o_dz[kOwnB];
+#pragma unroll
+              for (int i = 0; i < kOwnB; ++i) {
+                const int km = i * TPC + q;
+                const int kr = kFull ? km : min(km, nv - 1);
+                float4 acc = part[kr * kPartRow + cl * TPC];
+#pragma unroll
+                for (int r = 1; r < TPC; ++r) {
+                  const float4 o = part[kr * kPartRow + cl * TPC + r];
+                  acc = make_float4(acc.x + o.x, acc.y + o.y, acc.z + o.z, 0.f);
+                }
+                const float2 dv = dsub[kr * kRow + cl];
+                const float2 bp = bprep[kr * kRow + cl];
+                const float uo = lds_at(su, (ks + kr) * kRB + (kFull ? colo[i] : AT::col(kr, cl)));
+                const float dsp = kFast ? dsoftplus_fast(dv.x) : -expm1f(-dv.x);
+                const float draw = fmaf(uo, acc.y, acc.z) * dsp;
+                o_du[i] = fmaf(Dd, bp.x, dv.x * acc.y);
+                o_dr[i] = draw;
+                o_dz[i] = fmaf(Dd, uo, acc.x) * bp.y;
+                const bool ok = kFull || km < nv;
+                accD += ok ? bp.x * uo : 0.f;
+                accBias += ok ? draw : 0.f;
+              }
+#pragma unroll
+              for (int i = 0; i < kOwnB; ++i) {
+                const int km = i * TPC + q;
+                if (dvalid && (kFull || km < nv)) {
+                  const size_t o = (size_t)(t0 + cstep + km) * D;
+                  st_act(static_cast<Act*>(p.du) + bd_off + o, o_du[i]);
+                  st_act(static_cast<Act*>(p.d_delta_raw) + bd_off + o, o_dr[i]);
+                  if (kGate) st_act(static_cast<Act*>(p.dz) + bd_off + o, o_dz[i]);
+                }
+              }
+            };
+            if (cnt8 == kSub)
+              sub(std::true_type{});
+            else
+              sub(std::false_type{});
+            // B5: hand the sub-chunk's per-warp partials to the reducer warp
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&wfull[slot]);
+            ++nsub_done;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (++s == S) {
+          s = 0;
+          par ^= 1;
         }
       }
+      // chunk sums -> compensated running totals (per-lane private smem)
+      kahan_add(my_tot[0], my_cmp[0], accA[0].x);
+      kahan_add(my_tot[1], my_cmp[1], accA[0].y);
+      kahan_add(my_tot[2], my_cmp[2], accA[1].x);
+      kahan_add(my_tot[3], my_cmp[3], accA[1].y);
+      kahan_add(my_tot[4], my_cmp[4], accD);
+      kahan_add(my_tot[5], my_cmp[5], accBias);
     }
-    if (p.seq_flag && kp > 0) {
-      // hand-over mode, the sequence's last piece: its final carry enters the
-      // first piece's last step; publish it and raise the flag
-      if (dvalid) {
-        float* co = p.seg_carry + (((size_t)b * p.nseg + kp - 1) * D + d) * N + 4 * q;
-        __stcg(co, carry[0].x);
-        __stcg(co + 1, carry[0].y);
-        __stcg(co + 2, carry[1].x);
-        __stcg(co + 3, carry[1].y);
+    // ---------------- the piece's parameter partials (row b * nseg + kp) and dh0
+    {
+      // dDp and d_delta_bias: each lane summed its owned steps; add the channel's TPC lanes
+      float tD = my_tot[4], tBs = my_tot[5];
+#pragma unroll
+      for (int m = 1; m < TPC; m <<= 1) {
+        tD += __shfl_xor_sync(0xffffffffu, tD, m);
+        tBs += __shfl_xor_sync(0xffffffffu, tBs, m);
       }
-      __threadfence();
-      named_bar_sync(2, kLanes);
-      if (tid == 0) st_release_gpu(p.seq_flag + sq, 1);
+      if (dvalid) {
+        float* wp = p.ws_param + (((size_t)b * p.nseg + kp) * D + d) * (N + 2);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int n = 4 * q + 2 * i;
+          wp[n] = (A2[i].x * kAscale) * my_tot[2 * i];
+          wp[n + 1] = (A2[i].y * kAscale) * my_tot[2 * i + 1];
+          if (p.dh0 && c_lo == 0) *reinterpret_cast<float2*>(p.dh0 + ((size_t)b * D + d) * N + n) = carry[i];
+        }
+        if (q == 0) {
+          wp[N] = tD;
+          wp[N + 1] = tBs;
+        }
+        if (p.seq_flag) {
+          // rows of pieces this sequence does not have stay zero for the finalize
+          for (int k2 = plan_pieces(pl, sq); k2 < p.nseg; ++k2) {
+            float* wz = p.ws_param + (((size_t)b * p.nseg + k2) * D + d) * (N + 2);
+            wz[4 * q] = wz[4 * q + 1] = wz[4 * q + 2] = wz[4 * q + 3] = 0.f;
+            if (q == 0) wz[N] = wz[N + 1] = 0.f;
+          }
+        }
+      }
+      if (p.seq_flag && kp > 0) {
+        // hand-over mode, the sequence's last piece: its final carry enters the
+        // first piece's last step; publish it and raise the flag
+        if (dvalid) {
+          float* co = p.seg_carry + (((size_t)b * p.nseg + kp - 1) * D + d) * N + 4 * q;
+          __stcg(co, carry[0].x);
+          __stcg(co + 1, carry[0].y);
+          __stcg(co + 2, carry[1].x);
+          __stcg(co + 3, carry[1].y);
+        }
+        __threadfence();
+        named_bar_sync(2, kLanes);
+        if (tid == 0) st_release_gpu(p.seq_flag + sq, 1);
+      }
     }
-  }
   }  // pieces
   // every consumer is done with TMEM (loads waited for inline, stores before
   // the loads of the same chunk): free it
