@@ -42,7 +42,8 @@ def test_status_strings_and_sizes(lib):
     assert lib.ssm_status_string(3) == b"SSM_ERR_WORKSPACE"
     assert lib.ssm_status_string(99) == b"SSM_ERR_UNKNOWN"
     assert lib.ssm_version() >= 100
-    assert [lib.ssm_num_chunks(x) for x in (0, 1, 64, 65, 4096)] == [0, 1, 1, 2, 64]
+    c = s6.CHUNK_LEN
+    assert [lib.ssm_num_chunks(x) for x in (0, 1, c, c + 1, 4096)] == [0, 1, 1, 2, 4096 // c]
     assert lib.ssm_fwd_workspace_bytes(1, 64, 16, 4, 0) == 0
     ws = lib.ssm_bwd_workspace_bytes(4, 4096, 4096, 16, 1)
     # per-64-channel-tile dBm/dCm partials plus per-batch parameter partials
@@ -108,8 +109,8 @@ def test_segment_plan(lib):
     assert s6.plan_segments(4, 4096, 4096, 16, bf16) == (1, 1)
     # 152 sequences: one range each, no cut
     assert s6.plan_segments(2, 4096, 76 * 64, 16, bf16)[1] == 1
-    # one sequence of 18 chunks: 18 ranges of one chunk
-    assert s6.plan_segments(1, 1100, 64, 16, f32)[1] == 18
+    # one sequence of 35 chunks: 35 ranges of one chunk
+    assert s6.plan_segments(1, 1100, 64, 16, f32)[1] == -(-1100 // s6.CHUNK_LEN)
     f, b = s6.plan_segments(1, 65536, 2048, 16, f32)
     assert f > 1 and b > 1
     for shape in [(1, 64, 16, 4), (2, 1023, 64, 16), (3, 5000, 200, 8), (1, 4096, 32, 16)]:

@@ -30,7 +30,7 @@ SMALL = [
     # B, L, D, N, act
     (1, 64, 16, 4, "f32"),     # the tiny workload's shape
     (2, 1, 3, 1, "f32"),       # single step, single state
-    (1, 65, 17, 3, "f32"),     # ragged chunk (65 = 64 + 1), ragged tile, odd N
+    (1, 65, 17, 3, "f32"),     # ragged chunk and tile (65 = 2*32 + 1), odd N
     (3, 130, 70, 16, "f32"),   # two tiles, three chunks
     (2, 200, 65, 5, "bf16"),
     (1, 64, 64, 16, "bf16"),
@@ -68,14 +68,16 @@ def test_tiny_workload_every_output_and_chunk_states():
     gpu = gpu_fwd_bwd(to_dev(x))
     ref = oracle_fwd_bwd(x)
     compare_all(gpu, ref, TOL["f32"])
-    # chunk state c = state before step c*64 = h_last of the first c*64 steps
+    # chunk state c = state before step c*CHUNK_LEN = h_last of the first c*CHUNK_LEN steps
+    cl = s6.CHUNK_LEN
     x2 = _inputs(2, 200, 24, 16, "f32", seed=5)
     g2 = gpu_fwd_bwd(to_dev(x2), want_bwd=False)
     cs = np64(g2["chunk_states"])
-    assert cs.shape == (2, 4, 24, 16)
+    nc = -(-200 // cl)
+    assert cs.shape == (2, nc, 24, 16)
     assert np.array_equal(cs[:, 0], x2["h0"].double().numpy())
-    for c in range(1, 4):
-        sub = {k: (v[:, : c * 64].contiguous() if k in ("u", "delta_raw", "z", "Bm", "Cm") else v)
+    for c in range(1, nc):
+        sub = {k: (v[:, : c * cl].contiguous() if k in ("u", "delta_raw", "z", "Bm", "Cm") else v)
                for k, v in x2.items()}
         _, h_ref = oracle.fwd(*[sub[k] for k in ARGS], sub["h0"])
         assert rel_err(cs[:, c], h_ref) <= TOL["f32"]
