@@ -370,28 +370,32 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
   }
 }
 
-// One decode step (T = 1).  TPC = N/4 lanes per channel, 4 states per lane,
-// with the arithmetic of the scan kernel above in the same order (softplus,
-// decays, state update, per-lane readout, the channel's lanes added in lane
-// order, skip, gate), so that L steps equal one L-step scan bit for bit.
-// Bound by HBM: each lane reads and writes its 16 bytes of state once; u,
-// delta_raw, z and Bm, Cm are shared by the lanes of a channel / a batch row.
+// One decode step (T = 1).  A thread owns 4 states of one channel for TPC
+// batch rows (TPC = N/4 lanes per channel): the channel's TPC lanes together
+// cover TPC x N states.  Work that depends only on (b, d) -- softplus of
+// delta, silu of the gate -- is done once per (b, d), by lane j for batch row
+// j of the group, and passed round with shuffles; A = -exp(A_log) is taken
+// once per thread for all its rows.  The arithmetic is the scan kernel's, in
+// the same order (softplus, decays, state update, per-lane readout, the
+// channel's lanes added in lane order, skip, gate), so that L steps equal one
+// L-step scan bit for bit.  Bound by HBM: every state is read and written
+// once (16 bytes per lane and row each way).
 template <typename Act, int TPC, bool kFast, bool kGate>
 __global__ void __launch_bounds__(256) s6_step_kernel(const FwdParams p) {
   constexpr int N = 4 * TPC;
-  const long long total = (long long)p.B * p.D * TPC;
+  const int B = p.B, D = p.D;
+  const int ngroups = (B + TPC - 1) / TPC;  // groups of TPC batch rows
+  const long long total = (long long)ngroups * D * TPC;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const bool active = idx < total;
   const long long i = active ? idx : total - 1;  // idle lanes still take part in the shuffles
   const int q = (int)(i % TPC);
-  const long long bd = i / TPC;  // b * D + d
-  const int d = (int)(bd % p.D);
-  const long long b = bd / p.D;
+  const long long gd = i / TPC;  // group * D + d
+  const int d = (int)(gd % D);
+  const int g = (int)(gd / D);
   const int lane = threadIdx.x & 31;
+  const int lead = lane - q;  // lane 0 of this channel's group
 
-  const Act* u_p = static_cast<const Act*>(p.u);
-  const float u = ld_act(u_p + bd);
-  const float raw = ld_act(static_cast<const Act*>(p.delta_raw) + bd);
   const float4 al = __ldg(reinterpret_cast<const float4*>(p.A_log + (size_t)d * N + 4 * q));
   float2 A2[2];
   {
@@ -399,40 +403,58 @@ __global__ void __launch_bounds__(256) s6_step_kernel(const FwdParams p) {
     A2[0] = kFast ? make_float2(a0 * kLog2e, a1 * kLog2e) : make_float2(a0, a1);
     A2[1] = kFast ? make_float2(a2 * kLog2e, a3 * kLog2e) : make_float2(a2, a3);
   }
-  float2 Bv[2], Cv[2];
-  if constexpr (std::is_same<Act, float>::value) {
-    const float4 bb = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.Bm) + b * N + 4 * q));
-    const float4 cc = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.Cm) + b * N + 4 * q));
-    Bv[0] = make_float2(bb.x, bb.y), Bv[1] = make_float2(bb.z, bb.w);
-    Cv[0] = make_float2(cc.x, cc.y), Cv[1] = make_float2(cc.z, cc.w);
-  } else {
-    const __nv_bfloat162* bb = reinterpret_cast<const __nv_bfloat162*>(static_cast<const Act*>(p.Bm) + b * N + 4 * q);
-    const __nv_bfloat162* cc = reinterpret_cast<const __nv_bfloat162*>(static_cast<const Act*>(p.Cm) + b * N + 4 * q);
-    Bv[0] = __bfloat1622float2(bb[0]), Bv[1] = __bfloat1622float2(bb[1]);
-    Cv[0] = __bfloat1622float2(cc[0]), Cv[1] = __bfloat1622float2(cc[1]);
-  }
-  const float4 hv = *reinterpret_cast<const float4*>(p.h0 + bd * N + 4 * q);
-  float2 h[2] = {make_float2(hv.x, hv.y), make_float2(hv.z, hv.w)};
+  const float bias = p.delta_bias[d];
+  const float Dd = p.Dp[d];
+  const Act* u_p = static_cast<const Act*>(p.u);
 
-  const float sp = softplus_k<kFast>(raw + p.delta_bias[d]);
-  const float du = sp * u;
-  const float2 dd = make_float2(sp, sp), uu = make_float2(du, du);
-  const float2 a0 = decay2<kFast>(dd, A2[0]);
-  const float2 a1 = decay2<kFast>(dd, A2[1]);
-  h[0] = ffma2(a0, h[0], fmul2(uu, Bv[0]));
-  h[1] = ffma2(a1, h[1], fmul2(uu, Bv[1]));
-  const float2 y2 = ffma2(Cv[1], h[1], fmul2(Cv[0], h[0]));
-  const float part = y2.x + y2.y;
-  // the channel's lanes are consecutive: add their partial readouts in lane order
-  float y = __shfl_sync(0xffffffffu, part, lane - q);
+  // this lane's batch row of the group: delta and the gate factor
+  const int bq = min(g * TPC + q, B - 1);
+  const float sp_q = softplus_k<kFast>(ld_act(static_cast<const Act*>(p.delta_raw) + (size_t)bq * D + d) + bias);
+  const float sl_q = kGate ? silu_k<kFast>(ld_act(static_cast<const Act*>(p.z) + (size_t)bq * D + d)) : 1.f;
+
 #pragma unroll
-  for (int r = 1; r < TPC; ++r) y += __shfl_sync(0xffffffffu, part, lane - q + r);
-  if (!active) return;
-  *reinterpret_cast<float4*>(p.h_last + bd * N + 4 * q) = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
-  if (q == 0) {
-    float o = fmaf(p.Dp[d], u, y);
-    if (kGate) o *= silu_k<kFast>(ld_act(static_cast<const Act*>(p.z) + bd));
-    st_act(static_cast<Act*>(p.out) + bd, o);
+  for (int j = 0; j < TPC; ++j) {
+    const int bj = g * TPC + j;
+    const bool row_ok = active && bj < B;
+    const long long b = row_ok ? bj : B - 1;
+    const long long bd = b * D + d;
+    const float sp = __shfl_sync(0xffffffffu, sp_q, lead + j);
+    const float sl = __shfl_sync(0xffffffffu, sl_q, lead + j);
+    const float u = ld_act(u_p + bd);
+    float2 Bv[2], Cv[2];
+    if constexpr (std::is_same<Act, float>::value) {
+      const float4 bb = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.Bm) + b * N + 4 * q));
+      const float4 cc = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.Cm) + b * N + 4 * q));
+      Bv[0] = make_float2(bb.x, bb.y), Bv[1] = make_float2(bb.z, bb.w);
+      Cv[0] = make_float2(cc.x, cc.y), Cv[1] = make_float2(cc.z, cc.w);
+    } else {
+      const __nv_bfloat162* bb = reinterpret_cast<const __nv_bfloat162*>(static_cast<const Act*>(p.Bm) + b * N + 4 * q);
+      const __nv_bfloat162* cc = reinterpret_cast<const __nv_bfloat162*>(static_cast<const Act*>(p.Cm) + b * N + 4 * q);
+      Bv[0] = __bfloat1622float2(bb[0]), Bv[1] = __bfloat1622float2(bb[1]);
+      Cv[0] = __bfloat1622float2(cc[0]), Cv[1] = __bfloat1622float2(cc[1]);
+    }
+    const float4 hv = *reinterpret_cast<const float4*>(p.h0 + bd * N + 4 * q);
+    float2 h[2] = {make_float2(hv.x, hv.y), make_float2(hv.z, hv.w)};
+    const float du = sp * u;
+    const float2 dd = make_float2(sp, sp), uu = make_float2(du, du);
+    const float2 a0 = decay2<kFast>(dd, A2[0]);
+    const float2 a1 = decay2<kFast>(dd, A2[1]);
+    h[0] = ffma2(a0, h[0], fmul2(uu, Bv[0]));
+    h[1] = ffma2(a1, h[1], fmul2(uu, Bv[1]));
+    const float2 y2 = ffma2(Cv[1], h[1], fmul2(Cv[0], h[0]));
+    const float part = y2.x + y2.y;
+    // the channel's partial readouts, added in lane order
+    float y = __shfl_sync(0xffffffffu, part, lead);
+#pragma unroll
+    for (int r = 1; r < TPC; ++r) y += __shfl_sync(0xffffffffu, part, lead + r);
+    if (row_ok) {
+      *reinterpret_cast<float4*>(p.h_last + bd * N + 4 * q) = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+      if (q == j) {
+        float o = fmaf(Dd, u, y);
+        if (kGate) o *= sl;
+        st_act(static_cast<Act*>(p.out) + bd, o);
+      }
+    }
   }
 }
 
@@ -532,7 +554,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 template <typename Act, int TPC, bool kFast>
 cudaError_t launch_step_tpc(const FwdParams& p, cudaStream_t stream) {
-  const long long threads = (long long)p.B * p.D * TPC;
+  const long long threads = (long long)((p.B + TPC - 1) / TPC) * p.D * TPC;
   const unsigned blocks = (unsigned)((threads + 255) / 256);
   if (p.z)
     s6_step_kernel<Act, TPC, kFast, true><<<blocks, 256, 0, stream>>>(p);
