@@ -305,3 +305,26 @@ def test_handover_mode(B, L, D, N, act):
             assert torch.equal(got[k], again[k]), k
     ref = oracle_fwd_bwd(x, dh_last=x["dh_last"])
     compare_all(got, ref, TOL[act])
+
+
+def _sweep_shapes(n=14, seed=1234):
+    """Seeded random shapes over the plan's regimes: dstate 4/8/16 (TMA path)
+    and others (generic path), ragged channel tiles and chunks, both dtypes."""
+    rng = np.random.default_rng(seed)
+    shapes = []
+    for _ in range(n):
+        act = "bf16" if rng.random() < 0.5 else "f32"
+        N = int(rng.choice([4, 8, 16, 16, 16, 6])) if act == "f32" else int(rng.choice([8, 16, 16]))
+        B = int(rng.integers(1, 5))
+        L = int(rng.integers(1, 700))
+        D = int(rng.integers(1, 40)) * 8
+        shapes.append((B, L, D, N, act))
+    return shapes
+
+
+@pytest.mark.parametrize("B,L,D,N,act", _sweep_shapes())
+def test_random_shape_sweep(B, L, D, N, act):
+    x = _inputs(B, L, D, N, act, seed=B * 7 + L)
+    gpu = gpu_fwd_bwd(to_dev(x), dh_last=to_dev(x)["dh_last"])
+    ref = oracle_fwd_bwd(x, dh_last=x["dh_last"])
+    compare_all(gpu, ref, TOL[act])
