@@ -102,16 +102,24 @@ int check_ws(const void* ws, size_t ws_bytes, int64_t total) {
 constexpr int kPlanSms = 152;
 
 struct FwdWorkspace {
+  s6::FwdPlan plan;  // stream plan (plan.handover) or not
   int nseg, seg_len;
-  int64_t agg_off, start_off, total;
+  int64_t agg_off, start_off, flag_off, carry_off, total;
 };
 
-FwdWorkspace fwd_ws_layout(int64_t B, int64_t L, int64_t D, int64_t N) {
+FwdWorkspace fwd_ws_layout(int64_t B, int64_t L, int64_t D, int64_t N, int act) {
   FwdWorkspace w;
-  w.nseg = s6::fwd_segments((int)B, (int)L, (int)D, (int)N, kPlanSms);
+  w.plan = s6::fwd_stream_plan((int)B, (int)L, (int)D, (int)N, act, kPlanSms);
+  w.nseg = w.plan.handover ? 1 : s6::fwd_segments((int)B, (int)L, (int)D, (int)N, kPlanSms);
   w.seg_len = (int)L;
-  w.agg_off = w.start_off = w.total = 0;
-  if (w.nseg > 1) {
+  w.agg_off = w.start_off = w.flag_off = w.carry_off = w.total = 0;
+  if (w.plan.handover) {
+    // one flag and one hand-over state (128/TPC channels x N = 512 floats) per sequence
+    const int64_t nseq = B * (int64_t)w.plan.ndt;
+    w.flag_off = 0;
+    w.carry_off = align_up(nseq * (int64_t)sizeof(int), 256);
+    w.total = align_up(w.carry_off + nseq * 512 * (int64_t)sizeof(float), 256);
+  } else if (w.nseg > 1) {
     w.seg_len = (int)(((L + w.nseg - 1) / w.nseg + SSM_CHUNK_LEN - 1) / SSM_CHUNK_LEN * SSM_CHUNK_LEN);
     w.nseg = (int)((L + w.seg_len - 1) / w.seg_len);
     const int64_t cells = B * w.nseg * D * N;
@@ -187,12 +195,19 @@ int fwd_common(int64_t B, int64_t L, int64_t D, int64_t N, int act, const void* 
   p.nchunks = (int)ssm_num_chunks(L);
   p.status = s6::device_status_word();
   if (!p.status) return fail(SSM_ERR_CUDA, "cannot locate the device status word");
-  const FwdWorkspace w = fwd_ws_layout(B, L, D, N);
+  const FwdWorkspace w = fwd_ws_layout(B, L, D, N, act);
   S6_TRY(check_ws(ws, ws_bytes, w.total));
   p.nseg = 1;
   p.seg_len = (int)L;
   p.seg_agg = p.seg_start = nullptr;
+  p.plan = w.plan;
+  p.seq_flag = nullptr;
+  p.seq_carry = nullptr;
   const bool tma = s6::fwd_tma_supported(p, act);
+  if (tma && w.plan.handover && !step) {
+    p.seq_flag = reinterpret_cast<int*>(static_cast<char*>(ws) + w.flag_off);
+    p.seq_carry = reinterpret_cast<float*>(static_cast<char*>(ws) + w.carry_off);
+  }
   if (tma && w.nseg > 1) {
     p.nseg = w.nseg;
     p.seg_len = w.seg_len;
@@ -286,7 +301,7 @@ int64_t ssm_num_chunks(int64_t seqlen) {
 
 int64_t ssm_fwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act) {
   if (check_shape(batch, seqlen, dim, dstate, act) != SSM_OK) return -1;
-  return fwd_ws_layout(batch, seqlen, dim, dstate).total;
+  return fwd_ws_layout(batch, seqlen, dim, dstate, act).total;
 }
 
 int64_t ssm_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act) {
@@ -298,7 +313,7 @@ int ssm_plan_segments(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate
                       int* fwd_segments, int* bwd_segments) {
   const int rc = check_shape(batch, seqlen, dim, dstate, act);
   if (rc != SSM_OK) return rc;
-  if (fwd_segments) *fwd_segments = fwd_ws_layout(batch, seqlen, dim, dstate).nseg;
+  if (fwd_segments) *fwd_segments = fwd_ws_layout(batch, seqlen, dim, dstate, act).nseg;
   if (bwd_segments) {
     const BwdWorkspace w = bwd_ws_layout(batch, seqlen, dim, dstate);
     *bwd_segments = w.plan.handover ? 1 : w.nseg;

@@ -108,7 +108,7 @@ __device__ __forceinline__ float2 decay2(float2 dd, float2 A) {
 // aggregate pass of the chunked parallel scan -- from a zero state, run the
 // segment and store its end state and its decay product exp(A * sum(delta))
 // (no readout, no output; z and Cm are not loaded).
-template <typename Act, int TPC, bool kSave, bool kFast, bool kGate, bool kAgg = false>
+template <typename Act, int TPC, bool kSave, bool kFast, bool kGate, bool kAgg = false, bool kStream = false>
 __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid_constant__ FwdTmaParams P) {
   constexpr int N = 4 * TPC;
   constexpr int kCh = kScanThreads / TPC;  // channels per CTA
@@ -144,11 +144,46 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
     return;
   }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.y, d0 = blockIdx.x * kCh, seg = blockIdx.z;
   const int L = p.L, D = p.D;
-  const int t_begin = seg * p.seg_len;                  // first step of this segment
-  const int t_end = min(L, t_begin + p.seg_len);
-  const int ntiles = (t_end - t_begin + kTT - 1) / kTT;
+  // Work items, walked in the same order by every role.  Grid mode: one item,
+  // (channel tile blockIdx.x, batch blockIdx.y, time segment blockIdx.z).
+  // Stream mode (kStream): the CTA's range of the plan's chunk units, laid
+  // out sequence by sequence with time running backwards inside a sequence,
+  // so that a range starts with the first piece (in time) of a sequence and
+  // ends with the last piece of another; item = (sequence, its chunks).
+  const FwdPlan& pl = p.plan;
+  const int u_begin = kStream ? (int)plan_bound(pl, blockIdx.x) : 0;
+  const int u_end = kStream ? (int)plan_bound(pl, blockIdx.x + 1) : 1;
+  struct Item {
+    int b, d0, t_begin, t_end, next, sq;
+    bool first, last;  // the item starts / ends its sequence
+  };
+  auto item_at = [&](int u) {
+    Item it;
+    if (kStream) {
+      const int sq = u / pl.nch, S0 = sq * pl.nch;
+      it.next = min(S0 + pl.nch, u_end);
+      const int c_lo = pl.nch - (it.next - S0), c_hi = pl.nch - (u - S0);
+      it.sq = sq;
+      it.b = sq / pl.ndt;
+      it.d0 = (sq % pl.ndt) * kCh;
+      it.t_begin = c_lo * kChunk;
+      it.t_end = min(L, c_hi * kChunk);
+      it.first = c_lo == 0;
+      it.last = c_hi == pl.nch;
+    } else {
+      const int seg = blockIdx.z;
+      it.next = 1;
+      it.sq = 0;
+      it.b = blockIdx.y;
+      it.d0 = blockIdx.x * kCh;
+      it.t_begin = seg * p.seg_len;
+      it.t_end = min(L, it.t_begin + p.seg_len);
+      it.first = seg == 0;
+      it.last = seg == (int)gridDim.z - 1;
+    }
+    return it;
+  };
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -166,7 +201,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
   auto tile_B = [&](int s) { return tile_u(s) + 3 * kTile; };
   auto tile_C = [&](int s) { return tile_u(s) + 3 * kTile + kBC; };
   // activation tile: kNBox boxes of kChBox channels side by side
-  auto load_act = [&](Act* dst, const CUtensorMap* m, uint64_t* bar, int row) {
+  auto load_act = [&](Act* dst, const CUtensorMap* m, uint64_t* bar, int d0, int row) {
 #pragma unroll
     for (int bx = 0; bx < AT::kNBox; ++bx)
       tma_load_2d(reinterpret_cast<unsigned char*>(dst) + bx * (kTT * AT::kRowB), m, bar, d0 + bx * AT::kChBox, row);
@@ -182,19 +217,28 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
       tma_prefetch_desc(&P.map_C);
       constexpr bool kZ = kGate && !kAgg;
       const uint32_t bytes = (uint32_t)(((kZ ? 3 : 2) * kTile + (kAgg ? 1 : 2) * kBC) * sizeof(Act));
-      int issued = 0;
-      for (int k = 0; k < ntiles; ++k) {
-        const int s = k % S;
-        const uint32_t use = (uint32_t)(k / S);
-        if (k >= S && !mbar_wait(&empty[s], (use - 1) & 1, p.status)) break;
-        mbar_arrive_expect_tx(&full[s], bytes);
-        const int row = b * L + t_begin + k * kTT;
-        load_act(tile_u(s), &P.map_u, &full[s], row);
-        load_act(tile_raw(s), &P.map_raw, &full[s], row);
-        if (kZ) load_act(tile_z(s), &P.map_z, &full[s], row);
-        tma_load_2d(tile_B(s), &P.map_B, &full[s], 0, row);
-        if (!kAgg) tma_load_2d(tile_C(s), &P.map_C, &full[s], 0, row);
-        issued = k + 1;
+      int issued = 0;  // tiles issued over all items
+      bool ok = true;
+      for (int u = u_begin; u < u_end && ok;) {
+        const Item it = item_at(u);
+        u = it.next;
+        const int ntiles = (it.t_end - it.t_begin + kTT - 1) / kTT;
+        for (int k = 0; k < ntiles; ++k) {
+          const int s = issued % S;
+          const uint32_t use = (uint32_t)(issued / S);
+          if (issued >= S && !mbar_wait(&empty[s], (use - 1) & 1, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], bytes);
+          const int row = it.b * L + it.t_begin + k * kTT;
+          load_act(tile_u(s), &P.map_u, &full[s], it.d0, row);
+          load_act(tile_raw(s), &P.map_raw, &full[s], it.d0, row);
+          if (kZ) load_act(tile_z(s), &P.map_z, &full[s], it.d0, row);
+          tma_load_2d(tile_B(s), &P.map_B, &full[s], 0, row);
+          if (!kAgg) tma_load_2d(tile_C(s), &P.map_C, &full[s], 0, row);
+          ++issued;
+        }
       }
       // never leave with copies in flight: wait for the last use of every stage
       for (int s = 0; s < S && s < issued; ++s) {
@@ -207,19 +251,29 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
   if (warp == 5) {
     // ---------------- converter: bf16 Bm/Cm tile -> f32, once per stage use
     if (kBf16) {
-      for (int k = 0; k < ntiles; ++k) {
-        const int s = k % S;
-        if (!mbar_wait(&full[s], (uint32_t)(k / S) & 1, p.status)) break;
-        const __nv_bfloat162* tb = reinterpret_cast<const __nv_bfloat162*>(tile_B(s));
-        const __nv_bfloat162* tc = reinterpret_cast<const __nv_bfloat162*>(tile_C(s));
-        float* dst = bcf + (size_t)s * kTT * 2 * N;
+      int kt = 0;  // tiles over all items
+      bool ok = true;
+      for (int u = u_begin; u < u_end && ok;) {
+        const Item it = item_at(u);
+        u = it.next;
+        const int ntiles = (it.t_end - it.t_begin + kTT - 1) / kTT;
+        for (int k = 0; k < ntiles; ++k, ++kt) {
+          const int s = kt % S;
+          if (!mbar_wait(&full[s], (uint32_t)(kt / S) & 1, p.status)) {
+            ok = false;
+            break;
+          }
+          const __nv_bfloat162* tb = reinterpret_cast<const __nv_bfloat162*>(tile_B(s));
+          const __nv_bfloat162* tc = reinterpret_cast<const __nv_bfloat162*>(tile_C(s));
+          float* dst = bcf + (size_t)s * kTT * 2 * N;
 #pragma unroll 4
-        for (int e = lane; e < kBC / 2; e += 32) {
-          const int t = (2 * e) / N, n = (2 * e) % N;
-          *reinterpret_cast<float2*>(dst + (t * 2 + 0) * N + n) = __bfloat1622float2(tb[e]);
-          if (!kAgg) *reinterpret_cast<float2*>(dst + (t * 2 + 1) * N + n) = __bfloat1622float2(tc[e]);
+          for (int e = lane; e < kBC / 2; e += 32) {
+            const int t = (2 * e) / N, n = (2 * e) % N;
+            *reinterpret_cast<float2*>(dst + (t * 2 + 0) * N + n) = __bfloat1622float2(tb[e]);
+            if (!kAgg) *reinterpret_cast<float2*>(dst + (t * 2 + 1) * N + n) = __bfloat1622float2(tc[e]);
+          }
+          mbar_arrive(&conv[s]);
         }
-        mbar_arrive(&conv[s]);
       }
     }
     return;
@@ -227,16 +281,40 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
 
   // ---------------- consumers
   const int q = tid % TPC;    // state group: states 4q .. 4q+3
-  const int cl = tid / TPC;   // channel within the CTA
-  const int d = d0 + cl;
-  const bool dvalid = d < D;
-  const int dc = dvalid ? d : D - 1;
+  const int cl = tid / TPC;   // channel within the tile
   // swizzled offsets of this lane's channel in the rows of its owned steps
   // (minus the row's own offset; the pattern repeats every 8 rows)
   int colo[kPer];
 #pragma unroll
   for (int j = 0; j < kPer; ++j) colo[j] = AT::col(j * TPC + q, cl);
 
+  // A wait that gives up marks the CTA failed (status word set); the
+  // consumers then skip every later wait but keep the same control flow, so
+  // that every named barrier is still reached by all of them.
+  int kt = 0;  // tiles over all items
+  bool failed = false;
+  for (int u = u_begin; u < u_end;) {
+  const Item it = item_at(u);
+  u = it.next;
+  const int b = it.b, t_begin = it.t_begin, t_end = it.t_end;
+  const int ntiles = (t_end - t_begin + kTT - 1) / kTT;
+  const int d = it.d0 + cl;
+  const bool dvalid = d < D;
+  const int dc = dvalid ? d : D - 1;
+  const float* hin;  // initial state: zero (aggregate pass), handed over, the composed segment start, or h0
+  if (kAgg) {
+    hin = nullptr;
+  } else if (kStream && !it.first) {
+    // stream mode: the state at t_begin comes from the CTA walking the sequence's first piece
+    if (lane == 0 && !failed) failed = !flag_wait(p.seq_flag + it.sq, p.status);
+    failed = __shfl_sync(0xffffffffu, failed, 0);
+    __syncwarp();
+    hin = p.seq_carry + ((size_t)it.sq * kCh + cl) * N;
+  } else if (!kStream && p.nseg > 1) {
+    hin = p.seg_start + (((size_t)b * p.nseg + blockIdx.z) * D + dc) * N;
+  } else {
+    hin = p.h0 ? p.h0 + ((size_t)b * D + dc) * N : nullptr;
+  }
   float2 A2[2], h[2];
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
@@ -244,21 +322,18 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
     const float a0 = -expf(p.A_log[dc * N + n]);
     const float a1 = -expf(p.A_log[dc * N + n + 1]);
     A2[i] = kFast ? make_float2(a0 * kLog2e, a1 * kLog2e) : make_float2(a0, a1);
-    // initial state: zero (aggregate pass), the composed segment start, or h0
-    const float* hin = kAgg ? nullptr
-                            : (p.nseg > 1 ? p.seg_start + (((size_t)b * p.nseg + seg) * D + dc) * N : (p.h0 ? p.h0 + ((size_t)b * D + dc) * N : nullptr));
-    h[i] = hin ? make_float2(hin[n], hin[n + 1]) : make_float2(0.f, 0.f);
+    h[i] = hin ? make_float2(__ldcg(hin + n), __ldcg(hin + n + 1)) : make_float2(0.f, 0.f);
   }
   const float bias = p.delta_bias[dc];
   const float Dd = p.Dp[dc];
   Act* outp = static_cast<Act*>(p.out) + (size_t)b * L * D + d;
   float dsum = 0.f;  // aggregate pass: sum of delta over the segment (per-tile partials added)
 
-  for (int k = 0; k < ntiles; ++k) {
-    const int s = k % S;
-    const uint32_t par = (uint32_t)(k / S) & 1;
-    if (!mbar_wait(&full[s], par, p.status)) break;
-    if (kBf16 && !mbar_wait(&conv[s], par, p.status)) break;
+  for (int k = 0; k < ntiles; ++k, ++kt) {
+    const int s = kt % S;
+    const uint32_t par = (uint32_t)(kt / S) & 1;
+    if (!failed) failed = !mbar_wait(&full[s], par, p.status);
+    if (kBf16 && !failed) failed = !mbar_wait(&conv[s], par, p.status);
     const int tbase = t_begin + k * kTT;
     const int cnt = min(kTT, t_end - tbase);
     if (kSave && !kAgg && (tbase % kChunk) == 0 && dvalid) {
@@ -356,7 +431,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
   if (kAgg) {
     if (dvalid) {
       // decay product over the segment, exp(A * sum(delta)), and the end state from zero
-      float* ag = p.seg_agg + ((((size_t)b * p.nseg + seg) * D + d) * N + 4 * q) * 2;
+      float* ag = p.seg_agg + ((((size_t)b * p.nseg + blockIdx.z) * D + d) * N + 4 * q) * 2;
       const float2 x0 = fmul2(make_float2(dsum, dsum), A2[0]);
       const float2 x1 = fmul2(make_float2(dsum, dsum), A2[1]);
       const float P0 = kFast ? ex2_approx(x0.x) : expf(x0.x), P1 = kFast ? ex2_approx(x0.y) : expf(x0.y);
@@ -364,10 +439,22 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
       reinterpret_cast<float4*>(ag)[0] = make_float4(P0, h[0].x, P1, h[0].y);
       reinterpret_cast<float4*>(ag)[1] = make_float4(P2, h[1].x, P3, h[1].y);
     }
-  } else if (p.h_last && dvalid && seg == (int)gridDim.z - 1) {
+  } else if (p.h_last && dvalid && it.last) {
     float* hl = p.h_last + ((size_t)b * D + d) * N + 4 * q;
     *reinterpret_cast<float4*>(hl) = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
   }
+  if (kStream && !it.last) {
+    // stream mode, the sequence's first piece: hand the state at t_end over
+    float* co = p.seq_carry + ((size_t)it.sq * kCh + cl) * N + 4 * q;
+    __stcg(co, h[0].x);
+    __stcg(co + 1, h[0].y);
+    __stcg(co + 2, h[1].x);
+    __stcg(co + 3, h[1].y);
+    __threadfence();
+    named_bar_sync(1, kScanThreads);
+    if (tid == 0) st_release_gpu(p.seq_flag + it.sq, 1);
+  }
+  }  // items
 }
 
 // One decode step (T = 1).  A thread owns 4 states of one channel for TPC
@@ -528,8 +615,45 @@ cudaError_t launch_kernel(const FwdTmaParams& P, int nz, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// Stream mode: the plan's P CTAs, exactly three per SM (the shared memory
+// request is raised so that a fourth does not fit), launched cooperatively so
+// that all are resident while they hand states over.  Returns
+// cudaErrorCooperativeLaunchTooLarge when this GPU cannot hold them.
+constexpr size_t kStreamSmemFloor = 60 * 1024;
+template <typename Act, int TPC, bool kSave, bool kFast, bool kGate>
+cudaError_t launch_stream(const FwdTmaParams& P, cudaStream_t stream) {
+  auto kern = s6_fwd_tma_kernel<Act, TPC, kSave, kFast, kGate, false, true>;
+  const size_t smem = std::max<size_t>(fwd_smem_bytes<Act, TPC>(), kStreamSmemFloor);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0, sms = 0, dev = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFwdWarps * 32, smem);
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (per_sm != 3 || (long long)per_sm * sms < P.p.plan.P) return cudaErrorCooperativeLaunchTooLarge;
+  e = cudaMemsetAsync(P.p.seq_flag, 0, sizeof(int) * (size_t)P.p.B * P.p.plan.ndt, stream);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)P.p.plan.P);
+  cfg.blockDim = dim3(kFwdWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, P);
+}
+
 template <typename Act, int TPC, bool kSave, bool kFast, bool kGate>
 cudaError_t launch_one(const FwdTmaParams& P, cudaStream_t stream) {
+  if (P.p.plan.handover && P.p.seq_flag) {
+    const cudaError_t e = launch_stream<Act, TPC, kSave, kFast, kGate>(P, stream);
+    if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+    (void)cudaGetLastError();  // not three resident per SM here: the grid mode gives the same result
+  }
   if (P.p.nseg > 1) {
     // chunked parallel scan: segment aggregates -> carries -> all segments at once
     cudaError_t e = launch_kernel<Act, TPC, false, kFast, kGate, true>(P, P.p.nseg - 1, stream);
@@ -590,6 +714,36 @@ cudaError_t launch_step(const FwdParams& p, int act, cudaStream_t stream) {
   if (tpc == 2) return launch_step_tpc<float, 2, false>(p, stream);
   if (tpc == 1) return launch_step_tpc<float, 1, false>(p, stream);
   return cudaErrorInvalidValue;
+}
+
+// Stream plan: 3 * sms equal ranges of chunk units over the (batch,
+// 128/TPC-channel tile) sequences.  Taken when some sequence is cut, none
+// more than once, and no range is shorter than a sequence (so the first
+// piece of a cut sequence is done before its last piece is reached); the
+// grid mode's tail wave (sequences not a multiple of the resident CTAs) then
+// disappears.
+FwdPlan fwd_stream_plan(int B, int L, int D, int N, int act, int sms) {
+  FwdPlan pl;
+  pl.handover = false;
+  pl.maxp = 1;
+  pl.P = 1;
+  pl.U = 1;
+  pl.nch = L > 0 ? (L + kChunk - 1) / kChunk : 0;
+  if (!(N == 4 || N == 8 || N == 16) || (act == SSM_BF16 && N == 4) || B <= 0 || D <= 0 || pl.nch == 0) return pl;
+  const int kch = kScanThreads / (N / 4);
+  pl.ndt = (D + kch - 1) / kch;
+  const long long U = (long long)B * pl.ndt * pl.nch;
+  const int P = 3 * sms;
+  if (U < P || U >= (1LL << 31)) return pl;
+  pl.U = U;
+  pl.P = P;
+  const long long nseq = (long long)B * pl.ndt;
+  for (long long sq = 0; sq < nseq; ++sq) pl.maxp = std::max(pl.maxp, plan_pieces(pl, sq));
+  pl.handover = pl.maxp == 2 && (long long)pl.nch <= pl.U / pl.P;
+  // only worth it when the grid mode has a tail wave: sequences not a
+  // multiple of the four resident CTAs per SM
+  if (nseq % (4LL * sms) == 0) pl.handover = false;
+  return pl;
 }
 
 // Segments are used when the (batch x channel-tile) grid alone would leave

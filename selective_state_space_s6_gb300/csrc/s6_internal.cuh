@@ -20,6 +20,53 @@ constexpr unsigned int kStatusLayoutBit = 2u;       // same bit as kStatusLayout
 
 // ---------------------------------------------------------------- params
 
+// Work plan of a persistent scan: the (batch, channel tile) sequences, each
+// of nch chunks, are laid end to end as U = nseq * nch chunk units
+// (sequence s = b * ndt + j) and cut into P equal ranges, one per persistent
+// CTA (range w = [bound(w), bound(w + 1)), bound(w) = floor(w * U / P)).  A
+// range covers pieces of one or more sequences; a sequence cut by range
+// boundaries has K > 1 pieces, numbered in time order.  The plan is a
+// function of the shape only.
+//   Backward (64-channel tiles, unit s * nch + c): piece k > 0 needs the
+//   adjoint carry of the pieces after it -- handed over between CTAs, or
+//   composed from piece aggregates (the chunked parallel scan); piece k of
+//   sequence (b, j) owns row b * maxp + k of the parameter partials.
+//   Forward (128/TPC-channel tiles, unit s * nch + (nch - 1 - c)): a range
+//   starts with a sequence's first piece and ends with another's last, whose
+//   start state the CTA holding the first piece hands over.
+struct ScanPlan {
+  long long U;  // chunk units
+  int P;        // worker CTAs (ranges), 1 <= P <= U
+  int nch;      // chunks per sequence
+  int ndt;      // 64-channel tiles
+  int maxp;     // most pieces any sequence has
+  // carries handed from CTA to CTA (no aggregate pass): every sequence in at
+  // most two pieces and no range shorter than a sequence
+  bool handover;
+};
+
+__host__ __device__ inline long long plan_bound(const ScanPlan& pl, long long w) { return w * pl.U / pl.P; }
+// number of w in [0, P] with plan_bound(w) <= X, for 0 <= X < U
+__host__ __device__ inline long long plan_count_le(const ScanPlan& pl, long long X) {
+  return ((X + 1) * pl.P + pl.U - 1) / pl.U;
+}
+// pieces of sequence s
+__host__ __device__ inline int plan_pieces(const ScanPlan& pl, long long s) {
+  const long long S0 = s * pl.nch, S1 = S0 + pl.nch;
+  return (int)(plan_count_le(pl, S1 - 1) - plan_count_le(pl, S0)) + 1;
+}
+// chunk range [c_lo, c_hi) of piece k of sequence s
+__host__ __device__ inline void plan_piece_range(const ScanPlan& pl, long long s, int k, int& c_lo, int& c_hi) {
+  const long long S0 = s * pl.nch;
+  const long long wa = plan_count_le(pl, S0);  // first range boundary after the sequence start
+  const int K = plan_pieces(pl, s);
+  c_lo = k == 0 ? 0 : (int)(plan_bound(pl, wa + k - 1) - S0);
+  c_hi = k == K - 1 ? pl.nch : (int)(plan_bound(pl, wa + k) - S0);
+}
+
+using BwdPlan = ScanPlan;
+using FwdPlan = ScanPlan;
+
 struct FwdParams {
   const void* u;
   const void* delta_raw;
@@ -42,47 +89,15 @@ struct FwdParams {
   int seg_len, nseg;
   float* seg_agg;
   float* seg_start;
+  // Stream mode (plan.handover, cooperative launch of plan.P CTAs): the CTA
+  // walking a sequence's first piece stores the state it ends with in
+  // seq_carry [nseq][128/TPC][N] and raises seq_flag[sequence]; the CTA
+  // walking the last piece waits for it.  nullptr = grid mode.
+  FwdPlan plan;
+  int* seq_flag;
+  float* seq_carry;
   int B, L, D, N, nchunks;
 };
-
-// Work plan of the TMA backward: the (batch, 64-channel tile) sequences,
-// each of nch chunks, are laid end to end as U = nseq * nch chunk units
-// (sequence s = b * ndt + j, unit s * nch + c) and cut into P equal ranges,
-// one per persistent CTA (range w = [bound(w), bound(w + 1)), bound(w) =
-// floor(w * U / P)).  A range covers pieces of one or more sequences; a
-// sequence cut by range boundaries has K > 1 pieces, numbered in time order.
-// Piece k > 0 needs the adjoint aggregate of the pieces after it (the chunked
-// parallel scan); piece k of sequence (b, j) owns row b * maxp + k of the
-// parameter partials.  The plan is a function of the shape only.
-struct BwdPlan {
-  long long U;  // chunk units
-  int P;        // worker CTAs (ranges), 1 <= P <= U
-  int nch;      // chunks per sequence
-  int ndt;      // 64-channel tiles
-  int maxp;     // most pieces any sequence has
-  // carries handed from CTA to CTA (no aggregate pass): every sequence in at
-  // most two pieces and no range shorter than a sequence
-  bool handover;
-};
-
-__host__ __device__ inline long long plan_bound(const BwdPlan& pl, long long w) { return w * pl.U / pl.P; }
-// number of w in [0, P] with plan_bound(w) <= X, for 0 <= X < U
-__host__ __device__ inline long long plan_count_le(const BwdPlan& pl, long long X) {
-  return ((X + 1) * pl.P + pl.U - 1) / pl.U;
-}
-// pieces of sequence s
-__host__ __device__ inline int plan_pieces(const BwdPlan& pl, long long s) {
-  const long long S0 = s * pl.nch, S1 = S0 + pl.nch;
-  return (int)(plan_count_le(pl, S1 - 1) - plan_count_le(pl, S0)) + 1;
-}
-// chunk range [c_lo, c_hi) of piece k of sequence s
-__host__ __device__ inline void plan_piece_range(const BwdPlan& pl, long long s, int k, int& c_lo, int& c_hi) {
-  const long long S0 = s * pl.nch;
-  const long long wa = plan_count_le(pl, S0);  // first range boundary after the sequence start
-  const int K = plan_pieces(pl, s);
-  c_lo = k == 0 ? 0 : (int)(plan_bound(pl, wa + k - 1) - S0);
-  c_hi = k == K - 1 ? pl.nch : (int)(plan_bound(pl, wa + k) - S0);
-}
 
 struct BwdParams {
   const void* u;
@@ -139,6 +154,9 @@ bool bwd_tma_supported(const BwdParams& p, int act);
 cudaError_t launch_bwd_tma(const BwdParams& p, int act, cudaStream_t stream);
 // The TMA backward's work plan for this shape with `sms` worker CTAs.
 BwdPlan bwd_plan(int B, int L, int D, int N, int sms);
+// The TMA forward's stream plan (three CTAs on each of `sms` SMs); handover
+// is false when the grid mode is kept.
+FwdPlan fwd_stream_plan(int B, int L, int D, int N, int act, int sms);
 cudaError_t launch_reduce_dbc(const float* ws_dbc, int ndt, int B, int L, int N, void* dBm,
                               void* dCm, int act, cudaStream_t stream);
 cudaError_t launch_reduce_params(const float* ws_param, int B, int D, int N, float* dA_log,

@@ -328,3 +328,24 @@ def test_random_shape_sweep(B, L, D, N, act):
     gpu = gpu_fwd_bwd(to_dev(x), dh_last=to_dev(x)["dh_last"])
     ref = oracle_fwd_bwd(x, dh_last=x["dh_last"])
     compare_all(gpu, ref, TOL[act])
+
+
+@pytest.mark.parametrize("B,L,D,N,act", [(5, 192, 3072, 16, "f32"), (4, 160, 4096, 16, "bf16")])
+def test_forward_stream_mode(B, L, D, N, act):
+    """Shapes whose forward runs in stream mode (3 CTAs per SM over equal
+    ranges of chunks, the state of a cut sequence handed from CTA to CTA):
+    outputs, final state and chunk states against the oracle."""
+    a = s6.SSM_BF16 if act == "bf16" else s6.SSM_F32
+    assert s6.plan_segments(B, L, D, N, a)[0] == 1 and s6.fwd_workspace_bytes(B, L, D, N, a) > 0
+    x = _inputs(B, L, D, N, act, seed=31)
+    xd = to_dev(x)
+    got = gpu_fwd_bwd(xd, dh_last=xd["dh_last"])
+    ref = oracle_fwd_bwd(x, dh_last=x["dh_last"])
+    compare_all(got, ref, TOL[act])
+    cl = s6.CHUNK_LEN
+    cs = np64(got["chunk_states"])
+    for c in (1, (L - 1) // cl):
+        sub = {k: (v[:, : c * cl].contiguous() if k in ("u", "delta_raw", "z", "Bm", "Cm") else v)
+               for k, v in x.items()}
+        _, h_ref = oracle.fwd(*[sub[k] for k in ARGS], sub["h0"])
+        assert rel_err(cs[:, c], h_ref) <= TOL[act]
