@@ -174,3 +174,103 @@ def step(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h):
     if rc != 0:
         raise ValueError(f"s6o_step failed with code {rc}")
     return out, h_new
+
+
+# ------------------------------------------------------------------ conv1d
+# The causal depthwise conv1d + SiLU in front of the scan: ``conv1d_oracle.c``
+# (plain sequential C, f64), built into its own library.
+
+_CONV_SRC = os.path.join(_HERE, "conv1d_oracle.c")
+_CONV_LIB_PATH = os.path.join(_BUILD_DIR, "libconv1d_oracle.so")
+_conv_lib = None
+
+
+def build_conv1d(force: bool = False, src: str = None, out: str = None) -> str:
+    """Compile ``conv1d_oracle.c`` (or ``src``) into a shared library (gcc, -O2)."""
+    src = src or _CONV_SRC
+    out = out or _CONV_LIB_PATH
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+                    "-Wall", "-o", tmp, src, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _open_conv(path):
+    lib = ctypes.CDLL(path)
+    i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    lib.c1o_fwd.argtypes = [i64] * 4 + [vp] * 6
+    lib.c1o_fwd.restype = ci
+    lib.c1o_bwd.argtypes = [i64] * 4 + [vp] * 9
+    lib.c1o_bwd.restype = ci
+    lib.c1o_step.argtypes = [i64] * 3 + [vp] * 5
+    lib.c1o_step.restype = ci
+    return lib
+
+
+def _load_conv():
+    global _conv_lib
+    with _lock:
+        if _conv_lib is None:
+            _conv_lib = _open_conv(build_conv1d())
+    return _conv_lib
+
+
+@contextlib.contextmanager
+def override_conv1d_library(path):
+    """Run the conv1d wrappers against another build (planted-mistake tests)."""
+    global _conv_lib
+    prev = _load_conv()
+    with _lock:
+        _conv_lib = _open_conv(path)
+    try:
+        yield
+    finally:
+        with _lock:
+            _conv_lib = prev
+
+
+def conv1d_fwd(x, w, bias, state0=None):
+    """Causal depthwise conv1d + SiLU.  x [B,L,D], w [D,K], bias [D], state0
+    [B,D,K-1] (the K-1 inputs before t = 0; zeros when None).  Returns
+    ``(out [B,L,D], state_last [B,D,K-1])`` as f64 arrays."""
+    x, w, bias, state0 = map(_f64, (x, w, bias, state0))
+    B, L, D = x.shape
+    K = w.shape[1]
+    out = np.full((B, L, D), np.nan)
+    state_last = np.full((B, D, max(K - 1, 0)), np.nan)
+    rc = _load_conv().c1o_fwd(B, L, D, K, _ptr(x), _ptr(w), _ptr(bias), _ptr(state0), _ptr(out),
+                              _ptr(state_last))
+    if rc != 0:
+        raise ValueError(f"c1o_fwd failed with code {rc}")
+    return out, state_last
+
+
+def conv1d_bwd(x, w, bias, state0, dout):
+    """Backward of ``loss = sum(dout * out)``: dict of f64 arrays dx, dw, dbias, dstate0."""
+    x, w, bias, state0, dout = map(_f64, (x, w, bias, state0, dout))
+    B, L, D = x.shape
+    K = w.shape[1]
+    r = {"dx": np.full((B, L, D), np.nan), "dw": np.full((D, K), np.nan), "dbias": np.full((D,), np.nan),
+         "dstate0": np.full((B, D, max(K - 1, 0)), np.nan)}
+    rc = _load_conv().c1o_bwd(B, L, D, K, _ptr(x), _ptr(w), _ptr(bias), _ptr(state0), _ptr(dout),
+                              _ptr(r["dx"]), _ptr(r["dw"]), _ptr(r["dbias"]), _ptr(r["dstate0"]))
+    if rc != 0:
+        raise ValueError(f"c1o_bwd failed with code {rc}")
+    return r
+
+
+def conv1d_step(x_t, w, bias, state):
+    """One step: x_t [B,D], state [B,D,K-1] (not modified).  Returns ``(out [B,D], state_new)``."""
+    x_t, w, bias = map(_f64, (x_t, w, bias))
+    st = _f64(state).copy()
+    B, D = x_t.shape
+    K = w.shape[1]
+    out = np.full((B, D), np.nan)
+    rc = _load_conv().c1o_step(B, D, K, _ptr(x_t), _ptr(w), _ptr(bias), _ptr(st), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"c1o_step failed with code {rc}")
+    return out, st
