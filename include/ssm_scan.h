@@ -238,6 +238,46 @@ int ssm_step(int64_t batch, int64_t dim, int64_t dstate, int act, const void *u,
              const float *A_log, const float *Dp, const float *delta_bias, float *h, void *out,
              void *stream);
 
+/* ---------------------------------------------------------------------------
+ * Causal depthwise conv1d + SiLU, the convolution in front of the scan in a
+ * Mamba block (kernels.rs page: "Multi-step conv1d forward with state saves
+ * for backward", "Multi-step conv1d backward", "Single-step depthwise conv1d
+ * forward with SiLU"; deterministic_backward.py page: weight and bias
+ * gradients summed in a fixed order).  K = width taps per channel, 1..8:
+ *   pre[b,t,d] = bias[d] + sum_{k<K} w[d][k] * xx(b, t-(K-1)+k, d)
+ *   out[b,t,d] = pre * sigmoid(pre)
+ * where xx(b,t,d) = x[b][t][d] for t >= 0 and state0[b][d][K-1+t] for t < 0
+ * (the K-1 inputs before the first step, oldest first; zeros when state0 is
+ * NULL).  Layouts: x, out, dout, dx [B][L][D] (act dtype); w [D][K], bias
+ * [D] f32; states [B][D][K-1] in the act dtype; dstate0 [B][D][K-1] f32.
+ * Same pointer and error rules as the scan entry points.
+ */
+#define SSM_MAX_CONV_WIDTH 8
+
+/* Forward.  state_last (nullable) receives the last K-1 inputs (the state to
+ * continue from: a second call on the next steps with state0 = state_last
+ * equals one call on the whole sequence, bit for bit). */
+int ssm_conv1d_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t width, int act,
+                   const void *x, const float *w, const float *bias, const void *state0, void *out,
+                   void *state_last, void *stream);
+
+/* Scratch bytes ssm_conv1d_bwd needs in `ws` (per-run partial sums of dw and
+ * dbias); -1 for an invalid shape. */
+int64_t ssm_conv1d_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t dim, int64_t width, int act);
+
+/* Backward of loss = sum dout * out: dx (act), dw, dbias (f32, overwritten;
+ * sums over (b, t) in a fixed order, bit-identical from call to call), and
+ * dstate0 (nullable, f32) = the gradient of the initial state. */
+int ssm_conv1d_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t width, int act,
+                   const void *x, const float *w, const float *bias, const void *state0,
+                   const void *dout, void *dx, float *dw, float *dbias, float *dstate0, void *ws,
+                   size_t ws_bytes, void *stream);
+
+/* One step: x [B][D], state [B][D][K-1] read and shifted in place (it takes
+ * x as its newest entry), out [B][D].  Steps in a row equal ssm_conv1d_fwd. */
+int ssm_conv1d_step(int64_t batch, int64_t dim, int64_t width, int act, const void *x,
+                    const float *w, const float *bias, void *state, void *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -464,4 +464,95 @@ int ssm_step(int64_t batch, int64_t dim, int64_t dstate, int act, const void* u,
                     h, out, h, nullptr, false, nullptr, 0, stream, /*step=*/true);
 }
 
+// ---------------------------------------------------------------- conv1d
+
+int check_conv(int64_t B, int64_t L, int64_t D, int64_t K, int act) {
+  if (act != SSM_F32 && act != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "act must be SSM_F32 or SSM_BF16, got %d", act);
+  if (B < 0 || L < 0 || D < 0) return fail(SSM_ERR_INVALID_ARG, "negative shape");
+  if (K < 1) return fail(SSM_ERR_INVALID_ARG, "width must be >= 1, got %lld", (long long)K);
+  if (K > SSM_MAX_CONV_WIDTH) return fail(SSM_ERR_UNSUPPORTED, "width %lld > %d is not supported", (long long)K, SSM_MAX_CONV_WIDTH);
+  if (B * L * D >= kMaxElems || B * D * K >= kMaxElems) return fail(SSM_ERR_UNSUPPORTED, "problem too large for 31-bit indexing");
+  return SSM_OK;
+}
+
+int ssm_conv1d_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t width, int act, const void* x,
+                   const float* w, const float* bias, const void* state0, void* out, void* state_last,
+                   void* stream) {
+  const int64_t B = batch, L = seqlen, D = dim, K = width;
+  S6_TRY(check_conv(B, L, D, K, act));
+  const size_t e = act_size(act);
+  S6_TRY(need(x, B * L * D, e, "x"));
+  S6_TRY(need(w, D * K, 4, "w"));
+  S6_TRY(need(bias, D, 4, "bias"));
+  S6_TRY(opt(state0, e, "state0"));
+  S6_TRY(need(out, B * L * D, e, "out"));
+  S6_TRY(opt(state_last, e, "state_last"));
+  g_last_error[0] = 0;
+  if (B == 0 || D == 0) return SSM_OK;
+  s6::ConvParams p = {};
+  p.x = x; p.w = w; p.bias = bias; p.state0 = state0; p.out = out; p.state_last = state_last;
+  p.B = (int)B; p.L = (int)L; p.D = (int)D; p.K = (int)K;
+  const cudaError_t ce = s6::launch_conv1d(p, act, false, static_cast<cudaStream_t>(stream));
+  return ce == cudaSuccess ? SSM_OK : cuda_fail(ce, "ssm_conv1d_fwd launch");
+}
+
+int64_t ssm_conv1d_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t dim, int64_t width, int act) {
+  if (check_conv(batch, seqlen, dim, width, act) != SSM_OK) return -1;
+  return (int64_t)s6::conv1d_bwd_workspace_bytes((int)batch, (int)seqlen, (int)dim, (int)width);
+}
+
+int ssm_conv1d_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t width, int act, const void* x,
+                   const float* w, const float* bias, const void* state0, const void* dout, void* dx,
+                   float* dw, float* dbias, float* dstate0, void* ws, size_t ws_bytes, void* stream) {
+  const int64_t B = batch, L = seqlen, D = dim, K = width;
+  S6_TRY(check_conv(B, L, D, K, act));
+  const size_t e = act_size(act);
+  S6_TRY(need(x, B * L * D, e, "x"));
+  S6_TRY(need(w, D * K, 4, "w"));
+  S6_TRY(need(bias, D, 4, "bias"));
+  S6_TRY(opt(state0, e, "state0"));
+  S6_TRY(need(dout, B * L * D, e, "dout"));
+  S6_TRY(need(dx, B * L * D, e, "dx"));
+  S6_TRY(need(dw, D * K, 4, "dw"));
+  S6_TRY(need(dbias, D, 4, "dbias"));
+  S6_TRY(opt(dstate0, 4, "dstate0"));
+  const int64_t total = (int64_t)s6::conv1d_bwd_workspace_bytes((int)B, (int)L, (int)D, (int)K);
+  S6_TRY(check_ws(ws, ws_bytes, total));
+  g_last_error[0] = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (D == 0) return SSM_OK;
+  if (B == 0 || L == 0) {
+    // no steps: zero weight and bias gradients (and the state's)
+    cudaError_t ce = cudaMemsetAsync(dw, 0, sizeof(float) * D * K, st);
+    if (ce == cudaSuccess) ce = cudaMemsetAsync(dbias, 0, sizeof(float) * D, st);
+    if (ce == cudaSuccess && dstate0 && B > 0 && K > 1) ce = cudaMemsetAsync(dstate0, 0, sizeof(float) * B * D * (K - 1), st);
+    return ce == cudaSuccess ? SSM_OK : cuda_fail(ce, "ssm_conv1d_bwd");
+  }
+  s6::ConvParams p = {};
+  p.x = x; p.w = w; p.bias = bias; p.state0 = state0; p.dout = dout; p.dx = dx; p.dw = dw; p.dbias = dbias;
+  p.dstate0 = dstate0; p.ws = static_cast<float*>(ws);
+  p.B = (int)B; p.L = (int)L; p.D = (int)D; p.K = (int)K;
+  const cudaError_t ce = s6::launch_conv1d(p, act, true, st);
+  return ce == cudaSuccess ? SSM_OK : cuda_fail(ce, "ssm_conv1d_bwd launch");
+}
+
+int ssm_conv1d_step(int64_t batch, int64_t dim, int64_t width, int act, const void* x, const float* w,
+                    const float* bias, void* state, void* out, void* stream) {
+  const int64_t B = batch, D = dim, K = width;
+  S6_TRY(check_conv(B, 1, D, K, act));
+  const size_t e = act_size(act);
+  S6_TRY(need(x, B * D, e, "x"));
+  S6_TRY(need(w, D * K, 4, "w"));
+  S6_TRY(need(bias, D, 4, "bias"));
+  S6_TRY(need(state, K > 1 ? B * D * (K - 1) : 0, e, "state"));
+  S6_TRY(need(out, B * D, e, "out"));
+  g_last_error[0] = 0;
+  if (B == 0 || D == 0) return SSM_OK;
+  s6::ConvParams p = {};
+  p.x = x; p.w = w; p.bias = bias; p.state_last = state; p.out = out;
+  p.B = (int)B; p.L = 1; p.D = (int)D; p.K = (int)K;
+  const cudaError_t ce = s6::launch_conv1d_step(p, act, static_cast<cudaStream_t>(stream));
+  return ce == cudaSuccess ? SSM_OK : cuda_fail(ce, "ssm_conv1d_step launch");
+}
+
 }  // extern "C"

@@ -135,6 +135,24 @@ struct BwdParams {
   int B, L, D, N, nchunks;
 };
 
+// Causal depthwise conv1d + SiLU (s6_conv1d.cu).  For the step, x is x_t
+// [B][D], state_last is the state [B][D][K-1] read and updated in place.
+struct ConvParams {
+  const void* x;
+  const float* w;        // [D][K]
+  const float* bias;     // [D]
+  const void* state0;    // [B][D][K-1] nullable (zeros)
+  void* out;
+  void* state_last;      // [B][D][K-1] nullable
+  const void* dout;
+  void* dx;
+  float* dw;
+  float* dbias;
+  float* dstate0;        // nullable
+  float* ws;             // backward partial sums
+  int B, L, D, K;
+};
+
 // ---------------------------------------------------------------- launchers
 // Each returns the cudaError_t of its launch(es).
 
@@ -152,6 +170,9 @@ int report_error(int code, const char* fmt, ...);
 cudaError_t launch_bwd(const BwdParams& p, int act, cudaStream_t stream);
 bool bwd_tma_supported(const BwdParams& p, int act);
 cudaError_t launch_bwd_tma(const BwdParams& p, int act, cudaStream_t stream);
+size_t conv1d_bwd_workspace_bytes(int B, int L, int D, int K);
+cudaError_t launch_conv1d(const ConvParams& p, int act, bool bwd, cudaStream_t stream);
+cudaError_t launch_conv1d_step(const ConvParams& p, int act, cudaStream_t stream);
 // The TMA backward's work plan for this shape with `sms` worker CTAs.
 BwdPlan bwd_plan(int B, int L, int D, int N, int sms);
 // The TMA forward's stream plan (three CTAs on each of `sms` SMs); handover

@@ -71,6 +71,14 @@ def load_library():
         lib.ssm_scan_bwd_finalize.restype = ci
         lib.ssm_step.argtypes = [i64] * 3 + [ci] + [vp] * 10 + [vp]
         lib.ssm_step.restype = ci
+        lib.ssm_conv1d_fwd.argtypes = [i64] * 4 + [ci] + [vp] * 6 + [vp]
+        lib.ssm_conv1d_fwd.restype = ci
+        lib.ssm_conv1d_bwd_workspace_bytes.argtypes = [i64] * 4 + [ci]
+        lib.ssm_conv1d_bwd_workspace_bytes.restype = i64
+        lib.ssm_conv1d_bwd.argtypes = [i64] * 4 + [ci] + [vp] * 9 + [vp, sz, vp]
+        lib.ssm_conv1d_bwd.restype = ci
+        lib.ssm_conv1d_step.argtypes = [i64] * 3 + [ci] + [vp] * 5 + [vp]
+        lib.ssm_conv1d_step.restype = ci
         lib.ssm_selftest_wait_timeout.argtypes = [vp]
         lib.ssm_selftest_wait_timeout.restype = ci
         lib.ssm_plan_segments.argtypes = [i64] * 4 + [ci, ctypes.POINTER(ci), ctypes.POINTER(ci)]
@@ -256,3 +264,50 @@ def selftest_wait_timeout(stream=None):
 def check_device_status(stream=None):
     """Synchronise the stream and raise if a kernel's bounded wait gave up."""
     _check("ssm_check_device_status", load_library().ssm_check_device_status(_stream(stream)))
+
+
+# ------------------------------------------------------------------ conv1d
+
+def conv1d_fwd(x, w, bias, state0=None, *, out=None, state_last=None, want_state=True, stream=None):
+    """Causal depthwise conv1d + SiLU.  x [B,L,D] (bf16/f32), w [D,K] f32, bias [D] f32,
+    state0 [B,D,K-1] (act dtype, nullable).  Returns ``(out, state_last)``."""
+    B, L, D = x.shape
+    K = w.shape[1]
+    if out is None:
+        out = torch.empty_like(x)
+    if want_state and state_last is None:
+        state_last = torch.empty((B, D, K - 1), dtype=x.dtype, device=x.device)
+    rc = load_library().ssm_conv1d_fwd(B, L, D, K, _act(x), _p(x), _p(w), _p(bias), _p(state0), _p(out),
+                                       _p(state_last), _stream(stream))
+    _check("ssm_conv1d_fwd", rc)
+    return out, state_last
+
+
+def conv1d_bwd_workspace_bytes(batch, seqlen, dim, width, act) -> int:
+    return int(load_library().ssm_conv1d_bwd_workspace_bytes(batch, seqlen, dim, width, act))
+
+
+def conv1d_bwd(x, w, bias, state0, dout, *, want_dstate0=True, ws=None, stream=None):
+    """Backward of ``sum(dout * out)``: dict dx (act dtype), dw, dbias, dstate0 (f32)."""
+    B, L, D = x.shape
+    K = w.shape[1]
+    g = {"dx": torch.empty_like(x), "dw": torch.empty_like(w), "dbias": torch.empty_like(bias),
+         "dstate0": torch.empty((B, D, K - 1), dtype=torch.float32, device=x.device) if want_dstate0 else None}
+    ws, wsb = _workspace(conv1d_bwd_workspace_bytes(B, L, D, K, _act(x)), x.device, ws)
+    rc = load_library().ssm_conv1d_bwd(B, L, D, K, _act(x), _p(x), _p(w), _p(bias), _p(state0), _p(dout),
+                                       _p(g["dx"]), _p(g["dw"]), _p(g["dbias"]), _p(g["dstate0"]), _p(ws),
+                                       wsb, _stream(stream))
+    _check("ssm_conv1d_bwd", rc)
+    return g
+
+
+def conv1d_step(x, w, bias, state, *, out=None, stream=None):
+    """One step: x [B,D]; ``state`` [B,D,K-1] is shifted in place.  Returns ``out`` [B,D]."""
+    B, D = x.shape
+    K = w.shape[1]
+    if out is None:
+        out = torch.empty_like(x)
+    rc = load_library().ssm_conv1d_step(B, D, K, _act(x), _p(x), _p(w), _p(bias), _p(state), _p(out),
+                                        _stream(stream))
+    _check("ssm_conv1d_step", rc)
+    return out
