@@ -91,9 +91,11 @@ def algorithmic_bytes(B, L, D, N, e, chunk):
 def time_step(dev, reps=50, rounds=5):
     """The decode step (ssm_step) on the decode workload's shape (B=256,
     D=1536, N=16, f32), each step on a cold L2: CUDA graphs of `reps` x
-    (256 MB write + step) and of `reps` x (256 MB write) are replayed and the
-    step time is their difference.  Also the L2-resident time (graph of
-    chained steps only; h is 25 MB, smaller than L2)."""
+    (256 MB read + step) and of `reps` x (256 MB read) are replayed and the
+    step time is their difference (a read leaves L2 full of clean lines, so
+    the step pays for its own misses and no write-backs).  Also the
+    L2-resident time (graph of chained steps only; h is 25 MB, smaller than
+    L2)."""
     from selective_state_space_s6_gb300 import s6
 
     w = inputs.WORKLOADS["decode"]
@@ -104,14 +106,15 @@ def time_step(dev, reps=50, rounds=5):
     sl = {k: x[k][:, 0].contiguous() for k in ("u", "delta_raw", "z", "Bm", "Cm")}
     h = x["h0"].clone()
     out = torch.empty_like(sl["u"])
-    scratch = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    scratch = torch.ones((256 << 20) // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
 
     def step():
         s6.ssm_step(sl["u"], sl["delta_raw"], sl["z"], sl["Bm"], sl["Cm"], x["A_log"], x["Dp"],
                     x["delta_bias"], h, out=out)
 
     def flush():
-        scratch.fill_(1)
+        torch.sum(scratch, out=sink)
 
     side = torch.cuda.Stream(dev)
     side.wait_stream(torch.cuda.current_stream(dev))
@@ -154,7 +157,57 @@ def time_step(dev, reps=50, rounds=5):
     return {"workload": f"decode: {w.description}", "us_per_step": round(us_cold, 2),
             "us_per_step_l2_resident": round(t_s * 1e3, 2), "algorithmic_bytes": nbytes,
             "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),
-            "timing": f"CUDA graphs of {reps} steps; cold L2 = (write 256 MB + step) - (write 256 MB)"}
+            "timing": f"CUDA graphs of {reps} steps; cold L2 = (read 256 MB + step) - (read 256 MB)"}
+
+
+def time_conv1d(dev, B, L, D, act, K=4, reps=10):
+    """The causal conv1d + SiLU in front of the scan, on the workload's [B,L,D]
+    shape (K = 4 taps), forward and backward, CUDA events over `reps` calls;
+    inputs are larger than L2.  HBM roofline: x read + out written (forward);
+    x, dout read + dx written (backward)."""
+    from selective_state_space_s6_gb300 import s6
+
+    g = torch.Generator().manual_seed(0)
+    dt = torch.bfloat16 if act == "bf16" else torch.float32
+    e = 2 if act == "bf16" else 4
+    x = torch.randn(B, L, D, generator=g).to(dt).to(dev)
+    dout = torch.randn(B, L, D, generator=g).to(dt).to(dev)
+    w = (torch.randn(D, K, generator=g) * 0.5).to(dev)
+    bias = (torch.randn(D, generator=g) * 0.2).to(dev)
+    s0 = torch.zeros(B, D, K - 1, dtype=dt, device=dev)
+    out = torch.empty_like(x)
+    s_last = torch.empty_like(s0)
+    ws = torch.empty((s6.conv1d_bwd_workspace_bytes(B, L, D, K, s6.SSM_BF16 if act == "bf16" else s6.SSM_F32) + 256,),
+                     dtype=torch.uint8, device=dev)
+
+    def fwd():
+        s6.conv1d_fwd(x, w, bias, s0, out=out, state_last=s_last)
+
+    def bwd():
+        s6.conv1d_bwd(x, w, bias, s0, dout, ws=ws)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / reps
+
+    peak, _ = load_peaks()
+    bld = B * L * D
+    res = {"workload": f"B={B} L={L} D={D} K={K} {act}", "timing": f"CUDA events over {reps} calls"}
+    for name, fn, nbytes in (("fwd", fwd, 2 * bld * e), ("bwd", bwd, 3 * bld * e)):
+        ms = timed(fn)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"ms": round(ms, 4), "algorithmic_bytes": nbytes, "hbm_gbs": round(gbs, 1),
+                     "hbm_frac": round(gbs / peak, 4)}
+    return res
 
 
 # ------------------------------------------------------------------ clocks
@@ -462,6 +515,26 @@ def run_ours(args, world, rank, local):
     e2e_ms = timed(pipelined_step, ke, s_in, s_out)
     e2e_value = world * cells / (e2e_ms * 1e-3) / 1e9
     serial_value = world * cells / (serial_ms * 1e-3) / 1e9
+    # the host link alone: the same copies with no compute, each direction by
+    # itself and both at once (the floor under the pipelined e2e step)
+    in_ms = timed(lambda k: copy_in(sets[k % 2]), ke, stream, stream)
+    out_ms = timed(lambda k: copy_out(sets[k % 2], h_out[k % 2]), ke, stream, stream)
+
+    def both(k):
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        with torch.cuda.stream(s_in):
+            copy_in(sets[k % 2])
+        with torch.cuda.stream(s_out):
+            copy_out(sets[(k + 1) % 2], h_out[k % 2])
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+
+    both_ms = timed(both, ke, stream, stream)
+    torch.cuda.synchronize(dev)
+    link = {"h2d_gbs": round(h2d / (in_ms * 1e-3) / 1e9, 1), "d2h_gbs": round(d2h / (out_ms * 1e-3) / 1e9, 1),
+            "both_ms_per_step": round(both_ms, 4),
+            "note": "pinned-host copies of one step's inputs and results alone, no compute"}
 
     # ---- roofline of the dominant kernel (the backward scan), live event timing.
     # The scans are bound by instruction issue on the FP32/SFU pipes, not by
@@ -497,6 +570,7 @@ def run_ours(args, world, rank, local):
     fwd_seg, bwd_seg = s6.plan_segments(B, L, D, N, act)
 
     step_line = time_step(dev) if not args.no_step else None
+    conv_line = time_conv1d(dev, B, L, D, w.act) if not args.no_step else None
 
     cpu_base = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -518,12 +592,14 @@ def run_ours(args, world, rank, local):
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "steps": ke,
                 "overlap": "copy-in of step k+1 and copy-out of step k-1 overlap step k "
                            "(three streams, two device buffer sets)",
-                "serial": {"value": round(serial_value, 2), "ms_per_step": round(serial_ms, 4)}},
+                "serial": {"value": round(serial_value, 2), "ms_per_step": round(serial_ms, 4)},
+                "host_link": link},
         "gpu_launches": launches_per_step(fwd_seg, bwd_seg) * K,
         "segments": {"fwd": fwd_seg, "bwd": bwd_seg},
         "roofline": roofline,
         "kernels": per_kernel,
         "step": step_line,
+        "conv1d": conv_line,
         "cpu_baseline": cpu_base,
         "clocks": clk,
     }
@@ -586,7 +662,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-step", action="store_true", help="skip the decode-step measurement")
+    ap.add_argument("--no-step", action="store_true", help="skip the decode-step and conv1d measurements")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     world, rank, local = dist_setup()

@@ -21,6 +21,7 @@
 #include <type_traits>
 
 #include "s6_internal.cuh"
+#include "s6_tma.cuh"
 
 namespace s6 {
 
@@ -70,7 +71,15 @@ struct Vec<__nv_bfloat16, 4> {
     *reinterpret_cast<uint2*>(p) = a;
   }
 };
-__device__ __forceinline__ float silu_of(float pre) { return pre * sigmoid_f(pre); }
+// sigmoid: on the SFU (ex2, rcp approximations) for bf16 activations, whose
+// rounding dwarfs their error; expf and an IEEE division for f32
+template <typename Act>
+__device__ __forceinline__ float sig(float v) {
+  if constexpr (std::is_same<Act, __nv_bfloat16>::value)
+    return rcp_approx(1.f + ex2_approx(-v * 1.4426950408889634f));
+  else
+    return sigmoid_f(v);
+}
 
 // x row t (t >= 0) or, for t < 0, the state entries of the same V channels
 template <typename Act, int V>
@@ -87,9 +96,11 @@ __device__ __forceinline__ void load_in(const Act* x, const Act* state0, int L, 
 
 // Forward: a thread walks kRun steps of V channels.
 template <typename Act, int V, int K>
-__global__ void __launch_bounds__(kConvThreads) s6_conv1d_fwd_kernel(const Act* x, const float* w,
-                                                                     const float* bias, const Act* state0,
-                                                                     Act* out, int B, int L, int D) {
+__global__ void __launch_bounds__(kConvThreads) s6_conv1d_fwd_kernel(const Act* __restrict__ x,
+                                                                     const float* __restrict__ w,
+                                                                     const float* __restrict__ bias,
+                                                                     const Act* __restrict__ state0,
+                                                                     Act* __restrict__ out, int B, int L, int D) {
   const int nvec = D / V;
   const int nrun = (L + kRun - 1) / kRun;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -109,6 +120,7 @@ __global__ void __launch_bounds__(kConvThreads) s6_conv1d_fwd_kernel(const Act* 
   float win[K][V];  // win[k] = input t - (K-1) + k
 #pragma unroll
   for (int k = 0; k < K - 1; ++k) load_in<Act, V>(x, state0, L, D, K, b, t0 - (K - 1) + k, d, win[k]);
+#pragma unroll 4
   for (int t = t0; t < t1; ++t) {
     Vec<Act, V>::load(x + ((size_t)b * L + t) * D + d, win[K - 1]);
     float o[V];
@@ -117,7 +129,7 @@ __global__ void __launch_bounds__(kConvThreads) s6_conv1d_fwd_kernel(const Act* 
       float pre = bs[i];
 #pragma unroll
       for (int k = 0; k < K; ++k) pre += wk[k][i] * win[k][i];
-      o[i] = silu_of(pre);
+      o[i] = pre * sig<Act>(pre);
     }
     Vec<Act, V>::store(out + ((size_t)b * L + t) * D + d, o);
 #pragma unroll
@@ -149,8 +161,9 @@ __global__ void s6_conv1d_state_kernel(const Act* x, const Act* state0, Act* sta
 // and dbias terms of its own steps are summed in step order (last first).
 template <typename Act, int V, int K>
 __global__ void __launch_bounds__(kConvThreads) s6_conv1d_bwd_kernel(
-    const Act* x, const float* w, const float* bias, const Act* state0, const Act* dout, Act* dx,
-    float* dstate0, float* part, int B, int L, int D) {
+    const Act* __restrict__ x, const float* __restrict__ w, const float* __restrict__ bias,
+    const Act* __restrict__ state0, const Act* __restrict__ dout, Act* __restrict__ dx,
+    float* __restrict__ dstate0, float* __restrict__ part, int B, int L, int D) {
   const int nvec = D / V;
   const int nrun = (L + kRun - 1) / kRun;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -181,7 +194,7 @@ __global__ void __launch_bounds__(kConvThreads) s6_conv1d_bwd_kernel(
       float pre = bs[i];
 #pragma unroll
       for (int k = 0; k < K; ++k) pre += wk[k][i] * in[k][i];
-      const float s = sigmoid_f(pre);
+      const float s = sig<Act>(pre);
       g[i] = go[i] * s * fmaf(pre, 1.f - s, 1.f);
     }
   };
@@ -206,6 +219,7 @@ __global__ void __launch_bounds__(kConvThreads) s6_conv1d_bwd_kernel(
 #pragma unroll
     for (int k = 0; k < K; ++k) aw[k][i] = 0.f;
   }
+#pragma unroll 4
   for (int t = t1 - 1; t >= t0; --t) {
     load_in<Act, V>(x, state0, L, D, K, b, t - (K - 1), d, xw[0]);
     dpre_from(t, xw, gw[0]);
@@ -285,7 +299,7 @@ __global__ void s6_conv1d_step_kernel(const Act* x, const float* w, const float*
   float pre = bias[d];
 #pragma unroll
   for (int k = 0; k < K; ++k) pre += w[(size_t)d * K + k] * in[k];
-  st_act(out + idx, silu_of(pre));
+  st_act(out + idx, pre * sig<Act>(pre));
 #pragma unroll
   for (int k = 0; k < K - 1; ++k) st_act(st + k, in[k + 1]);
 }

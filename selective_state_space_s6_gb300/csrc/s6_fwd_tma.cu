@@ -499,6 +499,30 @@ __global__ void __launch_bounds__(256) s6_step_kernel(const FwdParams p) {
   const float sp_q = softplus_k<kFast>(ld_act(static_cast<const Act*>(p.delta_raw) + (size_t)bq * D + d) + bias);
   const float sl_q = kGate ? silu_k<kFast>(ld_act(static_cast<const Act*>(p.z) + (size_t)bq * D + d)) : 1.f;
 
+  // every row's loads first (independent of one another; the state is
+  // written in place, so the loads must not wait behind earlier stores)
+  float uj[TPC], hj[TPC][4], bj4[TPC][4], cj4[TPC][4];
+#pragma unroll
+  for (int j = 0; j < TPC; ++j) {
+    const long long b = min(g * TPC + j, B - 1);
+    const long long bd = b * D + d;
+    uj[j] = ld_act(u_p + bd);
+    const float4 hv = *reinterpret_cast<const float4*>(p.h0 + bd * N + 4 * q);
+    hj[j][0] = hv.x, hj[j][1] = hv.y, hj[j][2] = hv.z, hj[j][3] = hv.w;
+    if constexpr (std::is_same<Act, float>::value) {
+      const float4 bb = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.Bm) + b * N + 4 * q));
+      const float4 cc = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.Cm) + b * N + 4 * q));
+      bj4[j][0] = bb.x, bj4[j][1] = bb.y, bj4[j][2] = bb.z, bj4[j][3] = bb.w;
+      cj4[j][0] = cc.x, cj4[j][1] = cc.y, cj4[j][2] = cc.z, cj4[j][3] = cc.w;
+    } else {
+      const __nv_bfloat162* bb = reinterpret_cast<const __nv_bfloat162*>(static_cast<const Act*>(p.Bm) + b * N + 4 * q);
+      const __nv_bfloat162* cc = reinterpret_cast<const __nv_bfloat162*>(static_cast<const Act*>(p.Cm) + b * N + 4 * q);
+      const float2 b0 = __bfloat1622float2(bb[0]), b1 = __bfloat1622float2(bb[1]);
+      const float2 c0 = __bfloat1622float2(cc[0]), c1 = __bfloat1622float2(cc[1]);
+      bj4[j][0] = b0.x, bj4[j][1] = b0.y, bj4[j][2] = b1.x, bj4[j][3] = b1.y;
+      cj4[j][0] = c0.x, cj4[j][1] = c0.y, cj4[j][2] = c1.x, cj4[j][3] = c1.y;
+    }
+  }
 #pragma unroll
   for (int j = 0; j < TPC; ++j) {
     const int bj = g * TPC + j;
@@ -507,21 +531,10 @@ __global__ void __launch_bounds__(256) s6_step_kernel(const FwdParams p) {
     const long long bd = b * D + d;
     const float sp = __shfl_sync(0xffffffffu, sp_q, lead + j);
     const float sl = __shfl_sync(0xffffffffu, sl_q, lead + j);
-    const float u = ld_act(u_p + bd);
-    float2 Bv[2], Cv[2];
-    if constexpr (std::is_same<Act, float>::value) {
-      const float4 bb = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.Bm) + b * N + 4 * q));
-      const float4 cc = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.Cm) + b * N + 4 * q));
-      Bv[0] = make_float2(bb.x, bb.y), Bv[1] = make_float2(bb.z, bb.w);
-      Cv[0] = make_float2(cc.x, cc.y), Cv[1] = make_float2(cc.z, cc.w);
-    } else {
-      const __nv_bfloat162* bb = reinterpret_cast<const __nv_bfloat162*>(static_cast<const Act*>(p.Bm) + b * N + 4 * q);
-      const __nv_bfloat162* cc = reinterpret_cast<const __nv_bfloat162*>(static_cast<const Act*>(p.Cm) + b * N + 4 * q);
-      Bv[0] = __bfloat1622float2(bb[0]), Bv[1] = __bfloat1622float2(bb[1]);
-      Cv[0] = __bfloat1622float2(cc[0]), Cv[1] = __bfloat1622float2(cc[1]);
-    }
-    const float4 hv = *reinterpret_cast<const float4*>(p.h0 + bd * N + 4 * q);
-    float2 h[2] = {make_float2(hv.x, hv.y), make_float2(hv.z, hv.w)};
+    const float u = uj[j];
+    float2 Bv[2] = {make_float2(bj4[j][0], bj4[j][1]), make_float2(bj4[j][2], bj4[j][3])};
+    float2 Cv[2] = {make_float2(cj4[j][0], cj4[j][1]), make_float2(cj4[j][2], cj4[j][3])};
+    float2 h[2] = {make_float2(hj[j][0], hj[j][1]), make_float2(hj[j][2], hj[j][3])};
     const float du = sp * u;
     const float2 dd = make_float2(sp, sp), uu = make_float2(du, du);
     const float2 a0 = decay2<kFast>(dd, A2[0]);
