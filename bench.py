@@ -114,7 +114,7 @@ def time_step(dev, reps=50, rounds=5):
                     x["delta_bias"], h, out=out)
 
     def flush():
-        torch.sum(scratch, out=sink)
+        torch.sum(scratch, dim=0, out=sink)
 
     side = torch.cuda.Stream(dev)
     side.wait_stream(torch.cuda.current_stream(dev))

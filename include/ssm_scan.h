@@ -278,6 +278,19 @@ int ssm_conv1d_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t width, in
 int ssm_conv1d_step(int64_t batch, int64_t dim, int64_t width, int act, const void *x,
                     const float *w, const float *bias, void *state, void *out, void *stream);
 
+/* Which kernels a conv1d call with these shapes and pointers runs (host-only
+ * query, no launch): SSM_CONV_PATH_TILE (TMA tiles of 64 steps x 128
+ * channels: D*elem a multiple of 16 bytes, x and dout 16-byte aligned),
+ * SSM_CONV_PATH_VECTOR (4 channels per thread: D % 4 == 0, 8-byte (bf16) or
+ * 16-byte (f32) aligned) or SSM_CONV_PATH_SCALAR; dout NULL asks about the
+ * forward (y = out), else the backward (y = dx).  All three give the same
+ * results within rounding.  Negative status on an invalid shape. */
+#define SSM_CONV_PATH_SCALAR 0
+#define SSM_CONV_PATH_VECTOR 1
+#define SSM_CONV_PATH_TILE 2
+int ssm_conv1d_path(int64_t batch, int64_t seqlen, int64_t dim, int64_t width, int act,
+                    const void *x, const void *dout, const void *y);
+
 #ifdef __cplusplus
 }
 #endif

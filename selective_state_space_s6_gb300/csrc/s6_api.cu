@@ -492,6 +492,8 @@ int ssm_conv1d_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t width, in
   s6::ConvParams p = {};
   p.x = x; p.w = w; p.bias = bias; p.state0 = state0; p.out = out; p.state_last = state_last;
   p.B = (int)B; p.L = (int)L; p.D = (int)D; p.K = (int)K;
+  p.status = s6::device_status_word();
+  if (!p.status) return fail(SSM_ERR_CUDA, "cannot locate the device status word");
   const cudaError_t ce = s6::launch_conv1d(p, act, false, static_cast<cudaStream_t>(stream));
   return ce == cudaSuccess ? SSM_OK : cuda_fail(ce, "ssm_conv1d_fwd launch");
 }
@@ -532,8 +534,25 @@ int ssm_conv1d_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t width, in
   p.x = x; p.w = w; p.bias = bias; p.state0 = state0; p.dout = dout; p.dx = dx; p.dw = dw; p.dbias = dbias;
   p.dstate0 = dstate0; p.ws = static_cast<float*>(ws);
   p.B = (int)B; p.L = (int)L; p.D = (int)D; p.K = (int)K;
+  p.status = s6::device_status_word();
+  if (!p.status) return fail(SSM_ERR_CUDA, "cannot locate the device status word");
   const cudaError_t ce = s6::launch_conv1d(p, act, true, st);
   return ce == cudaSuccess ? SSM_OK : cuda_fail(ce, "ssm_conv1d_bwd launch");
+}
+
+int ssm_conv1d_path(int64_t batch, int64_t seqlen, int64_t dim, int64_t width, int act, const void* x,
+                    const void* dout, const void* y) {
+  const int st = check_conv(batch, seqlen, dim, width, act);
+  if (st != SSM_OK) return -st;
+  s6::ConvParams p = {};
+  p.x = x;
+  p.dout = dout;
+  if (dout)
+    p.dx = const_cast<void*>(y);
+  else
+    p.out = const_cast<void*>(y);
+  p.B = (int)batch; p.L = (int)seqlen; p.D = (int)dim; p.K = (int)width;
+  return s6::conv1d_path(p, act, dout != nullptr);
 }
 
 int ssm_conv1d_step(int64_t batch, int64_t dim, int64_t width, int act, const void* x, const float* w,

@@ -947,33 +947,14 @@ cudaError_t launch_agg(const BwdTmaParams& P, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
+// 2D map over a row-major [rows][cols] tensor, box [box_rows][box_cols].
 bool make_map(CUtensorMap* m, const void* base, int act, uint64_t rows, uint64_t cols, uint32_t box_rows,
               uint32_t box_cols, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
-  auto enc = get_encode();
-  if (!enc) return false;
-  const size_t e = act == SSM_BF16 ? 2 : 4;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * e};
-  const cuuint32_t box[2] = {box_cols, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(m, act == SSM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t e = act == SSM_BF16 ? 2 : 4;
+  const uint64_t dims[2] = {cols, rows};
+  const uint64_t strides[1] = {cols * e};
+  const uint32_t box[2] = {box_cols, box_rows};
+  return encode_tile_map(m, base, act == SSM_BF16, 2, dims, strides, box, swizzle);
 }
 
 template <typename Act, int TPC>
@@ -1089,7 +1070,7 @@ bool bwd_tma_supported(const BwdParams& p, int act) {
   if (p.z && !aligned16(p.z)) return false;
   if (p.dh0 && !aligned16(p.dh0)) return false;
   if (p.dh_last && (reinterpret_cast<uintptr_t>(p.dh_last) & 7)) return false;
-  return get_encode() != nullptr;
+  return tensor_map_encoder() != nullptr;
 }
 
 cudaError_t launch_bwd_tma(const BwdParams& p, int act, cudaStream_t stream) {

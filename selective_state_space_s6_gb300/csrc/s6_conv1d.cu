@@ -46,6 +46,10 @@ struct Vec<float, 4> {
   static __device__ __forceinline__ void store(float* p, const float* v) {
     *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
   }
+  static __device__ __forceinline__ void lds(const float* p, float* v) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w;
+  }
 };
 template <>
 struct Vec<__nv_bfloat16, 1> {
@@ -69,6 +73,15 @@ struct Vec<__nv_bfloat16, 4> {
 #pragma unroll
     for (int i = 0; i < 2; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
     *reinterpret_cast<uint2*>(p) = a;
+  }
+  static __device__ __forceinline__ void lds(const __nv_bfloat16* p, float* v) {
+    const uint2 a = *reinterpret_cast<const uint2*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&a);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      v[2 * i] = f.x, v[2 * i + 1] = f.y;
+    }
   }
 };
 // sigmoid: on the SFU (ex2, rcp approximations) for bf16 activations, whose
@@ -269,17 +282,280 @@ __global__ void __launch_bounds__(kConvThreads) s6_conv1d_bwd_kernel(
   }
 }
 
-// dw[d][k], dbias[d] = sum over (b, run), ascending, of the partials
-__global__ void s6_conv1d_reduce_kernel(const float* part, int R, int D, int K, float* dw, float* dbias) {
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;  // (d, k) with k = K meaning the bias
-  if (e >= D * (K + 1)) return;
-  const int d = e / (K + 1), k = e % (K + 1);
+// ---------------------------------------------------------------- TMA tiles
+// A CTA of kTileWarps warps owns kTileT steps x kTileCh channels of one batch
+// row.  One TMA load per tensor brings the tile's inputs into shared memory
+// (forward: x for its steps and the K-1 before; backward: x for its steps
+// and the K-1 on either side, dout for its steps and the K-1 after), so a
+// CTA has its whole tile in flight whatever its register count, and the
+// copy engine rather than the threads carries the halo rows.  Warp w then
+// walks steps w*16 .. w*16+15 of the tile from shared memory, lane l on
+// channels 4l .. 4l+3 (one 8- or 16-byte access per row: conflict-free).
+// Rows outside [0, L) and channels past D arrive as zeros (the bounds of the
+// 3D tensor map [B][L][D]): that is the causal padding when there is no
+// state0, and it makes dpre = 0 for steps past the end; with state0 the
+// inputs before t = 0 are read from it.
+constexpr int kTileT = kRun;                   // steps per CTA (one partial-sum row)
+constexpr int kTileWarps = 4;
+constexpr int kTileSeg = kTileT / kTileWarps;  // steps per warp
+constexpr int kTileCh = 128;                   // channels per CTA: 32 lanes x 4
+static_assert(kTileSeg >= SSM_MAX_CONV_WIDTH - 1, "a warp's segment must hold the state gradient's steps");
+
+struct ConvTileParams {
+  CUtensorMap map_x, map_dout;
+  ConvParams p;
+};
+
+template <typename Act>
+constexpr size_t tile_rows_bytes(int rows) {
+  return ((size_t)rows * kTileCh * sizeof(Act) + 127) / 128 * 128;
+}
+
+template <typename Act, int K>
+constexpr size_t fwd_tile_smem() {
+  return tile_rows_bytes<Act>(kTileT + K - 1) + 16;
+}
+
+template <typename Act, int K>
+constexpr size_t bwd_tile_smem() {
+  return tile_rows_bytes<Act>(kTileT + 2 * (K - 1)) + tile_rows_bytes<Act>(kTileT + K - 1) +
+         (size_t)kTileWarps * kTileCh * (K + 1) * 4 + 16;
+}
+
+// weights and bias of channels d .. d+3 (zeros past D)
+template <int K>
+__device__ __forceinline__ void load_weights(const ConvParams& p, int d, bool cv, float (&wk)[K][4], float (&bs)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    bs[i] = cv ? __ldg(p.bias + d + i) : 0.f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) wk[k][i] = cv ? __ldg(p.w + (size_t)(d + i) * K + k) : 0.f;
+  }
+}
+
+// thread 0 sets up the barrier; all threads see it before anyone waits
+__device__ __forceinline__ void tile_barrier_init(uint64_t* bar) {
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+}
+
+template <typename Act, int K>
+__global__ void __launch_bounds__(kTileWarps * 32) s6_conv1d_fwd_tile_kernel(const __grid_constant__ ConvTileParams P) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int kRows = kTileT + K - 1;  // smem row r holds input t0 - (K-1) + r
+  const ConvParams& p = P.p;
+  Act* xs = reinterpret_cast<Act*>(smem);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + tile_rows_bytes<Act>(kRows));
+  const int c0 = blockIdx.x * kTileCh, t0 = blockIdx.y * kTileT, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  tile_barrier_init(bar);
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(bar, (uint32_t)(kRows * kTileCh * sizeof(Act)));
+    tma_load_3d(xs, &P.map_x, bar, c0, t0 - (K - 1), b);
+  }
+  const int d = c0 + 4 * lane;
+  const bool cv = d < p.D;
+  float wk[K][4], bs[4];
+  load_weights<K>(p, d, cv, wk, bs);
+  const Act* __restrict__ s0 = static_cast<const Act*>(p.state0);
+  const int ts = t0 + warp * kTileSeg;
+  float win[K][4];  // win[k] = input t - (K-1) + k
+  // the window's first K-1 inputs: from state0 before t = 0, if given (then
+  // ts = 0 and input ts-(K-1)+k is state entry k), else from the tile
+#pragma unroll
+  for (int k = 0; k < K - 1; ++k)
+    if (s0 && ts - (K - 1) + k < 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) win[k][i] = cv ? ld_act(s0 + ((size_t)b * p.D + d + i) * (K - 1) + k) : 0.f;
+    }
+  if (!mbar_wait(bar, 0, p.status)) return;
+  if (ts >= p.L) return;
+#pragma unroll
+  for (int k = 0; k < K - 1; ++k)
+    if (!(s0 && ts - (K - 1) + k < 0)) Vec<Act, 4>::lds(xs + (warp * kTileSeg + k) * kTileCh + 4 * lane, win[k]);
+  Act* __restrict__ out = static_cast<Act*>(p.out);
+#pragma unroll 4
+  for (int i = 0; i < kTileSeg; ++i) {
+    const int t = ts + i;
+    Vec<Act, 4>::lds(xs + (warp * kTileSeg + i + K - 1) * kTileCh + 4 * lane, win[K - 1]);
+    float o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float pre = bs[j];
+#pragma unroll
+      for (int k = 0; k < K; ++k) pre += wk[k][j] * win[k][j];
+      o[j] = pre * sig<Act>(pre);
+    }
+    if (cv && t < p.L) Vec<Act, 4>::store(out + ((size_t)b * p.L + t) * p.D + d, o);
+#pragma unroll
+    for (int k = 0; k < K - 1; ++k)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) win[k][j] = win[k + 1][j];
+  }
+}
+
+template <typename Act, int K>
+__global__ void __launch_bounds__(kTileWarps * 32) s6_conv1d_bwd_tile_kernel(const __grid_constant__ ConvTileParams P) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int kXRows = kTileT + 2 * (K - 1);  // xs row r: input t0 - (K-1) + r
+  constexpr int kGRows = kTileT + K - 1;        // gs row r: dout of step t0 + r
+  const ConvParams& p = P.p;
+  Act* xs = reinterpret_cast<Act*>(smem);
+  Act* gs = reinterpret_cast<Act*>(smem + tile_rows_bytes<Act>(kXRows));
+  float* red = reinterpret_cast<float*>(smem + tile_rows_bytes<Act>(kXRows) + tile_rows_bytes<Act>(kGRows));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(red + kTileWarps * kTileCh * (K + 1));
+  const int c0 = blockIdx.x * kTileCh, t0 = blockIdx.y * kTileT, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  tile_barrier_init(bar);
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(bar, (uint32_t)((kXRows + kGRows) * kTileCh * sizeof(Act)));
+    tma_load_3d(xs, &P.map_x, bar, c0, t0 - (K - 1), b);
+    tma_load_3d(gs, &P.map_dout, bar, c0, t0, b);
+  }
+  const int d = c0 + 4 * lane;
+  const bool cv = d < p.D;
+  float wk[K][4], bs[4];
+  load_weights<K>(p, d, cv, wk, bs);
+  const Act* __restrict__ s0 = static_cast<const Act*>(p.state0);
+  const bool ok = mbar_wait(bar, 0, p.status);
+  const int ts = t0 + warp * kTileSeg;
+  // input tau of this thread's channels
+  auto xin = [&](int tau, float* v) {
+    if (tau < 0 && s0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = cv ? ld_act(s0 + ((size_t)b * p.D + d + i) * (K - 1) + (K - 1 + tau)) : 0.f;
+    } else {
+      Vec<Act, 4>::lds(xs + (tau - t0 + K - 1) * kTileCh + 4 * lane, v);
+    }
+  };
+  // dpre of step t from its inputs in[k] = input t-(K-1)+k (0 past L: dout is 0 there)
+  auto dpre_from = [&](int t, const float (&in)[K][4], float* g) {
+    float go[4];
+    Vec<Act, 4>::lds(gs + (t - t0) * kTileCh + 4 * lane, go);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float pre = bs[i];
+#pragma unroll
+      for (int k = 0; k < K; ++k) pre += wk[k][i] * in[k][i];
+      const float s = sig<Act>(pre);
+      g[i] = go[i] * s * fmaf(pre, 1.f - s, 1.f);
+    }
+  };
+  float aw[K][4], ab[4];  // this warp's sums of the dw[k] and dbias terms
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    ab[i] = 0.f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) aw[k][i] = 0.f;
+  }
+  if (ok && ts < p.L) {
+    float gw[K][4];  // gw[k] = dpre[t + k]
+#pragma unroll
+    for (int k = 1; k < K; ++k) {
+      const int t = ts + kTileSeg - 1 + k;
+      float in[K][4];
+#pragma unroll
+      for (int j = 0; j < K; ++j) xin(t - (K - 1) + j, in[j]);
+      dpre_from(t, in, gw[k]);
+    }
+    float xw[K][4];  // xw[k] = input t - (K-1) + k
+#pragma unroll
+    for (int k = 1; k < K; ++k) xin(ts + kTileSeg - 1 - (K - 1) + k, xw[k]);
+    Act* __restrict__ dx = static_cast<Act*>(p.dx);
+#pragma unroll 4
+    for (int i = kTileSeg - 1; i >= 0; --i) {
+      const int t = ts + i;
+      xin(t - (K - 1), xw[0]);
+      dpre_from(t, xw, gw[0]);
+      float o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < K; ++k) acc += wk[k][j] * gw[K - 1 - k][j];
+        o[j] = acc;
+        ab[j] += gw[0][j];
+#pragma unroll
+        for (int k = 0; k < K; ++k) aw[k][j] += gw[0][j] * xw[k][j];
+      }
+      if (cv && t < p.L) Vec<Act, 4>::store(dx + ((size_t)b * p.L + t) * p.D + d, o);
+#pragma unroll
+      for (int k = K - 1; k > 0; --k)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          gw[k][j] = gw[k - 1][j];
+          xw[k][j] = xw[k - 1][j];
+        }
+    }
+    // the first warp of the first tile owns the state's gradient; here
+    // gw[m + 1] = dpre[m]: dstate0[j] = sum_{k<=j} w[k] * dpre[j - k]
+    if (ts == 0 && p.dstate0 && K > 1 && cv) {
+#pragma unroll
+      for (int j = 0; j < K - 1; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float acc = 0.f;
+#pragma unroll
+          for (int k = 0; k <= j; ++k) acc += wk[k][i] * gw[j - k + 1][i];
+          p.dstate0[((size_t)b * p.D + d + i) * (K - 1) + j] = acc;
+        }
+    }
+  }
+  // the tile's partial sums: warps added in order 0..3 (fixed), written as
+  // row (b, tile) of partials [b][tile][d][K+1]
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float* r = red + ((size_t)warp * kTileCh + 4 * lane + i) * (K + 1);
+#pragma unroll
+    for (int k = 0; k < K; ++k) r[k] = aw[k][i];
+    r[K] = ab[i];
+  }
+  __syncthreads();
+  if (!ok) return;
+  const int nrun = (p.L + kTileT - 1) / kTileT;
+  const int nvalid = min(kTileCh, p.D - c0) * (K + 1);
+  float* pp = p.ws + (((size_t)b * nrun + blockIdx.y) * p.D + c0) * (K + 1);
+  for (int e = threadIdx.x; e < nvalid; e += kTileWarps * 32) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kTileWarps; ++w) s += red[w * kTileCh * (K + 1) + e];
+    pp[e] = s;
+  }
+}
+
+// dw[d][k], dbias[d] = sum of the partial rows r = 0 .. R-1 (one per batch
+// row and run): a block covers kRedCols columns (d, k), k = K meaning the
+// bias; its kRedGroups warps sum the rows r = g (mod kRedGroups), each in
+// ascending r, and the group sums are added in ascending g.  A fixed order,
+// so the result does not depend on timing.
+constexpr int kRedCols = 32, kRedGroups = 8;
+
+__global__ void __launch_bounds__(kRedCols * kRedGroups) s6_conv1d_reduce_kernel(const float* __restrict__ part, int R,
+                                                                                int D, int K, float* dw,
+                                                                                float* dbias) {
+  __shared__ float gsum[kRedGroups][kRedCols];
+  const int col = threadIdx.x % kRedCols, g = threadIdx.x / kRedCols;
+  const int ncol = D * (K + 1);
+  const int e = blockIdx.x * kRedCols + col;
   float s = 0.f;
-  for (int r = 0; r < R; ++r) s += part[((size_t)r * D + d) * (K + 1) + k];
+  if (e < ncol) {
+#pragma unroll 8
+    for (int r = g; r < R; r += kRedGroups) s += __ldg(part + (size_t)r * ncol + e);
+  }
+  gsum[g][col] = s;
+  __syncthreads();
+  if (g != 0 || e >= ncol) return;
+  float t = gsum[0][col];
+#pragma unroll
+  for (int j = 1; j < kRedGroups; ++j) t += gsum[j][col];
+  const int d = e / (K + 1), k = e % (K + 1);
   if (k < K)
-    dw[(size_t)d * K + k] = s;
+    dw[(size_t)d * K + k] = t;
   else
-    dbias[d] = s;
+    dbias[d] = t;
 }
 
 // One step: state [B][D][K-1] (oldest first) and x_t give out_t; the state
@@ -304,6 +580,17 @@ __global__ void s6_conv1d_step_kernel(const Act* x, const float* w, const float*
   for (int k = 0; k < K - 1; ++k) st_act(st + k, in[k + 1]);
 }
 
+// state_last (K > 1 and asked for): the last K-1 inputs
+template <typename Act>
+cudaError_t launch_state(const ConvParams& p, cudaStream_t stream) {
+  if (!p.state_last || p.K == 1) return cudaSuccess;
+  const long long n = (long long)p.B * p.D * (p.K - 1);
+  s6_conv1d_state_kernel<Act><<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(
+      static_cast<const Act*>(p.x), static_cast<const Act*>(p.state0), static_cast<Act*>(p.state_last), p.B, p.L,
+      p.D, p.K);
+  return cudaGetLastError();
+}
+
 template <typename Act, int V, int K>
 cudaError_t fwd_vk(const ConvParams& p, cudaStream_t stream) {
   const int nrun = (p.L + kRun - 1) / kRun;
@@ -314,11 +601,14 @@ cudaError_t fwd_vk(const ConvParams& p, cudaStream_t stream) {
                                                  static_cast<const Act*>(p.state0), static_cast<Act*>(p.out),
                                                  p.B, p.L, p.D);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || !p.state_last || K == 1) return e;
-  const long long n = (long long)p.B * p.D * (K - 1);
-  s6_conv1d_state_kernel<Act><<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(
-      static_cast<const Act*>(p.x), static_cast<const Act*>(p.state0), static_cast<Act*>(p.state_last), p.B, p.L,
-      p.D, K);
+  if (e != cudaSuccess) return e;
+  return launch_state<Act>(p, stream);
+}
+
+cudaError_t launch_reduce(const ConvParams& p, int nrun, cudaStream_t stream) {
+  const int n = p.D * (p.K + 1);
+  s6_conv1d_reduce_kernel<<<(n + kRedCols - 1) / kRedCols, kRedCols * kRedGroups, 0, stream>>>(
+      p.ws, p.B * nrun, p.D, p.K, p.dw, p.dbias);
   return cudaGetLastError();
 }
 
@@ -333,9 +623,51 @@ cudaError_t bwd_vk(const ConvParams& p, cudaStream_t stream) {
         static_cast<const Act*>(p.dout), static_cast<Act*>(p.dx), p.dstate0, p.ws, p.B, p.L, p.D);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int n = p.D * (K + 1);
-  s6_conv1d_reduce_kernel<<<(n + 255) / 256, 256, 0, stream>>>(p.ws, p.B * nrun, p.D, K, p.dw, p.dbias);
-  return cudaGetLastError();
+  return launch_reduce(p, nrun, stream);
+}
+
+template <typename Act, int K>
+cudaError_t tile_k(const ConvTileParams& P, bool bwd, cudaStream_t stream) {
+  const ConvParams& p = P.p;
+  const dim3 grid((p.D + kTileCh - 1) / kTileCh, (p.L + kTileT - 1) / kTileT, p.B);
+  if (!bwd) {
+    auto kern = s6_conv1d_fwd_tile_kernel<Act, K>;
+    constexpr size_t smem = fwd_tile_smem<Act, K>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kTileWarps * 32, smem, stream>>>(P);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_state<Act>(p, stream);
+  }
+  auto kern = s6_conv1d_bwd_tile_kernel<Act, K>;
+  constexpr size_t smem = bwd_tile_smem<Act, K>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kTileWarps * 32, smem, stream>>>(P);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_reduce(p, (p.L + kTileT - 1) / kTileT, stream);
+}
+
+template <typename Act>
+cudaError_t tile_dispatch(const ConvTileParams& P, bool bwd, cudaStream_t stream) {
+  switch (P.p.K) {
+#define S6_CONV_K(KK) \
+  case KK:            \
+    return tile_k<Act, KK>(P, bwd, stream);
+    S6_CONV_K(1)
+    S6_CONV_K(2)
+    S6_CONV_K(3)
+    S6_CONV_K(4)
+    S6_CONV_K(5)
+    S6_CONV_K(6)
+    S6_CONV_K(7)
+    S6_CONV_K(8)
+#undef S6_CONV_K
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 template <typename Act, int V>
@@ -367,6 +699,30 @@ bool vec_ok(const ConvParams& p, int act) {
   const void* ptrs[] = {p.x, p.out, p.dout, p.dx};
   for (const void* q : ptrs)
     if (q && (reinterpret_cast<uintptr_t>(q) & mask)) return false;
+  return true;
+}
+
+// Tile path: the vector path's conditions, rows of a whole number of 16-byte
+// units (what a tensor map's strides need), 16-byte aligned TMA sources, the
+// grid within its limits, and tensor maps the driver accepts.
+bool tile_maps(const ConvParams& p, int act, bool bwd, ConvTileParams* P) {
+  if (!vec_ok(p, act) || p.L < 1 || p.B < 1 || p.D < 1) return false;
+  const uint64_t e = act == SSM_BF16 ? 2 : 4;
+  if ((p.D * e) % 16 != 0) return false;
+  if (reinterpret_cast<uintptr_t>(p.x) & 15) return false;
+  if (bwd && (reinterpret_cast<uintptr_t>(p.dout) & 15)) return false;
+  if ((p.L + kTileT - 1) / kTileT > 65535 || p.B > 65535) return false;
+  const uint64_t dims[3] = {(uint64_t)p.D, (uint64_t)p.L, (uint64_t)p.B};
+  const uint64_t strides[2] = {p.D * e, (uint64_t)p.L * p.D * e};
+  const uint32_t box_x[3] = {kTileCh, (uint32_t)(kTileT + (bwd ? 2 : 1) * (p.K - 1)), 1};
+  if (!encode_tile_map(&P->map_x, p.x, act == SSM_BF16, 3, dims, strides, box_x)) return false;
+  if (bwd) {
+    const uint32_t box_g[3] = {kTileCh, (uint32_t)(kTileT + p.K - 1), 1};
+    if (!encode_tile_map(&P->map_dout, p.dout, act == SSM_BF16, 3, dims, strides, box_g)) return false;
+  } else {
+    P->map_dout = P->map_x;
+  }
+  P->p = p;
   return true;
 }
 
@@ -407,7 +763,16 @@ size_t conv1d_bwd_workspace_bytes(int B, int L, int D, int K) {
   return (size_t)B * nrun * D * (K + 1) * sizeof(float);
 }
 
+int conv1d_path(const ConvParams& p, int act, bool bwd) {
+  ConvTileParams P;
+  if (tile_maps(p, act, bwd, &P)) return SSM_CONV_PATH_TILE;
+  return vec_ok(p, act) ? SSM_CONV_PATH_VECTOR : SSM_CONV_PATH_SCALAR;
+}
+
 cudaError_t launch_conv1d(const ConvParams& p, int act, bool bwd, cudaStream_t stream) {
+  ConvTileParams P;
+  if (tile_maps(p, act, bwd, &P))
+    return act == SSM_BF16 ? tile_dispatch<__nv_bfloat16>(P, bwd, stream) : tile_dispatch<float>(P, bwd, stream);
   const bool vec = vec_ok(p, act);
   if (act == SSM_BF16)
     return vec ? dispatch_k<__nv_bfloat16, 4>(p, bwd, stream) : dispatch_k<__nv_bfloat16, 1>(p, bwd, stream);

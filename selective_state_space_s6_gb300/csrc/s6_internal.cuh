@@ -150,6 +150,7 @@ struct ConvParams {
   float* dbias;
   float* dstate0;        // nullable
   float* ws;             // backward partial sums
+  unsigned int* status;  // device status word (bounded waits report here)
   int B, L, D, K;
 };
 
@@ -172,6 +173,8 @@ bool bwd_tma_supported(const BwdParams& p, int act);
 cudaError_t launch_bwd_tma(const BwdParams& p, int act, cudaStream_t stream);
 size_t conv1d_bwd_workspace_bytes(int B, int L, int D, int K);
 cudaError_t launch_conv1d(const ConvParams& p, int act, bool bwd, cudaStream_t stream);
+// SSM_CONV_PATH_* that launch_conv1d would take for these parameters
+int conv1d_path(const ConvParams& p, int act, bool bwd);
 cudaError_t launch_conv1d_step(const ConvParams& p, int act, cudaStream_t stream);
 // The TMA backward's work plan for this shape with `sms` worker CTAs.
 BwdPlan bwd_plan(int B, int L, int D, int N, int sms);

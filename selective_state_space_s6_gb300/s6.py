@@ -21,6 +21,7 @@ _lock = threading.Lock()
 _lib = None
 
 SSM_F32, SSM_BF16 = 0, 1
+CONV_PATHS = {0: "scalar", 1: "vector", 2: "tile"}
 CHUNK_LEN = 64
 MAX_DSTATE = 16
 
@@ -79,6 +80,8 @@ def load_library():
         lib.ssm_conv1d_bwd.restype = ci
         lib.ssm_conv1d_step.argtypes = [i64] * 3 + [ci] + [vp] * 5 + [vp]
         lib.ssm_conv1d_step.restype = ci
+        lib.ssm_conv1d_path.argtypes = [i64] * 4 + [ci] + [vp] * 3
+        lib.ssm_conv1d_path.restype = ci
         lib.ssm_selftest_wait_timeout.argtypes = [vp]
         lib.ssm_selftest_wait_timeout.restype = ci
         lib.ssm_plan_segments.argtypes = [i64] * 4 + [ci, ctypes.POINTER(ci), ctypes.POINTER(ci)]
@@ -287,11 +290,11 @@ def conv1d_bwd_workspace_bytes(batch, seqlen, dim, width, act) -> int:
     return int(load_library().ssm_conv1d_bwd_workspace_bytes(batch, seqlen, dim, width, act))
 
 
-def conv1d_bwd(x, w, bias, state0, dout, *, want_dstate0=True, ws=None, stream=None):
+def conv1d_bwd(x, w, bias, state0, dout, *, dx=None, want_dstate0=True, ws=None, stream=None):
     """Backward of ``sum(dout * out)``: dict dx (act dtype), dw, dbias, dstate0 (f32)."""
     B, L, D = x.shape
     K = w.shape[1]
-    g = {"dx": torch.empty_like(x), "dw": torch.empty_like(w), "dbias": torch.empty_like(bias),
+    g = {"dx": torch.empty_like(x) if dx is None else dx, "dw": torch.empty_like(w), "dbias": torch.empty_like(bias),
          "dstate0": torch.empty((B, D, K - 1), dtype=torch.float32, device=x.device) if want_dstate0 else None}
     ws, wsb = _workspace(conv1d_bwd_workspace_bytes(B, L, D, K, _act(x)), x.device, ws)
     rc = load_library().ssm_conv1d_bwd(B, L, D, K, _act(x), _p(x), _p(w), _p(bias), _p(state0), _p(dout),
@@ -311,3 +314,15 @@ def conv1d_step(x, w, bias, state, *, out=None, stream=None):
                                         _stream(stream))
     _check("ssm_conv1d_step", rc)
     return out
+
+
+def conv1d_path(x, w, dout=None, y=None):
+    """Name of the kernel path ("tile", "vector" or "scalar") a conv1d call on
+    these tensors takes; ``dout`` given asks about the backward (``y`` = dx),
+    else the forward (``y`` = out).  A host-side query: nothing is launched."""
+    B, L, D = x.shape
+    K = w.shape[1]
+    rc = load_library().ssm_conv1d_path(B, L, D, K, _act(x), _p(x), _p(dout), _p(y if y is not None else x))
+    if rc < 0:
+        _check("ssm_conv1d_path", -rc)
+    return CONV_PATHS[rc]

@@ -29,20 +29,27 @@ def _dev(*ts):
     return [None if t is None else t.cuda() for t in ts]
 
 
+# (B, L, D, K, act, kernel path of both directions)
 SHAPES = [
-    (2, 100, 64, 4, "f32"), (2, 100, 64, 4, "bf16"),   # vector path
-    (3, 67, 37, 4, "f32"), (1, 130, 21, 3, "bf16"),    # odd channels: scalar path
-    (2, 2, 16, 4, "f32"),                              # shorter than the window
-    (1, 200, 32, 1, "f32"), (2, 150, 24, 8, "bf16"),   # width 1 and the widest
-    (2, 129, 256, 4, "bf16"),                          # ragged run (64-step runs)
+    (2, 100, 64, 4, "f32", "tile"), (2, 100, 64, 4, "bf16", "tile"),
+    (3, 67, 37, 4, "f32", "scalar"), (1, 130, 21, 3, "bf16", "scalar"),  # odd channel counts
+    (2, 100, 12, 4, "bf16", "vector"),        # rows of 24 bytes: no tensor map
+    (2, 2, 16, 4, "f32", "tile"),             # shorter than the window
+    (3, 1, 8, 4, "bf16", "tile"),             # a single step
+    (1, 200, 32, 1, "f32", "tile"), (2, 150, 24, 8, "bf16", "tile"),  # width 1 and the widest
+    (2, 129, 256, 4, "bf16", "tile"),         # ragged last tile of 64 steps
+    (2, 300, 200, 5, "f32", "tile"),          # ragged channel tile (128 + 72)
+    (1, 70, 136, 8, "bf16", "tile"),          # channel tile of 8, widest window
 ]
 
 
-@pytest.mark.parametrize("B,L,D,K,act", SHAPES)
+@pytest.mark.parametrize("B,L,D,K,act,path", SHAPES)
 @pytest.mark.parametrize("state", [True, False])
-def test_conv1d_fwd_bwd_parity(B, L, D, K, act, state):
+def test_conv1d_fwd_bwd_parity(B, L, D, K, act, path, state):
     x, w, bias, s0, dout = _case(B, L, D, K, act, seed=B + L + K, state=state)
     xd, wd, bd, sd, dd = _dev(x, w, bias, s0, dout)
+    assert s6.conv1d_path(xd, wd) == path
+    assert s6.conv1d_path(xd, wd, dout=dd, y=torch.empty_like(dd)) == path
     out, s_last = s6.conv1d_fwd(xd, wd, bd, sd)
     g = s6.conv1d_bwd(xd, wd, bd, sd, dd)
     torch.cuda.synchronize()
@@ -101,3 +108,40 @@ def test_conv1d_empty():
     torch.cuda.synchronize()
     assert torch.count_nonzero(g["dw"]) == 0 and torch.count_nonzero(g["dbias"]) == 0
     assert torch.count_nonzero(g["dstate0"]) == 0
+
+
+def _offset_copy(t, elems):
+    """A copy of ``t`` whose data starts ``elems`` elements into a fresh buffer
+    (to steer the kernel choice by alignment)."""
+    buf = torch.empty(t.numel() + elems, dtype=t.dtype, device=t.device)
+    v = buf[elems:].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+def test_conv1d_paths_agree():
+    """The tile, vector and scalar kernels on the same bf16 problem, steered
+    by the alignment of x, dout, out and dx: forward outputs and dx agree bit
+    for bit (same arithmetic per element); dw and dbias, summed in other
+    orders, agree to rounding."""
+    B, L, D, K = 2, 333, 192, 4
+    x, w, bias, s0, dout = _case(B, L, D, K, "bf16", seed=8)
+    xd, wd, bd, sd, dd = _dev(x, w, bias, s0, dout)
+    res = {}
+    for off, path in ((0, "tile"), (4, "vector"), (1, "scalar")):
+        xo, do = _offset_copy(xd, off), _offset_copy(dd, off)
+        out = _offset_copy(torch.empty_like(xd), off)
+        assert s6.conv1d_path(xo, wd, y=out) == path
+        s6.conv1d_fwd(xo, wd, bd, sd, out=out)
+        dx = _offset_copy(torch.empty_like(xd), off)
+        assert s6.conv1d_path(xo, wd, dout=do, y=dx) == path
+        g = s6.conv1d_bwd(xo, wd, bd, sd, do, dx=dx)
+        res[path] = (out.clone(), g)
+    torch.cuda.synchronize()
+    ref_out, ref_g = res["tile"]
+    for path in ("vector", "scalar"):
+        out, g = res[path]
+        assert torch.equal(out, ref_out), path
+        assert torch.equal(g["dx"], ref_g["dx"]), path
+        for k in ("dw", "dbias", "dstate0"):
+            assert rel_err(np64(g[k]), np64(ref_g[k])) <= 1e-5, (path, k)
