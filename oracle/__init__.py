@@ -12,7 +12,9 @@ the recurrence, discretisation and readout of the final selective_scan_kernel
 on the POPCORNBENCH transcript page (FW-GLM-5-1__l2_p30), with the softplus,
 exp_negate, SiLU-gate and gating-backward steps named by the mamba-rs
 kernels.rs page (MambaKernels doc comments), and a chain-rule backward that no
-page writes out (pinned in tests by finite differences).
+page writes out (pinned in tests by finite differences).  The optional limit
+on Δ (``dt_limit``) is the clamp and gradient mask of the
+mamba3_preprocess_backward.slang page.
 """
 from __future__ import annotations
 
@@ -51,11 +53,12 @@ def build(force: bool = False) -> str:
 def _open(path):
     lib = ctypes.CDLL(path)
     i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
-    lib.s6o_fwd.argtypes = [i64] * 4 + [vp] * 9 + [vp] * 2 + [i64] * 4 + [ci]
+    f64 = ctypes.c_double
+    lib.s6o_fwd.argtypes = [i64] * 4 + [vp] * 9 + [vp] * 2 + [i64] * 4 + [ci, f64, f64]
     lib.s6o_fwd.restype = ci
-    lib.s6o_bwd.argtypes = [i64] * 4 + [vp] * 9 + [vp] * 2 + [vp] * 9 + [i64] * 4 + [ci]
+    lib.s6o_bwd.argtypes = [i64] * 4 + [vp] * 9 + [vp] * 2 + [vp] * 9 + [i64] * 4 + [ci, f64, f64]
     lib.s6o_bwd.restype = ci
-    lib.s6o_step.argtypes = [i64] * 3 + [vp] * 8 + [vp] * 2
+    lib.s6o_step.argtypes = [i64] * 3 + [vp] * 8 + [vp] * 2 + [f64, f64]
     lib.s6o_step.restype = ci
     return lib
 
@@ -99,6 +102,14 @@ def default_threads() -> int:
     return max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count() or 1)
 
 
+def _limits(dt_limit):
+    """(dt_min, dt_max) of the Δ clamp; None means no limit, (0, +inf)."""
+    if dt_limit is None:
+        return 0.0, float("inf")
+    lo, hi = float(dt_limit[0]), float(dt_limit[1])
+    return lo, hi
+
+
 def _shapes(u, Bm):
     B, L, D = u.shape
     N = Bm.shape[2]
@@ -106,11 +117,12 @@ def _shapes(u, Bm):
 
 
 def fwd(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0=None, *, b_range=None,
-        d_range=None, threads=None):
+        d_range=None, threads=None, dt_limit=None):
     """Forward scan.  Returns ``(out [B,L,D], h_last [B,D,N])`` as f64 arrays.
 
     With ``b_range``/``d_range`` only those batches/channels are computed; the
-    other entries of the returned arrays are NaN.
+    other entries of the returned arrays are NaN.  ``dt_limit = (dt_min,
+    dt_max)`` clamps Δ = softplus(s) to that range.
     """
     u, delta_raw, z, Bm, Cm = map(_f64, (u, delta_raw, z, Bm, Cm))
     A_log, Dp, delta_bias, h0 = map(_f64, (A_log, Dp, delta_bias, h0))
@@ -121,14 +133,14 @@ def fwd(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0=None, *, b_range=None
     h_last = np.full((B, D, N), np.nan)
     rc = _load().s6o_fwd(B, L, D, N, _ptr(u), _ptr(delta_raw), _ptr(z), _ptr(Bm), _ptr(Cm),
                          _ptr(A_log), _ptr(Dp), _ptr(delta_bias), _ptr(h0), _ptr(out),
-                         _ptr(h_last), b0, b1, d0, d1, threads or default_threads())
+                         _ptr(h_last), b0, b1, d0, d1, threads or default_threads(), *_limits(dt_limit))
     if rc != 0:
         raise ValueError(f"s6o_fwd failed with code {rc}")
     return out, h_last
 
 
 def bwd(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0, dout, dh_last=None, *,
-        b_range=None, d_range=None, threads=None):
+        b_range=None, d_range=None, threads=None, dt_limit=None):
     """Backward of ``loss = sum(dout*out) + sum(dh_last*h_last)``.
 
     Returns a dict of f64 arrays: du, d_delta_raw, dz (NaN where not computed),
@@ -152,13 +164,13 @@ def bwd(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0, dout, dh_last=None, 
                          _ptr(dh_last), _ptr(r["du"]), _ptr(r["d_delta_raw"]), _ptr(r["dz"]),
                          _ptr(r["dBm"]), _ptr(r["dCm"]), _ptr(r["dA_log"]), _ptr(r["dD"]),
                          _ptr(r["d_delta_bias"]), _ptr(r["dh0"]), b0, b1, d0, d1,
-                         threads or default_threads())
+                         threads or default_threads(), *_limits(dt_limit))
     if rc != 0:
         raise ValueError(f"s6o_bwd failed with code {rc}")
     return r
 
 
-def step(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h):
+def step(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h, *, dt_limit=None):
     """One decode step (T = 1).  u, delta_raw, z: [B,D]; Bm, Cm: [B,N]; h: [B,D,N].
 
     Returns ``(out [B,D], h_new [B,D,N])``; the input ``h`` is not modified.
@@ -170,7 +182,8 @@ def step(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h):
     N = Bm.shape[1]
     out = np.full((B, D), np.nan)
     rc = _load().s6o_step(B, D, N, _ptr(u), _ptr(delta_raw), _ptr(z), _ptr(Bm), _ptr(Cm),
-                          _ptr(A_log), _ptr(Dp), _ptr(delta_bias), _ptr(h_new), _ptr(out))
+                          _ptr(A_log), _ptr(Dp), _ptr(delta_bias), _ptr(h_new), _ptr(out),
+                          *_limits(dt_limit))
     if rc != 0:
         raise ValueError(f"s6o_step failed with code {rc}")
     return out, h_new

@@ -16,6 +16,16 @@
  *            h_t   = a * h_{t-1} + delta * Bm[b,t,n] * u   (h_{-1} = h0 or 0)
  *            y     = sum_n Cm[b,t,n] * h_t + Dp[d] * u
  *            out   = y * z * sigmoid(z)                  (out = y when z is absent)
+ *   optional Δ limit [dt_min, dt_max] (no limit: 0 and +inf):
+ *            delta = min(max(softplus(s), dt_min), dt_max)
+ *            and in the backward d_delta_raw is multiplied by the mask
+ *            [dt_min <= softplus(s) <= dt_max] (both ends inclusive): the
+ *            clamped steps pass no gradient to delta_raw and delta_bias.
+ *            Source: the mamba3_preprocess_backward.slang page (oarust crate)
+ *            clamps softplus(raw dt + bias) to [dt_min, dt_max] and masks the
+ *            raw-dt gradient with that inclusive test; the
+ *            deterministic_backward.py page passes dt_limit = (0, inf) as the
+ *            default of the same clamp.
  *   Sources: the recurrence, discretisation and readout are the ones the final
  *   selective_scan_kernel computes on the POPCORNBENCH page (transcript
  *   FW-GLM-5-1__l2_p30): "A_val = -expf(A_log[d*N+n])", "dA = expf(delta*A)",
@@ -31,7 +41,7 @@
  *            g_t = dy_t * Cm_t + a_{t+1} * g_{t+1},  g at t = L-1 starts from dh_last
  *            du  = Dp * dy + delta * sum_n g * Bm
  *            ddelta = sum_n g * (A * a * h_{t-1} + Bm * u)
- *            d_delta_raw = ddelta * sigmoid(s)          (softplus' = sigmoid)
+ *            d_delta_raw = ddelta * sigmoid(s) * mask   (softplus' = sigmoid)
  *            dBm[b,t,n] = sum_d g * delta * u           dCm[b,t,n] = sum_d dy * h_t
  *            dDp[d] = sum_{b,t} dy * u                  d_delta_bias[d] = sum_{b,t} d_delta_raw
  *            dA_log[d,n] = A * sum_{b,t} g * delta * a * h_{t-1}   (dA/dA_log = A)
@@ -54,11 +64,19 @@
 typedef struct {
   int64_t B, L, D, N;
   const double *u, *delta_raw, *z, *Bm, *Cm, *A_log, *Dp, *delta_bias, *h0;
+  double dt_min, dt_max; /* the limit on delta (0 and +inf: none) */
 } s6o_problem;
 
 /* softplus(s) = log(1 + e^s), written so that neither branch overflows. */
 static double s6o_softplus(double s) {
   return s > 0.0 ? s + log1p(exp(-s)) : log1p(exp(s));
+}
+
+/* delta = softplus(s) clamped to [dt_min, dt_max] */
+static double s6o_delta(const s6o_problem *p, double sp) {
+  if (sp < p->dt_min) return p->dt_min;
+  if (sp > p->dt_max) return p->dt_max;
+  return sp;
 }
 
 /* logistic sigmoid; for x -> -inf exp(-x) overflows to inf and the result is 0. */
@@ -88,7 +106,7 @@ static void s6o_scan_channel(const s6o_problem *p, int64_t b, int64_t d, double 
   for (int64_t t = 0; t < p->L; ++t) {
     const double u = p->u[ix_bld(p, b, t, d)];
     const double s = p->delta_raw[ix_bld(p, b, t, d)] + p->delta_bias[d];
-    const double delta = s6o_softplus(s);
+    const double delta = s6o_delta(p, s6o_softplus(s));
     double y = 0.0;
     for (int64_t n = 0; n < N; ++n) {
       const double A = -exp(p->A_log[d * N + n]);
@@ -158,11 +176,11 @@ int s6o_fwd(int64_t B, int64_t L, int64_t D, int64_t N, const double *u,
             const double *delta_raw, const double *z, const double *Bm, const double *Cm,
             const double *A_log, const double *Dp, const double *delta_bias,
             const double *h0, double *out, double *h_last, int64_t b0, int64_t b1,
-            int64_t d0, int64_t d1, int nthreads) {
+            int64_t d0, int64_t d1, int nthreads, double dt_min, double dt_max) {
   if (B < 0 || L < 0 || D < 0 || N < 0 || b0 < 0 || b1 > B || b0 > b1 || d0 < 0 || d1 > D ||
-      d0 > d1)
+      d0 > d1 || !(dt_min <= dt_max))
     return -1;
-  s6o_problem p = {B, L, D, N, u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0};
+  s6o_problem p = {B, L, D, N, u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0, dt_min, dt_max};
   s6o_fwd_job job;
   job.p = &p;
   job.b0 = b0; job.b1 = b1; job.d0 = d0; job.d1 = d1;
@@ -185,9 +203,10 @@ int s6o_fwd(int64_t B, int64_t L, int64_t D, int64_t N, const double *u,
  */
 int s6o_step(int64_t B, int64_t D, int64_t N, const double *u, const double *delta_raw,
              const double *z, const double *Bm, const double *Cm, const double *A_log,
-             const double *Dp, const double *delta_bias, double *h, double *out) {
-  if (B < 0 || D < 0 || N < 0) return -1;
-  s6o_problem p = {B, 1, D, N, u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, NULL};
+             const double *Dp, const double *delta_bias, double *h, double *out, double dt_min,
+             double dt_max) {
+  if (B < 0 || D < 0 || N < 0 || !(dt_min <= dt_max)) return -1;
+  s6o_problem p = {B, 1, D, N, u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, NULL, dt_min, dt_max};
   for (int64_t b = 0; b < B; ++b)
     for (int64_t d = 0; d < D; ++d) s6o_scan_channel(&p, b, d, h + (b * D + d) * N, out, NULL, NULL, NULL);
   return 0;
@@ -223,7 +242,9 @@ static void s6o_bwd_channel(s6o_bwd_job *job, int64_t b, int64_t d, double *hist
     const int64_t i = ix_bld(p, b, t, d);
     const double u = p->u[i];
     const double s = p->delta_raw[i] + p->delta_bias[d];
-    const double delta = s6o_softplus(s);
+    const double sp = s6o_softplus(s);
+    const double delta = s6o_delta(p, sp);
+    const double mask = (sp >= p->dt_min && sp <= p->dt_max) ? 1.0 : 0.0;
     const double y = hist_y[t];
     const double dout = job->dout[i];
     double dy;
@@ -252,7 +273,7 @@ static void s6o_bwd_channel(s6o_bwd_job *job, int64_t b, int64_t d, double *hist
       g[n] = a * gt; /* carry for step t-1 */
     }
     if (job->du) job->du[i] = p->Dp[d] * dy + delta * sum_gB;
-    const double d_raw = sum_dh_ddelta * s6o_sigmoid(s);
+    const double d_raw = sum_dh_ddelta * s6o_sigmoid(s) * mask;
     if (job->d_delta_raw) job->d_delta_raw[i] = d_raw;
     *acc_dD += dy * u;
     *acc_dbias += d_raw;
@@ -311,11 +332,11 @@ int s6o_bwd(int64_t B, int64_t L, int64_t D, int64_t N, const double *u,
             const double *h0, const double *dout, const double *dh_last, double *du,
             double *d_delta_raw, double *dz, double *dBm, double *dCm, double *dA_log,
             double *dDp, double *d_delta_bias, double *dh0, int64_t b0, int64_t b1,
-            int64_t d0, int64_t d1, int nthreads) {
+            int64_t d0, int64_t d1, int nthreads, double dt_min, double dt_max) {
   if (B < 0 || L < 0 || D < 0 || N < 0 || b0 < 0 || b1 > B || b0 > b1 || d0 < 0 || d1 > D ||
-      d0 > d1)
+      d0 > d1 || !(dt_min <= dt_max))
     return -1;
-  s6o_problem p = {B, L, D, N, u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0};
+  s6o_problem p = {B, L, D, N, u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0, dt_min, dt_max};
   s6o_bwd_job job;
   memset(&job, 0, sizeof(job));
   job.p = &p;

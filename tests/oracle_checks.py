@@ -37,14 +37,14 @@ def rand_problem(B, L, D, N, seed, *, with_z=True, with_h0=True, with_dh_last=Tr
     return p, dout, dh_last
 
 
-def _fwd(p):
+def _fwd(p, dt_limit=None):
     return oracle.fwd(p["u"], p["delta_raw"], p["z"], p["Bm"], p["Cm"], p["A_log"], p["Dp"],
-                      p["delta_bias"], p["h0"], threads=1)
+                      p["delta_bias"], p["h0"], threads=1, dt_limit=dt_limit)
 
 
-def _bwd(p, dout, dh_last):
+def _bwd(p, dout, dh_last, dt_limit=None):
     return oracle.bwd(p["u"], p["delta_raw"], p["z"], p["Bm"], p["Cm"], p["A_log"], p["Dp"],
-                      p["delta_bias"], p["h0"], dout, dh_last, threads=1)
+                      p["delta_bias"], p["h0"], dout, dh_last, threads=1, dt_limit=dt_limit)
 
 
 # --------------------------------------------------------------- closed form
@@ -85,8 +85,8 @@ def check_closed_form(seed=0, shape=(2, 9, 3, 5), **kw):
 
 # --------------------------------------------------------------- finite differences
 
-def _loss(p, dout, dh_last):
-    out, h_last = _fwd(p)
+def _loss(p, dout, dh_last, dt_limit=None):
+    out, h_last = _fwd(p, dt_limit)
     v = float(np.sum(dout * out))
     if dh_last is not None:
         v += float(np.sum(dh_last * h_last))
@@ -97,10 +97,13 @@ GRAD_OF = {"u": "du", "delta_raw": "d_delta_raw", "z": "dz", "Bm": "dBm", "Cm": 
            "A_log": "dA_log", "Dp": "dD", "delta_bias": "d_delta_bias", "h0": "dh0"}
 
 
-def check_finite_differences(seed=0, shape=(2, 7, 3, 2), eps=1e-6, **kw):
+def check_finite_differences(seed=0, shape=(2, 7, 3, 2), eps=1e-6, dt_limit=None, p=None, **kw):
     """max over inputs of  max|fd - analytic| / max|analytic|  (central differences)."""
-    p, dout, dh_last = rand_problem(*shape, seed, **kw)
-    g = _bwd(p, dout, dh_last)
+    if p is None:
+        p, dout, dh_last = rand_problem(*shape, seed, **kw)
+    else:
+        p, dout, dh_last = p
+    g = _bwd(p, dout, dh_last, dt_limit)
     worst = 0.0
     for name, gname in GRAD_OF.items():
         x = p[name]
@@ -113,9 +116,9 @@ def check_finite_differences(seed=0, shape=(2, 7, 3, 2), eps=1e-6, **kw):
             old = flat[i]
             h = eps * max(1.0, abs(old))
             flat[i] = old + h
-            lp = _loss(p, dout, dh_last)
+            lp = _loss(p, dout, dh_last, dt_limit)
             flat[i] = old - h
-            lm = _loss(p, dout, dh_last)
+            lm = _loss(p, dout, dh_last, dt_limit)
             flat[i] = old
             fdf[i] = (lp - lm) / (2 * h)
         an = g[gname]
@@ -215,6 +218,73 @@ def check_internal_consistency(seed=6):
     return float(max(e1, e2))
 
 
+# --------------------------------------------------------------- the limit on Δ
+
+def _softplus(s):
+    return np.logaddexp(0.0, s)
+
+
+def dt_limit_problem(B, L, D, N, seed, lo_q=0.3, hi_q=0.7, margin=1e-3):
+    """A random problem and a limit [dt_min, dt_max] at the lo_q / hi_q
+    quantiles of its Δ = softplus(s), so that both ends clamp; every s whose
+    softplus lies within ``margin`` of a limit is moved off it (a finite
+    difference or an f32 rounding must not cross a kink)."""
+    p, dout, dh_last = rand_problem(B, L, D, N, seed)
+    sp = _softplus(p["delta_raw"] + p["delta_bias"])
+    lo, hi = np.quantile(sp, lo_q), np.quantile(sp, hi_q)
+    for _ in range(8):
+        sp = _softplus(p["delta_raw"] + p["delta_bias"])
+        near = (np.abs(sp - lo) < margin) | (np.abs(sp - hi) < margin)
+        if not near.any():
+            break
+        p["delta_raw"][near] += 4 * margin
+    return (p, dout, dh_last), (float(lo), float(hi))
+
+
+def check_dt_limit_finite_differences(seed=11):
+    """With both ends of the limit active: every gradient against central
+    differences of the clamped loss (the clamped steps give delta_raw and
+    delta_bias no gradient; du, dB, dA_log use the clamped Δ)."""
+    prob, lim = dt_limit_problem(2, 7, 3, 2, seed)
+    return check_finite_differences(p=prob, dt_limit=lim)
+
+
+def check_dt_limit_reparam(seed=12):
+    """The limit acts on Δ = softplus(s): the clamped forward equals the
+    unclamped forward of delta_raw' = softplus^-1(clamp(softplus(s))) - bias."""
+    (p, _, _), (lo, hi) = dt_limit_problem(2, 9, 3, 4, seed, margin=0.0)
+    out, h_last = _fwd(p, (lo, hi))
+    s = p["delta_raw"] + p["delta_bias"]
+    delta = np.clip(_softplus(s), lo, hi)
+    q = dict(p)
+    q["delta_raw"] = np.log(np.expm1(delta)) - p["delta_bias"]
+    ref_out, ref_h = _fwd(q)
+    return max(float(np.max(np.abs(out - ref_out)) / np.max(np.abs(ref_out))),
+               float(np.max(np.abs(h_last - ref_h)) / np.max(np.abs(ref_h))))
+
+
+def check_dt_constant(L=40, N=3, seed=13):
+    """dt_min = dt_max = c fixes Δ = c whatever delta_raw is: with constant
+    u, B, C, z the state is the geometric series c B u (1 - a^{t+1}) / (1 - a),
+    a = e^{c A}; and no gradient reaches delta_raw or delta_bias."""
+    r = np.random.default_rng(seed)
+    D, c = 2, 0.37
+    u0, z0 = 0.7, 0.8
+    B0, C0 = np.array([1.5, -0.4, 0.9])[:N], np.array([0.2, 1.1, -0.6])[:N]
+    A_log = np.tile(np.log(np.arange(1, N + 1, dtype=float)), (D, 1))
+    p = {"u": np.full((1, L, D), u0), "delta_raw": r.standard_normal((1, L, D)),
+         "z": np.full((1, L, D), z0), "Bm": np.tile(B0, (1, L, 1)), "Cm": np.tile(C0, (1, L, 1)),
+         "A_log": A_log, "Dp": np.array([0.5, -1.0]), "delta_bias": np.zeros(D), "h0": None}
+    out, _ = _fwd(p, (c, c))
+    a = np.exp(-c * np.arange(1, N + 1))
+    t = np.arange(L)[:, None]
+    h = c * B0 * u0 * (1 - a[None, :] ** (t + 1)) / (1 - a[None, :])
+    ref = ((h @ C0)[:, None] + p["Dp"][None, :] * u0) * z0 * expit(z0)
+    g = _bwd(p, r.standard_normal((1, L, D)), None, (c, c))
+    return max(float(np.max(np.abs(out[0] - ref)) / np.max(np.abs(ref))),
+               float(np.max(np.abs(g["d_delta_raw"]))), float(np.max(np.abs(g["d_delta_bias"]))))
+
+
 ALL_CHECKS = {
     "closed_form": (lambda: check_closed_form(), 1e-12),
     "closed_form_nogate": (lambda: check_closed_form(seed=1, with_z=False, with_h0=False), 1e-12),
@@ -225,4 +295,7 @@ ALL_CHECKS = {
     "state_reset": (lambda: check_state_reset(), 1e-13),
     "lti_convolution": (lambda: check_lti_convolution(), 1e-12),
     "internal_consistency": (lambda: check_internal_consistency(), 1e-12),
+    "dt_limit_finite_differences": (lambda: check_dt_limit_finite_differences(), 1e-6),
+    "dt_limit_reparam": (lambda: check_dt_limit_reparam(), 1e-12),
+    "dt_constant": (lambda: check_dt_constant(), 1e-12),
 }

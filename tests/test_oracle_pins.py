@@ -129,8 +129,8 @@ MUTANTS = {
                             "const double bt = p->Bm[ix_bln(p, b, t, n)] * u;"),
     "softplus_branch": ("s + log1p(exp(-s))", "log1p(exp(-s))"),
     "gate_without_z": ("o = y * z * s6o_sigmoid(z);", "o = y * s6o_sigmoid(z);"),
-    "bias_index": ("p->delta_bias[d];\n    const double delta = s6o_softplus(s);\n    double y",
-                   "p->delta_bias[0];\n    const double delta = s6o_softplus(s);\n    double y"),
+    "bias_index": ("p->delta_bias[d];\n    const double delta = s6o_delta(p, s6o_softplus(s));\n    double y",
+                   "p->delta_bias[0];\n    const double delta = s6o_delta(p, s6o_softplus(s));\n    double y"),
     "dz_formula": ("(1.0 + z * (1.0 - sz))", "(1.0 + z * sz)"),
     "g_no_decay": ("g[n] = a * gt;", "g[n] = gt;"),
     "ddelta_drop_state_term": ("gt * (A * a * h_prev + Bn * u)", "gt * (Bn * u)"),
@@ -142,6 +142,12 @@ MUTANTS = {
     "h_prev_off_by_one": ("hist_h[(t - 1) * N + n]", "hist_h[t * N + n]"),
     "dh_last_ignored": ("g[n] = job->dh_last ? job->dh_last[(b * p->D + d) * N + n] : 0.0;",
                         "g[n] = 0.0;"),
+    "dt_mask_dropped": ("sum_dh_ddelta * s6o_sigmoid(s) * mask", "sum_dh_ddelta * s6o_sigmoid(s)"),
+    "dt_mask_inverted": ("? 1.0 : 0.0;", "? 0.0 : 1.0;"),
+    "dt_clamp_on_s": ("const double delta = s6o_delta(p, s6o_softplus(s));",
+                      "const double delta = s6o_softplus(s6o_delta(p, s));"),
+    "dt_max_ignored": ("if (sp > p->dt_max) return p->dt_max;", ""),
+    "dt_bwd_unclamped_delta": ("const double delta = s6o_delta(p, sp);", "const double delta = sp;"),
 }
 
 
