@@ -510,9 +510,15 @@ def run_ours(args, world, rank, local):
         pipelined_step(k)
     torch.cuda.synchronize(dev)
     ke = max(2, args.e2e_steps)
-    serial_ms = timed(lambda k: serial_step(), ke, stream, stream)
-    s_in.wait_stream(stream)
-    e2e_ms = timed(pipelined_step, ke, s_in, s_out)
+    # three runs of each, the median reported: the host link's rate moves
+    # between runs (other work on the host's memory), the kernels' does not
+    serial_runs, e2e_runs = [], []
+    for _ in range(3):
+        serial_runs.append(timed(lambda k: serial_step(), ke, stream, stream))
+        s_in.wait_stream(stream)
+        e2e_runs.append(timed(pipelined_step, ke, s_in, s_out))
+    serial_ms = sorted(serial_runs)[1]
+    e2e_ms = sorted(e2e_runs)[1]
     e2e_value = world * cells / (e2e_ms * 1e-3) / 1e9
     serial_value = world * cells / (serial_ms * 1e-3) / 1e9
     # the host link alone: the same copies with no compute, each direction by
@@ -592,7 +598,9 @@ def run_ours(args, world, rank, local):
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "steps": ke,
                 "overlap": "copy-in of step k+1 and copy-out of step k-1 overlap step k "
                            "(three streams, two device buffer sets)",
-                "serial": {"value": round(serial_value, 2), "ms_per_step": round(serial_ms, 4)},
+                "runs_ms_per_step": [round(v, 4) for v in e2e_runs], "reported": "median of 3 runs",
+                "serial": {"value": round(serial_value, 2), "ms_per_step": round(serial_ms, 4),
+                           "runs_ms_per_step": [round(v, 4) for v in serial_runs]},
                 "host_link": link},
         "gpu_launches": launches_per_step(fwd_seg, bwd_seg) * K,
         "segments": {"fwd": fwd_seg, "bwd": bwd_seg},

@@ -239,6 +239,53 @@ int ssm_step(int64_t batch, int64_t dim, int64_t dstate, int act, const void *u,
              void *stream);
 
 /* ---------------------------------------------------------------------------
+ * Limit on delta (dt_limit).  The _ex entry points below are the ones above
+ * with one more argument, `opts` (NULL: the defaults, identical to the plain
+ * calls).  With opts->dt_min / dt_max the discretisation step is clamped,
+ *   delta = min(max(softplus(s), dt_min), dt_max)
+ * (mamba3_preprocess_backward.slang page: dt = clamp(softplus, dt_min,
+ * dt_max)), and the backward passes no gradient to delta_raw / delta_bias
+ * through a clamped step (that page's dt mask).  The forward, the backward
+ * and the step of one problem must be given the same limit.  0 <= dt_min <=
+ * dt_max (dt_max may be +inf), else SSM_ERR_INVALID_ARG.  Defaults: 0, +inf
+ * (no limit).  At a step whose softplus falls exactly on a bound the mask
+ * may take either value.
+ */
+typedef struct ssm_scan_options {
+  float dt_min;
+  float dt_max;
+} ssm_scan_options;
+
+/* ssm_scan_fwd with options; chunk_states nullable (no saves, as
+ * ssm_scan_fwd_nosave). */
+int ssm_scan_fwd_ex(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
+                    const void *u, const void *delta_raw, const void *z, const void *Bm,
+                    const void *Cm, const float *A_log, const float *Dp, const float *delta_bias,
+                    const float *h0, void *out, float *h_last, float *chunk_states, void *ws,
+                    size_t ws_bytes, void *stream, const ssm_scan_options *opts);
+
+int ssm_scan_bwd_ex(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
+                    const void *u, const void *delta_raw, const void *z, const void *Bm,
+                    const void *Cm, const float *A_log, const float *Dp, const float *delta_bias,
+                    const float *h0, const float *chunk_states, const void *dout,
+                    const float *dh_last, void *du, void *d_delta_raw, void *dz, void *dBm,
+                    void *dCm, float *dA_log, float *dDp, float *d_delta_bias, float *dh0,
+                    void *ws, size_t ws_bytes, void *stream, const ssm_scan_options *opts);
+
+int ssm_scan_bwd_partials_ex(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
+                             const void *u, const void *delta_raw, const void *z, const void *Bm,
+                             const void *Cm, const float *A_log, const float *Dp,
+                             const float *delta_bias, const float *chunk_states, const void *dout,
+                             const float *dh_last, void *du, void *d_delta_raw, void *dz,
+                             float *dh0, void *ws, size_t ws_bytes, void *stream,
+                             const ssm_scan_options *opts);
+
+int ssm_step_ex(int64_t batch, int64_t dim, int64_t dstate, int act, const void *u,
+                const void *delta_raw, const void *z, const void *Bm, const void *Cm,
+                const float *A_log, const float *Dp, const float *delta_bias, float *h, void *out,
+                void *stream, const ssm_scan_options *opts);
+
+/* ---------------------------------------------------------------------------
  * Causal depthwise conv1d + SiLU, the convolution in front of the scan in a
  * Mamba block (kernels.rs page: "Multi-step conv1d forward with state saves
  * for backward", "Multi-step conv1d backward", "Single-step depthwise conv1d

@@ -1,5 +1,6 @@
 // Host side of the C ABI declared in include/ssm_scan.h: argument checks,
 // workspace sizing and kernel dispatch.  No allocation, no synchronisation.
+#include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -155,11 +156,26 @@ BwdWorkspace bwd_ws_layout(int64_t B, int64_t L, int64_t D, int64_t N) {
   return w;
 }
 
+// dt_limit of an options struct (NULL: 0, +inf); 0 <= dt_min <= dt_max
+int read_opts(const ssm_scan_options* o, float* lo, float* hi) {
+  *lo = 0.f;
+  *hi = INFINITY;
+  if (!o) return SSM_OK;
+  if (!(o->dt_min >= 0.f) || !(o->dt_min <= o->dt_max))
+    return fail(SSM_ERR_INVALID_ARG, "dt limit needs 0 <= dt_min <= dt_max, got [%g, %g]", (double)o->dt_min,
+                (double)o->dt_max);
+  *lo = o->dt_min;
+  *hi = o->dt_max;
+  return SSM_OK;
+}
+
 int fwd_common(int64_t B, int64_t L, int64_t D, int64_t N, int act, const void* u,
                const void* delta_raw, const void* z, const void* Bm, const void* Cm,
                const float* A_log, const float* Dp, const float* delta_bias, const float* h0,
                void* out, float* h_last, float* chunk_states, bool save, void* ws,
-               size_t ws_bytes, void* stream, bool step = false) {
+               size_t ws_bytes, void* stream, const ssm_scan_options* opts, bool step = false) {
+  float dt_lo, dt_hi;
+  S6_TRY(read_opts(opts, &dt_lo, &dt_hi));
   S6_TRY(check_shape(B, L, D, N, act));
   const size_t e = act_size(act);
   const int64_t bld = B * L * D, bln = B * L * N, dn = D * N;
@@ -193,6 +209,8 @@ int fwd_common(int64_t B, int64_t L, int64_t D, int64_t N, int act, const void* 
   p.out = out; p.h_last = h_last; p.chunk_states = save ? chunk_states : nullptr;
   p.B = (int)B; p.L = (int)L; p.D = (int)D; p.N = (int)N;
   p.nchunks = (int)ssm_num_chunks(L);
+  p.dt_min = dt_lo;
+  p.dt_max = dt_hi;
   p.status = s6::device_status_word();
   if (!p.status) return fail(SSM_ERR_CUDA, "cannot locate the device status word");
   const FwdWorkspace w = fwd_ws_layout(B, L, D, N, act);
@@ -327,7 +345,17 @@ int ssm_scan_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int
                  const float* h0, void* out, float* h_last, float* chunk_states, void* ws,
                  size_t ws_bytes, void* stream) {
   return fwd_common(batch, seqlen, dim, dstate, act, u, delta_raw, z, Bm, Cm, A_log, Dp,
-                    delta_bias, h0, out, h_last, chunk_states, true, ws, ws_bytes, stream);
+                    delta_bias, h0, out, h_last, chunk_states, true, ws, ws_bytes, stream, nullptr);
+}
+
+int ssm_scan_fwd_ex(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
+                    const void* u, const void* delta_raw, const void* z, const void* Bm,
+                    const void* Cm, const float* A_log, const float* Dp, const float* delta_bias,
+                    const float* h0, void* out, float* h_last, float* chunk_states, void* ws,
+                    size_t ws_bytes, void* stream, const ssm_scan_options* opts) {
+  return fwd_common(batch, seqlen, dim, dstate, act, u, delta_raw, z, Bm, Cm, A_log, Dp,
+                    delta_bias, h0, out, h_last, chunk_states, chunk_states != nullptr, ws, ws_bytes,
+                    stream, opts);
 }
 
 int ssm_scan_fwd_nosave(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
@@ -336,7 +364,7 @@ int ssm_scan_fwd_nosave(int64_t batch, int64_t seqlen, int64_t dim, int64_t dsta
                         const float* delta_bias, const float* h0, void* out, float* h_last,
                         void* ws, size_t ws_bytes, void* stream) {
   return fwd_common(batch, seqlen, dim, dstate, act, u, delta_raw, z, Bm, Cm, A_log, Dp,
-                    delta_bias, h0, out, h_last, nullptr, false, ws, ws_bytes, stream);
+                    delta_bias, h0, out, h_last, nullptr, false, ws, ws_bytes, stream, nullptr);
 }
 
 int ssm_scan_bwd_partials(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
@@ -345,7 +373,21 @@ int ssm_scan_bwd_partials(int64_t batch, int64_t seqlen, int64_t dim, int64_t ds
                           const float* delta_bias, const float* chunk_states, const void* dout,
                           const float* dh_last, void* du, void* d_delta_raw, void* dz,
                           float* dh0, void* ws, size_t ws_bytes, void* stream) {
+  return ssm_scan_bwd_partials_ex(batch, seqlen, dim, dstate, act, u, delta_raw, z, Bm, Cm, A_log, Dp,
+                                  delta_bias, chunk_states, dout, dh_last, du, d_delta_raw, dz, dh0, ws,
+                                  ws_bytes, stream, nullptr);
+}
+
+int ssm_scan_bwd_partials_ex(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
+                             const void* u, const void* delta_raw, const void* z, const void* Bm,
+                             const void* Cm, const float* A_log, const float* Dp,
+                             const float* delta_bias, const float* chunk_states, const void* dout,
+                             const float* dh_last, void* du, void* d_delta_raw, void* dz,
+                             float* dh0, void* ws, size_t ws_bytes, void* stream,
+                             const ssm_scan_options* opts) {
   const int64_t B = batch, L = seqlen, D = dim, N = dstate;
+  float dt_lo, dt_hi;
+  S6_TRY(read_opts(opts, &dt_lo, &dt_hi));
   S6_TRY(check_shape(B, L, D, N, act));
   const size_t e = act_size(act);
   const int64_t bld = B * L * D, bln = B * L * N, dn = D * N;
@@ -377,6 +419,8 @@ int ssm_scan_bwd_partials(int64_t batch, int64_t seqlen, int64_t dim, int64_t ds
   p.ws_param = reinterpret_cast<float*>(static_cast<char*>(ws) + w.param_off);
   p.B = (int)B; p.L = (int)L; p.D = (int)D; p.N = (int)N;
   p.nchunks = (int)ssm_num_chunks(L);
+  p.dt_min = dt_lo;
+  p.dt_max = dt_hi;
   p.status = s6::device_status_word();
   if (!p.status) return fail(SSM_ERR_CUDA, "cannot locate the device status word");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -437,9 +481,23 @@ int ssm_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int
                  const float* dh_last, void* du, void* d_delta_raw, void* dz, void* dBm,
                  void* dCm, float* dA_log, float* dDp, float* d_delta_bias, float* dh0,
                  void* ws, size_t ws_bytes, void* stream) {
+  return ssm_scan_bwd_ex(batch, seqlen, dim, dstate, act, u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0,
+                         chunk_states, dout, dh_last, du, d_delta_raw, dz, dBm, dCm, dA_log, dDp, d_delta_bias,
+                         dh0, ws, ws_bytes, stream, nullptr);
+}
+
+int ssm_scan_bwd_ex(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
+                    const void* u, const void* delta_raw, const void* z, const void* Bm,
+                    const void* Cm, const float* A_log, const float* Dp, const float* delta_bias,
+                    const float* h0, const float* chunk_states, const void* dout,
+                    const float* dh_last, void* du, void* d_delta_raw, void* dz, void* dBm,
+                    void* dCm, float* dA_log, float* dDp, float* d_delta_bias, float* dh0,
+                    void* ws, size_t ws_bytes, void* stream, const ssm_scan_options* opts) {
   // h0 is not read: the chunk states already start from it.  It is checked so
   // that a caller passing a bad pointer hears about it.
   S6_TRY(opt(h0, 4, "h0"));
+  float dt_lo, dt_hi;
+  S6_TRY(read_opts(opts, &dt_lo, &dt_hi));
   const size_t e = (act == SSM_BF16) ? 2 : 4;
   // validate the finalize outputs before enqueueing the first half
   S6_TRY(check_shape(batch, seqlen, dim, dstate, act));
@@ -448,9 +506,9 @@ int ssm_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int
   S6_TRY(need(dA_log, dim * dstate, 4, "dA_log"));
   S6_TRY(need(dDp, dim, 4, "dDp"));
   S6_TRY(need(d_delta_bias, dim, 4, "d_delta_bias"));
-  S6_TRY(ssm_scan_bwd_partials(batch, seqlen, dim, dstate, act, u, delta_raw, z, Bm, Cm, A_log,
-                               Dp, delta_bias, chunk_states, dout, dh_last, du, d_delta_raw, dz,
-                               dh0, ws, ws_bytes, stream));
+  S6_TRY(ssm_scan_bwd_partials_ex(batch, seqlen, dim, dstate, act, u, delta_raw, z, Bm, Cm, A_log,
+                                  Dp, delta_bias, chunk_states, dout, dh_last, du, d_delta_raw, dz,
+                                  dh0, ws, ws_bytes, stream, opts));
   return ssm_scan_bwd_finalize(batch, seqlen, dim, dstate, act, dBm, dCm, dA_log, dDp,
                                d_delta_bias, ws, ws_bytes, stream);
 }
@@ -459,9 +517,17 @@ int ssm_step(int64_t batch, int64_t dim, int64_t dstate, int act, const void* u,
              const void* delta_raw, const void* z, const void* Bm, const void* Cm,
              const float* A_log, const float* Dp, const float* delta_bias, float* h, void* out,
              void* stream) {
+  return ssm_step_ex(batch, dim, dstate, act, u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h, out, stream,
+                     nullptr);
+}
+
+int ssm_step_ex(int64_t batch, int64_t dim, int64_t dstate, int act, const void* u,
+                const void* delta_raw, const void* z, const void* Bm, const void* Cm,
+                const float* A_log, const float* Dp, const float* delta_bias, float* h, void* out,
+                void* stream, const ssm_scan_options* opts) {
   S6_TRY(need(h, batch * dim * (dstate > 0 ? dstate : 0), 4, "h"));
   return fwd_common(batch, 1, dim, dstate, act, u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias,
-                    h, out, h, nullptr, false, nullptr, 0, stream, /*step=*/true);
+                    h, out, h, nullptr, false, nullptr, 0, stream, opts, /*step=*/true);
 }
 
 // ---------------------------------------------------------------- conv1d

@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kScanThreads)
         for (int i = 0; i < NG; ++i) ck[i] = h[i];
       }
       const size_t o = (size_t)t * D;
-      const float delta = softplus_f(ld_act(rp + o) + bias);
+      const float delta = clamp_dt(softplus_f(ld_act(rp + o) + bias), p.dt_min, p.dt_max);
       const float du = delta * ld_act(up + o);
 #pragma unroll
       for (int i = 0; i < NG; ++i) {
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kScanThreads)
         if (k < cnt) {
           const int t = ts + k;
           const size_t o = (size_t)t * D;
-          const float delta = softplus_f(ld_act(rp + o) + bias);
+          const float delta = clamp_dt(softplus_f(ld_act(rp + o) + bias), p.dt_min, p.dt_max);
           const float du = delta * ld_act(up + o);
 #pragma unroll
           for (int i = 0; i < NG; ++i) {
@@ -154,8 +154,10 @@ __global__ void __launch_bounds__(kScanThreads)
           const size_t o = (size_t)t * D;
           const float u = ld_act(up + o);
           const float s = ld_act(rp + o) + bias;
-          const float delta = softplus_f(s);
-          const float sig_s = sigmoid_f(s);
+          const float sp = softplus_f(s);
+          const float delta = clamp_dt(sp, p.dt_min, p.dt_max);
+          // softplus' = sigmoid, masked where the limit clamps (both ends inclusive)
+          const float sig_s = (sp >= p.dt_min && sp <= p.dt_max) ? sigmoid_f(s) : 0.f;
           const float dout = ld_act(gp + o);
           float Bn[NG], Cn[NG];
           float ypart = 0.f;

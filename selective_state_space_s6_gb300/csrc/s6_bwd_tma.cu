@@ -122,8 +122,9 @@ __device__ __forceinline__ float lds_at(const Act* tile, int byte_off) {
 
 // TPC lanes per channel, 4 states per lane (N = 4 * TPC); a CTA covers 64
 // channels with 64 * TPC consumer threads (2 * TPC warps), plus a producer
-// and a converter warp.
-template <typename Act, int TPC, bool kFast, bool kGate>
+// and a converter warp.  kLimit: delta is clamped to [dt_min, dt_max] (a
+// separate instance, so the unlimited scan pays nothing for it).
+template <typename Act, int TPC, bool kFast, bool kGate, bool kLimit>
 __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const __grid_constant__ BwdTmaParams P) {
   constexpr int N = 4 * TPC;
   constexpr int kLanes = kDTile * TPC;  // consumer threads
@@ -443,7 +444,8 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
               const int kr = kFull ? km : min(km, nv - 1);
               const int o = kr * kRB + (kFull ? colo[i % kOwnB] : AT::col(kr, cl));
               const float sv = lds_at(sr, o) + bias;
-              const float sp = kFast ? softplus_fast(sv) : softplus_f(sv);
+              const float sp0 = kFast ? softplus_fast(sv) : softplus_f(sv);
+              const float sp = kLimit ? clamp_dt(sp0, p.dt_min, p.dt_max) : sp0;
               if (kFull || km < nv) dtile[km * kRow + cl] = make_float2(sp, sp * lds_at(su, o));
             }
             __syncwarp();
@@ -607,7 +609,11 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
                 const float2 dv = dsub[kr * kRow + cl];
                 const float2 bp = bprep[kr * kRow + cl];
                 const float uo = lds_at(su, (ks + kr) * kRB + (kFull ? colo[i] : AT::col(kr, cl)));
-                const float dsp = kFast ? dsoftplus_fast(dv.x) : -expm1f(-dv.x);
+                // softplus' = sigmoid(s) = 1 - e^{-delta}; zero where the limit
+                // clamped delta (delta sits on a bound: a clamped step, or a
+                // softplus exactly on it, which has measure zero)
+                const bool free_dt = !kLimit || ((dv.x > p.dt_min || p.dt_min <= 0.f) && dv.x < p.dt_max);
+                const float dsp = free_dt ? (kFast ? dsoftplus_fast(dv.x) : -expm1f(-dv.x)) : 0.f;
                 const float draw = fmaf(uo, acc.y, acc.z) * dsp;
                 o_du[i] = fmaf(Dd, bp.x, dv.x * acc.y);
                 o_dr[i] = draw;
@@ -857,7 +863,8 @@ __global__ void __launch_bounds__(kAggWarps * 32) s6_bwd_agg_kernel(const __grid
       const int km = i * TPC + q;
       const int kr = min(km, cnt - 1);
       const int o = full_tile ? km * AT::kRowB + colo[i % kPer] : AT::off(kr, cl);
-      const float sp = kFast ? softplus_fast(lds_at(sr, o) + bias) : softplus_f(lds_at(sr, o) + bias);
+      const float sp = clamp_dt(kFast ? softplus_fast(lds_at(sr, o) + bias) : softplus_f(lds_at(sr, o) + bias),
+                                p.dt_min, p.dt_max);
       float dy = lds_at(sg, o);
       if (kGate) {
         const float zz = lds_at(sz, o);
@@ -975,9 +982,9 @@ size_t bwd_smem_bytes() {
   return bytes;
 }
 
-template <typename Act, int TPC, bool kFast, bool kGate>
+template <typename Act, int TPC, bool kFast, bool kGate, bool kLimit>
 cudaError_t launch_one(const BwdTmaParams& P, cudaStream_t stream, bool cooperative) {
-  auto kern = s6_bwd_tma_kernel<Act, TPC, kFast, kGate>;
+  auto kern = s6_bwd_tma_kernel<Act, TPC, kFast, kGate, kLimit>;
   const size_t smem = bwd_smem_bytes<Act, TPC>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -999,6 +1006,17 @@ cudaError_t launch_one(const BwdTmaParams& P, cudaStream_t stream, bool cooperat
   return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
+// the main kernel's instance for this call: gate or not, limit on delta or not
+template <typename Act, int TPC, bool kFast>
+cudaError_t launch_main(const BwdTmaParams& P, cudaStream_t stream, bool cooperative) {
+  const bool lim = P.p.dt_min > 0.f || P.p.dt_max < INFINITY;
+  if (P.p.z)
+    return lim ? launch_one<Act, TPC, kFast, true, true>(P, stream, cooperative)
+               : launch_one<Act, TPC, kFast, true, false>(P, stream, cooperative);
+  return lim ? launch_one<Act, TPC, kFast, false, true>(P, stream, cooperative)
+             : launch_one<Act, TPC, kFast, false, false>(P, stream, cooperative);
+}
+
 // TPC lanes per channel: 4 states per lane in both the main and the aggregate pass
 template <typename Act, int TPC, bool kFast>
 cudaError_t launch_tpc(BwdTmaParams& P, BwdTmaParams& Pagg, cudaStream_t stream) {
@@ -1010,7 +1028,7 @@ cudaError_t launch_tpc(BwdTmaParams& P, BwdTmaParams& Pagg, cudaStream_t stream)
     // last) gets there; a cooperative launch keeps every CTA resident
     cudaError_t e = cudaMemsetAsync(P.p.seq_flag, 0, sizeof(int) * (size_t)P.p.B * pl.ndt, stream);
     if (e != cudaSuccess) return e;
-    e = P.p.z ? launch_one<Act, TPC, kFast, true>(P, stream, true) : launch_one<Act, TPC, kFast, false>(P, stream, true);
+    e = launch_main<Act, TPC, kFast>(P, stream, true);
     if (e != cudaErrorCooperativeLaunchTooLarge) return e;
     (void)cudaGetLastError();  // not resident at once on this GPU: aggregate mode
   }
@@ -1026,7 +1044,7 @@ cudaError_t launch_tpc(BwdTmaParams& P, BwdTmaParams& Pagg, cudaStream_t stream)
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  return P.p.z ? launch_one<Act, TPC, kFast, true>(P, stream, false) : launch_one<Act, TPC, kFast, false>(P, stream, false);
+  return launch_main<Act, TPC, kFast>(P, stream, false);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }

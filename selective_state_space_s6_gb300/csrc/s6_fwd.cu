@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(kScanThreads)
     }
     const size_t o = (size_t)t * D;
     const float u = ld_act(up + o);
-    const float delta = softplus_f(ld_act(rp + o) + bias);
+    const float delta = clamp_dt(softplus_f(ld_act(rp + o) + bias), p.dt_min, p.dt_max);
     const float du = delta * u;
     float y = 0.f;
 #pragma unroll

@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
       for (int i = 0; i < kOwn; ++i) {
         const int km = i * TPC + q;
         const int kr = kFull ? km : min(km, n_valid - 1);
-        const float sp = softplus_k<kFast>(act_at(sr, kr, i, kFull) + bias);
+        const float sp = clamp_dt(softplus_k<kFast>(act_at(sr, kr, i, kFull) + bias), p.dt_min, p.dt_max);
         pv[i] = make_float2(sp, sp * act_at(su, kr, i, kFull));
         if (!kFull && km >= n_valid) pv[i] = make_float2(0.f, 0.f);
       }
@@ -496,7 +496,8 @@ __global__ void __launch_bounds__(256) s6_step_kernel(const FwdParams p) {
 
   // this lane's batch row of the group: delta and the gate factor
   const int bq = min(g * TPC + q, B - 1);
-  const float sp_q = softplus_k<kFast>(ld_act(static_cast<const Act*>(p.delta_raw) + (size_t)bq * D + d) + bias);
+  const float sp_q = clamp_dt(softplus_k<kFast>(ld_act(static_cast<const Act*>(p.delta_raw) + (size_t)bq * D + d) + bias),
+                                p.dt_min, p.dt_max);
   const float sl_q = kGate ? silu_k<kFast>(ld_act(static_cast<const Act*>(p.z) + (size_t)bq * D + d)) : 1.f;
 
   // every row's loads first (independent of one another; the state is

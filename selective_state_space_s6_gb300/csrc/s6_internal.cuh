@@ -81,6 +81,7 @@ struct FwdParams {
   float* h_last;        // nullable (may alias h0 for the decode step)
   float* chunk_states;  // nullable (nosave)
   unsigned int* status;  // device status word (bounded waits report here)
+  float dt_min, dt_max;   // limit on delta = softplus(s); 0 and +inf: none
   // Time segments (long sequences): the steps are split into nseg segments
   // of seg_len steps (a multiple of kChunk), run in parallel.  seg_agg
   // ([B][nseg][D][N][2] f32: decay product and zero-start end state of each
@@ -118,6 +119,7 @@ struct BwdParams {
   float* ws_dbc;    // [ndt][B][L][2][N] per-CTA sums of the dBm / dCm terms
   float* ws_param;  // [B][nseg][D][N+2] per-(batch, segment) sums: A*sum(...), dDp, d_delta_bias
   unsigned int* status;  // device status word (bounded waits report here)
+  float dt_min, dt_max;   // limit on delta = softplus(s); 0 and +inf: none
   // Pieces (chunked parallel scan): nseg = plan.maxp rows per batch;
   // seg_agg [B][nseg][D][N][2] holds each piece's decay product and
   // zero-carry adjoint carry-out, seg_carry [B][nseg][D][N] the adjoint carry
@@ -214,6 +216,10 @@ __device__ __forceinline__ void st_act<__nv_bfloat16>(__nv_bfloat16* p, float v)
 // softplus(s) = log(1 + e^s); above 20 it equals s to within 2e-9 relative
 // (the threshold the POPCORNBENCH kernel's softplus uses).
 __device__ __forceinline__ float softplus_f(float s) { return s > 20.f ? s : log1pf(expf(s)); }
+
+// delta limited to [lo, hi] (the dt_limit clamp; lo = 0, hi = +inf leaves
+// every softplus value as it is)
+__device__ __forceinline__ float clamp_dt(float sp, float lo, float hi) { return fminf(fmaxf(sp, lo), hi); }
 
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
 

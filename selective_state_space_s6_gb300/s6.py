@@ -26,6 +26,16 @@ CHUNK_LEN = 64
 MAX_DSTATE = 16
 
 
+class ScanOptions(ctypes.Structure):
+    """``ssm_scan_options``: the limit [dt_min, dt_max] on delta."""
+    _fields_ = [("dt_min", ctypes.c_float), ("dt_max", ctypes.c_float)]
+
+
+def _opts(dt_limit):
+    """ctypes pointer to the options for ``dt_limit = (dt_min, dt_max)``."""
+    return ctypes.byref(ScanOptions(float(dt_limit[0]), float(dt_limit[1])))
+
+
 class SSMError(RuntimeError):
     def __init__(self, fn, code, msg):
         super().__init__(f"{fn} failed: {code} ({msg})")
@@ -72,6 +82,15 @@ def load_library():
         lib.ssm_scan_bwd_finalize.restype = ci
         lib.ssm_step.argtypes = [i64] * 3 + [ci] + [vp] * 10 + [vp]
         lib.ssm_step.restype = ci
+        op = ctypes.POINTER(ScanOptions)
+        lib.ssm_scan_fwd_ex.argtypes = [i64] * 4 + [ci] + [vp] * 12 + [vp, sz, vp, op]
+        lib.ssm_scan_fwd_ex.restype = ci
+        lib.ssm_scan_bwd_ex.argtypes = [i64] * 4 + [ci] + [vp] * 21 + [vp, sz, vp, op]
+        lib.ssm_scan_bwd_ex.restype = ci
+        lib.ssm_scan_bwd_partials_ex.argtypes = [i64] * 4 + [ci] + [vp] * 15 + [vp, sz, vp, op]
+        lib.ssm_scan_bwd_partials_ex.restype = ci
+        lib.ssm_step_ex.argtypes = [i64] * 3 + [ci] + [vp] * 10 + [vp, op]
+        lib.ssm_step_ex.restype = ci
         lib.ssm_conv1d_fwd.argtypes = [i64] * 4 + [ci] + [vp] * 6 + [vp]
         lib.ssm_conv1d_fwd.restype = ci
         lib.ssm_conv1d_bwd_workspace_bytes.argtypes = [i64] * 4 + [ci]
@@ -153,9 +172,10 @@ def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]):
 
 def ssm_scan_fwd(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0=None, *, out=None,
                  h_last=None, chunk_states=None, save=True, want_h_last=True, ws=None,
-                 stream=None):
+                 stream=None, dt_limit=None):
     """Forward scan.  Returns ``(out, h_last, chunk_states)`` (chunk_states None when
-    ``save=False``).  Shapes as in include/ssm_scan.h."""
+    ``save=False``).  Shapes as in include/ssm_scan.h.  ``dt_limit = (dt_min,
+    dt_max)`` clamps delta (the ``_ex`` entry point)."""
     B, L, D = u.shape
     N = Bm.shape[-1]
     act = _act(u)
@@ -166,9 +186,16 @@ def ssm_scan_fwd(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0=None, *, out
         h_last = torch.empty((B, D, N), dtype=torch.float32, device=dev)
     lib = load_library()
     ws, ws_bytes = _workspace(fwd_workspace_bytes(B, L, D, N, act), dev, ws)
+    if save and chunk_states is None:
+        chunk_states = torch.empty((B, num_chunks(L), D, N), dtype=torch.float32, device=dev)
+    if dt_limit is not None:
+        cs = chunk_states if save else None
+        rc = lib.ssm_scan_fwd_ex(B, L, D, N, act, _p(u), _p(delta_raw), _p(z), _p(Bm), _p(Cm),
+                                 _p(A_log), _p(Dp), _p(delta_bias), _p(h0), _p(out), _p(h_last),
+                                 _p(cs), _p(ws), ws_bytes, _stream(stream), _opts(dt_limit))
+        _check("ssm_scan_fwd_ex", rc)
+        return out, h_last, cs
     if save:
-        if chunk_states is None:
-            chunk_states = torch.empty((B, num_chunks(L), D, N), dtype=torch.float32, device=dev)
         rc = lib.ssm_scan_fwd(B, L, D, N, act, _p(u), _p(delta_raw), _p(z), _p(Bm), _p(Cm),
                               _p(A_log), _p(Dp), _p(delta_bias), _p(h0), _p(out), _p(h_last),
                               _p(chunk_states), _p(ws), ws_bytes, _stream(stream))
@@ -188,7 +215,8 @@ def ssm_scan_fwd_nosave(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0=None,
 
 
 def ssm_scan_bwd(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0, chunk_states, dout,
-                 dh_last=None, *, grads=None, want_dh0=True, ws=None, stream=None, split=False):
+                 dh_last=None, *, grads=None, want_dh0=True, ws=None, stream=None, split=False,
+                 dt_limit=None):
     """Backward.  Returns a dict with du, d_delta_raw, dz (None without z), dBm, dCm,
     dA_log, dD, d_delta_bias, dh0 (None unless ``want_dh0``).  Pass ``grads`` (a dict
     of preallocated tensors with those keys) to write into existing buffers."""
@@ -210,8 +238,17 @@ def ssm_scan_bwd(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0, chunk_state
     ws, ws_bytes = _workspace(bwd_workspace_bytes(B, L, D, N, act), dev, ws)
     if split:
         bwd_partials(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, chunk_states, dout, dh_last,
-                     g, ws, stream)
+                     g, ws, stream, dt_limit=dt_limit)
         bwd_finalize(B, L, D, N, act, g, ws, stream)
+        return g
+    if dt_limit is not None:
+        rc = lib.ssm_scan_bwd_ex(B, L, D, N, act, _p(u), _p(delta_raw), _p(z), _p(Bm), _p(Cm),
+                                 _p(A_log), _p(Dp), _p(delta_bias), _p(h0), _p(chunk_states),
+                                 _p(dout), _p(dh_last), _p(g["du"]), _p(g["d_delta_raw"]),
+                                 _p(g["dz"]), _p(g["dBm"]), _p(g["dCm"]), _p(g["dA_log"]),
+                                 _p(g["dD"]), _p(g["d_delta_bias"]), _p(g["dh0"]), _p(ws), ws_bytes,
+                                 _stream(stream), _opts(dt_limit))
+        _check("ssm_scan_bwd_ex", rc)
         return g
     rc = lib.ssm_scan_bwd(B, L, D, N, act, _p(u), _p(delta_raw), _p(z), _p(Bm), _p(Cm),
                           _p(A_log), _p(Dp), _p(delta_bias), _p(h0), _p(chunk_states),
@@ -224,15 +261,18 @@ def ssm_scan_bwd(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h0, chunk_state
 
 
 def bwd_partials(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, chunk_states, dout, dh_last,
-                 g, ws, stream=None):
+                 g, ws, stream=None, dt_limit=None):
     """First half of the backward (the scan); ``g`` holds preallocated outputs."""
     B, L, D = u.shape
     N = Bm.shape[-1]
-    rc = load_library().ssm_scan_bwd_partials(
-        B, L, D, N, _act(u), _p(u), _p(delta_raw), _p(z), _p(Bm), _p(Cm), _p(A_log), _p(Dp),
-        _p(delta_bias), _p(chunk_states), _p(dout), _p(dh_last), _p(g["du"]),
-        _p(g["d_delta_raw"]), _p(g["dz"]), _p(g.get("dh0")), _p(ws),
-        0 if ws is None else ws.numel(), _stream(stream))
+    args = (B, L, D, N, _act(u), _p(u), _p(delta_raw), _p(z), _p(Bm), _p(Cm), _p(A_log), _p(Dp),
+            _p(delta_bias), _p(chunk_states), _p(dout), _p(dh_last), _p(g["du"]),
+            _p(g["d_delta_raw"]), _p(g["dz"]), _p(g.get("dh0")), _p(ws),
+            0 if ws is None else ws.numel(), _stream(stream))
+    if dt_limit is not None:
+        _check("ssm_scan_bwd_partials_ex", load_library().ssm_scan_bwd_partials_ex(*args, _opts(dt_limit)))
+        return
+    rc = load_library().ssm_scan_bwd_partials(*args)
     _check("ssm_scan_bwd_partials", rc)
 
 
@@ -244,16 +284,20 @@ def bwd_finalize(B, L, D, N, act, g, ws, stream=None):
     _check("ssm_scan_bwd_finalize", rc)
 
 
-def ssm_step(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h, *, out=None, stream=None):
+def ssm_step(u, delta_raw, z, Bm, Cm, A_log, Dp, delta_bias, h, *, out=None, stream=None,
+             dt_limit=None):
     """One decode step; ``h`` [B,D,N] f32 is updated in place.  Returns ``out`` [B,D]."""
     B, D = u.shape
     N = Bm.shape[-1]
     act = _act(u)
     if out is None:
         out = torch.empty_like(u)
-    rc = load_library().ssm_step(B, D, N, act, _p(u), _p(delta_raw), _p(z), _p(Bm), _p(Cm),
-                                 _p(A_log), _p(Dp), _p(delta_bias), _p(h), _p(out),
-                                 _stream(stream))
+    args = (B, D, N, act, _p(u), _p(delta_raw), _p(z), _p(Bm), _p(Cm), _p(A_log), _p(Dp),
+            _p(delta_bias), _p(h), _p(out), _stream(stream))
+    if dt_limit is not None:
+        _check("ssm_step_ex", load_library().ssm_step_ex(*args, _opts(dt_limit)))
+        return out
+    rc = load_library().ssm_step(*args)
     _check("ssm_step", rc)
     return out
 

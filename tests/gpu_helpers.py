@@ -40,12 +40,13 @@ def rel_err(got, ref):
     return float(diff / scale) if scale > 0 else float(diff)
 
 
-def gpu_fwd_bwd(xd, dh_last=None, want_bwd=True):
+def gpu_fwd_bwd(xd, dh_last=None, want_bwd=True, dt_limit=None):
     """Run the CUDA path on device inputs ``xd``; returns dict of torch tensors."""
-    out, h_last, cs = s6.ssm_scan_fwd(*[xd[k] for k in ARGS], xd.get("h0"))
+    out, h_last, cs = s6.ssm_scan_fwd(*[xd[k] for k in ARGS], xd.get("h0"), dt_limit=dt_limit)
     r = {"out": out, "h_last": h_last, "chunk_states": cs}
     if want_bwd:
-        g = s6.ssm_scan_bwd(*[xd[k] for k in ARGS], xd.get("h0"), cs, xd["dout"], dh_last)
+        g = s6.ssm_scan_bwd(*[xd[k] for k in ARGS], xd.get("h0"), cs, xd["dout"], dh_last,
+                            dt_limit=dt_limit)
         r.update(g)
     s6.check_device_status()  # synchronises; raises if a bounded device wait gave up
     return r

@@ -96,6 +96,28 @@ def test_step_validation(lib):
     assert b"h must not be NULL" in lib.ssm_last_error()
 
 
+def test_dt_limit_validation(lib):
+    """The _ex entry points check the limit first: 0 <= dt_min <= dt_max."""
+    def opts(lo, hi):
+        return ctypes.byref(s6.ScanOptions(lo, hi))
+
+    fwd12 = [FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, FAKE]
+    for lo, hi in ((0.5, 0.1), (-0.1, 1.0), (float("nan"), 1.0), (0.0, float("nan"))):
+        assert lib.ssm_scan_fwd_ex(1, 8, 8, 4, 0, *fwd12, None, 0, None, opts(lo, hi)) == 1
+        assert b"dt limit" in lib.ssm_last_error()
+        assert lib.ssm_scan_bwd_ex(2, 16, 8, 4, 0, *([FAKE] * 21), FAKE, 1 << 20, None, opts(lo, hi)) == 1
+        assert lib.ssm_scan_bwd_partials_ex(2, 16, 8, 4, 0, *([FAKE] * 15), FAKE, 1 << 20, None,
+                                            opts(lo, hi)) == 1
+        assert lib.ssm_step_ex(2, 8, 4, 0, *([FAKE] * 10), None, opts(lo, hi)) == 1
+        assert b"dt limit" in lib.ssm_last_error()
+    # accepted limits (equal ends, an infinite top, none at all) reach the next check
+    for o in (opts(0.25, 0.25), opts(0.0, float("inf")), None):
+        bad = list(fwd12)
+        bad[0] = None
+        assert lib.ssm_scan_fwd_ex(1, 8, 8, 4, 0, *bad, None, 0, None, o) == 1
+        assert b"u must not be NULL" in lib.ssm_last_error()
+
+
 def test_segment_plan(lib):
     """The plans are functions of the shape.  Forward: one pass where the grid
     fills the GPU, time segments of at least 512 steps for long sequences over
