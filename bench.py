@@ -629,7 +629,7 @@ def load_traffic(kernel):
         return None
     try:
         from selective_state_space_s6_gb300 import build as _b
-        src = _b.kernel_source_digest()
+        src = _b.kernel_source_digest(ent.get("sources"))
     except Exception:
         return None
     return ent.get("bytes_per_launch") if ent.get("source_digest") == src else None

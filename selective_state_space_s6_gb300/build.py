@@ -47,12 +47,15 @@ def _deps() -> list:
     return out
 
 
-def kernel_source_digest() -> str:
-    """sha256 over the CUDA sources and headers (identifies the kernels a profile was taken on)."""
+def kernel_source_digest(sources=None) -> str:
+    """sha256 over CUDA sources and every header (identifies the kernels a
+    profile was taken on): the given ``csrc/*.cu`` files (all when None)."""
     import hashlib
     h = hashlib.sha256()
     for path in sorted(_deps()):
         if path.endswith(".py"):
+            continue
+        if sources is not None and path.endswith(".cu") and os.path.basename(path) not in sources:
             continue
         with open(path, "rb") as f:
             h.update(os.path.basename(path).encode() + b"\0" + f.read())

@@ -39,6 +39,7 @@
 #include <type_traits>
 
 #include "s6_internal.cuh"
+#include "s6_math.cuh"
 #include "s6_tma.cuh"
 
 namespace s6 {
@@ -46,14 +47,11 @@ namespace s6 {
 namespace {
 
 constexpr int kTT = 32;           // steps per tile
-constexpr int kTilesPerChunk = kChunk / kTT;
 constexpr int kAggWarps = 6;  // aggregate pass: 4 consumer warps + producer + converter
 template <typename Act>
 struct BwdStages {
   static constexpr int value = std::is_same<Act, float>::value ? 2 : 3;
 };
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 // Warp-local reduction scratch of one step: two blocks (dBm terms, dCm terms),
 // each holding one 16-byte chunk (a lane's 4 states) per lane in lane order,
 // padded to 144 floats so that the 64-bit reads of a half-warp hit distinct
@@ -66,40 +64,6 @@ struct BwdTmaParams {
   CUtensorMap map_u, map_raw, map_z, map_dout, map_B, map_C;
   BwdParams p;
 };
-
-template <typename Act>
-__device__ __forceinline__ float lds_act(const Act* p);
-template <>
-__device__ __forceinline__ float lds_act<float>(const float* p) { return *p; }
-template <>
-__device__ __forceinline__ float lds_act<__nv_bfloat16>(const __nv_bfloat16* p) {
-  return __bfloat162float(*p);
-}
-
-__device__ __forceinline__ float softplus_fast(float s) {
-  const float e = ex2_approx(-fabsf(s) * kLog2e);
-  const float lg = lg2_approx(1.f + e) * kLn2;
-  const float ser = e * fmaf(e, fmaf(e, 1.f / 3.f, -0.5f), 1.f);
-  return fmaxf(s, 0.f) + (e < 0.015625f ? ser : lg);
-}
-
-// sigmoid(s) written through delta = softplus(s): sigmoid(s) = 1 - e^{-delta}
-// (the identity the oarust Slang page uses for its dt gradient), with a
-// series for small delta where 1 - e^{-delta} would cancel.
-__device__ __forceinline__ float dsoftplus_fast(float delta) {
-  const float em = ex2_approx(-delta * kLog2e);
-  const float ser = delta * fmaf(delta, fmaf(delta, 1.f / 6.f, -0.5f), 1.f);
-  return delta < 0.03125f ? ser : 1.f - em;
-}
-
-__device__ __forceinline__ float sigmoid_fast(float z) { return rcp_approx(1.f + ex2_approx(-z * kLog2e)); }
-
-template <bool kFast>
-__device__ __forceinline__ float2 decay2(float2 dd, float2 A) {
-  const float2 x = fmul2(dd, A);
-  if (kFast) return make_float2(ex2_approx(x.x), ex2_approx(x.y));
-  return make_float2(expf(x.x), expf(x.y));
-}
 
 __device__ __forceinline__ void kahan_add(float& sum, float& comp, float x) {
   const float y = __fsub_rn(x, comp);

@@ -21,6 +21,7 @@
 #include <type_traits>
 
 #include "s6_internal.cuh"
+#include "s6_math.cuh"
 #include "s6_tma.cuh"
 
 namespace s6 {
@@ -89,7 +90,7 @@ struct Vec<__nv_bfloat16, 4> {
 template <typename Act>
 __device__ __forceinline__ float sig(float v) {
   if constexpr (std::is_same<Act, __nv_bfloat16>::value)
-    return rcp_approx(1.f + ex2_approx(-v * 1.4426950408889634f));
+    return sigmoid_fast(v);
   else
     return sigmoid_f(v);
 }
@@ -465,7 +466,7 @@ __global__ void __launch_bounds__(kTileWarps * 32) s6_conv1d_bwd_tile_kernel(con
 #pragma unroll
     for (int k = 1; k < K; ++k) xin(ts + kTileSeg - 1 - (K - 1) + k, xw[k]);
     Act* __restrict__ dx = static_cast<Act*>(p.dx);
-#pragma unroll 4
+#pragma unroll
     for (int i = kTileSeg - 1; i >= 0; --i) {
       const int t = ts + i;
       xin(t - (K - 1), xw[0]);

@@ -32,6 +32,7 @@
 #include <type_traits>
 
 #include "s6_internal.cuh"
+#include "s6_math.cuh"
 #include "s6_tma.cuh"
 
 namespace s6 {
@@ -40,8 +41,6 @@ namespace {
 
 constexpr int kTT = 32;          // steps per pipeline stage
 constexpr int kFwdWarps = 6;     // 4 consumers + producer + converter
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 
 template <typename Act>
 struct FwdCfg {
@@ -61,47 +60,6 @@ struct FwdTmaParams {
   CUtensorMap map_u, map_raw, map_z, map_B, map_C;  // 64-byte aligned members first
   FwdParams p;
 };
-
-template <typename Act>
-__device__ __forceinline__ float lds_act(const Act* p);
-template <>
-__device__ __forceinline__ float lds_act<float>(const float* p) { return *p; }
-template <>
-__device__ __forceinline__ float lds_act<__nv_bfloat16>(const __nv_bfloat16* p) {
-  return __bfloat162float(*p);
-}
-
-// softplus(s) = max(s, 0) + log1p(e^-|s|), evaluated on the special-function
-// unit; the series e - e^2/2 + e^3/3 covers e < 2^-6, where log2(1 + e) loses
-// relative precision.
-__device__ __forceinline__ float softplus_fast(float s) {
-  const float e = ex2_approx(-fabsf(s) * kLog2e);
-  const float lg = lg2_approx(1.f + e) * kLn2;
-  const float ser = e * fmaf(e, fmaf(e, 1.f / 3.f, -0.5f), 1.f);
-  return fmaxf(s, 0.f) + (e < 0.015625f ? ser : lg);
-}
-
-__device__ __forceinline__ float silu_fast(float z) {
-  return z * rcp_approx(1.f + ex2_approx(-z * kLog2e));
-}
-
-template <bool kFast>
-__device__ __forceinline__ float softplus_k(float s) {
-  return kFast ? softplus_fast(s) : softplus_f(s);
-}
-template <bool kFast>
-__device__ __forceinline__ float silu_k(float z) {
-  return kFast ? silu_fast(z) : z * sigmoid_f(z);
-}
-
-// Abar for a pair of states: fast path 2^(delta * A*log2e) on the SFU,
-// accurate path expf(delta * A).
-template <bool kFast>
-__device__ __forceinline__ float2 decay2(float2 dd, float2 A) {
-  const float2 x = fmul2(dd, A);
-  if (kFast) return make_float2(ex2_approx(x.x), ex2_approx(x.y));
-  return make_float2(expf(x.x), expf(x.y));
-}
 
 // TPC lanes per channel, 4 states per lane (N = 4 * TPC); 128 consumer lanes
 // cover kCh = 128 / TPC channels.  grid.z = time segment.  kAgg: the
@@ -457,108 +415,6 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
   }  // items
 }
 
-// One decode step (T = 1).  A thread owns 4 states of one channel for TPC
-// batch rows (TPC = N/4 lanes per channel): the channel's TPC lanes together
-// cover TPC x N states.  Work that depends only on (b, d) -- softplus of
-// delta, silu of the gate -- is done once per (b, d), by lane j for batch row
-// j of the group, and passed round with shuffles; A = -exp(A_log) is taken
-// once per thread for all its rows.  The arithmetic is the scan kernel's, in
-// the same order (softplus, decays, state update, per-lane readout, the
-// channel's lanes added in lane order, skip, gate), so that L steps equal one
-// L-step scan bit for bit.  Bound by HBM: every state is read and written
-// once (16 bytes per lane and row each way).
-template <typename Act, int TPC, bool kFast, bool kGate>
-__global__ void __launch_bounds__(256) s6_step_kernel(const FwdParams p) {
-  constexpr int N = 4 * TPC;
-  const int B = p.B, D = p.D;
-  const int ngroups = (B + TPC - 1) / TPC;  // groups of TPC batch rows
-  const long long total = (long long)ngroups * D * TPC;
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const bool active = idx < total;
-  const long long i = active ? idx : total - 1;  // idle lanes still take part in the shuffles
-  const int q = (int)(i % TPC);
-  const long long gd = i / TPC;  // group * D + d
-  const int d = (int)(gd % D);
-  const int g = (int)(gd / D);
-  const int lane = threadIdx.x & 31;
-  const int lead = lane - q;  // lane 0 of this channel's group
-
-  const float4 al = __ldg(reinterpret_cast<const float4*>(p.A_log + (size_t)d * N + 4 * q));
-  float2 A2[2];
-  {
-    const float a0 = -expf(al.x), a1 = -expf(al.y), a2 = -expf(al.z), a3 = -expf(al.w);
-    A2[0] = kFast ? make_float2(a0 * kLog2e, a1 * kLog2e) : make_float2(a0, a1);
-    A2[1] = kFast ? make_float2(a2 * kLog2e, a3 * kLog2e) : make_float2(a2, a3);
-  }
-  const float bias = p.delta_bias[d];
-  const float Dd = p.Dp[d];
-  const Act* u_p = static_cast<const Act*>(p.u);
-
-  // this lane's batch row of the group: delta and the gate factor
-  const int bq = min(g * TPC + q, B - 1);
-  const float sp_q = clamp_dt(softplus_k<kFast>(ld_act(static_cast<const Act*>(p.delta_raw) + (size_t)bq * D + d) + bias),
-                                p.dt_min, p.dt_max);
-  const float sl_q = kGate ? silu_k<kFast>(ld_act(static_cast<const Act*>(p.z) + (size_t)bq * D + d)) : 1.f;
-
-  // every row's loads first (independent of one another; the state is
-  // written in place, so the loads must not wait behind earlier stores)
-  float uj[TPC], hj[TPC][4], bj4[TPC][4], cj4[TPC][4];
-#pragma unroll
-  for (int j = 0; j < TPC; ++j) {
-    const long long b = min(g * TPC + j, B - 1);
-    const long long bd = b * D + d;
-    uj[j] = ld_act(u_p + bd);
-    const float4 hv = *reinterpret_cast<const float4*>(p.h0 + bd * N + 4 * q);
-    hj[j][0] = hv.x, hj[j][1] = hv.y, hj[j][2] = hv.z, hj[j][3] = hv.w;
-    if constexpr (std::is_same<Act, float>::value) {
-      const float4 bb = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.Bm) + b * N + 4 * q));
-      const float4 cc = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.Cm) + b * N + 4 * q));
-      bj4[j][0] = bb.x, bj4[j][1] = bb.y, bj4[j][2] = bb.z, bj4[j][3] = bb.w;
-      cj4[j][0] = cc.x, cj4[j][1] = cc.y, cj4[j][2] = cc.z, cj4[j][3] = cc.w;
-    } else {
-      const __nv_bfloat162* bb = reinterpret_cast<const __nv_bfloat162*>(static_cast<const Act*>(p.Bm) + b * N + 4 * q);
-      const __nv_bfloat162* cc = reinterpret_cast<const __nv_bfloat162*>(static_cast<const Act*>(p.Cm) + b * N + 4 * q);
-      const float2 b0 = __bfloat1622float2(bb[0]), b1 = __bfloat1622float2(bb[1]);
-      const float2 c0 = __bfloat1622float2(cc[0]), c1 = __bfloat1622float2(cc[1]);
-      bj4[j][0] = b0.x, bj4[j][1] = b0.y, bj4[j][2] = b1.x, bj4[j][3] = b1.y;
-      cj4[j][0] = c0.x, cj4[j][1] = c0.y, cj4[j][2] = c1.x, cj4[j][3] = c1.y;
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < TPC; ++j) {
-    const int bj = g * TPC + j;
-    const bool row_ok = active && bj < B;
-    const long long b = row_ok ? bj : B - 1;
-    const long long bd = b * D + d;
-    const float sp = __shfl_sync(0xffffffffu, sp_q, lead + j);
-    const float sl = __shfl_sync(0xffffffffu, sl_q, lead + j);
-    const float u = uj[j];
-    float2 Bv[2] = {make_float2(bj4[j][0], bj4[j][1]), make_float2(bj4[j][2], bj4[j][3])};
-    float2 Cv[2] = {make_float2(cj4[j][0], cj4[j][1]), make_float2(cj4[j][2], cj4[j][3])};
-    float2 h[2] = {make_float2(hj[j][0], hj[j][1]), make_float2(hj[j][2], hj[j][3])};
-    const float du = sp * u;
-    const float2 dd = make_float2(sp, sp), uu = make_float2(du, du);
-    const float2 a0 = decay2<kFast>(dd, A2[0]);
-    const float2 a1 = decay2<kFast>(dd, A2[1]);
-    h[0] = ffma2(a0, h[0], fmul2(uu, Bv[0]));
-    h[1] = ffma2(a1, h[1], fmul2(uu, Bv[1]));
-    const float2 y2 = ffma2(Cv[1], h[1], fmul2(Cv[0], h[0]));
-    const float part = y2.x + y2.y;
-    // the channel's partial readouts, added in lane order
-    float y = __shfl_sync(0xffffffffu, part, lead);
-#pragma unroll
-    for (int r = 1; r < TPC; ++r) y += __shfl_sync(0xffffffffu, part, lead + r);
-    if (row_ok) {
-      *reinterpret_cast<float4*>(p.h_last + bd * N + 4 * q) = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
-      if (q == j) {
-        float o = fmaf(Dd, u, y);
-        if (kGate) o *= sl;
-        st_act(static_cast<Act*>(p.out) + bd, o);
-      }
-    }
-  }
-}
-
 // Carry pass of the chunked parallel scan: per (b, d, n), in segment order,
 // seg_start[s] = state before segment s, seg_start[s+1] = P_s * seg_start[s] + hloc_s.
 __global__ void s6_fwd_seg_carry_kernel(const FwdParams p) {
@@ -669,45 +525,8 @@ cudaError_t launch_tpc(const FwdTmaParams& P, cudaStream_t stream) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-template <typename Act, int TPC, bool kFast>
-cudaError_t launch_step_tpc(const FwdParams& p, cudaStream_t stream) {
-  const long long threads = (long long)((p.B + TPC - 1) / TPC) * p.D * TPC;
-  const unsigned blocks = (unsigned)((threads + 255) / 256);
-  if (p.z)
-    s6_step_kernel<Act, TPC, kFast, true><<<blocks, 256, 0, stream>>>(p);
-  else
-    s6_step_kernel<Act, TPC, kFast, false><<<blocks, 256, 0, stream>>>(p);
-  return cudaGetLastError();
-}
-
 }  // namespace
 
-// The step kernel takes N in {4, 8, 16} with 16-byte aligned h and A_log and
-// Bm/Cm rows aligned to their 4-element loads (the same N as the TMA scan,
-// whose arithmetic it repeats); other shapes take one step of the generic scan.
-bool step_supported(const FwdParams& p, int act) {
-  if (!(p.N == 4 || p.N == 8 || p.N == 16)) return false;
-  if (act == SSM_BF16 && p.N == 4) return false;  // the TMA scan's rule for bf16
-  const uintptr_t bc_align = act == SSM_BF16 ? 7 : 15;
-  if ((reinterpret_cast<uintptr_t>(p.Bm) & bc_align) || (reinterpret_cast<uintptr_t>(p.Cm) & bc_align)) return false;
-  if (!aligned16(p.A_log) || !aligned16(p.h0) || !aligned16(p.h_last)) return false;
-  if ((long long)p.B * p.D * (p.N / 4) >= (1LL << 40)) return false;
-  // bit-identity with the scan needs the scan of the same shape to take the TMA path
-  return fwd_tma_supported(p, act);
-}
-
-cudaError_t launch_step(const FwdParams& p, int act, cudaStream_t stream) {
-  const int tpc = p.N / 4;
-  if (act == SSM_BF16) {
-    if (tpc == 4) return launch_step_tpc<__nv_bfloat16, 4, true>(p, stream);
-    if (tpc == 2) return launch_step_tpc<__nv_bfloat16, 2, true>(p, stream);
-    return cudaErrorInvalidValue;
-  }
-  if (tpc == 4) return launch_step_tpc<float, 4, false>(p, stream);
-  if (tpc == 2) return launch_step_tpc<float, 2, false>(p, stream);
-  if (tpc == 1) return launch_step_tpc<float, 1, false>(p, stream);
-  return cudaErrorInvalidValue;
-}
 
 // Stream plan: 3 * sms equal ranges of chunk units over the (batch,
 // 128/TPC-channel tile) sequences.  Taken when some sequence is cut, none
