@@ -287,3 +287,72 @@ def conv1d_step(x_t, w, bias, state):
     if rc != 0:
         raise ValueError(f"c1o_step failed with code {rc}")
     return out, st
+
+
+# ------------------------------------------------------------------ Mamba-2 SSD
+# The scalar-A-per-head variant of the scan (``ssd_oracle.c``, plain
+# sequential C, f64), built into its own library.
+
+_SSD_SRC = os.path.join(_HERE, "ssd_oracle.c")
+_SSD_LIB_PATH = os.path.join(_BUILD_DIR, "libssd_oracle.so")
+_ssd_lib = None
+
+
+def build_ssd(force: bool = False, src: str = None, out: str = None) -> str:
+    """Compile ``ssd_oracle.c`` (or ``src``) into a shared library (gcc, -O2)."""
+    src = src or _SSD_SRC
+    out = out or _SSD_LIB_PATH
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+                    "-Wall", "-o", tmp, src, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _open_ssd(path):
+    lib = ctypes.CDLL(path)
+    i64, vp, ci, f64 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+    lib.ssdo_fwd.argtypes = [i64] * 6 + [vp] * 8 + [f64, f64] + [vp] * 2
+    lib.ssdo_fwd.restype = ci
+    return lib
+
+
+def _load_ssd():
+    global _ssd_lib
+    with _lock:
+        if _ssd_lib is None:
+            _ssd_lib = _open_ssd(build_ssd())
+    return _ssd_lib
+
+
+@contextlib.contextmanager
+def override_ssd_library(path):
+    """Run the SSD wrapper against another build (planted-mistake tests)."""
+    global _ssd_lib
+    prev = _load_ssd()
+    with _lock:
+        _ssd_lib = _open_ssd(path)
+    try:
+        yield
+    finally:
+        with _lock:
+            _ssd_lib = prev
+
+
+def ssd_fwd(x, dt_raw, dt_bias, A_log, Bm, Cm, Dp, h0=None, *, dt_limit=None):
+    """Mamba-2 SSD forward, step by step.  x [B,L,H,P], dt_raw [B,L,H], dt_bias /
+    A_log / Dp [H], Bm / Cm [B,L,G,N], h0 [B,H,N,P] (zeros when None).  Returns
+    ``(y [B,L,H,P], h_last [B,H,N,P])`` as f64 arrays."""
+    x, dt_raw, dt_bias, A_log, Bm, Cm, Dp, h0 = map(_f64, (x, dt_raw, dt_bias, A_log, Bm, Cm, Dp, h0))
+    B, L, H, P = x.shape
+    G, N = Bm.shape[2], Bm.shape[3]
+    y = np.full((B, L, H, P), np.nan)
+    h_last = np.full((B, H, N, P), np.nan)
+    rc = _load_ssd().ssdo_fwd(B, L, H, P, G, N, _ptr(x), _ptr(dt_raw), _ptr(dt_bias), _ptr(A_log), _ptr(Bm),
+                              _ptr(Cm), _ptr(Dp), _ptr(h0), *_limits(dt_limit), _ptr(y), _ptr(h_last))
+    if rc != 0:
+        raise ValueError(f"ssdo_fwd failed with code {rc}")
+    return y, h_last
