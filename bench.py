@@ -661,6 +661,45 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_kernel(args):
+    """One kernel family alone, a few calls on its own workload, for a
+    profiler's capture (`--kernel`): the decode step (four calls, each after
+    a 256 MB read that empties L2) or conv1d + SiLU on the 1.4B block's shape
+    (three forward and three backward calls).  Prints one JSON line."""
+    from selective_state_space_s6_gb300 import s6
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    res = {"kernel": args.kernel}
+    if args.kernel == "step":
+        w = inputs.WORKLOADS["decode"]
+        x = inputs.make_inputs(w.batch, 1, w.dim, w.dstate, w.act, seed=0, h0_std=w.h0_std)
+        xd = {k: (v.to(dev) if v is not None else None) for k, v in x.items()}
+        a = [xd[k][:, 0].contiguous() if k in ("u", "delta_raw", "z", "Bm", "Cm") else xd[k] for k in ARGS]
+        h = xd["h0"].clone()
+        scratch = torch.ones((256 << 20) // 4, dtype=torch.float32, device=dev)
+        sink = torch.empty((), dtype=torch.float32, device=dev)
+        for _ in range(4):
+            torch.sum(scratch, dim=0, out=sink)
+            s6.ssm_step(*a, h)
+        res["workload"] = w.description
+    elif args.kernel == "conv1d":
+        B, L, D, K = 4, 4096, 4096, 4
+        g = torch.Generator(device=dev).manual_seed(0)
+        x = torch.randn(B, L, D, device=dev, generator=g).to(torch.bfloat16)
+        dout = torch.randn(B, L, D, device=dev, generator=g).to(torch.bfloat16)
+        wt = torch.randn(D, K, device=dev, generator=g) * 0.5
+        bias = torch.randn(D, device=dev, generator=g) * 0.2
+        for _ in range(3):
+            s6.conv1d_fwd(x, wt, bias, None, want_state=False)
+            s6.conv1d_bwd(x, wt, bias, None, dout, want_dstate0=False)
+        res["workload"] = f"B={B} L={L} D={D} K={K} bf16"
+        res["path"] = s6.conv1d_path(x, wt)
+    torch.cuda.synchronize(dev)
+    s6.check_device_status()
+    print(json.dumps(res), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -671,7 +710,12 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-step", action="store_true", help="skip the decode-step and conv1d measurements")
+    ap.add_argument("--kernel", choices=["step", "conv1d"],
+                    help="run only this kernel family a few times (for a profiler) and exit")
     args = ap.parse_args(argv)
+    if args.kernel:
+        run_kernel(args)
+        return
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     world, rank, local = dist_setup()
     try:

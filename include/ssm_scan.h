@@ -286,6 +286,27 @@ int ssm_step_ex(int64_t batch, int64_t dim, int64_t dstate, int act, const void 
                 void *stream, const ssm_scan_options *opts);
 
 /* ---------------------------------------------------------------------------
+ * Mamba-2 SSD forward: the scan with one scalar decay per head (the
+ * deterministic_backward.py page's ssd_combined kernels: dt per (batch, step,
+ * head), one A and one dt_bias per head, softplus and dt_limit).  For each
+ * (b, h), t = 0 .. L-1, with g = h / (H / G) the head's group:
+ *   delta = min(max(softplus(dt_raw[b,t,h] + dt_bias[h]), dt_min), dt_max)
+ *   S[n][p] = exp(-exp(A_log[h]) * delta) * S[n][p] + delta * Bm[b,t,g,n] * x[b,t,h,p]
+ *   y[b,t,h,p] = sum_n Cm[b,t,g,n] * S[n][p] + Dp[h] * x[b,t,h,p]
+ * evaluated in its chunked matrix form (64-step chunks, tensor cores).
+ *   x, y [B][L][H][P]; dt_raw [B][L][H]; Bm, Cm [B][L][G][N] (act dtype);
+ *   dt_bias, A_log, Dp [H] f32; h0 (nullable: zeros), h_last (nullable)
+ *   [B][H][N][P] f32.  opts: the limit on delta (NULL: none).
+ * Supported: act = SSM_BF16, P = headdim = 64, N = dstate in {64, 128},
+ * H % G == 0; x, dt_raw, Bm, Cm, y 16-byte aligned.  Other shapes return
+ * SSM_ERR_UNSUPPORTED.  Asynchronous on `stream`; allocates nothing.
+ */
+int ssm_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups,
+                int64_t dstate, int act, const void *x, const void *dt_raw, const float *dt_bias,
+                const float *A_log, const void *Bm, const void *Cm, const float *Dp, const float *h0,
+                void *y, float *h_last, const ssm_scan_options *opts, void *stream);
+
+/* ---------------------------------------------------------------------------
  * Causal depthwise conv1d + SiLU, the convolution in front of the scan in a
  * Mamba block (kernels.rs page: "Multi-step conv1d forward with state saves
  * for backward", "Multi-step conv1d backward", "Single-step depthwise conv1d

@@ -621,6 +621,55 @@ int ssm_conv1d_path(int64_t batch, int64_t seqlen, int64_t dim, int64_t width, i
   return s6::conv1d_path(p, act, dout != nullptr);
 }
 
+int ssm_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups,
+                int64_t dstate, int act, const void* x, const void* dt_raw, const float* dt_bias,
+                const float* A_log, const void* Bm, const void* Cm, const float* Dp, const float* h0,
+                void* y, float* h_last, const ssm_scan_options* opts, void* stream) {
+  const int64_t B = batch, L = seqlen, H = nheads, P = headdim, G = ngroups, N = dstate;
+  float dt_lo, dt_hi;
+  S6_TRY(read_opts(opts, &dt_lo, &dt_hi));
+  if (act != SSM_F32 && act != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "act must be SSM_F32 or SSM_BF16, got %d", act);
+  if (B < 0 || L < 0 || H < 1 || P < 1 || G < 1 || N < 1)
+    return fail(SSM_ERR_INVALID_ARG, "bad SSD shape (B=%lld L=%lld H=%lld P=%lld G=%lld N=%lld)", (long long)B,
+                (long long)L, (long long)H, (long long)P, (long long)G, (long long)N);
+  if (H % G != 0) return fail(SSM_ERR_INVALID_ARG, "nheads %lld is not a multiple of ngroups %lld", (long long)H, (long long)G);
+  if (!s6::ssd_supported(act, (int)P, (int)N))
+    return fail(SSM_ERR_UNSUPPORTED, "SSD forward supports bf16 activations, headdim 64 and dstate 64 or 128");
+  if (B * L * H * P >= kMaxElems || B * L * G * N >= kMaxElems || B * H >= kMaxElems || L >= kMaxElems)
+    return fail(SSM_ERR_UNSUPPORTED, "problem too large for 31-bit indexing");
+  S6_TRY(need(x, B * L * H * P, 16, "x"));
+  S6_TRY(need(dt_raw, B * L * H, 2, "dt_raw"));
+  S6_TRY(need(dt_bias, H, 4, "dt_bias"));
+  S6_TRY(need(A_log, H, 4, "A_log"));
+  S6_TRY(need(Bm, B * L * G * N, 16, "Bm"));
+  S6_TRY(need(Cm, B * L * G * N, 16, "Cm"));
+  S6_TRY(need(Dp, H, 4, "Dp"));
+  S6_TRY(opt(h0, 4, "h0"));
+  S6_TRY(need(y, B * L * H * P, 16, "y"));
+  S6_TRY(opt(h_last, 8, "h_last"));
+  g_last_error[0] = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (B == 0) return SSM_OK;
+  if (L == 0) {
+    if (h_last) {
+      const size_t bytes = sizeof(float) * (size_t)(B * H * N * P);
+      const cudaError_t ce = h0 ? cudaMemcpyAsync(h_last, h0, bytes, cudaMemcpyDeviceToDevice, st)
+                                : cudaMemsetAsync(h_last, 0, bytes, st);
+      if (ce != cudaSuccess) return cuda_fail(ce, "ssm_ssd_fwd(L=0)");
+    }
+    return SSM_OK;
+  }
+  s6::SsdArgs a = {};
+  a.x = x; a.dt_raw = dt_raw; a.Bm = Bm; a.Cm = Cm; a.dt_bias = dt_bias; a.A_log = A_log; a.Dp = Dp;
+  a.h0 = h0; a.y = y; a.h_last = h_last;
+  a.status = s6::device_status_word();
+  if (!a.status) return fail(SSM_ERR_CUDA, "cannot locate the device status word");
+  a.dt_min = dt_lo; a.dt_max = dt_hi;
+  a.B = (int)B; a.L = (int)L; a.H = (int)H; a.G = (int)G; a.N = (int)N;
+  const cudaError_t ce = s6::launch_ssd_fwd(a, st);
+  return ce == cudaSuccess ? SSM_OK : cuda_fail(ce, "ssm_ssd_fwd launch");
+}
+
 int ssm_conv1d_step(int64_t batch, int64_t dim, int64_t width, int act, const void* x, const float* w,
                     const float* bias, void* state, void* out, void* stream) {
   const int64_t B = batch, D = dim, K = width;

@@ -177,6 +177,25 @@ size_t conv1d_bwd_workspace_bytes(int B, int L, int D, int K);
 cudaError_t launch_conv1d(const ConvParams& p, int act, bool bwd, cudaStream_t stream);
 // SSM_CONV_PATH_* that launch_conv1d would take for these parameters
 int conv1d_path(const ConvParams& p, int act, bool bwd);
+
+// Mamba-2 SSD forward (s6_ssd.cu)
+struct SsdArgs {
+  const void* x;       // [B][L][H][P] act
+  const void* dt_raw;  // [B][L][H] act
+  const void* Bm;      // [B][L][G][N] act
+  const void* Cm;
+  const float* dt_bias;  // [H]
+  const float* A_log;    // [H]
+  const float* Dp;       // [H]
+  const float* h0;       // [B][H][N][P] or null
+  void* y;               // [B][L][H][P] act
+  float* h_last;         // [B][H][N][P] or null
+  unsigned int* status;
+  float dt_min, dt_max;
+  int B, L, H, G, N;
+};
+bool ssd_supported(int act, int P, int N);
+cudaError_t launch_ssd_fwd(const SsdArgs& a, cudaStream_t stream);
 cudaError_t launch_conv1d_step(const ConvParams& p, int act, cudaStream_t stream);
 // The TMA backward's work plan for this shape with `sms` worker CTAs.
 BwdPlan bwd_plan(int B, int L, int D, int N, int sms);

@@ -1,0 +1,430 @@
+// Mamba-2 SSD forward (scalar A per head; deterministic_backward.py page: the
+// ssd_combined kernels -- chunk_cumsum, bmm, chunk_state, state_passing,
+// chunk_scan -- with dt per (batch, step, head), one A and one dt_bias per
+// head, dt_softplus and dt_limit):
+//   delta_t = min(max(softplus(dt_raw_t + dt_bias_h), dt_min), dt_max)
+//   S_t = exp(delta_t A_h) S_{t-1} + delta_t B_t x_t^T     (S: N x P per head)
+//   y_t = C_t S_t + D_h x_t
+// evaluated in its chunked matrix form: per chunk of Q = 64 steps, with
+// cum_t the running sum of delta*A inside the chunk,
+//   y = ((C B^T) o L) (delta x) + diag(e^cum) C S_in + D x,
+//   L[t][s] = e^(cum_t - cum_s) for s <= t, else 0
+//   S_out = e^(cum_end) S_in + B^T (w o delta x),  w_s = e^(cum_end - cum_s)
+//
+// A CTA owns one (batch, head) sequence and walks its chunks in order,
+// carrying S (N x 64, f32) in the accumulator registers of its four warps;
+// the chunk's x, Bm and Cm tiles arrive by TMA (128-byte swizzled boxes of
+// 64 steps x 64 columns) into a two-deep ring.  The four products run on
+// the tensor cores with mma.sync (bf16 operands, f32 accumulation): C B^T
+// and C S_in share their A operand; the masked, scaled C B^T goes from the
+// accumulators straight into the A operand of the next product; the causal
+// structure skips the blocks above the diagonal.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+
+#include "s6_internal.cuh"
+#include "s6_math.cuh"
+#include "s6_tma.cuh"
+
+namespace s6 {
+
+namespace {
+
+constexpr int kQ = 64;           // steps per chunk
+constexpr int kP = 64;           // head dimension
+constexpr int kSsdThreads = 128;  // 4 warps: warp w owns rows 16w..16w+15 of a chunk, 32w..32w+31 of S
+constexpr int kTileBytes = 64 * 128;  // one 64 x 64 bf16 box (128-byte rows)
+
+struct SsdParams {
+  CUtensorMap map_x, map_B, map_C;  // 64-byte aligned members first
+  const __nv_bfloat16* dt_raw;      // [B][L][H]
+  const float* dt_bias;             // [H]
+  const float* A_log;               // [H]
+  const float* Dp;                  // [H]
+  const float* h0;                  // [B][H][N][P] or null
+  __nv_bfloat16* y;                 // [B][L][H][P]
+  float* h_last;                    // [B][H][N][P] or null
+  unsigned int* status;
+  float dt_min, dt_max;
+  int B, L, H, G, N;
+};
+
+// byte offset of the 16-byte chunk `c8` (elements 8 c8 .. 8 c8 + 7) of row r
+// in a 128-byte swizzled box of 128-byte rows (the TMA's 128B swizzle: the
+// chunk index is XORed with the row's position in its 8-row group)
+__device__ __forceinline__ uint32_t swz(int r, int c8) { return (uint32_t)(r * 128 + ((c8 ^ (r & 7)) << 4)); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// d += a (16 x 16, row) * b (16 x 8, col), bf16 operands, f32 accumulators
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ float2 unpack_bf16(uint32_t v) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+}
+__device__ __forceinline__ float fast_exp(float x) { return ex2_approx(x * kLog2e); }
+
+template <int N>
+struct SsdSmem {
+  static constexpr int NT = N / 64;                    // 64-column boxes of Bm / Cm
+  static constexpr int kX = 0;                         // x box [64 s][64 p]
+  static constexpr int kBo = kTileBytes;               // Bm boxes [NT][64 s][64 n]
+  static constexpr int kCo = kBo + NT * kTileBytes;    // Cm boxes
+  static constexpr int kBuf = kCo + NT * kTileBytes;   // one stage
+  static constexpr int kStage = 2 * kBuf;              // x' / y staging box [64][64]
+  static constexpr int kS = kStage + kTileBytes;       // S_in (bf16) [N n][64 p]
+  static constexpr int kVec = kS + N * 128;            // cum, delta, w*delta [3][64] f32 + decay
+  static constexpr int kBar = kVec + 4 * 64 * 4;       // two mbarriers
+  static constexpr int kBytes = kBar + 64;
+  static constexpr uint32_t kTx = (1 + 2 * NT) * kTileBytes;
+  static_assert(kBuf % 1024 == 0 && kStage % 1024 == 0 && kS % 1024 == 0, "swizzled boxes on 1024-byte boundaries");
+};
+
+template <int N>
+__global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_constant__ SsdParams P) {
+  using SM = SsdSmem<N>;
+  constexpr int NT = SM::NT;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // the 128B swizzle repeats every 1024 bytes: align the base
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char* smem = smem_raw + (base - raw);
+  float* cum = reinterpret_cast<float*>(smem + SM::kVec);
+  float* dlt = cum + 64;
+  float* wd = cum + 128;
+  float* misc = cum + 192;  // [0] = e^(cum_end)
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBar);
+
+  const int b = blockIdx.x / P.H, h = blockIdx.x % P.H;
+  const int g = h / (P.H / P.G);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, cq = lane & 3;  // fragment row group, column pair
+  const int nch = (P.L + kQ - 1) / kQ;
+  const float A = -expf(P.A_log[h]);
+  const float bias = P.dt_bias[h];
+  const float Dh = P.Dp[h];
+
+  if (tid == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto issue = [&](int c) {  // chunk c's boxes into stage c & 1 (one thread)
+    const int s = c & 1;
+    unsigned char* st = smem + s * SM::kBuf;
+    mbar_arrive_expect_tx(&full[s], SM::kTx);
+    tma_load_3d(st + SM::kX, &P.map_x, &full[s], h * kP, c * kQ, b);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      tma_load_3d(st + SM::kBo + j * kTileBytes, &P.map_B, &full[s], g * N + 64 * j, c * kQ, b);
+      tma_load_3d(st + SM::kCo + j * kTileBytes, &P.map_C, &full[s], g * N + 64 * j, c * kQ, b);
+    }
+  };
+  if (tid == 0) {
+    tma_prefetch_desc(&P.map_x);
+    if (nch > 0) issue(0);
+    if (nch > 1) issue(1);
+  }
+
+  // the state: warp w holds rows n = 32w + 16 mt + {gq, gq + 8}, columns p = 8 j + 2 cq + {0, 1}
+  constexpr int kMT = N / 64;  // 16-row tiles of S per warp (N / 4 rows per warp)
+  float S[kMT][8][4];
+  {
+    const float* h0 = P.h0 ? P.h0 + ((size_t)b * P.H + h) * N * kP : nullptr;
+#pragma unroll
+    for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int n = warp * (N / 4) + 16 * mt + gq + 8 * (e >> 1), p = 8 * j + 2 * cq + (e & 1);
+          S[mt][j][e] = h0 ? h0[(size_t)n * kP + p] : 0.f;
+        }
+  }
+  auto store_S_bf16 = [&]() {  // S_in for the next chunk's readout, [n][p] swizzled
+#pragma unroll
+    for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int hlf = 0; hlf < 2; ++hlf) {
+          const int n = warp * (N / 4) + 16 * mt + gq + 8 * hlf;
+          *reinterpret_cast<uint32_t*>(smem + SM::kS + swz(n, j) + 4 * cq) =
+              pack_bf16(S[mt][j][2 * hlf], S[mt][j][2 * hlf + 1]);
+        }
+  };
+  store_S_bf16();
+
+  for (int c = 0; c < nch; ++c) {
+    const int s = c & 1;
+    const int t0 = c * kQ;
+    const bool ok = mbar_wait(&full[s], (c >> 1) & 1, P.status);
+    if (__syncthreads_or(!ok)) break;  // the copy never came: stop, uniformly
+    const unsigned char* st = smem + s * SM::kBuf;
+    const uint32_t xs = base + s * SM::kBuf + SM::kX;
+    const uint32_t bs = base + s * SM::kBuf + SM::kBo;
+    const uint32_t cs = base + s * SM::kBuf + SM::kCo;
+    const uint32_t ss = base + SM::kS;
+    const uint32_t stg = base + SM::kStage;
+
+    // ---- delta, the running sum of delta*A (two steps per lane), weights
+    if (warp == 0) {
+      float d2[2], a2[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int t = t0 + 2 * lane + i;
+        float d = 0.f;
+        if (t < P.L) {
+          const float raw = __bfloat162float(P.dt_raw[((size_t)b * P.L + t) * P.H + h]);
+          d = clamp_dt(softplus_fast(raw + bias), P.dt_min, P.dt_max);
+        }
+        d2[i] = d;
+        a2[i] = d * A;
+      }
+      float run = a2[0] + a2[1];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float v = __shfl_up_sync(0xffffffffu, run, o);
+        if (lane >= o) run += v;
+      }
+      const float end = __shfl_sync(0xffffffffu, run, 31);
+      const float c1 = run, c0 = run - a2[1];
+      cum[2 * lane] = c0;
+      cum[2 * lane + 1] = c1;
+      dlt[2 * lane] = d2[0];
+      dlt[2 * lane + 1] = d2[1];
+      wd[2 * lane] = fast_exp(end - c0) * d2[0];
+      wd[2 * lane + 1] = fast_exp(end - c1) * d2[1];
+      if (lane == 0) misc[0] = fast_exp(end);
+    }
+    __syncthreads();
+
+    // ---- y rows 16w .. 16w+15: (C B^T o L)(delta x) + e^cum (C S_in) + D x
+    const int r0 = 16 * warp;
+    float G[8][4], CS[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) G[j][e] = CS[j][e] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < N / 16; ++kk) {
+      const int k0 = 16 * kk;
+      const int sub = k0 / 64, kc = (k0 % 64) / 8;
+      uint32_t a[4];
+      ldsm_x4(cs + sub * kTileBytes + swz(r0 + (lane & 7) + 8 * ((lane >> 3) & 1), kc + (lane >> 4)), a);
+      // C B^T: only the s blocks at or below this warp's rows
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        if (jj > warp) break;
+        uint32_t bb[4];
+        ldsm_x4(bs + sub * kTileBytes + swz(16 * jj + (lane & 7) + 8 * (lane >> 4), kc + ((lane >> 3) & 1)), bb);
+        mma16816(G[2 * jj], a, bb[0], bb[1]);
+        mma16816(G[2 * jj + 1], a, bb[2], bb[3]);
+      }
+      // C S_in
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        uint32_t bb[4];
+        ldsm_x4_t(ss + swz(k0 + (lane & 7) + 8 * ((lane >> 3) & 1), 2 * jj + (lane >> 4)), bb);
+        mma16816(CS[2 * jj], a, bb[0], bb[1]);
+        mma16816(CS[2 * jj + 1], a, bb[2], bb[3]);
+      }
+    }
+    // mask and scale: M[t][s] = G[t][s] e^(cum_t - cum_s) delta_s for s <= t
+    const int ta = r0 + gq, tb = ta + 8;
+    const float cta = cum[ta], ctb = cum[tb];
+    uint32_t M[4][4];  // A operand of (M)(x): k block kk2 = s in [16 kk2, 16 kk2 + 16)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int s0 = 8 * j + 2 * cq;
+      float m[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int t = (e < 2) ? ta : tb;
+        const int sx = s0 + (e & 1);
+        const float ct = (e < 2) ? cta : ctb;
+        m[e] = (sx <= t) ? G[j][e] * fast_exp(ct - cum[sx]) * dlt[sx] : 0.f;
+      }
+      M[j >> 1][(j & 1) * 2] = pack_bf16(m[0], m[1]);
+      M[j >> 1][(j & 1) * 2 + 1] = pack_bf16(m[2], m[3]);
+    }
+    float Y[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) Y[j][e] = 0.f;
+#pragma unroll
+    for (int kk2 = 0; kk2 < 4; ++kk2) {
+      if (kk2 > warp) break;
+      const uint32_t a[4] = {M[kk2][0], M[kk2][1], M[kk2][2], M[kk2][3]};
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        uint32_t bb[4];
+        ldsm_x4_t(xs + swz(16 * kk2 + (lane & 7) + 8 * ((lane >> 3) & 1), 2 * jj + (lane >> 4)), bb);
+        mma16816(Y[2 * jj], a, bb[0], bb[1]);
+        mma16816(Y[2 * jj + 1], a, bb[2], bb[3]);
+      }
+    }
+    const float eta = fast_exp(cta), etb = fast_exp(ctb);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float2 xa = unpack_bf16(*reinterpret_cast<const uint32_t*>(st + SM::kX + swz(ta, j) + 4 * cq));
+      const float2 xb = unpack_bf16(*reinterpret_cast<const uint32_t*>(st + SM::kX + swz(tb, j) + 4 * cq));
+      const float y0 = Y[j][0] + eta * CS[j][0] + Dh * xa.x;
+      const float y1 = Y[j][1] + eta * CS[j][1] + Dh * xa.y;
+      const float y2 = Y[j][2] + etb * CS[j][2] + Dh * xb.x;
+      const float y3 = Y[j][3] + etb * CS[j][3] + Dh * xb.y;
+      *reinterpret_cast<uint32_t*>(smem + SM::kStage + swz(ta, j) + 4 * cq) = pack_bf16(y0, y1);
+      *reinterpret_cast<uint32_t*>(smem + SM::kStage + swz(tb, j) + 4 * cq) = pack_bf16(y2, y3);
+    }
+    __syncthreads();
+    // the chunk's y rows to global memory, 16 bytes per thread and pass
+    {
+      __nv_bfloat16* yb = P.y + ((size_t)b * P.L) * P.H * kP + (size_t)h * kP;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int q = tid + kSsdThreads * i;  // 512 chunks of 16 bytes
+        const int row = q >> 3, c8 = q & 7;
+        if (t0 + row < P.L) {
+          const uint4 v = *reinterpret_cast<const uint4*>(smem + SM::kStage + swz(row, c8));
+          *reinterpret_cast<uint4*>(yb + (size_t)(t0 + row) * P.H * kP + 8 * c8) = v;
+        }
+      }
+    }
+    __syncthreads();
+    // x' = w o delta x into the staging box
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int q = tid + kSsdThreads * i;
+      const int row = q >> 3, c8 = q & 7;
+      const float f = wd[row];
+      const uint4 v = *reinterpret_cast<const uint4*>(st + SM::kX + swz(row, c8));
+      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+      uint32_t out[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 e = unpack_bf16(in[k]);
+        out[k] = pack_bf16(f * e.x, f * e.y);
+      }
+      *reinterpret_cast<uint4*>(smem + SM::kStage + swz(row, c8)) = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+    __syncthreads();
+    // ---- S = e^(cum_end) S + B^T x'   (warp w: rows n = 32w .. 32w+31 for N = 128)
+    const float dec = misc[0];
+#pragma unroll
+    for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) S[mt][j][e] *= dec;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {  // s blocks
+      uint32_t bx[4][4];
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj)
+        ldsm_x4_t(stg + swz(16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1), 2 * jj + (lane >> 4)), bx[jj]);
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt) {
+        const int m0 = warp * (N / 4) + 16 * mt;  // rows n
+        const int sub = m0 / 64, mc = (m0 % 64) / 8;
+        uint32_t a[4];
+        ldsm_x4_t(bs + sub * kTileBytes + swz(16 * kk + (lane & 7) + 8 * (lane >> 4), mc + ((lane >> 3) & 1)), a);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          mma16816(S[mt][2 * jj], a, bx[jj][0], bx[jj][1]);
+          mma16816(S[mt][2 * jj + 1], a, bx[jj][2], bx[jj][3]);
+        }
+      }
+    }
+    __syncthreads();  // every warp is done with S_in, the stage and x'
+    store_S_bf16();
+    if (tid == 0 && c + 2 < nch) issue(c + 2);
+  }
+  if (P.h_last) {
+    float* hl = P.h_last + ((size_t)b * P.H + h) * N * kP;
+#pragma unroll
+    for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int hlf = 0; hlf < 2; ++hlf) {
+          const int n = warp * (N / 4) + 16 * mt + gq + 8 * hlf, p = 8 * j + 2 * cq;
+          *reinterpret_cast<float2*>(hl + (size_t)n * kP + p) = make_float2(S[mt][j][2 * hlf], S[mt][j][2 * hlf + 1]);
+        }
+  }
+}
+
+template <int N>
+cudaError_t launch_n(const SsdParams& P, cudaStream_t stream) {
+  auto kern = s6_ssd_fwd_kernel<N>;
+  const size_t smem = SsdSmem<N>::kBytes + 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)(P.B * P.H), kSsdThreads, smem, stream>>>(P);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool ssd_supported(int act, int P, int N) { return act == SSM_BF16 && P == kP && (N == 64 || N == 128); }
+
+cudaError_t launch_ssd_fwd(const SsdArgs& a, cudaStream_t stream) {
+  SsdParams P;
+  memset(&P, 0, sizeof(P));
+  const uint64_t e = 2;
+  {
+    const uint64_t dims[3] = {(uint64_t)a.H * kP, (uint64_t)a.L, (uint64_t)a.B};
+    const uint64_t strides[2] = {(uint64_t)a.H * kP * e, (uint64_t)a.L * a.H * kP * e};
+    const uint32_t box[3] = {64, kQ, 1};
+    if (!encode_tile_map(&P.map_x, a.x, true, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)a.G * a.N, (uint64_t)a.L, (uint64_t)a.B};
+    const uint64_t strides[2] = {(uint64_t)a.G * a.N * e, (uint64_t)a.L * a.G * a.N * e};
+    const uint32_t box[3] = {64, kQ, 1};
+    if (!encode_tile_map(&P.map_B, a.Bm, true, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tile_map(&P.map_C, a.Cm, true, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  P.dt_raw = static_cast<const __nv_bfloat16*>(a.dt_raw);
+  P.dt_bias = a.dt_bias;
+  P.A_log = a.A_log;
+  P.Dp = a.Dp;
+  P.h0 = a.h0;
+  P.y = static_cast<__nv_bfloat16*>(a.y);
+  P.h_last = a.h_last;
+  P.status = a.status;
+  P.dt_min = a.dt_min;
+  P.dt_max = a.dt_max;
+  P.B = a.B;
+  P.L = a.L;
+  P.H = a.H;
+  P.G = a.G;
+  P.N = a.N;
+  return a.N == 128 ? launch_n<128>(P, stream) : launch_n<64>(P, stream);
+}
+
+}  // namespace s6

@@ -122,3 +122,54 @@ def make_workload(name: str, *, seed: int = 0, batch: Optional[int] = None,
                        delta_lo=w.delta_lo, delta_hi=w.delta_hi, h0_std=w.h0_std,
                        with_dout=with_dout)
 
+
+# ------------------------------------------------------------------ Mamba-2 SSD
+
+@dataclasses.dataclass(frozen=True)
+class SsdWorkload:
+    name: str
+    batch: int
+    seqlen: int
+    nheads: int
+    headdim: int
+    ngroups: int
+    dstate: int
+    act: str
+    description: str = ""
+
+    @property
+    def cells(self) -> int:
+        return self.batch * self.seqlen * self.nheads * self.headdim * self.dstate
+
+
+SSD_WORKLOADS = {
+    "mamba2_1p3b": SsdWorkload("mamba2_1p3b", 4, 4096, 64, 64, 1, 128, "bf16",
+                               description="Mamba-2-1.3B-shaped SSD forward: B=4 L=4096 heads=64 "
+                                           "headdim=64 groups=1 N=128, bf16 activations"),
+}
+
+
+def make_ssd_inputs(batch: int, seqlen: int, nheads: int, headdim: int, ngroups: int, dstate: int,
+                    act: str = "bf16", *, seed: int = 0, h0_std: Optional[float] = None) -> dict:
+    """Draw one SSD problem on the CPU (Mamba-2 initialisation: softplus(dt_bias)
+    ~ U[1e-3, 0.1] and A = exp(A_log) ~ U[1, 16] per head, Dp = 1).  Returns
+    x [B,L,H,P], dt_raw [B,L,H], Bm / Cm [B,L,G,N] (act dtype); dt_bias, A_log,
+    Dp [H] and h0 [B,H,N,P] (or None) float32."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    dt = act_dtype(act)
+
+    def normal(shape):
+        return torch.randn(shape, generator=g, dtype=torch.float32)
+
+    x = normal((batch, seqlen, nheads, headdim))
+    dt_raw = normal((batch, seqlen, nheads))
+    Bm = normal((batch, seqlen, ngroups, dstate))
+    Cm = normal((batch, seqlen, ngroups, dstate))
+    U = torch.rand((nheads,), generator=g, dtype=torch.float64) * (0.1 - 1e-3) + 1e-3
+    Aval = torch.rand((nheads,), generator=g, dtype=torch.float64) * 15.0 + 1.0
+    h0 = normal((batch, nheads, dstate, headdim)) * h0_std if h0_std is not None else None
+    cast = (lambda v: v.to(dt).contiguous()) if dt != torch.float32 else (lambda v: v.contiguous())
+    return {"x": cast(x), "dt_raw": cast(dt_raw), "Bm": cast(Bm), "Cm": cast(Cm),
+            "dt_bias": torch.log(torch.expm1(U)).to(torch.float32), "A_log": torch.log(Aval).to(torch.float32),
+            "Dp": torch.ones((nheads,), dtype=torch.float32), "h0": h0}

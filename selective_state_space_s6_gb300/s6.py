@@ -91,6 +91,8 @@ def load_library():
         lib.ssm_scan_bwd_partials_ex.restype = ci
         lib.ssm_step_ex.argtypes = [i64] * 3 + [ci] + [vp] * 10 + [vp, op]
         lib.ssm_step_ex.restype = ci
+        lib.ssm_ssd_fwd.argtypes = [i64] * 6 + [ci] + [vp] * 10 + [op, vp]
+        lib.ssm_ssd_fwd.restype = ci
         lib.ssm_conv1d_fwd.argtypes = [i64] * 4 + [ci] + [vp] * 6 + [vp]
         lib.ssm_conv1d_fwd.restype = ci
         lib.ssm_conv1d_bwd_workspace_bytes.argtypes = [i64] * 4 + [ci]
@@ -370,3 +372,21 @@ def conv1d_path(x, w, dout=None, y=None):
     if rc < 0:
         _check("ssm_conv1d_path", -rc)
     return CONV_PATHS[rc]
+
+
+def ssd_fwd(x, dt_raw, dt_bias, A_log, Bm, Cm, Dp, h0=None, *, y=None, h_last=None, want_h_last=True,
+            dt_limit=None, stream=None):
+    """Mamba-2 SSD forward.  x [B,L,H,P], dt_raw [B,L,H], Bm/Cm [B,L,G,N] (bf16);
+    dt_bias, A_log, Dp [H] f32; h0 [B,H,N,P] f32 (zeros when None).  Returns
+    ``(y [B,L,H,P], h_last [B,H,N,P] or None)``."""
+    B, L, H, P = x.shape
+    G, N = Bm.shape[2], Bm.shape[3]
+    if y is None:
+        y = torch.empty_like(x)
+    if h_last is None and want_h_last:
+        h_last = torch.empty((B, H, N, P), dtype=torch.float32, device=x.device)
+    rc = load_library().ssm_ssd_fwd(B, L, H, P, G, N, _act(x), _p(x), _p(dt_raw), _p(dt_bias), _p(A_log), _p(Bm),
+                                    _p(Cm), _p(Dp), _p(h0), _p(y), _p(h_last),
+                                    _opts(dt_limit) if dt_limit is not None else None, _stream(stream))
+    _check("ssm_ssd_fwd", rc)
+    return y, h_last

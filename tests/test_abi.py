@@ -118,6 +118,21 @@ def test_dt_limit_validation(lib):
         assert b"u must not be NULL" in lib.ssm_last_error()
 
 
+def test_ssd_validation(lib):
+    """Host-side checks of ssm_ssd_fwd: unsupported shapes and dtypes, groups
+    that do not divide the heads, misaligned tensors -- all before any launch."""
+    args = [FAKE] * 10
+    def call(B=1, L=8, H=2, P=64, G=1, N=64, act=1, a=None):
+        return lib.ssm_ssd_fwd(B, L, H, P, G, N, act, *(a or args), None, None)
+    assert call(P=32) == 2 and b"headdim 64" in lib.ssm_last_error()
+    assert call(N=16) == 2
+    assert call(act=0) == 2                      # f32 activations: not built
+    assert call(H=3, G=2) == 1 and b"multiple of ngroups" in lib.ssm_last_error()
+    bad = list(args)
+    bad[0] = ctypes.c_void_p(0x10008)            # x only 8-byte aligned
+    assert call(a=bad) == 1 and b"x is not 16-byte aligned" in lib.ssm_last_error()
+
+
 def test_segment_plan(lib):
     """The plans are functions of the shape.  Forward: one pass where the grid
     fills the GPU, time segments of at least 512 steps for long sequences over

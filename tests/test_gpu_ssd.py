@@ -1,0 +1,88 @@
+"""Mamba-2 SSD forward on the GPU (through the C ABI) against the f64 SSD
+oracle: ragged last chunks, one and several groups, both state sizes, an
+initial state and the final state, the limit on delta, a single step, the
+full Mamba-2-1.3B shape on sampled heads, and bit-identical repeated calls.
+Tolerance: the bf16 I/O bound, normwise max relative error <= 2e-2."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import TOL, np64, rel_err
+from selective_state_space_s6_gb300 import inputs, s6
+
+pytestmark = pytest.mark.gpu
+
+KEYS = ("x", "dt_raw", "dt_bias", "A_log", "Bm", "Cm", "Dp")
+
+
+def _dev(x):
+    return {k: (v.cuda() if v is not None else None) for k, v in x.items()}
+
+
+SHAPES = [
+    # B, L, H, P, G, N
+    (2, 200, 4, 64, 2, 64),    # ragged last chunk, two groups
+    (1, 130, 3, 64, 1, 128),
+    (2, 64, 2, 64, 1, 128),    # exactly one chunk
+    (1, 1, 2, 64, 1, 64),      # a single step
+    (3, 300, 6, 64, 3, 128),   # three groups of two heads
+]
+
+
+@pytest.mark.parametrize("B,L,H,P,G,N", SHAPES)
+@pytest.mark.parametrize("with_h0", [True, False])
+def test_ssd_parity(B, L, H, P, G, N, with_h0):
+    x = inputs.make_ssd_inputs(B, L, H, P, G, N, "bf16", seed=B + L + N, h0_std=0.5 if with_h0 else None)
+    xd = _dev(x)
+    y, h_last = s6.ssd_fwd(*[xd[k] for k in KEYS], xd["h0"])
+    s6.check_device_status()
+    ry, rh = oracle.ssd_fwd(*[x[k] for k in KEYS], x["h0"])
+    assert rel_err(np64(y), ry) <= TOL["bf16"]
+    assert rel_err(np64(h_last), rh) <= TOL["bf16"]
+
+
+def test_ssd_dt_limit():
+    x = inputs.make_ssd_inputs(2, 150, 4, 64, 1, 128, "bf16", seed=5, h0_std=0.5)
+    sp = torch.nn.functional.softplus(x["dt_raw"].double() + x["dt_bias"].double())
+    lim = (float(np.float32(torch.quantile(sp.flatten()[::7].float(), 0.25))),
+           float(np.float32(torch.quantile(sp.flatten()[::7].float(), 0.75))))
+    xd = _dev(x)
+    y, h_last = s6.ssd_fwd(*[xd[k] for k in KEYS], xd["h0"], dt_limit=lim)
+    s6.check_device_status()
+    ry, rh = oracle.ssd_fwd(*[x[k] for k in KEYS], x["h0"], dt_limit=lim)
+    ny, _ = oracle.ssd_fwd(*[x[k] for k in KEYS], x["h0"])
+    assert rel_err(ry, ny) > 0.05  # the limit changes the answer
+    assert rel_err(np64(y), ry) <= TOL["bf16"]
+    assert rel_err(np64(h_last), rh) <= TOL["bf16"]
+
+
+def test_ssd_full_shape_sampled_heads():
+    w = inputs.SSD_WORKLOADS["mamba2_1p3b"]
+    x = inputs.make_ssd_inputs(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.act, seed=0)
+    xd = _dev(x)
+    y, h_last = s6.ssd_fwd(*[xd[k] for k in KEYS], None)
+    s6.check_device_status()
+    for b, h in ((0, 0), (1, 33), (3, 63)):
+        g = h // (w.nheads // w.ngroups)
+        sub = {"x": x["x"][b:b + 1, :, h:h + 1], "dt_raw": x["dt_raw"][b:b + 1, :, h:h + 1],
+               "dt_bias": x["dt_bias"][h:h + 1], "A_log": x["A_log"][h:h + 1],
+               "Bm": x["Bm"][b:b + 1, :, g:g + 1], "Cm": x["Cm"][b:b + 1, :, g:g + 1], "Dp": x["Dp"][h:h + 1]}
+        ry, rh = oracle.ssd_fwd(*[sub[k] for k in KEYS])
+        assert rel_err(np64(y[b:b + 1, :, h:h + 1]), ry) <= TOL["bf16"], (b, h)
+        assert rel_err(np64(h_last[b:b + 1, h:h + 1]), rh) <= TOL["bf16"], (b, h)
+
+
+def test_ssd_deterministic():
+    x = _dev(inputs.make_ssd_inputs(2, 500, 8, 64, 2, 128, "bf16", seed=7, h0_std=0.5))
+    y0, h0 = s6.ssd_fwd(*[x[k] for k in KEYS], x["h0"])
+    for _ in range(3):
+        y1, h1 = s6.ssd_fwd(*[x[k] for k in KEYS], x["h0"])
+        assert torch.equal(y0, y1) and torch.equal(h0, h1)
+
+
+def test_ssd_empty_sequence_keeps_the_state():
+    x = _dev(inputs.make_ssd_inputs(2, 0, 2, 64, 1, 64, "bf16", seed=1, h0_std=0.5))
+    y, h_last = s6.ssd_fwd(*[x[k] for k in KEYS], x["h0"])
+    torch.cuda.synchronize()
+    assert y.numel() == 0 and torch.equal(h_last, x["h0"])
