@@ -61,14 +61,16 @@ def launches_per_step(fwd_segments, bwd_segments):
     return (1 if fwd_segments == 1 else 3) + (1 if bwd_segments == 1 else 3) + 2
 
 
-def load_peaks():
+def load_peaks(key="hbm_gbs"):
+    """A measured peak from MEASURED_PEAKS.json (HBM copy GB/s by default, or
+    bf16_tflops), else the fallback figure."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             pk = json.load(f)
-        return float(pk["hbm_gbs"]), "measured"
+        return float(pk[key]), "measured"
     except Exception:
-        return 6800.0, "fallback"
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}[key], "fallback"
 
 
 def algorithmic_bytes(B, L, D, N, e, chunk):
@@ -208,6 +210,56 @@ def time_conv1d(dev, B, L, D, act, K=4, reps=10):
         res[name] = {"ms": round(ms, 4), "algorithmic_bytes": nbytes, "hbm_gbs": round(gbs, 1),
                      "hbm_frac": round(gbs / peak, 4)}
     return res
+
+
+def ssd_algorithmic(w):
+    """Algorithmic bytes and tensor flops of one SSD forward: x, dt, Bm, Cm read
+    and y written once, the final state written once; per (b, t, h) the four
+    chunk products at 64-step chunks: C B^T (2 Q N), its product with delta x
+    (2 Q P), C S_in (2 N P) and the state update B^T x' (2 N P)."""
+    B, L, H, P, G, N = w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate
+    e = 2 if w.act == "bf16" else 4
+    nbytes = 2 * B * L * H * P * e + 2 * B * L * G * N * e + B * L * H * e + B * H * N * P * 4
+    flops = B * L * H * (2 * 64 * N + 2 * 64 * P + 4 * N * P)
+    return nbytes, flops
+
+
+def time_ssd(dev, reps=10):
+    """The Mamba-2 SSD forward on the 1.3B block's shape, CUDA events over
+    `reps` calls (inputs larger than L2)."""
+    from selective_state_space_s6_gb300 import s6
+
+    w = inputs.SSD_WORKLOADS["mamba2_1p3b"]
+    x = inputs.make_ssd_inputs(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.act, seed=0)
+    xd = {k: (v.to(dev) if v is not None else None) for k, v in x.items()}
+    keys = ("x", "dt_raw", "dt_bias", "A_log", "Bm", "Cm", "Dp")
+    y = torch.empty_like(xd["x"])
+    hl = torch.empty((w.batch, w.nheads, w.dstate, w.headdim), dtype=torch.float32, device=dev)
+
+    def run():
+        s6.ssd_fwd(*[xd[k] for k in keys], None, y=y, h_last=hl)
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        run()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / reps
+    nbytes, flops = ssd_algorithmic(w)
+    peak, _ = load_peaks()
+    tpeak = load_peaks("bf16_tflops")[0]
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    tfl = flops / (ms * 1e-3) / 1e12
+    return {"workload": w.description, "ms": round(ms, 4), "gcells_s": round(w.cells / (ms * 1e-3) / 1e9, 1),
+            "algorithmic_bytes": nbytes, "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),
+            "algorithmic_flops": flops, "tensor_tflops": round(tfl, 1), "tensor_frac": round(tfl / tpeak, 4),
+            "peaks": "measured hbm_gbs (copy) and bf16_tflops (cuBLAS, burst)",
+            "timing": f"CUDA events over {reps} calls"}
 
 
 # ------------------------------------------------------------------ clocks
@@ -577,6 +629,7 @@ def run_ours(args, world, rank, local):
 
     step_line = time_step(dev) if not args.no_step else None
     conv_line = time_conv1d(dev, B, L, D, w.act) if not args.no_step else None
+    ssd_line = time_ssd(dev) if not args.no_step else None
 
     cpu_base = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -608,6 +661,7 @@ def run_ours(args, world, rank, local):
         "kernels": per_kernel,
         "step": step_line,
         "conv1d": conv_line,
+        "ssd": ssd_line,
         "cpu_baseline": cpu_base,
         "clocks": clk,
     }
@@ -664,8 +718,9 @@ def run_reference(args, world, rank):
 def run_kernel(args):
     """One kernel family alone, a few calls on its own workload, for a
     profiler's capture (`--kernel`): the decode step (four calls, each after
-    a 256 MB read that empties L2) or conv1d + SiLU on the 1.4B block's shape
-    (three forward and three backward calls).  Prints one JSON line."""
+    a 256 MB read that empties L2), conv1d + SiLU on the 1.4B block's shape
+    (three forward and three backward calls) or the SSD forward on the
+    Mamba-2-1.3B shape (three calls).  Prints one JSON line."""
     from selective_state_space_s6_gb300 import s6
 
     dev = torch.device("cuda", 0)
@@ -695,6 +750,13 @@ def run_kernel(args):
             s6.conv1d_bwd(x, wt, bias, None, dout, want_dstate0=False)
         res["workload"] = f"B={B} L={L} D={D} K={K} bf16"
         res["path"] = s6.conv1d_path(x, wt)
+    elif args.kernel == "ssd":
+        w = inputs.SSD_WORKLOADS["mamba2_1p3b"]
+        x = inputs.make_ssd_inputs(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.act, seed=0)
+        xd = {k: (v.to(dev) if v is not None else None) for k, v in x.items()}
+        for _ in range(3):
+            s6.ssd_fwd(*[xd[k] for k in ("x", "dt_raw", "dt_bias", "A_log", "Bm", "Cm", "Dp")], None)
+        res["workload"] = w.description
     torch.cuda.synchronize(dev)
     s6.check_device_status()
     print(json.dumps(res), flush=True)
@@ -709,8 +771,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-step", action="store_true", help="skip the decode-step and conv1d measurements")
-    ap.add_argument("--kernel", choices=["step", "conv1d"],
+    ap.add_argument("--no-step", action="store_true", help="skip the decode-step, conv1d and SSD measurements")
+    ap.add_argument("--kernel", choices=["step", "conv1d", "ssd"],
                     help="run only this kernel family a few times (for a profiler) and exit")
     args = ap.parse_args(argv)
     if args.kernel:

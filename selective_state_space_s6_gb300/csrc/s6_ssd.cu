@@ -94,8 +94,8 @@ struct SsdSmem {
   static constexpr int kBuf = kCo + NT * kTileBytes;   // one stage
   static constexpr int kStage = 2 * kBuf;              // x' / y staging box [64][64]
   static constexpr int kS = kStage + kTileBytes;       // S_in (bf16) [N n][64 p]
-  static constexpr int kVec = kS + N * 128;            // cum, delta, w*delta [3][64] f32 + decay
-  static constexpr int kBar = kVec + 4 * 64 * 4;       // two mbarriers
+  static constexpr int kVec = kS + N * 128;            // two sets of cum, delta, w*delta [3][64] f32 + decay
+  static constexpr int kBar = kVec + 2 * 4 * 64 * 4;   // two mbarriers
   static constexpr int kBytes = kBar + 64;
   static constexpr uint32_t kTx = (1 + 2 * NT) * kTileBytes;
   static_assert(kBuf % 1024 == 0 && kStage % 1024 == 0 && kS % 1024 == 0, "swizzled boxes on 1024-byte boundaries");
@@ -110,10 +110,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* smem = smem_raw + (base - raw);
-  float* cum = reinterpret_cast<float*>(smem + SM::kVec);
-  float* dlt = cum + 64;
-  float* wd = cum + 128;
-  float* misc = cum + 192;  // [0] = e^(cum_end)
+  float* vec = reinterpret_cast<float*>(smem + SM::kVec);  // [2][cum, delta, w*delta, e^(cum_end)][64]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBar);
 
   const int b = blockIdx.x / P.H, h = blockIdx.x % P.H;
@@ -177,49 +174,64 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   };
   store_S_bf16();
 
+  // Warp 0 reads each chunk's dt one chunk ahead (two steps per lane) and,
+  // during the state update of the chunk before, turns them into delta, the
+  // running sum of delta*A, the weights e^(cum_end - cum_s) delta_s and the
+  // chunk's total decay (set c & 1 of `vec`).
+  float raw_next[2] = {0.f, 0.f};
+  auto load_dt = [&](int c) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int t = c * kQ + 2 * lane + i;
+      raw_next[i] = (c < nch && t < P.L) ? __bfloat162float(P.dt_raw[((size_t)b * P.L + t) * P.H + h]) : 0.f;
+    }
+  };
+  auto chunk_decays = [&](int c) {
+    float* v = vec + (c & 1) * 256;
+    float d2[2], a2[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int t = c * kQ + 2 * lane + i;
+      const float d = t < P.L ? clamp_dt(softplus_fast(raw_next[i] + bias), P.dt_min, P.dt_max) : 0.f;
+      d2[i] = d;
+      a2[i] = d * A;
+    }
+    float run = a2[0] + a2[1];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float u = __shfl_up_sync(0xffffffffu, run, o);
+      if (lane >= o) run += u;
+    }
+    const float end = __shfl_sync(0xffffffffu, run, 31);
+    const float c1 = run, c0 = run - a2[1];
+    v[2 * lane] = c0;
+    v[2 * lane + 1] = c1;
+    v[64 + 2 * lane] = d2[0];
+    v[64 + 2 * lane + 1] = d2[1];
+    v[128 + 2 * lane] = fast_exp(end - c0) * d2[0];
+    v[128 + 2 * lane + 1] = fast_exp(end - c1) * d2[1];
+    if (lane == 0) v[192] = fast_exp(end);
+  };
+  if (warp == 0) {
+    load_dt(0);
+    chunk_decays(0);
+    load_dt(1);
+  }
+  __syncthreads();
+
   for (int c = 0; c < nch; ++c) {
     const int s = c & 1;
     const int t0 = c * kQ;
     const bool ok = mbar_wait(&full[s], (c >> 1) & 1, P.status);
     if (__syncthreads_or(!ok)) break;  // the copy never came: stop, uniformly
-    const unsigned char* st = smem + s * SM::kBuf;
+    unsigned char* st = smem + s * SM::kBuf;
     const uint32_t xs = base + s * SM::kBuf + SM::kX;
     const uint32_t bs = base + s * SM::kBuf + SM::kBo;
     const uint32_t cs = base + s * SM::kBuf + SM::kCo;
     const uint32_t ss = base + SM::kS;
-    const uint32_t stg = base + SM::kStage;
-
-    // ---- delta, the running sum of delta*A (two steps per lane), weights
-    if (warp == 0) {
-      float d2[2], a2[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int t = t0 + 2 * lane + i;
-        float d = 0.f;
-        if (t < P.L) {
-          const float raw = __bfloat162float(P.dt_raw[((size_t)b * P.L + t) * P.H + h]);
-          d = clamp_dt(softplus_fast(raw + bias), P.dt_min, P.dt_max);
-        }
-        d2[i] = d;
-        a2[i] = d * A;
-      }
-      float run = a2[0] + a2[1];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float v = __shfl_up_sync(0xffffffffu, run, o);
-        if (lane >= o) run += v;
-      }
-      const float end = __shfl_sync(0xffffffffu, run, 31);
-      const float c1 = run, c0 = run - a2[1];
-      cum[2 * lane] = c0;
-      cum[2 * lane + 1] = c1;
-      dlt[2 * lane] = d2[0];
-      dlt[2 * lane + 1] = d2[1];
-      wd[2 * lane] = fast_exp(end - c0) * d2[0];
-      wd[2 * lane + 1] = fast_exp(end - c1) * d2[1];
-      if (lane == 0) misc[0] = fast_exp(end);
-    }
-    __syncthreads();
+    const float* cum = vec + s * 256;
+    const float* dlt = cum + 64;
+    const float* wd = cum + 128;
 
     // ---- y rows 16w .. 16w+15: (C B^T o L)(delta x) + e^cum (C S_in) + D x
     const int r0 = 16 * warp;
@@ -299,8 +311,9 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
       *reinterpret_cast<uint32_t*>(smem + SM::kStage + swz(ta, j) + 4 * cq) = pack_bf16(y0, y1);
       *reinterpret_cast<uint32_t*>(smem + SM::kStage + swz(tb, j) + 4 * cq) = pack_bf16(y2, y3);
     }
-    __syncthreads();
-    // the chunk's y rows to global memory, 16 bytes per thread and pass
+    __syncthreads();  // y rows staged; every read of x done
+    // the chunk's y rows to global memory (16 bytes per thread and pass), and
+    // x' = w o delta x in place of x
     {
       __nv_bfloat16* yb = P.y + ((size_t)b * P.L) * P.H * kP + (size_t)h * kP;
 #pragma unroll
@@ -311,28 +324,21 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
           const uint4 v = *reinterpret_cast<const uint4*>(smem + SM::kStage + swz(row, c8));
           *reinterpret_cast<uint4*>(yb + (size_t)(t0 + row) * P.H * kP + 8 * c8) = v;
         }
-      }
-    }
-    __syncthreads();
-    // x' = w o delta x into the staging box
+        const float f = wd[row];
+        const uint4 xv = *reinterpret_cast<const uint4*>(st + SM::kX + swz(row, c8));
+        const uint32_t in[4] = {xv.x, xv.y, xv.z, xv.w};
+        uint32_t out[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int q = tid + kSsdThreads * i;
-      const int row = q >> 3, c8 = q & 7;
-      const float f = wd[row];
-      const uint4 v = *reinterpret_cast<const uint4*>(st + SM::kX + swz(row, c8));
-      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-      uint32_t out[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 e = unpack_bf16(in[k]);
-        out[k] = pack_bf16(f * e.x, f * e.y);
+        for (int k = 0; k < 4; ++k) {
+          const float2 e = unpack_bf16(in[k]);
+          out[k] = pack_bf16(f * e.x, f * e.y);
+        }
+        *reinterpret_cast<uint4*>(st + SM::kX + swz(row, c8)) = make_uint4(out[0], out[1], out[2], out[3]);
       }
-      *reinterpret_cast<uint4*>(smem + SM::kStage + swz(row, c8)) = make_uint4(out[0], out[1], out[2], out[3]);
     }
     __syncthreads();
     // ---- S = e^(cum_end) S + B^T x'   (warp w: rows n = 32w .. 32w+31 for N = 128)
-    const float dec = misc[0];
+    const float dec = cum[192];
 #pragma unroll
     for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
@@ -344,7 +350,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
       uint32_t bx[4][4];
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj)
-        ldsm_x4_t(stg + swz(16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1), 2 * jj + (lane >> 4)), bx[jj]);
+        ldsm_x4_t(xs + swz(16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1), 2 * jj + (lane >> 4)), bx[jj]);
 #pragma unroll
       for (int mt = 0; mt < kMT; ++mt) {
         const int m0 = warp * (N / 4) + 16 * mt;  // rows n
@@ -357,6 +363,10 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
           mma16816(S[mt][2 * jj + 1], a, bx[jj][2], bx[jj][3]);
         }
       }
+    }
+    if (warp == 0 && c + 1 < nch) {  // the next chunk's decays; its successor's dt in flight
+      chunk_decays(c + 1);
+      load_dt(c + 2);
     }
     __syncthreads();  // every warp is done with S_in, the stage and x'
     store_S_bf16();
