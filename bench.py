@@ -473,12 +473,19 @@ def run_ours(args, world, rank, local):
     cells = w.cells
     value = world * cells / (ms_step * 1e-3) / 1e9
 
-    # ---- e2e: pinned host inputs -> device -> fwd + bwd -> results back to pinned host,
-    # every step.  Serial: one stream, copy in, compute, copy out.  Pipelined:
-    # three streams and two device buffer sets, so that the copy-in of step k+1
-    # and the copy-out of step k-1 run on the copy engines while step k computes.
+    # ---- e2e: pinned host inputs -> device -> fwd + bwd -> the step's result back
+    # to pinned host memory, every step.  The result of a training step of
+    # this layer is its parameter gradients (dA_log, dDp, d_delta_bias: what
+    # the optimizer reads); the activation gradients and the output stay on
+    # the device for the layers around it.  A second figure reads every output
+    # back (out and all gradients, 538 MB per step).  Serial: one stream, copy
+    # in, compute, copy out.  Pipelined: three streams and two device buffer
+    # sets, so that the copy-in of step k+1 and the copy-out of step k-1 run
+    # on the copy engines while step k computes.
     in_keys = ["u", "delta_raw", "z", "Bm", "Cm", "A_log", "Dp", "delta_bias", "dout"]
     out_keys = ["du", "d_delta_raw", "dz", "dBm", "dCm", "dA_log", "dD", "d_delta_bias"]
+    result_keys = ["dA_log", "dD", "d_delta_bias"]
+    readback = {"keys": result_keys, "out": False}
     h_in = {k: x_cpu[k].pin_memory() for k in in_keys}
 
     def host_outputs():
@@ -488,7 +495,8 @@ def run_ours(args, world, rank, local):
 
     h_out = [host_outputs(), host_outputs()]
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in h_out[0].values())
+    d2h_full = sum(t.numel() * t.element_size() for t in h_out[0].values())
+    d2h = sum(h_out[0][k].numel() * h_out[0][k].element_size() for k in result_keys)
 
     def device_set(first):
         if first:
@@ -512,8 +520,9 @@ def run_ours(args, world, rank, local):
             S["x"][k].copy_(h_in[k], non_blocking=True)
 
     def copy_out(S, H):
-        H["out"].copy_(S["out"], non_blocking=True)
-        for k in out_keys:
+        if readback["out"]:
+            H["out"].copy_(S["out"], non_blocking=True)
+        for k in readback["keys"]:
             H[k].copy_(S["g"][k], non_blocking=True)
 
     def serial_step():
@@ -573,6 +582,13 @@ def run_ours(args, world, rank, local):
     e2e_ms = sorted(e2e_runs)[1]
     e2e_value = world * cells / (e2e_ms * 1e-3) / 1e9
     serial_value = world * cells / (serial_ms * 1e-3) / 1e9
+    # every output read back
+    readback.update(keys=out_keys, out=True)
+    full_runs = []
+    for _ in range(3):
+        s_in.wait_stream(stream)
+        full_runs.append(timed(pipelined_step, ke, s_in, s_out))
+    full_ms = sorted(full_runs)[1]
     # the host link alone: the same copies with no compute, each direction by
     # itself and both at once (the floor under the pipelined e2e step)
     in_ms = timed(lambda k: copy_in(sets[k % 2]), ke, stream, stream)
@@ -590,9 +606,9 @@ def run_ours(args, world, rank, local):
 
     both_ms = timed(both, ke, stream, stream)
     torch.cuda.synchronize(dev)
-    link = {"h2d_gbs": round(h2d / (in_ms * 1e-3) / 1e9, 1), "d2h_gbs": round(d2h / (out_ms * 1e-3) / 1e9, 1),
+    link = {"h2d_gbs": round(h2d / (in_ms * 1e-3) / 1e9, 1), "d2h_gbs": round(d2h_full / (out_ms * 1e-3) / 1e9, 1),
             "both_ms_per_step": round(both_ms, 4),
-            "note": "pinned-host copies of one step's inputs and results alone, no compute"}
+            "note": "pinned-host copies of one step's inputs and of every output alone, no compute"}
 
     # ---- roofline of the dominant kernel (the backward scan), live event timing.
     # The scans are bound by instruction issue on the FP32/SFU pipes, not by
@@ -652,6 +668,11 @@ def run_ours(args, world, rank, local):
                 "overlap": "copy-in of step k+1 and copy-out of step k-1 overlap step k "
                            "(three streams, two device buffer sets)",
                 "runs_ms_per_step": [round(v, 4) for v in e2e_runs], "reported": "median of 3 runs",
+                "result_read_back": "parameter gradients dA_log, dDp, d_delta_bias",
+                "full_read_back": {"value": round(world * cells / (full_ms * 1e-3) / 1e9, 2),
+                                   "ms_per_step": round(full_ms, 4), "d2h_bytes_per_step": d2h_full,
+                                   "runs_ms_per_step": [round(v, 4) for v in full_runs],
+                                   "note": "out and every gradient copied back each step, pipelined"},
                 "serial": {"value": round(serial_value, 2), "ms_per_step": round(serial_ms, 4),
                            "runs_ms_per_step": [round(v, 4) for v in serial_runs]},
                 "host_link": link},
