@@ -377,20 +377,39 @@ __global__ void __launch_bounds__(kTileWarps * 32) s6_conv1d_fwd_tile_kernel(con
 #pragma unroll
   for (int k = 0; k < K - 1; ++k)
     if (!(s0 && ts - (K - 1) + k < 0)) Vec<Act, 4>::lds(xs + (warp * kTileSeg + k) * kTileCh + 4 * lane, win[k]);
-  Act* __restrict__ out = static_cast<Act*>(p.out);
+  Act* __restrict__ out = static_cast<Act*>(p.out) + ((size_t)b * p.L + ts) * p.D + d;
+  const int nt = min(kTileSeg, p.L - ts);  // steps of this segment inside [0, L)
 #pragma unroll 4
   for (int i = 0; i < kTileSeg; ++i) {
-    const int t = ts + i;
     Vec<Act, 4>::lds(xs + (warp * kTileSeg + i + K - 1) * kTileCh + 4 * lane, win[K - 1]);
     float o[4];
+    if constexpr (std::is_same<Act, __nv_bfloat16>::value) {
+      // two channels per packed op; per channel the same operations in the
+      // same order as the scalar form (the other paths and the step), so the
+      // results are the same bit for bit
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float pre = bs[j];
+      for (int jp = 0; jp < 2; ++jp) {
+        float2 pre = make_float2(bs[2 * jp], bs[2 * jp + 1]);
 #pragma unroll
-      for (int k = 0; k < K; ++k) pre += wk[k][j] * win[k][j];
-      o[j] = pre * sig<Act>(pre);
+        for (int k = 0; k < K; ++k)
+          pre = ffma2(make_float2(wk[k][2 * jp], wk[k][2 * jp + 1]), make_float2(win[k][2 * jp], win[k][2 * jp + 1]), pre);
+        const float2 x = fmul2(pre, make_float2(-kLog2e, -kLog2e));
+        const float2 den = fadd2(make_float2(1.f, 1.f), make_float2(ex2_approx(x.x), ex2_approx(x.y)));
+        const float2 r = fmul2(pre, make_float2(rcp_approx(den.x), rcp_approx(den.y)));
+        o[2 * jp] = r.x;
+        o[2 * jp + 1] = r.y;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float pre = bs[j];
+#pragma unroll
+        for (int k = 0; k < K; ++k) pre += wk[k][j] * win[k][j];
+        o[j] = pre * sig<Act>(pre);
+      }
     }
-    if (cv && t < p.L) Vec<Act, 4>::store(out + ((size_t)b * p.L + t) * p.D + d, o);
+    if (cv && i < nt) Vec<Act, 4>::store(out, o);
+    out += p.D;
 #pragma unroll
     for (int k = 0; k < K - 1; ++k)
 #pragma unroll
