@@ -455,13 +455,32 @@ __global__ void __launch_bounds__(kTileWarps * 32) s6_conv1d_bwd_tile_kernel(con
   auto dpre_from = [&](int t, const float (&in)[K][4], float* g) {
     float go[4];
     Vec<Act, 4>::lds(gs + (t - t0) * kTileCh + 4 * lane, go);
+    if constexpr (std::is_same<Act, __nv_bfloat16>::value) {
+      // two channels per packed op, per channel the scalar form's operations
+      // in its order (bit-identical to the other paths)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float pre = bs[i];
+      for (int jp = 0; jp < 2; ++jp) {
+        float2 pre = make_float2(bs[2 * jp], bs[2 * jp + 1]);
 #pragma unroll
-      for (int k = 0; k < K; ++k) pre += wk[k][i] * in[k][i];
-      const float s = sig<Act>(pre);
-      g[i] = go[i] * s * fmaf(pre, 1.f - s, 1.f);
+        for (int k = 0; k < K; ++k)
+          pre = ffma2(make_float2(wk[k][2 * jp], wk[k][2 * jp + 1]), make_float2(in[k][2 * jp], in[k][2 * jp + 1]), pre);
+        const float2 x = fmul2(pre, make_float2(-kLog2e, -kLog2e));
+        const float2 den = fadd2(make_float2(1.f, 1.f), make_float2(ex2_approx(x.x), ex2_approx(x.y)));
+        const float2 s = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+        const float2 f = ffma2(pre, fadd2(make_float2(1.f, 1.f), make_float2(-s.x, -s.y)), make_float2(1.f, 1.f));
+        const float2 gg = fmul2(fmul2(make_float2(go[2 * jp], go[2 * jp + 1]), s), f);
+        g[2 * jp] = gg.x;
+        g[2 * jp + 1] = gg.y;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float pre = bs[i];
+#pragma unroll
+        for (int k = 0; k < K; ++k) pre += wk[k][i] * in[k][i];
+        const float s = sig<Act>(pre);
+        g[i] = go[i] * s * fmaf(pre, 1.f - s, 1.f);
+      }
     }
   };
   float aw[K][4], ab[4];  // this warp's sums of the dw[k] and dbias terms
@@ -492,14 +511,24 @@ __global__ void __launch_bounds__(kTileWarps * 32) s6_conv1d_bwd_tile_kernel(con
       dpre_from(t, xw, gw[0]);
       float o[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float acc = 0.f;
+      for (int jp = 0; jp < 2; ++jp) {
+        const int j0 = 2 * jp, j1 = 2 * jp + 1;
+        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < K; ++k) acc += wk[k][j] * gw[K - 1 - k][j];
-        o[j] = acc;
-        ab[j] += gw[0][j];
+        for (int k = 0; k < K; ++k)
+          acc = ffma2(make_float2(wk[k][j0], wk[k][j1]), make_float2(gw[K - 1 - k][j0], gw[K - 1 - k][j1]), acc);
+        o[j0] = acc.x;
+        o[j1] = acc.y;
+        const float2 g0 = make_float2(gw[0][j0], gw[0][j1]);
+        const float2 sb = fadd2(make_float2(ab[j0], ab[j1]), g0);
+        ab[j0] = sb.x;
+        ab[j1] = sb.y;
 #pragma unroll
-        for (int k = 0; k < K; ++k) aw[k][j] += gw[0][j] * xw[k][j];
+        for (int k = 0; k < K; ++k) {
+          const float2 sw = ffma2(g0, make_float2(xw[k][j0], xw[k][j1]), make_float2(aw[k][j0], aw[k][j1]));
+          aw[k][j0] = sw.x;
+          aw[k][j1] = sw.y;
+        }
       }
       if (cv && t < p.L) Vec<Act, 4>::store(dx + ((size_t)b * p.L + t) * p.D + d, o);
 #pragma unroll
