@@ -27,9 +27,11 @@
  *            deterministic_backward.py page passes dt_limit = (0, inf) as the
  *            default of the same clamp.
  *   Sources: the recurrence, discretisation and readout are the ones the final
- *   selective_scan_kernel computes on the POPCORNBENCH page (transcript
- *   FW-GLM-5-1__l2_p30): "A_val = -expf(A_log[d*N+n])", "dA = expf(delta*A)",
- *   "h = dA*h + x*B*delta", "y = sum_n h*C + x*D".  The softplus on delta, the
+ *   selective_scan_kernel on the POPCORNBENCH page (transcript
+ *   FW-GLM-5-1__l2_p30) computes: A as minus the exponential of A_log, the
+ *   decay as the exponential of delta times A, the state scaled by the decay
+ *   plus delta times B times the input, and the output as the sum over n of
+ *   C times the state plus D times the input.  The softplus on delta, the
  *   exp_negate of A_log, the SiLU gate and gating_backward are the kernels the
  *   mamba-rs kernels.rs page registers (MambaKernels, "SSM recurrence",
  *   "Activations" and "Elementwise" groups).
