@@ -145,3 +145,36 @@ def test_conv1d_paths_agree():
         assert torch.equal(g["dx"], ref_g["dx"]), path
         for k in ("dw", "dbias", "dstate0"):
             assert rel_err(np64(g[k]), np64(ref_g[k])) <= 1e-5, (path, k)
+
+
+def _sweep_shapes(n=10, seed=123):
+    r = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        B = int(r.integers(1, 4))
+        L = int(r.integers(1, 400))
+        D = int(r.choice([8, 24, 40, 64, 100, 136, 264]))
+        K = int(r.integers(1, 9))
+        act = str(r.choice(["f32", "bf16"]))
+        state = bool(r.integers(0, 2))
+        out.append((B, L, D, K, act, state))
+    return out
+
+
+@pytest.mark.parametrize("B,L,D,K,act,state", _sweep_shapes())
+def test_conv1d_random_shape_sweep(B, L, D, K, act, state):
+    """Seeded random shapes over every path, width and edge (L < K, ragged
+    tiles and channel tiles), forward and backward against the oracle."""
+    x, w, bias, s0, dout = _case(B, L, D, K, act, seed=B * 31 + L + K, state=state)
+    xd, wd, bd, sd, dd = _dev(x, w, bias, s0, dout)
+    out, s_last = s6.conv1d_fwd(xd, wd, bd, sd)
+    g = s6.conv1d_bwd(xd, wd, bd, sd, dd)
+    torch.cuda.synchronize()
+    ref_out, ref_s = oracle.conv1d_fwd(x, w, bias, s0)
+    ref = oracle.conv1d_bwd(x, w, bias, s0, dout)
+    tol = TOL[act]
+    assert rel_err(np64(out), ref_out) <= tol
+    if K > 1:
+        assert np.array_equal(np64(s_last), ref_s)
+    for k in ("dx", "dw", "dbias"):
+        assert rel_err(np64(g[k]), ref[k]) <= tol, k

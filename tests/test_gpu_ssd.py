@@ -86,3 +86,32 @@ def test_ssd_empty_sequence_keeps_the_state():
     y, h_last = s6.ssd_fwd(*[x[k] for k in KEYS], x["h0"])
     torch.cuda.synchronize()
     assert y.numel() == 0 and torch.equal(h_last, x["h0"])
+
+
+def _sweep(n=8, seed=321):
+    r = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        B = int(r.integers(1, 4))
+        L = int(r.integers(1, 300))
+        G = int(r.integers(1, 4))
+        H = G * int(r.integers(1, 4))
+        N = int(r.choice([64, 128]))
+        h0 = bool(r.integers(0, 2))
+        lim = bool(r.integers(0, 2))
+        out.append((B, L, H, G, N, h0, lim))
+    return out
+
+
+@pytest.mark.parametrize("B,L,H,G,N,with_h0,limited", _sweep())
+def test_ssd_random_shape_sweep(B, L, H, G, N, with_h0, limited):
+    """Seeded random shapes (lengths from one step to several ragged chunks,
+    groups, both state sizes, with and without h0 and a limit on delta)."""
+    x = inputs.make_ssd_inputs(B, L, H, 64, G, N, "bf16", seed=B * 7 + L, h0_std=0.5 if with_h0 else None)
+    lim = (0.01, 0.05) if limited else None
+    xd = _dev(x)
+    y, h_last = s6.ssd_fwd(*[xd[k] for k in KEYS], xd["h0"], dt_limit=lim)
+    s6.check_device_status()
+    ry, rh = oracle.ssd_fwd(*[x[k] for k in KEYS], x["h0"], dt_limit=lim)
+    assert rel_err(np64(y), ry) <= TOL["bf16"]
+    assert rel_err(np64(h_last), rh) <= TOL["bf16"]
