@@ -141,6 +141,19 @@ def test_bitwise_deterministic_10_runs(shape):
     assert len(digests) == 1
 
 
+@pytest.mark.parametrize("name", ["mamba130m", "mamba1p4b", "long"])
+def test_bitwise_deterministic_10_runs_full_size(name):
+    """Ten forward + backward runs of a full-size workload give identical
+    bytes in every output (compared on the device against the first run)."""
+    xd = to_dev(inputs.make_workload(name))
+    first = gpu_fwd_bwd(xd)
+    keep = {k: v.clone() for k, v in first.items() if v is not None}
+    for _ in range(9):
+        r = gpu_fwd_bwd(xd)
+        for k, v in keep.items():
+            assert torch.equal(r[k], v), k
+
+
 def test_empty_inputs():
     # L = 0: no steps; h_last = h0, parameter gradients 0, dh0 = dh_last
     x = to_dev(_inputs(2, 0, 5, 3, "f32", seed=1))
