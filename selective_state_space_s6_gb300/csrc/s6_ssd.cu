@@ -110,7 +110,9 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* smem = smem_raw + (base - raw);
-  float* vec = reinterpret_cast<float*>(smem + SM::kVec);  // [2][cum, delta, w*delta, e^(cum_end)][64]
+  // per chunk set (two sets, by chunk parity): (cum, delta) pairs of steps
+  // [0, 64) interleaved [0, 128), w*delta [128, 192), e^(cum_end) [192]
+  float* vec = reinterpret_cast<float*>(smem + SM::kVec);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBar);
 
   const int b = blockIdx.x / P.H, h = blockIdx.x % P.H;
@@ -204,10 +206,8 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     }
     const float end = __shfl_sync(0xffffffffu, run, 31);
     const float c1 = run, c0 = run - a2[1];
-    v[2 * lane] = c0;
-    v[2 * lane + 1] = c1;
-    v[64 + 2 * lane] = d2[0];
-    v[64 + 2 * lane + 1] = d2[1];
+    // (cum, delta) of steps 2 lane and 2 lane + 1 side by side: one 16-byte read per pair
+    *reinterpret_cast<float4*>(v + 4 * lane) = make_float4(c0, d2[0], c1, d2[1]);
     v[128 + 2 * lane] = fast_exp(end - c0) * d2[0];
     v[128 + 2 * lane + 1] = fast_exp(end - c1) * d2[1];
     if (lane == 0) v[192] = fast_exp(end);
@@ -229,8 +229,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     const uint32_t bs = base + s * SM::kBuf + SM::kBo;
     const uint32_t cs = base + s * SM::kBuf + SM::kCo;
     const uint32_t ss = base + SM::kS;
-    const float* cum = vec + s * 256;
-    const float* dlt = cum + 64;
+    const float* cum = vec + s * 256;  // cum of step t at cum[2 t], delta at cum[2 t + 1]
     const float* wd = cum + 128;
 
     // ---- y rows 16w .. 16w+15: (C B^T o L)(delta x) + e^cum (C S_in) + D x
@@ -266,18 +265,20 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     }
     // mask and scale: M[t][s] = G[t][s] e^(cum_t - cum_s) delta_s for s <= t
     const int ta = r0 + gq, tb = ta + 8;
-    const float cta = cum[ta], ctb = cum[tb];
+    const float cta = cum[2 * ta], ctb = cum[2 * tb];
     uint32_t M[4][4];  // A operand of (M)(x): k block kk2 = s in [16 kk2, 16 kk2 + 16)
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int s0 = 8 * j + 2 * cq;
+      const float4 cd = *reinterpret_cast<const float4*>(cum + 2 * s0);  // steps s0, s0 + 1
       float m[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int t = (e < 2) ? ta : tb;
         const int sx = s0 + (e & 1);
         const float ct = (e < 2) ? cta : ctb;
-        m[e] = (sx <= t) ? G[j][e] * fast_exp(ct - cum[sx]) * dlt[sx] : 0.f;
+        const float cs_ = (e & 1) ? cd.z : cd.x, ds_ = (e & 1) ? cd.w : cd.y;
+        m[e] = (sx <= t) ? G[j][e] * fast_exp(ct - cs_) * ds_ : 0.f;
       }
       M[j >> 1][(j & 1) * 2] = pack_bf16(m[0], m[1]);
       M[j >> 1][(j & 1) * 2 + 1] = pack_bf16(m[2], m[3]);
