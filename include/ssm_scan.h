@@ -16,6 +16,11 @@
  * activation saves, local backward plus dB/dC/dD/dA_log reductions) of the
  * mamba-rs kernels.rs page (MambaKernels).
  *
+ * Entry points: the scan (forward with and without saves, backward, its two
+ * halves, a no-allocation backward, the decode step), their _ex variants with
+ * a limit on delta, the causal depthwise conv1d + SiLU in front of the scan
+ * (forward, backward, step), and the Mamba-2 SSD forward.
+ *
  * Conventions shared by every entry point
  *   - Shapes: B = batch, L = seqlen, D = dim (d_inner), N = dstate, 1 <= N <= 16.
  *   - Layouts are dense row-major, last index contiguous:

@@ -47,9 +47,19 @@ def _deps() -> list:
     return out
 
 
+def _code_only(text: str) -> str:
+    """Source text without C/C++ comments and with runs of whitespace
+    collapsed: what the compiler sees (an edit to a comment leaves it)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_digest(sources=None) -> str:
-    """sha256 over CUDA sources and every header (identifies the kernels a
-    profile was taken on): the given ``csrc/*.cu`` files (all when None)."""
+    """sha256 over the code (comments stripped) of CUDA sources and every
+    header -- identifies the kernels a profile was taken on: the given
+    ``csrc/*.cu`` files (all when None)."""
     import hashlib
     h = hashlib.sha256()
     for path in sorted(_deps()):
@@ -57,8 +67,8 @@ def kernel_source_digest(sources=None) -> str:
             continue
         if sources is not None and path.endswith(".cu") and os.path.basename(path) not in sources:
             continue
-        with open(path, "rb") as f:
-            h.update(os.path.basename(path).encode() + b"\0" + f.read())
+        with open(path, encoding="utf-8") as f:
+            h.update(os.path.basename(path).encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
