@@ -85,6 +85,36 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t v) {
 }
 __device__ __forceinline__ float fast_exp(float x) { return ex2_approx(x * kLog2e); }
 
+// ---- tcgen05 (5th-generation tensor core) helpers for the state update
+// Shared-memory matrix descriptor of a 128-byte-swizzled operand: start
+// address, leading-dimension byte offset (between 64-element blocks of the
+// M/N dimension for an MN-major operand), stride byte offset (between 8-row
+// groups of K), descriptor version 1, swizzle mode 128B.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor, kind::f16: f32 accumulator, bf16 A and B, both
+// MN-major, N = 64, M = 128.
+constexpr uint32_t kUmmaIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) | ((64u >> 3) << 17) |
+                                ((128u >> 4) << 24);
+// D[tmem] (+)= A (smem) x B (smem), issued by one thread
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrive on `bar` once every tcgen05 operation this thread issued has completed
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+// make this thread's generic-proxy shared-memory writes visible to the tensor core
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 template <int N>
 struct SsdSmem {
   static constexpr int NT = N / 64;                    // 64-column boxes of Bm / Cm
@@ -95,7 +125,7 @@ struct SsdSmem {
   static constexpr int kStage = 2 * kBuf;              // x' / y staging box [64][64]
   static constexpr int kS = kStage + kTileBytes;       // S_in (bf16) [N n][64 p]
   static constexpr int kVec = kS + N * 128;            // two sets of cum, delta, w*delta [3][64] f32 + decay
-  static constexpr int kBar = kVec + 2 * 4 * 64 * 4;   // two mbarriers
+  static constexpr int kBar = kVec + 2 * 4 * 64 * 4;   // three mbarriers and the TMEM address
   static constexpr int kBytes = kBar + 64;
   static constexpr uint32_t kTx = (1 + 2 * NT) * kTileBytes;
   static_assert(kBuf % 1024 == 0 && kStage % 1024 == 0 && kS % 1024 == 0, "swizzled boxes on 1024-byte boundaries");
@@ -114,6 +144,12 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   // [0, 64) interleaved [0, 128), w*delta [128, 192), e^(cum_end) [192]
   float* vec = reinterpret_cast<float*>(smem + SM::kVec);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBar);
+  uint64_t* mma_bar = full + 2;  // the state update's completion (tcgen05 path)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 3);
+  // N = 128: the state lives in tensor memory (128 lanes = rows n, 64 columns
+  // = p, f32) and its update S = e^(cum_end) S + B^T x' runs as tcgen05.mma;
+  // N = 64: in the accumulators of the four warps (mma.sync)
+  constexpr bool kUmma = N == 128;
 
   const int b = blockIdx.x / P.H, h = blockIdx.x % P.H;
   const int g = h / (P.H / P.G);
@@ -127,9 +163,15 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   if (tid == 0) {
     mbar_init(&full[0], 1);
     mbar_init(&full[1], 1);
+    mbar_init(mma_bar, 1);
     fence_mbar_init();
   }
+  if (kUmma && warp == 0) tmem_alloc(tmem_slot, 64);
+  tmem_fence_before_sync();
   __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t tmem = kUmma ? *tmem_slot : 0u;
+  const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);  // this thread's lane (row n = tid)
   auto issue = [&](int c) {  // chunk c's boxes into stage c & 1 (one thread)
     const int s = c & 1;
     unsigned char* st = smem + s * SM::kBuf;
@@ -147,10 +189,40 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     if (nch > 1) issue(1);
   }
 
-  // the state: warp w holds rows n = 32w + 16 mt + {gq, gq + 8}, columns p = 8 j + 2 cq + {0, 1}
+  // the state (mma.sync path): warp w holds rows n = 32w + 16 mt + {gq, gq + 8}, columns p = 8 j + 2 cq + {0, 1}
   constexpr int kMT = N / 64;  // 16-row tiles of S per warp (N / 4 rows per warp)
-  float S[kMT][8][4];
-  {
+  float S[kMT][8][4];  // (unused on the tcgen05 path)
+  // tcgen05 path: thread tid owns row n = tid of S (one TMEM lane, 64 columns)
+  auto row_to_smem_bf16 = [&](const float (&v)[64]) {  // S_in for the next readout, [n][p] swizzled
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8)
+      *reinterpret_cast<uint4*>(smem + SM::kS + swz(tid, c8)) =
+          make_uint4(pack_bf16(v[8 * c8], v[8 * c8 + 1]), pack_bf16(v[8 * c8 + 2], v[8 * c8 + 3]),
+                     pack_bf16(v[8 * c8 + 4], v[8 * c8 + 5]), pack_bf16(v[8 * c8 + 6], v[8 * c8 + 7]));
+  };
+  auto tmem_row_ld = [&](float (&v)[64]) {
+    float a[32], c[32];
+    tmem_ld32(trow, a);
+    tmem_ld32(trow + 32u, c);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = a[i], v[32 + i] = c[i];
+  };
+  auto tmem_row_st = [&](const float (&v)[64]) {
+    float a[32], c[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) a[i] = v[i], c[i] = v[32 + i];
+    tmem_st32(trow, a);
+    tmem_st32(trow + 32u, c);
+  };
+  if constexpr (kUmma) {
+    float v[64];
+    const float* h0 = P.h0 ? P.h0 + (((size_t)b * P.H + h) * N + tid) * kP : nullptr;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = h0 ? h0[i] : 0.f;
+    row_to_smem_bf16(v);
+    tmem_row_st(v);
+    tmem_wait_st();
+  } else {
     const float* h0 = P.h0 ? P.h0 + ((size_t)b * P.H + h) * N * kP : nullptr;
 #pragma unroll
     for (int mt = 0; mt < kMT; ++mt)
@@ -174,7 +246,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
               pack_bf16(S[mt][j][2 * hlf], S[mt][j][2 * hlf + 1]);
         }
   };
-  store_S_bf16();
+  if constexpr (!kUmma) store_S_bf16();
 
   // Warp 0 reads each chunk's dt one chunk ahead (two steps per lane) and,
   // during the state update of the chunk before, turns them into delta, the
@@ -231,6 +303,17 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     const uint32_t ss = base + SM::kS;
     const float* cum = vec + s * 256;  // cum of step t at cum[2 t], delta at cum[2 t + 1]
     const float* wd = cum + 128;
+    if constexpr (kUmma) {  // S_in in TMEM takes the chunk's decay before the update accumulates onto it
+      tmem_fence_after_sync();
+      float v[64];
+      tmem_row_ld(v);
+      const float dec0 = cum[192];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) v[i] *= dec0;
+      tmem_row_st(v);
+      tmem_wait_st();
+      tmem_fence_before_sync();
+    }
 
     // ---- y rows 16w .. 16w+15: (C B^T o L)(delta x) + e^cum (C S_in) + D x
     const int r0 = 16 * warp;
@@ -337,31 +420,48 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
         *reinterpret_cast<uint4*>(st + SM::kX + swz(row, c8)) = make_uint4(out[0], out[1], out[2], out[3]);
       }
     }
+    if constexpr (kUmma) fence_proxy_async_smem();  // x' is read by the tensor core
     __syncthreads();
-    // ---- S = e^(cum_end) S + B^T x'   (warp w: rows n = 32w .. 32w+31 for N = 128)
-    const float dec = cum[192];
+    // ---- S = e^(cum_end) S + B^T x'
+    if constexpr (kUmma) {
+      // one thread issues the 128 x 64 x 64 product as four K = 16 steps:
+      // A = B^T from the Bm boxes (MN-major: n contiguous, the two 64-column
+      // boxes 8 KB apart), B = x' (MN-major), D = S in TMEM (already scaled)
+      if (tid == 0) {
+        tmem_fence_after_sync();
 #pragma unroll
-    for (int mt = 0; mt < kMT; ++mt)
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t da = umma_desc_sw128(bs + kk * 2048u, kTileBytes, 1024u);
+          const uint64_t db = umma_desc_sw128(xs + kk * 2048u, kTileBytes, 1024u);
+          umma_f16(tmem, da, db, kUmmaIdesc, 1u);
+        }
+        umma_commit(mma_bar);
+      }
+    } else {  // warp w: rows n = 16 w .. 16 w + 15 of S (N = 64)
+      const float dec = cum[192];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+      for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) S[mt][j][e] *= dec;
+        for (int j = 0; j < 8; ++j)
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {  // s blocks
-      uint32_t bx[4][4];
+          for (int e = 0; e < 4; ++e) S[mt][j][e] *= dec;
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj)
-        ldsm_x4_t(xs + swz(16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1), 2 * jj + (lane >> 4)), bx[jj]);
+      for (int kk = 0; kk < 4; ++kk) {  // s blocks
+        uint32_t bx[4][4];
 #pragma unroll
-      for (int mt = 0; mt < kMT; ++mt) {
-        const int m0 = warp * (N / 4) + 16 * mt;  // rows n
-        const int sub = m0 / 64, mc = (m0 % 64) / 8;
-        uint32_t a[4];
-        ldsm_x4_t(bs + sub * kTileBytes + swz(16 * kk + (lane & 7) + 8 * (lane >> 4), mc + ((lane >> 3) & 1)), a);
+        for (int jj = 0; jj < 4; ++jj)
+          ldsm_x4_t(xs + swz(16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1), 2 * jj + (lane >> 4)), bx[jj]);
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          mma16816(S[mt][2 * jj], a, bx[jj][0], bx[jj][1]);
-          mma16816(S[mt][2 * jj + 1], a, bx[jj][2], bx[jj][3]);
+        for (int mt = 0; mt < kMT; ++mt) {
+          const int m0 = warp * (N / 4) + 16 * mt;  // rows n
+          const int sub = m0 / 64, mc = (m0 % 64) / 8;
+          uint32_t a[4];
+          ldsm_x4_t(bs + sub * kTileBytes + swz(16 * kk + (lane & 7) + 8 * (lane >> 4), mc + ((lane >> 3) & 1)), a);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            mma16816(S[mt][2 * jj], a, bx[jj][0], bx[jj][1]);
+            mma16816(S[mt][2 * jj + 1], a, bx[jj][2], bx[jj][3]);
+          }
         }
       }
     }
@@ -369,11 +469,30 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
       chunk_decays(c + 1);
       load_dt(c + 2);
     }
+    if constexpr (kUmma) {
+      // the updated state: S_in of the next chunk's readout (bf16), or h_last
+      mbar_wait(mma_bar, (uint32_t)(c & 1), P.status);
+      tmem_fence_after_sync();
+      float v[64];
+      tmem_row_ld(v);
+      if (c + 1 < nch) {
+        row_to_smem_bf16(v);
+      } else if (P.h_last) {
+        float* hl = P.h_last + (((size_t)b * P.H + h) * N + tid) * kP;
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) *reinterpret_cast<float2*>(hl + i) = make_float2(v[i], v[i + 1]);
+      }
+      tmem_fence_before_sync();
+    }
     __syncthreads();  // every warp is done with S_in, the stage and x'
-    store_S_bf16();
+    if constexpr (!kUmma) store_S_bf16();
     if (tid == 0 && c + 2 < nch) issue(c + 2);
   }
-  if (P.h_last) {
+  if constexpr (kUmma) {
+    __syncthreads();
+    tmem_fence_after_sync();
+    if (warp == 0) tmem_dealloc(tmem, 64);
+  } else if (P.h_last) {
     float* hl = P.h_last + ((size_t)b * P.H + h) * N * kP;
 #pragma unroll
     for (int mt = 0; mt < kMT; ++mt)
