@@ -11,14 +11,16 @@
 //   L[t][s] = e^(cum_t - cum_s) for s <= t, else 0
 //   S_out = e^(cum_end) S_in + B^T (w o delta x),  w_s = e^(cum_end - cum_s)
 //
-// A CTA owns one (batch, head) sequence and walks its chunks in order,
-// carrying S (N x 64, f32) in the accumulator registers of its four warps;
-// the chunk's x, Bm and Cm tiles arrive by TMA (128-byte swizzled boxes of
-// 64 steps x 64 columns) into a two-deep ring.  The four products run on
-// the tensor cores with mma.sync (bf16 operands, f32 accumulation): C B^T
-// and C S_in share their A operand; the masked, scaled C B^T goes from the
-// accumulators straight into the A operand of the next product; the causal
-// structure skips the blocks above the diagonal.
+// A CTA owns one (batch, head) sequence and walks its chunks in order; the
+// chunk's x, Bm and Cm tiles arrive by TMA (128-byte swizzled boxes of 64
+// steps x 64 columns) into a two-deep ring.  All four products run on the
+// 5th-generation tensor core (bf16 operands straight from the swizzled
+// boxes, f32 accumulators in tensor memory, one issuing thread, completion
+// on an mbarrier): G = C B^T and C S_in, then Y = M x with M = G o L o delta
+// written back to shared memory as bf16, then the state update
+// S = e^(cum_end) S + B^T x'.  The state S (N x 64, f32) stays in tensor
+// memory for the whole sequence; its bf16 copy in shared memory feeds the
+// next chunk's readout.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -36,7 +38,7 @@ namespace {
 
 constexpr int kQ = 64;           // steps per chunk
 constexpr int kP = 64;           // head dimension
-constexpr int kSsdThreads = 128;  // 4 warps: warp w owns rows 16w..16w+15 of a chunk, 32w..32w+31 of S
+constexpr int kSsdThreads = 128;  // 4 warps, one per quarter of the tensor-memory lanes
 constexpr int kTileBytes = 64 * 128;  // one 64 x 64 bf16 box (128-byte rows)
 
 struct SsdParams {
@@ -58,24 +60,6 @@ struct SsdParams {
 // chunk index is XORed with the row's position in its 8-row group)
 __device__ __forceinline__ uint32_t swz(int r, int c8) { return (uint32_t)(r * 128 + ((c8 ^ (r & 7)) << 4)); }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-// d += a (16 x 16, row) * b (16 x 8, col), bf16 operands, f32 accumulators
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -85,7 +69,7 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t v) {
 }
 __device__ __forceinline__ float fast_exp(float x) { return ex2_approx(x * kLog2e); }
 
-// ---- tcgen05 (5th-generation tensor core) helpers for the state update
+// ---- tcgen05 (5th-generation tensor core) helpers
 // Shared-memory matrix descriptor of a 128-byte-swizzled operand: start
 // address, leading-dimension byte offset (between 64-element blocks of the
 // M/N dimension for an MN-major operand), stride byte offset (between 8-row
@@ -94,10 +78,6 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo
   return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
-// Instruction descriptor, kind::f16: f32 accumulator, bf16 A and B, both
-// MN-major, N = 64, M = 128.
-constexpr uint32_t kUmmaIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) | ((64u >> 3) << 17) |
-                                ((128u >> 4) << 24);
 // D[tmem] (+)= A (smem) x B (smem), issued by one thread
 __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
@@ -118,18 +98,31 @@ __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.p
 template <int N>
 struct SsdSmem {
   static constexpr int NT = N / 64;                    // 64-column boxes of Bm / Cm
-  static constexpr int kX = 0;                         // x box [64 s][64 p]
+  static constexpr int kX = 0;                         // x box [64 s][64 p] (x' in place)
   static constexpr int kBo = kTileBytes;               // Bm boxes [NT][64 s][64 n]
   static constexpr int kCo = kBo + NT * kTileBytes;    // Cm boxes
   static constexpr int kBuf = kCo + NT * kTileBytes;   // one stage
-  static constexpr int kStage = 2 * kBuf;              // x' / y staging box [64][64]
-  static constexpr int kS = kStage + kTileBytes;       // S_in (bf16) [N n][64 p]
-  static constexpr int kVec = kS + N * 128;            // two sets of cum, delta, w*delta [3][64] f32 + decay
-  static constexpr int kBar = kVec + 2 * 4 * 64 * 4;   // three mbarriers and the TMEM address
-  static constexpr int kBytes = kBar + 64;
+  static constexpr int kM = 2 * kBuf;                  // masked C B^T, bf16 [64 t][64 s] (K-major)
+  static constexpr int kS = kM + kTileBytes;           // S_in (bf16) [N n][64 p] (MN-major)
+  static constexpr int kVec = kS + N * 128;            // two sets of decays (see `vec`)
+  static constexpr int kBar = kVec + 2 * 4 * 64 * 4;   // mbarriers and the TMEM address
+  static constexpr int kBytes = kBar + 128;
   static constexpr uint32_t kTx = (1 + 2 * NT) * kTileBytes;
-  static_assert(kBuf % 1024 == 0 && kStage % 1024 == 0 && kS % 1024 == 0, "swizzled boxes on 1024-byte boundaries");
+  static_assert(kBuf % 1024 == 0 && kM % 1024 == 0 && kS % 1024 == 0, "swizzled boxes on 1024-byte boundaries");
 };
+
+// TMEM columns of a CTA: the state S (N lanes x 64, f32), and three 64 x 64
+// accumulators of the chunk: G = C B^T, Y = M x, CS = C S_in.
+constexpr uint32_t kColS = 0, kColG = 64, kColY = 128, kColCS = 192, kTmemColsSsd = 256;
+
+// instruction descriptor, kind::f16: f32 D, bf16 A and B, M x 64
+__host__ __device__ constexpr uint32_t ssd_idesc(int m, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((64u >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+
+// TMEM lane of row r of an M = 64 accumulator: 16 rows in each warp's quarter
+__device__ __forceinline__ int m64_lane(int r) { return (r >> 4) * 32 + (r & 15); }
 
 template <int N>
 __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_constant__ SsdParams P) {
@@ -143,18 +136,15 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   // per chunk set (two sets, by chunk parity): (cum, delta) pairs of steps
   // [0, 64) interleaved [0, 128), w*delta [128, 192), e^(cum_end) [192]
   float* vec = reinterpret_cast<float*>(smem + SM::kVec);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBar);
-  uint64_t* mma_bar = full + 2;  // the state update's completion (tcgen05 path)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 3);
-  // N = 128: the state lives in tensor memory (128 lanes = rows n, 64 columns
-  // = p, f32) and its update S = e^(cum_end) S + B^T x' runs as tcgen05.mma;
-  // N = 64: in the accumulators of the four warps (mma.sync)
-  constexpr bool kUmma = N == 128;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBar);  // [2]: the stages' TMA copies
+  uint64_t* bar_g = full + 2;    // C B^T done
+  uint64_t* bar_ycs = full + 3;  // C S_in and M x done
+  uint64_t* bar_s = full + 4;    // the state update done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 5);
 
   const int b = blockIdx.x / P.H, h = blockIdx.x % P.H;
   const int g = h / (P.H / P.G);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gq = lane >> 2, cq = lane & 3;  // fragment row group, column pair
   const int nch = (P.L + kQ - 1) / kQ;
   const float A = -expf(P.A_log[h]);
   const float bias = P.dt_bias[h];
@@ -163,15 +153,24 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   if (tid == 0) {
     mbar_init(&full[0], 1);
     mbar_init(&full[1], 1);
-    mbar_init(mma_bar, 1);
+    mbar_init(bar_g, 1);
+    mbar_init(bar_ycs, 1);
+    mbar_init(bar_s, 1);
     fence_mbar_init();
   }
-  if (kUmma && warp == 0) tmem_alloc(tmem_slot, 64);
+  if (warp == 0) tmem_alloc(tmem_slot, kTmemColsSsd);
   tmem_fence_before_sync();
   __syncthreads();
   tmem_fence_after_sync();
-  const uint32_t tmem = kUmma ? *tmem_slot : 0u;
-  const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);  // this thread's lane (row n = tid)
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tquarter = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's lane quarter
+  // rows of the M = 64 accumulators (G, Y, CS) held by this thread: lanes 0..15 of each quarter
+  const bool has_row = lane < 16;
+  const int row = 16 * warp + (lane & 15);
+  // rows of S: N = 128 -> row n = tid (every lane); N = 64 -> the M = 64 layout
+  const bool has_srow = N == 128 || has_row;
+  const int srow = N == 128 ? tid : row;
+
   auto issue = [&](int c) {  // chunk c's boxes into stage c & 1 (one thread)
     const int s = c & 1;
     unsigned char* st = smem + s * SM::kBuf;
@@ -189,64 +188,43 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     if (nch > 1) issue(1);
   }
 
-  // the state (mma.sync path): warp w holds rows n = 32w + 16 mt + {gq, gq + 8}, columns p = 8 j + 2 cq + {0, 1}
-  constexpr int kMT = N / 64;  // 16-row tiles of S per warp (N / 4 rows per warp)
-  float S[kMT][8][4];  // (unused on the tcgen05 path)
-  // tcgen05 path: thread tid owns row n = tid of S (one TMEM lane, 64 columns)
-  auto row_to_smem_bf16 = [&](const float (&v)[64]) {  // S_in for the next readout, [n][p] swizzled
-#pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8)
-      *reinterpret_cast<uint4*>(smem + SM::kS + swz(tid, c8)) =
-          make_uint4(pack_bf16(v[8 * c8], v[8 * c8 + 1]), pack_bf16(v[8 * c8 + 2], v[8 * c8 + 3]),
-                     pack_bf16(v[8 * c8 + 4], v[8 * c8 + 5]), pack_bf16(v[8 * c8 + 6], v[8 * c8 + 7]));
-  };
-  auto tmem_row_ld = [&](float (&v)[64]) {
+  auto ld64 = [&](uint32_t col, float (&v)[64]) {  // 64 columns of this thread's lane
     float a[32], c[32];
-    tmem_ld32(trow, a);
-    tmem_ld32(trow + 32u, c);
+    __syncwarp();
+    tmem_ld32(tquarter + col, a);
+    tmem_ld32(tquarter + col + 32u, c);
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = a[i], v[32 + i] = c[i];
   };
-  auto tmem_row_st = [&](const float (&v)[64]) {
+  auto st64 = [&](uint32_t col, const float (&v)[64]) {
     float a[32], c[32];
+    __syncwarp();
 #pragma unroll
     for (int i = 0; i < 32; ++i) a[i] = v[i], c[i] = v[32 + i];
-    tmem_st32(trow, a);
-    tmem_st32(trow + 32u, c);
+    tmem_st32(tquarter + col, a);
+    tmem_st32(tquarter + col + 32u, c);
   };
-  if constexpr (kUmma) {
+  // a 64-element bf16 row into a 128B-swizzled [rows][64] image
+  auto row_to_smem = [&](uint32_t off, int r, const float (&v)[64]) {
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8)
+      *reinterpret_cast<uint4*>(smem + off + swz(r, c8)) =
+          make_uint4(pack_bf16(v[8 * c8], v[8 * c8 + 1]), pack_bf16(v[8 * c8 + 2], v[8 * c8 + 3]),
+                     pack_bf16(v[8 * c8 + 4], v[8 * c8 + 5]), pack_bf16(v[8 * c8 + 6], v[8 * c8 + 7]));
+  };
+
+  // the initial state: S (TMEM, f32) and its bf16 copy for the first readout
+  {
     float v[64];
-    const float* h0 = P.h0 ? P.h0 + (((size_t)b * P.H + h) * N + tid) * kP : nullptr;
+    const float* h0 = (P.h0 && has_srow) ? P.h0 + (((size_t)b * P.H + h) * N + srow) * kP : nullptr;
 #pragma unroll
     for (int i = 0; i < 64; ++i) v[i] = h0 ? h0[i] : 0.f;
-    row_to_smem_bf16(v);
-    tmem_row_st(v);
+    st64(kColS, v);
+    if (has_srow) row_to_smem(SM::kS, srow, v);
     tmem_wait_st();
-  } else {
-    const float* h0 = P.h0 ? P.h0 + ((size_t)b * P.H + h) * N * kP : nullptr;
-#pragma unroll
-    for (int mt = 0; mt < kMT; ++mt)
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int n = warp * (N / 4) + 16 * mt + gq + 8 * (e >> 1), p = 8 * j + 2 * cq + (e & 1);
-          S[mt][j][e] = h0 ? h0[(size_t)n * kP + p] : 0.f;
-        }
+    fence_proxy_async_smem();
+    tmem_fence_before_sync();
   }
-  auto store_S_bf16 = [&]() {  // S_in for the next chunk's readout, [n][p] swizzled
-#pragma unroll
-    for (int mt = 0; mt < kMT; ++mt)
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int hlf = 0; hlf < 2; ++hlf) {
-          const int n = warp * (N / 4) + 16 * mt + gq + 8 * hlf;
-          *reinterpret_cast<uint32_t*>(smem + SM::kS + swz(n, j) + 4 * cq) =
-              pack_bf16(S[mt][j][2 * hlf], S[mt][j][2 * hlf + 1]);
-        }
-  };
-  if constexpr (!kUmma) store_S_bf16();
 
   // Warp 0 reads each chunk's dt one chunk ahead (two steps per lane) and,
   // during the state update of the chunk before, turns them into delta, the
@@ -278,7 +256,6 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     }
     const float end = __shfl_sync(0xffffffffu, run, 31);
     const float c1 = run, c0 = run - a2[1];
-    // (cum, delta) of steps 2 lane and 2 lane + 1 side by side: one 16-byte read per pair
     *reinterpret_cast<float4*>(v + 4 * lane) = make_float4(c0, d2[0], c1, d2[1]);
     v[128 + 2 * lane] = fast_exp(end - c0) * d2[0];
     v[128 + 2 * lane + 1] = fast_exp(end - c1) * d2[1];
@@ -291,219 +268,157 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   }
   __syncthreads();
 
+  constexpr uint32_t kIdG = ssd_idesc(64, false, false);   // C (K-major) x B^T (K-major rows of Bm)
+  constexpr uint32_t kIdKM = ssd_idesc(64, false, true);   // K-major A x MN-major B: C S_in, M x
+  constexpr uint32_t kIdS = ssd_idesc(N, true, true);      // B^T (MN-major) x x' (MN-major)
+  int done = -1;  // the last chunk walked completely
   for (int c = 0; c < nch; ++c) {
     const int s = c & 1;
     const int t0 = c * kQ;
-    const bool ok = mbar_wait(&full[s], (c >> 1) & 1, P.status);
+    const uint32_t ph = (uint32_t)(c & 1);
+    const bool ok = mbar_wait(&full[s], (uint32_t)((c >> 1) & 1), P.status);
     if (__syncthreads_or(!ok)) break;  // the copy never came: stop, uniformly
     unsigned char* st = smem + s * SM::kBuf;
     const uint32_t xs = base + s * SM::kBuf + SM::kX;
     const uint32_t bs = base + s * SM::kBuf + SM::kBo;
     const uint32_t cs = base + s * SM::kBuf + SM::kCo;
-    const uint32_t ss = base + SM::kS;
     const float* cum = vec + s * 256;  // cum of step t at cum[2 t], delta at cum[2 t + 1]
     const float* wd = cum + 128;
-    if constexpr (kUmma) {  // S_in in TMEM takes the chunk's decay before the update accumulates onto it
+
+    // ---- G = C B^T and CS = C S_in on the tensor core (one thread)
+    if (tid == 0) {
+      tmem_fence_after_sync();
+#pragma unroll
+      for (int k = 0; k < N / 16; ++k) {  // K = n, 16 at a time, 32 bytes into a 128-byte row
+        const uint32_t ko = (uint32_t)((k / 4) * kTileBytes + (k % 4) * 32);
+        umma_f16(tmem + kColG, umma_desc_sw128(cs + ko, 16u, 1024u), umma_desc_sw128(bs + ko, 16u, 1024u), kIdG,
+                 k > 0 ? 1u : 0u);
+      }
+      umma_commit(bar_g);
+#pragma unroll
+      for (int k = 0; k < N / 16; ++k) {  // B = S_in [n][p]: 16 rows of n per K step
+        const uint32_t ko = (uint32_t)((k / 4) * kTileBytes + (k % 4) * 32);
+        umma_f16(tmem + kColCS, umma_desc_sw128(cs + ko, 16u, 1024u),
+                 umma_desc_sw128(base + SM::kS + (uint32_t)k * 2048u, (uint32_t)kTileBytes, 1024u), kIdKM,
+                 k > 0 ? 1u : 0u);
+      }
+    }
+    // ---- the chunk's decay on S (TMEM), while the tensor core works
+    {
+      const float dec0 = cum[192];
       tmem_fence_after_sync();
       float v[64];
-      tmem_row_ld(v);
-      const float dec0 = cum[192];
+      ld64(kColS, v);
 #pragma unroll
       for (int i = 0; i < 64; ++i) v[i] *= dec0;
-      tmem_row_st(v);
+      st64(kColS, v);
       tmem_wait_st();
-      tmem_fence_before_sync();
     }
-
-    // ---- y rows 16w .. 16w+15: (C B^T o L)(delta x) + e^cum (C S_in) + D x
-    const int r0 = 16 * warp;
-    float G[8][4], CS[8][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) G[j][e] = CS[j][e] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < N / 16; ++kk) {
-      const int k0 = 16 * kk;
-      const int sub = k0 / 64, kc = (k0 % 64) / 8;
-      uint32_t a[4];
-      ldsm_x4(cs + sub * kTileBytes + swz(r0 + (lane & 7) + 8 * ((lane >> 3) & 1), kc + (lane >> 4)), a);
-      // C B^T: only the s blocks at or below this warp's rows
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        if (jj > warp) break;
-        uint32_t bb[4];
-        ldsm_x4(bs + sub * kTileBytes + swz(16 * jj + (lane & 7) + 8 * (lane >> 4), kc + ((lane >> 3) & 1)), bb);
-        mma16816(G[2 * jj], a, bb[0], bb[1]);
-        mma16816(G[2 * jj + 1], a, bb[2], bb[3]);
-      }
-      // C S_in
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        uint32_t bb[4];
-        ldsm_x4_t(ss + swz(k0 + (lane & 7) + 8 * ((lane >> 3) & 1), 2 * jj + (lane >> 4)), bb);
-        mma16816(CS[2 * jj], a, bb[0], bb[1]);
-        mma16816(CS[2 * jj + 1], a, bb[2], bb[3]);
-      }
-    }
-    // mask and scale: M[t][s] = G[t][s] e^(cum_t - cum_s) delta_s for s <= t
-    const int ta = r0 + gq, tb = ta + 8;
-    const float cta = cum[2 * ta], ctb = cum[2 * tb];
-    uint32_t M[4][4];  // A operand of (M)(x): k block kk2 = s in [16 kk2, 16 kk2 + 16)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int s0 = 8 * j + 2 * cq;
-      const float4 cd = *reinterpret_cast<const float4*>(cum + 2 * s0);  // steps s0, s0 + 1
-      float m[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int t = (e < 2) ? ta : tb;
-        const int sx = s0 + (e & 1);
-        const float ct = (e < 2) ? cta : ctb;
-        const float cs_ = (e & 1) ? cd.z : cd.x, ds_ = (e & 1) ? cd.w : cd.y;
-        m[e] = (sx <= t) ? G[j][e] * fast_exp(ct - cs_) * ds_ : 0.f;
-      }
-      M[j >> 1][(j & 1) * 2] = pack_bf16(m[0], m[1]);
-      M[j >> 1][(j & 1) * 2 + 1] = pack_bf16(m[2], m[3]);
-    }
-    float Y[8][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) Y[j][e] = 0.f;
-#pragma unroll
-    for (int kk2 = 0; kk2 < 4; ++kk2) {
-      if (kk2 > warp) break;
-      const uint32_t a[4] = {M[kk2][0], M[kk2][1], M[kk2][2], M[kk2][3]};
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        uint32_t bb[4];
-        ldsm_x4_t(xs + swz(16 * kk2 + (lane & 7) + 8 * ((lane >> 3) & 1), 2 * jj + (lane >> 4)), bb);
-        mma16816(Y[2 * jj], a, bb[0], bb[1]);
-        mma16816(Y[2 * jj + 1], a, bb[2], bb[3]);
-      }
-    }
-    const float eta = fast_exp(cta), etb = fast_exp(ctb);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float2 xa = unpack_bf16(*reinterpret_cast<const uint32_t*>(st + SM::kX + swz(ta, j) + 4 * cq));
-      const float2 xb = unpack_bf16(*reinterpret_cast<const uint32_t*>(st + SM::kX + swz(tb, j) + 4 * cq));
-      const float y0 = Y[j][0] + eta * CS[j][0] + Dh * xa.x;
-      const float y1 = Y[j][1] + eta * CS[j][1] + Dh * xa.y;
-      const float y2 = Y[j][2] + etb * CS[j][2] + Dh * xb.x;
-      const float y3 = Y[j][3] + etb * CS[j][3] + Dh * xb.y;
-      *reinterpret_cast<uint32_t*>(smem + SM::kStage + swz(ta, j) + 4 * cq) = pack_bf16(y0, y1);
-      *reinterpret_cast<uint32_t*>(smem + SM::kStage + swz(tb, j) + 4 * cq) = pack_bf16(y2, y3);
-    }
-    __syncthreads();  // y rows staged; every read of x done
-    // the chunk's y rows to global memory (16 bytes per thread and pass), and
-    // x' = w o delta x in place of x
+    // ---- M[t][s] = G[t][s] e^(cum_t - cum_s) delta_s for s <= t, as bf16 (K-major A of M x)
+    mbar_wait(bar_g, ph, P.status);
+    tmem_fence_after_sync();
     {
-      __nv_bfloat16* yb = P.y + ((size_t)b * P.L) * P.H * kP + (size_t)h * kP;
+      float v[64];
+      ld64(kColG, v);
+      if (has_row) {
+        const float ct = cum[2 * row];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int q = tid + kSsdThreads * i;  // 512 chunks of 16 bytes
-        const int row = q >> 3, c8 = q & 7;
-        if (t0 + row < P.L) {
-          const uint4 v = *reinterpret_cast<const uint4*>(smem + SM::kStage + swz(row, c8));
-          *reinterpret_cast<uint4*>(yb + (size_t)(t0 + row) * P.H * kP + 8 * c8) = v;
+        for (int s2 = 0; s2 < 32; ++s2) {
+          const float4 cd = *reinterpret_cast<const float4*>(cum + 4 * s2);  // steps 2 s2, 2 s2 + 1
+          const int sa = 2 * s2, sb2 = 2 * s2 + 1;
+          v[sa] = sa <= row ? v[sa] * fast_exp(ct - cd.x) * cd.y : 0.f;
+          v[sb2] = sb2 <= row ? v[sb2] * fast_exp(ct - cd.z) * cd.w : 0.f;
         }
-        const float f = wd[row];
-        const uint4 xv = *reinterpret_cast<const uint4*>(st + SM::kX + swz(row, c8));
-        const uint32_t in[4] = {xv.x, xv.y, xv.z, xv.w};
-        uint32_t out[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 e = unpack_bf16(in[k]);
-          out[k] = pack_bf16(f * e.x, f * e.y);
-        }
-        *reinterpret_cast<uint4*>(st + SM::kX + swz(row, c8)) = make_uint4(out[0], out[1], out[2], out[3]);
+        row_to_smem(SM::kM, row, v);
       }
     }
-    if constexpr (kUmma) fence_proxy_async_smem();  // x' is read by the tensor core
-    __syncthreads();
-    // ---- S = e^(cum_end) S + B^T x'
-    if constexpr (kUmma) {
-      // one thread issues the 128 x 64 x 64 product as four K = 16 steps:
-      // A = B^T from the Bm boxes (MN-major: n contiguous, the two 64-column
-      // boxes 8 KB apart), B = x' (MN-major), D = S in TMEM (already scaled)
-      if (tid == 0) {
-        tmem_fence_after_sync();
+    fence_proxy_async_smem();
+    tmem_fence_before_sync();
+    __syncthreads();  // M complete; S scaled
+    // ---- Y = M x
+    if (tid == 0) {
+      tmem_fence_after_sync();
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t da = umma_desc_sw128(bs + kk * 2048u, kTileBytes, 1024u);
-          const uint64_t db = umma_desc_sw128(xs + kk * 2048u, kTileBytes, 1024u);
-          umma_f16(tmem, da, db, kUmmaIdesc, 1u);
-        }
-        umma_commit(mma_bar);
-      }
-    } else {  // warp w: rows n = 16 w .. 16 w + 15 of S (N = 64)
-      const float dec = cum[192];
+      for (int k = 0; k < 4; ++k)  // K = s
+        umma_f16(tmem + kColY, umma_desc_sw128(base + SM::kM + (uint32_t)k * 32u, 16u, 1024u),
+                 umma_desc_sw128(xs + (uint32_t)k * 2048u, (uint32_t)kTileBytes, 1024u), kIdKM, k > 0 ? 1u : 0u);
+      umma_commit(bar_ycs);
+    }
+    // ---- y = Y + e^cum CS + D x for this thread's row; then x' = w delta x in place
+    mbar_wait(bar_ycs, ph, P.status);
+    tmem_fence_after_sync();
+    {
+      const float et = fast_exp(cum[2 * row]);
+      const float w = wd[row];
+      const bool store = has_row && t0 + row < P.L;
+      __nv_bfloat16* yrow = P.y + (((size_t)b * P.L + t0 + row) * P.H + h) * kP;
 #pragma unroll
-      for (int mt = 0; mt < kMT; ++mt)
+      for (int half = 0; half < 2; ++half) {  // 32 columns of p at a time
+        float yv[32], cv[32];
+        __syncwarp();
+        tmem_ld32(tquarter + kColY + 32u * half, yv);
+        tmem_ld32(tquarter + kColCS + 32u * half, cv);
+        if (has_row) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+          for (int q = 0; q < 4; ++q) {
+            const int c8 = 4 * half + q;
+            const uint4 xv = *reinterpret_cast<const uint4*>(st + SM::kX + swz(row, c8));
+            const uint32_t xin[4] = {xv.x, xv.y, xv.z, xv.w};
+            uint32_t yo[4], xo[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) S[mt][j][e] *= dec;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {  // s blocks
-        uint32_t bx[4][4];
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-          ldsm_x4_t(xs + swz(16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1), 2 * jj + (lane >> 4)), bx[jj]);
-#pragma unroll
-        for (int mt = 0; mt < kMT; ++mt) {
-          const int m0 = warp * (N / 4) + 16 * mt;  // rows n
-          const int sub = m0 / 64, mc = (m0 % 64) / 8;
-          uint32_t a[4];
-          ldsm_x4_t(bs + sub * kTileBytes + swz(16 * kk + (lane & 7) + 8 * (lane >> 4), mc + ((lane >> 3) & 1)), a);
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            mma16816(S[mt][2 * jj], a, bx[jj][0], bx[jj][1]);
-            mma16816(S[mt][2 * jj + 1], a, bx[jj][2], bx[jj][3]);
+            for (int k = 0; k < 4; ++k) {
+              const float2 xe = unpack_bf16(xin[k]);
+              const int j = 8 * q + 2 * k;
+              yo[k] = pack_bf16(yv[j] + et * cv[j] + Dh * xe.x, yv[j + 1] + et * cv[j + 1] + Dh * xe.y);
+              xo[k] = pack_bf16(w * xe.x, w * xe.y);
+            }
+            if (store) *reinterpret_cast<uint4*>(yrow + 8 * c8) = make_uint4(yo[0], yo[1], yo[2], yo[3]);
+            *reinterpret_cast<uint4*>(st + SM::kX + swz(row, c8)) = make_uint4(xo[0], xo[1], xo[2], xo[3]);
           }
         }
       }
+    }
+    fence_proxy_async_smem();
+    tmem_fence_before_sync();
+    __syncthreads();  // x' complete
+    // ---- S = e^(cum_end) S + B^T x'
+    if (tid == 0) {
+      tmem_fence_after_sync();
+#pragma unroll
+      for (int k = 0; k < 4; ++k)  // K = s
+        umma_f16(tmem + kColS, umma_desc_sw128(bs + (uint32_t)k * 2048u, (uint32_t)kTileBytes, 1024u),
+                 umma_desc_sw128(xs + (uint32_t)k * 2048u, (uint32_t)kTileBytes, 1024u), kIdS, 1u);
+      umma_commit(bar_s);
     }
     if (warp == 0 && c + 1 < nch) {  // the next chunk's decays; its successor's dt in flight
       chunk_decays(c + 1);
       load_dt(c + 2);
     }
-    if constexpr (kUmma) {
-      // the updated state: S_in of the next chunk's readout (bf16), or h_last
-      mbar_wait(mma_bar, (uint32_t)(c & 1), P.status);
-      tmem_fence_after_sync();
-      float v[64];
-      tmem_row_ld(v);
-      if (c + 1 < nch) {
-        row_to_smem_bf16(v);
-      } else if (P.h_last) {
-        float* hl = P.h_last + (((size_t)b * P.H + h) * N + tid) * kP;
-#pragma unroll
-        for (int i = 0; i < 64; i += 2) *reinterpret_cast<float2*>(hl + i) = make_float2(v[i], v[i + 1]);
-      }
-      tmem_fence_before_sync();
-    }
-    __syncthreads();  // every warp is done with S_in, the stage and x'
-    if constexpr (!kUmma) store_S_bf16();
-    if (tid == 0 && c + 2 < nch) issue(c + 2);
-  }
-  if constexpr (kUmma) {
-    __syncthreads();
+    // ---- the updated state: S_in of the next readout (bf16), or h_last
+    mbar_wait(bar_s, ph, P.status);
     tmem_fence_after_sync();
-    if (warp == 0) tmem_dealloc(tmem, 64);
-  } else if (P.h_last) {
-    float* hl = P.h_last + ((size_t)b * P.H + h) * N * kP;
+    {
+      float v[64];
+      ld64(kColS, v);
+      if (has_srow) {
+        if (c + 1 < nch) {
+          row_to_smem(SM::kS, srow, v);
+        } else if (P.h_last) {
+          float* hl = P.h_last + (((size_t)b * P.H + h) * N + srow) * kP;
 #pragma unroll
-    for (int mt = 0; mt < kMT; ++mt)
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int hlf = 0; hlf < 2; ++hlf) {
-          const int n = warp * (N / 4) + 16 * mt + gq + 8 * hlf, p = 8 * j + 2 * cq;
-          *reinterpret_cast<float2*>(hl + (size_t)n * kP + p) = make_float2(S[mt][j][2 * hlf], S[mt][j][2 * hlf + 1]);
+          for (int i = 0; i < 64; i += 2) *reinterpret_cast<float2*>(hl + i) = make_float2(v[i], v[i + 1]);
         }
+      }
+    }
+    fence_proxy_async_smem();
+    tmem_fence_before_sync();
+    __syncthreads();  // S_in complete; every product on this stage done
+    if (tid == 0 && c + 2 < nch) issue(c + 2);
+    done = c;
   }
+  (void)done;
+  tmem_fence_after_sync();
+  if (warp == 0) tmem_dealloc(tmem, kTmemColsSsd);
 }
 
 template <int N>
