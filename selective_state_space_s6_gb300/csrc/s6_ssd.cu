@@ -95,20 +95,35 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 // make this thread's generic-proxy shared-memory writes visible to the tensor core
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// 32 columns of 16 lanes in two halves: threads 0..15 read lanes
+// base .. base + 15 at columns col .. col + 31, threads 16..31 the same
+// lanes at columns col + 32 .. col + 63 (one warp, converged; waits)
+__device__ __forceinline__ void tmem_ld16x2(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32], 32;\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 template <int N>
 struct SsdSmem {
   static constexpr int NT = N / 64;                    // 64-column boxes of Bm / Cm
-  static constexpr int kX = 0;                         // x box [64 s][64 p] (x' in place)
+  static constexpr int kX = 0;                         // x box [64 s][64 p]
   static constexpr int kBo = kTileBytes;               // Bm boxes [NT][64 s][64 n]
-  static constexpr int kCo = kBo + NT * kTileBytes;    // Cm boxes
+  static constexpr int kCo = kBo + NT * kTileBytes;    // Cm boxes; M = (C B^T) o L o delta over box 0
   static constexpr int kBuf = kCo + NT * kTileBytes;   // one stage
-  static constexpr int kM = 2 * kBuf;                  // masked C B^T, bf16 [64 t][64 s] (K-major)
-  static constexpr int kS = kM + kTileBytes;           // S_in (bf16) [N n][64 p] (MN-major)
+  static constexpr int kXp = 2 * kBuf;                 // x' = w delta x, bf16 [64 s][64 p] (MN-major)
+  static constexpr int kS = kXp + kTileBytes;          // S_in (bf16) [N n][64 p] (MN-major)
   static constexpr int kVec = kS + N * 128;            // two sets of decays (see `vec`)
   static constexpr int kBar = kVec + 2 * 4 * 64 * 4;   // mbarriers and the TMEM address
   static constexpr int kBytes = kBar + 128;
   static constexpr uint32_t kTx = (1 + 2 * NT) * kTileBytes;
-  static_assert(kBuf % 1024 == 0 && kM % 1024 == 0 && kS % 1024 == 0, "swizzled boxes on 1024-byte boundaries");
+  static_assert(kBuf % 1024 == 0 && kXp % 1024 == 0 && kS % 1024 == 0, "swizzled boxes on 1024-byte boundaries");
 };
 
 // TMEM columns of a CTA: the state S (N lanes x 64, f32), and three 64 x 64
@@ -120,9 +135,6 @@ __host__ __device__ constexpr uint32_t ssd_idesc(int m, bool a_mn, bool b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((64u >> 3) << 17) |
          ((uint32_t)(m >> 4) << 24);
 }
-
-// TMEM lane of row r of an M = 64 accumulator: 16 rows in each warp's quarter
-__device__ __forceinline__ int m64_lane(int r) { return (r >> 4) * 32 + (r & 15); }
 
 template <int N>
 __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_constant__ SsdParams P) {
@@ -137,10 +149,9 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   // [0, 64) interleaved [0, 128), w*delta [128, 192), e^(cum_end) [192]
   float* vec = reinterpret_cast<float*>(smem + SM::kVec);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBar);  // [2]: the stages' TMA copies
-  uint64_t* bar_g = full + 2;    // C B^T done
-  uint64_t* bar_ycs = full + 3;  // C S_in and M x done
-  uint64_t* bar_s = full + 4;    // the state update done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 5);
+  uint64_t* bar_g = full + 2;  // C B^T and C S_in done
+  uint64_t* bar_y = full + 3;  // M x and the state update done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 4);
 
   const int b = blockIdx.x / P.H, h = blockIdx.x % P.H;
   const int g = h / (P.H / P.G);
@@ -154,8 +165,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     mbar_init(&full[0], 1);
     mbar_init(&full[1], 1);
     mbar_init(bar_g, 1);
-    mbar_init(bar_ycs, 1);
-    mbar_init(bar_s, 1);
+    mbar_init(bar_y, 1);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tmem_slot, kTmemColsSsd);
@@ -164,11 +174,12 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   tmem_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tquarter = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's lane quarter
-  // rows of the M = 64 accumulators (G, Y, CS) held by this thread: lanes 0..15 of each quarter
-  const bool has_row = lane < 16;
+  // The 64 x 64 accumulators (M = 64) keep row r in lane (r / 16) * 32 + r % 16;
+  // read in two halves, every thread holds 32 columns of one row.
   const int row = 16 * warp + (lane & 15);
+  const int hf = lane >> 4;  // columns [32 hf, 32 hf + 32)
   // rows of S: N = 128 -> row n = tid (every lane); N = 64 -> the M = 64 layout
-  const bool has_srow = N == 128 || has_row;
+  const bool has_srow = N == 128 || lane < 16;
   const int srow = N == 128 ? tid : row;
 
   auto issue = [&](int c) {  // chunk c's boxes into stage c & 1 (one thread)
@@ -204,32 +215,16 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     tmem_st32(tquarter + col, a);
     tmem_st32(tquarter + col + 32u, c);
   };
-  // a 64-element bf16 row into a 128B-swizzled [rows][64] image
-  auto row_to_smem = [&](uint32_t off, int r, const float (&v)[64]) {
-#pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8)
-      *reinterpret_cast<uint4*>(smem + off + swz(r, c8)) =
-          make_uint4(pack_bf16(v[8 * c8], v[8 * c8 + 1]), pack_bf16(v[8 * c8 + 2], v[8 * c8 + 3]),
-                     pack_bf16(v[8 * c8 + 4], v[8 * c8 + 5]), pack_bf16(v[8 * c8 + 6], v[8 * c8 + 7]));
+  // 8 consecutive values as one 16-byte unit of a 128B-swizzled [rows][64] bf16 image
+  auto put8 = [&](uint32_t off, int r, int c8, const float* v) {
+    *reinterpret_cast<uint4*>(smem + off + swz(r, c8)) =
+        make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
   };
 
-  // the initial state: S (TMEM, f32) and its bf16 copy for the first readout
-  {
-    float v[64];
-    const float* h0 = (P.h0 && has_srow) ? P.h0 + (((size_t)b * P.H + h) * N + srow) * kP : nullptr;
-#pragma unroll
-    for (int i = 0; i < 64; ++i) v[i] = h0 ? h0[i] : 0.f;
-    st64(kColS, v);
-    if (has_srow) row_to_smem(SM::kS, srow, v);
-    tmem_wait_st();
-    fence_proxy_async_smem();
-    tmem_fence_before_sync();
-  }
-
-  // Warp 0 reads each chunk's dt one chunk ahead (two steps per lane) and,
-  // during the state update of the chunk before, turns them into delta, the
-  // running sum of delta*A, the weights e^(cum_end - cum_s) delta_s and the
-  // chunk's total decay (set c & 1 of `vec`).
+  // Warp 0 reads each chunk's dt one chunk ahead (two steps per lane) and
+  // turns them into delta, the running sum of delta*A, the weights
+  // e^(cum_end - cum_s) delta_s and the chunk's total decay (set c & 1 of
+  // `vec`) while the tensor core works on the chunk before.
   float raw_next[2] = {0.f, 0.f};
   auto load_dt = [&](int c) {
 #pragma unroll
@@ -267,11 +262,41 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     load_dt(1);
   }
   __syncthreads();
+  // the initial state: S = e^(cum_end of chunk 0) h0 in TMEM (ready for the
+  // first update), h0 as bf16 for the first readout
+  {
+    float v[64];
+    const float* h0 = (P.h0 && has_srow) ? P.h0 + (((size_t)b * P.H + h) * N + srow) * kP : nullptr;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = h0 ? h0[i] : 0.f;
+    if (has_srow)
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) put8(SM::kS, srow, c8, v + 8 * c8);
+    const float dec0 = vec[192];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] *= dec0;
+    st64(kColS, v);
+    tmem_wait_st();
+    fence_proxy_async_smem();
+    tmem_fence_before_sync();
+  }
+  __syncthreads();
 
-  constexpr uint32_t kIdG = ssd_idesc(64, false, false);   // C (K-major) x B^T (K-major rows of Bm)
-  constexpr uint32_t kIdKM = ssd_idesc(64, false, true);   // K-major A x MN-major B: C S_in, M x
-  constexpr uint32_t kIdS = ssd_idesc(N, true, true);      // B^T (MN-major) x x' (MN-major)
-  int done = -1;  // the last chunk walked completely
+  constexpr uint32_t kIdG = ssd_idesc(64, false, false);  // C (K-major) x B^T (K-major rows of Bm)
+  constexpr uint32_t kIdKM = ssd_idesc(64, false, true);  // K-major A x MN-major B: C S_in, M x
+  constexpr uint32_t kIdS = ssd_idesc(N, true, true);     // B^T (MN-major) x x' (MN-major)
+  // G = C B^T of the chunk in stage s: K = n, 16 at a time, 32 bytes into a
+  // 128-byte row, the next 64 n one box on
+  auto issue_g = [&](int s) {
+    const uint32_t bs = base + s * SM::kBuf + SM::kBo, cs = base + s * SM::kBuf + SM::kCo;
+#pragma unroll
+    for (int k = 0; k < N / 16; ++k) {
+      const uint32_t ko = (uint32_t)((k / 4) * kTileBytes + (k % 4) * 32);
+      umma_f16(tmem + kColG, umma_desc_sw128(cs + ko, 16u, 1024u), umma_desc_sw128(bs + ko, 16u, 1024u), kIdG,
+               k > 0 ? 1u : 0u);
+    }
+  };
+  bool g_issued = false;  // thread 0: G of the next chunk already on the tensor core
   for (int c = 0; c < nch; ++c) {
     const int s = c & 1;
     const int t0 = c * kQ;
@@ -285,16 +310,10 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     const float* cum = vec + s * 256;  // cum of step t at cum[2 t], delta at cum[2 t + 1]
     const float* wd = cum + 128;
 
-    // ---- G = C B^T and CS = C S_in on the tensor core (one thread)
+    // ---- G = C B^T (unless already issued) and CS = C S_in (one thread)
     if (tid == 0) {
       tmem_fence_after_sync();
-#pragma unroll
-      for (int k = 0; k < N / 16; ++k) {  // K = n, 16 at a time, 32 bytes into a 128-byte row
-        const uint32_t ko = (uint32_t)((k / 4) * kTileBytes + (k % 4) * 32);
-        umma_f16(tmem + kColG, umma_desc_sw128(cs + ko, 16u, 1024u), umma_desc_sw128(bs + ko, 16u, 1024u), kIdG,
-                 k > 0 ? 1u : 0u);
-      }
-      umma_commit(bar_g);
+      if (!g_issued) issue_g(s);
 #pragma unroll
       for (int k = 0; k < N / 16; ++k) {  // B = S_in [n][p]: 16 rows of n per K step
         const uint32_t ko = (uint32_t)((k / 4) * kTileBytes + (k % 4) * 32);
@@ -302,121 +321,121 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
                  umma_desc_sw128(base + SM::kS + (uint32_t)k * 2048u, (uint32_t)kTileBytes, 1024u), kIdKM,
                  k > 0 ? 1u : 0u);
       }
+      umma_commit(bar_g);
     }
-    // ---- the chunk's decay on S (TMEM), while the tensor core works
-    {
-      const float dec0 = cum[192];
-      tmem_fence_after_sync();
-      float v[64];
-      ld64(kColS, v);
-#pragma unroll
-      for (int i = 0; i < 64; ++i) v[i] *= dec0;
-      st64(kColS, v);
-      tmem_wait_st();
-    }
-    // ---- M[t][s] = G[t][s] e^(cum_t - cum_s) delta_s for s <= t, as bf16 (K-major A of M x)
-    mbar_wait(bar_g, ph, P.status);
-    tmem_fence_after_sync();
-    {
-      float v[64];
-      ld64(kColG, v);
-      if (has_row) {
-        const float ct = cum[2 * row];
-#pragma unroll
-        for (int s2 = 0; s2 < 32; ++s2) {
-          const float4 cd = *reinterpret_cast<const float4*>(cum + 4 * s2);  // steps 2 s2, 2 s2 + 1
-          const int sa = 2 * s2, sb2 = 2 * s2 + 1;
-          v[sa] = sa <= row ? v[sa] * fast_exp(ct - cd.x) * cd.y : 0.f;
-          v[sb2] = sb2 <= row ? v[sb2] * fast_exp(ct - cd.z) * cd.w : 0.f;
-        }
-        row_to_smem(SM::kM, row, v);
-      }
-    }
-    fence_proxy_async_smem();
-    tmem_fence_before_sync();
-    __syncthreads();  // M complete; S scaled
-    // ---- Y = M x
-    if (tid == 0) {
-      tmem_fence_after_sync();
-#pragma unroll
-      for (int k = 0; k < 4; ++k)  // K = s
-        umma_f16(tmem + kColY, umma_desc_sw128(base + SM::kM + (uint32_t)k * 32u, 16u, 1024u),
-                 umma_desc_sw128(xs + (uint32_t)k * 2048u, (uint32_t)kTileBytes, 1024u), kIdKM, k > 0 ? 1u : 0u);
-      umma_commit(bar_ycs);
-    }
-    // ---- y = Y + e^cum CS + D x for this thread's row; then x' = w delta x in place
-    mbar_wait(bar_ycs, ph, P.status);
-    tmem_fence_after_sync();
-    {
-      const float et = fast_exp(cum[2 * row]);
-      const float w = wd[row];
-      const bool store = has_row && t0 + row < P.L;
-      __nv_bfloat16* yrow = P.y + (((size_t)b * P.L + t0 + row) * P.H + h) * kP;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {  // 32 columns of p at a time
-        float yv[32], cv[32];
-        __syncwarp();
-        tmem_ld32(tquarter + kColY + 32u * half, yv);
-        tmem_ld32(tquarter + kColCS + 32u * half, cv);
-        if (has_row) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int c8 = 4 * half + q;
-            const uint4 xv = *reinterpret_cast<const uint4*>(st + SM::kX + swz(row, c8));
-            const uint32_t xin[4] = {xv.x, xv.y, xv.z, xv.w};
-            uint32_t yo[4], xo[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float2 xe = unpack_bf16(xin[k]);
-              const int j = 8 * q + 2 * k;
-              yo[k] = pack_bf16(yv[j] + et * cv[j] + Dh * xe.x, yv[j + 1] + et * cv[j + 1] + Dh * xe.y);
-              xo[k] = pack_bf16(w * xe.x, w * xe.y);
-            }
-            if (store) *reinterpret_cast<uint4*>(yrow + 8 * c8) = make_uint4(yo[0], yo[1], yo[2], yo[3]);
-            *reinterpret_cast<uint4*>(st + SM::kX + swz(row, c8)) = make_uint4(xo[0], xo[1], xo[2], xo[3]);
-          }
-        }
-      }
-    }
-    fence_proxy_async_smem();
-    tmem_fence_before_sync();
-    __syncthreads();  // x' complete
-    // ---- S = e^(cum_end) S + B^T x'
-    if (tid == 0) {
-      tmem_fence_after_sync();
-#pragma unroll
-      for (int k = 0; k < 4; ++k)  // K = s
-        umma_f16(tmem + kColS, umma_desc_sw128(bs + (uint32_t)k * 2048u, (uint32_t)kTileBytes, 1024u),
-                 umma_desc_sw128(xs + (uint32_t)k * 2048u, (uint32_t)kTileBytes, 1024u), kIdS, 1u);
-      umma_commit(bar_s);
-    }
-    if (warp == 0 && c + 1 < nch) {  // the next chunk's decays; its successor's dt in flight
+    // the next chunk's decays; its successor's dt in flight
+    if (warp == 0 && c + 1 < nch) {
       chunk_decays(c + 1);
       load_dt(c + 2);
     }
-    // ---- the updated state: S_in of the next readout (bf16), or h_last
-    mbar_wait(bar_s, ph, P.status);
+    // ---- x' = w delta x (state-update operand) and, once G is there,
+    // M[t][s] = G[t][s] e^(cum_t - cum_s) delta_s for s <= t as bf16 over Cm box 0
+    {
+      const float w = wd[row];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c8 = 4 * hf + q;
+        const uint4 xv = *reinterpret_cast<const uint4*>(st + SM::kX + swz(row, c8));
+        const uint32_t xin[4] = {xv.x, xv.y, xv.z, xv.w};
+        uint32_t xo[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 xe = unpack_bf16(xin[k]);
+          xo[k] = pack_bf16(w * xe.x, w * xe.y);
+        }
+        *reinterpret_cast<uint4*>(smem + SM::kXp + swz(row, c8)) = make_uint4(xo[0], xo[1], xo[2], xo[3]);
+      }
+    }
+    mbar_wait(bar_g, ph, P.status);
     tmem_fence_after_sync();
+    {
+      float v[32];
+      __syncwarp();
+      tmem_ld16x2(tquarter + kColG, v);
+      const float ct = cum[2 * row];
+      const int s0 = 32 * hf;
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const float4 cd = *reinterpret_cast<const float4*>(cum + 2 * (s0 + j));  // steps s0 + j, s0 + j + 1
+        v[j] = s0 + j <= row ? v[j] * fast_exp(ct - cd.x) * cd.y : 0.f;
+        v[j + 1] = s0 + j + 1 <= row ? v[j + 1] * fast_exp(ct - cd.z) * cd.w : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) put8(SM::kCo + s * SM::kBuf, row, 4 * hf + q, v + 8 * q);
+    }
+    fence_proxy_async_smem();
+    tmem_fence_before_sync();
+    __syncthreads();  // M and x' complete; decays of the next chunk published
+    // ---- Y = M x and S += B^T x' (S already carries this chunk's decay);
+    // then the next chunk's G as soon as its boxes are in
+    if (tid == 0) {
+      tmem_fence_after_sync();
+#pragma unroll
+      for (int k = 0; k < 4; ++k)  // K = s
+        umma_f16(tmem + kColY, umma_desc_sw128(cs + (uint32_t)k * 32u, 16u, 1024u),
+                 umma_desc_sw128(xs + (uint32_t)k * 2048u, (uint32_t)kTileBytes, 1024u), kIdKM, k > 0 ? 1u : 0u);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        umma_f16(tmem + kColS, umma_desc_sw128(bs + (uint32_t)k * 2048u, (uint32_t)kTileBytes, 1024u),
+                 umma_desc_sw128(base + SM::kXp + (uint32_t)k * 2048u, (uint32_t)kTileBytes, 1024u), kIdS, 1u);
+      umma_commit(bar_y);
+      g_issued = false;
+      if (c + 1 < nch && mbar_wait(&full[s ^ 1], (uint32_t)(((c + 1) >> 1) & 1), P.status)) {
+        issue_g(s ^ 1);
+        g_issued = true;
+      }
+    }
+    mbar_wait(bar_y, ph, P.status);
+    tmem_fence_after_sync();
+    // ---- y = Y + e^cum CS + D x for this thread's row and half
+    {
+      float yv[32], cv[32];
+      __syncwarp();
+      tmem_ld16x2(tquarter + kColY, yv);
+      tmem_ld16x2(tquarter + kColCS, cv);
+      const float et = fast_exp(cum[2 * row]);
+      __nv_bfloat16* yrow = P.y + (((size_t)b * P.L + t0 + row) * P.H + h) * kP;
+      const bool store = t0 + row < P.L;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c8 = 4 * hf + q;
+        const uint4 xv = *reinterpret_cast<const uint4*>(st + SM::kX + swz(row, c8));
+        const uint32_t xin[4] = {xv.x, xv.y, xv.z, xv.w};
+        uint32_t yo[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 xe = unpack_bf16(xin[k]);
+          const int j = 8 * q + 2 * k;
+          yo[k] = pack_bf16(yv[j] + et * cv[j] + Dh * xe.x, yv[j + 1] + et * cv[j + 1] + Dh * xe.y);
+        }
+        if (store) *reinterpret_cast<uint4*>(yrow + 8 * c8) = make_uint4(yo[0], yo[1], yo[2], yo[3]);
+      }
+    }
+    // ---- the state after the chunk: S_in of the next readout (bf16) and,
+    // scaled by the next chunk's decay, back into TMEM; or h_last
     {
       float v[64];
       ld64(kColS, v);
-      if (has_srow) {
-        if (c + 1 < nch) {
-          row_to_smem(SM::kS, srow, v);
-        } else if (P.h_last) {
-          float* hl = P.h_last + (((size_t)b * P.H + h) * N + srow) * kP;
+      if (c + 1 < nch) {
+        if (has_srow)
 #pragma unroll
-          for (int i = 0; i < 64; i += 2) *reinterpret_cast<float2*>(hl + i) = make_float2(v[i], v[i + 1]);
-        }
+          for (int c8 = 0; c8 < 8; ++c8) put8(SM::kS, srow, c8, v + 8 * c8);
+        const float dec1 = vec[(s ^ 1) * 256 + 192];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) v[i] *= dec1;
+        st64(kColS, v);
+        tmem_wait_st();
+      } else if (P.h_last && has_srow) {
+        float* hl = P.h_last + (((size_t)b * P.H + h) * N + srow) * kP;
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) *reinterpret_cast<float2*>(hl + i) = make_float2(v[i], v[i + 1]);
       }
     }
     fence_proxy_async_smem();
     tmem_fence_before_sync();
     __syncthreads();  // S_in complete; every product on this stage done
     if (tid == 0 && c + 2 < nch) issue(c + 2);
-    done = c;
   }
-  (void)done;
   tmem_fence_after_sync();
   if (warp == 0) tmem_dealloc(tmem, kTmemColsSsd);
 }
