@@ -140,6 +140,8 @@ template <int N>
 __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_constant__ SsdParams P) {
   using SM = SsdSmem<N>;
   constexpr int NT = SM::NT;
+  const int nch = (P.L + kQ - 1) / kQ;
+  if (nch == 0) return;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // the 128B swizzle repeats every 1024 bytes: align the base
   const uint32_t raw = smem_u32(smem_raw);
@@ -149,21 +151,26 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   // [0, 64) interleaved [0, 128), w*delta [128, 192), e^(cum_end) [192]
   float* vec = reinterpret_cast<float*>(smem + SM::kVec);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBar);  // [2]: the stages' TMA copies
-  uint64_t* bar_g = full + 2;  // C B^T and C S_in done
-  uint64_t* bar_y = full + 3;  // M x and the state update done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 4);
+  uint64_t* bar_cs = full + 2;  // C S_in done
+  uint64_t* bar_g = full + 3;   // C B^T done
+  uint64_t* bar_y = full + 4;   // M x and the state update done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 5);
 
   const int b = blockIdx.x / P.H, h = blockIdx.x % P.H;
   const int g = h / (P.H / P.G);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nch = (P.L + kQ - 1) / kQ;
   const float A = -expf(P.A_log[h]);
   const float bias = P.dt_bias[h];
   const float Dh = P.Dp[h];
+  // Roles beside the shared row work: thread 0 issues C S_in, M x and the
+  // state update; thread 32 issues C B^T one chunk ahead; thread 64 issues
+  // the TMA copies; warp 3 computes the decays one chunk ahead.
+  constexpr int kTidMma = 0, kTidG = 32, kTidTma = 64, kWarpDecay = 3;
 
-  if (tid == 0) {
+  if (tid == kTidMma) {
     mbar_init(&full[0], 1);
     mbar_init(&full[1], 1);
+    mbar_init(bar_cs, 1);
     mbar_init(bar_g, 1);
     mbar_init(bar_y, 1);
     fence_mbar_init();
@@ -193,10 +200,9 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
       tma_load_3d(st + SM::kCo + j * kTileBytes, &P.map_C, &full[s], g * N + 64 * j, c * kQ, b);
     }
   };
-  if (tid == 0) {
+  if (tid == kTidTma) {
     tma_prefetch_desc(&P.map_x);
-    if (nch > 0) issue(0);
-    if (nch > 1) issue(1);
+    issue(0);
   }
 
   auto ld64 = [&](uint32_t col, float (&v)[64]) {  // 64 columns of this thread's lane
@@ -221,16 +227,18 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
         make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
   };
 
-  // Warp 0 reads each chunk's dt one chunk ahead (two steps per lane) and
-  // turns them into delta, the running sum of delta*A, the weights
-  // e^(cum_end - cum_s) delta_s and the chunk's total decay (set c & 1 of
-  // `vec`) while the tensor core works on the chunk before.
-  float raw_next[2] = {0.f, 0.f};
+  // The decay warp reads each chunk's dt one chunk ahead (two steps per
+  // lane; the raw bits stay untouched until they are used, so the load's
+  // latency hides behind a whole chunk) and turns them into delta, the
+  // running sum of delta*A, the weights e^(cum_end - cum_s) delta_s and the
+  // chunk's total decay (set c & 1 of `vec`).
+  const unsigned short* dt_bits = reinterpret_cast<const unsigned short*>(P.dt_raw);
+  unsigned short raw_next[2] = {0, 0};
   auto load_dt = [&](int c) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      const int t = c * kQ + 2 * lane + i;
-      raw_next[i] = (c < nch && t < P.L) ? __bfloat162float(P.dt_raw[((size_t)b * P.L + t) * P.H + h]) : 0.f;
+      const int t = min(c * kQ + 2 * lane + i, P.L - 1);  // past the end: any valid step, masked later
+      raw_next[i] = dt_bits[((size_t)b * P.L + t) * P.H + h];
     }
   };
   auto chunk_decays = [&](int c) {
@@ -239,7 +247,8 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int t = c * kQ + 2 * lane + i;
-      const float d = t < P.L ? clamp_dt(softplus_fast(raw_next[i] + bias), P.dt_min, P.dt_max) : 0.f;
+      const float r = __bfloat162float(__ushort_as_bfloat16(raw_next[i]));
+      const float d = t < P.L ? clamp_dt(softplus_fast(r + bias), P.dt_min, P.dt_max) : 0.f;
       d2[i] = d;
       a2[i] = d * A;
     }
@@ -256,12 +265,43 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     v[128 + 2 * lane + 1] = fast_exp(end - c1) * d2[1];
     if (lane == 0) v[192] = fast_exp(end);
   };
-  if (warp == 0) {
+  if (warp == kWarpDecay) {
     load_dt(0);
     chunk_decays(0);
     load_dt(1);
   }
-  __syncthreads();
+
+  // Shared-memory matrix descriptors of the operands; the K steps add their
+  // byte offset / 16 to the start-address field.
+  const uint32_t st0 = base, st1 = base + SM::kBuf;
+  const uint64_t dC0 = umma_desc_sw128(st0 + SM::kCo, 16u, 1024u), dC1 = umma_desc_sw128(st1 + SM::kCo, 16u, 1024u);
+  const uint64_t dBk0 = umma_desc_sw128(st0 + SM::kBo, 16u, 1024u), dBk1 = umma_desc_sw128(st1 + SM::kBo, 16u, 1024u);
+  const uint64_t dBmn0 = umma_desc_sw128(st0 + SM::kBo, (uint32_t)kTileBytes, 1024u),
+                 dBmn1 = umma_desc_sw128(st1 + SM::kBo, (uint32_t)kTileBytes, 1024u);
+  const uint64_t dX0 = umma_desc_sw128(st0 + SM::kX, (uint32_t)kTileBytes, 1024u),
+                 dX1 = umma_desc_sw128(st1 + SM::kX, (uint32_t)kTileBytes, 1024u);
+  // Cm / M (K-major), Bm rows as a K-major B^T, Bm as an MN-major B^T, x (MN-major) of stage s
+  auto dC = [&](int s) { return s ? dC1 : dC0; };
+  auto dBk = [&](int s) { return s ? dBk1 : dBk0; };
+  auto dBmn = [&](int s) { return s ? dBmn1 : dBmn0; };
+  auto dX = [&](int s) { return s ? dX1 : dX0; };
+  const uint64_t dS = umma_desc_sw128(base + SM::kS, (uint32_t)kTileBytes, 1024u);    // S_in, MN-major
+  const uint64_t dXp = umma_desc_sw128(base + SM::kXp, (uint32_t)kTileBytes, 1024u);  // x', MN-major
+  constexpr uint32_t kIdG = ssd_idesc(64, false, false);  // C (K-major) x B^T (K-major rows of Bm)
+  constexpr uint32_t kIdKM = ssd_idesc(64, false, true);  // K-major A x MN-major B: C S_in, M x
+  constexpr uint32_t kIdS = ssd_idesc(N, true, true);     // B^T (MN-major) x x' (MN-major)
+  // G = C B^T of the chunk in stage s: K = n, 16 at a time (32 bytes into a
+  // 128-byte row), the next 64 n one box on; committed to bar_g
+  auto issue_g = [&](int s) {
+#pragma unroll
+    for (int k = 0; k < N / 16; ++k) {
+      const uint64_t ko = (uint64_t)(((k / 4) * kTileBytes + (k % 4) * 32) >> 4);
+      umma_f16(tmem + kColG, dC(s) + ko, dBk(s) + ko, kIdG, k > 0 ? 1u : 0u);
+    }
+    umma_commit(bar_g);
+  };
+
+  __syncthreads();  // decays of chunk 0 published
   // the initial state: S = e^(cum_end of chunk 0) h0 in TMEM (ready for the
   // first update), h0 as bf16 for the first readout
   {
@@ -280,23 +320,9 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     fence_proxy_async_smem();
     tmem_fence_before_sync();
   }
+  if (tid == kTidG && mbar_wait(&full[0], 0u, P.status)) issue_g(0);
   __syncthreads();
 
-  constexpr uint32_t kIdG = ssd_idesc(64, false, false);  // C (K-major) x B^T (K-major rows of Bm)
-  constexpr uint32_t kIdKM = ssd_idesc(64, false, true);  // K-major A x MN-major B: C S_in, M x
-  constexpr uint32_t kIdS = ssd_idesc(N, true, true);     // B^T (MN-major) x x' (MN-major)
-  // G = C B^T of the chunk in stage s: K = n, 16 at a time, 32 bytes into a
-  // 128-byte row, the next 64 n one box on
-  auto issue_g = [&](int s) {
-    const uint32_t bs = base + s * SM::kBuf + SM::kBo, cs = base + s * SM::kBuf + SM::kCo;
-#pragma unroll
-    for (int k = 0; k < N / 16; ++k) {
-      const uint32_t ko = (uint32_t)((k / 4) * kTileBytes + (k % 4) * 32);
-      umma_f16(tmem + kColG, umma_desc_sw128(cs + ko, 16u, 1024u), umma_desc_sw128(bs + ko, 16u, 1024u), kIdG,
-               k > 0 ? 1u : 0u);
-    }
-  };
-  bool g_issued = false;  // thread 0: G of the next chunk already on the tensor core
   for (int c = 0; c < nch; ++c) {
     const int s = c & 1;
     const int t0 = c * kQ;
@@ -304,32 +330,22 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     const bool ok = mbar_wait(&full[s], (uint32_t)((c >> 1) & 1), P.status);
     if (__syncthreads_or(!ok)) break;  // the copy never came: stop, uniformly
     unsigned char* st = smem + s * SM::kBuf;
-    const uint32_t xs = base + s * SM::kBuf + SM::kX;
-    const uint32_t bs = base + s * SM::kBuf + SM::kBo;
-    const uint32_t cs = base + s * SM::kBuf + SM::kCo;
     const float* cum = vec + s * 256;  // cum of step t at cum[2 t], delta at cum[2 t + 1]
     const float* wd = cum + 128;
 
-    // ---- G = C B^T (unless already issued) and CS = C S_in (one thread)
-    if (tid == 0) {
+    // ---- CS = C S_in (B = S_in [n][p]: 16 rows of n per K step)
+    if (tid == kTidMma) {
       tmem_fence_after_sync();
-      if (!g_issued) issue_g(s);
 #pragma unroll
-      for (int k = 0; k < N / 16; ++k) {  // B = S_in [n][p]: 16 rows of n per K step
-        const uint32_t ko = (uint32_t)((k / 4) * kTileBytes + (k % 4) * 32);
-        umma_f16(tmem + kColCS, umma_desc_sw128(cs + ko, 16u, 1024u),
-                 umma_desc_sw128(base + SM::kS + (uint32_t)k * 2048u, (uint32_t)kTileBytes, 1024u), kIdKM,
-                 k > 0 ? 1u : 0u);
+      for (int k = 0; k < N / 16; ++k) {
+        const uint64_t ko = (uint64_t)(((k / 4) * kTileBytes + (k % 4) * 32) >> 4);
+        umma_f16(tmem + kColCS, dC(s) + ko, dS + (uint64_t)(k * 2048 >> 4), kIdKM, k > 0 ? 1u : 0u);
       }
-      umma_commit(bar_g);
+      umma_commit(bar_cs);
     }
-    // the next chunk's decays; its successor's dt in flight
-    if (warp == 0 && c + 1 < nch) {
-      chunk_decays(c + 1);
-      load_dt(c + 2);
-    }
-    // ---- x' = w delta x (state-update operand) and, once G is there,
-    // M[t][s] = G[t][s] e^(cum_t - cum_s) delta_s for s <= t as bf16 over Cm box 0
+    // the next chunk's boxes into the other stage (free since the last chunk)
+    if (tid == kTidTma && c + 1 < nch) issue(c + 1);
+    // ---- x' = w delta x (state-update operand)
     {
       const float w = wd[row];
 #pragma unroll
@@ -346,7 +362,15 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
         *reinterpret_cast<uint4*>(smem + SM::kXp + swz(row, c8)) = make_uint4(xo[0], xo[1], xo[2], xo[3]);
       }
     }
+    // the next chunk's decays; its successor's dt in flight
+    if (warp == kWarpDecay && c + 1 < nch) {
+      chunk_decays(c + 1);
+      load_dt(c + 2);
+    }
+    // ---- M[t][s] = G[t][s] e^(cum_t - cum_s) delta_s for s <= t as bf16
+    // over Cm box 0, once C B^T and C S_in are done with it
     mbar_wait(bar_g, ph, P.status);
+    mbar_wait(bar_cs, ph, P.status);
     tmem_fence_after_sync();
     {
       float v[32];
@@ -366,24 +390,22 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     fence_proxy_async_smem();
     tmem_fence_before_sync();
     __syncthreads();  // M and x' complete; decays of the next chunk published
-    // ---- Y = M x and S += B^T x' (S already carries this chunk's decay);
-    // then the next chunk's G as soon as its boxes are in
-    if (tid == 0) {
+    // ---- Y = M x and S += B^T x' (S already carries this chunk's decay)
+    if (tid == kTidMma) {
       tmem_fence_after_sync();
 #pragma unroll
       for (int k = 0; k < 4; ++k)  // K = s
-        umma_f16(tmem + kColY, umma_desc_sw128(cs + (uint32_t)k * 32u, 16u, 1024u),
-                 umma_desc_sw128(xs + (uint32_t)k * 2048u, (uint32_t)kTileBytes, 1024u), kIdKM, k > 0 ? 1u : 0u);
+        umma_f16(tmem + kColY, dC(s) + (uint64_t)(k * 32 >> 4), dX(s) + (uint64_t)(k * 2048 >> 4), kIdKM,
+                 k > 0 ? 1u : 0u);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        umma_f16(tmem + kColS, umma_desc_sw128(bs + (uint32_t)k * 2048u, (uint32_t)kTileBytes, 1024u),
-                 umma_desc_sw128(base + SM::kXp + (uint32_t)k * 2048u, (uint32_t)kTileBytes, 1024u), kIdS, 1u);
+        umma_f16(tmem + kColS, dBmn(s) + (uint64_t)(k * 2048 >> 4), dXp + (uint64_t)(k * 2048 >> 4), kIdS, 1u);
       umma_commit(bar_y);
-      g_issued = false;
-      if (c + 1 < nch && mbar_wait(&full[s ^ 1], (uint32_t)(((c + 1) >> 1) & 1), P.status)) {
-        issue_g(s ^ 1);
-        g_issued = true;
-      }
+    }
+    // ---- the next chunk's G as soon as its boxes are in
+    if (tid == kTidG && c + 1 < nch) {
+      tmem_fence_after_sync();
+      if (mbar_wait(&full[s ^ 1], (uint32_t)(((c + 1) >> 1) & 1), P.status)) issue_g(s ^ 1);
     }
     mbar_wait(bar_y, ph, P.status);
     tmem_fence_after_sync();
@@ -434,7 +456,6 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     fence_proxy_async_smem();
     tmem_fence_before_sync();
     __syncthreads();  // S_in complete; every product on this stage done
-    if (tid == 0 && c + 2 < nch) issue(c + 2);
   }
   tmem_fence_after_sync();
   if (warp == 0) tmem_dealloc(tmem, kTmemColsSsd);
