@@ -40,6 +40,7 @@ constexpr int kQ = 64;           // steps per chunk
 constexpr int kP = 64;           // head dimension
 constexpr int kSsdThreads = 128;  // 4 warps, one per quarter of the tensor-memory lanes
 constexpr int kTileBytes = 64 * 128;  // one 64 x 64 bf16 box (128-byte rows)
+constexpr int kVecSet = 320;         // floats of one chunk's decay set
 
 struct SsdParams {
   CUtensorMap map_x, map_B, map_C;  // 64-byte aligned members first
@@ -120,7 +121,7 @@ struct SsdSmem {
   static constexpr int kXp = 2 * kBuf;                 // x' = w delta x, bf16 [64 s][64 p] (MN-major)
   static constexpr int kS = kXp + kTileBytes;          // S_in (bf16) [N n][64 p] (MN-major)
   static constexpr int kVec = kS + N * 128;            // two sets of decays (see `vec`)
-  static constexpr int kBar = kVec + 2 * 4 * 64 * 4;   // mbarriers and the TMEM address
+  static constexpr int kBar = kVec + 2 * kVecSet * 4;  // mbarriers and the TMEM address
   static constexpr int kBytes = kBar + 128;
   static constexpr uint32_t kTx = (1 + 2 * NT) * kTileBytes;
   static_assert(kBuf % 1024 == 0 && kXp % 1024 == 0 && kS % 1024 == 0, "swizzled boxes on 1024-byte boundaries");
@@ -148,7 +149,8 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* smem = smem_raw + (base - raw);
   // per chunk set (two sets, by chunk parity): (cum, delta) pairs of steps
-  // [0, 64) interleaved [0, 128), w*delta [128, 192), e^(cum_end) [192]
+  // [0, 64) interleaved [0, 128), w*delta [128, 192), e^(cum_end) [192],
+  // the blocked-decay flag [193], the blocked factors [256, 320)
   float* vec = reinterpret_cast<float*>(smem + SM::kVec);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBar);  // [2]: the stages' TMA copies
   uint64_t* bar_cs = full + 2;  // C S_in done
@@ -162,10 +164,11 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   const float A = -expf(P.A_log[h]);
   const float bias = P.dt_bias[h];
   const float Dh = P.Dp[h];
-  // Roles beside the shared row work: thread 0 issues C S_in, M x and the
-  // state update; thread 32 issues C B^T one chunk ahead; thread 64 issues
-  // the TMA copies; warp 3 computes the decays one chunk ahead.
-  constexpr int kTidMma = 0, kTidG = 32, kTidTma = 64, kWarpDecay = 3;
+  // Roles beside the shared row work: thread 0 issues the tensor-core
+  // products (C S_in, then M x and the state update, then the next chunk's
+  // C B^T, in that order on the tensor core); thread 64 issues the TMA
+  // copies; warp 3 computes the decays one chunk ahead.
+  constexpr int kTidMma = 0, kTidTma = 64, kWarpDecay = 3;
 
   if (tid == kTidMma) {
     mbar_init(&full[0], 1);
@@ -242,7 +245,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     }
   };
   auto chunk_decays = [&](int c) {
-    float* v = vec + (c & 1) * 256;
+    float* v = vec + (c & 1) * kVecSet;
     float d2[2], a2[2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -264,6 +267,13 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     v[128 + 2 * lane] = fast_exp(end - c0) * d2[0];
     v[128 + 2 * lane + 1] = fast_exp(end - c1) * d2[1];
     if (lane == 0) v[192] = fast_exp(end);
+    // per step s: e^(cum_b - cum_s) delta_s with b the first step of its
+    // 8-step block; usable when no block decays by more than e^64
+    const float cb = __shfl_sync(0xffffffffu, c0, lane & ~3);
+    v[256 + 2 * lane] = fast_exp(cb - c0) * d2[0];
+    v[256 + 2 * lane + 1] = fast_exp(cb - c1) * d2[1];
+    const bool blocked = __all_sync(0xffffffffu, cb - c1 < 64.f);
+    if (lane == 0) v[193] = blocked ? 1.f : 0.f;
   };
   if (warp == kWarpDecay) {
     load_dt(0);
@@ -320,7 +330,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     fence_proxy_async_smem();
     tmem_fence_before_sync();
   }
-  if (tid == kTidG && mbar_wait(&full[0], 0u, P.status)) issue_g(0);
+  if (tid == kTidMma && mbar_wait(&full[0], 0u, P.status)) issue_g(0);
   __syncthreads();
 
   for (int c = 0; c < nch; ++c) {
@@ -330,7 +340,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     const bool ok = mbar_wait(&full[s], (uint32_t)((c >> 1) & 1), P.status);
     if (__syncthreads_or(!ok)) break;  // the copy never came: stop, uniformly
     unsigned char* st = smem + s * SM::kBuf;
-    const float* cum = vec + s * 256;  // cum of step t at cum[2 t], delta at cum[2 t + 1]
+    const float* cum = vec + s * kVecSet;  // cum of step t at cum[2 t], delta at cum[2 t + 1]
     const float* wd = cum + 128;
 
     // ---- CS = C S_in (B = S_in [n][p]: 16 rows of n per K step)
@@ -378,11 +388,25 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
       tmem_ld16x2(tquarter + kColG, v);
       const float ct = cum[2 * row];
       const int s0 = 32 * hf;
+      if (cum[193] != 0.f) {  // e^(cum_t - cum_s) = e^(cum_t - cum_b) e^(cum_b - cum_s), 8-step blocks b
+        const float* qs = cum + 256;
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        const float4 cd = *reinterpret_cast<const float4*>(cum + 2 * (s0 + j));  // steps s0 + j, s0 + j + 1
-        v[j] = s0 + j <= row ? v[j] * fast_exp(ct - cd.x) * cd.y : 0.f;
-        v[j + 1] = s0 + j + 1 <= row ? v[j + 1] * fast_exp(ct - cd.z) * cd.w : 0.f;
+        for (int k = 0; k < 4; ++k) {
+          const int sb = s0 + 8 * k;
+          const float e = fast_exp(ct - cum[2 * sb]);
+          const float4 qa = *reinterpret_cast<const float4*>(qs + sb);
+          const float4 qb = *reinterpret_cast<const float4*>(qs + sb + 4);
+          const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[8 * k + i] = sb + i <= row ? v[8 * k + i] * e * qv[i] : 0.f;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float4 cd = *reinterpret_cast<const float4*>(cum + 2 * (s0 + j));  // steps s0 + j, s0 + j + 1
+          v[j] = s0 + j <= row ? v[j] * fast_exp(ct - cd.x) * cd.y : 0.f;
+          v[j + 1] = s0 + j + 1 <= row ? v[j + 1] * fast_exp(ct - cd.z) * cd.w : 0.f;
+        }
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q) put8(SM::kCo + s * SM::kBuf, row, 4 * hf + q, v + 8 * q);
@@ -401,11 +425,8 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
       for (int k = 0; k < 4; ++k)
         umma_f16(tmem + kColS, dBmn(s) + (uint64_t)(k * 2048 >> 4), dXp + (uint64_t)(k * 2048 >> 4), kIdS, 1u);
       umma_commit(bar_y);
-    }
-    // ---- the next chunk's G as soon as its boxes are in
-    if (tid == kTidG && c + 1 < nch) {
-      tmem_fence_after_sync();
-      if (mbar_wait(&full[s ^ 1], (uint32_t)(((c + 1) >> 1) & 1), P.status)) issue_g(s ^ 1);
+      // the next chunk's G, queued behind this chunk's products
+      if (c + 1 < nch && mbar_wait(&full[s ^ 1], (uint32_t)(((c + 1) >> 1) & 1), P.status)) issue_g(s ^ 1);
     }
     mbar_wait(bar_y, ph, P.status);
     tmem_fence_after_sync();
@@ -442,7 +463,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
         if (has_srow)
 #pragma unroll
           for (int c8 = 0; c8 < 8; ++c8) put8(SM::kS, srow, c8, v + 8 * c8);
-        const float dec1 = vec[(s ^ 1) * 256 + 192];
+        const float dec1 = vec[(s ^ 1) * kVecSet + 192];
 #pragma unroll
         for (int i = 0; i < 64; ++i) v[i] *= dec1;
         st64(kColS, v);

@@ -57,6 +57,25 @@ def test_ssd_dt_limit():
     assert rel_err(np64(h_last), rh) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("N", [64, 128])
+def test_ssd_steep_and_mixed_decays(N):
+    """Heads whose 8-step decay runs past e^64 (the readout then takes the
+    exact per-element exponentials) beside heads near that edge (chunks of
+    either kind) and mild ones, in one launch."""
+    x = inputs.make_ssd_inputs(2, 260, 6, 64, 2, N, "bf16", seed=31, h0_std=0.5)
+    sp_inv = lambda v: float(np.log(np.expm1(v)))  # noqa: E731
+    x["dt_bias"] = torch.tensor([sp_inv(3.0), sp_inv(1.0), sp_inv(0.05), sp_inv(6.0), sp_inv(0.9), sp_inv(0.01)],
+                                dtype=torch.float32)
+    x["A_log"] = torch.log(torch.tensor([16.0, 8.0, 4.0, 2.0, 9.0, 1.0], dtype=torch.float32))
+    xd = _dev(x)
+    y, h_last = s6.ssd_fwd(*[xd[k] for k in KEYS], xd["h0"])
+    s6.check_device_status()
+    ry, rh = oracle.ssd_fwd(*[x[k] for k in KEYS], x["h0"])
+    for h in range(6):
+        assert rel_err(np64(y)[:, :, h], ry[:, :, h]) <= TOL["bf16"], h
+    assert rel_err(np64(h_last), rh) <= TOL["bf16"]
+
+
 def test_ssd_full_shape_sampled_heads():
     w = inputs.SSD_WORKLOADS["mamba2_1p3b"]
     x = inputs.make_ssd_inputs(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.act, seed=0)
