@@ -38,7 +38,7 @@ namespace {
 
 constexpr int kQ = 64;           // steps per chunk
 constexpr int kP = 64;           // head dimension
-constexpr int kSsdThreads = 128;  // 4 warps, one per quarter of the tensor-memory lanes
+constexpr int kSsdThreads = 256;  // 8 warps, two per quarter of the tensor-memory lanes
 constexpr int kTileBytes = 64 * 128;  // one 64 x 64 bf16 box (128-byte rows)
 constexpr int kVecSet = 320;         // floats of one chunk's decay set
 
@@ -96,19 +96,19 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 // make this thread's generic-proxy shared-memory writes visible to the tensor core
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// 32 columns of 16 lanes in two halves: threads 0..15 read lanes
-// base .. base + 15 at columns col .. col + 31, threads 16..31 the same
-// lanes at columns col + 32 .. col + 63 (one warp, converged; waits)
-__device__ __forceinline__ void tmem_ld16x2(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// 16 columns of 16 lanes in two halves: threads 0..15 read lanes
+// base .. base + 15 at columns col .. col + 15, threads 16..31 the same
+// lanes at columns col + 16 .. col + 31 (one warp, converged; waits)
+__device__ __forceinline__ void tmem_ld16x2_16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
   asm volatile(
-      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32], 32;\n\t"
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16], 16;\n\t"
       "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 template <int N>
@@ -166,9 +166,9 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   const float Dh = P.Dp[h];
   // Roles beside the shared row work: thread 0 issues the tensor-core
   // products (C S_in, then M x and the state update, then the next chunk's
-  // C B^T, in that order on the tensor core); thread 64 issues the TMA
-  // copies; warp 3 computes the decays one chunk ahead.
-  constexpr int kTidMma = 0, kTidTma = 64, kWarpDecay = 3;
+  // C B^T, in that order on the tensor core); thread 192 issues the TMA
+  // copies; warp 7 computes the decays one chunk ahead.
+  constexpr int kTidMma = 0, kTidTma = 192, kWarpDecay = 7;
 
   if (tid == kTidMma) {
     mbar_init(&full[0], 1);
@@ -183,14 +183,17 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   __syncthreads();
   tmem_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tquarter = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's lane quarter
+  const uint32_t tquarter = tmem + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's lane quarter
+  const int kq = warp >> 2;  // warps w and w + 4 share a lane quarter and split the columns
   // The 64 x 64 accumulators (M = 64) keep row r in lane (r / 16) * 32 + r % 16;
-  // read in two halves, every thread holds 32 columns of one row.
-  const int row = 16 * warp + (lane & 15);
-  const int hf = lane >> 4;  // columns [32 hf, 32 hf + 32)
-  // rows of S: N = 128 -> row n = tid (every lane); N = 64 -> the M = 64 layout
+  // every thread holds 16 columns [col0, col0 + 16) of one row.
+  const int row = 16 * (warp & 3) + (lane & 15);
+  const int col0 = 32 * kq + 16 * (lane >> 4);
+  // rows of S: N = 128 -> row n = lane of the quarter (every lane); N = 64 ->
+  // the M = 64 layout; a thread holds 32 columns [sc, sc + 32)
   const bool has_srow = N == 128 || lane < 16;
-  const int srow = N == 128 ? tid : row;
+  const int srow = N == 128 ? 32 * (warp & 3) + lane : row;
+  const int sc = 32 * kq;
 
   auto issue = [&](int c) {  // chunk c's boxes into stage c & 1 (one thread)
     const int s = c & 1;
@@ -208,22 +211,6 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     issue(0);
   }
 
-  auto ld64 = [&](uint32_t col, float (&v)[64]) {  // 64 columns of this thread's lane
-    float a[32], c[32];
-    __syncwarp();
-    tmem_ld32(tquarter + col, a);
-    tmem_ld32(tquarter + col + 32u, c);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = a[i], v[32 + i] = c[i];
-  };
-  auto st64 = [&](uint32_t col, const float (&v)[64]) {
-    float a[32], c[32];
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) a[i] = v[i], c[i] = v[32 + i];
-    tmem_st32(tquarter + col, a);
-    tmem_st32(tquarter + col + 32u, c);
-  };
   // 8 consecutive values as one 16-byte unit of a 128B-swizzled [rows][64] bf16 image
   auto put8 = [&](uint32_t off, int r, int c8, const float* v) {
     *reinterpret_cast<uint4*>(smem + off + swz(r, c8)) =
@@ -315,17 +302,18 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   // the initial state: S = e^(cum_end of chunk 0) h0 in TMEM (ready for the
   // first update), h0 as bf16 for the first readout
   {
-    float v[64];
-    const float* h0 = (P.h0 && has_srow) ? P.h0 + (((size_t)b * P.H + h) * N + srow) * kP : nullptr;
+    float v[32];
+    const float* h0 = (P.h0 && has_srow) ? P.h0 + (((size_t)b * P.H + h) * N + srow) * kP + sc : nullptr;
 #pragma unroll
-    for (int i = 0; i < 64; ++i) v[i] = h0 ? h0[i] : 0.f;
+    for (int i = 0; i < 32; ++i) v[i] = h0 ? h0[i] : 0.f;
     if (has_srow)
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) put8(SM::kS, srow, c8, v + 8 * c8);
+      for (int q = 0; q < 4; ++q) put8(SM::kS, srow, 4 * kq + q, v + 8 * q);
     const float dec0 = vec[192];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) v[i] *= dec0;
-    st64(kColS, v);
+    for (int i = 0; i < 32; ++i) v[i] *= dec0;
+    __syncwarp();
+    tmem_st32(tquarter + kColS + (uint32_t)sc, v);
     tmem_wait_st();
     fence_proxy_async_smem();
     tmem_fence_before_sync();
@@ -359,8 +347,8 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     {
       const float w = wd[row];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int c8 = 4 * hf + q;
+      for (int q = 0; q < 2; ++q) {
+        const int c8 = col0 / 8 + q;
         const uint4 xv = *reinterpret_cast<const uint4*>(st + SM::kX + swz(row, c8));
         const uint32_t xin[4] = {xv.x, xv.y, xv.z, xv.w};
         uint32_t xo[4];
@@ -383,15 +371,15 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     mbar_wait(bar_cs, ph, P.status);
     tmem_fence_after_sync();
     {
-      float v[32];
+      float v[16];
       __syncwarp();
-      tmem_ld16x2(tquarter + kColG, v);
+      tmem_ld16x2_16(tquarter + kColG + (uint32_t)(32 * kq), v);
       const float ct = cum[2 * row];
-      const int s0 = 32 * hf;
+      const int s0 = col0;
       if (cum[193] != 0.f) {  // e^(cum_t - cum_s) = e^(cum_t - cum_b) e^(cum_b - cum_s), 8-step blocks b
         const float* qs = cum + 256;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 2; ++k) {
           const int sb = s0 + 8 * k;
           const float e = fast_exp(ct - cum[2 * sb]);
           const float4 qa = *reinterpret_cast<const float4*>(qs + sb);
@@ -402,14 +390,14 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
+        for (int j = 0; j < 16; j += 2) {
           const float4 cd = *reinterpret_cast<const float4*>(cum + 2 * (s0 + j));  // steps s0 + j, s0 + j + 1
           v[j] = s0 + j <= row ? v[j] * fast_exp(ct - cd.x) * cd.y : 0.f;
           v[j + 1] = s0 + j + 1 <= row ? v[j + 1] * fast_exp(ct - cd.z) * cd.w : 0.f;
         }
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) put8(SM::kCo + s * SM::kBuf, row, 4 * hf + q, v + 8 * q);
+      for (int q = 0; q < 2; ++q) put8(SM::kCo + s * SM::kBuf, row, s0 / 8 + q, v + 8 * q);
     }
     fence_proxy_async_smem();
     tmem_fence_before_sync();
@@ -432,16 +420,16 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     tmem_fence_after_sync();
     // ---- y = Y + e^cum CS + D x for this thread's row and half
     {
-      float yv[32], cv[32];
+      float yv[16], cv[16];
       __syncwarp();
-      tmem_ld16x2(tquarter + kColY, yv);
-      tmem_ld16x2(tquarter + kColCS, cv);
+      tmem_ld16x2_16(tquarter + kColY + (uint32_t)(32 * kq), yv);
+      tmem_ld16x2_16(tquarter + kColCS + (uint32_t)(32 * kq), cv);
       const float et = fast_exp(cum[2 * row]);
       __nv_bfloat16* yrow = P.y + (((size_t)b * P.L + t0 + row) * P.H + h) * kP;
       const bool store = t0 + row < P.L;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int c8 = 4 * hf + q;
+      for (int q = 0; q < 2; ++q) {
+        const int c8 = col0 / 8 + q;
         const uint4 xv = *reinterpret_cast<const uint4*>(st + SM::kX + swz(row, c8));
         const uint32_t xin[4] = {xv.x, xv.y, xv.z, xv.w};
         uint32_t yo[4];
@@ -457,21 +445,23 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     // ---- the state after the chunk: S_in of the next readout (bf16) and,
     // scaled by the next chunk's decay, back into TMEM; or h_last
     {
-      float v[64];
-      ld64(kColS, v);
+      float v[32];
+      __syncwarp();
+      tmem_ld32(tquarter + kColS + (uint32_t)sc, v);
       if (c + 1 < nch) {
         if (has_srow)
 #pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8) put8(SM::kS, srow, c8, v + 8 * c8);
+          for (int q = 0; q < 4; ++q) put8(SM::kS, srow, 4 * kq + q, v + 8 * q);
         const float dec1 = vec[(s ^ 1) * kVecSet + 192];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) v[i] *= dec1;
-        st64(kColS, v);
+        for (int i = 0; i < 32; ++i) v[i] *= dec1;
+        __syncwarp();
+        tmem_st32(tquarter + kColS + (uint32_t)sc, v);
         tmem_wait_st();
       } else if (P.h_last && has_srow) {
-        float* hl = P.h_last + (((size_t)b * P.H + h) * N + srow) * kP;
+        float* hl = P.h_last + (((size_t)b * P.H + h) * N + srow) * kP + sc;
 #pragma unroll
-        for (int i = 0; i < 64; i += 2) *reinterpret_cast<float2*>(hl + i) = make_float2(v[i], v[i + 1]);
+        for (int i = 0; i < 32; i += 2) *reinterpret_cast<float2*>(hl + i) = make_float2(v[i], v[i + 1]);
       }
     }
     fence_proxy_async_smem();
