@@ -317,6 +317,8 @@ def _open_ssd(path):
     i64, vp, ci, f64 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_double
     lib.ssdo_fwd.argtypes = [i64] * 6 + [vp] * 8 + [f64, f64] + [vp] * 2
     lib.ssdo_fwd.restype = ci
+    lib.ssdo_bwd.argtypes = [i64] * 6 + [vp] * 10 + [f64, f64] + [vp] * 8
+    lib.ssdo_bwd.restype = ci
     return lib
 
 
@@ -356,3 +358,25 @@ def ssd_fwd(x, dt_raw, dt_bias, A_log, Bm, Cm, Dp, h0=None, *, dt_limit=None):
     if rc != 0:
         raise ValueError(f"ssdo_fwd failed with code {rc}")
     return y, h_last
+
+
+def ssd_bwd(x, dt_raw, dt_bias, A_log, Bm, Cm, Dp, h0, dy, dh_last=None, *, dt_limit=None):
+    """Backward of ``loss = sum(dy*y) + sum(dh_last*h_last)`` through the SSD
+    recurrence, step by step.  Returns a dict of f64 arrays: dx [B,L,H,P],
+    ddt_raw [B,L,H], ddt_bias / dA_log / dDp [H] (sums over batch and steps),
+    dBm / dCm [B,L,G,N] (sums over the heads of a group), dh0 [B,H,N,P]."""
+    x, dt_raw, dt_bias, A_log, Bm, Cm, Dp, h0, dy, dh_last = map(
+        _f64, (x, dt_raw, dt_bias, A_log, Bm, Cm, Dp, h0, dy, dh_last))
+    B, L, H, P = x.shape
+    G, N = Bm.shape[2], Bm.shape[3]
+    r = {"dx": np.full((B, L, H, P), np.nan), "ddt_raw": np.full((B, L, H), np.nan),
+         "ddt_bias": np.full((H,), np.nan), "dA_log": np.full((H,), np.nan), "dDp": np.full((H,), np.nan),
+         "dBm": np.full((B, L, G, N), np.nan), "dCm": np.full((B, L, G, N), np.nan),
+         "dh0": np.full((B, H, N, P), np.nan)}
+    rc = _load_ssd().ssdo_bwd(B, L, H, P, G, N, _ptr(x), _ptr(dt_raw), _ptr(dt_bias), _ptr(A_log), _ptr(Bm),
+                              _ptr(Cm), _ptr(Dp), _ptr(h0), _ptr(dy), _ptr(dh_last), *_limits(dt_limit),
+                              _ptr(r["dx"]), _ptr(r["ddt_raw"]), _ptr(r["ddt_bias"]), _ptr(r["dA_log"]),
+                              _ptr(r["dBm"]), _ptr(r["dCm"]), _ptr(r["dDp"]), _ptr(r["dh0"]))
+    if rc != 0:
+        raise ValueError(f"ssdo_bwd failed with code {rc}")
+    return r

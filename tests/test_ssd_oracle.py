@@ -1,8 +1,10 @@
 """Pins for the Mamba-2 SSD oracle (CPU only): the reduction to the S6
 oracle (head h, element p as S6 channel (h, p) with A[d][n] = A_h and the
 group's B, C), the chunked matmul form written independently with numpy, a
-closed form for constant inputs, delta fixed by dt_min = dt_max, and planted
-mistakes that must each fail a pin."""
+closed form for constant inputs, delta fixed by dt_min = dt_max; for the
+backward, central finite differences of every gradient (with and without a
+limit on delta that clamps some steps) and the reduction to the S6 oracle's
+backward; and planted mistakes that must each fail a pin."""
 import os
 import shutil
 
@@ -139,6 +141,83 @@ def check_dt_fixed_by_limit(L=30, c=0.37):
     return err
 
 
+_KEYS = ("x", "dt_raw", "dt_bias", "A_log", "Bm", "Cm", "Dp", "h0")
+_GRAD = {"x": "dx", "dt_raw": "ddt_raw", "dt_bias": "ddt_bias", "A_log": "dA_log", "Bm": "dBm", "Cm": "dCm",
+         "Dp": "dDp", "h0": "dh0"}
+
+
+def check_bwd_finite_differences(dt_limit=None, seed=11):
+    """Central differences (h = 1e-6) of loss = sum(dy*y) + sum(dh_last*h_last)
+    against every gradient the backward returns; worst |fd - g| / max(1, |fd|)."""
+    p = _problem(B=2, L=6, H=4, P=2, G=2, N=3, seed=seed)
+    r = np.random.default_rng(seed + 100)
+    dy = r.standard_normal(p["x"].shape)
+    dhl = r.standard_normal(p["h0"].shape)
+    lim = None
+    if dt_limit == "quartiles":  # clamp about half the steps, at values no step sits on
+        sp = np.logaddexp(0.0, p["dt_raw"] + p["dt_bias"]).ravel()
+        lim = (float(np.quantile(sp, 0.25)) + 1e-3, float(np.quantile(sp, 0.75)) - 1e-3)
+
+    def loss():
+        y, hl = oracle.ssd_fwd(*[p[k] for k in _KEYS], dt_limit=lim)
+        return float(np.sum(dy * y) + np.sum(dhl * hl))
+
+    g = oracle.ssd_bwd(*[p[k] for k in _KEYS], dy, dhl, dt_limit=lim)
+    worst, eps = 0.0, 1e-6
+    for k in _KEYS:
+        a = p[k]
+        for idx in np.ndindex(a.shape):
+            keep = a[idx]
+            a[idx] = keep + eps
+            lp = loss()
+            a[idx] = keep - eps
+            lm = loss()
+            a[idx] = keep
+            fd = (lp - lm) / (2 * eps)
+            worst = max(worst, abs(fd - g[_GRAD[k]][idx]) / max(1.0, abs(fd)))
+    return worst
+
+
+def check_bwd_s6_reduction(dt_limit=None, seed=12):
+    """The backward of each group equals the S6 oracle's backward of the
+    mapped problem, summed over the head's P channels (delta, its bias, D),
+    over P x N (A_log), and transposed (h0)."""
+    p = _problem(seed=seed)
+    B, L, H, P = p["x"].shape
+    G, N = p["Bm"].shape[2], p["Bm"].shape[3]
+    hpg = H // G
+    r = np.random.default_rng(seed + 100)
+    dy = r.standard_normal(p["x"].shape)
+    dhl = r.standard_normal(p["h0"].shape)
+    g = oracle.ssd_bwd(*[p[k] for k in _KEYS], dy, dhl, dt_limit=dt_limit)
+    err = 0.0
+
+    def rel(a, b):
+        return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300))
+
+    for grp in range(G):
+        hs = slice(grp * hpg, (grp + 1) * hpg)
+        u = p["x"][:, :, hs, :].reshape(B, L, hpg * P)
+        raw = np.repeat(p["dt_raw"][:, :, hs], P, axis=2)
+        bias = np.repeat(p["dt_bias"][hs], P)
+        A_log = np.repeat(p["A_log"][hs], P)[:, None] * np.ones((1, N))
+        Dp = np.repeat(p["Dp"][hs], P)
+        h0 = np.transpose(p["h0"][:, hs], (0, 1, 3, 2)).reshape(B, hpg * P, N)
+        dout = dy[:, :, hs, :].reshape(B, L, hpg * P)
+        dh_last = np.transpose(dhl[:, hs], (0, 1, 3, 2)).reshape(B, hpg * P, N)
+        s6 = oracle.bwd(u, raw, None, p["Bm"][:, :, grp, :], p["Cm"][:, :, grp, :], A_log, Dp, bias, h0, dout,
+                        dh_last, dt_limit=dt_limit)
+        err = max(err, rel(g["dx"][:, :, hs, :], s6["du"].reshape(B, L, hpg, P)))
+        err = max(err, rel(g["ddt_raw"][:, :, hs], s6["d_delta_raw"].reshape(B, L, hpg, P).sum(-1)))
+        err = max(err, rel(g["ddt_bias"][hs], s6["d_delta_bias"].reshape(hpg, P).sum(-1)))
+        err = max(err, rel(g["dA_log"][hs], s6["dA_log"].reshape(hpg, P, N).sum(axis=(1, 2))))
+        err = max(err, rel(g["dDp"][hs], s6["dD"].reshape(hpg, P).sum(-1)))
+        err = max(err, rel(g["dBm"][:, :, grp, :], s6["dBm"]))
+        err = max(err, rel(g["dCm"][:, :, grp, :], s6["dCm"]))
+        err = max(err, rel(g["dh0"][:, hs], np.transpose(s6["dh0"].reshape(B, hpg, P, N), (0, 1, 3, 2))))
+    return err
+
+
 PINS = {
     "s6_reduction": (lambda: check_s6_reduction(), 1e-12),
     "s6_reduction_limited": (lambda: check_s6_reduction(dt_limit=(0.3, 0.9), seed=3), 1e-12),
@@ -146,6 +225,10 @@ PINS = {
     "chunked_form_q1": (lambda: check_chunked_form(seed=4, Q=1), 1e-12),
     "closed_form": (lambda: check_closed_form(), 1e-12),
     "dt_fixed_by_limit": (lambda: check_dt_fixed_by_limit(), 1e-12),
+    "bwd_finite_differences": (lambda: check_bwd_finite_differences(), 1e-7),
+    "bwd_finite_differences_limited": (lambda: check_bwd_finite_differences("quartiles", seed=13), 1e-7),
+    "bwd_s6_reduction": (lambda: check_bwd_s6_reduction(), 1e-12),
+    "bwd_s6_reduction_limited": (lambda: check_bwd_s6_reduction(dt_limit=(0.3, 0.9), seed=14), 1e-12),
 }
 
 
@@ -167,6 +250,15 @@ MUTANTS = {
     "readout_before_update": (
         "for (int64_t n = 0; n < N; ++n)\n          for (int64_t p = 0; p < P; ++p) S[n * P + p] = a * S[n * P + p] + delta * Bt[n] * xt[p];\n        double *yt",
         "double *yt"),
+    "bwd_no_decay_of_adjoint": ("for (int64_t i = 0; i < NP; ++i) Gr[i] *= at;", ""),
+    "bwd_dB_without_delta": ("dbv[n] += dl * sb;", "dbv[n] += sb;"),
+    "bwd_ddelta_without_A": ("const double ddl = Ah * at * gs + gbx;", "const double ddl = at * gs + gbx;"),
+    "bwd_dA_without_delta": ("dAh += dl * at * gs;", "dAh += at * gs;"),
+    "bwd_limit_mask_ignored": ("(sp >= dt_min && sp <= dt_max) ? ddl * ssdo_sigmoid(sarg) : 0.0", "ddl * ssdo_sigmoid(sarg)"),
+    "bwd_B_for_C_readout": ("Gr[n * P + p] += cv[n] * gy[p];", "Gr[n * P + p] += bv[n] * gy[p];"),
+    "bwd_dx_skip_dropped": ("dxv[p] = Dp[h] * gy[p] + dl * sg;", "dxv[p] = dl * sg;"),
+    "bwd_dh_last_ignored": ("if (dh_last)\n        memcpy(Gr,", "if (0)\n        memcpy(Gr,"),
+    "bwd_dA_log_chain": ("dA_log[h] += dAh * Ah;", "dA_log[h] += dAh;"),
 }
 
 
