@@ -23,6 +23,9 @@ def _free_port():
 
 
 def _rank_main(rank, world, port, out):
+    # CPU ranks over gloo, as on a machine without GPUs, whatever this one has
+    # (set before anything in the fresh process touches CUDA)
+    os.environ["CUDA_VISIBLE_DEVICES"] = ""
     os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port),
                        "RANK": str(rank), "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank)})
     w, r, local = bench.dist_setup()
