@@ -3,8 +3,9 @@ oracle (head h, element p as S6 channel (h, p) with A[d][n] = A_h and the
 group's B, C), the chunked matmul form written independently with numpy, a
 closed form for constant inputs, delta fixed by dt_min = dt_max; for the
 backward, central finite differences of every gradient (with and without a
-limit on delta that clamps some steps) and the reduction to the S6 oracle's
-backward; and planted mistakes that must each fail a pin."""
+limit on delta that clamps some steps), the reduction to the S6 oracle's
+backward and the chunked matrix form of the backward written independently
+in numpy; and planted mistakes that must each fail a pin."""
 import os
 import shutil
 
@@ -146,6 +147,89 @@ _GRAD = {"x": "dx", "dt_raw": "ddt_raw", "dt_bias": "ddt_bias", "A_log": "dA_log
          "Dp": "dDp", "h0": "dh0"}
 
 
+def chunked_backward(p, dy, dhl, Q):
+    """The backward in the chunked matrix form (numpy), per chunk of Q steps
+    walked last to first with dS = the gradient of the state leaving the
+    chunk: with L the masked decays, CB = C B^T, Z[t][s] = dy_t . x_s,
+    w_s = e^(cum_end - cum_s) and dec = e^(cum_end),
+      dx = D dy + diag(delta) (L o CB)^T dy + diag(delta w) B dS
+      dB = diag(delta) (L o Z)^T C + diag(delta w) x dS^T
+      dC = diag(e^cum) dy S_in^T + (L o Z o delta_s) B
+      dS_in = dec dS + C^T diag(e^cum) dy
+    and for delta the gradient of the log-decays cum:
+      dcum_t = row_t(F) - col_t(F) + e^(cum_t) dy_t . (C_t S_in) - w_t delta_t (B dS)_t . x_t
+               (+ dS . S_out at the chunk's last step),  F = L o CB o Z o delta_s,
+    ddelta_s = col_s(L o CB o Z) + w_s (B dS)_s . x_s + A sum_{t >= s} dcum_t,
+    dA = sum_s delta_s sum_{t >= s} dcum_t (no delta limit here)."""
+    x, Bm, Cm = p["x"], p["Bm"], p["Cm"]
+    B, L, H, P = x.shape
+    G, N = Bm.shape[2], Bm.shape[3]
+    hpg = H // G
+    sarg = p["dt_raw"] + p["dt_bias"]
+    delta = np.logaddexp(0.0, sarg)
+    A = -np.exp(p["A_log"])
+    r = {"dx": np.zeros_like(x), "ddt_raw": np.zeros_like(p["dt_raw"]), "ddt_bias": np.zeros(H),
+         "dA_log": np.zeros(H), "dDp": np.zeros(H), "dBm": np.zeros_like(Bm), "dCm": np.zeros_like(Cm),
+         "dh0": np.zeros_like(p["h0"])}
+    for b in range(B):
+        for h in range(H):
+            g = h // hpg
+            chunks = [(c0, min(L, c0 + Q)) for c0 in range(0, L, Q)]
+            # forward: the state entering each chunk
+            S = p["h0"][b, h].copy()
+            S_in = []
+            for c0, c1 in chunks:
+                S_in.append(S.copy())
+                dA_ = delta[b, c0:c1, h] * A[h]
+                cum = np.cumsum(dA_)
+                w = np.exp(cum[-1] - cum)
+                S = np.exp(cum[-1]) * S + Bm[b, c0:c1, g].T @ ((w * delta[b, c0:c1, h])[:, None] * x[b, c0:c1, h])
+            dS = dhl[b, h].copy()   # gradient of the state leaving the current chunk
+            dA_h = 0.0
+            for (c0, c1), Sin in reversed(list(zip(chunks, S_in))):
+                dl = delta[b, c0:c1, h]
+                cum = np.cumsum(dl * A[h])
+                Lm = np.tril(np.exp(cum[:, None] - cum[None, :]))
+                w = np.exp(cum[-1] - cum)
+                dec = np.exp(cum[-1])
+                xc, Bc, Cc, dyc = x[b, c0:c1, h], Bm[b, c0:c1, g], Cm[b, c0:c1, g], dy[b, c0:c1, h]
+                CB = Cc @ Bc.T
+                Z = dyc @ xc.T                       # Z[t][s] = dy_t . x_s
+                Sout = dec * Sin + Bc.T @ ((w * dl)[:, None] * xc)
+                BdS = Bc @ dS                        # [s][p]
+                r["dx"][b, c0:c1, h] = p["Dp"][h] * dyc + dl[:, None] * ((Lm * CB).T @ dyc) + (dl * w)[:, None] * BdS
+                r["dBm"][b, c0:c1, g] += dl[:, None] * ((Lm * Z).T @ Cc) + (dl * w)[:, None] * (xc @ dS.T)
+                r["dCm"][b, c0:c1, g] += np.exp(cum)[:, None] * (dyc @ Sin.T) + (Lm * Z * dl[None, :]) @ Bc
+                r["dDp"][h] += np.sum(dyc * xc)
+                E = Lm * CB * Z                      # dloss/d(delta_s) through the intra term, before summing over t
+                F = E * dl[None, :]
+                R = np.exp(cum) * np.sum(dyc * (Cc @ Sin), axis=1)
+                Wv = w * dl * np.sum(BdS * xc, axis=1)
+                dcum = F.sum(axis=1) - F.sum(axis=0) + R - Wv
+                dcum[-1] += np.sum(dS * Sout)
+                direct = E.sum(axis=0) + w * np.sum(BdS * xc, axis=1)
+                rev = np.cumsum(dcum[::-1])[::-1]    # sum over t >= i
+                ddl = direct + A[h] * rev
+                dA_h += np.sum(dl * rev)
+                sig = 1.0 / (1.0 + np.exp(-sarg[b, c0:c1, h]))
+                r["ddt_raw"][b, c0:c1, h] = ddl * sig
+                dS = dec * dS + Cc.T @ (np.exp(cum)[:, None] * dyc)
+            r["dh0"][b, h] = dS
+            r["dA_log"][h] += dA_h * A[h]
+    r["ddt_bias"] = r["ddt_raw"].sum(axis=(0, 1))
+    return r
+
+
+def check_bwd_chunked_form(seed=21, Q=4):
+    p = _problem(B=2, L=13, H=4, P=3, G=2, N=3, seed=seed)
+    r = np.random.default_rng(seed + 100)
+    dy = r.standard_normal(p["x"].shape)
+    dhl = r.standard_normal(p["h0"].shape)
+    ref = oracle.ssd_bwd(*[p[k] for k in _KEYS], dy, dhl)
+    got = chunked_backward(p, dy, dhl, Q)
+    return max(float(np.max(np.abs(got[k] - ref[k])) / max(float(np.max(np.abs(ref[k]))), 1e-300)) for k in ref)
+
+
 def check_bwd_finite_differences(dt_limit=None, seed=11):
     """Central differences (h = 1e-6) of loss = sum(dy*y) + sum(dh_last*h_last)
     against every gradient the backward returns; worst |fd - g| / max(1, |fd|)."""
@@ -228,6 +312,8 @@ PINS = {
     "bwd_finite_differences": (lambda: check_bwd_finite_differences(), 1e-7),
     "bwd_finite_differences_limited": (lambda: check_bwd_finite_differences("quartiles", seed=13), 1e-7),
     "bwd_s6_reduction": (lambda: check_bwd_s6_reduction(), 1e-12),
+    "bwd_chunked_form": (lambda: check_bwd_chunked_form(), 1e-12),
+    "bwd_chunked_form_ragged": (lambda: check_bwd_chunked_form(seed=22, Q=5), 1e-12),
     "bwd_s6_reduction_limited": (lambda: check_bwd_s6_reduction(dt_limit=(0.3, 0.9), seed=14), 1e-12),
 }
 
