@@ -54,6 +54,10 @@ struct SsdParams {
   unsigned int* status;
   float dt_min, dt_max;
   int B, L, H, G, N;
+  // 0: one CTA per sequence, all chunks; 1: the state over chunks
+  // [0, seg_chunks) only, from h0, into h_last; 2: two CTAs per sequence,
+  // chunks [0, seg_chunks) from h0 and [seg_chunks, end) from h_last
+  int mode, seg_chunks;
 };
 
 // byte offset of the 16-byte chunk `c8` (elements 8 c8 .. 8 c8 + 7) of row r
@@ -137,12 +141,20 @@ __host__ __device__ constexpr uint32_t ssd_idesc(int m, bool a_mn, bool b_mn) {
          ((uint32_t)(m >> 4) << 24);
 }
 
-template <int N>
+template <int N, bool kStateOnly>
 __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_constant__ SsdParams P) {
   using SM = SsdSmem<N>;
   constexpr int NT = SM::NT;
-  const int nch = (P.L + kQ - 1) / kQ;
-  if (nch == 0) return;
+  // this CTA's sequence and its chunks [c0, c0 + nch); chunk indices below are
+  // local to that range
+  const int seg = P.mode == 2 ? (int)(blockIdx.x & 1) : 0;
+  const int bh = P.mode == 2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int c0 = seg ? P.seg_chunks : 0;
+  const int c1 = (P.mode == 1 || (P.mode == 2 && seg == 0)) ? P.seg_chunks : (P.L + kQ - 1) / kQ;
+  const int nch = c1 - c0;
+  if (nch <= 0) return;
+  const float* init = seg ? P.h_last : P.h0;  // the state entering the range
+  const bool write_last = P.mode != 2 || seg == 1;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // the 128B swizzle repeats every 1024 bytes: align the base
   const uint32_t raw = smem_u32(smem_raw);
@@ -158,7 +170,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   uint64_t* bar_y = full + 4;   // M x and the state update done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 5);
 
-  const int b = blockIdx.x / P.H, h = blockIdx.x % P.H;
+  const int b = bh / P.H, h = bh % P.H;
   const int g = h / (P.H / P.G);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float A = -expf(P.A_log[h]);
@@ -195,15 +207,15 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   const int srow = N == 128 ? 32 * (warp & 3) + lane : row;
   const int sc = 32 * kq;
 
-  auto issue = [&](int c) {  // chunk c's boxes into stage c & 1 (one thread)
-    const int s = c & 1;
+  auto issue = [&](int ci) {  // chunk ci's boxes into stage ci & 1 (one thread; no Cm for the state alone)
+    const int s = ci & 1, c = c0 + ci;
     unsigned char* st = smem + s * SM::kBuf;
-    mbar_arrive_expect_tx(&full[s], SM::kTx);
+    mbar_arrive_expect_tx(&full[s], kStateOnly ? (uint32_t)((1 + NT) * kTileBytes) : SM::kTx);
     tma_load_3d(st + SM::kX, &P.map_x, &full[s], h * kP, c * kQ, b);
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       tma_load_3d(st + SM::kBo + j * kTileBytes, &P.map_B, &full[s], g * N + 64 * j, c * kQ, b);
-      tma_load_3d(st + SM::kCo + j * kTileBytes, &P.map_C, &full[s], g * N + 64 * j, c * kQ, b);
+      if (!kStateOnly) tma_load_3d(st + SM::kCo + j * kTileBytes, &P.map_C, &full[s], g * N + 64 * j, c * kQ, b);
     }
   };
   if (tid == kTidTma) {
@@ -221,22 +233,22 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   // lane; the raw bits stay untouched until they are used, so the load's
   // latency hides behind a whole chunk) and turns them into delta, the
   // running sum of delta*A, the weights e^(cum_end - cum_s) delta_s and the
-  // chunk's total decay (set c & 1 of `vec`).
+  // chunk's total decay (set ci & 1 of `vec`, ci the chunk within the CTA's range).
   const unsigned short* dt_bits = reinterpret_cast<const unsigned short*>(P.dt_raw);
   unsigned short raw_next[2] = {0, 0};
-  auto load_dt = [&](int c) {
+  auto load_dt = [&](int ci) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      const int t = min(c * kQ + 2 * lane + i, P.L - 1);  // past the end: any valid step, masked later
+      const int t = min((c0 + ci) * kQ + 2 * lane + i, P.L - 1);  // past the end: any valid step, masked later
       raw_next[i] = dt_bits[((size_t)b * P.L + t) * P.H + h];
     }
   };
-  auto chunk_decays = [&](int c) {
-    float* v = vec + (c & 1) * kVecSet;
+  auto chunk_decays = [&](int ci) {
+    float* v = vec + (ci & 1) * kVecSet;
     float d2[2], a2[2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      const int t = c * kQ + 2 * lane + i;
+      const int t = (c0 + ci) * kQ + 2 * lane + i;
       const float r = __bfloat162float(__ushort_as_bfloat16(raw_next[i]));
       const float d = t < P.L ? clamp_dt(softplus_fast(r + bias), P.dt_min, P.dt_max) : 0.f;
       d2[i] = d;
@@ -303,10 +315,10 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   // first update), h0 as bf16 for the first readout
   {
     float v[32];
-    const float* h0 = (P.h0 && has_srow) ? P.h0 + (((size_t)b * P.H + h) * N + srow) * kP + sc : nullptr;
+    const float* h0 = (init && has_srow) ? init + (((size_t)b * P.H + h) * N + srow) * kP + sc : nullptr;
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = h0 ? h0[i] : 0.f;
-    if (has_srow)
+    if (!kStateOnly && has_srow)
 #pragma unroll
       for (int q = 0; q < 4; ++q) put8(SM::kS, srow, 4 * kq + q, v + 8 * q);
     const float dec0 = vec[192];
@@ -318,21 +330,21 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     fence_proxy_async_smem();
     tmem_fence_before_sync();
   }
-  if (tid == kTidMma && mbar_wait(&full[0], 0u, P.status)) issue_g(0);
+  if (!kStateOnly && tid == kTidMma && mbar_wait(&full[0], 0u, P.status)) issue_g(0);
   __syncthreads();
 
-  for (int c = 0; c < nch; ++c) {
-    const int s = c & 1;
-    const int t0 = c * kQ;
-    const uint32_t ph = (uint32_t)(c & 1);
-    const bool ok = mbar_wait(&full[s], (uint32_t)((c >> 1) & 1), P.status);
+  for (int ci = 0; ci < nch; ++ci) {
+    const int s = ci & 1;
+    const int t0 = (c0 + ci) * kQ;
+    const uint32_t ph = (uint32_t)(ci & 1);
+    const bool ok = mbar_wait(&full[s], (uint32_t)((ci >> 1) & 1), P.status);
     if (__syncthreads_or(!ok)) break;  // the copy never came: stop, uniformly
     unsigned char* st = smem + s * SM::kBuf;
     const float* cum = vec + s * kVecSet;  // cum of step t at cum[2 t], delta at cum[2 t + 1]
     const float* wd = cum + 128;
 
     // ---- CS = C S_in (B = S_in [n][p]: 16 rows of n per K step)
-    if (tid == kTidMma) {
+    if (!kStateOnly && tid == kTidMma) {
       tmem_fence_after_sync();
 #pragma unroll
       for (int k = 0; k < N / 16; ++k) {
@@ -342,7 +354,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
       umma_commit(bar_cs);
     }
     // the next chunk's boxes into the other stage (free since the last chunk)
-    if (tid == kTidTma && c + 1 < nch) issue(c + 1);
+    if (tid == kTidTma && ci + 1 < nch) issue(ci + 1);
     // ---- x' = w delta x (state-update operand)
     {
       const float w = wd[row];
@@ -361,10 +373,11 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
       }
     }
     // the next chunk's decays; its successor's dt in flight
-    if (warp == kWarpDecay && c + 1 < nch) {
-      chunk_decays(c + 1);
-      load_dt(c + 2);
+    if (warp == kWarpDecay && ci + 1 < nch) {
+      chunk_decays(ci + 1);
+      load_dt(ci + 2);
     }
+    if constexpr (!kStateOnly) {
     // ---- M[t][s] = G[t][s] e^(cum_t - cum_s) delta_s for s <= t as bf16
     // over Cm box 0, once C B^T and C S_in are done with it
     mbar_wait(bar_g, ph, P.status);
@@ -399,6 +412,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
 #pragma unroll
       for (int q = 0; q < 2; ++q) put8(SM::kCo + s * SM::kBuf, row, s0 / 8 + q, v + 8 * q);
     }
+    }
     fence_proxy_async_smem();
     tmem_fence_before_sync();
     __syncthreads();  // M and x' complete; decays of the next chunk published
@@ -407,19 +421,21 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
       tmem_fence_after_sync();
 #pragma unroll
       for (int k = 0; k < 4; ++k)  // K = s
-        umma_f16(tmem + kColY, dC(s) + (uint64_t)(k * 32 >> 4), dX(s) + (uint64_t)(k * 2048 >> 4), kIdKM,
+        if (!kStateOnly)
+          umma_f16(tmem + kColY, dC(s) + (uint64_t)(k * 32 >> 4), dX(s) + (uint64_t)(k * 2048 >> 4), kIdKM,
                  k > 0 ? 1u : 0u);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         umma_f16(tmem + kColS, dBmn(s) + (uint64_t)(k * 2048 >> 4), dXp + (uint64_t)(k * 2048 >> 4), kIdS, 1u);
       umma_commit(bar_y);
       // the next chunk's G, queued behind this chunk's products
-      if (c + 1 < nch && mbar_wait(&full[s ^ 1], (uint32_t)(((c + 1) >> 1) & 1), P.status)) issue_g(s ^ 1);
+      if (!kStateOnly && ci + 1 < nch && mbar_wait(&full[s ^ 1], (uint32_t)(((ci + 1) >> 1) & 1), P.status))
+        issue_g(s ^ 1);
     }
     mbar_wait(bar_y, ph, P.status);
     tmem_fence_after_sync();
     // ---- y = Y + e^cum CS + D x for this thread's row and half
-    {
+    if constexpr (!kStateOnly) {
       float yv[16], cv[16];
       __syncwarp();
       tmem_ld16x2_16(tquarter + kColY + (uint32_t)(32 * kq), yv);
@@ -448,8 +464,8 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
       float v[32];
       __syncwarp();
       tmem_ld32(tquarter + kColS + (uint32_t)sc, v);
-      if (c + 1 < nch) {
-        if (has_srow)
+      if (ci + 1 < nch) {
+        if (!kStateOnly && has_srow)
 #pragma unroll
           for (int q = 0; q < 4; ++q) put8(SM::kS, srow, 4 * kq + q, v + 8 * q);
         const float dec1 = vec[(s ^ 1) * kVecSet + 192];
@@ -458,7 +474,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
         __syncwarp();
         tmem_st32(tquarter + kColS + (uint32_t)sc, v);
         tmem_wait_st();
-      } else if (P.h_last && has_srow) {
+      } else if (write_last && P.h_last && has_srow) {
         float* hl = P.h_last + (((size_t)b * P.H + h) * N + srow) * kP + sc;
 #pragma unroll
         for (int i = 0; i < 32; i += 2) *reinterpret_cast<float2*>(hl + i) = make_float2(v[i], v[i + 1]);
@@ -472,14 +488,40 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   if (warp == 0) tmem_dealloc(tmem, kTmemColsSsd);
 }
 
-template <int N>
-cudaError_t launch_n(const SsdParams& P, cudaStream_t stream) {
-  auto kern = s6_ssd_fwd_kernel<N>;
+template <int N, bool kStateOnly>
+cudaError_t launch_k(const SsdParams& P, unsigned grid, cudaStream_t stream) {
+  auto kern = s6_ssd_fwd_kernel<N, kStateOnly>;
   const size_t smem = SsdSmem<N>::kBytes + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)(P.B * P.H), kSsdThreads, smem, stream>>>(P);
+  kern<<<grid, kSsdThreads, smem, stream>>>(P);
   return cudaGetLastError();
+}
+
+// With at most half as many sequences as SMs, each sequence is cut in two: a
+// state-only pass over the first half writes the state at the cut into
+// h_last, then one launch runs both halves at once (the second from h_last),
+// every half on an SM of its own.  The state-only pass costs about half a
+// full chunk per chunk, so with more sequences, where halves would share SMs,
+// the cut does not pay.  Needs h_last and four chunks or more.
+template <int N>
+cudaError_t launch_n(SsdParams P, cudaStream_t stream) {
+  const int nch = (P.L + kQ - 1) / kQ;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 0;
+  const long long seqs = (long long)P.B * P.H;
+  if (P.h_last == nullptr || nch < 4 || 2 * seqs > sms) {
+    P.mode = 0;
+    P.seg_chunks = 0;
+    return launch_k<N, false>(P, (unsigned)seqs, stream);
+  }
+  P.seg_chunks = nch / 2;
+  P.mode = 1;
+  cudaError_t e = launch_k<N, true>(P, (unsigned)seqs, stream);
+  if (e != cudaSuccess) return e;
+  P.mode = 2;
+  return launch_k<N, false>(P, (unsigned)(2 * seqs), stream);
 }
 
 }  // namespace

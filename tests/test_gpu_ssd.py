@@ -100,6 +100,23 @@ def test_ssd_deterministic():
         assert torch.equal(y0, y1) and torch.equal(h0, h1)
 
 
+@pytest.mark.parametrize("B,L,H,G,N", [(1, 1000, 8, 2, 128), (2, 777, 4, 1, 64), (1, 256, 2, 1, 128)])
+def test_ssd_split_sequences_match_whole(B, L, H, G, N):
+    """With fewer sequences than SMs and h_last requested, each sequence is cut
+    in two (a state-only pass to the cut, then both halves at once): y equals
+    the uncut walk (no h_last asked) bit for bit, h_last matches the oracle."""
+    x = inputs.make_ssd_inputs(B, L, H, 64, G, N, "bf16", seed=B + L + H, h0_std=0.5)
+    xd = _dev(x)
+    y_split, h_split = s6.ssd_fwd(*[xd[k] for k in KEYS], xd["h0"])
+    y_whole, none = s6.ssd_fwd(*[xd[k] for k in KEYS], xd["h0"], want_h_last=False)
+    s6.check_device_status()
+    assert none is None
+    assert torch.equal(y_split, y_whole)
+    ry, rh = oracle.ssd_fwd(*[x[k] for k in KEYS], x["h0"])
+    assert rel_err(np64(y_split), ry) <= TOL["bf16"]
+    assert rel_err(np64(h_split), rh) <= TOL["bf16"]
+
+
 def test_ssd_empty_sequence_keeps_the_state():
     x = _dev(inputs.make_ssd_inputs(2, 0, 2, 64, 1, 64, "bf16", seed=1, h0_std=0.5))
     y, h_last = s6.ssd_fwd(*[x[k] for k in KEYS], x["h0"])
