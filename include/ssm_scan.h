@@ -301,7 +301,8 @@ int ssm_step_ex(int64_t batch, int64_t dim, int64_t dstate, int act, const void 
  * evaluated in its chunked matrix form (64-step chunks, tensor cores).
  *   x, y [B][L][H][P]; dt_raw [B][L][H]; Bm, Cm [B][L][G][N] (act dtype);
  *   dt_bias, A_log, Dp [H] f32; h0 (nullable: zeros), h_last (nullable)
- *   [B][H][N][P] f32.  opts: the limit on delta (NULL: none).
+ *   [B][H][N][P] f32; h0 and h_last may be the same buffer (the state
+ *   updated in place).  opts: the limit on delta (NULL: none).
  * Supported: act = SSM_BF16, P = headdim = 64, N = dstate in {64, 128},
  * H % G == 0; x, dt_raw, Bm, Cm, y 16-byte aligned.  Other shapes return
  * SSM_ERR_UNSUPPORTED.  Asynchronous on `stream`; allocates nothing.

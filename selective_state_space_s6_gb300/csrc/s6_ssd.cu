@@ -503,7 +503,8 @@ cudaError_t launch_k(const SsdParams& P, unsigned grid, cudaStream_t stream) {
 // h_last, then one launch runs both halves at once (the second from h_last),
 // every half on an SM of its own.  The state-only pass costs about half a
 // full chunk per chunk, so with more sequences, where halves would share SMs,
-// the cut does not pay.  Needs h_last and four chunks or more.
+// the cut does not pay.  Needs h_last (not overlapping h0) and four chunks
+// or more.
 template <int N>
 cudaError_t launch_n(SsdParams P, cudaStream_t stream) {
   const int nch = (P.L + kQ - 1) / kQ;
@@ -511,7 +512,12 @@ cudaError_t launch_n(SsdParams P, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 0;
   const long long seqs = (long long)P.B * P.H;
-  if (P.h_last == nullptr || nch < 4 || 2 * seqs > sms) {
+  // h0 and h_last may be one buffer (the state updated in place): then the
+  // first pass would overwrite h0 before the first halves read it
+  const size_t sbytes = (size_t)seqs * N * kP * sizeof(float);
+  const char *s0 = reinterpret_cast<const char*>(P.h0), *s1 = reinterpret_cast<const char*>(P.h_last);
+  const bool overlap = s0 && s1 && s0 < s1 + sbytes && s1 < s0 + sbytes;
+  if (P.h_last == nullptr || overlap || nch < 4 || 2 * seqs > sms) {
     P.mode = 0;
     P.seg_chunks = 0;
     return launch_k<N, false>(P, (unsigned)seqs, stream);

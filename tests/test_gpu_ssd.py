@@ -117,6 +117,20 @@ def test_ssd_split_sequences_match_whole(B, L, H, G, N):
     assert rel_err(np64(h_split), rh) <= TOL["bf16"]
 
 
+def test_ssd_state_in_place():
+    """h0 and h_last as one buffer (the state updated in place), on a shape
+    that would otherwise be cut in two: same y and final state as separate
+    buffers."""
+    x = _dev(inputs.make_ssd_inputs(1, 1000, 8, 64, 2, 128, "bf16", seed=41, h0_std=0.5))
+    y_ref, h_ref = s6.ssd_fwd(*[x[k] for k in KEYS], x["h0"])
+    state = x["h0"].clone()
+    y_in, h_in = s6.ssd_fwd(*[x[k] for k in KEYS], state, h_last=state)
+    s6.check_device_status()
+    assert h_in.data_ptr() == state.data_ptr()
+    assert torch.equal(y_in, y_ref)
+    assert torch.equal(state, h_ref)
+
+
 def test_ssd_empty_sequence_keeps_the_state():
     x = _dev(inputs.make_ssd_inputs(2, 0, 2, 64, 1, 64, "bf16", seed=1, h0_std=0.5))
     y, h_last = s6.ssd_fwd(*[x[k] for k in KEYS], x["h0"])
