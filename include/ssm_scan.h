@@ -126,6 +126,14 @@ int64_t ssm_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t dim, int6
 int ssm_plan_segments(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
                       int *fwd_segments, int *bwd_segments);
 
+/* Number of calls since the library was loaded (all threads and devices)
+ * whose plan's cooperative mode -- the forward's stream mode, the backward's
+ * hand-over mode -- could not be resident at once on the GPU (another SM
+ * count or shared-memory size than the plans assume) and that ran in the
+ * non-cooperative form instead: same results, bit for bit, but slower.
+ * Host-only; never fails. */
+int64_t ssm_plan_fallbacks(void);
+
 /*
  * Forward scan with saves for the backward (mamba-rs kernels.rs page:
  * MambaKernels "Multi-step SSM forward with activation saves for backward").
@@ -215,8 +223,9 @@ int ssm_scan_bwd_finalize(int64_t batch, int64_t seqlen, int64_t dim, int64_t ds
  *   - Shapes needing more scratch than that (ssm_bwd_workspace_bytes() >
  *     ssm_noalloc_scratch_bytes()) are rejected with SSM_ERR_UNSUPPORTED.
  *   - The first call on a device looks the array's device address up with
- *     cudaGetSymbolAddress (that device current); make it before any stream
- *     capture.
+ *     cudaGetSymbolAddress (that device current), and so does the first call
+ *     after that device's context was reset (cudaDeviceReset: the array may
+ *     then sit elsewhere); make those calls before any stream capture.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents; calls whose GPU work may overlap race on it and must be
  *     ordered by the caller (same stream, or events).

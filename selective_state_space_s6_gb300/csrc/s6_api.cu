@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "s6_internal.cuh"
@@ -17,18 +18,62 @@ namespace s6 {
 // clears it.  One copy per device; its address is looked up per device.
 __device__ unsigned int g_s6_status = 0;
 
-unsigned int* device_status_word() {
-  static std::mutex mu;
-  static unsigned int* addr[64] = {nullptr};
+void* current_context() {
+  using GetCtx = int (*)(void**);  // cuCtxGetCurrent(CUcontext*), CUresult 0 = success
+  static GetCtx fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (GetCtx) nullptr;
+    return reinterpret_cast<GetCtx>(f);
+  }();
+  void* ctx = nullptr;
+  if (!fn || fn(&ctx) != 0) return nullptr;
+  return ctx;
+}
+
+cudaError_t symbol_address(SymbolCache& cache, const void* symbol, void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* a = nullptr;
-    if (cudaGetSymbolAddress(&a, g_s6_status) != cudaSuccess) return nullptr;
-    addr[dev] = static_cast<unsigned int*>(a);
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= SymbolCache::kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(cache.mu);
+  void* ctx = current_context();
+  if (!cache.addr[dev] || !ctx || cache.ctx[dev] != ctx) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, symbol);
+    if (e != cudaSuccess) return e;
+    cache.addr[dev] = p;
+    cache.ctx[dev] = current_context();  // the lookup made the device's context current
   }
-  return addr[dev];
+  *out = cache.addr[dev];
+  return cudaSuccess;
+}
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int sms[SymbolCache::kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= SymbolCache::kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (sms[dev] <= 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    sms[dev] = n;
+  }
+  return sms[dev];
+}
+
+static std::atomic<long long> g_plan_fallbacks{0};
+void note_plan_fallback() { g_plan_fallbacks.fetch_add(1, std::memory_order_relaxed); }
+long long plan_fallbacks() { return g_plan_fallbacks.load(std::memory_order_relaxed); }
+
+unsigned int* device_status_word() {
+  static SymbolCache cache;
+  void* a = nullptr;
+  if (symbol_address(cache, &g_s6_status, &a) != cudaSuccess) return nullptr;
+  return static_cast<unsigned int*>(a);
 }
 
 }  // namespace s6
@@ -326,6 +371,8 @@ int64_t ssm_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t dim, int6
   if (check_shape(batch, seqlen, dim, dstate, act) != SSM_OK) return -1;
   return bwd_ws_layout(batch, seqlen, dim, dstate).total;
 }
+
+int64_t ssm_plan_fallbacks(void) { return (int64_t)s6::plan_fallbacks(); }
 
 int ssm_plan_segments(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int act,
                       int* fwd_segments, int* bwd_segments) {

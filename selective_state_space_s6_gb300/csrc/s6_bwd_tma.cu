@@ -995,6 +995,7 @@ cudaError_t launch_tpc(BwdTmaParams& P, BwdTmaParams& Pagg, cudaStream_t stream)
     e = launch_main<Act, TPC, kFast>(P, stream, true);
     if (e != cudaErrorCooperativeLaunchTooLarge) return e;
     (void)cudaGetLastError();  // not resident at once on this GPU: aggregate mode
+    note_plan_fallback();
   }
   P.p.seq_flag = nullptr;
   Pagg.p.seq_flag = nullptr;

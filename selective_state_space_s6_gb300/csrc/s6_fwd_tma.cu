@@ -475,11 +475,10 @@ cudaError_t launch_stream(const FwdTmaParams& P, cudaStream_t stream) {
   const size_t smem = std::max<size_t>(fwd_smem_bytes<Act, TPC>(), kStreamSmemFloor);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  int per_sm = 0, sms = 0, dev = 0;
+  int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFwdWarps * 32, smem);
-  if (e == cudaSuccess) e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
+  const int sms = device_sm_count();
   if (per_sm != 3 || (long long)per_sm * sms < P.p.plan.P) return cudaErrorCooperativeLaunchTooLarge;
   e = cudaMemsetAsync(P.p.seq_flag, 0, sizeof(int) * (size_t)P.p.B * P.p.plan.ndt, stream);
   if (e != cudaSuccess) return e;
@@ -502,6 +501,7 @@ cudaError_t launch_one(const FwdTmaParams& P, cudaStream_t stream) {
     const cudaError_t e = launch_stream<Act, TPC, kSave, kFast, kGate>(P, stream);
     if (e != cudaErrorCooperativeLaunchTooLarge) return e;
     (void)cudaGetLastError();  // not three resident per SM here: the grid mode gives the same result
+    note_plan_fallback();
   }
   if (P.p.nseg > 1) {
     // chunked parallel scan: segment aggregates -> carries -> all segments at once

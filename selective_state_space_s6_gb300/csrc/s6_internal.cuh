@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "ssm_scan.h"
 
 namespace s6 {
@@ -168,6 +170,26 @@ cudaError_t launch_step(const FwdParams& p, int act, cudaStream_t stream);
 int fwd_segments(int B, int L, int D, int N, int sms);
 // Device address of the library's status word on the current device (nullptr on error).
 unsigned int* device_status_word();
+// The calling thread's current CUDA context (driver handle), or nullptr.
+void* current_context();
+// Device addresses of a __device__ variable, one per device, looked up with
+// cudaGetSymbolAddress (the device current) on first use and again whenever
+// the device's context has changed since (e.g. after cudaDeviceReset, which
+// reloads the module: the variable may then sit at another address).
+struct SymbolCache {
+  static constexpr int kMaxDevices = 64;
+  std::mutex mu;
+  void* addr[kMaxDevices] = {nullptr};
+  void* ctx[kMaxDevices] = {nullptr};
+};
+cudaError_t symbol_address(SymbolCache& cache, const void* symbol, void** out);
+// SM count of the current device, queried once per device (0 on error).
+int device_sm_count();
+// Counts a call whose planned cooperative mode (forward stream mode, backward
+// hand-over mode) could not be resident on this GPU and ran in its
+// non-cooperative form instead (same results, slower); ssm_plan_fallbacks().
+void note_plan_fallback();
+long long plan_fallbacks();
 // Sets the calling thread's ssm_last_error() message; returns `code`.
 int report_error(int code, const char* fmt, ...);
 cudaError_t launch_bwd(const BwdParams& p, int act, cudaStream_t stream);

@@ -16,8 +16,9 @@
 //     ssm_bwd_workspace_bytes() exceeds that is rejected with
 //     SSM_ERR_UNSUPPORTED before anything is enqueued;
 //   - the first call on a device looks the array's device address up
-//     (cudaGetSymbolAddress) with that device current; make that first call
-//     before any stream capture;
+//     (cudaGetSymbolAddress) with that device current, and so does the first
+//     call after the device's context was reset (cudaDeviceReset reloads the
+//     library's device image); make those calls before any stream capture;
 //   - every call on a device shares the one array, which keeps the last
 //     call's contents: calls whose GPU work overlaps (different streams
 //     without ordering between them) race on it.  Nothing in the array has
@@ -32,28 +33,14 @@ constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
+s6::SymbolCache g_scratch_cache;
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device.  In host code the symbol names a host-side stand-in, not device
-// memory, so kernels must only ever be given this looked-up address.
-cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
-  return cudaSuccess;
-}
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the symbol names a host-side stand-in, not device memory, so kernels must
+// only ever be given this looked-up address.  It is looked up once per device
+// (and again if the device's context was reset since, as the array may then
+// have moved).
+cudaError_t scratch_address(void** out) { return s6::symbol_address(g_scratch_cache, &g_noalloc_scratch, out); }
 
 }  // namespace
 

@@ -508,9 +508,7 @@ cudaError_t launch_k(const SsdParams& P, unsigned grid, cudaStream_t stream) {
 template <int N>
 cudaError_t launch_n(SsdParams P, cudaStream_t stream) {
   const int nch = (P.L + kQ - 1) / kQ;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    sms = 0;
+  const int sms = device_sm_count();  // cached per device (0 on error: no cut)
   const long long seqs = (long long)P.B * P.H;
   // h0 and h_last may be one buffer (the state updated in place): then the
   // first pass would overwrite h0 before the first halves read it

@@ -219,11 +219,11 @@ cudaError_t launch_step_tpc(const FwdParams& p, cudaStream_t stream) {
   auto kern = p.z ? s6_step_kernel<Act, TPC, kFast, true> : s6_step_kernel<Act, TPC, kFast, false>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  int dev = 0, sms = 0, per_sm = 0;
-  err = cudaGetDevice(&dev);
-  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (err == cudaSuccess) err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kStepConsumers + 32, smem);
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kStepConsumers + 32, smem);
   if (err != cudaSuccess) return err;
+  const int sms = device_sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
   // channel tiles x batch-row groups, all resident at once
   P.ndt = (p.D + T::kCh - 1) / T::kCh;
   const int nblk = (p.B + T::R - 1) / T::R;

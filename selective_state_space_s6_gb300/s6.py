@@ -107,6 +107,8 @@ def load_library():
         lib.ssm_selftest_wait_timeout.restype = ci
         lib.ssm_plan_segments.argtypes = [i64] * 4 + [ci, ctypes.POINTER(ci), ctypes.POINTER(ci)]
         lib.ssm_plan_segments.restype = ci
+        lib.ssm_plan_fallbacks.argtypes = []
+        lib.ssm_plan_fallbacks.restype = i64
         _lib = lib
         return lib
 
@@ -159,6 +161,12 @@ def plan_segments(batch, seqlen, dim, dstate, act):
     _check("ssm_plan_segments", load_library().ssm_plan_segments(batch, seqlen, dim, dstate, act,
                                                                   ctypes.byref(f), ctypes.byref(b)))
     return f.value, b.value
+
+
+def plan_fallbacks():
+    """Calls so far whose cooperative plan mode (forward stream mode, backward
+    hand-over mode) did not fit on the GPU and ran non-cooperatively instead."""
+    return int(load_library().ssm_plan_fallbacks())
 
 
 def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]):

@@ -1,11 +1,10 @@
 """Parity of the CUDA path (through the C ABI) with the f64 oracle.
 
 Small shapes are compared element by element on every output; they span
-several 64-channel tiles and 64-step chunks with ragged tails, every state
-count 1..16 (padded lanes), with and without the gate, initial state and
-final-state gradient.  Full-size workloads are compared on sampled channels
-(every batch, every step) and, for the channel sums dBm/dCm, on one whole
-batch, all in the launch configuration the benchmark times.
+several channel tiles and chunks with ragged tails, every state count 1..16
+(padded lanes), with and without the gate, initial state and final-state
+gradient.  The full-size workloads are compared element by element on every
+output too, in the launch configuration the benchmark times.
 """
 import hashlib
 
@@ -193,94 +192,43 @@ def test_extreme_decay_and_skip():
 
 # ------------------------------------------------------------------ full-size workloads
 
-def _windows(D):
-    # tile edges and the middle: channels 0..3, D/2-2..D/2+1, D-4..D-1
-    return [(0, 4), (D // 2 - 2, D // 2 + 2), (D - 4, D)]
-
-
 BLD = ("u", "delta_raw", "z", "dout")
-PER_D = ("A_log", "Dp", "delta_bias")
 
 
-def slice_problem(x, b=None, d=None):
-    """The sub-problem on batches ``b`` / channels ``d`` (slices).  Channels are
-    independent scans, so every per-channel output of the sub-problem equals the
-    full problem's; only the channel sums dBm/dCm become partial sums."""
-    bs = b if b is not None else slice(None)
-    ds = d if d is not None else slice(None)
+def _batch_rows(x, b0, b1):
+    """The sub-problem on batch rows b0..b1-1 (per-batch inputs sliced, parameters kept)."""
     y = {}
     for k, v in x.items():
-        if v is None:
-            y[k] = None
-        elif k in BLD:
-            y[k] = v[bs, :, ds].contiguous()
-        elif k in ("Bm", "Cm"):
-            y[k] = v[bs].contiguous()
-        elif k in PER_D:
-            y[k] = v[ds].contiguous()
-        elif k in ("h0", "dh_last"):
-            y[k] = v[bs, ds].contiguous()
-        else:
+        if v is None or k in ("A_log", "Dp", "delta_bias"):
             y[k] = v
+        else:
+            y[k] = v[b0:b1].contiguous()
     return y
 
 
-def _check_sampled(x, gpu, act):
-    """Per-channel outputs and parameter gradients on sampled channel windows."""
-    tol = TOL[act]
-    errs = {}
-    for (d0, d1) in _windows(x["u"].shape[2]):
-        ref = oracle_fwd_bwd(slice_problem(x, d=slice(d0, d1)))
-        for k in ("out", "du", "d_delta_raw", "dz"):
-            errs[(k, d0)] = rel_err(np64(gpu[k][:, :, d0:d1]), ref[k])
-        errs[("h_last", d0)] = rel_err(np64(gpu["h_last"][:, d0:d1]), ref["h_last"])
-        for k in ("dA_log", "dD", "d_delta_bias"):
-            errs[(k, d0)] = rel_err(np64(gpu[k][d0:d1]), ref[k])
-    bad = {k: v for k, v in errs.items() if not v <= tol}
-    assert not bad, f"sampled errors above {tol}: {bad}"
-    return errs
-
-
-@pytest.mark.parametrize("name", ["mamba130m", "mamba1p4b"])
-def test_full_size_training_workloads(name):
+@pytest.mark.parametrize("name", ["mamba130m", "mamba1p4b", "long"])
+def test_full_size_every_output(name):
+    """The full-size workloads, in the launch configuration the benchmark
+    times: every element of every output and gradient (out, h_last, du,
+    d_delta_raw, dz, dBm, dCm, dA_log, dDp, d_delta_bias, dh0) against the
+    oracle on the whole problem, at the workload's tolerance."""
     x = inputs.make_workload(name)
     act = inputs.WORKLOADS[name].act
     xd = to_dev(x)
-    gpu = gpu_fwd_bwd(xd)
-    _check_sampled(x, gpu, act)
-    # channel sums dBm / dCm: one whole batch against the oracle over all channels
-    B = x["u"].shape[0]
-    xb = slice_problem(x, b=slice(B - 1, B))
-    ref = oracle.bwd(*[xb[k] for k in ARGS], None, xb["dout"])
-    for k in ("dBm", "dCm"):
-        assert rel_err(np64(gpu[k][B - 1:]), ref[k]) <= TOL[act], k
-    # bit-identical on repeat
-    d1 = _digest([gpu[k] for k in GRAD_KEYS])
-    d2 = _digest([v for k, v in gpu_fwd_bwd(xd).items() if k in GRAD_KEYS])
-    assert d1 == d2
-
-
-def test_full_size_long_sequence():
-    name = "long"
-    x = inputs.make_workload(name)
-    xd = to_dev(x)
-    gpu = gpu_fwd_bwd(xd)
-    _check_sampled(x, gpu, "f32")
-    # channel sums over a 128-channel slice (two tiles): the scan restricted to channels 0..127
-    sl = slice_problem(x, d=slice(0, 128))
-    gs = gpu_fwd_bwd(to_dev(sl))
-    ref = oracle.bwd(*[sl[k] for k in ARGS], None, sl["dout"])
-    for k in ("dBm", "dCm"):
-        assert rel_err(np64(gs[k]), ref[k]) <= TOL["f32"], k
-    # whole-problem identity at any size: sum dBm*Bm = sum (du - Dp*dy) * u
-    z = xd["z"].double()
-    dy = xd["dout"].double() * z * torch.sigmoid(z)
-    lhs = (gpu["dBm"].double() * xd["Bm"].double()).sum()
-    rhs = ((gpu["du"].double() - xd["Dp"].double() * dy) * xd["u"].double()).sum()
-    assert abs(float(lhs - rhs)) <= 1e-4 * float(torch.abs(gpu["dBm"].double() * xd["Bm"].double()).sum())
+    gpu = gpu_fwd_bwd(xd, dh_last=xd["dh_last"])
+    gpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in gpu.items()}
+    del xd
+    torch.cuda.empty_cache()
+    ref = oracle_fwd_bwd(x, dh_last=x["dh_last"])
+    errs = compare_all(gpu, ref, TOL[act])
+    assert set(errs) >= {"out", "h_last", "du", "d_delta_raw", "dz", "dBm", "dCm", "dA_log", "dD",
+                         "d_delta_bias", "dh0"}, errs
 
 
 def test_decode_1000_chained_steps():
+    """1000 chained decode steps (B=256, D=1536, N=16, f32) equal the scan over
+    the same tokens bit for bit, and every output and the final state match
+    the oracle's scan (compared in slices of 32 batch rows)."""
     w = inputs.WORKLOADS["decode"]
     x = inputs.make_workload("decode", with_dout=False)
     xd = to_dev(x)
@@ -293,13 +241,19 @@ def test_decode_1000_chained_steps():
     out_scan, h_scan, _ = s6.ssm_scan_fwd(*[xd[k] for k in ARGS], xd["h0"], save=False)
     assert torch.equal(out_steps, out_scan)
     assert torch.equal(h, h_scan)
-    errs = []
-    for (d0, d1) in _windows(w.dim):
-        xs = slice_problem(x, d=slice(d0, d1))
+    out_cpu, h_cpu = out_steps.cpu(), h.cpu()
+    del xd, out_steps, out_scan, h_scan
+    torch.cuda.empty_cache()
+    diff_o = diff_h = scale_o = scale_h = 0.0
+    for b0 in range(0, w.batch, 32):
+        xs = _batch_rows(x, b0, min(w.batch, b0 + 32))
         ref_out, ref_h = oracle.fwd(*[xs[k] for k in ARGS], xs["h0"])
-        errs.append(rel_err(np64(out_steps[:, :, d0:d1]), ref_out))
-        errs.append(rel_err(np64(h[:, d0:d1]), ref_h))
-    assert max(errs) <= TOL["f32"], errs
+        diff_o = max(diff_o, float(np.max(np.abs(np64(out_cpu[b0:b0 + 32]) - ref_out))))
+        diff_h = max(diff_h, float(np.max(np.abs(np64(h_cpu[b0:b0 + 32]) - ref_h))))
+        scale_o = max(scale_o, float(np.max(np.abs(ref_out))))
+        scale_h = max(scale_h, float(np.max(np.abs(ref_h))))
+    assert diff_o / scale_o <= TOL["f32"], diff_o / scale_o
+    assert diff_h / scale_h <= TOL["f32"], diff_h / scale_h
 
 
 @pytest.mark.parametrize("B,L,D,N,act", [(4, 256, 2560, 16, "bf16"), (3, 192, 4096, 16, "f32")])
