@@ -70,7 +70,7 @@ typedef enum {
 typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
 
 /* Steps between saved chunk states (the forward's checkpoints for the backward). */
-#define SSM_CHUNK_LEN 64
+#define SSM_CHUNK_LEN 32
 /* Largest supported state size N. */
 #define SSM_MAX_DSTATE 16
 

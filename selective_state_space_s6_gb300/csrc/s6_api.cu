@@ -179,17 +179,21 @@ FwdWorkspace fwd_ws_layout(int64_t B, int64_t L, int64_t D, int64_t N, int act) 
 struct BwdWorkspace {
   s6::BwdPlan plan;
   int nseg;
-  int64_t dbc_off, dbc_bytes, param_off, param_bytes, agg_off, carry_off, flag_off, total;
+  int64_t hdr_off, dbc_off, dbc_bytes, param_off, param_bytes, agg_off, carry_off, flag_off, total;
 };
 
 BwdWorkspace bwd_ws_layout(int64_t B, int64_t L, int64_t D, int64_t N) {
   BwdWorkspace w;
   w.plan = s6::bwd_plan((int)B, (int)L, (int)D, (int)N, kPlanSms);
   w.nseg = w.plan.maxp;
+  // tile rows of the dBm/dCm partials: 128-channel tiles (TMA kernel) or
+  // 64-channel tiles (generic kernel); room for the larger count.  The kernel
+  // that fills them writes their count into the header at offset 0.
   const int64_t ndt = (D + s6::kDTile - 1) / s6::kDTile;
-  w.dbc_off = 0;
+  w.hdr_off = 0;
+  w.dbc_off = 256;
   w.dbc_bytes = ndt * B * L * 2 * N * (int64_t)sizeof(float);
-  w.param_off = align_up(w.dbc_bytes, 256);
+  w.param_off = align_up(w.dbc_off + w.dbc_bytes, 256);
   w.param_bytes = B * w.nseg * D * (N + 2) * (int64_t)sizeof(float);
   w.agg_off = align_up(w.param_off + w.param_bytes, 256);
   const int64_t cells = w.nseg > 1 ? B * w.nseg * D * N : 0;
@@ -463,6 +467,7 @@ int ssm_scan_bwd_partials_ex(int64_t batch, int64_t seqlen, int64_t dim, int64_t
   p.dout = dout; p.dh_last = dh_last; p.du = du; p.d_delta_raw = d_delta_raw; p.dz = dz;
   p.dh0 = dh0;
   p.ws_dbc = reinterpret_cast<float*>(static_cast<char*>(ws) + w.dbc_off);
+  p.ws_ndt = reinterpret_cast<int*>(static_cast<char*>(ws) + w.hdr_off);
   p.ws_param = reinterpret_cast<float*>(static_cast<char*>(ws) + w.param_off);
   p.B = (int)B; p.L = (int)L; p.D = (int)D; p.N = (int)N;
   p.nchunks = (int)ssm_num_chunks(L);
@@ -512,7 +517,7 @@ int ssm_scan_bwd_finalize(int64_t batch, int64_t seqlen, int64_t dim, int64_t ds
   const float* ws_param = reinterpret_cast<const float*>(static_cast<const char*>(ws) + w.param_off);
   cudaError_t ce;
   if (B > 0) {
-    const int ndt = (int)((D + s6::kDTile - 1) / s6::kDTile);
+    const int* ndt = reinterpret_cast<const int*>(static_cast<const char*>(ws) + w.hdr_off);
     ce = s6::launch_reduce_dbc(ws_dbc, ndt, (int)B, (int)L, (int)N, dBm, dCm, act, st);
     if (ce != cudaSuccess) return cuda_fail(ce, "ssm_scan_bwd_finalize dBm/dCm reduction");
   }

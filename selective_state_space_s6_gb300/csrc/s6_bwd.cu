@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(kScanThreads)
   const int dl = tid >> 1;
   const int d = blockIdx.x * kDTile + dl;
   const int b = blockIdx.y;
+  if (blockIdx.x == 0 && b == 0 && tid == 0) *p.ws_ndt = gridDim.x;  // tile rows of ws_dbc, for the finalize
   const bool dvalid = d < p.D;
   const int dc = dvalid ? d : p.D - 1;
   const int L = p.L, D = p.D, N = p.N;
@@ -243,9 +244,10 @@ __global__ void __launch_bounds__(kScanThreads)
 
 // dBm/dCm[b,t,n] = sum over channel tiles k (ascending) of ws_dbc[k][b][t][q][n]
 template <typename Act>
-__global__ void s6_reduce_dbc_kernel(const float* __restrict__ ws, int ndt, int B, int L, int N,
-                                     Act* __restrict__ dBm, Act* __restrict__ dCm) {
+__global__ void s6_reduce_dbc_kernel(const float* __restrict__ ws, const int* __restrict__ ndt_ptr, int B, int L,
+                                     int N, Act* __restrict__ dBm, Act* __restrict__ dCm) {
   const size_t per = (size_t)B * L * 2 * N;
+  const int ndt = *ndt_ptr;
   for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < per;
        e += (size_t)gridDim.x * blockDim.x) {
     float s = 0.f;
@@ -304,7 +306,7 @@ cudaError_t launch_bwd(const BwdParams& p, int act, cudaStream_t stream) {
   return act == SSM_BF16 ? launch_bwd_t<__nv_bfloat16>(p, stream) : launch_bwd_t<float>(p, stream);
 }
 
-cudaError_t launch_reduce_dbc(const float* ws_dbc, int ndt, int B, int L, int N, void* dBm,
+cudaError_t launch_reduce_dbc(const float* ws_dbc, const int* ndt, int B, int L, int N, void* dBm,
                               void* dCm, int act, cudaStream_t stream) {
   const size_t per = (size_t)B * L * 2 * N;
   if (per == 0) return cudaSuccess;

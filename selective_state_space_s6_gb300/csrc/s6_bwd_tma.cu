@@ -1,36 +1,41 @@
-// S6 backward, TMA-pipelined (sm_103a).
+// S6 backward, TMA-pipelined, every state of a chunk in tensor memory (sm_103a).
 //
-// CTA = (64-channel tile, batch, time segment), 2*TPC + 3 warps: 2*TPC
-// consumer warps (TPC = N/4 lanes per channel, 4 states per lane), a TMA
-// producer warp, a converter warp (bf16: Bm/Cm tiles widened to f32 once per
-// tile) and a reducer warp (cross-warp sums of the dBm/dCm terms).
+// A persistent CTA walks a range of chunk units (plan: 152 equal ranges over
+// all (batch, 128-channel tile, 32-step chunk) units); each unit is one
+// 32-step chunk of 128 channels.  Warps: 2*TPC consumers (TPC = N/4), a TMA
+// producer, a converter (bf16: Bm/Cm rows widened to f32 once per chunk) and
+// a reducer (cross-warp sums of the dBm/dCm terms).
 //
-// Each lane walks its chunks (SSM_CHUNK_LEN = 64 steps, restarted from the
-// forward's chunk states) from last to first.  The producer streams each
-// chunk twice through an S-stage ring of 32-step tiles:
-//   pass A (tiles in forward order; delta_raw, u, Bm): recompute h from the
-//     chunk state, store (delta, delta*u) in shared memory for the chunk and
-//     every state of the chunk in tensor memory (TMEM: 64 steps x 4 states
-//     per lane, 8 steps per 32-column store);
-//   pass B (tiles in reverse order; all inputs): for each 8-step sub-chunk,
-//     last first, load its 8 states from TMEM into registers, then step
-//     backward with the adjoint g_t = dy_t*C_t + Abar_{t+1}*g_{t+1}, producing
-//     du, d_delta_raw, dz and the dBm/dCm/dA_log/dDp/d_delta_bias terms.
-// (The second read of a chunk's tiles comes from L2.)
+// Consumer lane (pair cp, group q) owns channels d0 + 2cp, d0 + 2cp + 1 and
+// states 4q .. 4q+3 of both: 8 cells per step, two packed f32x2 operations per
+// channel for each arithmetic step.  Per chunk, last chunk of the piece first:
+//   prep A: delta = softplus(delta_raw + bias) and delta*u of the lane's owned
+//     steps (step k with k % TPC == q inside every 4-step group) for both
+//     channels, into shared memory;
+//   pass A: the recurrence h_t = Abar_t h_{t-1} + delta*u*B_t from the saved
+//     chunk state, every state stored to tensor memory (8 columns per step,
+//     32 columns = 4 steps per tcgen05.st);
+//   pass B: 4-step sub-chunks, last first: the gate terms dy = dout*silu(z)
+//     and the dz factor of the owned steps, then the adjoint
+//     g_t = dy_t C_t + Abar_{t+1} g_{t+1} backwards with the states loaded from
+//     tensor memory, producing every gradient term of the step, then the
+//     outputs du, d_delta_raw, dz of the owned steps.
+// The tile's u, delta_raw, z, dout, Bm, Cm rows stay in one shared-memory stage
+// for both passes (the chunk is read from HBM once).
 //
-// Per step, the channel sums of the dBm and dCm terms over the CTA's 64
-// channels are taken in shared memory in a fixed order (within a warp: 4
-// channels per lane with packed adds, then an xor butterfly over the lane
-// groups; then the warps in ascending order) and stored as one partial per
-// CTA; the sums over t of the parameter terms stay in registers per chunk
-// and are added into per-lane totals with a compensated (Kahan) add.  A small
-// kernel adds the partials in ascending tile / batch order (s6_bwd.cu).  No
-// floating-point atomics: results are bit-identical from run to run (the
-// single-writer, fixed-order policy of deterministic_backward.py).
-//
-// Work that depends only on (t, d) -- softplus, the gate's sigmoid, dy, the
-// softplus derivative, the outputs du / d_delta_raw / dz -- is done for step
-// k by lane k % TPC of the channel and shared through shared memory.
+// Sums (the single-writer, fixed-order policy of deterministic_backward.py,
+// with the kernels.rs page's local-backward / reduction split):
+//   - over the 16 states of a channel (y, sum g*B, sum A*p): each lane adds its
+//     4 in registers, the TPC lanes of the pair are added in lane order by the
+//     lane that writes the step's outputs;
+//   - over channels (dBm, dCm): each lane adds its 2 channels inside the FMAs,
+//     a 3-round xor reduce-scatter adds the warp's lanes, the reducer warp adds
+//     the warps in ascending order into the tile's partial row, and a small
+//     kernel adds the tiles in ascending order (s6_bwd.cu);
+//   - over (b, t) (dA_log, dDp, d_delta_bias): per lane per chunk, then a
+//     compensated (Kahan) running total per piece, then the pieces and batches
+//     in ascending order (s6_bwd.cu).
+// No floating-point atomics: bit-identical results from run to run.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -46,19 +51,11 @@ namespace s6 {
 
 namespace {
 
-constexpr int kTT = 32;           // steps per tile
+constexpr int kTT = 32;       // steps per tile (the forward's and the aggregate pass's tiles)
+constexpr int kSC = 4;        // pass B: steps per sub-chunk (32 TMEM columns)
 constexpr int kAggWarps = 6;  // aggregate pass: 4 consumer warps + producer + converter
-template <typename Act>
-struct BwdStages {
-  static constexpr int value = std::is_same<Act, float>::value ? 2 : 3;
-};
-// Warp-local reduction scratch of one step: two blocks (dBm terms, dCm terms),
-// each holding one 16-byte chunk (a lane's 4 states) per lane in lane order,
-// padded to 144 floats so that the 64-bit reads of a half-warp hit distinct
-// banks.  Two step slots per warp.
-constexpr int kRedBlock = 32 * 4 + 16;
-constexpr int kRedSlot = 2 * kRedBlock;
-constexpr int kRedSlots = 2;
+constexpr int kBS = 2;        // stages of the main kernel's ring (one chunk each)
+static_assert(kChunk == kTT, "the backward's chunk is one tile");
 
 struct BwdTmaParams {
   CUtensorMap map_u, map_raw, map_z, map_dout, map_B, map_C;
@@ -72,62 +69,118 @@ __device__ __forceinline__ void kahan_add(float& sum, float& comp, float x) {
   sum = t;
 }
 
-// Row stride (float2) of the per-step channel arrays dbuf / bprep: 64 + 4, so
-// that consecutive rows (read at once by the lanes of a channel, which own
-// consecutive steps) start 32 bytes apart in the banks: a half-warp's 64-bit
-// accesses (4 channels x 4 rows) then fill the 32 banks once.
-constexpr int kRow = kDTile + 4;
-
-// activation at a byte offset of a (swizzled) tile
+// two adjacent activations at a byte offset of a (swizzled) tile
+__device__ __forceinline__ float2 lds_pair(const float* tile, int byte_off) {
+  return *reinterpret_cast<const float2*>(reinterpret_cast<const unsigned char*>(tile) + byte_off);
+}
+__device__ __forceinline__ float2 lds_pair(const __nv_bfloat16* tile, int byte_off) {
+  return __bfloat1622float2(
+      *reinterpret_cast<const __nv_bfloat162*>(reinterpret_cast<const unsigned char*>(tile) + byte_off));
+}
+// one activation at a byte offset of a (swizzled) tile
 template <typename Act>
 __device__ __forceinline__ float lds_at(const Act* tile, int byte_off) {
   return lds_act(reinterpret_cast<const Act*>(reinterpret_cast<const unsigned char*>(tile) + byte_off));
 }
+// store two adjacent outputs
+__device__ __forceinline__ void st_pair(float* p, float2 v) { *reinterpret_cast<float2*>(p) = v; }
+__device__ __forceinline__ void st_pair(__nv_bfloat16* p, float2 v) {
+  *reinterpret_cast<__nv_bfloat162*>(p) = __float22bfloat162_rn(v);
+}
 
-// TPC lanes per channel, 4 states per lane (N = 4 * TPC); a CTA covers 64
-// channels with 64 * TPC consumer threads (2 * TPC warps), plus a producer
-// and a converter warp.  kLimit: delta is clamped to [dt_min, dt_max] (a
-// separate instance, so the unlimited scan pays nothing for it).
+// load 8 consecutive columns of this thread's lane and wait
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// issue a load of 8 consecutive columns of this thread's lane (no wait)
+__device__ __forceinline__ void tmem_ld8_issue(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+}
+// wait for this thread's TMEM loads; the destination of the last one passes
+// through the statement, so nothing reads it before the wait
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[8]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
+               :
+               : "memory");
+}
+
+template <typename Act, int TPC>
+struct BwdLayout {
+  static constexpr int N = 4 * TPC;
+  static constexpr int kLanes = 64 * TPC;  // consumer threads: 64 channel pairs x TPC
+  static constexpr int kCW = kLanes / 32;  // consumer warps
+  static constexpr bool kBf16 = std::is_same<Act, __nv_bfloat16>::value;
+  using AT = SwzTile<Act, kBwdTile, kTT>;  // u, delta_raw, z, dout tiles
+  static constexpr int kTileB = kTT * kBwdTile * (int)sizeof(Act);
+  static constexpr int kBCB = kTT * N * (int)sizeof(Act);
+  // stage: u, raw, z, dout tiles, then the Bm and Cm rows; 1024-byte multiple
+  static constexpr int kStageB = ((4 * kTileB + 2 * kBCB) + 1023) / 1024 * 1024;
+  static constexpr int kBcfB = kBf16 ? kBS * kTT * 2 * N * 4 : 0;  // f32 Bm/Cm rows [S][TT][2][N]
+  static constexpr int kPAB = kTT * 64 * 16;                     // pA [TT][64 pairs] float4
+  static constexpr int kPYB = kSC * 64 * 8;                      // pY [SC][64 pairs] float2
+  static constexpr int kPart4B = kSC * kLanes * 16;              // [SC][lanes] (y0, gB0, y1, gB1)
+  static constexpr int kPart2B = kSC * kLanes * 8;               // [SC][lanes] (Ap0, Ap1)
+  static constexpr int kDsumB = 2 * kSC * kCW * 32 * 4;          // [2 slots][SC][kCW][32]
+  static constexpr int kTotB = 2 * 12 * kLanes * 4;              // [2 (sum, comp)][12][lanes] running totals
+  static constexpr int kOffBcf = kBS * kStageB;
+  static constexpr int kOffPA = kOffBcf + kBcfB;
+  static constexpr int kOffPY = kOffPA + kPAB;
+  static constexpr int kOffPart4 = kOffPY + kPYB;
+  static constexpr int kOffPart2 = kOffPart4 + kPart4B;
+  static constexpr int kOffDsum = kOffPart2 + kPart2B;
+  static constexpr int kOffTot = kOffDsum + kDsumB;
+  static constexpr int kOffBar = kOffTot + kTotB;
+  static constexpr int kBars = 3 * kBS + 4;
+  static constexpr int kBytes = kOffBar + kBars * 8 + 16;
+  static constexpr uint32_t kTmemCols = kCW > 4 ? 512 : 256;
+  static_assert(kCW <= 8, "two consumer warps per TMEM lane quarter at most");
+  static_assert(kBytes <= 227 * 1024, "shared memory");
+};
+
+// kLimit: delta is clamped to [dt_min, dt_max] (a separate instance, so the
+// unlimited scan pays nothing for it).
 template <typename Act, int TPC, bool kFast, bool kGate, bool kLimit>
 __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const __grid_constant__ BwdTmaParams P) {
-  constexpr int N = 4 * TPC;
-  constexpr int kLanes = kDTile * TPC;  // consumer threads
-  constexpr int kCW = kLanes / 32;      // consumer warps
-  constexpr int kTile = kTT * kDTile;
-  constexpr int kBC = kTT * N;
-  constexpr bool kBf16 = std::is_same<Act, __nv_bfloat16>::value;
-  constexpr int kStageElems = 4 * kTile + 2 * kBC;
-  constexpr int S = BwdStages<Act>::value;
-  constexpr int kBst = kBf16 ? 2 * N : N;  // f32 row stride of the B (and C) rows
-  constexpr int kOwnA = kTT / TPC;         // pass-A steps a lane owns per tile
-  constexpr int kOwnB = kSub / TPC;        // pass-B steps a lane owns per sub-chunk
-  // per-step rows of the lanes' partial sums, one float4 of padding: the TPC
-  // lanes of a channel read rows k, k+1, .. at once, 16 bytes apart in the banks
-  constexpr int kPartRow = kLanes + 1;
-  constexpr uint32_t kTmemCols = 512;
-  static_assert(kCW <= 8, "two consumer warps per TMEM lane quarter at most");
-  using AT = SwzTile<Act, kDTile, kTT>;  // u, delta_raw, z, dout tiles (128-byte rows)
+  using LY = BwdLayout<Act, TPC>;
+  using AT = typename LY::AT;
+  constexpr int N = LY::N;
+  constexpr int kLanes = LY::kLanes;
+  constexpr int kCW = LY::kCW;
+  constexpr bool kBf16 = LY::kBf16;
   constexpr int kRB = AT::kRowB;
+  constexpr int kOwn = kSC / TPC;  // owned steps of a lane per sub-chunk
+  // ln 2 on the fast path: sums weighted by A are taken with A*log2(e)
+  constexpr float kAscale = kFast ? kLn2 : 1.f;
 
   extern __shared__ __align__(1024) unsigned char smem[];
-  Act* stages = reinterpret_cast<Act*>(smem);
-  float* bcf = reinterpret_cast<float*>(smem + (size_t)S * kStageElems * sizeof(Act));  // [S][TT][2][N] (bf16)
-  float2* dbuf = reinterpret_cast<float2*>(bcf + (kBf16 ? S * kTT * 2 * N : 0));       // [kChunk][kRow] (delta, delta*u)
-  float4* hc0 = reinterpret_cast<float4*>(dbuf + kChunk * kRow);   // [kLanes] state at the chunk start
-  float* redw = reinterpret_cast<float*>(hc0 + kLanes);            // [kCW][kRedSlots][kRedSlot]
-  float* wpart = redw + kCW * kRedSlots * kRedSlot;                // [2][kSub][kCW][32]
-  float4* part = reinterpret_cast<float4*>(wpart + 2 * kSub * kCW * 32);  // [kSub][kPartRow] (y, gB, Ap, -)
-  float2* bprep = reinterpret_cast<float2*>(part + kSub * kPartRow);      // [kSub][kRow] (dy, dz factor)
-  float* tot = reinterpret_cast<float*>(bprep + kSub * kRow);             // [2 (sum, comp)][kLanes][6]
-  uint64_t* full = reinterpret_cast<uint64_t*>(tot + 2 * kLanes * 6);
-  uint64_t* conv = full + S;
-  uint64_t* empty = conv + S;
-  uint64_t* wfull = empty + S;  // [2] wpart slot written by every consumer warp
-  uint64_t* wempty = wfull + 2; // [2] wpart slot summed by the reducer warp
+  float* bcf = reinterpret_cast<float*>(smem + LY::kOffBcf);
+  float4* pA = reinterpret_cast<float4*>(smem + LY::kOffPA);
+  float2* pY = reinterpret_cast<float2*>(smem + LY::kOffPY);
+  float4* part4 = reinterpret_cast<float4*>(smem + LY::kOffPart4);
+  float2* part2 = reinterpret_cast<float2*>(smem + LY::kOffPart2);
+  float* dsum = reinterpret_cast<float*>(smem + LY::kOffDsum);
+  float* totS = reinterpret_cast<float*>(smem + LY::kOffTot);  // [2][12][lanes]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + LY::kOffBar);
+  uint64_t* conv = full + kBS;
+  uint64_t* empty = conv + kBS;
+  uint64_t* wfull = empty + kBS;  // [2] dsum slot written by every consumer warp
+  uint64_t* wempty = wfull + 2;   // [2] dsum slot summed by the reducer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wempty + 2);
 
   const BwdParams& p = P.p;
-  // the swizzled tiles need 1024-byte aligned stages (uniform: the whole CTA leaves)
   if (smem_u32(smem) & 1023u) {
     if (threadIdx.x == 0) atomicOr(p.status, kStatusLayout);
     return;
@@ -135,15 +188,12 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int L = p.L, D = p.D;
   const int nchunks = p.nchunks;
-  // this CTA's range of chunk units; every role walks its pieces in unit
-  // order: piece = sequence sq (batch sq / ndt, channel tile sq % ndt),
-  // chunks [c_lo, c_hi)
   const BwdPlan& pl = p.plan;
-  // (the plan keeps U below 2^31, so unit indices fit an int)
   const int u_begin = (int)plan_bound(pl, blockIdx.x), u_end = (int)plan_bound(pl, blockIdx.x + 1);
+  if (blockIdx.x == 0 && tid == 0) *p.ws_ndt = pl.ndt;  // the finalize reads the partial-row count
 
   if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < kBS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&conv[s], 32);
       mbar_init(&empty[s], kCW);
@@ -154,43 +204,28 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
     }
     fence_mbar_init();
   }
-  // TMEM holds every state of the chunk being processed: per consumer warp
-  // 256 columns (64 steps x 4 states) of its 32 lanes; warps w and w + 4
-  // share a lane quarter and take columns 0..255 / 256..511
-  if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 0) tmem_alloc(tmem_slot, LY::kTmemCols);
   tmem_fence_before_sync();
   __syncthreads();
   tmem_fence_after_sync();
 
-  auto tile_u = [&](int s) { return stages + (size_t)s * kStageElems; };
-  auto tile_raw = [&](int s) { return stages + (size_t)s * kStageElems + kTile; };
-  auto tile_z = [&](int s) { return stages + (size_t)s * kStageElems + 2 * kTile; };
-  auto tile_g = [&](int s) { return stages + (size_t)s * kStageElems + 3 * kTile; };
-  auto tile_B = [&](int s) { return stages + (size_t)s * kStageElems + 4 * kTile; };
-  auto tile_C = [&](int s) { return stages + (size_t)s * kStageElems + 4 * kTile + kBC; };
+  auto stage = [&](int s) { return smem + (size_t)s * LY::kStageB; };
+  auto tile = [&](int s, int i) { return reinterpret_cast<Act*>(stage(s) + i * LY::kTileB); };  // 0 u 1 raw 2 z 3 dout
+  auto tile_B = [&](int s) { return reinterpret_cast<Act*>(stage(s) + 4 * LY::kTileB); };
+  auto tile_C = [&](int s) { return reinterpret_cast<Act*>(stage(s) + 4 * LY::kTileB + LY::kBCB); };
 
-  // activation tile: AT::kNBox boxes of AT::kChBox channels side by side
-  auto load_act = [&](Act* dst, const CUtensorMap* m, uint64_t* bar, int d0, int row) {
-#pragma unroll
-    for (int bx = 0; bx < AT::kNBox; ++bx)
-      tma_load_2d(reinterpret_cast<unsigned char*>(dst) + bx * AT::kBoxBytes, m, bar, d0 + bx * AT::kChBox, row);
-  };
-
-  // The item sequence every role walks: for each piece, for chunk c =
-  // last..first of the piece, with ntl tiles: pass A tiles 0..ntl-1, then
-  // pass B tiles ntl-1..0.
-  auto chunk_tiles = [&](int c) { return (min(kChunk, L - c * kChunk) + kTT - 1) / kTT; };
   auto piece_at = [&](int u, int& b, int& d0, int& c_lo, int& c_hi, int& next) {
     const int sq = u / pl.nch, S0 = sq * pl.nch;
     next = min(S0 + pl.nch, u_end);
     b = sq / pl.ndt;
-    d0 = (sq % pl.ndt) * kDTile;
+    d0 = (sq % pl.ndt) * kBwdTile;
     c_lo = u - S0;
     c_hi = next - S0;
   };
+  auto chunk_len = [&](int c) { return min(kChunk, L - c * kChunk); };
 
   if (warp == kCW) {
-    // ---------------- producer
+    // ---------------- producer: one stage per chunk, chunks of each piece last first
     if (lane == 0) {
       tma_prefetch_desc(&P.map_u);
       tma_prefetch_desc(&P.map_raw);
@@ -198,105 +233,91 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
       if (kGate) tma_prefetch_desc(&P.map_z);
       tma_prefetch_desc(&P.map_B);
       tma_prefetch_desc(&P.map_C);
-      const uint32_t bytesA = (uint32_t)((2 * kTile + kBC) * sizeof(Act));
-      const uint32_t bytesB = (uint32_t)(((kGate ? 4 : 3) * kTile + 2 * kBC) * sizeof(Act));
+      const uint32_t bytes = (uint32_t)((kGate ? 4 : 3) * LY::kTileB + 2 * LY::kBCB);
       int item = 0;
       bool ok = true;
       for (int u = u_begin, next; u < u_end && ok; u = next) {
         int b, d0, c_lo, c_hi;
         piece_at(u, b, d0, c_lo, c_hi, next);
-        for (int c = c_hi - 1; c >= c_lo && ok; --c) {
-          const int ntl = chunk_tiles(c);
-          for (int it = 0; it < 2 * ntl; ++it, ++item) {
-            const bool passA = it < ntl;
-            const int j = passA ? it : 2 * ntl - 1 - it;
-            const int s = item % S;
-            const uint32_t use = (uint32_t)(item / S);
-            if (item >= S && !mbar_wait(&empty[s], (use - 1) & 1, p.status)) {
-              ok = false;
-              break;
-            }
-            const int row = b * L + c * kChunk + j * kTT;
-            mbar_arrive_expect_tx(&full[s], passA ? bytesA : bytesB);
-            load_act(tile_u(s), &P.map_u, &full[s], d0, row);
-            load_act(tile_raw(s), &P.map_raw, &full[s], d0, row);
-            tma_load_2d(tile_B(s), &P.map_B, &full[s], 0, row);
-            if (!passA) {
-              if (kGate) load_act(tile_z(s), &P.map_z, &full[s], d0, row);
-              load_act(tile_g(s), &P.map_dout, &full[s], d0, row);
-              tma_load_2d(tile_C(s), &P.map_C, &full[s], 0, row);
-            }
+        for (int c = c_hi - 1; c >= c_lo; --c, ++item) {
+          const int s = item % kBS;
+          if (item >= kBS && !mbar_wait(&empty[s], (uint32_t)(item / kBS - 1) & 1, p.status)) {
+            ok = false;
+            break;
           }
+          const int row = b * L + c * kChunk;
+          mbar_arrive_expect_tx(&full[s], bytes);
+#pragma unroll
+          for (int bx = 0; bx < AT::kNBox; ++bx) {
+            const int x = d0 + bx * AT::kChBox, o = bx * AT::kBoxBytes;
+            tma_load_2d(reinterpret_cast<unsigned char*>(tile(s, 0)) + o, &P.map_u, &full[s], x, row);
+            tma_load_2d(reinterpret_cast<unsigned char*>(tile(s, 1)) + o, &P.map_raw, &full[s], x, row);
+            if (kGate) tma_load_2d(reinterpret_cast<unsigned char*>(tile(s, 2)) + o, &P.map_z, &full[s], x, row);
+            tma_load_2d(reinterpret_cast<unsigned char*>(tile(s, 3)) + o, &P.map_dout, &full[s], x, row);
+          }
+          tma_load_2d(tile_B(s), &P.map_B, &full[s], 0, row);
+          tma_load_2d(tile_C(s), &P.map_C, &full[s], 0, row);
         }
       }
       // never leave with copies in flight: wait for the last use of every stage
-      for (int s = 0; s < S && s < item; ++s) {
-        const int k_last = s + S * ((item - 1 - s) / S);
-        mbar_wait(&full[s], (uint32_t)(k_last / S) & 1, p.status);
+      for (int s = 0; s < kBS && s < item; ++s) {
+        const int k_last = s + kBS * ((item - 1 - s) / kBS);
+        mbar_wait(&full[s], (uint32_t)(k_last / kBS) & 1, p.status);
       }
     }
     return;
   }
   if (warp == kCW + 1) {
-    // ---------------- converter (bf16): Bm (and Cm in pass B) -> f32
+    // ---------------- converter (bf16): the chunk's Bm and Cm rows -> f32 [TT][2][N]
     if (kBf16) {
       int item = 0;
       bool ok = true;
       for (int u = u_begin, next; u < u_end; u = next) {
         int b, d0, c_lo, c_hi;
         piece_at(u, b, d0, c_lo, c_hi, next);
-        for (int c = c_hi - 1; c >= c_lo; --c) {
-          const int ntl = chunk_tiles(c);
-          for (int it = 0; it < 2 * ntl; ++it, ++item) {
-            const bool passA = it < ntl;
-            const int s = item % S;
-            if (ok) ok = mbar_wait(&full[s], (uint32_t)(item / S) & 1, p.status);
-            const __nv_bfloat162* tb = reinterpret_cast<const __nv_bfloat162*>(tile_B(s));
-            const __nv_bfloat162* tc = reinterpret_cast<const __nv_bfloat162*>(tile_C(s));
-            float* dst = bcf + (size_t)s * kTT * 2 * N;
-            for (int e = lane; e < kBC / 2; e += 32) {
-              const int t = (2 * e) / N, n = (2 * e) % N;
-              *reinterpret_cast<float2*>(dst + (t * 2 + 0) * N + n) = __bfloat1622float2(tb[e]);
-              if (!passA) *reinterpret_cast<float2*>(dst + (t * 2 + 1) * N + n) = __bfloat1622float2(tc[e]);
-            }
-            mbar_arrive(&conv[s]);
+        for (int c = c_hi - 1; c >= c_lo; --c, ++item) {
+          const int s = item % kBS;
+          if (ok) ok = mbar_wait(&full[s], (uint32_t)(item / kBS) & 1, p.status);
+          const __nv_bfloat162* tb = reinterpret_cast<const __nv_bfloat162*>(tile_B(s));
+          const __nv_bfloat162* tc = reinterpret_cast<const __nv_bfloat162*>(tile_C(s));
+          float* dst = bcf + (size_t)s * kTT * 2 * N;
+          for (int e = lane; e < kTT * N / 2; e += 32) {
+            const int t = (2 * e) / N, n = (2 * e) % N;
+            *reinterpret_cast<float2*>(dst + (t * 2 + 0) * N + n) = __bfloat1622float2(tb[e]);
+            *reinterpret_cast<float2*>(dst + (t * 2 + 1) * N + n) = __bfloat1622float2(tc[e]);
           }
+          mbar_arrive(&conv[s]);
         }
       }
     }
     return;
   }
-
   if (warp == kCW + 2) {
-    // ---------------- reducer: cross-warp sums of each sub-chunk's dBm/dCm
-    // partials (fixed warp order) -> this CTA's partial row in ws_dbc
+    // ---------------- reducer: the warps' per-step dBm/dCm sums, added in
+    // ascending warp order, -> this tile's partial row [t][2][N]
     int n = 0;
     bool ok = true;
     for (int u = u_begin, next; u < u_end; u = next) {
       int b, d0, c_lo, c_hi;
       piece_at(u, b, d0, c_lo, c_hi, next);
-      float* ws_dbc_r = p.ws_dbc + ((size_t)(d0 / kDTile) * p.B + b) * (size_t)L * 2 * N;
+      float* ws_r = p.ws_dbc + ((size_t)(d0 / kBwdTile) * p.B + b) * (size_t)L * 2 * N;
       for (int c = c_hi - 1; c >= c_lo; --c) {
-        const int clen = min(kChunk, L - c * kChunk);
-        for (int j = chunk_tiles(c) - 1; j >= 0; --j) {
-          const int cnt = min(kTT, clen - j * kTT);
-          for (int sc = (cnt + kSub - 1) / kSub - 1; sc >= 0; --sc, ++n) {
-            const int cnt8 = min(kSub, cnt - sc * kSub);
-            const int slot = n & 1;
-            if (ok) ok = mbar_wait(&wfull[slot], (uint32_t)(n >> 1) & 1, p.status);
-            const float* wp = wpart + slot * (kSub * kCW * 32);
-            float* dst = ws_dbc_r + (size_t)(c * kChunk + j * kTT + sc * kSub) * 2 * N;
-            for (int idx = lane; idx < cnt8 * 2 * N; idx += 32) {
-              const int k = idx / (2 * N), o = idx % (2 * N);
-              const float* src = wp + k * kCW * 32 + o;
-              float v = src[0];
+        const int clen = chunk_len(c);
+        for (int sc = (clen + kSC - 1) / kSC - 1; sc >= 0; --sc, ++n) {
+          const int slot = n & 1;
+          if (ok) ok = mbar_wait(&wfull[slot], (uint32_t)(n >> 1) & 1, p.status);
+          const int cnt = min(kSC, clen - sc * kSC);
+          const float* src = dsum + slot * (kSC * kCW * 32);
+          if (lane < 2 * N) {
+            for (int k = 0; k < cnt; ++k) {
+              float v = src[(k * kCW) * 32 + lane];
 #pragma unroll
-              for (int w = 1; w < kCW; ++w) v += src[w * 32];
-              dst[idx] = v;
+              for (int w = 1; w < kCW; ++w) v += src[(k * kCW + w) * 32 + lane];
+              ws_r[(size_t)(c * kChunk + sc * kSC + k) * 2 * N + lane] = v;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&wempty[slot]);
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&wempty[slot]);
         }
       }
     }
@@ -304,352 +325,351 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   }
 
   // ---------------- consumers
-  const int q = tid % TPC;   // state group: states 4q .. 4q+3
-  const int cl = tid / TPC;  // channel within the tile
-  // Lane q owns the steps k with k % TPC == q (row % 8 of owned step i of an
-  // 8-step group is i*TPC + q): byte offsets of this lane's channel in those
-  // rows of a swizzled tile.
-  int colo[kOwnB];
-#pragma unroll
-  for (int i = 0; i < kOwnB; ++i) colo[i] = AT::col(i * TPC + q, cl);
-
-  // A2 = A*log2(e) on the fast path (2^x decays), A itself otherwise; sums
-  // weighted by A are taken with A2 and scaled by kAscale = A / A2 at the end.
-  constexpr float kAscale = kFast ? kLn2 : 1.f;
-  // this warp's TMEM region: column 32*j + 4*k + i = state i of step 8*j + k of the chunk
+  const int q = lane % TPC;                  // state group: states 4q .. 4q+3
+  const int cp = tid / TPC;                  // channel pair in the tile: channels 2cp, 2cp+1
   const uint32_t tm = *tmem_slot + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((warp >> 2) * 256);
-  float* my_tot = tot + tid * 6;               // running totals: 4 states, dDp, d_delta_bias
-  float* my_cmp = tot + kLanes * 6 + tid * 6;  // Kahan compensation
-
-  // warp-local reducer role: output pair op = lane % N (term r_q, states r_n,
-  // r_n + 1 of the channel), group r_g = lane / N of 4 channels
-  const int r_op = lane % N, r_g = lane / N;
-  const int r_q = r_op / (N / 2), r_n = 2 * (r_op % (N / 2));
-  const int r_src = r_n / 4, r_j = r_n % 4;  // owning lane-in-channel and index in its chunk
-  float* my_redw = redw + warp * kRedSlots * kRedSlot;
+  // reduce-scatter of the 8 dBm/dCm values over the warp's pairs: output of this lane
+  const int rs_o = ((lane >> 4) & 1) * N + 4 * q + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
+  const bool rs_store = (lane & (3 & ~(TPC - 1))) == 0;
+  // swizzled byte offset of the pair's channels in the rows of the lane's
+  // owned steps (it depends on the row % 8 only): owned step i of a 4-step
+  // sub-chunk at an even / odd sub-chunk index
+  int colE[kOwn], colO[kOwn];
+#pragma unroll
+  for (int i = 0; i < kOwn; ++i) {
+    colE[i] = AT::col(i * TPC + q, 2 * cp);
+    colO[i] = AT::col(kSC + i * TPC + q, 2 * cp);
+  }
 
   bool failed = false;
-  int s = 0;         // ring stage of the current item
+  int s = 0;         // ring stage of the current chunk
   uint32_t par = 0;  // its phase parity
-  int nsub_done = 0;  // sub-chunks handed to the reducer so far
+  int nsub = 0;      // sub-chunks handed to the reducer so far
   for (int u = u_begin, next; u < u_end; u = next) {
     int b, d0, c_lo, c_hi;
     piece_at(u, b, d0, c_lo, c_hi, next);
-    // piece index in time order within its sequence, and whether it ends the sequence
     const int kp = c_lo == 0 ? 0 : (int)(plan_count_le(pl, u) - plan_count_le(pl, u - c_lo));
     const bool last_piece = c_hi == pl.nch;
-    const int d = d0 + cl;
-    const bool dvalid = d < D;
-    const int dc = dvalid ? d : D - 1;
-    const int sq = (u - c_lo) / pl.nch;  // sequence index
+    const int sq = (u - c_lo) / pl.nch;
+    const int dA = d0 + 2 * cp;  // first channel of the pair (D is even: both valid or neither)
+    const bool dvalid = dA < D;
+    const int dc = dvalid ? dA : D - 2;
     if (!last_piece && p.seq_flag) {
       // hand-over mode: the carry comes from the CTA walking the sequence's last piece
       if (lane == 0 && !failed) failed = !flag_wait(p.seq_flag + sq, p.status);
       failed = __shfl_sync(0xffffffffu, failed, 0);
       __syncwarp();
     }
-    float2 A2[2], carry[2];
+    // A2[c][i]: states 4q + 2i, 4q + 2i + 1 of channel dc + c
+    float2 A2[2][2], carry[2][2];
     {
       const float* cin = !last_piece ? p.seg_carry + (((size_t)b * p.nseg + kp) * D + dc) * N
                                      : (p.dh_last ? p.dh_last + ((size_t)b * D + dc) * N : nullptr);
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int n = 4 * q + 2 * i;
-        const float a0 = -expf(p.A_log[dc * N + n]);
-        const float a1 = -expf(p.A_log[dc * N + n + 1]);
-        A2[i] = kFast ? make_float2(a0 * kLog2e, a1 * kLog2e) : make_float2(a0, a1);
-        // adjoint carry entering the piece's last step: dh_last for the last
-        // piece of the sequence, the composed carry of the pieces after it otherwise
-        carry[i] = (cin && dvalid) ? make_float2(__ldcg(cin + n), __ldcg(cin + n + 1)) : make_float2(0.f, 0.f);
+      for (int c = 0; c < 2; ++c) {
+        const float4 al = *reinterpret_cast<const float4*>(p.A_log + (size_t)(dc + c) * N + 4 * q);
+        const float a[4] = {-expf(al.x), -expf(al.y), -expf(al.z), -expf(al.w)};
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          A2[c][i] = kFast ? make_float2(a[2 * i] * kLog2e, a[2 * i + 1] * kLog2e) : make_float2(a[2 * i], a[2 * i + 1]);
+          carry[c][i] = (cin && dvalid) ? make_float2(__ldcg(cin + c * N + 4 * q + 2 * i), __ldcg(cin + c * N + 4 * q + 2 * i + 1))
+                                        : make_float2(0.f, 0.f);
+        }
       }
     }
-    const float bias = p.delta_bias[dc];
-    const float Dd = p.Dp[dc];
+    const float2 bias2 = make_float2(p.delta_bias[dc], p.delta_bias[dc + 1]);
+    const float2 Dp2 = make_float2(p.Dp[dc], p.Dp[dc + 1]);
+    // running totals of the piece: dA terms (8), dDp (2), d_delta_bias (2),
+    // with Kahan compensation; lane-private in shared memory
+    float* tot = totS + tid;
+    float* cmp = totS + 12 * kLanes + tid;
 #pragma unroll
-    for (int i = 0; i < 6; ++i) {
-      my_tot[i] = 0.f;
-      my_cmp[i] = 0.f;
-    }
-    const size_t bd_off = (size_t)b * L * D + d;  // du / d_delta_raw / dz of (b, t = 0, d)
+    for (int i = 0; i < 12; ++i) tot[i * kLanes] = cmp[i * kLanes] = 0.f;
+    const size_t bd_off = (size_t)b * L * D + dA;  // outputs of (b, t = 0, pair)
     for (int c = c_hi - 1; c >= c_lo; --c) {
       const int t0 = c * kChunk;
-      const int clen = min(kChunk, L - t0);
-      const int ntl = (clen + kTT - 1) / kTT;
-      float2 accA[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      float accD = 0.f, accBias = 0.f;
-      float2 h[2];
-      {
-        const float4 cs = *reinterpret_cast<const float4*>(p.chunk_states + (((size_t)b * nchunks + c) * D + dc) * N + 4 * q);
-        h[0] = make_float2(cs.x, cs.y);
-        h[1] = make_float2(cs.z, cs.w);
+      const int cnt = chunk_len(c);
+      const int nsc = (cnt + kSC - 1) / kSC;
+      // the chunk's saved start state (zeros for channels past D)
+      float2 h[2][2];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const float4 cs = dvalid ? __ldg(reinterpret_cast<const float4*>(
+                                       p.chunk_states + (((size_t)b * nchunks + c) * D + dc + cc) * N + 4 * q))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        h[cc][0] = make_float2(cs.x, cs.y);
+        h[cc][1] = make_float2(cs.z, cs.w);
       }
-      for (int it = 0; it < 2 * ntl; ++it) {
-        const bool passA = it < ntl;
-        const int j = passA ? it : 2 * ntl - 1 - it;
-        if (!failed) failed = !mbar_wait(&full[s], par, p.status);
-        if (kBf16 && !failed) failed = !mbar_wait(&conv[s], par, p.status);
-        __syncwarp();
-        const int tb = j * kTT;  // first step of the tile within the chunk
-        const int cnt = min(kTT, clen - tb);
-        const Act* su = tile_u(s);
-        const Act* sr = tile_raw(s);
-        const float* Bt = (kBf16 ? bcf + (size_t)s * kTT * 2 * N : reinterpret_cast<const float*>(tile_B(s))) + 4 * q;
-        const float* Ct = kBf16 ? Bt + N : reinterpret_cast<const float*>(tile_C(s)) + 4 * q;
-        float2* dtile = dbuf + tb * kRow;  // (delta, delta*u) rows of this tile
+      if (!failed) failed = !mbar_wait(&full[s], par, p.status);
+      if (kBf16 && !failed) failed = !mbar_wait(&conv[s], par, p.status);
+      __syncwarp();
+      const Act* su = tile(s, 0);
+      const Act* sr = tile(s, 1);
+      const Act* sz = tile(s, 2);
+      const Act* sg = tile(s, 3);
+      const float* Bt = (kBf16 ? bcf + (size_t)s * kTT * 2 * N : reinterpret_cast<const float*>(tile_B(s))) + 4 * q;
+      const float* Ct = kBf16 ? Bt + N : reinterpret_cast<const float*>(tile_C(s)) + 4 * q;
+      constexpr int kBst = kBf16 ? 2 * N : N;  // f32 row stride of the Bm (and Cm) rows
 
-        if (passA) {
-          // ---------- pass A: (delta, delta*u) of the owned steps, then the recurrence
-          auto pass_a = [&](auto full_tag) {
-            constexpr bool kFull = decltype(full_tag)::value;
-            const int nv = kFull ? kTT : cnt;
+      // ---------- prep A: (delta, delta*u) of the owned steps, both channels
+#pragma unroll 2
+      for (int j = 0; j < kTT / kSC; ++j) {
 #pragma unroll
-            for (int i = 0; i < kOwnA; ++i) {
-              const int km = i * TPC + q;
-              const int kr = kFull ? km : min(km, nv - 1);
-              const int o = kr * kRB + (kFull ? colo[i % kOwnB] : AT::col(kr, cl));
-              const float sv = lds_at(sr, o) + bias;
-              const float sp0 = kFast ? softplus_fast(sv) : softplus_f(sv);
-              const float sp = kLimit ? clamp_dt(sp0, p.dt_min, p.dt_max) : sp0;
-              if (kFull || km < nv) dtile[km * kRow + cl] = make_float2(sp, sp * lds_at(su, o));
-            }
-            __syncwarp();
-            if (tb == 0) hc0[tid] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
-            // states after each step, 8 steps at a time, then to TMEM
-            float hb[4 * kSub];
-            auto stepA = [&](int kk) {
-              const float2 dv = dtile[kk * kRow + cl];
-              const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
-              const float4 Bv = *reinterpret_cast<const float4*>(Bt + kk * kBst);
-              h[0] = ffma2(decay2<kFast>(dd, A2[0]), h[0], fmul2(uu2, make_float2(Bv.x, Bv.y)));
-              h[1] = ffma2(decay2<kFast>(dd, A2[1]), h[1], fmul2(uu2, make_float2(Bv.z, Bv.w)));
-              const int r = 4 * (kk % kSub);
-              hb[r] = h[0].x;
-              hb[r + 1] = h[0].y;
-              hb[r + 2] = h[1].x;
-              hb[r + 3] = h[1].y;
-            };
+        for (int i = 0; i < kOwn; ++i) {
+          const int k = j * kSC + i * TPC + q;
+          if (k < cnt) {
+            const int o = k * kRB + ((j & 1) ? colO[i] : colE[i]);
+            const float2 sv = fadd2(lds_pair(sr, o), bias2);
+            float2 sp = kFast ? make_float2(softplus_fast(sv.x), softplus_fast(sv.y))
+                              : make_float2(softplus_f(sv.x), softplus_f(sv.y));
+            if (kLimit) sp = make_float2(clamp_dt(sp.x, p.dt_min, p.dt_max), clamp_dt(sp.y, p.dt_min, p.dt_max));
+            const float2 du2 = fmul2(sp, lds_pair(su, o));
+            pA[k * 64 + cp] = make_float4(sp.x, du2.x, sp.y, du2.y);
+          }
+        }
+      }
+      __syncwarp();
+
+      // ---------- pass A: the states of the chunk into TMEM
+      {
+        float hb[32];
+        auto stepA = [&](int k, int kk) {  // kk = k % kSC (a constant)
+          const float4 v = pA[k * 64 + cp];
+          const float4 Bv = *reinterpret_cast<const float4*>(Bt + k * kBst);
+          const float2 B01 = make_float2(Bv.x, Bv.y), B23 = make_float2(Bv.z, Bv.w);
+          const float2 d0v = make_float2(v.x, v.x), u0v = make_float2(v.y, v.y);
+          const float2 d1v = make_float2(v.z, v.z), u1v = make_float2(v.w, v.w);
+          // the state before the step goes to TMEM (column block of step k)
+          const int r = 8 * kk;
+          hb[r] = h[0][0].x, hb[r + 1] = h[0][0].y, hb[r + 2] = h[0][1].x, hb[r + 3] = h[0][1].y;
+          hb[r + 4] = h[1][0].x, hb[r + 5] = h[1][0].y, hb[r + 6] = h[1][1].x, hb[r + 7] = h[1][1].y;
+          h[0][0] = ffma2(decay2<kFast>(d0v, A2[0][0]), h[0][0], fmul2(u0v, B01));
+          h[0][1] = ffma2(decay2<kFast>(d0v, A2[0][1]), h[0][1], fmul2(u0v, B23));
+          h[1][0] = ffma2(decay2<kFast>(d1v, A2[1][0]), h[1][0], fmul2(u1v, B01));
+          h[1][1] = ffma2(decay2<kFast>(d1v, A2[1][1]), h[1][1], fmul2(u1v, B23));
+        };
+#pragma unroll 1
+        for (int j = 0; j < nsc; ++j) {
+          if (j * kSC + kSC <= cnt) {
 #pragma unroll
-            for (int kk = 0; kk < kTT; ++kk) {
-              if (kFull || kk < nv) stepA(kk);
-              // a block with at least one valid step goes out (warp-uniform)
-              if ((kk % kSub) == kSub - 1 && (kFull || kk - (kSub - 1) < nv)) tmem_st32(tm + (uint32_t)(4 * (tb + kk - (kSub - 1))), hb);
-            }
-          };
-          if (cnt == kTT)
-            pass_a(std::true_type{});
-          else
-            pass_a(std::false_type{});
-        } else {
-          // ---------- pass B: 8-step sub-chunks of this tile, last first
-          const Act* sz = tile_z(s);
-          const Act* sg = tile_g(s);
-          const int nsub = (cnt + kSub - 1) / kSub;
-          if (it == ntl) tmem_wait_st();  // the chunk's states (pass A) are in TMEM
-          for (int sc = nsub - 1; sc >= 0; --sc) {
-            const int ks = sc * kSub;  // first step of the sub-chunk within the tile
-            const int cnt8 = min(kSub, cnt - ks);
-            const int cstep = tb + ks;  // ... within the chunk
-            // the state before the sub-chunk: last state of the previous block, or the chunk start
-            float hq[4];
-            if (cstep > 0) {
-              tmem_ld4(tm + (uint32_t)(4 * cstep - 4), hq);
+            for (int kk = 0; kk < kSC; ++kk) stepA(j * kSC + kk, kk);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kSC; ++kk)
+              if (j * kSC + kk < cnt) stepA(j * kSC + kk, kk);  // (warp-uniform)
+          }
+          tmem_st32(tm + (uint32_t)(8 * kSC * j), hb);
+        }
+        tmem_wait_st();
+      }
+
+      // ---------- pass B
+      float2 accA[2][2] = {{make_float2(0.f, 0.f), make_float2(0.f, 0.f)}, {make_float2(0.f, 0.f), make_float2(0.f, 0.f)}};
+      float2 accD = make_float2(0.f, 0.f), accBias = make_float2(0.f, 0.f);
+      // hk: the state after the step being walked -- pass A's final state for
+      // the last step, then the state TMEM holds before each step, loaded as
+      // that step is walked (issued at the step's start, waited for before its
+      // first use)
+      float hk[8] = {h[0][0].x, h[0][0].y, h[0][1].x, h[0][1].y, h[1][0].x, h[1][0].y, h[1][1].x, h[1][1].y};
+      for (int sc = nsc - 1; sc >= 0; --sc) {
+        const int kb = sc * kSC;  // first step of the sub-chunk
+        int colS[kOwn];
+#pragma unroll
+        for (int i = 0; i < kOwn; ++i) colS[i] = (sc & 1) ? colO[i] : colE[i];
+        // B1: gate terms of the owned steps
+        float2 dzf[kOwn];
+#pragma unroll
+        for (int i = 0; i < kOwn; ++i) {
+          const int k = kb + i * TPC + q;
+          float2 dy = make_float2(0.f, 0.f), f = make_float2(0.f, 0.f);
+          if (k < cnt) {
+            const int o = k * kRB + colS[i];
+            const float2 g = lds_pair(sg, o);
+            if (kGate) {
+              const float2 zz = lds_pair(sz, o);
+              const float2 sgz = kFast ? make_float2(sigmoid_fast(zz.x), sigmoid_fast(zz.y))
+                                       : make_float2(sigmoid_f(zz.x), sigmoid_f(zz.y));
+              dy = make_float2(g.x * zz.x * sgz.x, g.y * zz.y * sgz.y);
+              f = make_float2(g.x * sgz.x * fmaf(zz.x, 1.f - sgz.x, 1.f), g.y * sgz.y * fmaf(zz.y, 1.f - sgz.y, 1.f));
             } else {
-              const float4 c0 = hc0[tid];
-              hq[0] = c0.x, hq[1] = c0.y, hq[2] = c0.z, hq[3] = c0.w;
+              dy = g;
             }
-            const float2 hstart[2] = {make_float2(hq[0], hq[1]), make_float2(hq[2], hq[3])};
-            const float2* dsub = dbuf + cstep * kRow;
-            // wpart slot of this sub-chunk: wait until the reducer has summed its previous use
-            const int slot = nsub_done & 1;
-            if (nsub_done >= 2 && !failed) failed = !mbar_wait(&wempty[slot], (uint32_t)((nsub_done >> 1) - 1) & 1, p.status);
-            float* wp_sub = wpart + slot * (kSub * kCW * 32);
-            auto sub = [&](auto full_tag) {
-              constexpr bool kFull = decltype(full_tag)::value;
-              const int nv = kFull ? kSub : cnt8;
-              // B1: the sub-chunk's states from TMEM (written by pass A)
-              float hv[4 * kSub];
-              tmem_ld32(tm + (uint32_t)(4 * cstep), hv);
-              float2 hs[kSub][2];
+          }
+          dzf[i] = f;
+          pY[(i * TPC + q) * 64 + cp] = dy;
+        }
+        __syncwarp();
+        const int slot = nsub & 1;
+        if (nsub >= 2 && !failed) failed = !mbar_wait(&wempty[slot], (uint32_t)((nsub >> 1) - 1) & 1, p.status);
+        float* ds = dsum + slot * (kSC * kCW * 32);
+        // B3: reverse steps
+        auto stepB = [&](int kk) {
+          const int k = kb + kk;
+          uint32_t hq[8];
+          tmem_ld8_issue(tm + (uint32_t)(8 * k), hq);  // the state before step k
+          const float4 v = pA[k * 64 + cp];
+          const float2 dy = pY[kk * 64 + cp];
+          const float4 Bv = *reinterpret_cast<const float4*>(Bt + k * kBst);
+          const float4 Cv = *reinterpret_cast<const float4*>(Ct + k * kBst);
+          const float2 Bp[2] = {make_float2(Bv.x, Bv.y), make_float2(Bv.z, Bv.w)};
+          const float2 Cp[2] = {make_float2(Cv.x, Cv.y), make_float2(Cv.z, Cv.w)};
+          const float2 dd[2] = {make_float2(v.x, v.x), make_float2(v.z, v.z)};
+          const float2 uu[2] = {make_float2(v.y, v.y), make_float2(v.w, v.w)};
+          const float2 yy[2] = {make_float2(dy.x, dy.x), make_float2(dy.y, dy.y)};
+          float2 ya[2], gba[2], apa[2], dB[2], dC[2], agv[2][2];
 #pragma unroll
-              for (int k = 0; k < kSub; ++k) {
-                hs[k][0] = make_float2(hv[4 * k], hv[4 * k + 1]);
-                hs[k][1] = make_float2(hv[4 * k + 2], hv[4 * k + 3]);
-              }
-              // B2: gate terms of the owned steps: dy = dout*silu(z), dz factor
+          for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
-              for (int i = 0; i < kOwnB; ++i) {
-                const int km = i * TPC + q;
-                const int kr = ks + (kFull ? km : min(km, nv - 1));
-                const int o = kr * kRB + (kFull ? colo[i] : AT::col(kr, cl));
-                const float gout = lds_at(sg, o);
-                float2 v = make_float2(gout, 0.f);
-                if (kGate) {
-                  const float zz = lds_at(sz, o);
-                  const float sgz = kFast ? sigmoid_fast(zz) : sigmoid_f(zz);
-                  v.x = gout * zz * sgz;
-                  v.y = gout * sgz * fmaf(zz, 1.f - sgz, 1.f);
-                }
-                if (!kFull && km >= nv) v = make_float2(0.f, 0.f);
-                bprep[km * kRow + cl] = v;
-              }
-              __syncwarp();
-              // B3: reverse steps in pairs; the adjoint carry is the only
-              // loop-carried value.  Each step's dBm/dCm terms go to one of two
-              // warp-local slots and are summed over the warp's channels after
-              // each pair (fixed order) into the per-warp partial wp_sub.
+            for (int i = 0; i < 2; ++i) {
+              const int r = 4 * cc + 2 * i;
+              const float2 h_k = make_float2(hk[r], hk[r + 1]);
+              const float2 a = decay2<kFast>(dd[cc], A2[cc][i]);
+              const float2 g = ffma2(yy[cc], Cp[i], carry[cc][i]);
+              const float2 ag = fmul2(a, g);
+              gba[cc] = i == 0 ? fmul2(g, Bp[i]) : ffma2(g, Bp[i], gba[cc]);
+              ya[cc] = i == 0 ? fmul2(Cp[i], h_k) : ffma2(Cp[i], h_k, ya[cc]);
+              dB[i] = cc == 0 ? fmul2(g, uu[cc]) : ffma2(g, uu[cc], dB[i]);
+              dC[i] = cc == 0 ? fmul2(yy[cc], h_k) : ffma2(yy[cc], h_k, dC[i]);
+              agv[cc][i] = ag;
+              carry[cc][i] = ag;
+            }
+          }
+          tmem_wait_ld(hq);
 #pragma unroll
-              for (int gi = kSub / 2 - 1; gi >= 0; --gi) {
+          for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
-                for (int k = 2 * gi + 1; k >= 2 * gi; --k) {
-                  if (kFull || k < nv) {
-                    const float2 dv = dsub[k * kRow + cl];
-                    const float dy = bprep[k * kRow + cl].x;
-                    const float2 dd = make_float2(dv.x, dv.x), uu2 = make_float2(dv.y, dv.y);
-                    const float2 dy2 = make_float2(dy, dy);
-                    const float4 Bv4 = *reinterpret_cast<const float4*>(Bt + (ks + k) * kBst);
-                    const float4 Cv4 = *reinterpret_cast<const float4*>(Ct + (ks + k) * kBst);
-                    const float2 Bv[2] = {make_float2(Bv4.x, Bv4.y), make_float2(Bv4.z, Bv4.w)};
-                    const float2 Cv[2] = {make_float2(Cv4.x, Cv4.y), make_float2(Cv4.z, Cv4.w)};
-                    float2 ya = make_float2(0.f, 0.f), gba = make_float2(0.f, 0.f), apa = make_float2(0.f, 0.f);
-                    float2 tB[2], tC[2];
+            for (int i = 0; i < 2; ++i) {
+              const int r = 4 * cc + 2 * i;
+              const float2 hp = make_float2(__uint_as_float(hq[r]), __uint_as_float(hq[r + 1]));
+              const float2 pv = fmul2(agv[cc][i], hp);
+              apa[cc] = i == 0 ? fmul2(A2[cc][i], pv) : ffma2(A2[cc][i], pv, apa[cc]);
+              accA[cc][i] = ffma2(dd[cc], pv, accA[cc][i]);
+            }
+          }
 #pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                      const float2 a = decay2<kFast>(dd, A2[i]);
-                      const float2 hk = hs[k][i];
-                      const float2 hp = k == 0 ? hstart[i] : hs[k > 0 ? k - 1 : 0][i];
-                      const float2 g = ffma2(dy2, Cv[i], carry[i]);
-                      const float2 ag = fmul2(a, g);   // adjoint carried to step k-1
-                      const float2 pv = fmul2(ag, hp); // g * a * h_{k-1}
-                      apa = ffma2(A2[i], pv, apa);
-                      accA[i] = ffma2(dd, pv, accA[i]);
-                      gba = ffma2(g, Bv[i], gba);
-                      ya = ffma2(Cv[i], hk, ya);
-                      tB[i] = fmul2(g, uu2);
-                      tC[i] = fmul2(dy2, hk);
-                      carry[i] = ag;
-                    }
-                    float* rb = my_redw + (k & 1) * kRedSlot;
-                    // (channels past D: the tiles' zero fill makes dout and u,
-                    // hence dy, g and both terms, exactly 0)
-                    *reinterpret_cast<float4*>(rb + lane * 4) = make_float4(tB[0].x, tB[0].y, tB[1].x, tB[1].y);
-                    *reinterpret_cast<float4*>(rb + kRedBlock + lane * 4) = make_float4(tC[0].x, tC[0].y, tC[1].x, tC[1].y);
-                    part[k * kPartRow + tid] = make_float4(ya.x + ya.y, gba.x + gba.y, (apa.x + apa.y) * kAscale, 0.f);
-                  }
-                }
-                __syncwarp();
-                // channel sums of the pair's steps: 4 channels per lane, then across groups
+          for (int j = 0; j < 8; ++j) hk[j] = __uint_as_float(hq[j]);
+          part4[kk * kLanes + tid] = make_float4(ya[0].x + ya[0].y, gba[0].x + gba[0].y, ya[1].x + ya[1].y, gba[1].x + gba[1].y);
+          part2[kk * kLanes + tid] = make_float2(apa[0].x + apa[0].y, apa[1].x + apa[1].y);
+          // channel sums over the warp's pairs: xor reduce-scatter, 8 values -> 1
+          const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
+          float r0[4];
+          const float v8[8] = {dB[0].x, dB[0].y, dB[1].x, dB[1].y, dC[0].x, dC[0].y, dC[1].x, dC[1].y};
 #pragma unroll
-                for (int k = 2 * gi + 1; k >= 2 * gi; --k) {
-                  if (kFull || k < nv) {
-                    const float* rb = my_redw + (k & 1) * kRedSlot + r_q * kRedBlock;
-                    float2 v = make_float2(0.f, 0.f);
+          for (int i = 0; i < 4; ++i) {
+            const float send = h16 ? v8[i] : v8[4 + i];
+            const float keep = h16 ? v8[4 + i] : v8[i];
+            r0[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+          }
+          float r1[2];
 #pragma unroll
-                    for (int k2 = 0; k2 < 4; ++k2) {
-                      const int L2 = (r_g * 4 + k2) * TPC + r_src;
-                      v = fadd2(v, *reinterpret_cast<const float2*>(rb + L2 * 4 + r_j));
-                    }
+          for (int i = 0; i < 2; ++i) {
+            const float send = h8 ? r0[i] : r0[2 + i];
+            const float keep = h8 ? r0[2 + i] : r0[i];
+            r1[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+          }
+          float r2 = (h4 ? r1[1] : r1[0]) + __shfl_xor_sync(0xffffffffu, h4 ? r1[0] : r1[1], 4);
 #pragma unroll
-                    for (int m = N; m < 32; m <<= 1)
-                      v = fadd2(v, make_float2(__shfl_xor_sync(0xffffffffu, v.x, m), __shfl_xor_sync(0xffffffffu, v.y, m)));
-                    // every group holds the identical sum; all store it
-                    *reinterpret_cast<float2*>(wp_sub + (k * kCW + warp) * 32 + r_q * N + r_n) = v;
-                  }
-                }
-                __syncwarp();
-              }
-              // B4: owned steps: combine the channel's partial sums (fixed lane
-              // order), write du, d_delta_raw, dz
-              float o_du[kOwnB], o_dr[kOwnB], o_dz[kOwnB];
+          for (int mk = 2; mk >= TPC; mk >>= 1) r2 += __shfl_xor_sync(0xffffffffu, r2, mk);
+          if (rs_store) ds[(kk * kCW + warp) * 32 + rs_o] = r2;
+        };
+#pragma unroll 1
+        for (int kk = min(kSC, cnt - kb) - 1; kk >= 0; --kk) stepB(kk);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&wfull[slot]);
+        ++nsub;
+        // B4: owned steps: the pair's sums over its TPC lanes (lane order), outputs
 #pragma unroll
-              for (int i = 0; i < kOwnB; ++i) {
-                const int km = i * TPC + q;
-                const int kr = kFull ? km : min(km, nv - 1);
-                float4 acc = part[kr * kPartRow + cl * TPC];
+        for (int i = 0; i < kOwn; ++i) {
+          const int kk = i * TPC + q, k = kb + kk;
+          if (k < cnt) {
+            float4 a4 = part4[kk * kLanes + cp * TPC];
+            float2 a2 = part2[kk * kLanes + cp * TPC];
 #pragma unroll
-                for (int r = 1; r < TPC; ++r) {
-                  const float4 o = part[kr * kPartRow + cl * TPC + r];
-                  acc = make_float4(acc.x + o.x, acc.y + o.y, acc.z + o.z, 0.f);
-                }
-                const float2 dv = dsub[kr * kRow + cl];
-                const float2 bp = bprep[kr * kRow + cl];
-                const float uo = lds_at(su, (ks + kr) * kRB + (kFull ? colo[i] : AT::col(kr, cl)));
-                // softplus' = sigmoid(s) = 1 - e^{-delta}; zero where the limit
-                // clamped delta (delta sits on a bound: a clamped step, or a
-                // softplus exactly on it, which has measure zero)
-                const bool free_dt = !kLimit || ((dv.x > p.dt_min || p.dt_min <= 0.f) && dv.x < p.dt_max);
-                const float dsp = free_dt ? (kFast ? dsoftplus_fast(dv.x) : -expm1f(-dv.x)) : 0.f;
-                const float draw = fmaf(uo, acc.y, acc.z) * dsp;
-                o_du[i] = fmaf(Dd, bp.x, dv.x * acc.y);
-                o_dr[i] = draw;
-                o_dz[i] = fmaf(Dd, uo, acc.x) * bp.y;
-                const bool ok = kFull || km < nv;
-                accD += ok ? bp.x * uo : 0.f;
-                accBias += ok ? draw : 0.f;
-              }
+            for (int r = 1; r < TPC; ++r) {
+              const float4 o4 = part4[kk * kLanes + cp * TPC + r];
+              const float2 o2 = part2[kk * kLanes + cp * TPC + r];
+              a4 = make_float4(a4.x + o4.x, a4.y + o4.y, a4.z + o4.z, a4.w + o4.w);
+              a2 = make_float2(a2.x + o2.x, a2.y + o2.y);
+            }
+            const float4 v = pA[k * 64 + cp];
+            const float2 dy = pY[kk * 64 + cp];
+            const float2 uo = lds_pair(su, k * kRB + colS[i]);
+            const float dl[2] = {v.x, v.z};
+            float dsp[2];
 #pragma unroll
-              for (int i = 0; i < kOwnB; ++i) {
-                const int km = i * TPC + q;
-                if (dvalid && (kFull || km < nv)) {
-                  const size_t o = (size_t)(t0 + cstep + km) * D;
-                  st_act(static_cast<Act*>(p.du) + bd_off + o, o_du[i]);
-                  st_act(static_cast<Act*>(p.d_delta_raw) + bd_off + o, o_dr[i]);
-                  if (kGate) st_act(static_cast<Act*>(p.dz) + bd_off + o, o_dz[i]);
-                }
-              }
-            };
-            if (cnt8 == kSub)
-              sub(std::true_type{});
-            else
-              sub(std::false_type{});
-            // B5: hand the sub-chunk's per-warp partials to the reducer warp
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&wfull[slot]);
-            ++nsub_done;
+            for (int cc = 0; cc < 2; ++cc) {
+              // softplus' = sigmoid(s) = 1 - e^{-delta}; zero where the limit
+              // clamped delta (delta on a bound: a clamped step, or a softplus
+              // exactly on it, which has measure zero)
+              const bool free_dt = !kLimit || ((dl[cc] > p.dt_min || p.dt_min <= 0.f) && dl[cc] < p.dt_max);
+              dsp[cc] = free_dt ? (kFast ? dsoftplus_fast(dl[cc]) : -expm1f(-dl[cc])) : 0.f;
+            }
+            const float2 o_du = make_float2(fmaf(Dp2.x, dy.x, dl[0] * a4.y), fmaf(Dp2.y, dy.y, dl[1] * a4.w));
+            const float2 o_dr = make_float2(fmaf(uo.x, a4.y, a2.x * kAscale) * dsp[0], fmaf(uo.y, a4.w, a2.y * kAscale) * dsp[1]);
+            const float2 o_dz = make_float2(fmaf(Dp2.x, uo.x, a4.x) * dzf[i].x, fmaf(Dp2.y, uo.y, a4.z) * dzf[i].y);
+            accD = ffma2(dy, uo, accD);
+            accBias = fadd2(accBias, o_dr);
+            if (dvalid) {
+              const size_t o = bd_off + (size_t)(t0 + k) * D;
+              st_pair(static_cast<Act*>(p.du) + o, o_du);
+              st_pair(static_cast<Act*>(p.d_delta_raw) + o, o_dr);
+              if (kGate) st_pair(static_cast<Act*>(p.dz) + o, o_dz);
+            }
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        if (++s == S) {
-          s = 0;
-          par ^= 1;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      if (++s == kBS) {
+        s = 0;
+        par ^= 1;
+      }
+      // chunk sums -> compensated running totals
+      {
+        const float cs12[12] = {accA[0][0].x, accA[0][0].y, accA[0][1].x, accA[0][1].y,
+                                accA[1][0].x, accA[1][0].y, accA[1][1].x, accA[1][1].y,
+                                accD.x, accD.y, accBias.x, accBias.y};
+#pragma unroll
+        for (int i = 0; i < 12; ++i) {
+          float sm = tot[i * kLanes], cm = cmp[i * kLanes];
+          kahan_add(sm, cm, cs12[i]);
+          tot[i * kLanes] = sm;
+          cmp[i * kLanes] = cm;
         }
       }
-      // chunk sums -> compensated running totals (per-lane private smem)
-      kahan_add(my_tot[0], my_cmp[0], accA[0].x);
-      kahan_add(my_tot[1], my_cmp[1], accA[0].y);
-      kahan_add(my_tot[2], my_cmp[2], accA[1].x);
-      kahan_add(my_tot[3], my_cmp[3], accA[1].y);
-      kahan_add(my_tot[4], my_cmp[4], accD);
-      kahan_add(my_tot[5], my_cmp[5], accBias);
     }
     // ---------------- the piece's parameter partials (row b * nseg + kp) and dh0
     {
-      // dDp and d_delta_bias: each lane summed its owned steps; add the channel's TPC lanes
-      float tD = my_tot[4], tBs = my_tot[5];
+      // dDp and d_delta_bias: each lane summed its owned steps; add the pair's TPC lanes
+      float t4[4] = {tot[8 * kLanes], tot[9 * kLanes], tot[10 * kLanes], tot[11 * kLanes]};
 #pragma unroll
-      for (int m = 1; m < TPC; m <<= 1) {
-        tD += __shfl_xor_sync(0xffffffffu, tD, m);
-        tBs += __shfl_xor_sync(0xffffffffu, tBs, m);
-      }
+      for (int m = 1; m < TPC; m <<= 1)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) t4[i] += __shfl_xor_sync(0xffffffffu, t4[i], m);
       if (dvalid) {
-        float* wp = p.ws_param + (((size_t)b * p.nseg + kp) * D + d) * (N + 2);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int n = 4 * q + 2 * i;
-          wp[n] = (A2[i].x * kAscale) * my_tot[2 * i];
-          wp[n + 1] = (A2[i].y * kAscale) * my_tot[2 * i + 1];
-          if (p.dh0 && c_lo == 0) *reinterpret_cast<float2*>(p.dh0 + ((size_t)b * D + d) * N + n) = carry[i];
-        }
-        if (q == 0) {
-          wp[N] = tD;
-          wp[N + 1] = tBs;
-        }
-        if (p.seq_flag) {
-          // rows of pieces this sequence does not have stay zero for the finalize
-          for (int k2 = plan_pieces(pl, sq); k2 < p.nseg; ++k2) {
-            float* wz = p.ws_param + (((size_t)b * p.nseg + k2) * D + d) * (N + 2);
-            wz[4 * q] = wz[4 * q + 1] = wz[4 * q + 2] = wz[4 * q + 3] = 0.f;
-            if (q == 0) wz[N] = wz[N + 1] = 0.f;
+        for (int cc = 0; cc < 2; ++cc) {
+          float* wp = p.ws_param + (((size_t)b * p.nseg + kp) * D + dA + cc) * (N + 2);
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int n = 4 * q + 2 * i;
+            wp[n] = (A2[cc][i].x * kAscale) * tot[(4 * cc + 2 * i) * kLanes];
+            wp[n + 1] = (A2[cc][i].y * kAscale) * tot[(4 * cc + 2 * i + 1) * kLanes];
+            if (p.dh0 && c_lo == 0)
+              *reinterpret_cast<float2*>(p.dh0 + ((size_t)b * D + dA + cc) * N + n) = carry[cc][i];
+          }
+          if (q == 0) {
+            wp[N] = t4[cc];
+            wp[N + 1] = t4[2 + cc];
+          }
+          if (p.seq_flag) {
+            // rows of pieces this sequence does not have stay zero for the finalize
+            for (int k2 = plan_pieces(pl, sq); k2 < p.nseg; ++k2) {
+              float* wz = p.ws_param + (((size_t)b * p.nseg + k2) * D + dA + cc) * (N + 2);
+              wz[4 * q] = wz[4 * q + 1] = wz[4 * q + 2] = wz[4 * q + 3] = 0.f;
+              if (q == 0) wz[N] = wz[N + 1] = 0.f;
+            }
           }
         }
       }
@@ -657,11 +677,14 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
         // hand-over mode, the sequence's last piece: its final carry enters the
         // first piece's last step; publish it and raise the flag
         if (dvalid) {
-          float* co = p.seg_carry + (((size_t)b * p.nseg + kp - 1) * D + d) * N + 4 * q;
-          __stcg(co, carry[0].x);
-          __stcg(co + 1, carry[0].y);
-          __stcg(co + 2, carry[1].x);
-          __stcg(co + 3, carry[1].y);
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            float* co = p.seg_carry + (((size_t)b * p.nseg + kp - 1) * D + dA + cc) * N + 4 * q;
+            __stcg(co, carry[cc][0].x);
+            __stcg(co + 1, carry[cc][0].y);
+            __stcg(co + 2, carry[cc][1].x);
+            __stcg(co + 3, carry[cc][1].y);
+          }
         }
         __threadfence();
         named_bar_sync(2, kLanes);
@@ -669,13 +692,13 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
       }
     }
   }  // pieces
-  // every consumer is done with TMEM (loads waited for inline, stores before
-  // the loads of the same chunk): free it
+  // every consumer is done with TMEM (loads waited for inline, stores waited
+  // for before the loads of the same chunk): free it
   tmem_fence_before_sync();
   named_bar_sync(1, kLanes);
   if (warp == 0) {
     tmem_fence_after_sync();
-    tmem_dealloc(*tmem_slot, kTmemCols);
+    tmem_dealloc(*tmem_slot, LY::kTmemCols);
   }
 }
 
@@ -722,13 +745,14 @@ __global__ void __launch_bounds__(kAggWarps * 32) s6_bwd_agg_kernel(const __grid
     return;
   }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // channels [d0, d0 + kValid) of the 64-channel tile d0 / kDTile (for
-  // TPC = 1 the CTA's 128 lanes cover the tile and the next one, whose
-  // lanes only load); piece seg >= 1 of the sequence (b, tile), if it has one
+  // channels [d0, d0 + kValid) of the sequence's channel tile d0 / kBwdTile
+  // (for TPC = 1 the CTA's 128 lanes cover kValid = 64 channels and the next
+  // 64, whose lanes only load); piece seg >= 1 of the sequence (b, tile), if
+  // it has one
   constexpr int kValid = kCh < kDTile ? kCh : kDTile;
   const int b = blockIdx.y, d0 = blockIdx.x * kValid, seg = blockIdx.z + 1;
   const int L = p.L, D = p.D;
-  const long long sq = (long long)b * p.plan.ndt + d0 / kDTile;
+  const long long sq = (long long)b * p.plan.ndt + d0 / kBwdTile;
   if (seg >= plan_pieces(p.plan, sq)) return;  // the whole CTA, before any barrier or copy
   int c_lo, c_hi;
   plan_piece_range(p.plan, sq, seg, c_lo, c_hi);
@@ -881,7 +905,7 @@ __global__ void s6_bwd_seg_carry_kernel(const BwdParams p) {
   const int b = blockIdx.y;
   if (e >= per) return;
   const int d = (int)(e / p.N), n = (int)(e % p.N);
-  const int K = plan_pieces(p.plan, (long long)b * p.plan.ndt + d / kDTile);
+  const int K = plan_pieces(p.plan, (long long)b * p.plan.ndt + d / kBwdTile);
   float chi = p.dh_last ? p.dh_last[(size_t)b * per + e] : 0.f;
   for (int k = K - 1; k >= 0; --k) {
     p.seg_carry[((size_t)b * p.nseg + k) * per + e] = chi;
@@ -928,28 +952,10 @@ bool make_map(CUtensorMap* m, const void* base, int act, uint64_t rows, uint64_t
   return encode_tile_map(m, base, act == SSM_BF16, 2, dims, strides, box, swizzle);
 }
 
-template <typename Act, int TPC>
-size_t bwd_smem_bytes() {
-  const bool bf = std::is_same<Act, __nv_bfloat16>::value;
-  const int S = BwdStages<Act>::value;
-  const int N = 4 * TPC, lanes = kDTile * TPC, cw = lanes / 32;
-  size_t bytes = (size_t)S * (4 * kTT * kDTile + 2 * kTT * N) * sizeof(Act);
-  bytes += (bf ? (size_t)S * kTT * 2 * N : 0) * 4;      // bcf
-  bytes += (size_t)kChunk * kRow * 8;                    // dbuf (float2)
-  bytes += (size_t)lanes * 16;                           // hc0
-  bytes += (size_t)cw * kRedSlots * kRedSlot * 4;        // redw
-  bytes += (size_t)2 * kSub * cw * 32 * 4;               // wpart
-  bytes += (size_t)kSub * (lanes + 1) * 16;              // part (float4)
-  bytes += (size_t)kSub * kRow * 8;                      // bprep
-  bytes += (size_t)2 * lanes * 6 * 4;                    // tot
-  bytes += (3 * S + 4) * 8 + 16;                         // barriers, TMEM address
-  return bytes;
-}
-
 template <typename Act, int TPC, bool kFast, bool kGate, bool kLimit>
 cudaError_t launch_one(const BwdTmaParams& P, cudaStream_t stream, bool cooperative) {
   auto kern = s6_bwd_tma_kernel<Act, TPC, kFast, kGate, kLimit>;
-  const size_t smem = bwd_smem_bytes<Act, TPC>();
+  const size_t smem = BwdLayout<Act, TPC>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // persistent: one CTA per range of the plan
@@ -1023,7 +1029,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 BwdPlan bwd_plan(int B, int L, int D, int N, int sms) {
   BwdPlan pl;
   pl.nch = L > 0 ? (L + kChunk - 1) / kChunk : 0;
-  pl.ndt = D > 0 ? (D + kDTile - 1) / kDTile : 0;
+  pl.ndt = D > 0 ? (D + kBwdTile - 1) / kBwdTile : 0;
   pl.U = (long long)(B > 0 ? B : 0) * pl.ndt * pl.nch;
   pl.P = (int)std::max<long long>(1, std::min<long long>(std::max(sms, 1), pl.U));
   pl.maxp = 1;
@@ -1062,7 +1068,7 @@ cudaError_t launch_bwd_tma(const BwdParams& p, int act, cudaStream_t stream) {
   P.p = p;
   const uint64_t rows = (uint64_t)p.B * p.L;
   // activation tiles: 128-byte swizzled boxes of 128-byte rows (64 bf16 / 32 f32 channels)
-  const uint32_t abox = act == SSM_BF16 ? kDTile : kDTile / 2;
+  const uint32_t abox = act == SSM_BF16 ? 64 : 32;
   bool ok = make_map(&P.map_u, p.u, act, rows, p.D, kTT, abox, CU_TENSOR_MAP_SWIZZLE_128B) &&
             make_map(&P.map_raw, p.delta_raw, act, rows, p.D, kTT, abox, CU_TENSOR_MAP_SWIZZLE_128B) &&
             make_map(&P.map_dout, p.dout, act, rows, p.D, kTT, abox, CU_TENSOR_MAP_SWIZZLE_128B) &&

@@ -13,7 +13,8 @@
 namespace s6 {
 
 constexpr int kChunk = SSM_CHUNK_LEN;  // steps between saved chunk states
-constexpr int kDTile = 64;             // channels per CTA in the scan kernels
+constexpr int kDTile = 64;             // channels per CTA in the forward scan kernels
+constexpr int kBwdTile = 128;          // channels per CTA (and per sequence) in the TMA backward
 constexpr int kThreadsPerChannel = 2;  // each channel's N states are split over 2 lanes
 constexpr int kScanThreads = kDTile * kThreadsPerChannel;
 constexpr int kSub = 8;                // backward: steps kept in registers per sub-chunk
@@ -29,7 +30,7 @@ constexpr unsigned int kStatusLayoutBit = 2u;       // same bit as kStatusLayout
 // range covers pieces of one or more sequences; a sequence cut by range
 // boundaries has K > 1 pieces, numbered in time order.  The plan is a
 // function of the shape only.
-//   Backward (64-channel tiles, unit s * nch + c): piece k > 0 needs the
+//   Backward (128-channel tiles, unit s * nch + c): piece k > 0 needs the
 //   adjoint carry of the pieces after it -- handed over between CTAs, or
 //   composed from piece aggregates (the chunked parallel scan); piece k of
 //   sequence (b, j) owns row b * maxp + k of the parameter partials.
@@ -118,7 +119,8 @@ struct BwdParams {
   void* d_delta_raw;
   void* dz;    // non-null iff z non-null
   float* dh0;  // nullable
-  float* ws_dbc;    // [ndt][B][L][2][N] per-CTA sums of the dBm / dCm terms
+  float* ws_dbc;    // [ndt][B][L][2][N] per-channel-tile sums of the dBm / dCm terms
+  int* ws_ndt;      // the number ndt of those tile rows, written by the kernel that fills them
   float* ws_param;  // [B][nseg][D][N+2] per-(batch, segment) sums: A*sum(...), dDp, d_delta_bias
   unsigned int* status;  // device status word (bounded waits report here)
   float dt_min, dt_max;   // limit on delta = softplus(s); 0 and +inf: none
@@ -224,7 +226,8 @@ BwdPlan bwd_plan(int B, int L, int D, int N, int sms);
 // The TMA forward's stream plan (three CTAs on each of `sms` SMs); handover
 // is false when the grid mode is kept.
 FwdPlan fwd_stream_plan(int B, int L, int D, int N, int act, int sms);
-cudaError_t launch_reduce_dbc(const float* ws_dbc, int ndt, int B, int L, int N, void* dBm,
+// ndt: the device int the partials kernel wrote (how many tile rows ws_dbc holds)
+cudaError_t launch_reduce_dbc(const float* ws_dbc, const int* ndt, int B, int L, int N, void* dBm,
                               void* dCm, int act, cudaStream_t stream);
 cudaError_t launch_reduce_params(const float* ws_param, int B, int D, int N, float* dA_log,
                                  float* dDp, float* d_delta_bias, cudaStream_t stream);

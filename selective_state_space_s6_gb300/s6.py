@@ -22,7 +22,7 @@ _lib = None
 
 SSM_F32, SSM_BF16 = 0, 1
 CONV_PATHS = {0: "scalar", 1: "vector", 2: "tile"}
-CHUNK_LEN = 64
+CHUNK_LEN = 32
 MAX_DSTATE = 16
 
 

@@ -136,16 +136,19 @@ def test_ssd_validation(lib):
 def test_segment_plan(lib):
     """The plans are functions of the shape.  Forward: one pass where the grid
     fills the GPU, time segments of at least 512 steps for long sequences over
-    few channels.  Backward: the (batch x 64-channel tile) sequences are cut
-    into 152 equal ranges of 64-step chunks; it reports 1 when no aggregate
+    few channels.  Backward: the (batch x 128-channel tile) sequences are cut
+    into 152 equal ranges of 32-step chunks; it reports 1 when no aggregate
     pass is needed (no cut, or cut sequences hand their carry over), else the
     most pieces any sequence has."""
     bf16, f32 = s6.SSM_BF16, s6.SSM_F32
-    # 4 x 64 sequences of 64 chunks over 152 ranges of ~108 chunks: at most one
+    # 4 x 32 sequences of 128 chunks over 152 ranges of ~108 chunks: ranges
+    # shorter than a sequence, some sequences cut twice: aggregate pass
+    assert s6.plan_segments(4, 4096, 4096, 16, bf16) == (1, 3)
+    # 4 x 40 sequences of 8 chunks over 152 ranges of ~8.4 chunks: at most one
     # cut each, ranges longer than a sequence: carries handed over
-    assert s6.plan_segments(4, 4096, 4096, 16, bf16) == (1, 1)
+    assert s6.plan_segments(4, 256, 5120, 16, bf16)[1] == 1
     # 152 sequences: one range each, no cut
-    assert s6.plan_segments(2, 4096, 76 * 64, 16, bf16)[1] == 1
+    assert s6.plan_segments(2, 4096, 76 * 128, 16, bf16)[1] == 1
     # one sequence of 35 chunks: 35 ranges of one chunk
     assert s6.plan_segments(1, 1100, 64, 16, f32)[1] == -(-1100 // s6.CHUNK_LEN)
     f, b = s6.plan_segments(1, 65536, 2048, 16, f32)

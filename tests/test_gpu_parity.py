@@ -267,7 +267,7 @@ def test_decode_1000_chained_steps():
     assert diff_h / scale_h <= TOL["f32"], diff_h / scale_h
 
 
-@pytest.mark.parametrize("B,L,D,N,act", [(4, 256, 2560, 16, "bf16"), (3, 192, 4096, 16, "f32")])
+@pytest.mark.parametrize("B,L,D,N,act", [(4, 256, 5120, 16, "bf16"), (3, 192, 8192, 16, "f32")])
 def test_handover_mode(B, L, D, N, act):
     """Shapes whose backward cuts every (batch, channel tile) sequence at most
     once, with ranges longer than a sequence: the carry is handed from the CTA
