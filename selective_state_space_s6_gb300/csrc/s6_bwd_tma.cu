@@ -129,11 +129,24 @@ struct BwdLayout {
   // stage: u, raw, z, dout tiles, then the Bm and Cm rows; 1024-byte multiple
   static constexpr int kStageB = ((4 * kTileB + 2 * kBCB) + 1023) / 1024 * 1024;
   static constexpr int kBcfB = kBf16 ? kBS * kTT * 2 * N * 4 : 0;  // f32 Bm/Cm rows [S][TT][2][N]
-  static constexpr int kPAB = kTT * 64 * 16;                     // pA [TT][64 pairs] float4
-  static constexpr int kPYB = kSC * 64 * 8;                      // pY [SC][64 pairs] float2
-  static constexpr int kPart4B = kSC * kLanes * 16;              // [SC][lanes] (y0, gB0, y1, gB1)
-  static constexpr int kPart2B = kSC * kLanes * 8;               // [SC][lanes] (Ap0, Ap1)
-  static constexpr int kDsumB = 2 * kSC * kCW * 32 * 4;          // [2 slots][SC][kCW][32]
+  // Row strides, padded so that the lanes of a pair (which own different
+  // steps, i.e. rows) hit different banks: pA rows of 64 float4 + 2, pY rows of
+  // 64 float2 + 4, part4 / part2 rows of kLanes + 1 elements.
+  // (f32: pA unpadded, to fit the larger tiles)
+  static constexpr int kRA = kBf16 ? 64 + 2 : 64, kRY = 64 + 4, kRP4 = kLanes + 1, kRP2 = kLanes + 1;
+  static constexpr int kPAB = kTT * kRA * 16;                    // pA [TT][kRA] float4 (delta, delta*u) x 2
+  static constexpr int kPYB = kSC * kRY * 8;                     // pY [SC][kRY] float2 (dy0, dy1)
+  static constexpr int kPart4B = kSC * kRP4 * 16;                // [SC][kRP4] (y0, gB0, y1, gB1)
+  static constexpr int kPart2B = kSC * kRP2 * 8;                 // [SC][kRP2] (Ap0, Ap1)
+  // dBm/dCm terms over the CTA's channels: bf16 -- each lane's 8 values of a
+  // step in shared memory ([2 slots][SC][64 pairs][TPC groups][8] floats),
+  // added by the reducer warp; f32 (less
+  // shared memory) -- a warp-level xor reduce-scatter first, the warps' sums
+  // ([2 slots][SC][kCW][32]) added by the reducer warp
+  static constexpr bool kRedSmem = kBf16;
+  static constexpr int kRedPair = TPC * 8;  // floats per channel pair in a step's block
+  static constexpr int kRedStep = 64 * kRedPair;
+  static constexpr int kDsumB = kRedSmem ? 2 * kSC * kRedStep * 4 : 2 * kSC * kCW * 32 * 4;
   static constexpr int kTotB = 2 * 12 * kLanes * 4;              // [2 (sum, comp)][12][lanes] running totals
   static constexpr int kOffBcf = kBS * kStageB;
   static constexpr int kOffPA = kOffBcf + kBcfB;
@@ -307,8 +320,32 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
           const int slot = n & 1;
           if (ok) ok = mbar_wait(&wfull[slot], (uint32_t)(n >> 1) & 1, p.status);
           const int cnt = min(kSC, clen - sc * kSC);
-          const float* src = dsum + slot * (kSC * kCW * 32);
-          if (lane < 2 * N) {
+          const float* src = dsum + slot * (LY::kDsumB / 8);
+          if constexpr (LY::kRedSmem) {
+            // lane = slice * nG + group: group (q, qty) = 4 outputs, the slice
+            // a contiguous run of kCPL pairs; slices added by an xor butterfly
+            constexpr int nG = 2 * TPC, kLPG = 32 / nG, kCPL = 64 / kLPG;
+            const int og = lane % nG, sl = lane / nG;
+            const int gq = og >> 1, qty = og & 1;
+            for (int k = 0; k < cnt; ++k) {
+              const float* rp = src + k * LY::kRedStep + (sl * kCPL) * LY::kRedPair + 8 * gq + 4 * qty;
+              float2 a = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
+#pragma unroll
+              for (int i = 0; i < kCPL; ++i) {
+                const float4 v = *reinterpret_cast<const float4*>(rp + i * LY::kRedPair);
+                a = fadd2(a, make_float2(v.x, v.y));
+                b2 = fadd2(b2, make_float2(v.z, v.w));
+              }
+#pragma unroll
+              for (int m = nG; m < 32; m <<= 1) {
+                a = fadd2(a, make_float2(__shfl_xor_sync(0xffffffffu, a.x, m), __shfl_xor_sync(0xffffffffu, a.y, m)));
+                b2 = fadd2(b2, make_float2(__shfl_xor_sync(0xffffffffu, b2.x, m), __shfl_xor_sync(0xffffffffu, b2.y, m)));
+              }
+              if (sl == 0)
+                *reinterpret_cast<float4*>(ws_r + (size_t)(c * kChunk + sc * kSC + k) * 2 * N + qty * N + 4 * gq) =
+                    make_float4(a.x, a.y, b2.x, b2.y);
+            }
+          } else if (lane < 2 * N) {
             for (int k = 0; k < cnt; ++k) {
               float v = src[(k * kCW) * 32 + lane];
 #pragma unroll
@@ -424,7 +461,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
                               : make_float2(softplus_f(sv.x), softplus_f(sv.y));
             if (kLimit) sp = make_float2(clamp_dt(sp.x, p.dt_min, p.dt_max), clamp_dt(sp.y, p.dt_min, p.dt_max));
             const float2 du2 = fmul2(sp, lds_pair(su, o));
-            pA[k * 64 + cp] = make_float4(sp.x, du2.x, sp.y, du2.y);
+            pA[k * LY::kRA + cp] = make_float4(sp.x, du2.x, sp.y, du2.y);
           }
         }
       }
@@ -434,7 +471,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
       {
         float hb[32];
         auto stepA = [&](int k, int kk) {  // kk = k % kSC (a constant)
-          const float4 v = pA[k * 64 + cp];
+          const float4 v = pA[k * LY::kRA + cp];
           const float4 Bv = *reinterpret_cast<const float4*>(Bt + k * kBst);
           const float2 B01 = make_float2(Bv.x, Bv.y), B23 = make_float2(Bv.z, Bv.w);
           const float2 d0v = make_float2(v.x, v.x), u0v = make_float2(v.y, v.y);
@@ -496,19 +533,19 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
             }
           }
           dzf[i] = f;
-          pY[(i * TPC + q) * 64 + cp] = dy;
+          pY[(i * TPC + q) * LY::kRY + cp] = dy;
         }
         __syncwarp();
         const int slot = nsub & 1;
         if (nsub >= 2 && !failed) failed = !mbar_wait(&wempty[slot], (uint32_t)((nsub >> 1) - 1) & 1, p.status);
-        float* ds = dsum + slot * (kSC * kCW * 32);
+        float* ds = dsum + slot * (LY::kDsumB / 8);
         // B3: reverse steps
         auto stepB = [&](int kk) {
           const int k = kb + kk;
           uint32_t hq[8];
           tmem_ld8_issue(tm + (uint32_t)(8 * k), hq);  // the state before step k
-          const float4 v = pA[k * 64 + cp];
-          const float2 dy = pY[kk * 64 + cp];
+          const float4 v = pA[k * LY::kRA + cp];
+          const float2 dy = pY[kk * LY::kRY + cp];
           const float4 Bv = *reinterpret_cast<const float4*>(Bt + k * kBst);
           const float4 Cv = *reinterpret_cast<const float4*>(Ct + k * kBst);
           const float2 Bp[2] = {make_float2(Bv.x, Bv.y), make_float2(Bv.z, Bv.w)};
@@ -548,8 +585,15 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
           }
 #pragma unroll
           for (int j = 0; j < 8; ++j) hk[j] = __uint_as_float(hq[j]);
-          part4[kk * kLanes + tid] = make_float4(ya[0].x + ya[0].y, gba[0].x + gba[0].y, ya[1].x + ya[1].y, gba[1].x + gba[1].y);
-          part2[kk * kLanes + tid] = make_float2(apa[0].x + apa[0].y, apa[1].x + apa[1].y);
+          part4[kk * LY::kRP4 + tid] = make_float4(ya[0].x + ya[0].y, gba[0].x + gba[0].y, ya[1].x + ya[1].y, gba[1].x + gba[1].y);
+          part2[kk * LY::kRP2 + tid] = make_float2(apa[0].x + apa[0].y, apa[1].x + apa[1].y);
+          if constexpr (LY::kRedSmem) {
+            // this lane's 8 terms (summed over its 2 channels) for the reducer warp
+            float* rp = ds + kk * LY::kRedStep + cp * LY::kRedPair + 8 * q;
+            *reinterpret_cast<float4*>(rp) = make_float4(dB[0].x, dB[0].y, dB[1].x, dB[1].y);
+            *reinterpret_cast<float4*>(rp + 4) = make_float4(dC[0].x, dC[0].y, dC[1].x, dC[1].y);
+            return;
+          }
           // channel sums over the warp's pairs: xor reduce-scatter, 8 values -> 1
           const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
           float r0[4];
@@ -572,7 +616,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
           for (int mk = 2; mk >= TPC; mk >>= 1) r2 += __shfl_xor_sync(0xffffffffu, r2, mk);
           if (rs_store) ds[(kk * kCW + warp) * 32 + rs_o] = r2;
         };
-#pragma unroll 1
+#pragma unroll 2
         for (int kk = min(kSC, cnt - kb) - 1; kk >= 0; --kk) stepB(kk);
         __syncwarp();
         if (lane == 0) mbar_arrive(&wfull[slot]);
@@ -582,17 +626,17 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
         for (int i = 0; i < kOwn; ++i) {
           const int kk = i * TPC + q, k = kb + kk;
           if (k < cnt) {
-            float4 a4 = part4[kk * kLanes + cp * TPC];
-            float2 a2 = part2[kk * kLanes + cp * TPC];
+            float4 a4 = part4[kk * LY::kRP4 + cp * TPC];
+            float2 a2 = part2[kk * LY::kRP2 + cp * TPC];
 #pragma unroll
             for (int r = 1; r < TPC; ++r) {
-              const float4 o4 = part4[kk * kLanes + cp * TPC + r];
-              const float2 o2 = part2[kk * kLanes + cp * TPC + r];
+              const float4 o4 = part4[kk * LY::kRP4 + cp * TPC + r];
+              const float2 o2 = part2[kk * LY::kRP2 + cp * TPC + r];
               a4 = make_float4(a4.x + o4.x, a4.y + o4.y, a4.z + o4.z, a4.w + o4.w);
               a2 = make_float2(a2.x + o2.x, a2.y + o2.y);
             }
-            const float4 v = pA[k * 64 + cp];
-            const float2 dy = pY[kk * 64 + cp];
+            const float4 v = pA[k * LY::kRA + cp];
+            const float2 dy = pY[kk * LY::kRY + cp];
             const float2 uo = lds_pair(su, k * kRB + colS[i]);
             const float dl[2] = {v.x, v.z};
             float dsp[2];
