@@ -19,7 +19,8 @@
  * Entry points: the scan (forward with and without saves, backward, its two
  * halves, a no-allocation backward, the decode step), their _ex variants with
  * a limit on delta, the causal depthwise conv1d + SiLU in front of the scan
- * (forward, backward, step), and the Mamba-2 SSD forward.
+ * (forward, backward, step), and the Mamba-2 SSD forward (with and without
+ * state saves) and backward.
  *
  * Conventions shared by every entry point
  *   - Shapes: B = batch, L = seqlen, D = dim (d_inner), N = dstate, 1 <= N <= 16.
@@ -320,6 +321,55 @@ int ssm_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, 
                 int64_t dstate, int act, const void *x, const void *dt_raw, const float *dt_bias,
                 const float *A_log, const void *Bm, const void *Cm, const float *Dp, const float *h0,
                 void *y, float *h_last, const ssm_scan_options *opts, void *stream);
+
+/* Steps per chunk of the SSD's chunked form (and between its saved states). */
+#define SSM_SSD_CHUNK_LEN 64
+
+/*
+ * ssm_ssd_fwd that also saves, for the backward, the state entering every
+ * chunk: chunk_states [B][H][ceil(L/64)][N][P] bf16 (device, caller-owned,
+ * 16-byte aligned), chunk c holding the state before step 64c as the bf16
+ * copy the chunk's readout uses (chunk 0: h0, or zeros).  Otherwise the same
+ * as ssm_ssd_fwd (same results, bit for bit).
+ */
+int ssm_ssd_fwd_save(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups,
+                     int64_t dstate, int act, const void *x, const void *dt_raw, const float *dt_bias,
+                     const float *A_log, const void *Bm, const void *Cm, const float *Dp, const float *h0,
+                     void *y, float *h_last, void *chunk_states, const ssm_scan_options *opts, void *stream);
+
+/* Scratch bytes ssm_ssd_bwd needs in `ws` (per-head dBm / dCm terms and
+ * per-(batch, head) parameter sums); -1 for an invalid or unsupported shape. */
+int64_t ssm_ssd_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                                    int64_t ngroups, int64_t dstate, int act);
+
+/*
+ * Mamba-2 SSD backward (deterministic_backward.py page: the backward of the
+ * ssd_combined kernels -- dx, dB, dC, the dt and A gradients -- by single
+ * writers with every sum in a fixed order, no float atomics).  The gradient of
+ *   loss = sum(dy * y) + sum(dh_last * h_last)
+ * through the recurrence of ssm_ssd_fwd (same shapes, same limit `opts`):
+ *   inputs : the forward's inputs; chunk_states from ssm_ssd_fwd_save on
+ *            them; dy [B][L][H][P]; dh_last nullable (zeros) [B][H][N][P] f32
+ *   outputs: dx [B][L][H][P]; ddt_raw [B][L][H] (the gradient w.r.t. dt_raw,
+ *            softplus' applied, zero where the limit clamped delta; the mask
+ *            is inclusive at both bounds); dBm, dCm [B][L][G][N] (summed over
+ *            the heads of a group in ascending head order) -- act dtype;
+ *            ddt_bias, dA_log, dDp [H] f32 (summed over batch and steps in a
+ *            fixed order); dh0 nullable [B][H][N][P] f32.
+ *   ws/ws_bytes: at least ssm_ssd_bwd_workspace_bytes() bytes, 256-byte
+ *            aligned.
+ * Evaluated per chunk of 64 steps, last chunk first, in the chunked matrix
+ * form on the tensor cores (bf16 operands, f32 accumulation; the state's
+ * gradient in f32).  Supported: as ssm_ssd_fwd (bf16, P = 64, N in {64,
+ * 128}); dy, dx, dh_last, dh0, chunk_states 16-byte aligned.  Results are
+ * bit-identical from call to call.  Asynchronous on `stream`.
+ */
+int ssm_ssd_bwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups,
+                int64_t dstate, int act, const void *x, const void *dt_raw, const float *dt_bias,
+                const float *A_log, const void *Bm, const void *Cm, const float *Dp,
+                const void *chunk_states, const void *dy, const float *dh_last, void *dx, void *ddt_raw,
+                float *ddt_bias, float *dA_log, void *dBm, void *dCm, float *dDp, float *dh0, void *ws,
+                size_t ws_bytes, const ssm_scan_options *opts, void *stream);
 
 /* ---------------------------------------------------------------------------
  * Causal depthwise conv1d + SiLU, the convolution in front of the scan in a

@@ -673,22 +673,29 @@ int ssm_conv1d_path(int64_t batch, int64_t seqlen, int64_t dim, int64_t width, i
   return s6::conv1d_path(p, act, dout != nullptr);
 }
 
-int ssm_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups,
-                int64_t dstate, int act, const void* x, const void* dt_raw, const float* dt_bias,
-                const float* A_log, const void* Bm, const void* Cm, const float* Dp, const float* h0,
-                void* y, float* h_last, const ssm_scan_options* opts, void* stream) {
-  const int64_t B = batch, L = seqlen, H = nheads, P = headdim, G = ngroups, N = dstate;
-  float dt_lo, dt_hi;
-  S6_TRY(read_opts(opts, &dt_lo, &dt_hi));
+// shape checks shared by the SSD entry points
+int check_ssd(int64_t B, int64_t L, int64_t H, int64_t P, int64_t G, int64_t N, int act, const char* what) {
   if (act != SSM_F32 && act != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "act must be SSM_F32 or SSM_BF16, got %d", act);
   if (B < 0 || L < 0 || H < 1 || P < 1 || G < 1 || N < 1)
     return fail(SSM_ERR_INVALID_ARG, "bad SSD shape (B=%lld L=%lld H=%lld P=%lld G=%lld N=%lld)", (long long)B,
                 (long long)L, (long long)H, (long long)P, (long long)G, (long long)N);
   if (H % G != 0) return fail(SSM_ERR_INVALID_ARG, "nheads %lld is not a multiple of ngroups %lld", (long long)H, (long long)G);
   if (!s6::ssd_supported(act, (int)P, (int)N))
-    return fail(SSM_ERR_UNSUPPORTED, "SSD forward supports bf16 activations, headdim 64 and dstate 64 or 128");
-  if (B * L * H * P >= kMaxElems || B * L * G * N >= kMaxElems || B * H >= kMaxElems || L >= kMaxElems)
+    return fail(SSM_ERR_UNSUPPORTED, "SSD %s supports bf16 activations, headdim 64 and dstate 64 or 128", what);
+  const int64_t nch = (L + SSM_SSD_CHUNK_LEN - 1) / SSM_SSD_CHUNK_LEN;
+  if (B * L * H * P >= kMaxElems || B * L * H * N >= kMaxElems || B * H * nch * N >= kMaxElems || L >= kMaxElems)
     return fail(SSM_ERR_UNSUPPORTED, "problem too large for 31-bit indexing");
+  return SSM_OK;
+}
+
+int ssd_fwd_common(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups,
+                   int64_t dstate, int act, const void* x, const void* dt_raw, const float* dt_bias,
+                   const float* A_log, const void* Bm, const void* Cm, const float* Dp, const float* h0,
+                   void* y, float* h_last, void* chunk_states, const ssm_scan_options* opts, void* stream) {
+  const int64_t B = batch, L = seqlen, H = nheads, P = headdim, G = ngroups, N = dstate;
+  float dt_lo, dt_hi;
+  S6_TRY(read_opts(opts, &dt_lo, &dt_hi));
+  S6_TRY(check_ssd(B, L, H, P, G, N, act, "forward"));
   S6_TRY(need(x, B * L * H * P, 16, "x"));
   S6_TRY(need(dt_raw, B * L * H, 2, "dt_raw"));
   S6_TRY(need(dt_bias, H, 4, "dt_bias"));
@@ -699,6 +706,7 @@ int ssm_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, 
   S6_TRY(opt(h0, 4, "h0"));
   S6_TRY(need(y, B * L * H * P, 16, "y"));
   S6_TRY(opt(h_last, 8, "h_last"));
+  S6_TRY(opt(chunk_states, 16, "chunk_states"));
   g_last_error[0] = 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (B == 0) return SSM_OK;
@@ -713,13 +721,95 @@ int ssm_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, 
   }
   s6::SsdArgs a = {};
   a.x = x; a.dt_raw = dt_raw; a.Bm = Bm; a.Cm = Cm; a.dt_bias = dt_bias; a.A_log = A_log; a.Dp = Dp;
-  a.h0 = h0; a.y = y; a.h_last = h_last;
+  a.h0 = h0; a.y = y; a.h_last = h_last; a.chunk_states = chunk_states;
   a.status = s6::device_status_word();
   if (!a.status) return fail(SSM_ERR_CUDA, "cannot locate the device status word");
   a.dt_min = dt_lo; a.dt_max = dt_hi;
   a.B = (int)B; a.L = (int)L; a.H = (int)H; a.G = (int)G; a.N = (int)N;
   const cudaError_t ce = s6::launch_ssd_fwd(a, st);
   return ce == cudaSuccess ? SSM_OK : cuda_fail(ce, "ssm_ssd_fwd launch");
+}
+
+int ssm_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups,
+                int64_t dstate, int act, const void* x, const void* dt_raw, const float* dt_bias,
+                const float* A_log, const void* Bm, const void* Cm, const float* Dp, const float* h0,
+                void* y, float* h_last, const ssm_scan_options* opts, void* stream) {
+  return ssd_fwd_common(batch, seqlen, nheads, headdim, ngroups, dstate, act, x, dt_raw, dt_bias, A_log, Bm, Cm,
+                        Dp, h0, y, h_last, nullptr, opts, stream);
+}
+
+int ssm_ssd_fwd_save(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups,
+                     int64_t dstate, int act, const void* x, const void* dt_raw, const float* dt_bias,
+                     const float* A_log, const void* Bm, const void* Cm, const float* Dp, const float* h0,
+                     void* y, float* h_last, void* chunk_states, const ssm_scan_options* opts, void* stream) {
+  const int64_t nch = seqlen > 0 ? (seqlen + SSM_SSD_CHUNK_LEN - 1) / SSM_SSD_CHUNK_LEN : 0;
+  S6_TRY(need(chunk_states, batch * nheads * nch * dstate * headdim, 16, "chunk_states"));
+  return ssd_fwd_common(batch, seqlen, nheads, headdim, ngroups, dstate, act, x, dt_raw, dt_bias, A_log, Bm, Cm,
+                        Dp, h0, y, h_last, chunk_states, opts, stream);
+}
+
+int64_t ssm_ssd_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                                    int64_t ngroups, int64_t dstate, int act) {
+  if (check_ssd(batch, seqlen, nheads, headdim, ngroups, dstate, act, "backward") != SSM_OK) return -1;
+  return (int64_t)s6::ssd_bwd_workspace_bytes((int)batch, (int)seqlen, (int)nheads, (int)ngroups, (int)dstate);
+}
+
+int ssm_ssd_bwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups,
+                int64_t dstate, int act, const void* x, const void* dt_raw, const float* dt_bias,
+                const float* A_log, const void* Bm, const void* Cm, const float* Dp,
+                const void* chunk_states, const void* dy, const float* dh_last, void* dx, void* ddt_raw,
+                float* ddt_bias, float* dA_log, void* dBm, void* dCm, float* dDp, float* dh0, void* ws,
+                size_t ws_bytes, const ssm_scan_options* opts, void* stream) {
+  const int64_t B = batch, L = seqlen, H = nheads, P = headdim, G = ngroups, N = dstate;
+  float dt_lo, dt_hi;
+  S6_TRY(read_opts(opts, &dt_lo, &dt_hi));
+  S6_TRY(check_ssd(B, L, H, P, G, N, act, "backward"));
+  const int64_t nch = L > 0 ? (L + SSM_SSD_CHUNK_LEN - 1) / SSM_SSD_CHUNK_LEN : 0;
+  S6_TRY(need(x, B * L * H * P, 16, "x"));
+  S6_TRY(need(dt_raw, B * L * H, 2, "dt_raw"));
+  S6_TRY(need(dt_bias, H, 4, "dt_bias"));
+  S6_TRY(need(A_log, H, 4, "A_log"));
+  S6_TRY(need(Bm, B * L * G * N, 16, "Bm"));
+  S6_TRY(need(Cm, B * L * G * N, 16, "Cm"));
+  S6_TRY(need(Dp, H, 4, "Dp"));
+  S6_TRY(need(chunk_states, B * H * nch * N * P, 16, "chunk_states"));
+  S6_TRY(need(dy, B * L * H * P, 16, "dy"));
+  S6_TRY(opt(dh_last, 16, "dh_last"));
+  S6_TRY(need(dx, B * L * H * P, 16, "dx"));
+  S6_TRY(need(ddt_raw, B * L * H, 2, "ddt_raw"));
+  S6_TRY(need(ddt_bias, H, 4, "ddt_bias"));
+  S6_TRY(need(dA_log, H, 4, "dA_log"));
+  S6_TRY(need(dBm, B * L * G * N, 2, "dBm"));
+  S6_TRY(need(dCm, B * L * G * N, 2, "dCm"));
+  S6_TRY(need(dDp, H, 4, "dDp"));
+  S6_TRY(opt(dh0, 16, "dh0"));
+  S6_TRY(check_ws(ws, ws_bytes, (int64_t)s6::ssd_bwd_workspace_bytes((int)B, (int)L, (int)H, (int)G, (int)N)));
+  g_last_error[0] = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t ce;
+  if (B == 0 || L == 0) {
+    // no steps: no gradient but the one passing straight through to h0
+    ce = cudaMemsetAsync(ddt_bias, 0, sizeof(float) * H, st);
+    if (ce == cudaSuccess) ce = cudaMemsetAsync(dA_log, 0, sizeof(float) * H, st);
+    if (ce == cudaSuccess) ce = cudaMemsetAsync(dDp, 0, sizeof(float) * H, st);
+    if (ce == cudaSuccess && dh0 && B > 0) {
+      const size_t bytes = sizeof(float) * (size_t)(B * H * N * P);
+      ce = dh_last ? cudaMemcpyAsync(dh0, dh_last, bytes, cudaMemcpyDeviceToDevice, st) : cudaMemsetAsync(dh0, 0, bytes, st);
+    }
+    return ce == cudaSuccess ? SSM_OK : cuda_fail(ce, "ssm_ssd_bwd(empty)");
+  }
+  s6::SsdBwdArgs a = {};
+  a.f.x = x; a.f.dt_raw = dt_raw; a.f.Bm = Bm; a.f.Cm = Cm; a.f.dt_bias = dt_bias; a.f.A_log = A_log; a.f.Dp = Dp;
+  a.f.chunk_states = const_cast<void*>(chunk_states);
+  a.f.status = s6::device_status_word();
+  if (!a.f.status) return fail(SSM_ERR_CUDA, "cannot locate the device status word");
+  a.f.dt_min = dt_lo; a.f.dt_max = dt_hi;
+  a.f.B = (int)B; a.f.L = (int)L; a.f.H = (int)H; a.f.G = (int)G; a.f.N = (int)N;
+  a.dy = dy; a.dh_last = dh_last; a.dx = dx; a.ddt_raw = ddt_raw; a.dBm = dBm; a.dCm = dCm;
+  a.dA_log = dA_log; a.ddt_bias = ddt_bias; a.dDp = dDp; a.dh0 = dh0;
+  a.ws = static_cast<float*>(ws);
+  ce = s6::launch_ssd_bwd(a, st);
+  return ce == cudaSuccess ? SSM_OK : cuda_fail(ce, "ssm_ssd_bwd launch");
 }
 
 int ssm_conv1d_step(int64_t batch, int64_t dim, int64_t width, int act, const void* x, const float* w,

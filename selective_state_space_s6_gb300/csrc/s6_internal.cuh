@@ -214,10 +214,28 @@ struct SsdArgs {
   const float* h0;       // [B][H][N][P] or null
   void* y;               // [B][L][H][P] act
   float* h_last;         // [B][H][N][P] or null
+  void* chunk_states;    // [B][H][ceil(L/64)][N][P] bf16 or null (forward: written; backward: read)
   unsigned int* status;
   float dt_min, dt_max;
   int B, L, H, G, N;
 };
+// Mamba-2 SSD backward (s6_ssd_bwd.cu); the forward's SsdArgs plus these
+struct SsdBwdArgs {
+  SsdArgs f;             // the forward's inputs; f.chunk_states read, f.y unused
+  const void* dy;        // [B][L][H][P] act
+  const float* dh_last;  // [B][H][N][P] or null
+  void* dx;              // [B][L][H][P] act
+  void* ddt_raw;         // [B][L][H] act
+  void* dBm;             // [B][L][G][N] act
+  void* dCm;
+  float* dA_log;         // [H]
+  float* ddt_bias;       // [H]
+  float* dDp;            // [H]
+  float* dh0;            // [B][H][N][P] or null
+  float* ws;             // scratch: per-head dBm/dCm terms, per-(batch, head) scalars
+};
+size_t ssd_bwd_workspace_bytes(int B, int L, int H, int G, int N);
+cudaError_t launch_ssd_bwd(const SsdBwdArgs& a, cudaStream_t stream);
 bool ssd_supported(int act, int P, int N);
 cudaError_t launch_ssd_fwd(const SsdArgs& a, cudaStream_t stream);
 cudaError_t launch_conv1d_step(const ConvParams& p, int act, cudaStream_t stream);

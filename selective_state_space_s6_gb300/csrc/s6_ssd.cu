@@ -31,6 +31,7 @@
 #include "s6_internal.cuh"
 #include "s6_math.cuh"
 #include "s6_tma.cuh"
+#include "s6_umma.cuh"
 
 namespace s6 {
 
@@ -51,6 +52,9 @@ struct SsdParams {
   const float* h0;                  // [B][H][N][P] or null
   __nv_bfloat16* y;                 // [B][L][H][P]
   float* h_last;                    // [B][H][N][P] or null
+  // [B][H][nch][N][P] bf16 or null: the state entering every chunk, as the
+  // bf16 copy the chunk's readout uses (for the backward)
+  __nv_bfloat16* chunk_states;
   unsigned int* status;
   float dt_min, dt_max;
   int B, L, H, G, N;
@@ -59,61 +63,6 @@ struct SsdParams {
   // chunks [0, seg_chunks) from h0 and [seg_chunks, end) from h_last
   int mode, seg_chunks;
 };
-
-// byte offset of the 16-byte chunk `c8` (elements 8 c8 .. 8 c8 + 7) of row r
-// in a 128-byte swizzled box of 128-byte rows (the TMA's 128B swizzle: the
-// chunk index is XORed with the row's position in its 8-row group)
-__device__ __forceinline__ uint32_t swz(int r, int c8) { return (uint32_t)(r * 128 + ((c8 ^ (r & 7)) << 4)); }
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-__device__ __forceinline__ float2 unpack_bf16(uint32_t v) {
-  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
-}
-__device__ __forceinline__ float fast_exp(float x) { return ex2_approx(x * kLog2e); }
-
-// ---- tcgen05 (5th-generation tensor core) helpers
-// Shared-memory matrix descriptor of a 128-byte-swizzled operand: start
-// address, leading-dimension byte offset (between 64-element blocks of the
-// M/N dimension for an MN-major operand), stride byte offset (between 8-row
-// groups of K), descriptor version 1, swizzle mode 128B.
-__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-// D[tmem] (+)= A (smem) x B (smem), issued by one thread
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// arrive on `bar` once every tcgen05 operation this thread issued has completed
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-// make this thread's generic-proxy shared-memory writes visible to the tensor core
-__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-// 16 columns of 16 lanes in two halves: threads 0..15 read lanes
-// base .. base + 15 at columns col .. col + 15, threads 16..31 the same
-// lanes at columns col + 16 .. col + 31 (one warp, converged; waits)
-__device__ __forceinline__ void tmem_ld16x2_16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16], 16;\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 template <int N>
 struct SsdSmem {
@@ -136,10 +85,7 @@ struct SsdSmem {
 constexpr uint32_t kColS = 0, kColG = 64, kColY = 128, kColCS = 192, kTmemColsSsd = 256;
 
 // instruction descriptor, kind::f16: f32 D, bf16 A and B, M x 64
-__host__ __device__ constexpr uint32_t ssd_idesc(int m, bool a_mn, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((64u >> 3) << 17) |
-         ((uint32_t)(m >> 4) << 24);
-}
+__host__ __device__ constexpr uint32_t ssd_idesc(int m, bool a_mn, bool b_mn) { return umma_idesc_bf16(m, 64, a_mn, b_mn); }
 
 template <int N, bool kStateOnly>
 __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_constant__ SsdParams P) {
@@ -227,6 +173,17 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   auto put8 = [&](uint32_t off, int r, int c8, const float* v) {
     *reinterpret_cast<uint4*>(smem + off + swz(r, c8)) =
         make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
+  };
+  // this thread's 32 values of the state entering chunk c (row srow, columns
+  // sc .. sc + 31) to the saved chunk states, as bf16 (the readout's copy)
+  const int nch_all = (P.L + kQ - 1) / kQ;
+  auto save_state = [&](int c, const float* v) {
+    if (!P.chunk_states || kStateOnly || !has_srow) return;
+    uint4* dst = reinterpret_cast<uint4*>(P.chunk_states + ((((size_t)b * P.H + h) * nch_all + c) * N + srow) * kP + sc);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      dst[q] = make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                          pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
   };
 
   // The decay warp reads each chunk's dt one chunk ahead (two steps per
@@ -321,6 +278,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
     if (!kStateOnly && has_srow)
 #pragma unroll
       for (int q = 0; q < 4; ++q) put8(SM::kS, srow, 4 * kq + q, v + 8 * q);
+    save_state(c0, v);
     const float dec0 = vec[192];
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] *= dec0;
@@ -468,6 +426,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
         if (!kStateOnly && has_srow)
 #pragma unroll
           for (int q = 0; q < 4; ++q) put8(SM::kS, srow, 4 * kq + q, v + 8 * q);
+        save_state(c0 + ci + 1, v);
         const float dec1 = vec[(s ^ 1) * kVecSet + 192];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= dec1;
@@ -558,6 +517,7 @@ cudaError_t launch_ssd_fwd(const SsdArgs& a, cudaStream_t stream) {
   P.h0 = a.h0;
   P.y = static_cast<__nv_bfloat16*>(a.y);
   P.h_last = a.h_last;
+  P.chunk_states = static_cast<__nv_bfloat16*>(a.chunk_states);
   P.status = a.status;
   P.dt_min = a.dt_min;
   P.dt_max = a.dt_max;

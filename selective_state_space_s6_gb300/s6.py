@@ -93,6 +93,12 @@ def load_library():
         lib.ssm_step_ex.restype = ci
         lib.ssm_ssd_fwd.argtypes = [i64] * 6 + [ci] + [vp] * 10 + [op, vp]
         lib.ssm_ssd_fwd.restype = ci
+        lib.ssm_ssd_fwd_save.argtypes = [i64] * 6 + [ci] + [vp] * 11 + [op, vp]
+        lib.ssm_ssd_fwd_save.restype = ci
+        lib.ssm_ssd_bwd_workspace_bytes.argtypes = [i64] * 6 + [ci]
+        lib.ssm_ssd_bwd_workspace_bytes.restype = i64
+        lib.ssm_ssd_bwd.argtypes = [i64] * 6 + [ci] + [vp] * 19 + [sz, op, vp]
+        lib.ssm_ssd_bwd.restype = ci
         lib.ssm_conv1d_fwd.argtypes = [i64] * 4 + [ci] + [vp] * 6 + [vp]
         lib.ssm_conv1d_fwd.restype = ci
         lib.ssm_conv1d_bwd_workspace_bytes.argtypes = [i64] * 4 + [ci]
@@ -382,19 +388,67 @@ def conv1d_path(x, w, dout=None, y=None):
     return CONV_PATHS[rc]
 
 
+SSD_CHUNK_LEN = 64
+
+
 def ssd_fwd(x, dt_raw, dt_bias, A_log, Bm, Cm, Dp, h0=None, *, y=None, h_last=None, want_h_last=True,
-            dt_limit=None, stream=None):
+            dt_limit=None, stream=None, save=False, chunk_states=None):
     """Mamba-2 SSD forward.  x [B,L,H,P], dt_raw [B,L,H], Bm/Cm [B,L,G,N] (bf16);
     dt_bias, A_log, Dp [H] f32; h0 [B,H,N,P] f32 (zeros when None).  Returns
-    ``(y [B,L,H,P], h_last [B,H,N,P] or None)``."""
+    ``(y [B,L,H,P], h_last [B,H,N,P] or None)``, and with ``save`` also the
+    chunk states ``[B,H,ceil(L/64),N,P]`` (bf16) that ssd_bwd reads."""
     B, L, H, P = x.shape
     G, N = Bm.shape[2], Bm.shape[3]
     if y is None:
         y = torch.empty_like(x)
     if h_last is None and want_h_last:
         h_last = torch.empty((B, H, N, P), dtype=torch.float32, device=x.device)
-    rc = load_library().ssm_ssd_fwd(B, L, H, P, G, N, _act(x), _p(x), _p(dt_raw), _p(dt_bias), _p(A_log), _p(Bm),
-                                    _p(Cm), _p(Dp), _p(h0), _p(y), _p(h_last),
-                                    _opts(dt_limit) if dt_limit is not None else None, _stream(stream))
-    _check("ssm_ssd_fwd", rc)
-    return y, h_last
+    opts = _opts(dt_limit) if dt_limit is not None else None
+    if not save:
+        rc = load_library().ssm_ssd_fwd(B, L, H, P, G, N, _act(x), _p(x), _p(dt_raw), _p(dt_bias), _p(A_log),
+                                        _p(Bm), _p(Cm), _p(Dp), _p(h0), _p(y), _p(h_last), opts, _stream(stream))
+        _check("ssm_ssd_fwd", rc)
+        return y, h_last
+    nch = -(-L // SSD_CHUNK_LEN)
+    if chunk_states is None:
+        chunk_states = torch.empty((B, H, nch, N, P), dtype=torch.bfloat16, device=x.device)
+    rc = load_library().ssm_ssd_fwd_save(B, L, H, P, G, N, _act(x), _p(x), _p(dt_raw), _p(dt_bias), _p(A_log),
+                                         _p(Bm), _p(Cm), _p(Dp), _p(h0), _p(y), _p(h_last), _p(chunk_states),
+                                         opts, _stream(stream))
+    _check("ssm_ssd_fwd_save", rc)
+    return y, h_last, chunk_states
+
+
+def ssd_bwd_workspace_bytes(B, L, H, P, G, N, act=None) -> int:
+    return int(load_library().ssm_ssd_bwd_workspace_bytes(B, L, H, P, G, N, SSM_BF16 if act is None else act))
+
+
+def ssd_bwd(x, dt_raw, dt_bias, A_log, Bm, Cm, Dp, chunk_states, dy, dh_last=None, *, want_dh0=True,
+            dt_limit=None, ws=None, grads=None, stream=None):
+    """Mamba-2 SSD backward of ``sum(dy*y) + sum(dh_last*h_last)``.  Returns a
+    dict: dx [B,L,H,P], ddt_raw [B,L,H], dBm/dCm [B,L,G,N] (bf16), ddt_bias,
+    dA_log, dDp [H] (f32), dh0 [B,H,N,P] f32 (None unless ``want_dh0``)."""
+    B, L, H, P = x.shape
+    G, N = Bm.shape[2], Bm.shape[3]
+    dev = x.device
+    g = dict(grads or {})
+    g.setdefault("dx", torch.empty_like(x))
+    g.setdefault("ddt_raw", torch.empty_like(dt_raw))
+    g.setdefault("dBm", torch.empty_like(Bm))
+    g.setdefault("dCm", torch.empty_like(Cm))
+    g.setdefault("ddt_bias", torch.empty((H,), dtype=torch.float32, device=dev))
+    g.setdefault("dA_log", torch.empty((H,), dtype=torch.float32, device=dev))
+    g.setdefault("dDp", torch.empty((H,), dtype=torch.float32, device=dev))
+    g.setdefault("dh0", torch.empty((B, H, N, P), dtype=torch.float32, device=dev) if want_dh0 else None)
+    need = ssd_bwd_workspace_bytes(B, L, H, P, G, N, _act(x))
+    if need < 0:
+        raise SSMError("ssm_ssd_bwd_workspace_bytes", "SSM_ERR_UNSUPPORTED", f"shape {(B, L, H, P, G, N)}")
+    ws, ws_bytes = _workspace(need, dev, ws)
+    opts = _opts(dt_limit) if dt_limit is not None else None
+    rc = load_library().ssm_ssd_bwd(B, L, H, P, G, N, _act(x), _p(x), _p(dt_raw), _p(dt_bias), _p(A_log), _p(Bm),
+                                    _p(Cm), _p(Dp), _p(chunk_states), _p(dy), _p(dh_last), _p(g["dx"]),
+                                    _p(g["ddt_raw"]), _p(g["ddt_bias"]), _p(g["dA_log"]), _p(g["dBm"]),
+                                    _p(g["dCm"]), _p(g["dDp"]), _p(g["dh0"]), _p(ws), ws_bytes, opts,
+                                    _stream(stream))
+    _check("ssm_ssd_bwd", rc)
+    return g

@@ -165,3 +165,26 @@ def test_segment_plan(lib):
     assert s6.plan_segments(1, 1000, 64, 16, f32)[0] == 1
     with pytest.raises(s6.SSMError):
         s6.plan_segments(1, 10, 16, 32, f32)  # dstate above 16
+
+
+def test_ssd_bwd_validation(lib):
+    """Host-side checks of ssm_ssd_bwd and its workspace query: unsupported
+    shapes, misaligned tensors, a missing or short workspace -- before any
+    launch."""
+    assert lib.ssm_ssd_bwd_workspace_bytes(1, 8, 2, 64, 1, 16, 1) == -1   # dstate 16: not supported
+    assert lib.ssm_ssd_bwd_workspace_bytes(1, 8, 3, 64, 2, 64, 1) == -1   # heads not a multiple of groups
+    need = lib.ssm_ssd_bwd_workspace_bytes(2, 100, 4, 64, 2, 128, 1)
+    assert need >= 2 * 2 * 100 * 4 * 128 * 4 and need % 256 == 0
+    args = [FAKE] * 19  # x .. dh0, ws
+
+    def call(B=2, L=100, H=4, P=64, G=2, N=128, act=1, a=None, ws_bytes=None):
+        return lib.ssm_ssd_bwd(B, L, H, P, G, N, act, *(a or args), need if ws_bytes is None else ws_bytes, None, None)
+    assert call(N=32) == 2 and b"dstate 64 or 128" in lib.ssm_last_error()
+    assert call(act=0) == 2
+    bad = list(args)
+    bad[8] = ctypes.c_void_p(0x10008)            # dy only 8-byte aligned
+    assert call(a=bad) == 1 and b"dy is not 16-byte aligned" in lib.ssm_last_error()
+    bad = list(args)
+    bad[7] = None                                # chunk_states missing
+    assert call(a=bad) == 1 and b"chunk_states must not be NULL" in lib.ssm_last_error()
+    assert call(ws_bytes=need - 256) == 3        # SSM_ERR_WORKSPACE
