@@ -232,42 +232,82 @@ def ssd_algorithmic(w):
     return nbytes, flops
 
 
+def ssd_bwd_algorithmic(w):
+    """Algorithmic bytes and tensor flops of one SSD backward: x, dy, dt, Bm,
+    Cm and the saved chunk states (bf16, one per 64 steps) read, dx, ddt_raw,
+    dBm, dCm written once; per 64-step chunk the ten products G = C B^T,
+    Z = dy x^T, dx's (L o G)^T dy, dB's (L o Z)^T C and dC's (L o Z) B
+    (2 Q^2 N or 2 Q^2 P each) and C S_in, B dS, the state-gradient update,
+    x'' dS^T, dy' S_in^T (2 Q N P each)."""
+    B, L, H, P, G, N = w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate
+    e = 2 if w.act == "bf16" else 4
+    nch = -(-L // 64)
+    nbytes = 3 * B * L * H * P * e + 4 * B * L * G * N * e + 2 * B * L * H * e + B * H * nch * N * P * 2
+    flops = B * L * H * (2 * 64 * (3 * N + 2 * P) + 10 * N * P)
+    return nbytes, flops
+
+
 def time_ssd(dev, reps=10):
-    """The Mamba-2 SSD forward on the 1.3B block's shape, CUDA events over
-    `reps` calls (inputs larger than L2)."""
+    """The Mamba-2 SSD forward (plain and with state saves) and backward on the
+    1.3B block's shape, CUDA events over `reps` calls each (inputs larger than
+    L2)."""
     from selective_state_space_s6_gb300 import s6
 
     w = inputs.SSD_WORKLOADS["mamba2_1p3b"]
     x = inputs.make_ssd_inputs(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.act, seed=0)
     xd = {k: (v.to(dev) if v is not None else None) for k, v in x.items()}
+    gen = torch.Generator(device=dev).manual_seed(1)
+    dy = torch.randn(xd["x"].shape, device=dev, generator=gen).to(torch.bfloat16)
     keys = ("x", "dt_raw", "dt_bias", "A_log", "Bm", "Cm", "Dp")
     y = torch.empty_like(xd["x"])
     hl = torch.empty((w.batch, w.nheads, w.dstate, w.headdim), dtype=torch.float32, device=dev)
+    _, _, cs = s6.ssd_fwd(*[xd[k] for k in keys], None, save=True)
+    grads = s6.ssd_bwd(*[xd[k] for k in keys], cs, dy, None, want_dh0=False)
+    ws = torch.empty((s6.ssd_bwd_workspace_bytes(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate)
+                      + 256,), dtype=torch.uint8, device=dev)
 
-    def run():
+    def fwd():
         s6.ssd_fwd(*[xd[k] for k in keys], None, y=y, h_last=hl)
 
-    for _ in range(3):
-        run()
-    torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
-        run()
-    e1.record()
-    torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1) / reps
-    nbytes, flops = ssd_algorithmic(w)
+    def fwd_save():
+        s6.ssd_fwd(*[xd[k] for k in keys], None, y=y, h_last=hl, save=True, chunk_states=cs)
+
+    def bwd():
+        s6.ssd_bwd(*[xd[k] for k in keys], cs, dy, None, want_dh0=False, ws=ws, grads=grads)
+
+    def timed(run):
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            run()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / reps
+
     peak, _ = load_peaks()
     tpeak = load_peaks("bf16_tflops")[0]
-    gbs = nbytes / (ms * 1e-3) / 1e9
-    tfl = flops / (ms * 1e-3) / 1e12
-    return {"workload": w.description, "ms": round(ms, 4), "gcells_s": round(w.cells / (ms * 1e-3) / 1e9, 1),
-            "algorithmic_bytes": nbytes, "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),
-            "algorithmic_flops": flops, "tensor_tflops": round(tfl, 1), "tensor_frac": round(tfl / tpeak, 4),
-            "peaks": "measured hbm_gbs (copy) and bf16_tflops (cuBLAS, burst)",
-            "timing": f"CUDA events over {reps} calls"}
+
+    def line(ms, nbytes, flops):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        tfl = flops / (ms * 1e-3) / 1e12
+        return {"ms": round(ms, 4), "gcells_s": round(w.cells / (ms * 1e-3) / 1e9, 1), "algorithmic_bytes": nbytes,
+                "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4), "algorithmic_flops": flops,
+                "tensor_tflops": round(tfl, 1), "tensor_frac": round(tfl / tpeak, 4)}
+
+    fb, ff = ssd_algorithmic(w)
+    bb, bf = ssd_bwd_algorithmic(w)
+    res = line(timed(fwd), fb, ff)
+    res.update({"workload": w.description,
+                "fwd_save": line(timed(fwd_save), fb + w.batch * w.nheads * (-(-w.seqlen // 64)) * w.dstate
+                                 * w.headdim * 2, ff),
+                "bwd": line(timed(bwd), bb, bf),
+                "peaks": "measured hbm_gbs (copy) and bf16_tflops (cuBLAS, burst)",
+                "timing": f"CUDA events over {reps} calls each"})
+    return res
 
 
 # ------------------------------------------------------------------ clocks
@@ -763,8 +803,9 @@ def run_kernel(args):
     """One kernel family alone, a few calls on its own workload, for a
     profiler's capture (`--kernel`): the decode step (four calls, each after
     a 256 MB read that empties L2), conv1d + SiLU on the 1.4B block's shape
-    (three forward and three backward calls) or the SSD forward on the
-    Mamba-2-1.3B shape (three calls).  Prints one JSON line."""
+    (three forward and three backward calls), the SSD forward on the
+    Mamba-2-1.3B shape (three calls) or its backward (one saving forward,
+    three backward calls).  Prints one JSON line."""
     from selective_state_space_s6_gb300 import s6
 
     dev = torch.device("cuda", 0)
@@ -794,12 +835,19 @@ def run_kernel(args):
             s6.conv1d_bwd(x, wt, bias, None, dout, want_dstate0=False)
         res["workload"] = f"B={B} L={L} D={D} K={K} bf16"
         res["path"] = s6.conv1d_path(x, wt)
-    elif args.kernel == "ssd":
+    elif args.kernel in ("ssd", "ssd_bwd"):
         w = inputs.SSD_WORKLOADS["mamba2_1p3b"]
         x = inputs.make_ssd_inputs(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.act, seed=0)
         xd = {k: (v.to(dev) if v is not None else None) for k, v in x.items()}
-        for _ in range(3):
-            s6.ssd_fwd(*[xd[k] for k in ("x", "dt_raw", "dt_bias", "A_log", "Bm", "Cm", "Dp")], None)
+        keys = ("x", "dt_raw", "dt_bias", "A_log", "Bm", "Cm", "Dp")
+        if args.kernel == "ssd":
+            for _ in range(3):
+                s6.ssd_fwd(*[xd[k] for k in keys], None)
+        else:
+            dy = torch.randn(xd["x"].shape, device=dev).to(torch.bfloat16)
+            _, _, cs = s6.ssd_fwd(*[xd[k] for k in keys], None, save=True)
+            for _ in range(3):
+                s6.ssd_bwd(*[xd[k] for k in keys], cs, dy, None, want_dh0=False)
         res["workload"] = w.description
     torch.cuda.synchronize(dev)
     s6.check_device_status()
@@ -816,7 +864,7 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-step", action="store_true", help="skip the decode-step, conv1d and SSD measurements")
-    ap.add_argument("--kernel", choices=["step", "conv1d", "ssd"],
+    ap.add_argument("--kernel", choices=["step", "conv1d", "ssd", "ssd_bwd"],
                     help="run only this kernel family a few times (for a profiler) and exit")
     args = ap.parse_args(argv)
     if args.kernel:
