@@ -178,7 +178,7 @@ FwdWorkspace fwd_ws_layout(int64_t B, int64_t L, int64_t D, int64_t N, int act) 
 
 struct BwdWorkspace {
   s6::BwdPlan plan;
-  int nseg;
+  int nseg, nslot;
   int64_t hdr_off, dbc_off, dbc_bytes, param_off, param_bytes, agg_off, carry_off, flag_off, total;
 };
 
@@ -196,8 +196,10 @@ BwdWorkspace bwd_ws_layout(int64_t B, int64_t L, int64_t D, int64_t N) {
   w.param_off = align_up(w.dbc_off + w.dbc_bytes, 256);
   w.param_bytes = B * w.nseg * D * (N + 2) * (int64_t)sizeof(float);
   w.agg_off = align_up(w.param_off + w.param_bytes, 256);
+  w.nslot = w.nseg > 1 ? s6::agg_slots(w.plan) : 0;
   const int64_t cells = w.nseg > 1 ? B * w.nseg * D * N : 0;
-  w.carry_off = align_up(w.agg_off + cells * 2 * (int64_t)sizeof(float), 256);
+  const int64_t agg_cells = B * (int64_t)w.nslot * D * N;
+  w.carry_off = align_up(w.agg_off + agg_cells * 2 * (int64_t)sizeof(float), 256);
   // one hand-over flag per (batch, channel tile) sequence
   const int64_t nseq = w.nseg > 1 ? B * (int64_t)w.plan.ndt : 0;
   w.flag_off = align_up(w.carry_off + cells * (int64_t)sizeof(float), 256);
@@ -478,6 +480,7 @@ int ssm_scan_bwd_partials_ex(int64_t batch, int64_t seqlen, int64_t dim, int64_t
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   p.plan = w.plan;
   p.nseg = w.nseg;
+  p.nslot = w.nslot;
   p.seg_agg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.agg_off);
   p.seg_carry = reinterpret_cast<float*>(static_cast<char*>(ws) + w.carry_off);
   p.seq_flag = w.nseg > 1 ? reinterpret_cast<int*>(static_cast<char*>(ws) + w.flag_off) : nullptr;

@@ -423,20 +423,23 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
 #pragma unroll
     for (int i = 0; i < 12; ++i) tot[i * kLanes] = cmp[i * kLanes] = 0.f;
     const size_t bd_off = (size_t)b * L * D + dA;  // outputs of (b, t = 0, pair)
+    float4 nxt[2];
+    auto load_state = [&](int cs_c, float4 (&dst)[2]) {
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc)
+        dst[cc] = dvalid ? __ldg(reinterpret_cast<const float4*>(
+                               p.chunk_states + (((size_t)b * nchunks + cs_c) * D + dc + cc) * N + 4 * q))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
     for (int c = c_hi - 1; c >= c_lo; --c) {
       const int t0 = c * kChunk;
       const int cnt = chunk_len(c);
       const int nsc = (cnt + kSC - 1) / kSC;
-      // the chunk's saved start state (zeros for channels past D)
-      float2 h[2][2];
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const float4 cs = dvalid ? __ldg(reinterpret_cast<const float4*>(
-                                       p.chunk_states + (((size_t)b * nchunks + c) * D + dc + cc) * N + 4 * q))
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-        h[cc][0] = make_float2(cs.x, cs.y);
-        h[cc][1] = make_float2(cs.z, cs.w);
-      }
+      // the chunk's saved start state (zeros for channels past D), loaded
+      // during the previous chunk's pass B
+      if (c == c_hi - 1) load_state(c, nxt);
+      float2 h[2][2] = {{make_float2(nxt[0].x, nxt[0].y), make_float2(nxt[0].z, nxt[0].w)},
+                        {make_float2(nxt[1].x, nxt[1].y), make_float2(nxt[1].z, nxt[1].w)}};
       if (!failed) failed = !mbar_wait(&full[s], par, p.status);
       if (kBf16 && !failed) failed = !mbar_wait(&conv[s], par, p.status);
       __syncwarp();
@@ -501,6 +504,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
       }
 
       // ---------- pass B
+      if (c > c_lo) load_state(c - 1, nxt);  // the next chunk's start state, in flight during pass B
       float2 accA[2][2] = {{make_float2(0.f, 0.f), make_float2(0.f, 0.f)}, {make_float2(0.f, 0.f), make_float2(0.f, 0.f)}};
       float2 accD = make_float2(0.f, 0.f), accBias = make_float2(0.f, 0.f);
       // hk: the state after the step being walked -- pass A's final state for
@@ -747,11 +751,12 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
 }
 
 // ---------------------------------------------------------------- segment aggregates
-// Aggregate pass of the backward's chunked parallel scan.  For segment s >= 1
-// (grid.z + 1), from a zero carry, run the adjoint recurrence
+// Aggregate pass of the backward's chunked parallel scan.  For the sub-piece
+// in slot grid.z (at most kAggSub chunks of a later piece), from a zero
+// carry, run the adjoint recurrence
 //   g_t = dy_t * C_t + carry,  carry = Abar_t * g_t
-// from the segment's last step down to its first, and store per state the
-// segment's decay product exp(A * sum(delta)) and the final carry.  Same warp
+// from the sub-piece's last step down to its first, and store per state its
+// decay product exp(A * sum(delta)) and the final carry.  Same warp
 // roles and lane layout as the forward (TPC lanes per channel, 4 states each);
 // tiles are streamed last first.
 // one aggregate-pass stage: delta_raw, z, dout tiles [kTT][128/TPC] and a Cm
@@ -794,12 +799,11 @@ __global__ void __launch_bounds__(kAggWarps * 32) s6_bwd_agg_kernel(const __grid
   // 64, whose lanes only load); piece seg >= 1 of the sequence (b, tile), if
   // it has one
   constexpr int kValid = kCh < kDTile ? kCh : kDTile;
-  const int b = blockIdx.y, d0 = blockIdx.x * kValid, seg = blockIdx.z + 1;
+  const int b = blockIdx.y, d0 = blockIdx.x * kValid, seg = blockIdx.z;  // seg: the aggregate slot
   const int L = p.L, D = p.D;
   const long long sq = (long long)b * p.plan.ndt + d0 / kBwdTile;
-  if (seg >= plan_pieces(p.plan, sq)) return;  // the whole CTA, before any barrier or copy
-  int c_lo, c_hi;
-  plan_piece_range(p.plan, sq, seg, c_lo, c_hi);
+  int piece, c_lo, c_hi;
+  if (!agg_slot(p.plan, sq, seg, piece, c_lo, c_hi)) return;  // the whole CTA, before any barrier or copy
   const int t_lo = c_lo * kChunk, t_hi = min(L, c_hi * kChunk);
   const int ntiles = (t_hi - t_lo + kTT - 1) / kTT;
 
@@ -928,7 +932,7 @@ __global__ void __launch_bounds__(kAggWarps * 32) s6_bwd_agg_kernel(const __grid
     if (lane == 0) mbar_arrive(&empty[s]);
   }
   if (dvalid) {
-    float* ag = p.seg_agg + ((((size_t)b * p.nseg + seg) * D + d) * N + 4 * q) * 2;
+    float* ag = p.seg_agg + ((((size_t)b * p.nslot + seg) * D + d) * N + 4 * q) * 2;
     const float2 x0 = fmul2(make_float2(dsum, dsum), A2[0]);
     const float2 x1 = fmul2(make_float2(dsum, dsum), A2[1]);
     const float P0 = kFast ? ex2_approx(x0.x) : expf(x0.x), P1 = kFast ? ex2_approx(x0.y) : expf(x0.y);
@@ -950,12 +954,18 @@ __global__ void s6_bwd_seg_carry_kernel(const BwdParams p) {
   if (e >= per) return;
   const int d = (int)(e / p.N), n = (int)(e % p.N);
   const int K = plan_pieces(p.plan, (long long)b * p.plan.ndt + d / kBwdTile);
+  const long long sq = (long long)b * p.plan.ndt + d / kBwdTile;
   float chi = p.dh_last ? p.dh_last[(size_t)b * per + e] : 0.f;
   for (int k = K - 1; k >= 0; --k) {
     p.seg_carry[((size_t)b * p.nseg + k) * per + e] = chi;
     if (k > 0) {
-      const float* ag = p.seg_agg + (((size_t)b * p.nseg + k) * per + e) * 2;
-      chi = fmaf(ag[0], chi, ag[1]);
+      // through piece k: its sub-pieces, last first
+      int z0, z1;
+      agg_piece_slots(p.plan, sq, k, z0, z1);
+      for (int z = z1; z >= z0; --z) {
+        const float* ag = p.seg_agg + (((size_t)b * p.nslot + z) * per + e) * 2;
+        chi = fmaf(ag[0], chi, ag[1]);
+      }
     }
   }
   for (int k = K; k < p.nseg; ++k) {
@@ -981,7 +991,7 @@ cudaError_t launch_agg(const BwdTmaParams& P, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   constexpr int kCh = kScanThreads / TPC;
   constexpr int kValid = kCh < kDTile ? kCh : kDTile;
-  const dim3 grid((P.p.D + kValid - 1) / kValid, P.p.B, P.p.nseg - 1);
+  const dim3 grid((P.p.D + kValid - 1) / kValid, P.p.B, P.p.nslot);
   kern<<<grid, kAggWarps * 32, smem, stream>>>(P);
   return cudaGetLastError();
 }

@@ -70,6 +70,36 @@ __host__ __device__ inline void plan_piece_range(const ScanPlan& pl, long long s
 using BwdPlan = ScanPlan;
 using FwdPlan = ScanPlan;
 
+// The backward's aggregate pass works on sub-pieces of at most kAggSub
+// chunks of the later pieces (k >= 1) of each sequence, so that its longest
+// sequential walk is kAggSub chunks; sub-piece (k, j) of a sequence has slot
+// floor(start chunk / kAggSub) + k, unique and increasing in time.
+constexpr int kAggSub = 8;
+__host__ __device__ inline int agg_slots(const ScanPlan& pl) { return (pl.nch + kAggSub - 1) / kAggSub + pl.maxp; }
+// slots [z0, z1] of piece k of sequence s
+__host__ __device__ inline void agg_piece_slots(const ScanPlan& pl, long long s, int k, int& z0, int& z1) {
+  int lo, hi;
+  plan_piece_range(pl, s, k, lo, hi);
+  z0 = lo / kAggSub + k;
+  z1 = (hi - 1) / kAggSub + k;
+}
+// the sub-piece in slot z of sequence s: piece k >= 1, chunks [cs, ce); false if none
+__host__ __device__ inline bool agg_slot(const ScanPlan& pl, long long s, int z, int& k, int& cs, int& ce) {
+  const int K = plan_pieces(pl, s);
+  for (int kk = 1; kk < K; ++kk) {
+    int lo, hi;
+    plan_piece_range(pl, s, kk, lo, hi);
+    const int z0 = lo / kAggSub + kk, z1 = (hi - 1) / kAggSub + kk;
+    if (z >= z0 && z <= z1) {
+      k = kk;
+      cs = lo > (z - kk) * kAggSub ? lo : (z - kk) * kAggSub;
+      ce = hi < (z - kk + 1) * kAggSub ? hi : (z - kk + 1) * kAggSub;
+      return cs < ce;
+    }
+  }
+  return false;
+}
+
 struct FwdParams {
   const void* u;
   const void* delta_raw;
@@ -125,11 +155,12 @@ struct BwdParams {
   unsigned int* status;  // device status word (bounded waits report here)
   float dt_min, dt_max;   // limit on delta = softplus(s); 0 and +inf: none
   // Pieces (chunked parallel scan): nseg = plan.maxp rows per batch;
-  // seg_agg [B][nseg][D][N][2] holds each piece's decay product and
-  // zero-carry adjoint carry-out, seg_carry [B][nseg][D][N] the adjoint carry
-  // entering each piece's last step.  The generic kernel uses row 0 only.
+  // seg_agg [B][nslot][D][N][2] holds each aggregate sub-piece's decay
+  // product and zero-carry adjoint carry-out (slots: agg_slot), seg_carry
+  // [B][nseg][D][N] the adjoint carry entering each piece's last step.  The
+  // generic kernel uses row 0 only.
   BwdPlan plan;
-  int nseg;
+  int nseg, nslot;
   float* seg_agg;
   float* seg_carry;
   // Hand-over mode (cooperative launch, every sequence in at most two
