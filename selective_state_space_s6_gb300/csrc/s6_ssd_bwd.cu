@@ -128,13 +128,20 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
   const float A = -expf(P.A_log[h]);
   const float bias = P.dt_bias[h];
   const float Dh = P.Dp[h];
-  constexpr int kTidMma = 0, kTidTma = 192, kWarpDecay = 7;
+  // Roles beside the row work: threads 0, 32 and 64 issue the tensor-core
+  // products (three issuers in three warps, each accumulator written by one
+  // of them; both groups complete when all three have committed); thread 192
+  // issues the TMA copies; warp 7 computes the decays a chunk ahead; warps 4
+  // and 5 form the log-decay gradient while the second group runs.
+  constexpr int kTidMma = 0, kTidTma = 192, kWarpDecay = 7, kIssuers = 3, kTidDcum = 128;
+  const bool issuer = tid < 32 * kIssuers && lane == 0;
+  const int iss = tid >> 5;  // which issuer
 
   if (tid == kTidMma) {
     mbar_init(&full[0], 1);
     mbar_init(&full[1], 1);
-    mbar_init(bar1, 1);
-    mbar_init(bar2, 1);
+    mbar_init(bar1, kIssuers);
+    mbar_init(bar2, kIssuers);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
@@ -188,8 +195,19 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
     }
   };
 
-  // decays of chunk c into set (ci & 1) (warp kWarpDecay; two steps per lane)
+  // decays of chunk c into set (ci & 1) (warp kWarpDecay; two steps per
+  // lane).  The dt of a chunk are read one chunk ahead and kept as raw bits
+  // until used, so that the load's latency hides behind a whole chunk.
   const unsigned short* dt_bits = reinterpret_cast<const unsigned short*>(P.dt_raw);
+  unsigned short raw_next[2] = {0, 0};
+  auto load_dt = [&](int ci) {
+    const int c = nch - 1 - ci;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int tc = min(c * kQ + 2 * lane + i, P.L - 1);  // past the end: any valid step, masked later
+      raw_next[i] = dt_bits[((size_t)b * P.L + tc) * P.H + h];
+    }
+  };
   auto chunk_decays = [&](int ci) {
     const int c = nch - 1 - ci;
     float* v = vec + (ci & 1) * kVecSet;
@@ -197,8 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int t = c * kQ + 2 * lane + i;
-      const int tc = min(t, P.L - 1);
-      const float r = __bfloat162float(__ushort_as_bfloat16(dt_bits[((size_t)b * P.L + tc) * P.H + h]));
+      const float r = __bfloat162float(__ushort_as_bfloat16(raw_next[i]));
       const float sarg = r + bias;
       const float sp = softplus_fast(sarg);
       const float d = t < P.L ? clamp_dt(sp, P.dt_min, P.dt_max) : 0.f;
@@ -228,7 +245,11 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
     }
     if (lane == 0) v[384] = fast_exp(end);
   };
-  if (warp == kWarpDecay) chunk_decays(0);
+  if (warp == kWarpDecay) {
+    load_dt(0);
+    chunk_decays(0);
+    if (nch > 1) load_dt(1);
+  }
 
   // operand descriptors (see the forward): K-major boxes/images with 32-byte
   // K steps, MN-major ones with 16-row (2048-byte) K steps
@@ -259,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
     tmem_st32(tquarter + kColS + (uint32_t)sc, v);
     tmem_wait_st();
   }
-  float accA = 0.f, accD = 0.f, accB = 0.f;  // this CTA's dA, dDp, ddt_bias (thread 0)
+  float accA = 0.f, accD = 0.f, accB = 0.f;  // this CTA's dA, dDp, ddt_bias (thread kTidDcum)
   bool ok = true;  // uniform over the CTA
 
   for (int ci = 0; ci < nch; ++ci) {
@@ -325,27 +346,44 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
     tmem_fence_before_sync();
     __syncthreads();
 
-    // ---- 2: G = C B^T, Z = dy x^T, CS = C S_in, X = B dS, dS += C^T dy'
-    if (tid == kTidMma) {
+    // ---- 2: G = C B^T and Z = dy x^T (issuer 0), CS = C S_in and the update
+    // dS += C^T dy' (issuer 1), X = B dS (issuer 2)
+    if (issuer) {
       tmem_fence_after_sync();
       const uint64_t dCk = kmaj(stb[s] + SM::kCo), dBk = kmaj(stb[s] + SM::kBo), dCmn = mnmaj(stb[s] + SM::kCo);
       const uint64_t dDYk = kmaj(stb[s] + SM::kDY), dXk = kmaj(stb[s] + SM::kX), dSmn = mnmaj(stb[s] + SM::kSo);
+      if (iss == 0) {
 #pragma unroll
-      for (int k = 0; k < N / 16; ++k) {  // K = n
-        const uint64_t ko = (uint64_t)(((k / 4) * kTileBytes + (k % 4) * 32) >> 4);
-        umma_f16(tmem + kColG, dCk + ko, dBk + ko, kId64kk, k > 0 ? 1u : 0u);
-        umma_f16(tmem + kColCS, dCk + ko, dSmn + (uint64_t)(k * 128), kId64km, k > 0 ? 1u : 0u);
-        umma_f16(tmem + kColX, dBk + ko, dDSmn + (uint64_t)(k * 128), kId64km, k > 0 ? 1u : 0u);
-      }
+        for (int k = 0; k < N / 16; ++k) {  // K = n
+          const uint64_t ko = (uint64_t)(((k / 4) * kTileBytes + (k % 4) * 32) >> 4);
+          umma_f16(tmem + kColG, dCk + ko, dBk + ko, kId64kk, k > 0 ? 1u : 0u);
+        }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {  // K = p (Z), K = t (the update)
-        umma_f16(tmem + kColZ, dDYk + (uint64_t)(2 * k), dXk + (uint64_t)(2 * k), kId64kk, k > 0 ? 1u : 0u);
-        umma_f16(tmem + kColS, dCmn + (uint64_t)(k * 128), dDYemn + (uint64_t)(k * 128), kIdNmm, 1u);
+        for (int k = 0; k < 4; ++k)  // K = p
+          umma_f16(tmem + kColZ, dDYk + (uint64_t)(2 * k), dXk + (uint64_t)(2 * k), kId64kk, k > 0 ? 1u : 0u);
+      } else if (iss == 1) {
+#pragma unroll
+        for (int k = 0; k < N / 16; ++k) {
+          const uint64_t ko = (uint64_t)(((k / 4) * kTileBytes + (k % 4) * 32) >> 4);
+          umma_f16(tmem + kColCS, dCk + ko, dSmn + (uint64_t)(k * 128), kId64km, k > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // K = t
+          umma_f16(tmem + kColS, dCmn + (uint64_t)(k * 128), dDYemn + (uint64_t)(k * 128), kIdNmm, 1u);
+      } else {
+#pragma unroll
+        for (int k = 0; k < N / 16; ++k) {
+          const uint64_t ko = (uint64_t)(((k / 4) * kTileBytes + (k % 4) * 32) >> 4);
+          umma_f16(tmem + kColX, dBk + ko, dDSmn + (uint64_t)(k * 128), kId64km, k > 0 ? 1u : 0u);
+        }
       }
       umma_commit(bar1);
     }
-    // the next chunk's decays (its dt read now; this chunk's set stays intact)
-    if (warp == kWarpDecay && ci + 1 < nch) chunk_decays(ci + 1);
+    // the next chunk's decays (its dt read a chunk ago), its successor's dt in flight
+    if (warp == kWarpDecay && ci + 1 < nch) {
+      chunk_decays(ci + 1);
+      if (ci + 2 < nch) load_dt(ci + 2);
+    }
     mbar_wait(bar1, ph, P.status);
     tmem_fence_after_sync();
 
@@ -420,26 +458,35 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
 
     // ---- 4: dx += (L o G o delta)^T dy; dB = (L o Z o delta)^T C + x'' dS^T;
     // dC = dy' S_in^T + (L o Z o delta) B
-    if (tid == kTidMma) {
+    // (dB on issuer 0, dC on issuer 1, dx on issuer 2)
+    if (issuer) {
       tmem_fence_after_sync();
       const uint64_t dDYmn = mnmaj(stb[s] + SM::kDY), dCmn = mnmaj(stb[s] + SM::kCo), dBmn = mnmaj(stb[s] + SM::kBo);
       const uint64_t dSk = kmaj(stb[s] + SM::kSo);
+      if (iss == 0) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {  // K = t (or s), 16 rows per step
-        umma_f16(tmem + kColX, dGlmn + (uint64_t)(k * 128), dDYmn + (uint64_t)(k * 128), kId64mm, 1u);
-        umma_f16(tmem + kColB, dZlmn + (uint64_t)(k * 128), dCmn + (uint64_t)(k * 128), kIdBmm, k > 0 ? 1u : 0u);
-        umma_f16(tmem + kColC, dDYek + (uint64_t)(2 * k), dSk + (uint64_t)(2 * k), kIdBkk, k > 0 ? 1u : 0u);
-      }
+        for (int k = 0; k < 4; ++k)  // K = t
+          umma_f16(tmem + kColB, dZlmn + (uint64_t)(k * 128), dCmn + (uint64_t)(k * 128), kIdBmm, k > 0 ? 1u : 0u);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {  // K = p (dB), K = s (dC)
-        umma_f16(tmem + kColB, dXw + (uint64_t)(2 * k), dDSk + (uint64_t)(2 * k), kIdBkk, 1u);
-        umma_f16(tmem + kColC, dZlk + (uint64_t)(2 * k), dBmn + (uint64_t)(k * 128), kIdCkm, 1u);
+        for (int k = 0; k < 4; ++k)  // K = p
+          umma_f16(tmem + kColB, dXw + (uint64_t)(2 * k), dDSk + (uint64_t)(2 * k), kIdBkk, 1u);
+      } else if (iss == 1) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // K = p
+          umma_f16(tmem + kColC, dDYek + (uint64_t)(2 * k), dSk + (uint64_t)(2 * k), kIdBkk, k > 0 ? 1u : 0u);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // K = s
+          umma_f16(tmem + kColC, dZlk + (uint64_t)(2 * k), dBmn + (uint64_t)(k * 128), kIdCkm, 1u);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // K = t
+          umma_f16(tmem + kColX, dGlmn + (uint64_t)(k * 128), dDYmn + (uint64_t)(k * 128), kId64mm, 1u);
       }
       umma_commit(bar2);
     }
-    // the gradient of the log-decays, delta and A (threads 0..63: step t = tid)
-    if (tid < 64) {
-      const int t = tid;
+    // the gradient of the log-decays, delta and A (warps 4 and 5: step t = tid - 128)
+    if (tid >= kTidDcum && tid < kTidDcum + 64) {
+      const int t = tid - kTidDcum;
       float colD2 = 0.f;
       for (int r = t; r < 64; ++r) colD2 += d2[r * 65 + t];  // rows r >= t (L is 0 above the diagonal)
       const float* rp0 = rowp + (0 * 64 + t) * 4;
@@ -482,8 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
         vb += __shfl_xor_sync(0xffffffffu, vb, o);
       }
       if (lane == 0) {
-        red[32 + 2 * warp] = va;
-        red[33 + 2 * warp] = vb;
+        red[32 + 2 * (warp - kTidDcum / 32)] = va;
+        red[33 + 2 * (warp - kTidDcum / 32)] = vb;
       }
       named_bar_sync(3, 64);
       if (t == 0) {
@@ -546,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
 #pragma unroll
       for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
     }
-    if (tid == 0) {
+    if (tid == kTidDcum) {
       float* w3 = P.ws_sc + ((size_t)b * P.H + h) * 3;
       w3[0] = accA;
       w3[1] = accD;
