@@ -143,9 +143,16 @@ struct BwdLayout {
   // added by the reducer warp; f32 (less
   // shared memory) -- a warp-level xor reduce-scatter first, the warps' sums
   // ([2 slots][SC][kCW][32]) added by the reducer warp
+  // Within a pair's block the 16-byte slot j (= 2q + 0 for the dBm terms,
+  // 2q + 1 for the dCm terms) sits at j ^ red_swz(pair): consecutive pairs
+  // rotate through the banks, so that a warp's stores (8 pairs x 4 groups)
+  // and the reducer's loads (4 slices x 8 slots) both take the minimum of
+  // four wavefronts.
   static constexpr bool kRedSmem = kBf16;
   static constexpr int kRedPair = TPC * 8;  // floats per channel pair in a step's block
   static constexpr int kRedStep = 64 * kRedPair;
+  static constexpr int kRedQ = kRedPair / 4;  // 16-byte slots per pair
+  __device__ static __forceinline__ int red_swz(int pair) { return (pair / (8 / kRedQ)) % kRedQ; }
   static constexpr int kDsumB = kRedSmem ? 2 * kSC * kRedStep * 4 : 2 * kSC * kCW * 32 * 4;
   static constexpr int kTotB = 2 * 12 * kLanes * 4;              // [2 (sum, comp)][12][lanes] running totals
   static constexpr int kOffBcf = kBS * kStageB;
@@ -227,13 +234,18 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   auto tile_B = [&](int s) { return reinterpret_cast<Act*>(stage(s) + 4 * LY::kTileB); };
   auto tile_C = [&](int s) { return reinterpret_cast<Act*>(stage(s) + 4 * LY::kTileB + LY::kBCB); };
 
-  auto piece_at = [&](int u, int& b, int& d0, int& c_lo, int& c_hi, int& next) {
-    const int sq = u / pl.nch, S0 = sq * pl.nch;
-    next = min(S0 + pl.nch, u_end);
+  // the item (a piece of one sequence) that starts at unit u of this CTA's range
+  auto item_at = [&](int u, int& b, int& d0, int& c_lo, int& c_hi, int& next, int& sq, int& kp) {
+    long long sq_l, next_l;
+    plan_item(pl, u, u_end, sq_l, c_lo, c_hi, kp, next_l);
+    sq = (int)sq_l;
+    next = (int)next_l;
     b = sq / pl.ndt;
     d0 = (sq % pl.ndt) * kBwdTile;
-    c_lo = u - S0;
-    c_hi = next - S0;
+  };
+  auto piece_at = [&](int u, int& b, int& d0, int& c_lo, int& c_hi, int& next) {
+    int sq, kp;
+    item_at(u, b, d0, c_lo, c_hi, next, sq, kp);
   };
   auto chunk_len = [&](int c) { return min(kChunk, L - c * kChunk); };
 
@@ -328,11 +340,12 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
             const int og = lane % nG, sl = lane / nG;
             const int gq = og >> 1, qty = og & 1;
             for (int k = 0; k < cnt; ++k) {
-              const float* rp = src + k * LY::kRedStep + (sl * kCPL) * LY::kRedPair + 8 * gq + 4 * qty;
+              const float* rp = src + k * LY::kRedStep + (sl * kCPL) * LY::kRedPair;
               float2 a = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
 #pragma unroll
               for (int i = 0; i < kCPL; ++i) {
-                const float4 v = *reinterpret_cast<const float4*>(rp + i * LY::kRedPair);
+                const int j = (2 * gq + qty) ^ LY::red_swz(sl * kCPL + i);
+                const float4 v = *reinterpret_cast<const float4*>(rp + i * LY::kRedPair + 4 * j);
                 a = fadd2(a, make_float2(v.x, v.y));
                 b2 = fadd2(b2, make_float2(v.z, v.w));
               }
@@ -368,6 +381,8 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   // reduce-scatter of the 8 dBm/dCm values over the warp's pairs: output of this lane
   const int rs_o = ((lane >> 4) & 1) * N + 4 * q + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
   const bool rs_store = (lane & (3 & ~(TPC - 1))) == 0;
+  // this lane's dBm slot in a step's block of the reducer (its dCm slot: ^ 4)
+  const int red_off = cp * LY::kRedPair + 4 * ((2 * q) ^ LY::red_swz(cp));
   // swizzled byte offset of the pair's channels in the rows of the lane's
   // owned steps (it depends on the row % 8 only): owned step i of a 4-step
   // sub-chunk at an even / odd sub-chunk index
@@ -383,11 +398,9 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   uint32_t par = 0;  // its phase parity
   int nsub = 0;      // sub-chunks handed to the reducer so far
   for (int u = u_begin, next; u < u_end; u = next) {
-    int b, d0, c_lo, c_hi;
-    piece_at(u, b, d0, c_lo, c_hi, next);
-    const int kp = c_lo == 0 ? 0 : (int)(plan_count_le(pl, u) - plan_count_le(pl, u - c_lo));
+    int b, d0, c_lo, c_hi, sq, kp;
+    item_at(u, b, d0, c_lo, c_hi, next, sq, kp);
     const bool last_piece = c_hi == pl.nch;
-    const int sq = (u - c_lo) / pl.nch;
     const int dA = d0 + 2 * cp;  // first channel of the pair (D is even: both valid or neither)
     const bool dvalid = dA < D;
     const int dc = dvalid ? dA : D - 2;
@@ -593,9 +606,10 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
           part2[kk * LY::kRP2 + tid] = make_float2(apa[0].x + apa[0].y, apa[1].x + apa[1].y);
           if constexpr (LY::kRedSmem) {
             // this lane's 8 terms (summed over its 2 channels) for the reducer warp
-            float* rp = ds + kk * LY::kRedStep + cp * LY::kRedPair + 8 * q;
-            *reinterpret_cast<float4*>(rp) = make_float4(dB[0].x, dB[0].y, dB[1].x, dB[1].y);
-            *reinterpret_cast<float4*>(rp + 4) = make_float4(dC[0].x, dC[0].y, dC[1].x, dC[1].y);
+            float* rp = ds + kk * LY::kRedStep;
+            const int off_c = red_off ^ 4;
+            *reinterpret_cast<float4*>(rp + red_off) = make_float4(dB[0].x, dB[0].y, dB[1].x, dB[1].y);
+            *reinterpret_cast<float4*>(rp + off_c) = make_float4(dC[0].x, dC[0].y, dC[1].x, dC[1].y);
             return;
           }
           // channel sums over the warp's pairs: xor reduce-scatter, 8 values -> 1
@@ -1076,9 +1090,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 }  // namespace
 
-// The work plan: sms ranges of equal length over all chunk units (one
-// persistent CTA per SM, no tail wave); sequences cut by a range boundary
-// get aggregates for their later pieces.  N outside {4, 8, 16} never takes
+// The work plan: sms ranges of (near) equal length over all chunk units (one
+// persistent CTA per SM, no tail wave) -- contiguous, or split into heads and
+// tails when there are fewer sequences than CTAs; sequences cut by a range
+// boundary get aggregates for their later pieces.  N outside {4, 8, 16} never takes
 // the TMA path: one piece per sequence.
 BwdPlan bwd_plan(int B, int L, int D, int N, int sms) {
   BwdPlan pl;
@@ -1087,6 +1102,7 @@ BwdPlan bwd_plan(int B, int L, int D, int N, int sms) {
   pl.U = (long long)(B > 0 ? B : 0) * pl.ndt * pl.nch;
   pl.P = (int)std::max<long long>(1, std::min<long long>(std::max(sms, 1), pl.U));
   pl.maxp = 1;
+  pl.H = 0;
   pl.handover = false;
   if (pl.U == 0 || !(N == 4 || N == 8 || N == 16)) {
     pl.U = std::max<long long>(pl.U, 1);
@@ -1094,8 +1110,18 @@ BwdPlan bwd_plan(int B, int L, int D, int N, int sms) {
     return pl;
   }
   const long long nseq = (long long)B * pl.ndt;
+  if (nseq < pl.P) {
+    // fewer sequences than CTAs: every sequence is cut.  Split layout --
+    // heads of ceil(U / P) chunks, one per CTA, and short tails for the rest
+    // (one sequence per CTA when the head would be the whole sequence)
+    const long long H = (pl.U + pl.P - 1) / pl.P;
+    if (H >= pl.nch)
+      pl.P = (int)nseq;
+    else
+      pl.H = (int)H;
+  }
   for (long long sq = 0; sq < nseq; ++sq) pl.maxp = std::max(pl.maxp, plan_pieces(pl, sq));
-  pl.handover = pl.maxp == 2 && (long long)pl.nch <= pl.U / pl.P;
+  pl.handover = pl.H == 0 && pl.maxp == 2 && (long long)pl.nch <= pl.U / pl.P;
   return pl;
 }
 

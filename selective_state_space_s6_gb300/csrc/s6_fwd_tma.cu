@@ -538,6 +538,7 @@ FwdPlan fwd_stream_plan(int B, int L, int D, int N, int act, int sms) {
   FwdPlan pl;
   pl.handover = false;
   pl.maxp = 1;
+  pl.H = 0;  // contiguous layout
   pl.P = 1;
   pl.U = 1;
   pl.nch = L > 0 ? (L + kChunk - 1) / kChunk : 0;

@@ -24,47 +24,118 @@ constexpr unsigned int kStatusLayoutBit = 2u;       // same bit as kStatusLayout
 // ---------------------------------------------------------------- params
 
 // Work plan of a persistent scan: the (batch, channel tile) sequences, each
-// of nch chunks, are laid end to end as U = nseq * nch chunk units
-// (sequence s = b * ndt + j) and cut into P equal ranges, one per persistent
-// CTA (range w = [bound(w), bound(w + 1)), bound(w) = floor(w * U / P)).  A
-// range covers pieces of one or more sequences; a sequence cut by range
+// of nch chunks, are laid out as U = nseq * nch chunk units (sequence
+// s = b * ndt + j) and cut into P ranges, one per persistent CTA.  A range
+// covers pieces of one or more sequences; a sequence cut by range
 // boundaries has K > 1 pieces, numbered in time order.  The plan is a
-// function of the shape only.
-//   Backward (128-channel tiles, unit s * nch + c): piece k > 0 needs the
-//   adjoint carry of the pieces after it -- handed over between CTAs, or
-//   composed from piece aggregates (the chunked parallel scan); piece k of
-//   sequence (b, j) owns row b * maxp + k of the parameter partials.
-//   Forward (128/TPC-channel tiles, unit s * nch + (nch - 1 - c)): a range
-//   starts with a sequence's first piece and ends with another's last, whose
-//   start state the CTA holding the first piece hands over.
+// function of the shape only.  Two layouts:
+//   contiguous (H == 0): unit s * nch + c, P equal ranges
+//     (range w = [bound(w), bound(w + 1)), bound(w) = floor(w * U / P));
+//   split (H > 0, backward only, when there are fewer sequences than
+//     ranges): every sequence is a head of its first H chunks, which is
+//     range s by itself, and a tail of the other T = nch - H chunks; the
+//     tails, laid end to end after the heads (unit nseq * H + s * T + c - H),
+//     are cut into the other P - nseq ranges equally.  H = ceil(U / P), so
+//     no range is longer than in the contiguous layout, and the later pieces
+//     -- the ones the aggregate pass walks -- are as short as a cut of every
+//     sequence allows.
+//   Backward (128-channel tiles): piece k > 0 needs the adjoint carry of the
+//   pieces after it -- handed over between CTAs, or composed from piece
+//   aggregates (the chunked parallel scan); piece k of sequence (b, j) owns
+//   row b * maxp + k of the parameter partials.
+//   Forward (128/TPC-channel tiles, contiguous, unit s * nch + (nch - 1 - c)):
+//   a range starts with a sequence's first piece and ends with another's
+//   last, whose start state the CTA holding the first piece hands over.
 struct ScanPlan {
   long long U;  // chunk units
   int P;        // worker CTAs (ranges), 1 <= P <= U
   int nch;      // chunks per sequence
   int ndt;      // 64-channel tiles
   int maxp;     // most pieces any sequence has
+  int H;        // split layout: head chunks per sequence (0: contiguous layout)
   // carries handed from CTA to CTA (no aggregate pass): every sequence in at
   // most two pieces and no range shorter than a sequence
   bool handover;
 };
 
-__host__ __device__ inline long long plan_bound(const ScanPlan& pl, long long w) { return w * pl.U / pl.P; }
-// number of w in [0, P] with plan_bound(w) <= X, for 0 <= X < U
-__host__ __device__ inline long long plan_count_le(const ScanPlan& pl, long long X) {
-  return ((X + 1) * pl.P + pl.U - 1) / pl.U;
+// M units (sequences of len units end to end) cut into R equal ranges
+struct PlanCut {
+  long long M, R;
+  int len;
+};
+__host__ __device__ inline long long cut_bound(const PlanCut& c, long long w) { return w * c.M / c.R; }
+// number of w in [0, R] with cut_bound(w) <= X, for 0 <= X < M
+__host__ __device__ inline long long cut_count_le(const PlanCut& c, long long X) { return ((X + 1) * c.R + c.M - 1) / c.M; }
+__host__ __device__ inline int cut_pieces(const PlanCut& c, long long s) {
+  const long long S0 = s * c.len, S1 = S0 + c.len;
+  return (int)(cut_count_le(c, S1 - 1) - cut_count_le(c, S0)) + 1;
+}
+__host__ __device__ inline void cut_piece_range(const PlanCut& c, long long s, int k, int& lo, int& hi) {
+  const long long S0 = s * c.len;
+  const long long wa = cut_count_le(c, S0);  // first range boundary after the sequence start
+  const int K = cut_pieces(c, s);
+  lo = k == 0 ? 0 : (int)(cut_bound(c, wa + k - 1) - S0);
+  hi = k == K - 1 ? c.len : (int)(cut_bound(c, wa + k) - S0);
+}
+
+__host__ __device__ inline long long plan_nseq(const ScanPlan& pl) { return pl.nch > 0 ? pl.U / pl.nch : 0; }
+// the cut of the contiguous layout, or of the split layout's tails
+__host__ __device__ inline PlanCut plan_cut(const ScanPlan& pl) {
+  PlanCut c;
+  if (pl.H == 0) {
+    c.M = pl.U;
+    c.R = pl.P;
+    c.len = pl.nch;
+  } else {
+    const long long ns = plan_nseq(pl);
+    c.len = pl.nch - pl.H;
+    c.M = ns * c.len;
+    c.R = pl.P - ns;
+  }
+  return c;
+}
+__host__ __device__ inline long long plan_bound(const ScanPlan& pl, long long w) {
+  if (pl.H == 0) return w * pl.U / pl.P;
+  const long long ns = plan_nseq(pl);
+  return w <= ns ? w * pl.H : ns * pl.H + cut_bound(plan_cut(pl), w - ns);
 }
 // pieces of sequence s
 __host__ __device__ inline int plan_pieces(const ScanPlan& pl, long long s) {
-  const long long S0 = s * pl.nch, S1 = S0 + pl.nch;
-  return (int)(plan_count_le(pl, S1 - 1) - plan_count_le(pl, S0)) + 1;
+  return (pl.H == 0 ? 0 : 1) + cut_pieces(plan_cut(pl), s);
 }
 // chunk range [c_lo, c_hi) of piece k of sequence s
 __host__ __device__ inline void plan_piece_range(const ScanPlan& pl, long long s, int k, int& c_lo, int& c_hi) {
-  const long long S0 = s * pl.nch;
-  const long long wa = plan_count_le(pl, S0);  // first range boundary after the sequence start
-  const int K = plan_pieces(pl, s);
-  c_lo = k == 0 ? 0 : (int)(plan_bound(pl, wa + k - 1) - S0);
-  c_hi = k == K - 1 ? pl.nch : (int)(plan_bound(pl, wa + k) - S0);
+  if (pl.H == 0) {
+    cut_piece_range(plan_cut(pl), s, k, c_lo, c_hi);
+  } else if (k == 0) {
+    c_lo = 0;
+    c_hi = pl.H;
+  } else {
+    cut_piece_range(plan_cut(pl), s, k - 1, c_lo, c_hi);
+    c_lo += pl.H;
+    c_hi += pl.H;
+  }
+}
+// The item of a range that starts at unit u (range end u_end): sequence sq,
+// its chunks [c_lo, c_hi), piece index k, and the unit after the item.
+__host__ __device__ inline void plan_item(const ScanPlan& pl, long long u, long long u_end, long long& sq, int& c_lo,
+                                          int& c_hi, int& k, long long& next) {
+  const long long heads = pl.H == 0 ? 0 : plan_nseq(pl) * pl.H;
+  if (u < heads) {  // a whole head
+    sq = u / pl.H;
+    next = (sq + 1) * pl.H < u_end ? (sq + 1) * pl.H : u_end;
+    c_lo = (int)(u - sq * pl.H);
+    c_hi = (int)(next - sq * pl.H);
+    k = 0;
+    return;
+  }
+  const PlanCut c = plan_cut(pl);
+  const long long v = u - heads, S0 = (v / c.len) * c.len;
+  sq = v / c.len;
+  next = heads + (S0 + c.len < u_end - heads ? S0 + c.len : u_end - heads);
+  c_lo = pl.H + (int)(v - S0);
+  c_hi = pl.H + (int)(next - heads - S0);
+  k = (pl.H == 0 ? 0 : 1) + (int)(cut_count_le(c, v) - cut_count_le(c, S0));
 }
 
 using BwdPlan = ScanPlan;
@@ -72,28 +143,40 @@ using FwdPlan = ScanPlan;
 
 // The backward's aggregate pass works on sub-pieces of at most kAggSub
 // chunks of the later pieces (k >= 1) of each sequence, so that its longest
-// sequential walk is kAggSub chunks; sub-piece (k, j) of a sequence has slot
-// floor(start chunk / kAggSub) + k, unique and increasing in time.
+// sequential walk is kAggSub chunks.  Sub-piece (k, j) of a sequence has
+// slot floor(start chunk / kAggSub) + k (contiguous layout), or
+// floor((start chunk - H) / kAggSub) + k - 1 (split layout: only the tails
+// are aggregated) -- unique and increasing in time.
 constexpr int kAggSub = 8;
-__host__ __device__ inline int agg_slots(const ScanPlan& pl) { return (pl.nch + kAggSub - 1) / kAggSub + pl.maxp; }
+__host__ __device__ inline int agg_slot_of(const ScanPlan& pl, int chunk, int k) {
+  return pl.H == 0 ? chunk / kAggSub + k : (chunk - pl.H) / kAggSub + k - 1;
+}
+__host__ __device__ inline int agg_slots(const ScanPlan& pl) {
+  return pl.H == 0 ? (pl.nch + kAggSub - 1) / kAggSub + pl.maxp
+                   : (pl.nch - pl.H + kAggSub - 1) / kAggSub + pl.maxp - 1;
+}
 // slots [z0, z1] of piece k of sequence s
 __host__ __device__ inline void agg_piece_slots(const ScanPlan& pl, long long s, int k, int& z0, int& z1) {
   int lo, hi;
   plan_piece_range(pl, s, k, lo, hi);
-  z0 = lo / kAggSub + k;
-  z1 = (hi - 1) / kAggSub + k;
+  z0 = agg_slot_of(pl, lo, k);
+  z1 = agg_slot_of(pl, hi - 1, k);
 }
 // the sub-piece in slot z of sequence s: piece k >= 1, chunks [cs, ce); false if none
 __host__ __device__ inline bool agg_slot(const ScanPlan& pl, long long s, int z, int& k, int& cs, int& ce) {
   const int K = plan_pieces(pl, s);
   for (int kk = 1; kk < K; ++kk) {
-    int lo, hi;
+    int z0, z1, lo, hi;
     plan_piece_range(pl, s, kk, lo, hi);
-    const int z0 = lo / kAggSub + kk, z1 = (hi - 1) / kAggSub + kk;
+    z0 = agg_slot_of(pl, lo, kk);
+    z1 = agg_slot_of(pl, hi - 1, kk);
     if (z >= z0 && z <= z1) {
       k = kk;
-      cs = lo > (z - kk) * kAggSub ? lo : (z - kk) * kAggSub;
-      ce = hi < (z - kk + 1) * kAggSub ? hi : (z - kk + 1) * kAggSub;
+      // sub-piece boundaries: multiples of kAggSub from the aggregated region's origin
+      const int org = pl.H;
+      const int j = z - z0 + (lo - org) / kAggSub;  // sub-block index from the origin
+      cs = lo > org + j * kAggSub ? lo : org + j * kAggSub;
+      ce = hi < org + (j + 1) * kAggSub ? hi : org + (j + 1) * kAggSub;
       return cs < ce;
     }
   }
