@@ -1,10 +1,11 @@
 // S6 backward, TMA-pipelined, every state of a chunk in tensor memory (sm_103a).
 //
-// A persistent CTA walks a range of chunk units (plan: 152 equal ranges over
-// all (batch, 128-channel tile, 32-step chunk) units); each unit is one
-// 32-step chunk of 128 channels.  Warps: 2*TPC consumers (TPC = N/4), a TMA
-// producer, a converter (bf16: Bm/Cm rows widened to f32 once per chunk) and
-// a reducer (cross-warp sums of the dBm/dCm terms).
+// A persistent CTA walks a range of chunk units (plan: one range per SM over
+// all (batch, 128-channel tile, 32-step chunk) units, contiguous or split into
+// heads and tails); each unit is one 32-step chunk of 128 channels.  Warps:
+// 2*TPC consumers (TPC = N/4), a TMA producer, a converter (bf16: Bm/Cm rows
+// widened to f32 once per chunk) and two reducers (the channel sums of the
+// dBm and of the dCm terms; one warp alone fell behind the consumers).
 //
 // Consumer lane (pair cp, group q) owns channels d0 + 2cp, d0 + 2cp + 1 and
 // states 4q .. 4q+3 of both: 8 cells per step, two packed f32x2 operations per
@@ -28,10 +29,13 @@
 //   - over the 16 states of a channel (y, sum g*B, sum A*p): each lane adds its
 //     4 in registers, the TPC lanes of the pair are added in lane order by the
 //     lane that writes the step's outputs;
-//   - over channels (dBm, dCm): each lane adds its 2 channels inside the FMAs,
-//     a 3-round xor reduce-scatter adds the warp's lanes, the reducer warp adds
-//     the warps in ascending order into the tile's partial row, and a small
-//     kernel adds the tiles in ascending order (s6_bwd.cu);
+//   - over channels (dBm, dCm): each lane adds its 2 channels inside the FMAs;
+//     bf16: the lanes' terms go to shared memory and the reducer warps add the
+//     64 pairs in a fixed order (interleaved slices, then an xor butterfly);
+//     f32: a 3-round xor reduce-scatter adds the warp's lanes and the
+//     reducers add the warps in ascending order; either way into the tile's
+//     partial row, and a small kernel adds the tiles in ascending order
+//     (s6_bwd.cu);
 //   - over (b, t) (dA_log, dDp, d_delta_bias): per lane per chunk, then a
 //     compensated (Kahan) running total per piece, then the pieces and batches
 //     in ascending order (s6_bwd.cu).
@@ -140,14 +144,14 @@ struct BwdLayout {
   static constexpr int kPart2B = kSC * kRP2 * 8;                 // [SC][kRP2] (Ap0, Ap1)
   // dBm/dCm terms over the CTA's channels: bf16 -- each lane's 8 values of a
   // step in shared memory ([2 slots][SC][64 pairs][TPC groups][8] floats),
-  // added by the reducer warp; f32 (less
-  // shared memory) -- a warp-level xor reduce-scatter first, the warps' sums
-  // ([2 slots][SC][kCW][32]) added by the reducer warp
+  // added by the reducer warps; f32 (less shared memory) -- a warp-level xor
+  // reduce-scatter first, the warps' sums ([2 slots][SC][kCW][32]) added by
+  // the reducer warps.
   // Within a pair's block the 16-byte slot j (= 2q + 0 for the dBm terms,
   // 2q + 1 for the dCm terms) sits at j ^ red_swz(pair): consecutive pairs
   // rotate through the banks, so that a warp's stores (8 pairs x 4 groups)
-  // and the reducer's loads (4 slices x 8 slots) both take the minimum of
-  // four wavefronts.
+  // and a reducer's loads (8 slices of pairs 8 apart x 4 groups) both take
+  // the minimum of four wavefronts.
   static constexpr bool kRedSmem = kBf16;
   static constexpr int kRedPair = TPC * 8;  // floats per channel pair in a step's block
   static constexpr int kRedStep = 64 * kRedPair;
@@ -173,7 +177,7 @@ struct BwdLayout {
 // kLimit: delta is clamped to [dt_min, dt_max] (a separate instance, so the
 // unlimited scan pays nothing for it).
 template <typename Act, int TPC, bool kFast, bool kGate, bool kLimit>
-__global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const __grid_constant__ BwdTmaParams P) {
+__global__ void __launch_bounds__((2 * TPC + 4) * 32, 1) s6_bwd_tma_kernel(const __grid_constant__ BwdTmaParams P) {
   using LY = BwdLayout<Act, TPC>;
   using AT = typename LY::AT;
   constexpr int N = LY::N;
@@ -220,7 +224,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&wfull[i], kCW);
-      mbar_init(&wempty[i], 1);
+      mbar_init(&wempty[i], 2);  // both reducer warps
     }
     fence_mbar_init();
   }
@@ -317,9 +321,11 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
     }
     return;
   }
-  if (warp == kCW + 2) {
-    // ---------------- reducer: the warps' per-step dBm/dCm sums, added in
-    // ascending warp order, -> this tile's partial row [t][2][N]
+  if (warp == kCW + 2 || warp == kCW + 3) {
+    // ---------------- reducers: the consumers' per-step dBm/dCm terms summed
+    // over the tile's channel pairs in a fixed order -> this tile's partial
+    // row [t][2][N]; reducer r takes the dBm (r = 0) or the dCm (r = 1) half
+    const int r = warp - kCW - 2;
     int n = 0;
     bool ok = true;
     for (int u = u_begin, next; u < u_end; u = next) {
@@ -334,18 +340,20 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
           const int cnt = min(kSC, clen - sc * kSC);
           const float* src = dsum + slot * (LY::kDsumB / 8);
           if constexpr (LY::kRedSmem) {
-            // lane = slice * nG + group: group (q, qty) = 4 outputs, the slice
-            // a contiguous run of kCPL pairs; slices added by an xor butterfly
-            constexpr int nG = 2 * TPC, kLPG = 32 / nG, kCPL = 64 / kLPG;
-            const int og = lane % nG, sl = lane / nG;
-            const int gq = og >> 1, qty = og & 1;
+            // lane = slice * TPC + group: group gq = states 4gq .. 4gq+3; slice
+            // sl adds pairs sl, sl + kLPG, sl + 2 kLPG, ... (so that the pairs'
+            // slot rotations spread a load over the banks); slices then added
+            // by an xor butterfly
+            constexpr int nG = TPC, kLPG = 32 / nG, kCPL = 64 / kLPG;
+            const int gq = lane % nG, sl = lane / nG;
             for (int k = 0; k < cnt; ++k) {
-              const float* rp = src + k * LY::kRedStep + (sl * kCPL) * LY::kRedPair;
+              const float* rp = src + k * LY::kRedStep;
               float2 a = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
 #pragma unroll
               for (int i = 0; i < kCPL; ++i) {
-                const int j = (2 * gq + qty) ^ LY::red_swz(sl * kCPL + i);
-                const float4 v = *reinterpret_cast<const float4*>(rp + i * LY::kRedPair + 4 * j);
+                const int pr = sl + i * kLPG;
+                const int j = (2 * gq + r) ^ LY::red_swz(pr);
+                const float4 v = *reinterpret_cast<const float4*>(rp + pr * LY::kRedPair + 4 * j);
                 a = fadd2(a, make_float2(v.x, v.y));
                 b2 = fadd2(b2, make_float2(v.z, v.w));
               }
@@ -355,15 +363,15 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
                 b2 = fadd2(b2, make_float2(__shfl_xor_sync(0xffffffffu, b2.x, m), __shfl_xor_sync(0xffffffffu, b2.y, m)));
               }
               if (sl == 0)
-                *reinterpret_cast<float4*>(ws_r + (size_t)(c * kChunk + sc * kSC + k) * 2 * N + qty * N + 4 * gq) =
+                *reinterpret_cast<float4*>(ws_r + (size_t)(c * kChunk + sc * kSC + k) * 2 * N + r * N + 4 * gq) =
                     make_float4(a.x, a.y, b2.x, b2.y);
             }
-          } else if (lane < 2 * N) {
+          } else if (lane < N) {
             for (int k = 0; k < cnt; ++k) {
-              float v = src[(k * kCW) * 32 + lane];
+              float v = src[(k * kCW) * 32 + r * N + lane];
 #pragma unroll
-              for (int w = 1; w < kCW; ++w) v += src[(k * kCW + w) * 32 + lane];
-              ws_r[(size_t)(c * kChunk + sc * kSC + k) * 2 * N + lane] = v;
+              for (int w = 1; w < kCW; ++w) v += src[(k * kCW + w) * 32 + r * N + lane];
+              ws_r[(size_t)(c * kChunk + sc * kSC + k) * 2 * N + r * N + lane] = v;
             }
           }
           __syncwarp();
@@ -605,7 +613,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
           part4[kk * LY::kRP4 + tid] = make_float4(ya[0].x + ya[0].y, gba[0].x + gba[0].y, ya[1].x + ya[1].y, gba[1].x + gba[1].y);
           part2[kk * LY::kRP2 + tid] = make_float2(apa[0].x + apa[0].y, apa[1].x + apa[1].y);
           if constexpr (LY::kRedSmem) {
-            // this lane's 8 terms (summed over its 2 channels) for the reducer warp
+            // this lane's 8 terms (summed over its 2 channels) for the reducer warps
             float* rp = ds + kk * LY::kRedStep;
             const int off_c = red_off ^ 4;
             *reinterpret_cast<float4*>(rp + red_off) = make_float4(dB[0].x, dB[0].y, dB[1].x, dB[1].y);
@@ -1028,12 +1036,12 @@ cudaError_t launch_one(const BwdTmaParams& P, cudaStream_t stream, bool cooperat
   if (e != cudaSuccess) return e;
   // persistent: one CTA per range of the plan
   if (!cooperative) {
-    kern<<<P.p.plan.P, (2 * TPC + 3) * 32, smem, stream>>>(P);
+    kern<<<P.p.plan.P, (2 * TPC + 4) * 32, smem, stream>>>(P);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)P.p.plan.P);
-  cfg.blockDim = dim3((2 * TPC + 3) * 32);
+  cfg.blockDim = dim3((2 * TPC + 4) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
