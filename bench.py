@@ -247,13 +247,13 @@ def ssd_bwd_algorithmic(w):
     return nbytes, flops
 
 
-def time_ssd(dev, reps=10):
+def time_ssd(dev, reps=10, workload="mamba2_1p3b", with_wide=True):
     """The Mamba-2 SSD forward (plain and with state saves) and backward on the
     1.3B block's shape, CUDA events over `reps` calls each (inputs larger than
-    L2)."""
+    L2); and (`wide`) the same on the same width in heads of 128 columns."""
     from selective_state_space_s6_gb300 import s6
 
-    w = inputs.SSD_WORKLOADS["mamba2_1p3b"]
+    w = inputs.SSD_WORKLOADS[workload]
     x = inputs.make_ssd_inputs(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.act, seed=0)
     xd = {k: (v.to(dev) if v is not None else None) for k, v in x.items()}
     gen = torch.Generator(device=dev).manual_seed(1)
@@ -307,6 +307,10 @@ def time_ssd(dev, reps=10):
                 "bwd": line(timed(bwd), bb, bf),
                 "peaks": "measured hbm_gbs (copy) and bf16_tflops (cuBLAS, burst)",
                 "timing": f"CUDA events over {reps} calls each"})
+    if with_wide:
+        wide = time_ssd(dev, reps, "mamba2_1p3b_p128", with_wide=False)
+        res["wide"] = {"workload": wide["workload"], "fwd": {k: wide[k] for k in ("ms", "tensor_frac", "hbm_frac")},
+                       "bwd": {k: wide["bwd"][k] for k in ("ms", "tensor_frac", "hbm_frac")}}
     return res
 
 

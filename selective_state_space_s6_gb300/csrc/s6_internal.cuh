@@ -332,6 +332,11 @@ struct SsdArgs {
   unsigned int* status;
   float dt_min, dt_max;
   int B, L, H, G, N;
+  // sub-heads per head: P / 64.  A head of P = 64 m columns is m sub-heads of
+  // 64 columns sharing the head's dt, A, D and the group's Bm, Cm (the p
+  // columns of the SSD recurrence evolve independently); the kernels walk
+  // sub-heads, x / y / dx / dy being [B][L][H m][64] in memory
+  int m;
 };
 // Mamba-2 SSD backward (s6_ssd_bwd.cu); the forward's SsdArgs plus these
 struct SsdBwdArgs {
@@ -346,9 +351,11 @@ struct SsdBwdArgs {
   float* ddt_bias;       // [H]
   float* dDp;            // [H]
   float* dh0;            // [B][H][N][P] or null
-  float* ws;             // scratch: per-head dBm/dCm terms, per-(batch, head) scalars
+  float* ws;             // scratch: per-sub-head dBm/dCm terms, per-(batch, sub-head) scalars,
+                         // per-sub-head ddt_raw terms (m > 1)
 };
-size_t ssd_bwd_workspace_bytes(int B, int L, int H, int G, int N);
+// H heads of m sub-heads (headdim 64 m)
+size_t ssd_bwd_workspace_bytes(int B, int L, int H, int m, int G, int N);
 cudaError_t launch_ssd_bwd(const SsdBwdArgs& a, cudaStream_t stream);
 bool ssd_supported(int act, int P, int N);
 cudaError_t launch_ssd_fwd(const SsdArgs& a, cudaStream_t stream);

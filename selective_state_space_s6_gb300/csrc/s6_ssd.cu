@@ -45,8 +45,11 @@ constexpr int kVecSet = 320;         // floats of one chunk's decay set
 
 struct SsdParams {
   CUtensorMap map_x, map_B, map_C;  // 64-byte aligned members first
-  const __nv_bfloat16* dt_raw;      // [B][L][H]
-  const float* dt_bias;             // [H]
+  // H below counts sub-heads (heads x m); the per-head parameters and dt are
+  // those of head h / m, and a sub-head's state is the 64 columns (h % m) * 64
+  // of its head's [N][64 m] state
+  const __nv_bfloat16* dt_raw;      // [B][L][H / m]
+  const float* dt_bias;             // [H / m]
   const float* A_log;               // [H]
   const float* Dp;                  // [H]
   const float* h0;                  // [B][H][N][P] or null
@@ -57,7 +60,7 @@ struct SsdParams {
   __nv_bfloat16* chunk_states;
   unsigned int* status;
   float dt_min, dt_max;
-  int B, L, H, G, N;
+  int B, L, H, G, N, m;
   // 0: one CTA per sequence, all chunks; 1: the state over chunks
   // [0, seg_chunks) only, from h0, into h_last; 2: two CTAs per sequence,
   // chunks [0, seg_chunks) from h0 and [seg_chunks, end) from h_last
@@ -116,12 +119,15 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   uint64_t* bar_y = full + 4;   // M x and the state update done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 5);
 
-  const int b = bh / P.H, h = bh % P.H;
-  const int g = h / (P.H / P.G);
+  const int b = bh / P.H, h = bh % P.H;   // h: the sub-head
+  const int Hr = P.H / P.m, hr = h / P.m;  // heads; this sub-head's head
+  const int g = hr / (Hr / P.G);
+  // this sub-head's state rows: [N][st_ld] f32 (or bf16 saves), from column st_c0
+  const int st_ld = kP * P.m, st_c0 = (h % P.m) * kP;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const float A = -expf(P.A_log[h]);
-  const float bias = P.dt_bias[h];
-  const float Dh = P.Dp[h];
+  const float A = -expf(P.A_log[hr]);
+  const float bias = P.dt_bias[hr];
+  const float Dh = P.Dp[hr];
   // Roles beside the shared row work: thread 0 issues the tensor-core
   // products (C S_in, then M x and the state update, then the next chunk's
   // C B^T, in that order on the tensor core); thread 192 issues the TMA
@@ -179,7 +185,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   const int nch_all = (P.L + kQ - 1) / kQ;
   auto save_state = [&](int c, const float* v) {
     if (!P.chunk_states || kStateOnly || !has_srow) return;
-    uint4* dst = reinterpret_cast<uint4*>(P.chunk_states + ((((size_t)b * P.H + h) * nch_all + c) * N + srow) * kP + sc);
+    uint4* dst = reinterpret_cast<uint4*>(P.chunk_states + ((((size_t)b * Hr + hr) * nch_all + c) * N + srow) * st_ld + st_c0 + sc);
 #pragma unroll
     for (int q = 0; q < 4; ++q)
       dst[q] = make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
@@ -197,7 +203,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int t = min((c0 + ci) * kQ + 2 * lane + i, P.L - 1);  // past the end: any valid step, masked later
-      raw_next[i] = dt_bits[((size_t)b * P.L + t) * P.H + h];
+      raw_next[i] = dt_bits[((size_t)b * P.L + t) * Hr + hr];
     }
   };
   auto chunk_decays = [&](int ci) {
@@ -272,7 +278,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   // first update), h0 as bf16 for the first readout
   {
     float v[32];
-    const float* h0 = (init && has_srow) ? init + (((size_t)b * P.H + h) * N + srow) * kP + sc : nullptr;
+    const float* h0 = (init && has_srow) ? init + (((size_t)b * Hr + hr) * N + srow) * st_ld + st_c0 + sc : nullptr;
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = h0 ? h0[i] : 0.f;
     if (!kStateOnly && has_srow)
@@ -434,7 +440,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
         tmem_st32(tquarter + kColS + (uint32_t)sc, v);
         tmem_wait_st();
       } else if (write_last && P.h_last && has_srow) {
-        float* hl = P.h_last + (((size_t)b * P.H + h) * N + srow) * kP + sc;
+        float* hl = P.h_last + (((size_t)b * Hr + hr) * N + srow) * st_ld + st_c0 + sc;
 #pragma unroll
         for (int i = 0; i < 32; i += 2) *reinterpret_cast<float2*>(hl + i) = make_float2(v[i], v[i + 1]);
       }
@@ -489,15 +495,20 @@ cudaError_t launch_n(SsdParams P, cudaStream_t stream) {
 
 }  // namespace
 
-bool ssd_supported(int act, int P, int N) { return act == SSM_BF16 && P == kP && (N == 64 || N == 128); }
+// headdim P = 64 m (m sub-heads per head; m <= 4 keeps every index in range
+// of the checks made on the whole tensors)
+bool ssd_supported(int act, int P, int N) {
+  return act == SSM_BF16 && P % kP == 0 && P >= kP && P <= 4 * kP && (N == 64 || N == 128);
+}
 
 cudaError_t launch_ssd_fwd(const SsdArgs& a, cudaStream_t stream) {
   SsdParams P;
   memset(&P, 0, sizeof(P));
   const uint64_t e = 2;
   {
-    const uint64_t dims[3] = {(uint64_t)a.H * kP, (uint64_t)a.L, (uint64_t)a.B};
-    const uint64_t strides[2] = {(uint64_t)a.H * kP * e, (uint64_t)a.L * a.H * kP * e};
+    const uint64_t Hs = (uint64_t)a.H * a.m;  // sub-heads
+    const uint64_t dims[3] = {Hs * kP, (uint64_t)a.L, (uint64_t)a.B};
+    const uint64_t strides[2] = {Hs * kP * e, (uint64_t)a.L * Hs * kP * e};
     const uint32_t box[3] = {64, kQ, 1};
     if (!encode_tile_map(&P.map_x, a.x, true, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
@@ -523,7 +534,8 @@ cudaError_t launch_ssd_fwd(const SsdArgs& a, cudaStream_t stream) {
   P.dt_max = a.dt_max;
   P.B = a.B;
   P.L = a.L;
-  P.H = a.H;
+  P.H = a.H * a.m;
+  P.m = a.m;
   P.G = a.G;
   P.N = a.N;
   return a.N == 128 ? launch_n<128>(P, stream) : launch_n<64>(P, stream);

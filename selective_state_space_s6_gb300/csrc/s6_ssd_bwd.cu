@@ -53,8 +53,11 @@ constexpr int kVecSet = 6 * 64 + 8;   // floats of one chunk's decay set
 
 struct SsdBwdParams {
   CUtensorMap map_x, map_dy, map_B, map_C, map_S;  // 64-byte aligned members first
-  const __nv_bfloat16* dt_raw;  // [B][L][H]
-  const float* dt_bias;         // [H]
+  // H below counts sub-heads (heads x m; headdim 64 m): the per-head
+  // parameters, dt and ddt_raw are those of head h / m, and a sub-head's state
+  // (gradient) is the 64 columns (h % m) * 64 of its head's [N][64 m] one
+  const __nv_bfloat16* dt_raw;  // [B][L][H / m]
+  const float* dt_bias;         // [H / m]
   const float* A_log;           // [H]
   const float* Dp;              // [H]
   const float* dh_last;         // [B][H][N][P] or null
@@ -64,9 +67,10 @@ struct SsdBwdParams {
   float* ws_dB;                 // [B][L][H][N] per-head dBm terms
   float* ws_dC;                 // [B][L][H][N] per-head dCm terms
   float* ws_sc;                 // [B][H][3]: sum dA, sum dDp, sum ddt_bias
+  float* ws_ddt;                // m > 1: [B][L][H] per-sub-head ddt_raw terms
   unsigned int* status;
   float dt_min, dt_max;
-  int B, L, H, G, N;
+  int B, L, H, G, N, m;
 };
 
 template <int N>
@@ -122,12 +126,15 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
   uint64_t* bar2 = full + 3;                                       // second products done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 4);
 
-  const int b = bh / P.H, h = bh % P.H;
-  const int g = h / (P.H / P.G);
+  const int b = bh / P.H, h = bh % P.H;   // h: the sub-head
+  const int Hr = P.H / P.m, hr = h / P.m;  // heads; this sub-head's head
+  const int g = hr / (Hr / P.G);
+  // this sub-head's state-gradient rows: [N][st_ld], from column st_c0
+  const int st_ld = kP * P.m, st_c0 = (h % P.m) * kP;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const float A = -expf(P.A_log[h]);
-  const float bias = P.dt_bias[h];
-  const float Dh = P.Dp[h];
+  const float A = -expf(P.A_log[hr]);
+  const float bias = P.dt_bias[hr];
+  const float Dh = P.Dp[hr];
   // Roles beside the row work: threads 0, 32 and 64 issue the tensor-core
   // products (three issuers in three warps, each accumulator written by one
   // of them; both groups complete when all three have committed); thread 192
@@ -172,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
     for (int j = 0; j < NT; ++j) {
       tma_load_3d(st + SM::kBo + j * kTileBytes, &P.map_B, &full[s], g * N + 64 * j, c * kQ, b);
       tma_load_3d(st + SM::kCo + j * kTileBytes, &P.map_C, &full[s], g * N + 64 * j, c * kQ, b);
-      tma_load_2d(st + SM::kSo + j * kTileBytes, &P.map_S, &full[s], 0, ((bh * nch) + c) * N + 64 * j);
+      tma_load_2d(st + SM::kSo + j * kTileBytes, &P.map_S, &full[s], st_c0, (((b * Hr + hr) * nch) + c) * N + 64 * j);
     }
   };
   if (tid == kTidTma) {
@@ -205,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int tc = min(c * kQ + 2 * lane + i, P.L - 1);  // past the end: any valid step, masked later
-      raw_next[i] = dt_bits[((size_t)b * P.L + tc) * P.H + h];
+      raw_next[i] = dt_bits[((size_t)b * P.L + tc) * Hr + hr];
     }
   };
   auto chunk_decays = [&](int ci) {
@@ -273,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
   // dS = dh_last (or 0) into TMEM
   {
     float v[32];
-    const float* src = (P.dh_last && has_srow) ? P.dh_last + (((size_t)b * P.H + h) * N + srow) * kP + sc : nullptr;
+    const float* src = (P.dh_last && has_srow) ? P.dh_last + (((size_t)b * Hr + hr) * N + srow) * st_ld + st_c0 + sc : nullptr;
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = src ? src[i] : 0.f;
     __syncwarp();
@@ -520,7 +527,12 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
       if (t < 32) suf += red[24];
       const float ddl = colD2 + wt * qv + A * suf;
       const float graw = ddl * vc[256 + t];
-      if (t0 + t < P.L) P.ddt_raw[((size_t)b * P.L + t0 + t) * P.H + h] = __float2bfloat16_rn(graw);
+      if (t0 + t < P.L) {
+        if (P.m == 1)
+          P.ddt_raw[((size_t)b * P.L + t0 + t) * Hr + hr] = __float2bfloat16_rn(graw);
+        else  // the head's sub-heads are added by the reduce kernel
+          P.ws_ddt[((size_t)b * P.L + t0 + t) * P.H + h] = graw;
+      }
       // chunk sums of dA terms and of ddt_raw, fixed order
       float va = dl * suf, vb = t0 + t < P.L ? graw : 0.f;
 #pragma unroll
@@ -589,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
     __syncwarp();
     tmem_ld32(tquarter + kColS + (uint32_t)sc, v);
     if (P.dh0 && has_srow) {
-      float* dst = P.dh0 + (((size_t)b * P.H + h) * N + srow) * kP + sc;
+      float* dst = P.dh0 + (((size_t)b * Hr + hr) * N + srow) * st_ld + st_c0 + sc;
 #pragma unroll
       for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
     }
@@ -606,15 +618,18 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// dBm / dCm[b,t,g,n] = sum over the group's heads (ascending) of the per-head
-// terms; dA_log[h] = A_h sum_b dA, dDp[h] = sum_b, ddt_bias[h] = sum_b
-// (ascending b).
+// dBm / dCm[b,t,g,n] = sum over the group's sub-heads (ascending) of the
+// per-sub-head terms; dA_log[h] = A_h sum_b sum_j dA, dDp[h] = sum_b sum_j,
+// ddt_bias[h] = sum_b sum_j (ascending b, then the head's sub-heads j); with
+// m > 1 sub-heads per head also ddt_raw[b,t,h] = sum_j (ascending).  H counts
+// sub-heads.
 __global__ void s6_ssd_bwd_reduce_kernel(const float* __restrict__ ws_dB, const float* __restrict__ ws_dC,
-                                         const float* __restrict__ ws_sc, const float* __restrict__ A_log,
-                                         int B, int L, int H, int G, int N, __nv_bfloat16* __restrict__ dBm,
-                                         __nv_bfloat16* __restrict__ dCm, float* __restrict__ dA_log,
+                                         const float* __restrict__ ws_sc, const float* __restrict__ ws_ddt,
+                                         const float* __restrict__ A_log, int B, int L, int H, int G, int N,
+                                         int m, __nv_bfloat16* __restrict__ dBm, __nv_bfloat16* __restrict__ dCm,
+                                         __nv_bfloat16* __restrict__ ddt_raw, float* __restrict__ dA_log,
                                          float* __restrict__ dDp, float* __restrict__ ddt_bias) {
-  const int hpg = H / G;
+  const int hpg = H / G, Hr = H / m;
   const size_t total = (size_t)B * L * G * N;
   for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
     const int n = (int)(e % N);
@@ -630,15 +645,25 @@ __global__ void s6_ssd_bwd_reduce_kernel(const float* __restrict__ ws_dB, const 
     dBm[e] = __float2bfloat16_rn(sb);
     dCm[e] = __float2bfloat16_rn(scv);
   }
+  if (m > 1) {
+    const size_t tot_d = (size_t)B * L * Hr;
+    for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < tot_d; e += (size_t)gridDim.x * blockDim.x) {
+      const float* w = ws_ddt + e * m;  // [b][t][h][j] = (b * L + t) * H + h * m + j
+      float v = w[0];
+      for (int j = 1; j < m; ++j) v += w[j];
+      ddt_raw[e] = __float2bfloat16_rn(v);
+    }
+  }
   if (blockIdx.x == 0) {
-    for (int hh = threadIdx.x; hh < H; hh += blockDim.x) {
+    for (int hh = threadIdx.x; hh < Hr; hh += blockDim.x) {
       float a = 0.f, d = 0.f, tb = 0.f;
-      for (int bb = 0; bb < B; ++bb) {
-        const float* w3 = ws_sc + ((size_t)bb * H + hh) * 3;
-        a += w3[0];
-        d += w3[1];
-        tb += w3[2];
-      }
+      for (int bb = 0; bb < B; ++bb)
+        for (int j = 0; j < m; ++j) {
+          const float* w3 = ws_sc + ((size_t)bb * H + (size_t)hh * m + j) * 3;
+          a += w3[0];
+          d += w3[1];
+          tb += w3[2];
+        }
       dA_log[hh] = -expf(A_log[hh]) * a;
       dDp[hh] = d;
       ddt_bias[hh] = tb;
@@ -658,11 +683,13 @@ cudaError_t launch_bwd_n(const SsdBwdParams& P, cudaStream_t stream) {
 
 }  // namespace
 
-size_t ssd_bwd_workspace_bytes(int B, int L, int H, int G, int N) {
+size_t ssd_bwd_workspace_bytes(int B, int L, int H, int m, int G, int N) {
   (void)G;
-  const size_t terms = (size_t)B * L * H * N * sizeof(float);
-  const size_t sc = ((size_t)B * H * 3 * sizeof(float) + 255) / 256 * 256;
-  return 2 * ((terms + 255) / 256 * 256) + sc;
+  const size_t Hs = (size_t)H * m;  // sub-heads
+  const size_t terms = (size_t)B * L * Hs * N * sizeof(float);
+  const size_t sc = ((size_t)B * Hs * 3 * sizeof(float) + 255) / 256 * 256;
+  const size_t ddt = m > 1 ? ((size_t)B * L * Hs * sizeof(float) + 255) / 256 * 256 : 0;
+  return 2 * ((terms + 255) / 256 * 256) + sc + ddt;
 }
 
 cudaError_t launch_ssd_bwd(const SsdBwdArgs& a, cudaStream_t stream) {
@@ -671,8 +698,9 @@ cudaError_t launch_ssd_bwd(const SsdBwdArgs& a, cudaStream_t stream) {
   memset(&P, 0, sizeof(P));
   const uint64_t e = 2;
   {
-    const uint64_t dims[3] = {(uint64_t)f.H * kP, (uint64_t)f.L, (uint64_t)f.B};
-    const uint64_t strides[2] = {(uint64_t)f.H * kP * e, (uint64_t)f.L * f.H * kP * e};
+    const uint64_t Hs = (uint64_t)f.H * f.m;  // sub-heads
+    const uint64_t dims[3] = {Hs * kP, (uint64_t)f.L, (uint64_t)f.B};
+    const uint64_t strides[2] = {Hs * kP * e, (uint64_t)f.L * Hs * kP * e};
     const uint32_t box[3] = {64, kQ, 1};
     if (!encode_tile_map(&P.map_x, f.x, true, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tile_map(&P.map_dy, a.dy, true, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -688,8 +716,9 @@ cudaError_t launch_ssd_bwd(const SsdBwdArgs& a, cudaStream_t stream) {
   }
   {
     const uint64_t nch = (uint64_t)(f.L + kQ - 1) / kQ;
-    const uint64_t dims[2] = {(uint64_t)kP, (uint64_t)f.B * f.H * nch * f.N};
-    const uint64_t strides[1] = {(uint64_t)kP * e};
+    // the saves [B][H][nch][N][64 m]: rows of 64 m, a sub-head's 64 columns at (h % m) * 64
+    const uint64_t dims[2] = {(uint64_t)kP * f.m, (uint64_t)f.B * f.H * nch * f.N};
+    const uint64_t strides[1] = {(uint64_t)kP * f.m * e};
     const uint32_t box[2] = {64, 64};
     if (!encode_tile_map(&P.map_S, f.chunk_states, true, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
@@ -702,26 +731,31 @@ cudaError_t launch_ssd_bwd(const SsdBwdArgs& a, cudaStream_t stream) {
   P.dx = static_cast<__nv_bfloat16*>(a.dx);
   P.ddt_raw = static_cast<__nv_bfloat16*>(a.ddt_raw);
   P.dh0 = a.dh0;
-  const size_t terms = ((size_t)f.B * f.L * f.H * f.N * sizeof(float) + 255) / 256 * 256;
+  const size_t Hs = (size_t)f.H * f.m;
+  const size_t terms = ((size_t)f.B * f.L * Hs * f.N * sizeof(float) + 255) / 256 * 256;
+  const size_t scb = ((size_t)f.B * Hs * 3 * sizeof(float) + 255) / 256 * 256;
   P.ws_dB = a.ws;
   P.ws_dC = reinterpret_cast<float*>(reinterpret_cast<char*>(a.ws) + terms);
   P.ws_sc = reinterpret_cast<float*>(reinterpret_cast<char*>(a.ws) + 2 * terms);
+  P.ws_ddt = f.m > 1 ? reinterpret_cast<float*>(reinterpret_cast<char*>(a.ws) + 2 * terms + scb) : nullptr;
   P.status = f.status;
   P.dt_min = f.dt_min;
   P.dt_max = f.dt_max;
   P.B = f.B;
   P.L = f.L;
-  P.H = f.H;
+  P.H = (int)Hs;
+  P.m = f.m;
   P.G = f.G;
   P.N = f.N;
   cudaError_t err = f.N == 128 ? launch_bwd_n<128>(P, stream) : launch_bwd_n<64>(P, stream);
   if (err != cudaSuccess) return err;
-  const size_t total = (size_t)f.B * f.L * f.G * f.N;
+  const size_t total = std::max((size_t)f.B * f.L * f.G * f.N, f.m > 1 ? (size_t)f.B * f.L * f.H : (size_t)0);
   const int threads = 256;
   const int blocks = (int)std::min<size_t>(std::max<size_t>((total + threads - 1) / threads, 1), 152 * 8);
   s6_ssd_bwd_reduce_kernel<<<blocks, threads, 0, stream>>>(
-      P.ws_dB, P.ws_dC, P.ws_sc, f.A_log, f.B, f.L, f.H, f.G, f.N, static_cast<__nv_bfloat16*>(a.dBm),
-      static_cast<__nv_bfloat16*>(a.dCm), a.dA_log, a.dDp, a.ddt_bias);
+      P.ws_dB, P.ws_dC, P.ws_sc, P.ws_ddt, f.A_log, f.B, f.L, (int)Hs, f.G, f.N, f.m,
+      static_cast<__nv_bfloat16*>(a.dBm), static_cast<__nv_bfloat16*>(a.dCm),
+      static_cast<__nv_bfloat16*>(a.ddt_raw), a.dA_log, a.dDp, a.ddt_bias);
   return cudaGetLastError();
 }
 

@@ -146,6 +146,10 @@ SSD_WORKLOADS = {
     "mamba2_1p3b": SsdWorkload("mamba2_1p3b", 4, 4096, 64, 64, 1, 128, "bf16",
                                description="Mamba-2-1.3B-shaped SSD forward: B=4 L=4096 heads=64 "
                                            "headdim=64 groups=1 N=128, bf16 activations"),
+    # the same block width in heads of 128 columns (two sub-heads per head)
+    "mamba2_1p3b_p128": SsdWorkload("mamba2_1p3b_p128", 4, 4096, 32, 128, 1, 128, "bf16",
+                                    description="Mamba-2-1.3B width, headdim 128: B=4 L=4096 heads=32 "
+                                                "headdim=128 groups=1 N=128, bf16 activations"),
 }
 
 

@@ -124,7 +124,8 @@ def test_ssd_validation(lib):
     args = [FAKE] * 10
     def call(B=1, L=8, H=2, P=64, G=1, N=64, act=1, a=None):
         return lib.ssm_ssd_fwd(B, L, H, P, G, N, act, *(a or args), None, None)
-    assert call(P=32) == 2 and b"headdim 64" in lib.ssm_last_error()
+    assert call(P=32) == 2 and b"headdim a multiple of 64" in lib.ssm_last_error()
+    assert call(P=96) == 2 and call(P=320) == 2  # 64 m columns, m <= 4
     assert call(N=16) == 2
     assert call(act=0) == 2                      # f32 activations: not built
     assert call(H=3, G=2) == 1 and b"multiple of ngroups" in lib.ssm_last_error()
@@ -175,6 +176,11 @@ def test_ssd_bwd_validation(lib):
     assert lib.ssm_ssd_bwd_workspace_bytes(1, 8, 3, 64, 2, 64, 1) == -1   # heads not a multiple of groups
     need = lib.ssm_ssd_bwd_workspace_bytes(2, 100, 4, 64, 2, 128, 1)
     assert need >= 2 * 2 * 100 * 4 * 128 * 4 and need % 256 == 0
+    # headdim 128: two sub-heads per head -- twice the per-sub-head terms,
+    # plus their ddt_raw terms
+    need2 = lib.ssm_ssd_bwd_workspace_bytes(2, 100, 4, 128, 2, 128, 1)
+    assert need2 >= 2 * 2 * 100 * 8 * 128 * 4 + 2 * 100 * 8 * 4 and need2 % 256 == 0
+    assert lib.ssm_ssd_bwd_workspace_bytes(2, 100, 4, 96, 2, 128, 1) == -1
     args = [FAKE] * 19  # x .. dh0, ws
 
     def call(B=2, L=100, H=4, P=64, G=2, N=128, act=1, a=None, ws_bytes=None):

@@ -27,6 +27,9 @@ SHAPES = [
     (2, 64, 2, 64, 1, 128),    # exactly one chunk
     (1, 1, 2, 64, 1, 64),      # a single step
     (3, 300, 6, 64, 3, 128),   # three groups of two heads
+    (2, 200, 4, 128, 2, 64),   # headdim 128: two sub-heads per head
+    (1, 130, 3, 192, 1, 128),  # headdim 192
+    (2, 100, 2, 256, 1, 64),   # headdim 256
 ]
 
 
@@ -111,6 +114,20 @@ def test_ssd_split_sequences_match_whole(B, L, H, G, N):
     y_whole, none = s6.ssd_fwd(*[xd[k] for k in KEYS], xd["h0"], want_h_last=False)
     s6.check_device_status()
     assert none is None
+    assert torch.equal(y_split, y_whole)
+    ry, rh = oracle.ssd_fwd(*[x[k] for k in KEYS], x["h0"])
+    assert rel_err(np64(y_split), ry) <= TOL["bf16"]
+    assert rel_err(np64(h_split), rh) <= TOL["bf16"]
+
+
+def test_ssd_wide_heads_split_match_whole():
+    """Headdim 128 on few sequences (16 sub-head sequences: cut in two): y
+    equals the uncut walk bit for bit and matches the oracle, with h_last."""
+    x = inputs.make_ssd_inputs(1, 1000, 8, 128, 2, 128, "bf16", seed=77, h0_std=0.5)
+    xd = _dev(x)
+    y_split, h_split = s6.ssd_fwd(*[xd[k] for k in KEYS], xd["h0"])
+    y_whole, _ = s6.ssd_fwd(*[xd[k] for k in KEYS], xd["h0"], want_h_last=False)
+    s6.check_device_status()
     assert torch.equal(y_split, y_whole)
     ry, rh = oracle.ssd_fwd(*[x[k] for k in KEYS], x["h0"])
     assert rel_err(np64(y_split), ry) <= TOL["bf16"]

@@ -25,11 +25,11 @@ def _dev(x):
     return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
 
 
-def _problem(B, L, H, G, N, seed, h0=True, dh=True):
-    x = inputs.make_ssd_inputs(B, L, H, 64, G, N, "bf16", seed=seed, h0_std=0.5 if h0 else None)
+def _problem(B, L, H, G, N, seed, h0=True, dh=True, P=64):
+    x = inputs.make_ssd_inputs(B, L, H, P, G, N, "bf16", seed=seed, h0_std=0.5 if h0 else None)
     gen = torch.Generator().manual_seed(seed + 1000)
-    x["dy"] = torch.randn((B, L, H, 64), generator=gen).to(torch.bfloat16)
-    x["dh_last"] = torch.randn((B, H, N, 64), generator=gen) if dh else None
+    x["dy"] = torch.randn((B, L, H, P), generator=gen).to(torch.bfloat16)
+    x["dh_last"] = torch.randn((B, H, N, P), generator=gen) if dh else None
     return x
 
 
@@ -70,6 +70,37 @@ def test_ssd_bwd_parity(B, L, H, G, N, variant):
     _, _, _, g = _gpu(_dev(x))
     ref = _oracle(x)
     _compare(g, ref)
+
+
+WIDE = [
+    # B, L, H, G, N, P: heads of 64 m columns run as m sub-heads
+    (2, 200, 4, 2, 64, 128),
+    (1, 130, 3, 1, 128, 192),
+    (1, 300, 2, 1, 128, 256),
+    (2, 64, 2, 2, 128, 128),    # exactly one chunk
+]
+
+
+@pytest.mark.parametrize("B,L,H,G,N,P", WIDE)
+@pytest.mark.parametrize("variant", ["h0_dh", "plain"])
+def test_ssd_bwd_wide_heads(B, L, H, G, N, P, variant):
+    """Headdim 128..256: every gradient (ddt_raw, dA_log, ddt_bias, dDp summed
+    over the head's sub-heads in a fixed order) against the oracle."""
+    full = variant == "h0_dh"
+    x = _problem(B, L, H, G, N, seed=B + L + P, h0=full, dh=full, P=P)
+    _, _, cs, g = _gpu(_dev(x))
+    assert cs.shape == (B, H, -(-L // 64), N, P)
+    _compare(g, _oracle(x))
+
+
+def test_ssd_bwd_wide_heads_deterministic():
+    xd = _dev(_problem(2, 300, 4, 2, 128, seed=9, P=128))
+    _, _, cs, g0 = _gpu(xd)
+    keep = {k: v.clone() for k, v in g0.items() if v is not None}
+    for _ in range(4):
+        g = s6.ssd_bwd(*[xd[k] for k in KEYS], cs, xd["dy"], xd["dh_last"])
+        for k, v in keep.items():
+            assert torch.equal(g[k], v), k
 
 
 def test_ssd_save_matches_plain_forward_and_the_oracle_states():
