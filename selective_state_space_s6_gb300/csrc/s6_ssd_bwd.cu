@@ -71,6 +71,7 @@ struct SsdBwdParams {
   unsigned int* status;
   float dt_min, dt_max;
   int B, L, H, G, N, m;
+  int Hr;  // heads (H / m)
 };
 
 template <int N>
@@ -127,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 4);
 
   const int b = bh / P.H, h = bh % P.H;   // h: the sub-head
-  const int Hr = P.H / P.m, hr = h / P.m;  // heads; this sub-head's head
+  const int Hr = P.Hr, hr = h / P.m;      // heads; this sub-head's head
   const int g = hr / (Hr / P.G);
   // this sub-head's state-gradient rows: [N][st_ld], from column st_c0
   const int st_ld = kP * P.m, st_c0 = (h % P.m) * kP;
@@ -624,12 +625,12 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
 // m > 1 sub-heads per head also ddt_raw[b,t,h] = sum_j (ascending).  H counts
 // sub-heads.
 __global__ void s6_ssd_bwd_reduce_kernel(const float* __restrict__ ws_dB, const float* __restrict__ ws_dC,
-                                         const float* __restrict__ ws_sc, const float* __restrict__ ws_ddt,
-                                         const float* __restrict__ A_log, int B, int L, int H, int G, int N,
-                                         int m, __nv_bfloat16* __restrict__ dBm, __nv_bfloat16* __restrict__ dCm,
-                                         __nv_bfloat16* __restrict__ ddt_raw, float* __restrict__ dA_log,
-                                         float* __restrict__ dDp, float* __restrict__ ddt_bias) {
-  const int hpg = H / G, Hr = H / m;
+                                         const float* __restrict__ ws_sc, const float* __restrict__ A_log,
+                                         int B, int L, int H, int G, int N, int m,
+                                         __nv_bfloat16* __restrict__ dBm, __nv_bfloat16* __restrict__ dCm,
+                                         float* __restrict__ dA_log, float* __restrict__ dDp,
+                                         float* __restrict__ ddt_bias) {
+  const int hpg = H / G;
   const size_t total = (size_t)B * L * G * N;
   for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
     const int n = (int)(e % N);
@@ -645,17 +646,8 @@ __global__ void s6_ssd_bwd_reduce_kernel(const float* __restrict__ ws_dB, const 
     dBm[e] = __float2bfloat16_rn(sb);
     dCm[e] = __float2bfloat16_rn(scv);
   }
-  if (m > 1) {
-    const size_t tot_d = (size_t)B * L * Hr;
-    for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < tot_d; e += (size_t)gridDim.x * blockDim.x) {
-      const float* w = ws_ddt + e * m;  // [b][t][h][j] = (b * L + t) * H + h * m + j
-      float v = w[0];
-      for (int j = 1; j < m; ++j) v += w[j];
-      ddt_raw[e] = __float2bfloat16_rn(v);
-    }
-  }
   if (blockIdx.x == 0) {
-    for (int hh = threadIdx.x; hh < Hr; hh += blockDim.x) {
+    for (int hh = threadIdx.x; hh < H / m; hh += blockDim.x) {
       float a = 0.f, d = 0.f, tb = 0.f;
       for (int bb = 0; bb < B; ++bb)
         for (int j = 0; j < m; ++j) {
@@ -668,6 +660,18 @@ __global__ void s6_ssd_bwd_reduce_kernel(const float* __restrict__ ws_dB, const 
       dDp[hh] = d;
       ddt_bias[hh] = tb;
     }
+  }
+}
+
+// m > 1 sub-heads per head: ddt_raw[b,t,h] = sum over the head's sub-heads
+// (ascending) of their terms ws_ddt[b][t][h m + j]
+__global__ void s6_ssd_bwd_ddt_kernel(const float* __restrict__ ws_ddt, size_t n_out, int m,
+                                      __nv_bfloat16* __restrict__ ddt_raw) {
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n_out; e += (size_t)gridDim.x * blockDim.x) {
+    const float* w = ws_ddt + e * m;
+    float v = w[0];
+    for (int j = 1; j < m; ++j) v += w[j];
+    ddt_raw[e] = __float2bfloat16_rn(v);
   }
 }
 
@@ -745,17 +749,22 @@ cudaError_t launch_ssd_bwd(const SsdBwdArgs& a, cudaStream_t stream) {
   P.L = f.L;
   P.H = (int)Hs;
   P.m = f.m;
+  P.Hr = f.H;
   P.G = f.G;
   P.N = f.N;
   cudaError_t err = f.N == 128 ? launch_bwd_n<128>(P, stream) : launch_bwd_n<64>(P, stream);
   if (err != cudaSuccess) return err;
-  const size_t total = std::max((size_t)f.B * f.L * f.G * f.N, f.m > 1 ? (size_t)f.B * f.L * f.H : (size_t)0);
+  const size_t total = (size_t)f.B * f.L * f.G * f.N;
   const int threads = 256;
   const int blocks = (int)std::min<size_t>(std::max<size_t>((total + threads - 1) / threads, 1), 152 * 8);
   s6_ssd_bwd_reduce_kernel<<<blocks, threads, 0, stream>>>(
-      P.ws_dB, P.ws_dC, P.ws_sc, P.ws_ddt, f.A_log, f.B, f.L, (int)Hs, f.G, f.N, f.m,
-      static_cast<__nv_bfloat16*>(a.dBm), static_cast<__nv_bfloat16*>(a.dCm),
-      static_cast<__nv_bfloat16*>(a.ddt_raw), a.dA_log, a.dDp, a.ddt_bias);
+      P.ws_dB, P.ws_dC, P.ws_sc, f.A_log, f.B, f.L, (int)Hs, f.G, f.N, f.m, static_cast<__nv_bfloat16*>(a.dBm),
+      static_cast<__nv_bfloat16*>(a.dCm), a.dA_log, a.dDp, a.ddt_bias);
+  err = cudaGetLastError();
+  if (err != cudaSuccess || f.m == 1) return err;
+  const size_t n_ddt = (size_t)f.B * f.L * f.H;
+  const int dblocks = (int)std::min<size_t>(std::max<size_t>((n_ddt + threads - 1) / threads, 1), 152 * 8);
+  s6_ssd_bwd_ddt_kernel<<<dblocks, threads, 0, stream>>>(P.ws_ddt, n_ddt, f.m, static_cast<__nv_bfloat16*>(a.ddt_raw));
   return cudaGetLastError();
 }
 
