@@ -182,3 +182,30 @@ def test_ssd_random_shape_sweep(B, L, H, G, N, with_h0, limited):
     ry, rh = oracle.ssd_fwd(*[x[k] for k in KEYS], x["h0"], dt_limit=lim)
     assert rel_err(np64(y), ry) <= TOL["bf16"]
     assert rel_err(np64(h_last), rh) <= TOL["bf16"]
+
+
+def _wide_sweep(n=6, seed=654):
+    r = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        B = int(r.integers(1, 3))
+        L = int(r.integers(1, 300))
+        G = int(r.integers(1, 3))
+        H = G * int(r.integers(1, 3))
+        N = int(r.choice([64, 128]))
+        P = int(r.choice([128, 192, 256]))
+        out.append((B, L, H, G, N, P, bool(r.integers(0, 2)), bool(r.integers(0, 2))))
+    return out
+
+
+@pytest.mark.parametrize("B,L,H,G,N,P,with_h0,limited", _wide_sweep())
+def test_ssd_wide_random_shape_sweep(B, L, H, G, N, P, with_h0, limited):
+    """Seeded random shapes with heads of 128-256 columns."""
+    x = inputs.make_ssd_inputs(B, L, H, P, G, N, "bf16", seed=B * 5 + L + P, h0_std=0.5 if with_h0 else None)
+    lim = (0.01, 0.05) if limited else None
+    xd = _dev(x)
+    y, h_last = s6.ssd_fwd(*[xd[k] for k in KEYS], xd["h0"], dt_limit=lim)
+    s6.check_device_status()
+    ry, rh = oracle.ssd_fwd(*[x[k] for k in KEYS], x["h0"], dt_limit=lim)
+    assert rel_err(np64(y), ry) <= TOL["bf16"]
+    assert rel_err(np64(h_last), rh) <= TOL["bf16"]

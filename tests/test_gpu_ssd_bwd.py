@@ -72,6 +72,42 @@ def test_ssd_bwd_parity(B, L, H, G, N, variant):
     _compare(g, ref)
 
 
+def _split_heads(x, P):
+    """The problem with each head of P = 64 m columns written as m heads of 64
+    (columns split, the head's dt, dt_bias, A_log, Dp repeated)."""
+    m = P // 64
+    B, L, H, _ = x["x"].shape
+    N = x["Bm"].shape[3]
+    y = {"Bm": x["Bm"], "Cm": x["Cm"]}
+    for k in ("x", "dy"):
+        y[k] = x[k].reshape(B, L, H * m, 64).contiguous()
+    y["dt_raw"] = x["dt_raw"].repeat_interleave(m, dim=2).contiguous()
+    for k in ("dt_bias", "A_log", "Dp"):
+        y[k] = x[k].repeat_interleave(m).contiguous()
+    for k in ("h0", "dh_last"):
+        y[k] = (None if x[k] is None else
+                x[k].reshape(B, H, N, m, 64).permute(0, 1, 3, 2, 4).reshape(B, H * m, N, 64).contiguous())
+    return y
+
+
+def _compare_wide(g, x, P, dt_limit=None):
+    """Every gradient against the oracle; the per-head sums (dA_log, ddt_bias,
+    dDp) of a head of m sub-heads to TOL times the sum of the magnitudes of
+    the sub-heads' parts (from the oracle on the split problem): a head's
+    value is a sum over its columns, which may cancel, so its error is
+    bounded by its parts' magnitudes, not by its own."""
+    ref = _oracle(x, dt_limit=dt_limit)
+    _compare(g, ref, keys=("dx", "ddt_raw", "dBm", "dCm", "dh0"))
+    m = P // 64
+    parts = _oracle(_split_heads(x, P), dt_limit=dt_limit)
+    for k in ("dA_log", "ddt_bias", "dDp"):
+        mag = np.abs(parts[k]).reshape(-1, m).sum(axis=1)
+        err = np.abs(np64(g[k]) - ref[k])
+        assert np.all(err <= TOL["bf16"] * mag + 1e-6), (k, err, mag)
+        # the oracle's head is the sum of its parts
+        assert np.allclose(parts[k].reshape(-1, m).sum(axis=1), ref[k], rtol=1e-9, atol=1e-9), k
+
+
 WIDE = [
     # B, L, H, G, N, P: heads of 64 m columns run as m sub-heads
     (2, 200, 4, 2, 64, 128),
@@ -90,7 +126,7 @@ def test_ssd_bwd_wide_heads(B, L, H, G, N, P, variant):
     x = _problem(B, L, H, G, N, seed=B + L + P, h0=full, dh=full, P=P)
     _, _, cs, g = _gpu(_dev(x))
     assert cs.shape == (B, H, -(-L // 64), N, P)
-    _compare(g, _oracle(x))
+    _compare_wide(g, x, P)
 
 
 def test_ssd_bwd_wide_heads_deterministic():
@@ -227,3 +263,25 @@ def test_ssd_bwd_random_shape_sweep(B, L, H, G, N, with_state, limited):
     lim = (0.01, 0.05) if limited else None
     _, _, _, g = _gpu(_dev(x), dt_limit=lim)
     _compare(g, _oracle(x, dt_limit=lim))
+
+
+def _wide_sweep(n=6, seed=97):
+    r = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        B = int(r.integers(1, 3))
+        L = int(r.integers(1, 260))
+        G = int(r.integers(1, 3))
+        H = G * int(r.integers(1, 3))
+        N = int(r.choice([64, 128]))
+        P = int(r.choice([128, 192, 256]))
+        out.append((B, L, H, G, N, P, bool(r.integers(0, 2)), bool(r.integers(0, 2))))
+    return out
+
+
+@pytest.mark.parametrize("B,L,H,G,N,P,with_state,limited", _wide_sweep())
+def test_ssd_bwd_wide_random_sweep(B, L, H, G, N, P, with_state, limited):
+    x = _problem(B, L, H, G, N, seed=B * 13 + L + P, h0=with_state, dh=with_state, P=P)
+    lim = (0.01, 0.05) if limited else None
+    _, _, _, g = _gpu(_dev(x), dt_limit=lim)
+    _compare_wide(g, x, P, dt_limit=lim)
