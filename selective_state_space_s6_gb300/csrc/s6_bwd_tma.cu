@@ -3,9 +3,11 @@
 // A persistent CTA walks a range of chunk units (plan: one range per SM over
 // all (batch, 128-channel tile, 32-step chunk) units, contiguous or split into
 // heads and tails); each unit is one 32-step chunk of 128 channels.  Warps:
-// 2*TPC consumers (TPC = N/4), a TMA producer, a converter (bf16: Bm/Cm rows
-// widened to f32 once per chunk) and two reducers (the channel sums of the
-// dBm and of the dCm terms; one warp alone fell behind the consumers).
+// 2*TPC consumers (TPC = N/4), a TMA producer and two reducers (the channel
+// sums of the dBm and of the dCm terms; one warp alone fell behind the
+// consumers).  A lane reads the Bm / Cm values of its 4 states straight from
+// the stage: 16 bytes each in f32, 8 bytes in bf16 widened in registers
+// (exact; half the shared-memory wavefronts of an f32 copy).
 //
 // Consumer lane (pair cp, group q) owns channels d0 + 2cp, d0 + 2cp + 1 and
 // states 4q .. 4q+3 of both: 8 cells per step, two packed f32x2 operations per
@@ -57,7 +59,7 @@ namespace {
 
 constexpr int kTT = 32;       // steps per tile (the forward's and the aggregate pass's tiles)
 constexpr int kSC = 4;        // pass B: steps per sub-chunk (32 TMEM columns)
-constexpr int kAggWarps = 6;  // aggregate pass: 4 consumer warps + producer + converter
+constexpr int kAggWarps = 5;  // aggregate pass: 4 consumer warps + producer
 constexpr int kBS = 2;        // stages of the main kernel's ring (one chunk each)
 static_assert(kChunk == kTT, "the backward's chunk is one tile");
 
@@ -132,7 +134,6 @@ struct BwdLayout {
   static constexpr int kBCB = kTT * N * (int)sizeof(Act);
   // stage: u, raw, z, dout tiles, then the Bm and Cm rows; 1024-byte multiple
   static constexpr int kStageB = ((4 * kTileB + 2 * kBCB) + 1023) / 1024 * 1024;
-  static constexpr int kBcfB = kBf16 ? kBS * kTT * 2 * N * 4 : 0;  // f32 Bm/Cm rows [S][TT][2][N]
   // Row strides, padded so that the lanes of a pair (which own different
   // steps, i.e. rows) hit different banks: pA rows of 64 float4 + 2, pY rows of
   // 64 float2 + 4, part4 / part2 rows of kLanes + 1 elements.
@@ -159,15 +160,14 @@ struct BwdLayout {
   __device__ static __forceinline__ int red_swz(int pair) { return (pair / (8 / kRedQ)) % kRedQ; }
   static constexpr int kDsumB = kRedSmem ? 2 * kSC * kRedStep * 4 : 2 * kSC * kCW * 32 * 4;
   static constexpr int kTotB = 2 * 12 * kLanes * 4;              // [2 (sum, comp)][12][lanes] running totals
-  static constexpr int kOffBcf = kBS * kStageB;
-  static constexpr int kOffPA = kOffBcf + kBcfB;
+  static constexpr int kOffPA = kBS * kStageB;
   static constexpr int kOffPY = kOffPA + kPAB;
   static constexpr int kOffPart4 = kOffPY + kPYB;
   static constexpr int kOffPart2 = kOffPart4 + kPart4B;
   static constexpr int kOffDsum = kOffPart2 + kPart2B;
   static constexpr int kOffTot = kOffDsum + kDsumB;
   static constexpr int kOffBar = kOffTot + kTotB;
-  static constexpr int kBars = 3 * kBS + 4;
+  static constexpr int kBars = 2 * kBS + 4;
   static constexpr int kBytes = kOffBar + kBars * 8 + 16;
   static constexpr uint32_t kTmemCols = kCW > 4 ? 512 : 256;
   static_assert(kCW <= 8, "two consumer warps per TMEM lane quarter at most");
@@ -177,7 +177,7 @@ struct BwdLayout {
 // kLimit: delta is clamped to [dt_min, dt_max] (a separate instance, so the
 // unlimited scan pays nothing for it).
 template <typename Act, int TPC, bool kFast, bool kGate, bool kLimit>
-__global__ void __launch_bounds__((2 * TPC + 4) * 32, 1) s6_bwd_tma_kernel(const __grid_constant__ BwdTmaParams P) {
+__global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const __grid_constant__ BwdTmaParams P) {
   using LY = BwdLayout<Act, TPC>;
   using AT = typename LY::AT;
   constexpr int N = LY::N;
@@ -190,7 +190,6 @@ __global__ void __launch_bounds__((2 * TPC + 4) * 32, 1) s6_bwd_tma_kernel(const
   constexpr float kAscale = kFast ? kLn2 : 1.f;
 
   extern __shared__ __align__(1024) unsigned char smem[];
-  float* bcf = reinterpret_cast<float*>(smem + LY::kOffBcf);
   float4* pA = reinterpret_cast<float4*>(smem + LY::kOffPA);
   float2* pY = reinterpret_cast<float2*>(smem + LY::kOffPY);
   float4* part4 = reinterpret_cast<float4*>(smem + LY::kOffPart4);
@@ -198,8 +197,7 @@ __global__ void __launch_bounds__((2 * TPC + 4) * 32, 1) s6_bwd_tma_kernel(const
   float* dsum = reinterpret_cast<float*>(smem + LY::kOffDsum);
   float* totS = reinterpret_cast<float*>(smem + LY::kOffTot);  // [2][12][lanes]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + LY::kOffBar);
-  uint64_t* conv = full + kBS;
-  uint64_t* empty = conv + kBS;
+  uint64_t* empty = full + kBS;
   uint64_t* wfull = empty + kBS;  // [2] dsum slot written by every consumer warp
   uint64_t* wempty = wfull + 2;   // [2] dsum slot summed by the reducer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wempty + 2);
@@ -219,7 +217,6 @@ __global__ void __launch_bounds__((2 * TPC + 4) * 32, 1) s6_bwd_tma_kernel(const
   if (tid == 0) {
     for (int s = 0; s < kBS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&conv[s], 32);
       mbar_init(&empty[s], kCW);
     }
     for (int i = 0; i < 2; ++i) {
@@ -296,36 +293,11 @@ __global__ void __launch_bounds__((2 * TPC + 4) * 32, 1) s6_bwd_tma_kernel(const
     }
     return;
   }
-  if (warp == kCW + 1) {
-    // ---------------- converter (bf16): the chunk's Bm and Cm rows -> f32 [TT][2][N]
-    if (kBf16) {
-      int item = 0;
-      bool ok = true;
-      for (int u = u_begin, next; u < u_end; u = next) {
-        int b, d0, c_lo, c_hi;
-        piece_at(u, b, d0, c_lo, c_hi, next);
-        for (int c = c_hi - 1; c >= c_lo; --c, ++item) {
-          const int s = item % kBS;
-          if (ok) ok = mbar_wait(&full[s], (uint32_t)(item / kBS) & 1, p.status);
-          const __nv_bfloat162* tb = reinterpret_cast<const __nv_bfloat162*>(tile_B(s));
-          const __nv_bfloat162* tc = reinterpret_cast<const __nv_bfloat162*>(tile_C(s));
-          float* dst = bcf + (size_t)s * kTT * 2 * N;
-          for (int e = lane; e < kTT * N / 2; e += 32) {
-            const int t = (2 * e) / N, n = (2 * e) % N;
-            *reinterpret_cast<float2*>(dst + (t * 2 + 0) * N + n) = __bfloat1622float2(tb[e]);
-            *reinterpret_cast<float2*>(dst + (t * 2 + 1) * N + n) = __bfloat1622float2(tc[e]);
-          }
-          mbar_arrive(&conv[s]);
-        }
-      }
-    }
-    return;
-  }
-  if (warp == kCW + 2 || warp == kCW + 3) {
+  if (warp == kCW + 1 || warp == kCW + 2) {
     // ---------------- reducers: the consumers' per-step dBm/dCm terms summed
     // over the tile's channel pairs in a fixed order -> this tile's partial
     // row [t][2][N]; reducer r takes the dBm (r = 0) or the dCm (r = 1) half
-    const int r = warp - kCW - 2;
+    const int r = warp - kCW - 1;
     int n = 0;
     bool ok = true;
     for (int u = u_begin, next; u < u_end; u = next) {
@@ -462,15 +434,24 @@ __global__ void __launch_bounds__((2 * TPC + 4) * 32, 1) s6_bwd_tma_kernel(const
       float2 h[2][2] = {{make_float2(nxt[0].x, nxt[0].y), make_float2(nxt[0].z, nxt[0].w)},
                         {make_float2(nxt[1].x, nxt[1].y), make_float2(nxt[1].z, nxt[1].w)}};
       if (!failed) failed = !mbar_wait(&full[s], par, p.status);
-      if (kBf16 && !failed) failed = !mbar_wait(&conv[s], par, p.status);
       __syncwarp();
       const Act* su = tile(s, 0);
       const Act* sr = tile(s, 1);
       const Act* sz = tile(s, 2);
       const Act* sg = tile(s, 3);
-      const float* Bt = (kBf16 ? bcf + (size_t)s * kTT * 2 * N : reinterpret_cast<const float*>(tile_B(s))) + 4 * q;
-      const float* Ct = kBf16 ? Bt + N : reinterpret_cast<const float*>(tile_C(s)) + 4 * q;
-      constexpr int kBst = kBf16 ? 2 * N : N;  // f32 row stride of the Bm (and Cm) rows
+      // Bm / Cm of the lane's 4 states in step k: one 16-byte (f32) or 8-byte
+      // (bf16, widened exactly) shared-memory read
+      const Act* Bt = tile_B(s) + 4 * q;
+      const Act* Ct = tile_C(s) + 4 * q;
+      auto ld4 = [&](const Act* row) -> float4 {
+        if constexpr (kBf16) {
+          const uint2 r = *reinterpret_cast<const uint2*>(row);
+          return make_float4(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xffff0000u),
+                             __uint_as_float(r.y << 16), __uint_as_float(r.y & 0xffff0000u));
+        } else {
+          return *reinterpret_cast<const float4*>(row);
+        }
+      };
 
       // ---------- prep A: (delta, delta*u) of the owned steps, both channels
 #pragma unroll 2
@@ -496,7 +477,7 @@ __global__ void __launch_bounds__((2 * TPC + 4) * 32, 1) s6_bwd_tma_kernel(const
         float hb[32];
         auto stepA = [&](int k, int kk) {  // kk = k % kSC (a constant)
           const float4 v = pA[k * LY::kRA + cp];
-          const float4 Bv = *reinterpret_cast<const float4*>(Bt + k * kBst);
+          const float4 Bv = ld4(Bt + k * N);
           const float2 B01 = make_float2(Bv.x, Bv.y), B23 = make_float2(Bv.z, Bv.w);
           const float2 d0v = make_float2(v.x, v.x), u0v = make_float2(v.y, v.y);
           const float2 d1v = make_float2(v.z, v.z), u1v = make_float2(v.w, v.w);
@@ -571,8 +552,8 @@ __global__ void __launch_bounds__((2 * TPC + 4) * 32, 1) s6_bwd_tma_kernel(const
           tmem_ld8_issue(tm + (uint32_t)(8 * k), hq);  // the state before step k
           const float4 v = pA[k * LY::kRA + cp];
           const float2 dy = pY[kk * LY::kRY + cp];
-          const float4 Bv = *reinterpret_cast<const float4*>(Bt + k * kBst);
-          const float4 Cv = *reinterpret_cast<const float4*>(Ct + k * kBst);
+          const float4 Bv = ld4(Bt + k * N);
+          const float4 Cv = ld4(Ct + k * N);
           const float2 Bp[2] = {make_float2(Bv.x, Bv.y), make_float2(Bv.z, Bv.w)};
           const float2 Cp[2] = {make_float2(Cv.x, Cv.y), make_float2(Cv.z, Cv.w)};
           const float2 dd[2] = {make_float2(v.x, v.x), make_float2(v.z, v.z)};
@@ -804,11 +785,9 @@ __global__ void __launch_bounds__(kAggWarps * 32) s6_bwd_agg_kernel(const __grid
 
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* stages = smem;
-  float* cf = reinterpret_cast<float*>(smem + (size_t)S * kStageBytes);  // [S][TT][N] (bf16)
-  float2* prep = reinterpret_cast<float2*>(cf + (kBf16 ? S * kTT * N : 0));  // [TT][kPrepRow] (delta, dy)
+  float2* prep = reinterpret_cast<float2*>(smem + (size_t)S * kStageBytes);  // [TT][kPrepRow] (delta, dy)
   uint64_t* full = reinterpret_cast<uint64_t*>(prep + kTT * kPrepRow);
-  uint64_t* conv = full + S;
-  uint64_t* empty = conv + S;
+  uint64_t* empty = full + S;
 
   const BwdParams& p = P.p;
   if (smem_u32(smem) & 1023u) {
@@ -832,7 +811,6 @@ __global__ void __launch_bounds__(kAggWarps * 32) s6_bwd_agg_kernel(const __grid
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&conv[s], 32);
       mbar_init(&empty[s], 4);
     }
     fence_mbar_init();
@@ -870,21 +848,6 @@ __global__ void __launch_bounds__(kAggWarps * 32) s6_bwd_agg_kernel(const __grid
     }
     return;
   }
-  if (warp == 5) {
-    if (kBf16) {
-      for (int k = 0; k < ntiles; ++k) {
-        const int s = k % S;
-        if (!mbar_wait(&full[s], (uint32_t)(k / S) & 1, p.status)) break;
-        const __nv_bfloat162* tc = reinterpret_cast<const __nv_bfloat162*>(tile_C(s));
-        float* dst = cf + (size_t)s * kTT * N;
-        for (int e = lane; e < kBC / 2; e += 32)
-          *reinterpret_cast<float2*>(dst + 2 * e) = __bfloat1622float2(tc[e]);
-        mbar_arrive(&conv[s]);
-      }
-    }
-    return;
-  }
-
   const int q = tid % TPC, cl = tid / TPC;
   const int d = d0 + cl;
   const bool dvalid = d < D && cl < kValid;
@@ -907,13 +870,12 @@ __global__ void __launch_bounds__(kAggWarps * 32) s6_bwd_agg_kernel(const __grid
     const int s = k % S;
     const uint32_t par = (uint32_t)(k / S) & 1;
     if (!mbar_wait(&full[s], par, p.status)) break;
-    if (kBf16 && !mbar_wait(&conv[s], par, p.status)) break;
     const int tbase = t_lo + (ntiles - 1 - k) * kTT;
     const int cnt = min(kTT, t_hi - tbase);
     const Act* sr = tile_raw(s);
     const Act* sz = tile_z(s);
     const Act* sg = tile_g(s);
-    const float* Ct = (kBf16 ? cf + (size_t)s * kTT * N : reinterpret_cast<const float*>(tile_C(s))) + 4 * q;
+    const Act* Ct = tile_C(s) + 4 * q;  // the Cm values of the lane's 4 states (bf16: widened exactly)
     // phase 1: (delta, dy) of the owned steps; steps past the end get (0, 0)
     const bool full_tile = cnt == kTT;
 #pragma unroll
@@ -936,7 +898,14 @@ __global__ void __launch_bounds__(kAggWarps * 32) s6_bwd_agg_kernel(const __grid
     auto rstep = [&](int kk) {
       const float2 v = prep[kk * kPrepRow + cl];
       const float2 dd = make_float2(v.x, v.x), dy2 = make_float2(v.y, v.y);
-      const float4 Cv = *reinterpret_cast<const float4*>(Ct + kk * N);
+      float4 Cv;
+      if constexpr (kBf16) {
+        const uint2 r = *reinterpret_cast<const uint2*>(Ct + kk * N);
+        Cv = make_float4(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xffff0000u), __uint_as_float(r.y << 16),
+                         __uint_as_float(r.y & 0xffff0000u));
+      } else {
+        Cv = *reinterpret_cast<const float4*>(Ct + kk * N);
+      }
       const float2 g0 = ffma2(dy2, make_float2(Cv.x, Cv.y), carry[0]);
       const float2 g1 = ffma2(dy2, make_float2(Cv.z, Cv.w), carry[1]);
       carry[0] = fmul2(decay2<kFast>(dd, A2[0]), g0);
@@ -999,10 +968,8 @@ __global__ void s6_bwd_seg_carry_kernel(const BwdParams p) {
 
 template <typename Act, int TPC>
 size_t bwd_agg_smem_bytes() {
-  constexpr int N = 4 * TPC, kCh = kScanThreads / TPC, S = 3;
-  constexpr bool bf = std::is_same<Act, __nv_bfloat16>::value;
-  return (size_t)S * agg_stage_bytes<Act, TPC>() + (bf ? (size_t)S * kTT * N * 4 : 0) +
-         (size_t)kTT * (kCh + 4) * 8 + 3 * S * 8;
+  constexpr int kCh = kScanThreads / TPC, S = 3;
+  return (size_t)S * agg_stage_bytes<Act, TPC>() + (size_t)kTT * (kCh + 4) * 8 + 2 * S * 8;
 }
 
 template <typename Act, int TPC, bool kFast, bool kGate>
@@ -1036,12 +1003,12 @@ cudaError_t launch_one(const BwdTmaParams& P, cudaStream_t stream, bool cooperat
   if (e != cudaSuccess) return e;
   // persistent: one CTA per range of the plan
   if (!cooperative) {
-    kern<<<P.p.plan.P, (2 * TPC + 4) * 32, smem, stream>>>(P);
+    kern<<<P.p.plan.P, (2 * TPC + 3) * 32, smem, stream>>>(P);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)P.p.plan.P);
-  cfg.blockDim = dim3((2 * TPC + 4) * 32);
+  cfg.blockDim = dim3((2 * TPC + 3) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -1,14 +1,16 @@
 // S6 forward, TMA-pipelined (sm_103a).
 //
-// CTA = (channel tile, batch); 6 warps:
+// CTA = (channel tile, batch); 5 warps:
 //   warps 0-3  consumers: each channel's N states are split over TPC = N/4
 //              lanes, 4 states per lane in registers (the tile is 128/TPC
 //              channels); every lane walks the sequence in order;
 //   warp 4     producer: one lane streams [TT x 64] tiles of u, delta_raw, z and
 //              [TT x N] tiles of Bm, Cm into an S-stage shared-memory ring with
-//              cp.async.bulk.tensor (TMA), completion tracked by mbarriers;
-//   warp 5     converter (bf16 only): widens each stage's Bm/Cm tile to f32 once,
-//              for all 64 channels.
+//              cp.async.bulk.tensor (TMA), completion tracked by mbarriers.
+// A lane reads the Bm and Cm values of its 4 states straight from the tiles:
+// 16 bytes each in f32, 8 bytes in bf16, widened in registers (exact).  (The
+// 8-byte reads take half the shared-memory wavefronts of 16-byte reads of an
+// f32 copy; the recurrence's step is bound in part by those wavefronts.)
 // A consumer handles a 32-step tile in three phases, so that only the state
 // update is carried from step to step and everything else has independent
 // work to overlap:
@@ -40,11 +42,11 @@ namespace s6 {
 namespace {
 
 constexpr int kTT = 32;          // steps per pipeline stage
-constexpr int kFwdWarps = 6;     // 4 consumers + producer + converter
+constexpr int kFwdWarps = 5;     // 4 consumers + producer
 
 template <typename Act>
 struct FwdCfg {
-  // bf16: two stages keep a CTA at ~50 KB of shared memory, four CTAs per SM
+  // bf16: two stages keep a CTA at ~42 KB of shared memory, four CTAs per SM
   // (a tile takes microseconds of compute, well above the copy latency)
   static constexpr int kStages = std::is_same<Act, float>::value ? 3 : 2;
   // one stage: u, delta_raw, z tiles [kTT][128/TPC] and Bm, Cm tiles [kTT][N],
@@ -75,7 +77,6 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
   constexpr int kBC = kTT * N;            // elements of a [TT x N] tile
   constexpr bool kBf16 = std::is_same<Act, __nv_bfloat16>::value;
   constexpr int kStageBytes = FwdCfg<Act>::template stage_bytes<TPC>();
-  constexpr int kBst = kBf16 ? 2 * N : N;  // f32 row stride of B (and C) rows
   constexpr int kOwn = kTT / TPC;          // steps whose (t, d) work a lane owns
   constexpr int kPer = 8 / TPC;            // owned steps per 8 rows (the swizzle period)
   constexpr int kPrepRow = kCh + 4;        // float2 row stride of prep (see below)
@@ -84,16 +85,14 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
 
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* stages = smem;
-  float* bcf = reinterpret_cast<float*>(smem + (size_t)S * kStageBytes);  // [S][TT][2][N]
   // (delta, delta*u) per (step, channel); rows padded by 32 bytes so that the
   // 64-bit accesses of a half-warp (4 rows x 4 channels) fill the banks once
-  float2* prep = reinterpret_cast<float2*>(bcf + (kBf16 ? S * kTT * 2 * N : 0));  // [TT][kPrepRow]
+  float2* prep = reinterpret_cast<float2*>(smem + (size_t)S * kStageBytes);  // [TT][kPrepRow]
   // per-lane partial readouts; rows padded by one float so that the TPC lanes
   // of a channel, reading rows k, k+1, .. at once, hit different banks
   float* ypart = reinterpret_cast<float*>(prep + kTT * kPrepRow);  // [TT][kYRow]
   uint64_t* full = reinterpret_cast<uint64_t*>(ypart + kTT * kYRow);
-  uint64_t* conv = full + S;
-  uint64_t* empty = conv + S;
+  uint64_t* empty = full + S;
 
   const FwdParams& p = P.p;
   // the swizzled tiles need 1024-byte aligned stages (uniform: the whole CTA leaves)
@@ -146,7 +145,6 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&conv[s], 32);
       mbar_init(&empty[s], 4);
     }
     fence_mbar_init();
@@ -206,37 +204,6 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
     }
     return;
   }
-  if (warp == 5) {
-    // ---------------- converter: bf16 Bm/Cm tile -> f32, once per stage use
-    if (kBf16) {
-      int kt = 0;  // tiles over all items
-      bool ok = true;
-      for (int u = u_begin; u < u_end && ok;) {
-        const Item it = item_at(u);
-        u = it.next;
-        const int ntiles = (it.t_end - it.t_begin + kTT - 1) / kTT;
-        for (int k = 0; k < ntiles; ++k, ++kt) {
-          const int s = kt % S;
-          if (!mbar_wait(&full[s], (uint32_t)(kt / S) & 1, p.status)) {
-            ok = false;
-            break;
-          }
-          const __nv_bfloat162* tb = reinterpret_cast<const __nv_bfloat162*>(tile_B(s));
-          const __nv_bfloat162* tc = reinterpret_cast<const __nv_bfloat162*>(tile_C(s));
-          float* dst = bcf + (size_t)s * kTT * 2 * N;
-#pragma unroll 4
-          for (int e = lane; e < kBC / 2; e += 32) {
-            const int t = (2 * e) / N, n = (2 * e) % N;
-            *reinterpret_cast<float2*>(dst + (t * 2 + 0) * N + n) = __bfloat1622float2(tb[e]);
-            if (!kAgg) *reinterpret_cast<float2*>(dst + (t * 2 + 1) * N + n) = __bfloat1622float2(tc[e]);
-          }
-          mbar_arrive(&conv[s]);
-        }
-      }
-    }
-    return;
-  }
-
   // ---------------- consumers
   const int q = tid % TPC;    // state group: states 4q .. 4q+3
   const int cl = tid / TPC;   // channel within the tile
@@ -291,7 +258,6 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
     const int s = kt % S;
     const uint32_t par = (uint32_t)(kt / S) & 1;
     if (!failed) failed = !mbar_wait(&full[s], par, p.status);
-    if (kBf16 && !failed) failed = !mbar_wait(&conv[s], par, p.status);
     const int tbase = t_begin + k * kTT;
     const int cnt = min(kTT, t_end - tbase);
     if (kSave && !kAgg && (tbase % kChunk) == 0 && dvalid) {
@@ -306,8 +272,19 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
       const int o = exact ? kr * AT::kRowB + colo[i % kPer] : AT::off(kr, cl);
       return lds_act(reinterpret_cast<const Act*>(t + o));
     };
-    const float* Bt = (kBf16 ? bcf + (size_t)s * kTT * 2 * N : reinterpret_cast<const float*>(tile_B(s))) + 4 * q;
-    const float* Ct = (kBf16 ? Bt + N : reinterpret_cast<const float*>(tile_C(s)) + 4 * q);
+    // Bm / Cm of the lane's 4 states in step kk: one 16-byte (f32) or 8-byte
+    // (bf16, widened exactly) shared-memory read
+    const Act* Bt = tile_B(s) + 4 * q;
+    const Act* Ct = tile_C(s) + 4 * q;
+    auto ld4 = [&](const Act* row) -> float4 {
+      if constexpr (kBf16) {
+        const uint2 r = *reinterpret_cast<const uint2*>(row);
+        return make_float4(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xffff0000u),
+                           __uint_as_float(r.y << 16), __uint_as_float(r.y & 0xffff0000u));
+      } else {
+        return *reinterpret_cast<const float4*>(row);
+      }
+    };
 
     // one recurrence step for this lane's 4 states; the partial readout goes to ypart
     float tsum = 0.f;
@@ -315,7 +292,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
       const float2 dv = prep[kk * kPrepRow + cl];
       const float2 dd = make_float2(dv.x, dv.x);
       const float2 uu = make_float2(dv.y, dv.y);
-      const float4 Bv = *reinterpret_cast<const float4*>(Bt + kk * kBst);
+      const float4 Bv = ld4(Bt + kk * N);
       const float2 a0 = decay2<kFast>(dd, A2[0]);
       const float2 a1 = decay2<kFast>(dd, A2[1]);
       h[0] = ffma2(a0, h[0], fmul2(uu, make_float2(Bv.x, Bv.y)));
@@ -323,7 +300,7 @@ __global__ void __launch_bounds__(kFwdWarps * 32) s6_fwd_tma_kernel(const __grid
       if (kAgg) {
         tsum += dv.x;
       } else {
-        const float4 Cv = *reinterpret_cast<const float4*>(Ct + kk * kBst);
+        const float4 Cv = ld4(Ct + kk * N);
         const float2 y2 = ffma2(make_float2(Cv.z, Cv.w), h[1], fmul2(make_float2(Cv.x, Cv.y), h[0]));
         ypart[kk * kYRow + tid] = y2.x + y2.y;
       }
@@ -446,10 +423,9 @@ bool make_map(CUtensorMap* m, const void* base, int act, uint64_t rows, uint64_t
 
 template <typename Act, int TPC>
 constexpr size_t fwd_smem_bytes() {
-  constexpr int N = 4 * TPC, kCh = kScanThreads / TPC, S = FwdCfg<Act>::kStages;
-  constexpr bool bf = std::is_same<Act, __nv_bfloat16>::value;
-  return (size_t)S * FwdCfg<Act>::template stage_bytes<TPC>() + (bf ? (size_t)S * kTT * 2 * N * 4 : 0) +
-         (size_t)kTT * (kCh + 4) * 8 + (size_t)kTT * (kScanThreads + 1) * 4 + 3 * S * 8;
+  constexpr int kCh = kScanThreads / TPC, S = FwdCfg<Act>::kStages;
+  return (size_t)S * FwdCfg<Act>::template stage_bytes<TPC>() + (size_t)kTT * (kCh + 4) * 8 +
+         (size_t)kTT * (kScanThreads + 1) * 4 + 2 * S * 8;
 }
 
 template <typename Act, int TPC, bool kSave, bool kFast, bool kGate, bool kAgg>
