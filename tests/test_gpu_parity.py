@@ -327,3 +327,20 @@ def test_forward_stream_mode(B, L, D, N, act):
                for k, v in x.items()}
         _, h_ref = oracle.fwd(*[sub[k] for k in ARGS], sub["h0"])
         assert rel_err(cs[:, c], h_ref) <= TOL[act]
+
+
+@pytest.mark.parametrize("B,L,D,N,act", [(2, 300, 72, 16, "f32"), (3, 700, 200, 8, "f32"),
+                                         (2, 500, 128, 16, "bf16"), (1, 4096, 256, 16, "bf16")])
+def test_gpu_gradients_internally_consistent(B, L, D, N, act):
+    """The identities d_delta_bias = sum_{b,t} d_delta_raw and
+    dD = sum_{b,t} dy * u (dy = dout * silu(z)) hold for the GPU's own
+    outputs: d_delta_raw re-summed from the returned tensor, dy formed in f64
+    from the inputs (the sums that produce d_delta_bias and dD run on the
+    device in a fixed order, separately from the per-step outputs)."""
+    x = _inputs(B, L, D, N, act, seed=B * 7 + L + D)
+    xd = to_dev(x)
+    r = gpu_fwd_bwd(xd, dh_last=xd["dh_last"])
+    assert rel_err(np64(r["d_delta_bias"]), np64(r["d_delta_raw"]).sum(axis=(0, 1))) <= TOL[act]
+    z, dout, u = np64(xd["z"]), np64(xd["dout"]), np64(xd["u"])
+    dy = dout * z / (1.0 + np.exp(-z))
+    assert rel_err(np64(r["dD"]), (dy * u).sum(axis=(0, 1))) <= TOL[act]
