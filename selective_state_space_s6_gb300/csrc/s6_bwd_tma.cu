@@ -199,7 +199,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + LY::kOffBar);
   uint64_t* empty = full + kBS;
   uint64_t* wfull = empty + kBS;  // [2] dsum slot written by every consumer warp
-  uint64_t* wempty = wfull + 2;   // [2] dsum slot summed by the reducer
+  uint64_t* wempty = wfull + 2;   // [2] dsum slot summed by both reducers
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wempty + 2);
 
   const BwdParams& p = P.p;
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   // reduce-scatter of the 8 dBm/dCm values over the warp's pairs: output of this lane
   const int rs_o = ((lane >> 4) & 1) * N + 4 * q + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1);
   const bool rs_store = (lane & (3 & ~(TPC - 1))) == 0;
-  // this lane's dBm slot in a step's block of the reducer (its dCm slot: ^ 4)
+  // this lane's dBm slot in a step's block of the reducers (its dCm slot: ^ 4)
   const int red_off = cp * LY::kRedPair + 4 * ((2 * q) ^ LY::red_swz(cp));
   // swizzled byte offset of the pair's channels in the rows of the lane's
   // owned steps (it depends on the row % 8 only): owned step i of a 4-step
@@ -376,7 +376,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   bool failed = false;
   int s = 0;         // ring stage of the current chunk
   uint32_t par = 0;  // its phase parity
-  int nsub = 0;      // sub-chunks handed to the reducer so far
+  int nsub = 0;      // sub-chunks handed to the reducers so far
   for (int u = u_begin, next; u < u_end; u = next) {
     int b, d0, c_lo, c_hi, sq, kp;
     item_at(u, b, d0, c_lo, c_hi, next, sq, kp);
