@@ -313,10 +313,12 @@ int ssm_step_ex(int64_t batch, int64_t dim, int64_t dstate, int act, const void 
  *   dt_bias, A_log, Dp [H] f32; h0 (nullable: zeros), h_last (nullable)
  *   [B][H][N][P] f32; h0 and h_last may be the same buffer (the state
  *   updated in place).  opts: the limit on delta (NULL: none).
- * Supported: act = SSM_BF16, P = headdim in {64, 128, 192, 256}, N = dstate
- * in {64, 128}, H % G == 0; x, dt_raw, Bm, Cm, y 16-byte aligned.  (A head
- * of P = 64 m columns runs as m sub-heads of 64 columns sharing the head's
- * dt, A, Dp and the group's Bm, Cm: the columns of S evolve independently.)
+ * Supported: act = SSM_BF16, P = headdim in {32, 64, 128, 192, 256}, N =
+ * dstate in {64, 128}, H % G == 0; x, dt_raw, Bm, Cm, y 16-byte aligned.  (A
+ * head of P = 64 m columns runs as m sub-heads of 64 columns sharing the
+ * head's dt, A, Dp and the group's Bm, Cm: the columns of S evolve
+ * independently.  A head of 32 columns runs as 64 whose last 32 are zero,
+ * which adds exact zeros to every sum; nothing is written past column 32.)
  * Other shapes return SSM_ERR_UNSUPPORTED.  Asynchronous on `stream`;
  * allocates nothing.
  */
@@ -363,8 +365,8 @@ int64_t ssm_ssd_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t nhead
  *            aligned.
  * Evaluated per chunk of 64 steps, last chunk first, in the chunked matrix
  * form on the tensor cores (bf16 operands, f32 accumulation; the state's
- * gradient in f32).  Supported: as ssm_ssd_fwd (bf16, P in {64, 128, 192, 256}, N in {64,
- * 128}); dy, dx, dh_last, dh0, chunk_states 16-byte aligned.  Results are
+ * gradient in f32).  Supported: as ssm_ssd_fwd (bf16, P in {32, 64, 128, 192,
+ * 256}, N in {64, 128}); dy, dx, dh_last, dh0, chunk_states 16-byte aligned.  Results are
  * bit-identical from call to call.  Asynchronous on `stream`.
  */
 int ssm_ssd_bwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups,

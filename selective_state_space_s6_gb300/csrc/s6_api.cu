@@ -684,7 +684,7 @@ int check_ssd(int64_t B, int64_t L, int64_t H, int64_t P, int64_t G, int64_t N, 
                 (long long)L, (long long)H, (long long)P, (long long)G, (long long)N);
   if (H % G != 0) return fail(SSM_ERR_INVALID_ARG, "nheads %lld is not a multiple of ngroups %lld", (long long)H, (long long)G);
   if (!s6::ssd_supported(act, (int)P, (int)N))
-    return fail(SSM_ERR_UNSUPPORTED, "SSD %s supports bf16 activations, headdim a multiple of 64 (up to 256) and dstate 64 or 128", what);
+    return fail(SSM_ERR_UNSUPPORTED, "SSD %s supports bf16 activations, headdim 32 or a multiple of 64 (up to 256) and dstate 64 or 128", what);
   const int64_t nch = (L + SSM_SSD_CHUNK_LEN - 1) / SSM_SSD_CHUNK_LEN;
   if (B * L * H * P >= kMaxElems || B * L * H * N >= kMaxElems || B * H * nch * N >= kMaxElems || L >= kMaxElems)
     return fail(SSM_ERR_UNSUPPORTED, "problem too large for 31-bit indexing");
@@ -728,7 +728,8 @@ int ssd_fwd_common(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdi
   a.status = s6::device_status_word();
   if (!a.status) return fail(SSM_ERR_CUDA, "cannot locate the device status word");
   a.dt_min = dt_lo; a.dt_max = dt_hi;
-  a.B = (int)B; a.L = (int)L; a.H = (int)H; a.G = (int)G; a.N = (int)N; a.m = (int)(P / 64);
+  a.B = (int)B; a.L = (int)L; a.H = (int)H; a.G = (int)G; a.N = (int)N; a.m = (int)std::max<int64_t>(P / 64, 1);
+  a.w = (int)std::min<int64_t>(P, 64);
   const cudaError_t ce = s6::launch_ssd_fwd(a, st);
   return ce == cudaSuccess ? SSM_OK : cuda_fail(ce, "ssm_ssd_fwd launch");
 }
@@ -754,7 +755,7 @@ int ssm_ssd_fwd_save(int64_t batch, int64_t seqlen, int64_t nheads, int64_t head
 int64_t ssm_ssd_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
                                     int64_t ngroups, int64_t dstate, int act) {
   if (check_ssd(batch, seqlen, nheads, headdim, ngroups, dstate, act, "backward") != SSM_OK) return -1;
-  return (int64_t)s6::ssd_bwd_workspace_bytes((int)batch, (int)seqlen, (int)nheads, (int)(headdim / 64),
+  return (int64_t)s6::ssd_bwd_workspace_bytes((int)batch, (int)seqlen, (int)nheads, (int)std::max<int64_t>(headdim / 64, 1),
                                               (int)ngroups, (int)dstate);
 }
 
@@ -787,7 +788,7 @@ int ssm_ssd_bwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, 
   S6_TRY(need(dCm, B * L * G * N, 2, "dCm"));
   S6_TRY(need(dDp, H, 4, "dDp"));
   S6_TRY(opt(dh0, 16, "dh0"));
-  S6_TRY(check_ws(ws, ws_bytes, (int64_t)s6::ssd_bwd_workspace_bytes((int)B, (int)L, (int)H, (int)(P / 64), (int)G, (int)N)));
+  S6_TRY(check_ws(ws, ws_bytes, (int64_t)s6::ssd_bwd_workspace_bytes((int)B, (int)L, (int)H, (int)std::max<int64_t>(P / 64, 1), (int)G, (int)N)));
   g_last_error[0] = 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t ce;
@@ -808,7 +809,8 @@ int ssm_ssd_bwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, 
   a.f.status = s6::device_status_word();
   if (!a.f.status) return fail(SSM_ERR_CUDA, "cannot locate the device status word");
   a.f.dt_min = dt_lo; a.f.dt_max = dt_hi;
-  a.f.B = (int)B; a.f.L = (int)L; a.f.H = (int)H; a.f.G = (int)G; a.f.N = (int)N; a.f.m = (int)(P / 64);
+  a.f.B = (int)B; a.f.L = (int)L; a.f.H = (int)H; a.f.G = (int)G; a.f.N = (int)N; a.f.m = (int)std::max<int64_t>(P / 64, 1);
+  a.f.w = (int)std::min<int64_t>(P, 64);
   a.dy = dy; a.dh_last = dh_last; a.dx = dx; a.ddt_raw = ddt_raw; a.dBm = dBm; a.dCm = dCm;
   a.dA_log = dA_log; a.ddt_bias = ddt_bias; a.dDp = dDp; a.dh0 = dh0;
   a.ws = static_cast<float*>(ws);

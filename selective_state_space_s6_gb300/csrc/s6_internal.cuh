@@ -335,8 +335,9 @@ struct SsdArgs {
   // sub-heads per head: P / 64.  A head of P = 64 m columns is m sub-heads of
   // 64 columns sharing the head's dt, A, D and the group's Bm, Cm (the p
   // columns of the SSD recurrence evolve independently); the kernels walk
-  // sub-heads, x / y / dx / dy being [B][L][H m][64] in memory
-  int m;
+  // sub-heads, x / y / dx / dy being [B][L][H m][64] in memory.  P = 32: m = 1
+  // and w = 32 (the sub-head's columns in memory; else w = 64)
+  int m, w;
 };
 // Mamba-2 SSD backward (s6_ssd_bwd.cu); the forward's SsdArgs plus these
 struct SsdBwdArgs {
@@ -359,6 +360,11 @@ size_t ssd_bwd_workspace_bytes(int B, int L, int H, int m, int G, int N);
 cudaError_t launch_ssd_bwd(const SsdBwdArgs& a, cudaStream_t stream);
 bool ssd_supported(int act, int P, int N);
 cudaError_t launch_ssd_fwd(const SsdArgs& a, cudaStream_t stream);
+// the tensor map of an x-shaped [B][L][H][P] bf16 tensor (x, dy) for the SSD
+// kernels' [64 steps][64 columns] boxes of one sub-head: 3D over
+// [B][L][H m * 64] when w = 64; 4D over [B][L][H][32] when w = 32, the box's
+// columns 32..63 past the tensor's inner extent (filled with zeros)
+bool ssd_encode_x_map(void* map, const void* base, const SsdArgs& a);
 cudaError_t launch_conv1d_step(const ConvParams& p, int act, cudaStream_t stream);
 // The TMA backward's work plan for this shape with `sms` worker CTAs.
 BwdPlan bwd_plan(int B, int L, int D, int N, int sms);

@@ -47,7 +47,10 @@ struct SsdParams {
   CUtensorMap map_x, map_B, map_C;  // 64-byte aligned members first
   // H below counts sub-heads (heads x m); the per-head parameters and dt are
   // those of head h / m, and a sub-head's state is the 64 columns (h % m) * 64
-  // of its head's [N][64 m] state
+  // of its head's [N][64 m] state.  w: a sub-head's columns in memory, 64, or
+  // 32 for heads of 32 columns (run as 64 with columns 32..63 zero: the x / dy
+  // boxes past a head's 32 columns arrive as zeros, which add exact zeros to
+  // every sum, and nothing is written past column 32)
   const __nv_bfloat16* dt_raw;      // [B][L][H / m]
   const float* dt_bias;             // [H / m]
   const float* A_log;               // [H]
@@ -60,7 +63,7 @@ struct SsdParams {
   __nv_bfloat16* chunk_states;
   unsigned int* status;
   float dt_min, dt_max;
-  int B, L, H, G, N, m;
+  int B, L, H, G, N, m, w;
   // 0: one CTA per sequence, all chunks; 1: the state over chunks
   // [0, seg_chunks) only, from h0, into h_last; 2: two CTAs per sequence,
   // chunks [0, seg_chunks) from h0 and [seg_chunks, end) from h_last
@@ -123,7 +126,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   const int Hr = P.H / P.m, hr = h / P.m;  // heads; this sub-head's head
   const int g = hr / (Hr / P.G);
   // this sub-head's state rows: [N][st_ld] f32 (or bf16 saves), from column st_c0
-  const int st_ld = kP * P.m, st_c0 = (h % P.m) * kP;
+  const int st_ld = P.w * P.m, st_c0 = (h % P.m) * kP;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float A = -expf(P.A_log[hr]);
   const float bias = P.dt_bias[hr];
@@ -158,12 +161,18 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   const bool has_srow = N == 128 || lane < 16;
   const int srow = N == 128 ? 32 * (warp & 3) + lane : row;
   const int sc = 32 * kq;
+  // this thread's state columns exist in memory (w = 32: columns 32..63 are
+  // the zero padding, exactly zero throughout, never read or written)
+  const bool mem_s = has_srow && sc < P.w;
 
   auto issue = [&](int ci) {  // chunk ci's boxes into stage ci & 1 (one thread; no Cm for the state alone)
     const int s = ci & 1, c = c0 + ci;
     unsigned char* st = smem + s * SM::kBuf;
     mbar_arrive_expect_tx(&full[s], kStateOnly ? (uint32_t)((1 + NT) * kTileBytes) : SM::kTx);
-    tma_load_3d(st + SM::kX, &P.map_x, &full[s], h * kP, c * kQ, b);
+    if (P.w == kP)
+      tma_load_3d(st + SM::kX, &P.map_x, &full[s], h * kP, c * kQ, b);
+    else  // [B][L][H][w] as 4D: the box's columns past w are zeros
+      tma_load_4d(st + SM::kX, &P.map_x, &full[s], 0, h, c * kQ, b);
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       tma_load_3d(st + SM::kBo + j * kTileBytes, &P.map_B, &full[s], g * N + 64 * j, c * kQ, b);
@@ -184,7 +193,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   // sc .. sc + 31) to the saved chunk states, as bf16 (the readout's copy)
   const int nch_all = (P.L + kQ - 1) / kQ;
   auto save_state = [&](int c, const float* v) {
-    if (!P.chunk_states || kStateOnly || !has_srow) return;
+    if (!P.chunk_states || kStateOnly || !mem_s) return;
     uint4* dst = reinterpret_cast<uint4*>(P.chunk_states + ((((size_t)b * Hr + hr) * nch_all + c) * N + srow) * st_ld + st_c0 + sc);
 #pragma unroll
     for (int q = 0; q < 4; ++q)
@@ -278,7 +287,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
   // first update), h0 as bf16 for the first readout
   {
     float v[32];
-    const float* h0 = (init && has_srow) ? init + (((size_t)b * Hr + hr) * N + srow) * st_ld + st_c0 + sc : nullptr;
+    const float* h0 = (init && mem_s) ? init + (((size_t)b * Hr + hr) * N + srow) * st_ld + st_c0 + sc : nullptr;
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = h0 ? h0[i] : 0.f;
     if (!kStateOnly && has_srow)
@@ -405,8 +414,8 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
       tmem_ld16x2_16(tquarter + kColY + (uint32_t)(32 * kq), yv);
       tmem_ld16x2_16(tquarter + kColCS + (uint32_t)(32 * kq), cv);
       const float et = fast_exp(cum[2 * row]);
-      __nv_bfloat16* yrow = P.y + (((size_t)b * P.L + t0 + row) * P.H + h) * kP;
-      const bool store = t0 + row < P.L;
+      __nv_bfloat16* yrow = P.y + (((size_t)b * P.L + t0 + row) * P.H + h) * P.w;
+      const bool store = t0 + row < P.L && col0 < P.w;
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         const int c8 = col0 / 8 + q;
@@ -439,7 +448,7 @@ __global__ void __launch_bounds__(kSsdThreads) s6_ssd_fwd_kernel(const __grid_co
         __syncwarp();
         tmem_st32(tquarter + kColS + (uint32_t)sc, v);
         tmem_wait_st();
-      } else if (write_last && P.h_last && has_srow) {
+      } else if (write_last && P.h_last && mem_s) {
         float* hl = P.h_last + (((size_t)b * Hr + hr) * N + srow) * st_ld + st_c0 + sc;
 #pragma unroll
         for (int i = 0; i < 32; i += 2) *reinterpret_cast<float2*>(hl + i) = make_float2(v[i], v[i + 1]);
@@ -477,7 +486,7 @@ cudaError_t launch_n(SsdParams P, cudaStream_t stream) {
   const long long seqs = (long long)P.B * P.H;
   // h0 and h_last may be one buffer (the state updated in place): then the
   // first pass would overwrite h0 before the first halves read it
-  const size_t sbytes = (size_t)seqs * N * kP * sizeof(float);
+  const size_t sbytes = (size_t)seqs * N * P.w * sizeof(float);
   const char *s0 = reinterpret_cast<const char*>(P.h0), *s1 = reinterpret_cast<const char*>(P.h_last);
   const bool overlap = s0 && s1 && s0 < s1 + sbytes && s1 < s0 + sbytes;
   if (P.h_last == nullptr || overlap || nch < 4 || 2 * seqs > sms) {
@@ -495,24 +504,33 @@ cudaError_t launch_n(SsdParams P, cudaStream_t stream) {
 
 }  // namespace
 
-// headdim P = 64 m (m sub-heads per head; m <= 4 keeps every index in range
-// of the checks made on the whole tensors)
+// headdim P = 32 (one sub-head of 32 columns), or 64 m (m sub-heads per head;
+// m <= 4 keeps every index in range of the checks made on the whole tensors)
 bool ssd_supported(int act, int P, int N) {
-  return act == SSM_BF16 && P % kP == 0 && P >= kP && P <= 4 * kP && (N == 64 || N == 128);
+  return act == SSM_BF16 && (P == kP / 2 || (P % kP == 0 && P >= kP && P <= 4 * kP)) && (N == 64 || N == 128);
+}
+
+bool ssd_encode_x_map(void* map, const void* base, const SsdArgs& a) {
+  const uint64_t e = 2, Hs = (uint64_t)a.H * a.m;  // sub-heads
+  CUtensorMap* m = static_cast<CUtensorMap*>(map);
+  if (a.w == kP) {
+    const uint64_t dims[3] = {Hs * kP, (uint64_t)a.L, (uint64_t)a.B};
+    const uint64_t strides[2] = {Hs * kP * e, (uint64_t)a.L * Hs * kP * e};
+    const uint32_t box[3] = {64, kQ, 1};
+    return encode_tile_map(m, base, true, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  const uint64_t w = (uint64_t)a.w;
+  const uint64_t dims[4] = {w, Hs, (uint64_t)a.L, (uint64_t)a.B};
+  const uint64_t strides[3] = {w * e, Hs * w * e, (uint64_t)a.L * Hs * w * e};
+  const uint32_t box[4] = {64, 1, kQ, 1};
+  return encode_tile_map(m, base, true, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 cudaError_t launch_ssd_fwd(const SsdArgs& a, cudaStream_t stream) {
   SsdParams P;
   memset(&P, 0, sizeof(P));
   const uint64_t e = 2;
-  {
-    const uint64_t Hs = (uint64_t)a.H * a.m;  // sub-heads
-    const uint64_t dims[3] = {Hs * kP, (uint64_t)a.L, (uint64_t)a.B};
-    const uint64_t strides[2] = {Hs * kP * e, (uint64_t)a.L * Hs * kP * e};
-    const uint32_t box[3] = {64, kQ, 1};
-    if (!encode_tile_map(&P.map_x, a.x, true, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-  }
+  if (!ssd_encode_x_map(&P.map_x, a.x, a)) return cudaErrorInvalidValue;
   {
     const uint64_t dims[3] = {(uint64_t)a.G * a.N, (uint64_t)a.L, (uint64_t)a.B};
     const uint64_t strides[2] = {(uint64_t)a.G * a.N * e, (uint64_t)a.L * a.G * a.N * e};
@@ -536,6 +554,7 @@ cudaError_t launch_ssd_fwd(const SsdArgs& a, cudaStream_t stream) {
   P.L = a.L;
   P.H = a.H * a.m;
   P.m = a.m;
+  P.w = a.w;
   P.G = a.G;
   P.N = a.N;
   return a.N == 128 ? launch_n<128>(P, stream) : launch_n<64>(P, stream);

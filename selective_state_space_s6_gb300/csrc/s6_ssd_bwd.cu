@@ -55,7 +55,11 @@ struct SsdBwdParams {
   CUtensorMap map_x, map_dy, map_B, map_C, map_S;  // 64-byte aligned members first
   // H below counts sub-heads (heads x m; headdim 64 m): the per-head
   // parameters, dt and ddt_raw are those of head h / m, and a sub-head's state
-  // (gradient) is the 64 columns (h % m) * 64 of its head's [N][64 m] one
+  // (gradient) is the 64 columns (h % m) * 64 of its head's [N][64 m] one.
+  // w: a sub-head's columns in memory, 64, or 32 for heads of 32 columns (run
+  // as 64 whose columns 32..63 are zero: the x, dy and saved-state boxes past
+  // column 32 arrive as zeros, so the state gradient's padding stays zero and
+  // every sum over columns only gains exact zeros; nothing is written there)
   const __nv_bfloat16* dt_raw;  // [B][L][H / m]
   const float* dt_bias;         // [H / m]
   const float* A_log;           // [H]
@@ -70,7 +74,7 @@ struct SsdBwdParams {
   float* ws_ddt;                // m > 1: [B][L][H] per-sub-head ddt_raw terms
   unsigned int* status;
   float dt_min, dt_max;
-  int B, L, H, G, N, m;
+  int B, L, H, G, N, m, w;
   int Hr;  // heads (H / m)
 };
 
@@ -131,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
   const int Hr = P.Hr, hr = h / P.m;      // heads; this sub-head's head
   const int g = hr / (Hr / P.G);
   // this sub-head's state-gradient rows: [N][st_ld], from column st_c0
-  const int st_ld = kP * P.m, st_c0 = (h % P.m) * kP;
+  const int st_ld = P.w * P.m, st_c0 = (h % P.m) * kP;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float A = -expf(P.A_log[hr]);
   const float bias = P.dt_bias[hr];
@@ -168,14 +172,20 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
   const bool has_srow = N == 128 || lane < 16;
   const int srow = N == 128 ? 32 * (warp & 3) + lane : row;
   const int sc = 32 * kq;
+  const bool mem_s = has_srow && sc < P.w;  // this thread's state columns exist in memory
 
   // chunk c (walk index ci = nch - 1 - c) into stage ci & 1
   auto issue = [&](int ci) {
     const int s = ci & 1, c = nch - 1 - ci;
     unsigned char* st = smem + s * SM::kBuf;
     mbar_arrive_expect_tx(&full[s], SM::kTx);
-    tma_load_3d(st + SM::kX, &P.map_x, &full[s], h * kP, c * kQ, b);
-    tma_load_3d(st + SM::kDY, &P.map_dy, &full[s], h * kP, c * kQ, b);
+    if (P.w == kP) {
+      tma_load_3d(st + SM::kX, &P.map_x, &full[s], h * kP, c * kQ, b);
+      tma_load_3d(st + SM::kDY, &P.map_dy, &full[s], h * kP, c * kQ, b);
+    } else {  // [B][L][H][w] as 4D: the box's columns past w are zeros
+      tma_load_4d(st + SM::kX, &P.map_x, &full[s], 0, h, c * kQ, b);
+      tma_load_4d(st + SM::kDY, &P.map_dy, &full[s], 0, h, c * kQ, b);
+    }
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       tma_load_3d(st + SM::kBo + j * kTileBytes, &P.map_B, &full[s], g * N + 64 * j, c * kQ, b);
@@ -281,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
   // dS = dh_last (or 0) into TMEM
   {
     float v[32];
-    const float* src = (P.dh_last && has_srow) ? P.dh_last + (((size_t)b * Hr + hr) * N + srow) * st_ld + st_c0 + sc : nullptr;
+    const float* src = (P.dh_last && mem_s) ? P.dh_last + (((size_t)b * Hr + hr) * N + srow) * st_ld + st_c0 + sc : nullptr;
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = src ? src[i] : 0.f;
     __syncwarp();
@@ -566,8 +576,8 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
       float yv[16];
       get8(SM::kDY + s * SM::kBuf, row, col0 / 8, yv);
       get8(SM::kDY + s * SM::kBuf, row, col0 / 8 + 1, yv + 8);
-      if (t0 + row < P.L) {
-        uint4* dst = reinterpret_cast<uint4*>(P.dx + (((size_t)b * P.L + t0 + row) * P.H + h) * kP + col0);
+      if (t0 + row < P.L && col0 < P.w) {
+        uint4* dst = reinterpret_cast<uint4*>(P.dx + (((size_t)b * P.L + t0 + row) * P.H + h) * P.w + col0);
         uint32_t o[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) o[k] = pack_bf16(fmaf(Dh, yv[2 * k], xv[2 * k]), fmaf(Dh, yv[2 * k + 1], xv[2 * k + 1]));
@@ -601,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
     float v[32];
     __syncwarp();
     tmem_ld32(tquarter + kColS + (uint32_t)sc, v);
-    if (P.dh0 && has_srow) {
+    if (P.dh0 && mem_s) {
       float* dst = P.dh0 + (((size_t)b * Hr + hr) * N + srow) * st_ld + st_c0 + sc;
 #pragma unroll
       for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
@@ -701,15 +711,7 @@ cudaError_t launch_ssd_bwd(const SsdBwdArgs& a, cudaStream_t stream) {
   SsdBwdParams P;
   memset(&P, 0, sizeof(P));
   const uint64_t e = 2;
-  {
-    const uint64_t Hs = (uint64_t)f.H * f.m;  // sub-heads
-    const uint64_t dims[3] = {Hs * kP, (uint64_t)f.L, (uint64_t)f.B};
-    const uint64_t strides[2] = {Hs * kP * e, (uint64_t)f.L * Hs * kP * e};
-    const uint32_t box[3] = {64, kQ, 1};
-    if (!encode_tile_map(&P.map_x, f.x, true, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tile_map(&P.map_dy, a.dy, true, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-  }
+  if (!ssd_encode_x_map(&P.map_x, f.x, f) || !ssd_encode_x_map(&P.map_dy, a.dy, f)) return cudaErrorInvalidValue;
   {
     const uint64_t dims[3] = {(uint64_t)f.G * f.N, (uint64_t)f.L, (uint64_t)f.B};
     const uint64_t strides[2] = {(uint64_t)f.G * f.N * e, (uint64_t)f.L * f.G * f.N * e};
@@ -720,9 +722,10 @@ cudaError_t launch_ssd_bwd(const SsdBwdArgs& a, cudaStream_t stream) {
   }
   {
     const uint64_t nch = (uint64_t)(f.L + kQ - 1) / kQ;
-    // the saves [B][H][nch][N][64 m]: rows of 64 m, a sub-head's 64 columns at (h % m) * 64
-    const uint64_t dims[2] = {(uint64_t)kP * f.m, (uint64_t)f.B * f.H * nch * f.N};
-    const uint64_t strides[1] = {(uint64_t)kP * f.m * e};
+    // the saves [B][H][nch][N][w m]: rows of w m, a sub-head's 64 columns at
+    // (h % m) * 64 (w = 32: the box's columns 32..63 are zeros)
+    const uint64_t dims[2] = {(uint64_t)f.w * f.m, (uint64_t)f.B * f.H * nch * f.N};
+    const uint64_t strides[1] = {(uint64_t)f.w * f.m * e};
     const uint32_t box[2] = {64, 64};
     if (!encode_tile_map(&P.map_S, f.chunk_states, true, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
@@ -749,6 +752,7 @@ cudaError_t launch_ssd_bwd(const SsdBwdArgs& a, cudaStream_t stream) {
   P.L = f.L;
   P.H = (int)Hs;
   P.m = f.m;
+  P.w = f.w;
   P.Hr = f.H;
   P.G = f.G;
   P.N = f.N;

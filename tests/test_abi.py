@@ -124,7 +124,8 @@ def test_ssd_validation(lib):
     args = [FAKE] * 10
     def call(B=1, L=8, H=2, P=64, G=1, N=64, act=1, a=None):
         return lib.ssm_ssd_fwd(B, L, H, P, G, N, act, *(a or args), None, None)
-    assert call(P=32) == 2 and b"headdim a multiple of 64" in lib.ssm_last_error()
+    assert call(P=16) == 2 and b"headdim 32 or a multiple of 64" in lib.ssm_last_error()
+    assert call(P=48) == 2                       # neither 32 nor 64 m columns
     assert call(P=96) == 2 and call(P=320) == 2  # 64 m columns, m <= 4
     assert call(N=16) == 2
     assert call(act=0) == 2                      # f32 activations: not built
@@ -181,6 +182,10 @@ def test_ssd_bwd_validation(lib):
     need2 = lib.ssm_ssd_bwd_workspace_bytes(2, 100, 4, 128, 2, 128, 1)
     assert need2 >= 2 * 2 * 100 * 8 * 128 * 4 + 2 * 100 * 8 * 4 and need2 % 256 == 0
     assert lib.ssm_ssd_bwd_workspace_bytes(2, 100, 4, 96, 2, 128, 1) == -1
+    # headdim 32: one sub-head per head (64 columns, the last 32 zero), the
+    # workspace of headdim 64
+    assert lib.ssm_ssd_bwd_workspace_bytes(2, 100, 4, 32, 2, 128, 1) == need
+    assert lib.ssm_ssd_bwd_workspace_bytes(2, 100, 4, 16, 2, 128, 1) == -1
     args = [FAKE] * 19  # x .. dh0, ws
 
     def call(B=2, L=100, H=4, P=64, G=2, N=128, act=1, a=None, ws_bytes=None):

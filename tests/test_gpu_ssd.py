@@ -30,6 +30,8 @@ SHAPES = [
     (2, 200, 4, 128, 2, 64),   # headdim 128: two sub-heads per head
     (1, 130, 3, 192, 1, 128),  # headdim 192
     (2, 100, 2, 256, 1, 64),   # headdim 256
+    (2, 200, 4, 32, 2, 64),    # headdim 32: run as 64 with the last 32 columns zero
+    (1, 130, 3, 32, 1, 128),
 ]
 
 

@@ -108,6 +108,45 @@ def _compare_wide(g, x, P, dt_limit=None):
         assert np.allclose(parts[k].reshape(-1, m).sum(axis=1), ref[k], rtol=1e-9, atol=1e-9), k
 
 
+HEAD32 = [
+    # B, L, H, G, N: headdim 32, run as 64 columns whose last 32 are zero
+    (2, 200, 4, 2, 64),
+    (1, 130, 3, 1, 128),
+    (1, 1000, 8, 2, 128),   # few sequences: the forward cuts each in two
+]
+
+
+@pytest.mark.parametrize("B,L,H,G,N", HEAD32)
+@pytest.mark.parametrize("variant", ["h0_dh", "plain"])
+def test_ssd_bwd_head32(B, L, H, G, N, variant):
+    full = variant == "h0_dh"
+    x = _problem(B, L, H, G, N, seed=B + L + N + 32, h0=full, dh=full, P=32)
+    y, h_last, cs, g = _gpu(_dev(x))
+    assert cs.shape == (B, H, -(-L // 64), N, 32)
+    ry, rh = oracle.ssd_fwd(*[x[k] for k in KEYS], x["h0"])
+    assert rel_err(np64(y), ry) <= TOL["bf16"] and rel_err(np64(h_last), rh) <= TOL["bf16"]
+    _compare(g, _oracle(x))
+
+
+@pytest.mark.parametrize("B,L,H,G,N", [(2, 200, 4, 2, 64), (1, 1000, 8, 2, 128)])
+def test_ssd_head32_is_head64_with_zero_columns(B, L, H, G, N):
+    """Headdim 32 gives, bit for bit, what headdim 64 gives on the same problem
+    with columns 32..63 of x, dy, h0 and dh_last set to zero: the same
+    arithmetic on the same operands (the padding adds exact zeros), nothing
+    written past column 32; and the padded run's own columns 32..63 of y,
+    h_last, the saves, dx and dh0 are zero."""
+    x32 = _problem(B, L, H, G, N, seed=77 + L, P=32)
+    pad = lambda t: torch.nn.functional.pad(t, (0, 32))  # noqa: E731
+    x64 = dict(x32, x=pad(x32["x"]), dy=pad(x32["dy"]), h0=pad(x32["h0"]), dh_last=pad(x32["dh_last"]))
+    y32, hl32, cs32, g32 = _gpu(_dev(x32))
+    y64, hl64, cs64, g64 = _gpu(_dev(x64))
+    for a, b in ((y32, y64), (hl32, hl64), (cs32, cs64), (g32["dx"], g64["dx"]), (g32["dh0"], g64["dh0"])):
+        assert torch.equal(a, b[..., :32].contiguous())
+        assert not b[..., 32:].any()
+    for k in ("ddt_raw", "ddt_bias", "dA_log", "dBm", "dCm", "dDp"):
+        assert torch.equal(g32[k], g64[k]), k
+
+
 WIDE = [
     # B, L, H, G, N, P: heads of 64 m columns run as m sub-heads
     (2, 200, 4, 2, 64, 128),
