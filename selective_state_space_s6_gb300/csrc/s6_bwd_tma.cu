@@ -3,9 +3,9 @@
 // A persistent CTA walks a range of chunk units (plan: one range per SM over
 // all (batch, 128-channel tile, 32-step chunk) units, contiguous or split into
 // heads and tails); each unit is one 32-step chunk of 128 channels.  Warps:
-// 2*TPC consumers (TPC = N/4), a TMA producer and two reducers (the channel
-// sums of the dBm and of the dCm terms; one warp alone fell behind the
-// consumers).  A lane reads the Bm / Cm values of its 4 states straight from
+// 2*TPC consumers (TPC = N/4), a TMA producer and three reducers (the channel
+// sums of the dBm and dCm terms, step halves dealt out in turn; fewer fell
+// behind the consumers).  A lane reads the Bm / Cm values of its 4 states straight from
 // the stage: 16 bytes each in f32, 8 bytes in bf16 widened in registers
 // (exact; half the shared-memory wavefronts of an f32 copy).
 //
@@ -177,7 +177,7 @@ struct BwdLayout {
 // kLimit: delta is clamped to [dt_min, dt_max] (a separate instance, so the
 // unlimited scan pays nothing for it).
 template <typename Act, int TPC, bool kFast, bool kGate, bool kLimit>
-__global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const __grid_constant__ BwdTmaParams P) {
+__global__ void __launch_bounds__((2 * TPC + 4) * 32, 1) s6_bwd_tma_kernel(const __grid_constant__ BwdTmaParams P) {
   using LY = BwdLayout<Act, TPC>;
   using AT = typename LY::AT;
   constexpr int N = LY::N;
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + LY::kOffBar);
   uint64_t* empty = full + kBS;
   uint64_t* wfull = empty + kBS;  // [2] dsum slot written by every consumer warp
-  uint64_t* wempty = wfull + 2;   // [2] dsum slot summed by both reducers
+  uint64_t* wempty = wfull + 2;   // [2] dsum slot summed by all three reducers
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wempty + 2);
 
   const BwdParams& p = P.p;
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&wfull[i], kCW);
-      mbar_init(&wempty[i], 2);  // both reducer warps
+      mbar_init(&wempty[i], 3);  // every reducer warp
     }
     fence_mbar_init();
   }
@@ -293,10 +293,13 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
     }
     return;
   }
-  if (warp == kCW + 1 || warp == kCW + 2) {
+  if (warp >= kCW + 1 && warp <= kCW + 3) {
     // ---------------- reducers: the consumers' per-step dBm/dCm terms summed
     // over the tile's channel pairs in a fixed order -> this tile's partial
-    // row [t][2][N]; reducer r takes the dBm (r = 0) or the dCm (r = 1) half
+    // row [t][2][N].  A sub-chunk's work is 2 cnt halves (step k, dBm or dCm
+    // half: item 2k + half); reducer r takes the items r, r + 3, ...  (The
+    // register file is allocated for 12 warps whether the CTA has 11 or 12,
+    // so the third reducer is free; two alone kept the consumers waiting.)
     const int r = warp - kCW - 1;
     int n = 0;
     bool ok = true;
@@ -318,13 +321,14 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
             // by an xor butterfly
             constexpr int nG = TPC, kLPG = 32 / nG, kCPL = 64 / kLPG;
             const int gq = lane % nG, sl = lane / nG;
-            for (int k = 0; k < cnt; ++k) {
+            for (int it = r; it < 2 * cnt; it += 3) {
+              const int k = it >> 1, hf = it & 1;
               const float* rp = src + k * LY::kRedStep;
               float2 a = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
 #pragma unroll
               for (int i = 0; i < kCPL; ++i) {
                 const int pr = sl + i * kLPG;
-                const int j = (2 * gq + r) ^ LY::red_swz(pr);
+                const int j = (2 * gq + hf) ^ LY::red_swz(pr);
                 const float4 v = *reinterpret_cast<const float4*>(rp + pr * LY::kRedPair + 4 * j);
                 a = fadd2(a, make_float2(v.x, v.y));
                 b2 = fadd2(b2, make_float2(v.z, v.w));
@@ -335,15 +339,16 @@ __global__ void __launch_bounds__((2 * TPC + 3) * 32, 1) s6_bwd_tma_kernel(const
                 b2 = fadd2(b2, make_float2(__shfl_xor_sync(0xffffffffu, b2.x, m), __shfl_xor_sync(0xffffffffu, b2.y, m)));
               }
               if (sl == 0)
-                *reinterpret_cast<float4*>(ws_r + (size_t)(c * kChunk + sc * kSC + k) * 2 * N + r * N + 4 * gq) =
+                *reinterpret_cast<float4*>(ws_r + (size_t)(c * kChunk + sc * kSC + k) * 2 * N + hf * N + 4 * gq) =
                     make_float4(a.x, a.y, b2.x, b2.y);
             }
           } else if (lane < N) {
-            for (int k = 0; k < cnt; ++k) {
-              float v = src[(k * kCW) * 32 + r * N + lane];
+            for (int it = r; it < 2 * cnt; it += 3) {
+              const int k = it >> 1, hf = it & 1;
+              float v = src[(k * kCW) * 32 + hf * N + lane];
 #pragma unroll
-              for (int w = 1; w < kCW; ++w) v += src[(k * kCW + w) * 32 + r * N + lane];
-              ws_r[(size_t)(c * kChunk + sc * kSC + k) * 2 * N + r * N + lane] = v;
+              for (int w = 1; w < kCW; ++w) v += src[(k * kCW + w) * 32 + hf * N + lane];
+              ws_r[(size_t)(c * kChunk + sc * kSC + k) * 2 * N + hf * N + lane] = v;
             }
           }
           __syncwarp();
@@ -1003,12 +1008,12 @@ cudaError_t launch_one(const BwdTmaParams& P, cudaStream_t stream, bool cooperat
   if (e != cudaSuccess) return e;
   // persistent: one CTA per range of the plan
   if (!cooperative) {
-    kern<<<P.p.plan.P, (2 * TPC + 3) * 32, smem, stream>>>(P);
+    kern<<<P.p.plan.P, (2 * TPC + 4) * 32, smem, stream>>>(P);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)P.p.plan.P);
-  cfg.blockDim = dim3((2 * TPC + 3) * 32);
+  cfg.blockDim = dim3((2 * TPC + 4) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
