@@ -19,9 +19,12 @@
 // These are the per-chunk products the oracle's backward is pinned to (its
 // chunked form, written independently in numpy).
 //
-// A CTA owns one (batch, head) and walks its chunks backwards; x, dy, Bm, Cm
-// and the chunk's entering state S_in (saved by the forward as bf16, the copy
-// its readout used) arrive by TMA into a two-deep ring of 128B-swizzled boxes.
+// A CTA owns one (batch, head) and walks its chunks backwards -- or, with
+// more sequences than SMs, a range of chunks per SM that cuts a sequence at
+// most once, the state gradient handed over between the two pieces (see
+// SsdBwdParams); x, dy, Bm, Cm and the chunk's entering state S_in (saved by
+// the forward as bf16, the copy its readout used) arrive by TMA into a
+// two-deep ring of 128B-swizzled boxes.
 // Every product runs on the 5th-generation tensor core (bf16 operands, f32
 // accumulators in tensor memory, one issuing thread): first G, Z, C S_in,
 // B dS and the state update dS <- e^(cum_end) dS + C^T dy', then -- after
@@ -70,12 +73,23 @@ struct SsdBwdParams {
   float* dh0;                   // [B][H][N][P] or null
   float* ws_dB;                 // [B][L][H][N] per-head dBm terms
   float* ws_dC;                 // [B][L][H][N] per-head dCm terms
-  float* ws_sc;                 // [B][H][3]: sum dA, sum dDp, sum ddt_bias
+  float* ws_sc;                 // [B][H][2 pieces][3]: sum dA, sum dDp, sum ddt_bias
   float* ws_ddt;                // m > 1: [B][L][H] per-sub-head ddt_raw terms
   unsigned int* status;
   float dt_min, dt_max;
   int B, L, H, G, N, m, w;
   int Hr;  // heads (H / m)
+  // The walk: the B H sequences (b major) of ceil(L / 64) chunks laid end to
+  // end, cut into gridDim.x equal ranges, one per CTA.  gridDim.x = B H: one
+  // sequence per CTA.  Fewer (one per SM, all resident: cooperative launch):
+  // a range is at least a sequence long, so a sequence is cut at most once,
+  // into a first piece at the end of one range and a last piece at the start
+  // of the next; the CTA holding the last piece walks it first and hands the
+  // state gradient it ends with (carry, [B H][N][64] f32) over through
+  // seq_flag ([B H], zeroed before the launch) to the CTA holding the first
+  // piece, which walks it last.
+  int* seq_flag;
+  float* carry;
 };
 
 template <int N>
@@ -112,12 +126,42 @@ constexpr uint32_t kColS = 0, kColG = 64, kColZ = 128, kColCS = 192, kColX = 256
 // decay set of a chunk (floats): delta [0,64), cum [64,128), e^cum [128,192),
 // w = e^(cum_end - cum) [192,256), sigmoid(s) * mask [256,320), w*delta
 // [320,384), e^(cum_end) [384]
-template <int N>
+// kCut: ranges of chunks that may cut sequences (one CTA per SM); else one
+// CTA per sequence (gridDim.x = B H), whose walk is that sequence alone.
+template <int N, bool kCut>
 __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_constant__ SsdBwdParams P) {
   using SM = BwdSmem<N>;
   constexpr int NT = SM::NT;
-  const int bh = blockIdx.x;
   const int nch = (P.L + kQ - 1) / kQ;
+  // this CTA's range of chunk units [u_begin, u_end) and the n-th chunk of
+  // its walk: pieces in order (the first from u_begin to its sequence's end,
+  // then whole sequences, the last possibly cut short), each piece's chunks
+  // last first
+  const long long U = (long long)P.B * P.H * nch;
+  const long long u_begin = (long long)blockIdx.x * U / gridDim.x;
+  const long long u_end = (long long)(blockIdx.x + 1) * U / gridDim.x;
+  const int nwalk = (int)(u_end - u_begin);
+  struct WalkPos {
+    int sq, c, c_lo, c_hi;  // sequence, chunk, the piece's chunks [c_lo, c_hi)
+  };
+  // the first piece [lo0, hi0) of sequence sq0; the last sequence sqz ends at hiz
+  const int sq0 = (int)(u_begin / nch), lo0 = (int)(u_begin - (long long)sq0 * nch);
+  const int hi0 = (int)min((long long)nch, u_end - (long long)sq0 * nch);
+  const int sqz = (int)((u_end - 1) / nch), hiz = (int)(u_end - (long long)sqz * nch);
+  // A walker starts before the walk's first chunk; step() moves it to the
+  // next chunk and says whether that chunk starts a piece.  (Every role that
+  // follows the walk -- the copies, the decays, the row work -- keeps one,
+  // so that no role divides per chunk.)
+  auto walk_start = [&]() { return WalkPos{sq0, hi0, lo0, hi0}; };
+  auto step = [&](WalkPos& w) {
+    if constexpr (!kCut) return --w.c == nch - 1;  // one sequence, chunks nch-1 .. 0
+    if (--w.c >= w.c_lo) return w.c == w.c_hi - 1;
+    ++w.sq;
+    w.c_lo = 0;
+    w.c_hi = w.sq == sqz ? hiz : nch;
+    w.c = w.c_hi - 1;
+    return true;
+  };
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -131,15 +175,12 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
   uint64_t* bar2 = full + 3;                                       // second products done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 4);
 
-  const int b = bh / P.H, h = bh % P.H;   // h: the sub-head
-  const int Hr = P.Hr, hr = h / P.m;      // heads; this sub-head's head
-  const int g = hr / (Hr / P.G);
-  // this sub-head's state-gradient rows: [N][st_ld], from column st_c0
-  const int st_ld = P.w * P.m, st_c0 = (h % P.m) * kP;
+  // a sequence sq is (batch sq / H, sub-head sq % H) of head (sq % H) / m;
+  // a sub-head's state-gradient rows: [N][st_ld] of its head, from column
+  // (h % m) * 64
+  const int Hr = P.Hr;  // heads
+  const int st_ld = P.w * P.m;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const float A = -expf(P.A_log[hr]);
-  const float bias = P.dt_bias[hr];
-  const float Dh = P.Dp[hr];
   // Roles beside the row work: threads 0, 32 and 64 issue the tensor-core
   // products (three issuers in three warps, each accumulator written by one
   // of them; both groups complete when all three have committed); thread 192
@@ -174,9 +215,13 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
   const int sc = 32 * kq;
   const bool mem_s = has_srow && sc < P.w;  // this thread's state columns exist in memory
 
-  // chunk c (walk index ci = nch - 1 - c) into stage ci & 1
-  auto issue = [&](int ci) {
-    const int s = ci & 1, c = nch - 1 - ci;
+  // the walk's chunk n into stage n & 1 (thread kTidTma, n = 0, 1, 2, ...)
+  WalkPos wt = walk_start();
+  int tb = sq0 / P.H, th = sq0 % P.H, thr = th / P.m, tg = thr / (Hr / P.G);
+  auto issue = [&](int n) {
+    if (step(wt) && kCut) tb = wt.sq / P.H, th = wt.sq % P.H, thr = th / P.m, tg = thr / (Hr / P.G);
+    const int s = n & 1, c = wt.c, b = tb, h = th, hr = thr, g = tg;
+    const int st_c0 = (h % P.m) * kP;
     unsigned char* st = smem + s * SM::kBuf;
     mbar_arrive_expect_tx(&full[s], SM::kTx);
     if (P.w == kP) {
@@ -213,22 +258,35 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
     }
   };
 
-  // decays of chunk c into set (ci & 1) (warp kWarpDecay; two steps per
+  // decays of the walk's chunk n into set (n & 1) (warp kWarpDecay; two steps per
   // lane).  The dt of a chunk are read one chunk ahead and kept as raw bits
   // until used, so that the load's latency hides behind a whole chunk.
   const unsigned short* dt_bits = reinterpret_cast<const unsigned short*>(P.dt_raw);
   unsigned short raw_next[2] = {0, 0};
-  auto load_dt = [&](int ci) {
-    const int c = nch - 1 - ci;
+  // the chunk's index and its head's A and dt_bias (with pieces: formed
+  // when its dt is read, a chunk ahead; else the sequence's, once)
+  int c_next = 0;
+  WalkPos wd = walk_start();
+  int db = sq0 / P.H, dhr = (sq0 % P.H) / P.m;
+  float a_next = -expf(P.A_log[dhr]), bias_next = P.dt_bias[dhr];
+  auto load_dt = [&](int n) {
+    if (step(wd) && kCut) {
+      db = wd.sq / P.H, dhr = (wd.sq % P.H) / P.m;
+      a_next = -expf(P.A_log[dhr]);
+      bias_next = P.dt_bias[dhr];
+    }
+    const int c = wd.c, b = db, hr = dhr;
+    c_next = c;
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int tc = min(c * kQ + 2 * lane + i, P.L - 1);  // past the end: any valid step, masked later
       raw_next[i] = dt_bits[((size_t)b * P.L + tc) * Hr + hr];
     }
   };
-  auto chunk_decays = [&](int ci) {
-    const int c = nch - 1 - ci;
-    float* v = vec + (ci & 1) * kVecSet;
+  auto chunk_decays = [&](int n) {
+    const int c = c_next;
+    const float A = a_next, bias = bias_next;
+    float* v = vec + (n & 1) * kVecSet;
     float d2v[2], a2[2], sg[2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -266,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
   if (warp == kWarpDecay) {
     load_dt(0);
     chunk_decays(0);
-    if (nch > 1) load_dt(1);
+    if (nwalk > 1) load_dt(1);
   }
 
   // operand descriptors (see the forward): K-major boxes/images with 32-byte
@@ -288,25 +346,86 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
   constexpr uint32_t kIdCkm = umma_idesc_bf16(64, N, false, true);   // dC second half
 
   __syncthreads();  // decays of the first chunk published
-  // dS = dh_last (or 0) into TMEM
-  {
-    float v[32];
-    const float* src = (P.dh_last && mem_s) ? P.dh_last + (((size_t)b * Hr + hr) * N + srow) * st_ld + st_c0 + sc : nullptr;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = src ? src[i] : 0.f;
-    __syncwarp();
-    tmem_st32(tquarter + kColS + (uint32_t)sc, v);
-    tmem_wait_st();
-  }
-  float accA = 0.f, accD = 0.f, accB = 0.f;  // this CTA's dA, dDp, ddt_bias (thread kTidDcum)
-  bool ok = true;  // uniform over the CTA
+  float accA = 0.f, accD = 0.f, accB = 0.f;  // the piece's dA, dDp, ddt_bias (thread kTidDcum)
+  bool ok = true;                            // no wait gave up (uniform over the CTA)
 
-  for (int ci = 0; ci < nch; ++ci) {
-    const int s = ci & 1;
-    const int c = nch - 1 - ci;
+  // a piece ends: dS is the gradient of the state entering chunk c_lo --
+  // dh0, or the carry for the CTA walking the sequence's first piece
+  auto piece_end = [&](const WalkPos& wp, int b, int h, int hr, int st_c0) {
+    tmem_fence_after_sync();
+    float v[32];
+    __syncwarp();
+    tmem_ld32(tquarter + kColS + (uint32_t)sc, v);
+    if (wp.c_lo == 0) {
+      if (P.dh0 && mem_s) {
+        float* dst = P.dh0 + (((size_t)b * Hr + hr) * N + srow) * st_ld + st_c0 + sc;
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+      }
+    } else if (has_srow) {
+      float* dst = P.carry + ((size_t)wp.sq * N + srow) * kP + sc;
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) __stcg(reinterpret_cast<float4*>(dst + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+    }
+    if (tid == kTidDcum) {
+      // the piece's sums: row 0 for the first piece (or the whole sequence), 1 for the last
+      float* w6 = P.ws_sc + ((size_t)b * P.H + h) * 6;
+      float* w3 = w6 + (wp.c_lo == 0 ? 0 : 3);
+      w3[0] = accA;
+      w3[1] = accD;
+      w3[2] = accB;
+      if (wp.c_lo == 0 && wp.c_hi == nch) w6[3] = w6[4] = w6[5] = 0.f;  // not cut
+      accA = accD = accB = 0.f;
+    }
+    if (wp.c_lo > 0) {
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) st_release_gpu(P.seq_flag + wp.sq, 1);
+    }
+  };
+  // the walk's position, advanced chunk by chunk (divisions only when the
+  // sequence changes): chunk c of the piece [c_lo, c_hi) of sequence sq =
+  // (batch b, sub-head h of head hr)
+  WalkPos wp = walk_start();
+  int b = sq0 / P.H, h = sq0 % P.H, hr = h / P.m, st_c0 = (h % P.m) * kP;
+  float A = -expf(P.A_log[hr]), Dh = P.Dp[hr];
+  for (int n = 0; n < nwalk; ++n) {
+    const bool piece_start = step(wp);
+    const int c = wp.c;
+    if (piece_start) {
+      if constexpr (kCut) {
+        b = wp.sq / P.H, h = wp.sq % P.H, hr = h / P.m;
+        st_c0 = (h % P.m) * kP;
+        A = -expf(P.A_log[hr]);
+        Dh = P.Dp[hr];
+      }
+      // a piece starts: dS = dh_last (or 0) into TMEM, or, for the first piece
+      // of a cut sequence, the carry that the CTA walking its last piece hands over
+      const bool handed = wp.c_hi < nch;
+      const bool came = !(handed && tid == 0) || flag_wait(P.seq_flag + wp.sq, P.status);
+      if (__syncthreads_or(!came)) {  // (bounded wait; the status word says so)
+        ok = false;
+        break;
+      }
+      float v[32];
+      if (handed) {
+        const float* src = P.carry + ((size_t)wp.sq * N + srow) * kP + sc;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = has_srow ? __ldcg(src + i) : 0.f;
+      } else {
+        const float* src =
+            (P.dh_last && mem_s) ? P.dh_last + (((size_t)b * Hr + hr) * N + srow) * st_ld + st_c0 + sc : nullptr;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = src ? src[i] : 0.f;
+      }
+      __syncwarp();
+      tmem_st32(tquarter + kColS + (uint32_t)sc, v);
+      tmem_wait_st();
+    }
+    const int s = n & 1;
     const int t0 = c * kQ;
-    const uint32_t ph = (uint32_t)(ci & 1);
-    const bool got = mbar_wait(&full[s], (uint32_t)((ci >> 1) & 1), P.status);
+    const uint32_t ph = (uint32_t)(n & 1);
+    const bool got = mbar_wait(&full[s], (uint32_t)((n >> 1) & 1), P.status);
     if (__syncthreads_or(!got)) {  // the copy never came: stop, uniformly
       ok = false;
       break;
@@ -314,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
     unsigned char* st = smem + s * SM::kBuf;
     const float* vc = vec + s * kVecSet;
     // the next chunk's boxes into the other stage (free since the last chunk)
-    if (tid == kTidTma && ci + 1 < nch) issue(ci + 1);
+    if (tid == kTidTma && n + 1 < nwalk) issue(n + 1);
 
     // ---- 1: dS as a bf16 image, <dS, S_in>, dS scaled by e^(cum_end) for the
     // update; x'' = diag(w delta) x and dy' = diag(e^cum) dy; dy . x
@@ -398,9 +517,9 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
       umma_commit(bar1);
     }
     // the next chunk's decays (its dt read a chunk ago), its successor's dt in flight
-    if (warp == kWarpDecay && ci + 1 < nch) {
-      chunk_decays(ci + 1);
-      if (ci + 2 < nch) load_dt(ci + 2);
+    if (warp == kWarpDecay && n + 1 < nwalk) {
+      chunk_decays(n + 1);
+      if (n + 2 < nwalk) load_dt(n + 2);
     }
     mbar_wait(bar1, ph, P.status);
     tmem_fence_after_sync();
@@ -604,25 +723,9 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
     }
     tmem_fence_before_sync();
     __syncthreads();  // every product of this stage done and read; images free
+    if (kCut && c == wp.c_lo) piece_end(wp, b, h, hr, st_c0);
   }
-  // dh0 = the state gradient entering chunk 0; the CTA's scalar sums
-  if (ok) {
-    tmem_fence_after_sync();
-    float v[32];
-    __syncwarp();
-    tmem_ld32(tquarter + kColS + (uint32_t)sc, v);
-    if (P.dh0 && mem_s) {
-      float* dst = P.dh0 + (((size_t)b * Hr + hr) * N + srow) * st_ld + st_c0 + sc;
-#pragma unroll
-      for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-    }
-    if (tid == kTidDcum) {
-      float* w3 = P.ws_sc + ((size_t)b * P.H + h) * 3;
-      w3[0] = accA;
-      w3[1] = accD;
-      w3[2] = accB;
-    }
-  }
+  if (!kCut && ok) piece_end(wp, b, h, hr, st_c0);  // the sequence's end (dh0)
   tmem_fence_before_sync();
   __syncthreads();
   tmem_fence_after_sync();
@@ -630,8 +733,9 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
 }
 
 // dBm / dCm[b,t,g,n] = sum over the group's sub-heads (ascending) of the
-// per-sub-head terms; dA_log[h] = A_h sum_b sum_j dA, dDp[h] = sum_b sum_j,
-// ddt_bias[h] = sum_b sum_j (ascending b, then the head's sub-heads j); with
+// per-sub-head terms; dA_log[h] = A_h sum_b sum_j sum_k dA, dDp[h] = sum_b
+// sum_j sum_k, ddt_bias[h] = sum_b sum_j sum_k (ascending b, then the head's
+// sub-heads j, then the sequence's pieces k: first, last); with
 // m > 1 sub-heads per head also ddt_raw[b,t,h] = sum_j (ascending).  H counts
 // sub-heads.
 __global__ void s6_ssd_bwd_reduce_kernel(const float* __restrict__ ws_dB, const float* __restrict__ ws_dC,
@@ -661,10 +765,13 @@ __global__ void s6_ssd_bwd_reduce_kernel(const float* __restrict__ ws_dB, const 
       float a = 0.f, d = 0.f, tb = 0.f;
       for (int bb = 0; bb < B; ++bb)
         for (int j = 0; j < m; ++j) {
-          const float* w3 = ws_sc + ((size_t)bb * H + (size_t)hh * m + j) * 3;
-          a += w3[0];
-          d += w3[1];
-          tb += w3[2];
+          const float* w6 = ws_sc + ((size_t)bb * H + (size_t)hh * m + j) * 6;
+          a += w6[0];
+          a += w6[3];
+          d += w6[1];
+          d += w6[4];
+          tb += w6[2];
+          tb += w6[5];
         }
       dA_log[hh] = -expf(A_log[hh]) * a;
       dDp[hh] = d;
@@ -685,13 +792,46 @@ __global__ void s6_ssd_bwd_ddt_kernel(const float* __restrict__ ws_ddt, size_t n
   }
 }
 
+// One CTA per sequence when they fit the SMs at once; with more sequences
+// than SMs, one range per SM (no tail wave), launched cooperatively so that
+// every CTA is resident while they hand state gradients over.  Where this
+// GPU cannot hold them all, the one-per-sequence grid (the same results).
 template <int N>
 cudaError_t launch_bwd_n(const SsdBwdParams& P, cudaStream_t stream) {
-  auto kern = s6_ssd_bwd_kernel<N>;
   const size_t smem = BwdSmem<N>::kBytes + 1024;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const int seqs = P.B * P.H;
+  const int sms = device_sm_count();
+  cudaError_t e;
+  if (sms > 0 && seqs > sms) {
+    auto kern = s6_ssd_bwd_kernel<N, true>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm >= 1) {
+      e = cudaMemsetAsync(P.seq_flag, 0, sizeof(int) * (size_t)seqs, stream);
+      if (e != cudaSuccess) return e;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)sms);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeCooperative;
+      attr[0].val.cooperative = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      e = cudaLaunchKernelEx(&cfg, kern, P);
+      if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+    }
+    (void)cudaGetLastError();
+    note_plan_fallback();
+  }
+  auto kern = s6_ssd_bwd_kernel<N, false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)(P.B * P.H), kThreads, smem, stream>>>(P);
+  kern<<<(unsigned)seqs, kThreads, smem, stream>>>(P);
   return cudaGetLastError();
 }
 
@@ -701,9 +841,11 @@ size_t ssd_bwd_workspace_bytes(int B, int L, int H, int m, int G, int N) {
   (void)G;
   const size_t Hs = (size_t)H * m;  // sub-heads
   const size_t terms = (size_t)B * L * Hs * N * sizeof(float);
-  const size_t sc = ((size_t)B * Hs * 3 * sizeof(float) + 255) / 256 * 256;
+  const size_t sc = ((size_t)B * Hs * 6 * sizeof(float) + 255) / 256 * 256;
   const size_t ddt = m > 1 ? ((size_t)B * L * Hs * sizeof(float) + 255) / 256 * 256 : 0;
-  return 2 * ((terms + 255) / 256 * 256) + sc + ddt;
+  const size_t flags = ((size_t)B * Hs * sizeof(int) + 255) / 256 * 256;
+  const size_t carry = (size_t)B * Hs * N * kP * sizeof(float);
+  return 2 * ((terms + 255) / 256 * 256) + sc + ddt + flags + carry;
 }
 
 cudaError_t launch_ssd_bwd(const SsdBwdArgs& a, cudaStream_t stream) {
@@ -740,11 +882,16 @@ cudaError_t launch_ssd_bwd(const SsdBwdArgs& a, cudaStream_t stream) {
   P.dh0 = a.dh0;
   const size_t Hs = (size_t)f.H * f.m;
   const size_t terms = ((size_t)f.B * f.L * Hs * f.N * sizeof(float) + 255) / 256 * 256;
-  const size_t scb = ((size_t)f.B * Hs * 3 * sizeof(float) + 255) / 256 * 256;
+  const size_t scb = ((size_t)f.B * Hs * 6 * sizeof(float) + 255) / 256 * 256;
+  const size_t ddtb = f.m > 1 ? ((size_t)f.B * f.L * Hs * sizeof(float) + 255) / 256 * 256 : 0;
+  const size_t flagb = ((size_t)f.B * Hs * sizeof(int) + 255) / 256 * 256;
+  char* wsb = reinterpret_cast<char*>(a.ws);
   P.ws_dB = a.ws;
-  P.ws_dC = reinterpret_cast<float*>(reinterpret_cast<char*>(a.ws) + terms);
-  P.ws_sc = reinterpret_cast<float*>(reinterpret_cast<char*>(a.ws) + 2 * terms);
-  P.ws_ddt = f.m > 1 ? reinterpret_cast<float*>(reinterpret_cast<char*>(a.ws) + 2 * terms + scb) : nullptr;
+  P.ws_dC = reinterpret_cast<float*>(wsb + terms);
+  P.ws_sc = reinterpret_cast<float*>(wsb + 2 * terms);
+  P.ws_ddt = f.m > 1 ? reinterpret_cast<float*>(wsb + 2 * terms + scb) : nullptr;
+  P.seq_flag = reinterpret_cast<int*>(wsb + 2 * terms + scb + ddtb);
+  P.carry = reinterpret_cast<float*>(wsb + 2 * terms + scb + ddtb + flagb);
   P.status = f.status;
   P.dt_min = f.dt_min;
   P.dt_max = f.dt_max;

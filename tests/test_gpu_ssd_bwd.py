@@ -108,6 +108,61 @@ def _compare_wide(g, x, P, dt_limit=None):
         assert np.allclose(parts[k].reshape(-1, m).sum(axis=1), ref[k], rtol=1e-9, atol=1e-9), k
 
 
+HANDOVER = [
+    # B, L, H, G, N, P: more (batch, sub-head) sequences than SMs, so one
+    # range of chunks per SM, sequences cut in two and the state gradient
+    # handed from the CTA walking a sequence's last piece to the one walking
+    # its first
+    (2, 200, 80, 2, 64, 64),    # 160 sequences of 4 chunks
+    (3, 130, 64, 1, 128, 64),   # 192 of 3, a ragged last chunk
+    (1, 300, 160, 4, 128, 64),  # 160 of 5, four groups
+    (2, 100, 20, 2, 64, 256),   # headdim 256: 160 sub-head sequences
+    (2, 200, 80, 2, 64, 32),    # headdim 32
+]
+
+
+@pytest.mark.parametrize("B,L,H,G,N,P", HANDOVER)
+def test_ssd_bwd_handover_parity(B, L, H, G, N, P):
+    x = _problem(B, L, H, G, N, seed=B + L + H + P, P=P)
+    _, _, _, g = _gpu(_dev(x))
+    if P > 64:
+        _compare_wide(g, x, P)
+    else:
+        _compare(g, _oracle(x))
+
+
+def test_ssd_bwd_handover_is_the_per_batch_result():
+    """Two batch rows of 80 heads (160 sequences: ranges per SM, cut
+    sequences) against each row alone (80 sequences: one CTA each, nothing
+    cut): the per-sequence results -- dx, ddt_raw, dBm, dCm, dh0 -- are the
+    same bit for bit (the handed-over state gradient is the same f32 values);
+    the sums over the batch, dA_log, ddt_bias, dDp, agree to rounding."""
+    x = _problem(2, 200, 80, 2, 64, seed=41)
+    xd = _dev(x)
+    _, _, _, g = _gpu(xd)
+    parts = []
+    for b in range(2):
+        xb = {k: (v[b:b + 1].contiguous() if k in ("x", "dt_raw", "Bm", "Cm", "dy", "h0", "dh_last") else v)
+              for k, v in xd.items()}
+        _, _, _, gb = _gpu(xb)
+        parts.append(gb)
+        for k in ("dx", "ddt_raw", "dBm", "dCm", "dh0"):
+            assert torch.equal(g[k][b:b + 1], gb[k]), (b, k)
+    for k in ("dA_log", "ddt_bias", "dDp"):
+        tot = np64(parts[0][k]) + np64(parts[1][k])
+        assert np.allclose(np64(g[k]), tot, rtol=1e-5, atol=1e-6 * np.abs(tot).max()), k
+
+
+def test_ssd_bwd_handover_deterministic():
+    xd = _dev(_problem(2, 300, 80, 2, 128, seed=13))
+    _, _, cs, g0 = _gpu(xd)
+    keep = {k: v.clone() for k, v in g0.items() if v is not None}
+    for _ in range(4):
+        g = s6.ssd_bwd(*[xd[k] for k in KEYS], cs, xd["dy"], xd["dh_last"])
+        for k, v in keep.items():
+            assert torch.equal(g[k], v), k
+
+
 HEAD32 = [
     # B, L, H, G, N: headdim 32, run as 64 columns whose last 32 are zero
     (2, 200, 4, 2, 64),
