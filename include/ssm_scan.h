@@ -342,8 +342,10 @@ int ssm_ssd_fwd_save(int64_t batch, int64_t seqlen, int64_t nheads, int64_t head
                      const float *A_log, const void *Bm, const void *Cm, const float *Dp, const float *h0,
                      void *y, float *h_last, void *chunk_states, const ssm_scan_options *opts, void *stream);
 
-/* Scratch bytes ssm_ssd_bwd needs in `ws` (per-head dBm / dCm terms and
- * per-(batch, head) parameter sums); -1 for an invalid or unsupported shape. */
+/* Scratch bytes ssm_ssd_bwd needs in `ws` (per-head dBm / dCm terms,
+ * per-(batch, head) parameter sums, and the flags and state gradients that
+ * CTAs hand over when sequences outnumber the SMs); -1 for an invalid or
+ * unsupported shape. */
 int64_t ssm_ssd_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
                                     int64_t ngroups, int64_t dstate, int act);
 
@@ -365,7 +367,9 @@ int64_t ssm_ssd_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t nhead
  *            aligned.
  * Evaluated per chunk of 64 steps, last chunk first, in the chunked matrix
  * form on the tensor cores (bf16 operands, f32 accumulation; the state's
- * gradient in f32).  Supported: as ssm_ssd_fwd (bf16, P in {32, 64, 128, 192,
+ * gradient in f32).  With more (batch, head) sequences than SMs, one range of
+ * chunks per SM, launched cooperatively (all resident; where the GPU cannot
+ * hold them, one CTA per sequence, same per-sequence results).  Supported: as ssm_ssd_fwd (bf16, P in {32, 64, 128, 192,
  * 256}, N in {64, 128}); dy, dx, dh_last, dh0, chunk_states 16-byte aligned.  Results are
  * bit-identical from call to call.  Asynchronous on `stream`.
  */

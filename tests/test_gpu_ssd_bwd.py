@@ -153,6 +153,16 @@ def test_ssd_bwd_handover_is_the_per_batch_result():
         assert np.allclose(np64(g[k]), tot, rtol=1e-5, atol=1e-6 * np.abs(tot).max()), k
 
 
+def test_ssd_bwd_handover_dt_limit():
+    """The limit on delta with sequences cut between CTAs."""
+    x = _problem(2, 200, 80, 2, 64, seed=43)
+    sp = torch.nn.functional.softplus(x["dt_raw"].double() + x["dt_bias"].double())
+    lim = (float(np.float32(torch.quantile(sp.flatten()[::7].float(), 0.25))),
+           float(np.float32(torch.quantile(sp.flatten()[::7].float(), 0.75))))
+    _, _, _, g = _gpu(_dev(x), dt_limit=lim)
+    _compare(g, _oracle(x, dt_limit=lim))
+
+
 def test_ssd_bwd_handover_deterministic():
     xd = _dev(_problem(2, 300, 80, 2, 128, seed=13))
     _, _, cs, g0 = _gpu(xd)
