@@ -91,11 +91,12 @@ def _split_heads(x, P):
 
 
 def _compare_wide(g, x, P, dt_limit=None):
-    """Every gradient against the oracle; the per-head sums (dA_log, ddt_bias,
-    dDp) of a head of m sub-heads to TOL times the sum of the magnitudes of
-    the sub-heads' parts (from the oracle on the split problem): a head's
-    value is a sum over its columns, which may cancel, so its error is
-    bounded by its parts' magnitudes, not by its own."""
+    """Every gradient against the oracle.  The per-head sums (dA_log,
+    ddt_bias, dDp) of a head of m sub-heads: the normwise bound (TOL times
+    the largest head's magnitude), raised for a head to TOL times the sum of
+    the magnitudes of its sub-heads' parts (from the oracle on the split
+    problem) -- a head's value is a sum over its columns, which may cancel,
+    so its error is bounded by its parts' magnitudes, not by its own."""
     ref = _oracle(x, dt_limit=dt_limit)
     _compare(g, ref, keys=("dx", "ddt_raw", "dBm", "dCm", "dh0"))
     m = P // 64
@@ -103,7 +104,8 @@ def _compare_wide(g, x, P, dt_limit=None):
     for k in ("dA_log", "ddt_bias", "dDp"):
         mag = np.abs(parts[k]).reshape(-1, m).sum(axis=1)
         err = np.abs(np64(g[k]) - ref[k])
-        assert np.all(err <= TOL["bf16"] * mag + 1e-6), (k, err, mag)
+        bound = TOL["bf16"] * np.maximum(mag, np.abs(ref[k]).max())
+        assert np.all(err <= bound + 1e-6), (k, err, bound)
         # the oracle's head is the sum of its parts
         assert np.allclose(parts[k].reshape(-1, m).sum(axis=1), ref[k], rtol=1e-9, atol=1e-9), k
 
@@ -367,6 +369,37 @@ def test_ssd_bwd_random_shape_sweep(B, L, H, G, N, with_state, limited):
     lim = (0.01, 0.05) if limited else None
     _, _, _, g = _gpu(_dev(x), dt_limit=lim)
     _compare(g, _oracle(x, dt_limit=lim))
+
+
+def _handover_sweep(n=6, seed=2718):
+    """Shapes with more (batch, sub-head) sequences than SMs (153..320): one
+    range of chunks per SM, sequences cut and handed over (or, with one
+    chunk each, never cut)."""
+    r = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        B = int(r.integers(1, 4))
+        G = int(r.integers(1, 3))
+        P = int(r.choice([32, 64, 128]))
+        m = max(1, P // 64)
+        H = G * int(r.integers(1, 200))
+        if not 152 < B * H * m <= 320:
+            continue
+        L = int(r.integers(1, 200))
+        N = int(r.choice([64, 128]))
+        out.append((B, L, H, G, N, P, bool(r.integers(0, 2)), bool(r.integers(0, 2))))
+    return out
+
+
+@pytest.mark.parametrize("B,L,H,G,N,P,with_state,limited", _handover_sweep())
+def test_ssd_bwd_handover_random_sweep(B, L, H, G, N, P, with_state, limited):
+    x = _problem(B, L, H, G, N, seed=B * 17 + L + H, h0=with_state, dh=with_state, P=P)
+    lim = (0.01, 0.05) if limited else None
+    _, _, _, g = _gpu(_dev(x), dt_limit=lim)
+    if P > 64:
+        _compare_wide(g, x, P, dt_limit=lim)
+    else:
+        _compare(g, _oracle(x, dt_limit=lim))
 
 
 def _wide_sweep(n=6, seed=97):
