@@ -126,6 +126,7 @@ constexpr uint32_t kColS = 0, kColG = 64, kColZ = 128, kColCS = 192, kColX = 256
 // decay set of a chunk (floats): delta [0,64), cum [64,128), e^cum [128,192),
 // w = e^(cum_end - cum) [192,256), sigmoid(s) * mask [256,320), w*delta
 // [320,384), e^(cum_end) [384]
+//
 // kCut: ranges of chunks that may cut sequences (one CTA per SM); else one
 // CTA per sequence (gridDim.x = B H), whose walk is that sequence alone.
 template <int N, bool kCut>
@@ -144,7 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1) s6_ssd_bwd_kernel(const __grid_co
   struct WalkPos {
     int sq, c, c_lo, c_hi;  // sequence, chunk, the piece's chunks [c_lo, c_hi)
   };
-  // the first piece [lo0, hi0) of sequence sq0; the last sequence sqz ends at hiz
+  // the walk's first piece: chunks [lo0, hi0) of sequence sq0; its last
+  // sequence sqz ends at chunk hiz
   const int sq0 = (int)(u_begin / nch), lo0 = (int)(u_begin - (long long)sq0 * nch);
   const int hi0 = (int)min((long long)nch, u_end - (long long)sq0 * nch);
   const int sqz = (int)((u_end - 1) / nch), hiz = (int)(u_end - (long long)sqz * nch);
